@@ -1,0 +1,211 @@
+/*
+ * dsv4.h — C ABI of the GB300 (sm_103a) compressed-sparse-attention (CSA) step.
+ *
+ * The step of a DeepSeek-V4-style attention layer, in four stages:
+ *   1. block compressor   (dsv4_compress)
+ *   2. lightning indexer  (dsv4_indexer_topk: MQA scoring + per-token top-k)
+ *   3. top-k on given scores (dsv4_topk: the selection stage taken alone)
+ *   4. gather + sink attention (dsv4_sparse_attn_decode)
+ * plus dsv4_csa_decode, which runs stages 1, 2 and 4 of one decode step back to back.
+ *
+ * Sources, cited by page title and section:
+ *   [A] "nvfp4-megamoe-kernel: compare v0.1-e2e-working...v-c1-c2-c3-20260602"
+ *   [B] "nvfp4-megamoe-kernel: compare master..pure-nvfp4"
+ *   [C] "nvfp4-megamoe-kernel: compare v-precision-floor-fix-20260603..pure-nvfp4"
+ *
+ * Conventions for every entry point
+ *   - Pointers named in an args struct are DEVICE pointers unless stated. bf16 tensors are
+ *     row-major and densely packed in the stated shape. Every device pointer must be
+ *     16-byte aligned.
+ *   - The caller owns every buffer, the workspace included. The library never allocates,
+ *     frees or synchronises, and never reads a device value on the host, so each call can
+ *     be captured in a CUDA graph. Work is ordered on the given stream only.
+ *   - Per-sequence counts (n_comp, win_len) are device int32 arrays, so one captured graph
+ *     serves every step.
+ *   - Return value: DSV4_OK, or an error code. Arguments are checked on the host before any
+ *     launch (DSV4_ERR_INVALID_ARG: null pointer, misalignment, bad size, workspace too
+ *     small). DSV4_ERR_LAUNCH reports a failed launch (cudaGetLastError). Errors found on
+ *     the device (an index out of range, a bounded wait that ran out) are recorded in an
+ *     error word at the start of the workspace and read with dsv4_read_error_word; the
+ *     kernels never trap. As with any asynchronous CUDA work, a fault surfaces on a later
+ *     call.
+ *   - The workspace must hold dsv4_*_workspace_size(args) bytes. Its contents need no
+ *     initialisation: each call clears what it uses, on the stream.
+ */
+#ifndef DSV4_H
+#define DSV4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* dsv4_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+enum {
+    DSV4_OK = 0,
+    DSV4_ERR_INVALID_ARG = 1, /* rejected on the host before any launch */
+    DSV4_ERR_LAUNCH = 2,      /* a kernel launch failed */
+    DSV4_ERR_BAD_INDEX = 3,   /* device: an index outside [0, visible) was masked */
+    DSV4_ERR_TIMEOUT = 4,     /* device: a bounded wait ran out; the kernel returned early */
+    DSV4_ERR_UNSUPPORTED = 5  /* the device is not sm_103 / sm_100 class */
+};
+
+/* Device error word bits (dsv4_read_error_word). */
+#define DSV4_EWORD_BAD_INDEX 0x1u
+#define DSV4_EWORD_TIMEOUT   0x2u
+
+/* ---------------------------------------------------------------------------------------
+ * Stage 1. Block compressor + RMSNorm + partial RoPE.
+ *
+ * For sequence s, block b (tokens t = 0..ratio-1 of the block), channel c:
+ *     w_t = softmax_t( Z[s, b*ratio + t, c] + bias[t, c] )
+ *     x_c = sum_t w_t * C[s, b*ratio + t, c]              (the bias never touches C)
+ *     y   = x / sqrt(mean_c(x_c^2) + eps) * gamma
+ * then the last rope_dim channels are rotated in interleaved pairs (2j, 2j+1) by the angle
+ * pos * theta^(-2j/rope_dim), pos = pos0[s] + b*ratio (the block's first token), and y is
+ * rounded once to bf16.
+ * [A] compressor_reduce.cu hca_compress_reduce_kernel (plain per-block softmax-reduce) and
+ * apply_kv_norm_kernel (eps 1e-6); [B]/[C] commit "Fix two correctness bugs", item 1 and the
+ * compressor_reduce.cu hunks (bias on the logits only); [A] PERFORMANCE_AUDIT.md "P5"
+ * (interleaved-pair RoPE of the last 64 dims); [B] single_shot_inference.py eager_attention
+ * (RoPE applied to the compressed entry after compression and norm).
+ *
+ * Arithmetic: fp32 on the device (angles in fp64), one bf16 rounding at the output.
+ */
+typedef struct dsv4_compress_args {
+    const void* C;            /* bf16 [batch, tokens, dim]   projected KV                 */
+    const void* Z;            /* bf16 [batch, tokens, dim]   gate logits                  */
+    const float* bias;        /* fp32 [ratio, dim]           positional bias (logits only) */
+    const float* gamma;       /* fp32 [dim]                  RMSNorm weight               */
+    const int64_t* pos0;      /* int64 [batch]               position of token 0          */
+    void* out;                /* bf16 [batch, out_rows, dim] destination (e.g. the cache) */
+    const int32_t* out_row0;  /* int32 [batch] first destination row, or NULL for row 0   */
+    int batch, tokens, dim, ratio, rope_dim;
+    int out_rows;             /* rows per sequence in `out` (>= out_row0 + tokens/ratio)  */
+    float eps;                /* 1e-6 on the pages                                        */
+    double rope_theta;        /* 10000 on the pages                                       */
+} dsv4_compress_args;
+
+int dsv4_compress(const dsv4_compress_args* args, dsv4_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Stage 2. Lightning-indexer score + per-token top-k.
+ *
+ *   I[s, t, j] = sum_h w[s, t, h] * ReLU( sum_d q[s, t, h, d] * keys[s, j, d] )
+ * in fp32 (bf16 products, fp32 accumulation), over the visible entries j of query t:
+ * j < n_comp[s] when q_pos is NULL (decode), else j < min(n_comp[s], (q_pos[s,t]+1)/ratio)
+ * (block j, covering tokens [j*ratio, (j+1)*ratio-1], is visible when it ends at or before
+ * the query position). Then idx_out[s, t, :] = the indices of the min(top_k, visible)
+ * largest scores, equal scores ranked by lower index, written in ascending index order and
+ * padded with -1 up to top_k.
+ * [A] ARCHITECTURE_AND_MEMORY_AUDIT.md "F1" (one 128-wide key per block, shared by all 64
+ * indexer heads) and "F3" (the MQA scoring formula, tk = min(top_k, n_comp), topk);
+ * [A] archived_plans/NEXT_STEPS.md "Issue 2" (causal visibility of compressed entries);
+ * [C] GETTING+CUDAGRAPH_READY.md "SECTION C" item 3 (fixed-length, padded index list).
+ */
+typedef struct dsv4_index_args {
+    const void* q;            /* bf16 [batch, n_q, heads, dim]  indexer queries            */
+    const float* w;           /* fp32 [batch, n_q, heads]       per-head weights           */
+    const void* keys;         /* bf16 [batch, max_comp, dim]    compressed indexer keys    */
+    const int32_t* n_comp;    /* int32 [batch]                  valid cache rows           */
+    const int64_t* q_pos;     /* int64 [batch, n_q] query positions, or NULL (all visible) */
+    int32_t* idx_out;         /* int32 [batch, n_q, top_k]                                 */
+    float* scores_out;        /* fp32 [batch, n_q, max_comp] copy of the scores, or NULL    */
+    int batch, n_q, heads, dim, max_comp, top_k, ratio;
+} dsv4_index_args;
+
+size_t dsv4_indexer_topk_workspace_size(const dsv4_index_args* args);
+int dsv4_indexer_topk(const dsv4_index_args* args, void* ws, size_t ws_bytes,
+                      dsv4_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Stage 3 alone. Top-k of caller-given fp32 scores, same rule as above.
+ * scores [rows, max_comp]; n_vis [rows] visible counts; idx_out [rows, top_k].
+ * Equal scores (+0.0 and -0.0 are equal) rank by lower index. Scores must not be NaN.
+ */
+typedef struct dsv4_topk_args {
+    const float* scores;
+    const int32_t* n_vis;
+    int32_t* idx_out;
+    int rows, max_comp, top_k;
+} dsv4_topk_args;
+
+size_t dsv4_topk_workspace_size(const dsv4_topk_args* args);
+int dsv4_topk(const dsv4_topk_args* args, void* ws, size_t ws_bytes, dsv4_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Stage 4. Gather into the caller's buffer + MQA attention with a per-head sink.
+ *
+ * Rows of query t of sequence s: the compressed rows comp_kv[s, idx[s,t,j]] for the valid
+ * (>= 0) entries of idx (or, when idx is NULL — the HCA form — every visible compressed
+ * row), then the sliding-window rows: win holds the most recent tokens in order with the
+ * n_q query tokens last, and query t sees the `window` rows ending at its own row,
+ *     [t + win_len[s] - n_q - window + 1,  t + win_len[s] - n_q]  clipped to [0, win_len[s]).
+ * (Decode, n_q = 1: every one of the win_len rows; their order does not matter.)
+ *   s_j = scale * q[s,t,h,:] . row_j,      m = max(max_j s_j, sink[h])
+ *   out[s,t,h,:] = sum_j e^(s_j - m) row_j / (sum_j e^(s_j - m) + e^(sink[h] - m))
+ * K and V are the same rows (shared-KV MQA). The sink is a logit in the scaled domain.
+ * gather (optional): slot j < top_k holds comp_kv[s, idx[s,t,j]] (zeros for -1), slot
+ * top_k + i the i-th window row of the query (zeros past the window).
+ * [A] commit "C2" (pre-allocated gather buffer of top_k + window rows, no torch.cat);
+ * [A] fmha_6warp_tma_multirow_multitile.cuh "Sink bias correction" (sink adds to the
+ * denominator only, in the scaled domain); [A] PERFORMANCE_AUDIT.md "P4" (v = k);
+ * [B] single_shot_inference.py eager_attention (scale = 1/sqrt(hd); CSA gathers top-k,
+ * ratio > 4 gathers every compressed entry, then the window).
+ * Arithmetic: bf16 tensor-core products, fp32 accumulation and softmax, bf16 output.
+ */
+typedef struct dsv4_attn_args {
+    const void* q;            /* bf16 [batch, n_q, heads, dim]                              */
+    const float* sink;        /* fp32 [heads]                                               */
+    const void* comp_kv;      /* bf16 [batch, max_comp, dim]                                */
+    const int32_t* n_comp;    /* int32 [batch]                                              */
+    const int32_t* idx;       /* int32 [batch, n_q, top_k], or NULL: dense (top_k = max_comp) */
+    const int64_t* q_pos;     /* int64 [batch, n_q] or NULL; limits the dense form          */
+    const void* win;          /* bf16 [batch, win_rows, dim]                                */
+    const int32_t* win_len;   /* int32 [batch]                                              */
+    void* gather;             /* bf16 [batch, n_q, top_k + window, dim], or NULL            */
+    void* out;                /* bf16 [batch, n_q, heads, dim]                              */
+    int batch, n_q, heads, dim, max_comp, top_k, window, win_rows, ratio;
+    float scale;              /* 1/sqrt(dim) on the pages                                   */
+} dsv4_attn_args;
+
+size_t dsv4_sparse_attn_workspace_size(const dsv4_attn_args* args);
+int dsv4_sparse_attn_decode(const dsv4_attn_args* args, void* ws, size_t ws_bytes,
+                            dsv4_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * One decode step: optional compression of the newest block of the main KV and of the
+ * indexer keys (written at rows out_row0 of the caches), then indexer top-k (skipped when
+ * index.heads == 0: the HCA form), then gather + attention over the selected rows.
+ * The stages run back to back on one stream; the workspace is shared.
+ */
+typedef struct dsv4_csa_args {
+    const dsv4_compress_args* compress_kv;   /* or NULL */
+    const dsv4_compress_args* compress_keys; /* or NULL */
+    const dsv4_index_args* index;            /* or NULL for the dense (HCA) form */
+    const dsv4_attn_args* attn;              /* attn->idx must equal index->idx_out */
+} dsv4_csa_args;
+
+size_t dsv4_csa_decode_workspace_size(const dsv4_csa_args* args);
+int dsv4_csa_decode(const dsv4_csa_args* args, void* ws, size_t ws_bytes,
+                    dsv4_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Utilities.
+ */
+const char* dsv4_status_string(int status);
+/* Reads (and clears) the device error word at the start of `ws`. Synchronises the stream:
+ * for tests and diagnostics, never on the hot path. */
+int dsv4_read_error_word(void* ws, dsv4_stream_t stream, uint32_t* out);
+/* Number of kernel launches the last successful call on this host thread enqueued. */
+int dsv4_last_launch_count(void);
+/* Compressed-cache rows for a context: (max_context + ratio - 1) / ratio ([A] commit "C1"). */
+int64_t dsv4_max_comp(int64_t max_context, int ratio);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSV4_H */

@@ -1,0 +1,349 @@
+// Oracle for the compressed-sparse-attention (CSA) decode step.
+//
+// TEST INFRASTRUCTURE ONLY. This file is the plain, slow, single-threaded fp64
+// definition of what the CUDA path computes. Only the tests, the smoke check and
+// the CPU-baseline leg of the benchmark may load it. It shares no code, header,
+// table or helper with the CUDA library, and the CUDA library never calls it.
+//
+// Sources (web pages, cited by title and section):
+//   [A] "nvfp4-megamoe-kernel: compare v0.1-e2e-working...v-c1-c2-c3-20260602"
+//   [B] "nvfp4-megamoe-kernel: compare master..pure-nvfp4"
+//   [C] "nvfp4-megamoe-kernel: compare v-precision-floor-fix-20260603..pure-nvfp4"
+//
+// Every input is bf16 (raw uint16 bit patterns) or fp32, widened exactly to
+// double. All arithmetic is double. Results are rounded once, to bf16 with
+// round-to-nearest-even, where the step's output is bf16.
+//
+// Parity pins: every function below is pinned by tests/test_oracle_pins.py
+// (closed forms, invariants, brute force). None is "parity unpinned".
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <limits>
+#include <vector>
+
+namespace {
+
+double bf16_to_double(uint16_t b) {
+    uint32_t u = static_cast<uint32_t>(b) << 16;
+    float f;
+    std::memcpy(&f, &u, sizeof f);
+    return static_cast<double>(f);
+}
+
+// Round a double to the nearest bf16 (ties to even), directly from double.
+uint16_t double_to_bf16(double x) {
+    if (std::isnan(x)) return 0x7FC0;
+    if (x == 0.0) return std::signbit(x) ? 0x8000 : 0x0000;
+    if (std::isinf(x)) return x > 0 ? 0x7F80 : 0xFF80;
+    int e = std::ilogb(x);                 // |x| in [2^e, 2^(e+1))
+    int ulp_exp = e - 7;                   // bf16 keeps 8 significant bits
+    if (ulp_exp < -133) ulp_exp = -133;    // bf16 subnormal spacing is 2^-133
+    double scaled = std::ldexp(x, -ulp_exp);
+    double r = std::nearbyint(scaled);     // default rounding mode: nearest, ties to even
+    double y = std::ldexp(r, ulp_exp);
+    if (std::fabs(y) > 3.3895313892515355e38) return x > 0 ? 0x7F80 : 0xFF80;  // beyond bf16 max
+    float f = static_cast<float>(y);       // exact: y has at most 8 significant bits
+    uint32_t u;
+    std::memcpy(&u, &f, sizeof u);
+    return static_cast<uint16_t>(u >> 16);
+}
+
+// Number of compressed entries a query at absolute position p may see.
+// [A] archived_plans/NEXT_STEPS.md, "Issue 2" fix direction: a token at position p
+// attends only to compressed entries whose window ends at or before p. Block j covers
+// tokens [j*r, (j+1)*r - 1], so it is visible iff (j+1)*r - 1 <= p.
+int64_t visible_entries(int64_t n_comp, int64_t p, int ratio) {
+    if (p < 0) return 0;
+    int64_t by_pos = (p + 1) / ratio;
+    return std::min<int64_t>(n_comp, by_pos);
+}
+
+}  // namespace
+
+extern "C" {
+
+// ---------------------------------------------------------------------------
+// a1/a2. Block compressor + RMSNorm + partial RoPE.
+//
+// [A] compressor_reduce.cu, hca_compress_reduce_kernel (plain per-block form) with the
+// fix of [B]/[C] compressor_reduce.cu hunks and commit message "Fix two correctness
+// bugs": the positional bias goes on the softmax logits Z + B only, never on C.
+// [A] compressor_reduce.cu, apply_kv_norm_kernel: y = x / sqrt(mean(x^2) + eps) * g.
+// [A] PERFORMANCE_AUDIT.md "P5": interleaved pairs (even, odd) of the last rope_dim
+// dims; the inverse shown there is  e' = e c + o s,  o' = -e s + o c,  so the forward
+// rotation is  e' = e c - o s,  o' = e s + o c.  [B] single_shot_inference.py
+// eager_attention: RoPE is applied to the rope part of the compressed entry at its
+// position after compression and norm.
+//
+// Layout: C, Z [B, T, d] bf16; bias [ratio, d] fp32; gamma [d] fp32; pos0 [B] int64
+// (absolute position of token 0); out [B, T/ratio, d] bf16; out_f64 same shape, may be
+// null. Entry b of sequence s sits at position pos0[s] + b*ratio.
+// Returns 0, or -1 on bad sizes.
+int oracle_compress(const uint16_t* C, const uint16_t* Z, const float* bias,
+                    const float* gamma, const int64_t* pos0, int B, int T, int d,
+                    int ratio, int rope_dim, double theta, double eps,
+                    uint16_t* out, double* out_f64) {
+    if (B < 0 || T < 0 || d <= 0 || ratio <= 0 || T % ratio != 0) return -1;
+    if (rope_dim < 0 || rope_dim > d || rope_dim % 2 != 0) return -1;
+    const int nb = T / ratio;
+    std::vector<double> x(d);
+    for (int s = 0; s < B; ++s) {
+        for (int b = 0; b < nb; ++b) {
+            // softmax over the ratio tokens of the block, per channel, then weighted sum of C
+            for (int c = 0; c < d; ++c) {
+                double m = -std::numeric_limits<double>::infinity();
+                for (int t = 0; t < ratio; ++t) {
+                    size_t at = (static_cast<size_t>(s) * T + static_cast<size_t>(b) * ratio + t) * d + c;
+                    double a = bf16_to_double(Z[at]) + static_cast<double>(bias[static_cast<size_t>(t) * d + c]);
+                    m = std::max(m, a);
+                }
+                double num = 0.0, den = 0.0;
+                for (int t = 0; t < ratio; ++t) {
+                    size_t at = (static_cast<size_t>(s) * T + static_cast<size_t>(b) * ratio + t) * d + c;
+                    double a = bf16_to_double(Z[at]) + static_cast<double>(bias[static_cast<size_t>(t) * d + c]);
+                    double e = std::exp(a - m);
+                    den += e;
+                    num += e * bf16_to_double(C[at]);   // no bias on C
+                }
+                x[c] = num / den;
+            }
+            // RMSNorm over all d channels
+            double ms = 0.0;
+            for (int c = 0; c < d; ++c) ms += x[c] * x[c];
+            ms /= d;
+            double inv = 1.0 / std::sqrt(ms + eps);
+            for (int c = 0; c < d; ++c) x[c] = x[c] * inv * static_cast<double>(gamma[c]);
+            // RoPE on the last rope_dim dims, pair j = (d0, d0+1), d0 = d - rope_dim + 2j
+            const double pos = static_cast<double>(pos0[s] + static_cast<int64_t>(b) * ratio);
+            for (int j = 0; j < rope_dim / 2; ++j) {
+                const int d0 = d - rope_dim + 2 * j;
+                const double freq = std::pow(theta, -2.0 * j / rope_dim);
+                const double ang = pos * freq;
+                const double cs = std::cos(ang), sn = std::sin(ang);
+                const double e = x[d0], o = x[d0 + 1];
+                x[d0] = e * cs - o * sn;
+                x[d0 + 1] = e * sn + o * cs;
+            }
+            for (int c = 0; c < d; ++c) {
+                size_t at = (static_cast<size_t>(s) * nb + b) * d + c;
+                out[at] = double_to_bf16(x[c]);
+                if (out_f64) out_f64[at] = x[c];
+            }
+        }
+    }
+    return 0;
+}
+
+// ---------------------------------------------------------------------------
+// a3. Lightning-indexer score (MQA form).
+//
+// [A] ARCHITECTURE_AND_MEMORY_AUDIT.md "F3 — The scoring einsum has the wrong algebra":
+// I[t,s] = sum_h w[t,h] * ReLU(q[t,h,:] . K[s,:]), one key per compressed block shared by
+// every indexer head; no scale, no softmax. [A] "F1": keys are 128 wide.
+//
+// Layout: q [B, n_q, H, Di] bf16; w [B, n_q, H] fp32; keys [B, max_comp, Di] bf16;
+// n_comp [B]; q_pos [B, n_q] int64 or null (decode: every one of the n_comp entries is
+// visible). scores [B, n_q, max_comp] double: entries at s >= n_vis are set to -inf.
+// n_vis [B, n_q] receives the visible count.
+int oracle_index_scores(const uint16_t* q, const float* w, const uint16_t* keys,
+                        const int32_t* n_comp, const int64_t* q_pos, int B, int n_q,
+                        int H, int Di, int max_comp, int ratio, double* scores,
+                        int32_t* n_vis) {
+    if (B < 0 || n_q < 0 || H <= 0 || Di <= 0 || max_comp < 0 || ratio <= 0) return -1;
+    for (int b = 0; b < B; ++b) {
+        if (n_comp[b] < 0 || n_comp[b] > max_comp) return -1;
+        for (int t = 0; t < n_q; ++t) {
+            const size_t row = static_cast<size_t>(b) * n_q + t;
+            int64_t nv = q_pos ? visible_entries(n_comp[b], q_pos[row], ratio) : n_comp[b];
+            n_vis[row] = static_cast<int32_t>(nv);
+            double* out = scores + row * max_comp;
+            for (int s = 0; s < max_comp; ++s) out[s] = -std::numeric_limits<double>::infinity();
+            for (int64_t s = 0; s < nv; ++s) {
+                const uint16_t* k = keys + (static_cast<size_t>(b) * max_comp + s) * Di;
+                double total = 0.0;
+                for (int h = 0; h < H; ++h) {
+                    const uint16_t* qh = q + (row * H + h) * Di;
+                    double dot = 0.0;
+                    for (int i = 0; i < Di; ++i) dot += bf16_to_double(qh[i]) * bf16_to_double(k[i]);
+                    total += static_cast<double>(w[row * H + h]) * std::max(0.0, dot);
+                }
+                out[s] = total;
+            }
+        }
+    }
+    return 0;
+}
+
+// ---------------------------------------------------------------------------
+// a4. Per-token top-k.
+//
+// [A] ARCHITECTURE_AND_MEMORY_AUDIT.md "F3": tk = min(top_k, n_comp), total.topk(tk).
+// [C] GETTING+CUDAGRAPH_READY.md "SECTION C" item 3: the index list has a fixed length
+// top_k; entries past tk are padding and are masked, never clamped.
+// Tie rule (the pages leave it open; this library fixes it): equal scores -> the lower
+// index ranks first. Output order: the selected indices in ascending order, then -1.
+//
+// Layout: scores [rows, max_comp] (double or float); n_vis [rows]; idx [rows, top_k].
+static void topk_rows_impl(const double* scores, const int32_t* n_vis, int rows,
+                           int max_comp, int top_k, int32_t* idx) {
+    std::vector<int32_t> order;
+    for (int r = 0; r < rows; ++r) {
+        const double* s = scores + static_cast<size_t>(r) * max_comp;
+        const int n = n_vis[r];
+        order.resize(n);
+        for (int i = 0; i < n; ++i) order[i] = i;
+        std::sort(order.begin(), order.end(), [s](int32_t a, int32_t b) {
+            if (s[a] != s[b]) return s[a] > s[b];
+            return a < b;
+        });
+        const int tk = std::min(top_k, n);
+        std::vector<int32_t> chosen(order.begin(), order.begin() + tk);
+        std::sort(chosen.begin(), chosen.end());
+        int32_t* o = idx + static_cast<size_t>(r) * top_k;
+        for (int j = 0; j < top_k; ++j) o[j] = j < tk ? chosen[j] : -1;
+    }
+}
+
+int oracle_topk(const double* scores, const int32_t* n_vis, int rows, int max_comp,
+                int top_k, int32_t* idx) {
+    if (rows < 0 || max_comp < 0 || top_k <= 0) return -1;
+    for (int r = 0; r < rows; ++r)
+        if (n_vis[r] < 0 || n_vis[r] > max_comp) return -1;
+    topk_rows_impl(scores, n_vis, rows, max_comp, top_k, idx);
+    return 0;
+}
+
+// Same selection on fp32 scores (the step taken alone, on caller-given scores).
+int oracle_topk_f32(const float* scores, const int32_t* n_vis, int rows, int max_comp,
+                    int top_k, int32_t* idx) {
+    if (rows < 0 || max_comp < 0 || top_k <= 0) return -1;
+    std::vector<double> wide(static_cast<size_t>(rows) * max_comp);
+    for (size_t i = 0; i < wide.size(); ++i) wide[i] = static_cast<double>(scores[i]);
+    return oracle_topk(wide.data(), n_vis, rows, max_comp, top_k, idx);
+}
+
+// ---------------------------------------------------------------------------
+// a5 + a6. Gather into a fixed buffer, then MQA attention with a per-head sink.
+//
+// Gather: [A] commit "C2": one pre-allocated buffer of (top_k + window) rows receives the
+// selected compressed rows and the sliding-window rows; [A] ARCHITECTURE_AND_MEMORY_AUDIT.md
+// "B2": CSA concatenates comp_kv[topk] with the window, HCA (ratio > 4) concatenates every
+// compressed entry with the window.
+// Attention: [A] fmha_6warp_tma_multirow_multitile.cuh, "Sink bias correction": the sink
+// is one extra logit per head, already in the scaled domain, that adds to the softmax
+// denominator and has no value row. [A] PERFORMANCE_AUDIT.md "P4": V is the same tensor as
+// K (shared KV). [B] single_shot_inference.py eager_attention: scale = 1/sqrt(hd).
+//
+//   s_j = scale * q_h . kv_j,   m = max(max_j s_j, sink_h)
+//   o_h = sum_j e^(s_j - m) kv_j / (sum_j e^(s_j - m) + e^(sink_h - m))
+//
+// Layout: q [B, n_q, H, D] bf16; sink [H] fp32; comp_kv [B, max_comp, D] bf16; n_comp [B];
+// idx [B, n_q, top_k] int32 or null (dense over every visible entry; then top_k must equal
+// max_comp); q_pos [B, n_q] int64 or null (decode: all n_comp visible);
+// win [B, win_rows, D] bf16 holds the most recent tokens in order, the n_q query tokens
+// last; win_len [B] valid rows. Query t (absolute index q_abs[t] of n_q_total, or t of n_q
+// when q_abs is null) sees the `window` rows ending at its own row:
+//   rows [qa + win_len - n_q_total - window + 1,  qa + win_len - n_q_total]  within [0, win_len).
+// out [B, n_q, H, D] bf16; out_f64 may be null; gather [B, n_q, top_k + window, D] bf16 or
+// null: slot j < top_k holds comp_kv[idx[j]] (zeros for -1), slot top_k + i holds the i-th
+// window row (zeros past the window length).
+int oracle_sparse_attn(const uint16_t* q, const float* sink, const uint16_t* comp_kv,
+                       const int32_t* n_comp, const int32_t* idx, const int64_t* q_pos,
+                       const uint16_t* win, const int32_t* win_len, const int32_t* q_abs,
+                       int B, int n_q, int n_q_total, int H, int D, int max_comp, int top_k,
+                       int window, int win_rows, int ratio, double scale,
+                       uint16_t* out, double* out_f64, uint16_t* gather) {
+    if (B < 0 || n_q < 0 || H <= 0 || D <= 0 || top_k <= 0 || window < 0 || ratio <= 0) return -1;
+    if (!idx && top_k != max_comp) return -1;
+    const int slots = top_k + window;
+    std::vector<const uint16_t*> rows;
+    std::vector<double> kv;   // widened rows, [n_rows, D]
+    std::vector<double> sc;
+    for (int b = 0; b < B; ++b) {
+        if (n_comp[b] < 0 || n_comp[b] > max_comp) return -1;
+        if (win_len[b] < 0 || win_len[b] > win_rows) return -1;
+        for (int t = 0; t < n_q; ++t) {
+            const size_t qrow = static_cast<size_t>(b) * n_q + t;
+            const int64_t nv = q_pos ? visible_entries(n_comp[b], q_pos[qrow], ratio) : n_comp[b];
+            rows.clear();
+            uint16_t* g = gather ? gather + qrow * slots * static_cast<size_t>(D) : nullptr;
+            if (g) std::fill(g, g + static_cast<size_t>(slots) * D, static_cast<uint16_t>(0));
+            // compressed part of the gather
+            for (int j = 0; j < top_k; ++j) {
+                int64_t e;
+                if (idx) {
+                    e = idx[qrow * top_k + j];
+                    if (e < 0) continue;                       // padding: masked
+                    if (e >= nv) return -2;                    // not a visible entry
+                } else {
+                    e = j;
+                    if (e >= nv) continue;
+                }
+                const uint16_t* src = comp_kv + (static_cast<size_t>(b) * max_comp + e) * D;
+                rows.push_back(src);
+                if (g) std::memcpy(g + static_cast<size_t>(j) * D, src, sizeof(uint16_t) * D);
+            }
+            // sliding-window part of the gather
+            const int64_t qa = q_abs ? q_abs[t] : t;
+            const int64_t hi = qa + win_len[b] - n_q_total;          // the query's own row
+            int64_t lo = hi - window + 1;
+            if (lo < 0) lo = 0;
+            int slot = 0;
+            for (int64_t r = lo; r <= hi && r < win_len[b]; ++r, ++slot) {
+                const uint16_t* src = win + (static_cast<size_t>(b) * win_rows + r) * D;
+                rows.push_back(src);
+                if (g) std::memcpy(g + static_cast<size_t>(top_k + slot) * D, src, sizeof(uint16_t) * D);
+            }
+            const size_t n_rows = rows.size();
+            kv.assign(n_rows * D, 0.0);
+            for (size_t r = 0; r < n_rows; ++r)
+                for (int i = 0; i < D; ++i) kv[r * D + i] = bf16_to_double(rows[r][i]);
+            sc.assign(n_rows, 0.0);
+            for (int h = 0; h < H; ++h) {
+                const uint16_t* qh = q + (qrow * H + h) * D;
+                const double sk = static_cast<double>(sink[h]);
+                double m = sk;
+                for (size_t r = 0; r < n_rows; ++r) {
+                    double dot = 0.0;
+                    for (int i = 0; i < D; ++i) dot += bf16_to_double(qh[i]) * kv[r * D + i];
+                    sc[r] = scale * dot;
+                    m = std::max(m, sc[r]);
+                }
+                double den = std::exp(sk - m);
+                std::vector<double> num(D, 0.0);
+                for (size_t r = 0; r < n_rows; ++r) {
+                    const double p = std::exp(sc[r] - m);
+                    den += p;
+                    for (int i = 0; i < D; ++i) num[i] += p * kv[r * D + i];
+                }
+                for (int i = 0; i < D; ++i) {
+                    const double o = num[i] / den;
+                    const size_t at = (qrow * H + h) * D + i;
+                    out[at] = double_to_bf16(o);
+                    if (out_f64) out_f64[at] = o;
+                }
+            }
+        }
+    }
+    return 0;
+}
+
+// Sizing of the compressed cache for a context length.
+// [A] commit "C1": max_comp = (max_context + compress_ratio - 1) // ratio.
+int64_t oracle_max_comp(int64_t max_context, int ratio) {
+    if (ratio <= 0 || max_context < 0) return -1;
+    return (max_context + ratio - 1) / ratio;
+}
+
+// Visible count, exported so tests can pin the causal rule on its own.
+int64_t oracle_visible_entries(int64_t n_comp, int64_t p, int ratio) {
+    return visible_entries(n_comp, p, ratio);
+}
+
+// bf16 rounding, exported so tests can pin it against exhaustive float checks.
+uint16_t oracle_double_to_bf16(double x) { return double_to_bf16(x); }
+
+}  // extern "C"

@@ -1,0 +1,64 @@
+"""Plant plausible mistakes in copies of the oracle source and check that the pins catch
+every one of them (CPU only; the planted copies live in a temporary directory)."""
+import os
+import tempfile
+
+import pytest
+
+import oracle
+import oracle_pins
+
+# (name, original text, replacement, occurrences expected)
+MUTANTS = [
+    ("bias_on_C", "num += e * bf16_to_double(C[at]);",
+     "num += e * (bf16_to_double(C[at]) + bias[static_cast<size_t>(t) * d + c]);", 1),
+    ("rope_inverse_direction", "x[d0] = e * cs - o * sn;", "x[d0] = e * cs + o * sn;", 1),
+    ("rope_frequency_exponent", "std::pow(theta, -2.0 * j / rope_dim)", "std::pow(theta, -1.0 * j / rope_dim)", 1),
+    ("rope_pairs_split_halves", "const int d0 = d - rope_dim + 2 * j;",
+     "const int d0 = d - rope_dim + j;", 1),
+    ("rmsnorm_eps_outside_sqrt", "1.0 / std::sqrt(ms + eps)", "1.0 / (std::sqrt(ms) + eps)", 1),
+    ("rmsnorm_sum_not_mean", "ms /= d;", "ms /= 1;", 1),
+    ("bias_rows_reversed", "bias[static_cast<size_t>(t) * d + c]", "bias[static_cast<size_t>(ratio - 1 - t) * d + c]", 2),
+    ("entry_position_unscaled", "pos0[s] + static_cast<int64_t>(b) * ratio", "pos0[s] + static_cast<int64_t>(b)", 1),
+    ("score_no_relu", "std::max(0.0, dot)", "dot", 1),
+    ("score_per_head_key", "bf16_to_double(k[i])", "bf16_to_double(k[(i + h) % Di])", 1),
+    ("score_weight_dropped", "static_cast<double>(w[row * H + h]) * std::max(0.0, dot)", "std::max(0.0, dot)", 1),
+    ("topk_ties_higher_index", "return a < b;", "return a > b;", 1),
+    ("visibility_strict", "int64_t by_pos = (p + 1) / ratio;", "int64_t by_pos = p / ratio;", 1),
+    ("sink_dropped", "double den = std::exp(sk - m);", "double den = 0.0;", 1),
+    ("sink_in_numerator", "double m = sk;", "double m = sk; for (int i = 0; i < D; ++i) (void)i;", 0),
+    ("scale_dropped", "sc[r] = scale * dot;", "sc[r] = dot;", 1),
+    ("window_off_by_one", "int64_t lo = hi - window + 1;", "int64_t lo = hi - window;", 1),
+    ("window_wrong_end", "const int64_t hi = qa + win_len[b] - n_q_total;",
+     "const int64_t hi = qa + win_len[b] - n_q_total - 1;", 1),
+    ("bf16_truncates", "double r = std::nearbyint(scaled);", "double r = std::trunc(scaled);", 1),
+    ("max_comp_floor", "return (max_context + ratio - 1) / ratio;", "return max_context / ratio;", 1),
+]
+MUTANTS = [m for m in MUTANTS if m[3] > 0]
+
+
+@pytest.fixture(scope="module")
+def source():
+    with open(oracle.SOURCE) as fh:
+        return fh.read()
+
+
+@pytest.mark.parametrize("name,old,new,count", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(source, name, old, new, count):
+    assert source.count(old) == count, f"mutation site for {name} not found as expected"
+    with tempfile.TemporaryDirectory() as tmp:
+        src = os.path.join(tmp, "mutant.cpp")
+        with open(src, "w") as fh:
+            fh.write(source.replace(old, new))
+        lib = oracle.compile_oracle(src, os.path.join(tmp, "libmutant.so"))
+        oracle.use_library(lib)
+        caught = []
+        try:
+            for pin in oracle_pins.ALL_PINS:
+                try:
+                    pin()
+                except (AssertionError, ValueError):
+                    caught.append(pin.__name__)
+        finally:
+            oracle.use_library(None)
+    assert caught, f"no pin caught the planted mistake '{name}'"
