@@ -1,0 +1,407 @@
+#!/usr/bin/env python
+"""Benchmark of the CSA decode step at 1M-token context (batch 4 per GPU), one JSON line.
+
+A step is one pass of the whole hot path over one batch: compress the newest 4-token block
+of the main KV and of the indexer keys into the caches, score all 262,144 compressed keys
+with 64 indexer heads, select the top 2048 per sequence, gather those rows plus the
+128-token window into the gather buffer and run 64-head sink attention over them. The step
+is captured once in a CUDA graph and replayed; inputs stay resident in HBM (256 MiB of
+keys and 1 GiB of compressed KV: larger than L2, so every step streams the keys from HBM).
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+Under torchrun each rank runs its own batch (weak scaling, no data-path collective); rank 0
+prints the line with the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "CSA decode tokens/s per layer @1M ctx; indexer+gather HBM GB/s vs ~8 TB/s"
+CFG = 3
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def step_bytes(wl):
+    """Algorithmic bytes of one step: index keys scanned + gathered KV rows + outputs."""
+    keys = wl.batch * wl.n_comp * wl.idx_dim * 2
+    gathered = wl.batch * (wl.top_k + wl.window) * wl.head_dim * 2
+    outputs = wl.batch * wl.heads * wl.head_dim * 2
+    return keys, gathered, outputs
+
+
+def scorer_bytes(wl):
+    """Algorithmic bytes of one scoring launch: every visible key (256 B) read once, one fp32
+    score written per key, plus the queries and head weights."""
+    return wl.batch * wl.n_comp * (wl.idx_dim * 2 + 4) + wl.batch * wl.idx_heads * (wl.idx_dim * 2 + 4)
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def profile_traffic():
+    """dram bytes per scoring launch from the committed ncu summary, if the kernel source
+    still matches the hash recorded there; else None."""
+    path = os.path.join(ROOT, "profiles", "index_score_kernel_csa_decode_ctx1048576_b4.md")
+    src = os.path.join(ROOT, "compressed_sparse_attention_08_gb300", "csrc", "indexer.cu")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m1 = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    m2 = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    if not (m1 and m2):
+        return None
+    if hashlib.sha256(open(src, "rb").read()).hexdigest() != m1.group(1):
+        return None
+    return int(m2.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples while the GPU is under load."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.dev)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([c.strip() for c in line.split(",")])
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            try:
+                sm.append(float(r[0]))
+                mx.append(float(r[1]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        busy = sorted(sm)[len(sm) // 2:] if sm else []
+        return {"sm_mhz": statistics.median(busy) if busy else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_baseline(wl, x0, seconds_hint=None):
+    """The oracle (single thread, fp64) on one sequence's step: newest-block compression of
+    the KV and the keys, the 262,144-key indexer scan, top-2048, 2,176-row sink attention."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    t0 = time.perf_counter()
+    kv_bits, _ = oracle.compress(x0["C"], x0["Z"], x0["bias"], x0["gamma"], x0["pos0"], wl.ratio)
+    key_bits, _ = oracle.compress(x0["C_I"], x0["Z_I"], x0["bias_I"], x0["gamma_I"], x0["pos0"], wl.ratio)
+    comp_kv = x0["comp_kv"]
+    keys = x0["keys"]
+    comp_kv[:, -1] = kv_bits[:, 0]
+    keys[:, -1] = key_bits[:, 0]
+    s, nv = oracle.index_scores(x0["q_I"], x0["w"], keys, x0["n_comp"], wl.ratio)
+    idx = oracle.topk(s, nv, wl.top_k)
+    oracle.sparse_attn(x0["q"], x0["sink"], comp_kv, x0["n_comp"], idx, x0["win"], x0["win_len"],
+                       wl.top_k, wl.window, wl.ratio)
+    dt = time.perf_counter() - t0
+    return {"value": 1.0 / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": "one sequence (1 token) of the 1M-context batch-4 decode step: newest-block "
+                      "compression of KV and keys, 262,144-key indexer scan, top-2048, 2,176-row "
+                      "sink attention; fp64, single thread",
+            "seconds": dt, "cpu": _cpu_model(), "nproc": os.cpu_count()}
+
+
+def _cpu_model():
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from compressed_sparse_attention_08_gb300.workloads import WORKLOADS, make_inputs
+    wl = WORKLOADS[CFG]
+    x0 = make_inputs(wl, batch=1)
+    for _ in range(args.warmup):
+        cpu_baseline(wl, dict(x0))
+    times = []
+    for _ in range(args.steps):
+        times.append(cpu_baseline(wl, dict(x0))["seconds"])
+    total = sum(times)
+    value = args.steps / total
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "batch": 1, "context": wl.context, "top_k": wl.top_k},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": "one sequence (1 token) of the 1M-context decode step per "
+                                       "timed step, fp64 oracle, single thread"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args):
+    import numpy as np
+    import torch
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import __graft_entry__
+    __graft_entry__.build()
+    import compressed_sparse_attention_08_gb300 as m
+    from compressed_sparse_attention_08_gb300 import _abi
+    from compressed_sparse_attention_08_gb300.workloads import WORKLOADS, make_inputs
+
+    wl = WORKLOADS[CFG]
+    t0 = time.time()
+    x = make_inputs(wl)
+    log(f"[rank {rank}] inputs generated in {time.time() - t0:.1f}s")
+    B, D, Di = wl.batch, wl.head_dim, wl.idx_dim
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a, np.uint16).view(np.int16)).cuda().view(torch.bfloat16)
+
+    def dv(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+    t = {}
+    t["kv"], t["keys"] = bf(x["comp_kv"]), bf(x["keys"])
+    for k in ("C", "Z", "C_I", "Z_I", "q_I", "q", "win"):
+        t[k] = bf(x[k])
+    for k in ("bias", "gamma", "bias_I", "gamma_I", "pos0", "append_row", "w", "n_comp", "sink", "win_len"):
+        t[k] = dv(x[k])
+    t["idx"] = torch.empty(B, 1, wl.top_k, dtype=torch.int32, device="cuda")
+    t["out"] = torch.empty(B, 1, wl.heads, D, dtype=torch.bfloat16, device="cuda")
+    t["gather"] = torch.empty(B, 1, wl.top_k + wl.window, D, dtype=torch.bfloat16, device="cuda")
+    t["scores"] = torch.empty(B, 1, wl.max_comp, dtype=torch.float32, device="cuda")
+    ck = _abi.compress_args(t["C"], t["Z"], t["bias"], t["gamma"], t["pos0"], t["kv"], ratio=wl.ratio,
+                            out_row0=t["append_row"])
+    cq = _abi.compress_args(t["C_I"], t["Z_I"], t["bias_I"], t["gamma_I"], t["pos0"], t["keys"],
+                            ratio=wl.ratio, out_row0=t["append_row"])
+    ia = _abi.index_args(t["q_I"], t["w"], t["keys"], t["n_comp"], t["idx"], ratio=wl.ratio)
+    aa = _abi.attn_args(t["q"], t["sink"], t["kv"], t["n_comp"], t["win"], t["win_len"], t["out"],
+                        idx=t["idx"], window=wl.window, ratio=wl.ratio, gather=t["gather"])
+    nbytes = m.dsv4_csa_decode_workspace_size(attn=aa, index=ia, compress_kv=ck, compress_keys=cq)
+    ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def step(s=None):
+        m.dsv4_csa_decode(ws, attn=aa, index=ia, compress_kv=ck, compress_keys=cq, stream=s)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step(stream)
+    stream.synchronize()
+    launches = m.dsv4_last_launch_count()
+    st, ew = m.dsv4_read_error_word(ws, stream)
+    if ew:
+        raise SystemExit(f"device error word {ew:#x} after warm-up")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            step(stream)
+    stream.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    # soak: keep the GPU busy ~1 s so clocks settle and the sampler sees load
+    with torch.cuda.stream(stream):
+        t_end = time.time() + 1.0
+        while time.time() < t_end:
+            for _ in range(50):
+                graph.replay()
+            stream.synchronize()
+        for _ in range(args.warmup):
+            graph.replay()
+    stream.synchronize()
+
+    # ---- timed region: exactly K steps
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+        dist.barrier()
+
+    # ---- dominant kernel alone: the scoring launch, events on its stream
+    score_ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            m.dsv4_index_score(t["q_I"], t["w"], t["keys"], t["n_comp"], t["scores"], score_ws,
+                               ratio=wl.ratio, stream=stream)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for a, b in evs:
+            a.record(stream)
+            m.dsv4_index_score(t["q_I"], t["w"], t["keys"], t["n_comp"], t["scores"], score_ws,
+                               ratio=wl.ratio, stream=stream)
+            b.record(stream)
+    torch.cuda.synchronize()
+    score_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+    # ---- end to end through the public API with host buffers (pinned), copies timed
+    per_step_in = ("q_I", "w", "q", "C", "Z", "C_I", "Z_I")
+    host_in = {k: torch.empty_like(t[k], device="cpu").pin_memory() for k in per_step_in}
+    for k in per_step_in:
+        host_in[k].copy_(t[k])
+    host_out = torch.empty_like(t["out"], device="cpu").pin_memory()
+    host_idx = torch.empty_like(t["idx"], device="cpu").pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = host_out.numel() * host_out.element_size() + host_idx.numel() * host_idx.element_size()
+
+    def e2e_step():
+        for k in per_step_in:
+            t[k].copy_(host_in[k], non_blocking=True)
+        graph.replay()
+        host_out.copy_(t["out"], non_blocking=True)
+        host_idx.copy_(t["idx"], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            e2e_step()
+        stream.synchronize()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        f1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = f0.elapsed_time(f1) / args.steps
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    clk = clocks.stop()
+
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peaks()
+    kb, gb, ob = step_bytes(wl)
+    sb = scorer_bytes(wl)
+    score_gbs = sb / (score_ms * 1e-3) / 1e9
+    tokens = world * B
+    line = {
+        "metric": METRIC, "value": tokens / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "batch_per_gpu": B, "context": wl.context,
+                   "n_comp": wl.n_comp, "top_k": wl.top_k, "window": wl.window,
+                   "idx_heads": wl.idx_heads, "heads": wl.heads, "head_dim": D,
+                   "l2": "inputs larger than L2: 256 MiB of keys streamed per step, 1 GiB KV cache",
+                   "graph": "one CUDA graph per step, replayed"},
+        "roofline": {"bound": "hbm", "kernel": "index_score_kernel", "achieved": score_gbs,
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": score_gbs / peak,
+                     "traffic": profile_traffic(), "bytes_per_launch": sb,
+                     "ms_per_launch": score_ms},
+        "step_roofline": {"bytes": kb + gb + ob, "keys": kb, "gathered": gb, "outputs": ob,
+                          "achieved": (kb + gb + ob) / (ms * 1e-3) / 1e9, "peak": peak,
+                          "frac": (kb + gb + ob) / (ms * 1e-3) / 1e9 / peak, "unit": "GB/s"},
+        "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches * args.steps, "launches_per_step": launches,
+        "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        x0 = make_inputs(wl, batch=1)
+        line["cpu_baseline"] = cpu_baseline(wl, x0)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,266 @@
+// C ABI of the CSA library: host-side argument checks (before any CUDA call), workspace
+// sizing, dispatch to the kernels on the caller's stream, and small utilities.
+// No entry point allocates, frees, synchronises or reads device memory on the host,
+// except dsv4_read_error_word, which exists for tests and diagnostics.
+#include <cmath>
+#include <cstdint>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace dsv4 {
+namespace {
+
+thread_local int g_launches = 0;
+thread_local int g_last_launches = 0;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool dev_ptr_ok(const void* p) { return p != nullptr && aligned16(p); }
+bool opt_ptr_ok(const void* p) { return p == nullptr || aligned16(p); }
+
+int device_check() {
+    static int ok_for_device[64] = {0};   // 0 unknown, 1 ok, 2 unsupported
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return DSV4_ERR_UNSUPPORTED;
+    if (dev < 64 && ok_for_device[dev] == 1) return DSV4_OK;
+    int major = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+        return DSV4_ERR_UNSUPPORTED;
+    const int res = major == 10 ? DSV4_OK : DSV4_ERR_UNSUPPORTED;
+    if (dev < 64) ok_for_device[dev] = res == DSV4_OK ? 1 : 2;
+    return res;
+}
+
+bool compress_ok(const dsv4_compress_args* a) {
+    if (!a) return false;
+    if (!dev_ptr_ok(a->C) || !dev_ptr_ok(a->Z) || !dev_ptr_ok(a->bias) || !dev_ptr_ok(a->gamma) ||
+        !dev_ptr_ok(a->pos0) || !dev_ptr_ok(a->out) || !opt_ptr_ok(a->out_row0))
+        return false;
+    if (a->batch < 0 || a->tokens < 0 || a->ratio < 1 || a->dim < 2 || a->dim > 1024) return false;
+    if (a->tokens % a->ratio != 0) return false;
+    if (a->rope_dim < 0 || a->rope_dim > a->dim || (a->rope_dim & 1)) return false;
+    if (a->out_rows < 1) return false;
+    if (!a->out_row0 && a->out_rows < a->tokens / a->ratio) return false;
+    if (!(a->eps >= 0.f) || !std::isfinite(a->eps) || !std::isfinite(a->rope_theta) || a->rope_theta <= 0.0)
+        return false;
+    return true;
+}
+
+bool index_ok(const dsv4_index_args* a) {
+    if (!a) return false;
+    if (!dev_ptr_ok(a->q) || !dev_ptr_ok(a->w) || !dev_ptr_ok(a->keys) || !dev_ptr_ok(a->n_comp) ||
+        !dev_ptr_ok(a->idx_out) || !opt_ptr_ok(a->q_pos) || !opt_ptr_ok(a->scores_out))
+        return false;
+    if (a->batch < 0 || a->n_q < 1 || a->dim != 128) return false;
+    if (a->heads < 8 || a->heads > 64 || (a->heads & 7)) return false;
+    if (a->max_comp < 1 || a->top_k < 1 || a->top_k > a->max_comp || a->ratio < 1) return false;
+    if (static_cast<long long>(a->batch) * a->n_q > (1ll << 30)) return false;
+    if (static_cast<long long>(a->batch) * a->n_q * a->heads > (1ll << 31) - 1) return false;
+    return true;
+}
+
+bool topk_ok(const dsv4_topk_args* a) {
+    if (!a) return false;
+    if (!dev_ptr_ok(a->scores) || !dev_ptr_ok(a->n_vis) || !dev_ptr_ok(a->idx_out)) return false;
+    if (a->rows < 0 || a->max_comp < 1 || a->top_k < 1 || a->top_k > a->max_comp) return false;
+    return true;
+}
+
+bool attn_ok(const dsv4_attn_args* a) {
+    if (!a) return false;
+    if (!dev_ptr_ok(a->q) || !dev_ptr_ok(a->sink) || !dev_ptr_ok(a->comp_kv) || !dev_ptr_ok(a->n_comp) ||
+        !dev_ptr_ok(a->win) || !dev_ptr_ok(a->win_len) || !dev_ptr_ok(a->out) ||
+        !opt_ptr_ok(a->idx) || !opt_ptr_ok(a->q_pos) || !opt_ptr_ok(a->gather))
+        return false;
+    if (a->batch < 0 || a->n_q < 1) return false;
+    if (a->dim != 128 && a->dim != 256 && a->dim != 512) return false;
+    if (a->heads < 1 || a->heads > 64) return false;
+    if (a->max_comp < 1 || a->top_k < 1 || a->window < 0 || a->win_rows < 1 || a->ratio < 1) return false;
+    if (a->idx ? a->top_k > a->max_comp : a->top_k != a->max_comp) return false;
+    if (!std::isfinite(a->scale)) return false;
+    if (static_cast<long long>(a->batch) * a->n_q > 65535ll) return false;   // grid.y
+    return true;
+}
+
+uint32_t* eword_of(void* ws) { return static_cast<uint32_t*>(ws); }
+uint8_t* body_of(void* ws) { return static_cast<uint8_t*>(ws) + kWsHeader; }
+
+struct LaunchScope {
+    LaunchScope() { g_launches = 0; }
+    ~LaunchScope() { g_last_launches = g_launches; }
+};
+
+}  // namespace
+
+void count_launch(int n) { g_launches += n; }
+
+int sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+    if (dev < 64 && cache[dev]) return cache[dev];
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (dev < 64) cache[dev] = n;
+    return n;
+}
+
+}  // namespace dsv4
+
+using namespace dsv4;
+
+extern "C" {
+
+const char* dsv4_status_string(int status) {
+    switch (status) {
+        case DSV4_OK: return "ok";
+        case DSV4_ERR_INVALID_ARG: return "invalid argument (rejected on the host before any launch)";
+        case DSV4_ERR_LAUNCH: return "kernel launch failed";
+        case DSV4_ERR_BAD_INDEX: return "an index outside the visible range was masked";
+        case DSV4_ERR_TIMEOUT: return "a bounded device wait ran out";
+        case DSV4_ERR_UNSUPPORTED: return "unsupported device (needs sm_100-class / sm_103)";
+        default: return "unknown status";
+    }
+}
+
+int dsv4_last_launch_count(void) { return g_last_launches; }
+
+int64_t dsv4_max_comp(int64_t max_context, int ratio) {
+    if (ratio < 1 || max_context < 0) return -1;
+    return (max_context + ratio - 1) / ratio;
+}
+
+int dsv4_compress(const dsv4_compress_args* a, dsv4_stream_t stream) {
+    LaunchScope scope;
+    if (!compress_ok(a)) return DSV4_ERR_INVALID_ARG;
+    if (int rc = device_check()) return rc;
+    return launch_compress(*a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t dsv4_indexer_topk_workspace_size(const dsv4_index_args* a) {
+    if (!a) return 0;
+    return kWsHeader + index_ws_bytes(*a);
+}
+
+int dsv4_indexer_topk(const dsv4_index_args* a, void* ws, size_t ws_bytes, dsv4_stream_t stream) {
+    LaunchScope scope;
+    if (!index_ok(a) || !dev_ptr_ok(ws) || ws_bytes < dsv4_indexer_topk_workspace_size(a))
+        return DSV4_ERR_INVALID_ARG;
+    if (int rc = device_check()) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), st) != cudaSuccess) return DSV4_ERR_LAUNCH;
+    return launch_indexer(*a, body_of(ws), eword_of(ws), st);
+}
+
+size_t dsv4_index_score_workspace_size(const dsv4_index_args* a) {
+    (void)a;
+    return kWsHeader;
+}
+
+int dsv4_index_score(const dsv4_index_args* a, void* ws, size_t ws_bytes, dsv4_stream_t stream) {
+    LaunchScope scope;
+    if (!index_ok(a) || !a->scores_out || !dev_ptr_ok(ws) || ws_bytes < dsv4_index_score_workspace_size(a))
+        return DSV4_ERR_INVALID_ARG;
+    if (int rc = device_check()) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), st) != cudaSuccess) return DSV4_ERR_LAUNCH;
+    return launch_index_score(*a, eword_of(ws), st);
+}
+
+size_t dsv4_topk_workspace_size(const dsv4_topk_args* a) {
+    if (!a) return 0;
+    return kWsHeader + topk_ws_bytes(a->rows, a->max_comp, a->top_k);
+}
+
+int dsv4_topk(const dsv4_topk_args* a, void* ws, size_t ws_bytes, dsv4_stream_t stream) {
+    LaunchScope scope;
+    if (!topk_ok(a) || !dev_ptr_ok(ws) || ws_bytes < dsv4_topk_workspace_size(a))
+        return DSV4_ERR_INVALID_ARG;
+    if (int rc = device_check()) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), st) != cudaSuccess) return DSV4_ERR_LAUNCH;
+    TopkRows t;
+    t.scores = a->scores;
+    t.n_vis = a->n_vis;
+    t.n_comp = nullptr;
+    t.q_pos = nullptr;
+    t.n_q = 1;
+    t.ratio = 1;
+    t.idx_out = a->idx_out;
+    t.rows = a->rows;
+    t.max_comp = a->max_comp;
+    t.top_k = a->top_k;
+    return launch_topk(t, body_of(ws), eword_of(ws), st);
+}
+
+size_t dsv4_sparse_attn_workspace_size(const dsv4_attn_args* a) {
+    if (!a) return 0;
+    return kWsHeader + attn_ws_bytes(*a);
+}
+
+int dsv4_sparse_attn_decode(const dsv4_attn_args* a, void* ws, size_t ws_bytes, dsv4_stream_t stream) {
+    LaunchScope scope;
+    if (!attn_ok(a) || !dev_ptr_ok(ws) || ws_bytes < dsv4_sparse_attn_workspace_size(a))
+        return DSV4_ERR_INVALID_ARG;
+    if (int rc = device_check()) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), st) != cudaSuccess) return DSV4_ERR_LAUNCH;
+    return launch_attn(*a, body_of(ws), eword_of(ws), st);
+}
+
+static bool csa_ok(const dsv4_csa_args* a) {
+    if (!a || !a->attn || !attn_ok(a->attn)) return false;
+    if (a->compress_kv && !compress_ok(a->compress_kv)) return false;
+    if (a->compress_keys && !compress_ok(a->compress_keys)) return false;
+    if (a->index) {
+        const dsv4_index_args& x = *a->index;
+        const dsv4_attn_args& y = *a->attn;
+        if (!index_ok(&x)) return false;
+        if (y.idx != x.idx_out || y.top_k != x.top_k || y.batch != x.batch || y.n_q != x.n_q ||
+            y.max_comp != x.max_comp || y.n_comp != x.n_comp || y.ratio != x.ratio || y.q_pos != x.q_pos)
+            return false;
+    } else if (a->attn->idx) {
+        return false;
+    }
+    return true;
+}
+
+size_t dsv4_csa_decode_workspace_size(const dsv4_csa_args* a) {
+    if (!a || !a->attn) return 0;
+    size_t body = attn_ws_bytes(*a->attn);
+    if (a->index) {
+        const size_t b2 = index_ws_bytes(*a->index);
+        body = body > b2 ? body : b2;
+    }
+    return kWsHeader + body;
+}
+
+int dsv4_csa_decode(const dsv4_csa_args* a, void* ws, size_t ws_bytes, dsv4_stream_t stream) {
+    LaunchScope scope;
+    if (!csa_ok(a) || !dev_ptr_ok(ws) || ws_bytes < dsv4_csa_decode_workspace_size(a))
+        return DSV4_ERR_INVALID_ARG;
+    if (int rc = device_check()) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), st) != cudaSuccess) return DSV4_ERR_LAUNCH;
+    int rc = DSV4_OK;
+    if (a->compress_kv && (rc = launch_compress(*a->compress_kv, st))) return rc;
+    if (a->compress_keys && (rc = launch_compress(*a->compress_keys, st))) return rc;
+    if (a->index && (rc = launch_indexer(*a->index, body_of(ws), eword_of(ws), st))) return rc;
+    return launch_attn(*a->attn, body_of(ws), eword_of(ws), st);
+}
+
+int dsv4_read_error_word(void* ws, dsv4_stream_t stream, uint32_t* out) {
+    if (!dev_ptr_ok(ws) || !out) return DSV4_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t v = 0;
+    if (cudaMemcpyAsync(&v, ws, sizeof v, cudaMemcpyDeviceToHost, st) != cudaSuccess) return DSV4_ERR_LAUNCH;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return DSV4_ERR_LAUNCH;
+    if (cudaMemsetAsync(ws, 0, sizeof v, st) != cudaSuccess) return DSV4_ERR_LAUNCH;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return DSV4_ERR_LAUNCH;
+    *out = v;
+    if (v & DSV4_EWORD_TIMEOUT) return DSV4_ERR_TIMEOUT;
+    if (v & DSV4_EWORD_BAD_INDEX) return DSV4_ERR_BAD_INDEX;
+    return DSV4_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,489 @@
+// Gather into the caller's fixed buffer + shared-KV MQA attention with a per-head sink.
+//
+// Sources: "nvfp4-megamoe-kernel: compare v0.1-e2e-working...v-c1-c2-c3-20260602",
+// commit "C2" (one pre-allocated gather buffer of top_k + window rows), ARCHITECTURE_AND_
+// MEMORY_AUDIT.md "B2" (CSA gathers comp_kv[topk] then the window; HCA every compressed
+// entry then the window), fmha_6warp_tma_multirow_multitile.cuh "Sink bias correction" (the
+// sink is one extra logit in the scaled domain that adds to the denominator only),
+// PERFORMANCE_AUDIT.md "P4" (V is the gathered K row itself); "nvfp4-megamoe-kernel: compare
+// master..pure-nvfp4", single_shot_inference.py eager_attention (scale = 1/sqrt(hd)).
+//
+// Design (decode: few queries, many rows; prefill: many queries):
+//   * the row list of one query is its top_k compressed slots then its window slots; it is
+//     cut into 64-row chunks and the chunks into `n_splits` contiguous ranges, one CTA per
+//     (range, query) so that a 4-sequence decode still fills the GPU (split-K);
+//   * each CTA stages Q (heads x D, zero-padded to a multiple of 16 heads) once, then
+//     streams chunks through two cp.async buffers: the rows are gathered by index straight
+//     from the cache (16-byte copies), written to the gather buffer from shared memory, and
+//     consumed by bf16 tensor-core MMAs (fp32 accumulate): S = Q K^T, an online softmax in
+//     fp32, O += P V with P rounded to bf16;
+//   * a split writes (m, l, O) partials; the combine kernel merges them per (query, head)
+//     and adds the sink once: o = sum_s O_s e^(m_s-M) / (sum_s l_s e^(m_s-M) + e^(sink-M)),
+//     M = max(sink, m_s). With one split the CTA finishes the output itself.
+// Shared-memory rows use a 16-byte-chunk XOR swizzle (chunk ^ (row & 7)) so the ldmatrix
+// reads are free of bank conflicts.
+#include "common.cuh"
+#include "internal.h"
+
+namespace dsv4 {
+namespace {
+
+constexpr int kCH = 64;      // rows per chunk
+constexpr int kNT = 256;     // 8 warps
+
+struct AttnParams {
+    const __nv_bfloat16* q;        // [rows, H, D]
+    const float* sink;             // [H]
+    const __nv_bfloat16* comp_kv;  // [B, max_comp, D]
+    const int32_t* n_comp;         // [B]
+    const int32_t* idx;            // [rows, top_k] or null
+    const int64_t* q_pos;          // [rows] or null
+    const __nv_bfloat16* win;      // [B, win_rows, D]
+    const int32_t* win_len;        // [B]
+    __nv_bfloat16* gather;         // [rows, slots, D] or null
+    __nv_bfloat16* out;            // [rows, H, D]
+    float* part_ml;                // [rows, n_splits, HP, 2]
+    float* part_o;                 // [rows, n_splits, HP, D]
+    uint32_t* eword;
+    int rows, n_q, H, max_comp, top_k, window, win_rows, ratio, slots, n_chunks,
+        chunks_per_split, n_splits;
+    float scale;
+};
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_u32(smem)), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t* r) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t* r) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
+                 : "=r"(r[0]), "=r"(r[1]) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t* r) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// byte offset of 16-byte chunk `c` of row `r` in a swizzled array with ROWB bytes per row
+template <int ROWB>
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+    return static_cast<uint32_t>(r * ROWB + ((c ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+template <int D, int HP>
+struct Cfg {
+    static constexpr int NHG = HP / 16;         // 16-head groups
+    static constexpr int NRG = 8 / NHG;         // row groups of the S tile
+    static constexpr int RW = kCH / NRG;        // chunk rows per warp in S
+    static constexpr int NDG = 8 / NHG;         // dim groups of the O tile
+    static constexpr int DW = D / NDG;          // dims per warp in O
+    static constexpr int ROWB = D * 2;
+    static constexpr size_t OFF_KV = static_cast<size_t>(HP) * ROWB;
+    static constexpr size_t OFF_P = OFF_KV + 2ull * kCH * ROWB;
+    static constexpr size_t OFF_F = OFF_P + static_cast<size_t>(HP) * 128;
+    static constexpr size_t N_F = 2ull * NRG * HP + 3ull * HP;
+    static constexpr size_t OFF_SRC = align_up(OFF_F + N_F * 4, 16);
+    static constexpr size_t SMEM = OFF_SRC + 2ull * kCH * sizeof(void*);
+    static_assert(RW % 8 == 0 && DW % 16 == 0, "tile split");
+};
+
+template <int D, int HP>
+__global__ void __launch_bounds__(kNT, 1)
+attn_kernel(AttnParams p) {
+    using C = Cfg<D, HP>;
+    constexpr int ROWB = C::ROWB, CPR = D / 8;            // 16-byte chunks per row
+    extern __shared__ __align__(128) uint8_t sm[];
+    uint8_t* sQ = sm;
+    uint8_t* sKV = sm + C::OFF_KV;
+    uint8_t* sP = sm + C::OFF_P;
+    float* red_max = reinterpret_cast<float*>(sm + C::OFF_F);
+    float* red_sum = red_max + C::NRG * HP;
+    float* m_run = red_sum + C::NRG * HP;
+    float* l_run = m_run + HP;
+    float* alpha_s = l_run + HP;
+    const __nv_bfloat16** rowsrc = reinterpret_cast<const __nv_bfloat16**>(sm + C::OFF_SRC);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, tq = lane & 3;
+    const int row = blockIdx.y, split = blockIdx.x;
+    const int b = row / p.n_q, t = row - b * p.n_q;
+    const int nv = row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, row, p.eword);
+    int wl = p.win_len[b];
+    wl = wl < 0 ? 0 : (wl > p.win_rows ? p.win_rows : wl);
+    const int w_hi = t + wl - p.n_q;                       // the query's own window row
+    const int w_lo = w_hi - p.window + 1 > 0 ? w_hi - p.window + 1 : 0;
+    const int w_top = w_hi < wl - 1 ? w_hi : wl - 1;
+    const int w_cnt = w_top >= w_lo ? w_top - w_lo + 1 : 0;
+    const int kc = p.top_k;                                // compressed slots
+    const int c0 = split * p.chunks_per_split;
+    const int c1 = c0 + p.chunks_per_split < p.n_chunks ? c0 + p.chunks_per_split : p.n_chunks;
+
+    if (tid < HP) { m_run[tid] = -INFINITY; l_run[tid] = 0.f; }
+    // Q (rows >= H are zero)
+    for (int i = tid; i < HP * CPR; i += kNT) {
+        const int h = i / CPR, c = i - h * CPR;
+        uint8_t* dst = sQ + swz<ROWB>(h, c);
+        if (h < p.H) cp_async16(dst, p.q + (static_cast<size_t>(row) * p.H + h) * D + c * 8);
+        else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+    }
+    auto resolve = [&](int chunk, int buf) {
+        if (tid < kCH) {
+            const int slot = chunk * kCH + tid;
+            const __nv_bfloat16* src = nullptr;
+            if (slot < kc) {
+                int e;
+                if (p.idx) {
+                    e = p.idx[static_cast<size_t>(row) * p.top_k + slot];
+                    if (e >= nv) { flag_error(p.eword, DSV4_EWORD_BAD_INDEX); e = -1; }
+                } else {
+                    e = slot < nv ? slot : -1;
+                }
+                if (e >= 0) src = p.comp_kv + (static_cast<size_t>(b) * p.max_comp + e) * D;
+            } else if (slot < p.slots) {
+                const int wi = slot - kc;
+                if (wi < w_cnt) src = p.win + (static_cast<size_t>(b) * p.win_rows + w_lo + wi) * D;
+            }
+            rowsrc[buf * kCH + tid] = src;
+        }
+    };
+    auto load = [&](int buf) {
+        uint8_t* dstb = sKV + static_cast<size_t>(buf) * kCH * ROWB;
+        for (int i = tid; i < kCH * CPR; i += kNT) {
+            const int r = i / CPR, c = i - r * CPR;
+            const __nv_bfloat16* src = rowsrc[buf * kCH + r];
+            uint8_t* dst = dstb + swz<ROWB>(r, c);
+            if (src) cp_async16(dst, src + c * 8);
+            else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+        }
+    };
+
+    // warp roles inside the two tiles
+    const int hg = warp % C::NHG;
+    const int rg = warp / C::NHG;                          // S: row group
+    const int dg = warp / C::NHG;                          // O: dim group
+    const int h0 = hg * 16 + g, h1 = h0 + 8;
+    float o[C::DW / 8][4];
+#pragma unroll
+    for (int i = 0; i < C::DW / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+
+    if (c0 < c1) {
+        resolve(c0, 0);
+        __syncthreads();
+        load(0);
+    }
+    cp_async_commit();
+    for (int c = c0; c < c1; ++c) {
+        const int buf = (c - c0) & 1;
+        if (c + 1 < c1) {
+            resolve(c + 1, buf ^ 1);
+            __syncthreads();
+            load(buf ^ 1);
+        }
+        cp_async_commit();
+        cp_async_wait1();
+        __syncthreads();
+        const uint8_t* kvb = sKV + static_cast<size_t>(buf) * kCH * ROWB;
+        const __nv_bfloat16* const* src = rowsrc + buf * kCH;
+        // gather buffer: every slot of the chunk, zeros where masked
+        if (p.gather) {
+            for (int i = tid; i < kCH * CPR; i += kNT) {
+                const int r = i / CPR, cc = i - r * CPR;
+                const int slot = c * kCH + r;
+                if (slot >= p.slots) continue;
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (src[r]) v = *reinterpret_cast<const uint4*>(kvb + swz<ROWB>(r, cc));
+                *reinterpret_cast<uint4*>(p.gather + (static_cast<size_t>(row) * p.slots + slot) * D + cc * 8) = v;
+            }
+        }
+        // ---- S = Q K^T for (16 heads) x (RW rows)
+        float s[C::RW / 8][4];
+#pragma unroll
+        for (int i = 0; i < C::RW / 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+        const uint32_t qa = smem_u32(sQ), kva = smem_u32(kvb);
+#pragma unroll 4
+        for (int k0 = 0; k0 < D; k0 += 16) {
+            uint32_t a[4];
+            ldsm_x4(qa + swz<ROWB>(hg * 16 + (lane & 15), (k0 >> 3) + (lane >> 4)), a);
+            if constexpr (C::RW >= 16) {
+#pragma unroll
+                for (int n2 = 0; n2 < C::RW / 16; ++n2) {
+                    uint32_t bb[4];
+                    const int rb = C::RW * rg + 16 * n2 + (lane & 7) + ((lane >> 4) << 3);
+                    ldsm_x4(kva + swz<ROWB>(rb, (k0 >> 3) + ((lane >> 3) & 1)), bb);
+                    mma_bf16(s[2 * n2], a, bb[0], bb[1]);
+                    mma_bf16(s[2 * n2 + 1], a, bb[2], bb[3]);
+                }
+            } else {
+                uint32_t bb[2];
+                const int rb = C::RW * rg + (lane & 7);
+                ldsm_x2(kva + swz<ROWB>(rb, (k0 >> 3) + ((lane >> 3) & 1)), bb);
+                mma_bf16(s[0], a, bb[0], bb[1]);
+            }
+        }
+        // ---- mask, scale, chunk max per head
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < C::RW / 8; ++nt) {
+            const int col = C::RW * rg + 8 * nt + 2 * tq;
+            const bool v0 = src[col] != nullptr, v1 = src[col + 1] != nullptr;
+            s[nt][0] = v0 ? s[nt][0] * p.scale : -INFINITY;
+            s[nt][1] = v1 ? s[nt][1] * p.scale : -INFINITY;
+            s[nt][2] = v0 ? s[nt][2] * p.scale : -INFINITY;
+            s[nt][3] = v1 ? s[nt][3] * p.scale : -INFINITY;
+            mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
+            mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
+        }
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        if (tq == 0) { red_max[rg * HP + h0] = mx0; red_max[rg * HP + h1] = mx1; }
+        __syncthreads();
+        float mn0 = m_run[h0], mn1 = m_run[h1];
+#pragma unroll
+        for (int r = 0; r < C::NRG; ++r) {
+            mn0 = fmaxf(mn0, red_max[r * HP + h0]);
+            mn1 = fmaxf(mn1, red_max[r * HP + h1]);
+        }
+        // ---- P = exp(S - m), row sums, P to shared memory as bf16
+        float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < C::RW / 8; ++nt) {
+            const float p0 = s[nt][0] == -INFINITY ? 0.f : expf(s[nt][0] - mn0);
+            const float p1 = s[nt][1] == -INFINITY ? 0.f : expf(s[nt][1] - mn0);
+            const float p2 = s[nt][2] == -INFINITY ? 0.f : expf(s[nt][2] - mn1);
+            const float p3 = s[nt][3] == -INFINITY ? 0.f : expf(s[nt][3] - mn1);
+            sum0 += p0 + p1;
+            sum1 += p2 + p3;
+            const int col = C::RW * rg + 8 * nt + 2 * tq;
+            *reinterpret_cast<uint32_t*>(sP + swz<128>(h0, col >> 3) + (col & 7) * 2) = pack_bf16(p0, p1);
+            *reinterpret_cast<uint32_t*>(sP + swz<128>(h1, col >> 3) + (col & 7) * 2) = pack_bf16(p2, p3);
+        }
+        sum0 += __shfl_xor_sync(0xffffffffu, sum0, 1);
+        sum0 += __shfl_xor_sync(0xffffffffu, sum0, 2);
+        sum1 += __shfl_xor_sync(0xffffffffu, sum1, 1);
+        sum1 += __shfl_xor_sync(0xffffffffu, sum1, 2);
+        if (tq == 0) { red_sum[rg * HP + h0] = sum0; red_sum[rg * HP + h1] = sum1; }
+        __syncthreads();
+        if (tid < HP) {
+            const float mo = m_run[tid];
+            float mn = mo, ls = 0.f;
+#pragma unroll
+            for (int r = 0; r < C::NRG; ++r) { mn = fmaxf(mn, red_max[r * HP + tid]); ls += red_sum[r * HP + tid]; }
+            const float al = mo == -INFINITY ? 0.f : expf(mo - mn);
+            l_run[tid] = l_run[tid] * al + ls;
+            m_run[tid] = mn;
+            alpha_s[tid] = al;
+        }
+        __syncthreads();
+        // ---- O = O * alpha + P V for (16 heads) x (DW dims)
+        {
+            const float al0 = alpha_s[h0], al1 = alpha_s[h1];
+#pragma unroll
+            for (int i = 0; i < C::DW / 8; ++i) { o[i][0] *= al0; o[i][1] *= al0; o[i][2] *= al1; o[i][3] *= al1; }
+            const uint32_t pa = smem_u32(sP);
+#pragma unroll
+            for (int kk = 0; kk < kCH / 16; ++kk) {
+                uint32_t a[4];
+                ldsm_x4(pa + swz<128>(hg * 16 + (lane & 15), 2 * kk + (lane >> 4)), a);
+#pragma unroll
+                for (int n2 = 0; n2 < C::DW / 16; ++n2) {
+                    const int d0 = C::DW * dg + 16 * n2;
+                    uint32_t bb[4];
+                    ldsm_x4_t(kva + swz<ROWB>(16 * kk + (lane & 7) + (((lane >> 3) & 1) << 3), (d0 >> 3) + (lane >> 4)), bb);
+                    mma_bf16(o[2 * n2], a, bb[0], bb[1]);
+                    mma_bf16(o[2 * n2 + 1], a, bb[2], bb[3]);
+                }
+            }
+        }
+        __syncthreads();
+    }
+    cp_async_wait1();
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();
+    if (p.n_splits == 1) {
+        // finish here: sink once, normalise, bf16
+        const float* sk = p.sink;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int h = half ? h1 : h0;
+            if (h >= p.H) continue;
+            const float m = m_run[h], l = l_run[h], snk = sk[h];
+            const float M = fmaxf(m, snk);
+            const float em = m == -INFINITY ? 0.f : expf(m - M);
+            const float f = em / (l * em + expf(snk - M));
+            __nv_bfloat16* dst = p.out + (static_cast<size_t>(row) * p.H + h) * D;
+#pragma unroll
+            for (int i = 0; i < C::DW / 8; ++i) {
+                const int d = C::DW * dg + 8 * i + 2 * tq;
+                *reinterpret_cast<uint32_t*>(dst + d) = pack_bf16(o[i][2 * half] * f, o[i][2 * half + 1] * f);
+            }
+        }
+    } else {
+        const size_t part = static_cast<size_t>(row) * p.n_splits + split;
+        float* po = p.part_o + part * HP * D;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int h = half ? h1 : h0;
+#pragma unroll
+            for (int i = 0; i < C::DW / 8; ++i) {
+                const int d = C::DW * dg + 8 * i + 2 * tq;
+                *reinterpret_cast<float2*>(po + static_cast<size_t>(h) * D + d) =
+                    make_float2(o[i][2 * half], o[i][2 * half + 1]);
+            }
+        }
+        if (tid < HP) {
+            p.part_ml[(part * HP + tid) * 2 + 0] = m_run[tid];
+            p.part_ml[(part * HP + tid) * 2 + 1] = l_run[tid];
+        }
+    }
+}
+
+template <int D, int HP>
+__global__ void __launch_bounds__(128)
+attn_combine_kernel(AttnParams p) {
+    __shared__ float wgt[256];
+    __shared__ float den_s;
+    const int row = blockIdx.x, h = blockIdx.y;
+    const int ns = p.n_splits;
+    const float* ml = p.part_ml + static_cast<size_t>(row) * ns * HP * 2;
+    if (threadIdx.x == 0) {
+        const float snk = p.sink[h];
+        float M = snk;
+        for (int s = 0; s < ns; ++s) M = fmaxf(M, ml[(s * HP + h) * 2]);
+        float den = expf(snk - M);
+        for (int s = 0; s < ns; ++s) {
+            const float m = ml[(s * HP + h) * 2], l = ml[(s * HP + h) * 2 + 1];
+            const float e = m == -INFINITY ? 0.f : expf(m - M);
+            wgt[s] = e;
+            den += l * e;
+        }
+        den_s = den;
+    }
+    __syncthreads();
+    const float inv = 1.0f / den_s;
+    const float* po = p.part_o + static_cast<size_t>(row) * ns * HP * D;
+    for (int d = threadIdx.x; d < D; d += 128) {
+        float acc = 0.f;
+        for (int s = 0; s < ns; ++s) acc = fmaf(po[(static_cast<size_t>(s) * HP + h) * D + d], wgt[s], acc);
+        p.out[(static_cast<size_t>(row) * p.H + h) * D + d] = __float2bfloat16_rn(acc * inv);
+    }
+}
+
+struct Plan { int slots, n_chunks, chunks_per_split, n_splits, hp; };
+
+Plan make_plan(const dsv4_attn_args& a) {
+    Plan pl;
+    const int rows = a.batch * a.n_q;
+    pl.slots = a.top_k + a.window;
+    pl.n_chunks = (pl.slots + kCH - 1) / kCH;
+    pl.hp = a.heads <= 16 ? 16 : (a.heads <= 32 ? 32 : 64);
+    const int sms = sm_count() > 0 ? sm_count() : 148;
+    int want = rows > 0 ? (sms + rows - 1) / rows : 1;
+    if (want < 1) want = 1;
+    if (want > pl.n_chunks) want = pl.n_chunks;
+    if (want > 256) want = 256;
+    pl.chunks_per_split = pl.n_chunks > 0 ? (pl.n_chunks + want - 1) / want : 1;
+    pl.n_splits = pl.n_chunks > 0 ? (pl.n_chunks + pl.chunks_per_split - 1) / pl.chunks_per_split : 1;
+    return pl;
+}
+
+template <int D, int HP>
+int run(const dsv4_attn_args& a, const Plan& pl, uint8_t* ws, uint32_t* eword, cudaStream_t st) {
+    using C = Cfg<D, HP>;
+    AttnParams p;
+    p.q = static_cast<const __nv_bfloat16*>(a.q);
+    p.sink = a.sink;
+    p.comp_kv = static_cast<const __nv_bfloat16*>(a.comp_kv);
+    p.n_comp = a.n_comp;
+    p.idx = a.idx;
+    p.q_pos = a.q_pos;
+    p.win = static_cast<const __nv_bfloat16*>(a.win);
+    p.win_len = a.win_len;
+    p.gather = static_cast<__nv_bfloat16*>(a.gather);
+    p.out = static_cast<__nv_bfloat16*>(a.out);
+    p.eword = eword;
+    p.rows = a.batch * a.n_q;
+    p.n_q = a.n_q;
+    p.H = a.heads;
+    p.max_comp = a.max_comp;
+    p.top_k = a.top_k;
+    p.window = a.window;
+    p.win_rows = a.win_rows;
+    p.ratio = a.ratio;
+    p.slots = pl.slots;
+    p.n_chunks = pl.n_chunks;
+    p.chunks_per_split = pl.chunks_per_split;
+    p.n_splits = pl.n_splits;
+    p.scale = a.scale;
+    const size_t ml_bytes = align_up(static_cast<size_t>(p.rows) * pl.n_splits * HP * 2 * 4, 256);
+    p.part_ml = reinterpret_cast<float*>(ws);
+    p.part_o = reinterpret_cast<float*>(ws + ml_bytes);
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaFuncSetAttribute(attn_kernel<D, HP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(C::SMEM));
+        attr_set = true;
+    }
+    dim3 grid(pl.n_splits, p.rows);
+    attn_kernel<D, HP><<<grid, kNT, C::SMEM, st>>>(p);
+    count_launch();
+    if (cudaGetLastError() != cudaSuccess) return DSV4_ERR_LAUNCH;
+    if (pl.n_splits > 1) {
+        dim3 g2(p.rows, a.heads);
+        attn_combine_kernel<D, HP><<<g2, 128, 0, st>>>(p);
+        count_launch();
+        if (cudaGetLastError() != cudaSuccess) return DSV4_ERR_LAUNCH;
+    }
+    return DSV4_OK;
+}
+
+}  // namespace
+
+size_t attn_ws_bytes(const dsv4_attn_args& a) {
+    const Plan pl = make_plan(a);
+    if (pl.n_splits <= 1) return 0;
+    const size_t rows = static_cast<size_t>(a.batch) * a.n_q;
+    return align_up(rows * pl.n_splits * pl.hp * 2 * 4, 256) +
+           align_up(rows * pl.n_splits * pl.hp * static_cast<size_t>(a.dim) * 4, 256);
+}
+
+int launch_attn(const dsv4_attn_args& a, uint8_t* ws, uint32_t* eword, cudaStream_t st) {
+    if (a.batch * a.n_q == 0) return DSV4_OK;
+    const Plan pl = make_plan(a);
+    if (a.dim == 512) {
+        if (pl.hp == 16) return run<512, 16>(a, pl, ws, eword, st);
+        if (pl.hp == 32) return run<512, 32>(a, pl, ws, eword, st);
+        return run<512, 64>(a, pl, ws, eword, st);
+    }
+    if (a.dim == 256) {
+        if (pl.hp == 16) return run<256, 16>(a, pl, ws, eword, st);
+        if (pl.hp == 32) return run<256, 32>(a, pl, ws, eword, st);
+        return run<256, 64>(a, pl, ws, eword, st);
+    }
+    if (a.dim == 128) {
+        if (pl.hp == 16) return run<128, 16>(a, pl, ws, eword, st);
+        if (pl.hp == 32) return run<128, 32>(a, pl, ws, eword, st);
+        return run<128, 64>(a, pl, ws, eword, st);
+    }
+    return DSV4_ERR_INVALID_ARG;
+}
+
+}  // namespace dsv4

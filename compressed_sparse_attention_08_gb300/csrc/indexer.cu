@@ -1,0 +1,351 @@
+// Lightning-indexer scoring on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+//   I[row, j] = sum_h w[row, h] * ReLU( q[row, h, :] . keys[b, j, :] )      row = b * n_q + t
+//
+// Sources: "nvfp4-megamoe-kernel: compare v0.1-e2e-working...v-c1-c2-c3-20260602",
+// ARCHITECTURE_AND_MEMORY_AUDIT.md "F1" (one 128-wide compressed key per block, shared by
+// all indexer heads: MQA) and "F3" (the scoring formula, fp32, no scale); PERFORMANCE_AUDIT.md
+// "P6" (the fp32 einsum on CUDA cores is the wall at long context).
+//
+// Why tensor cores: every 256-byte key meets 64 heads x 128 dims = 16,384 flops, 64 flop per
+// byte. Streaming keys at HBM speed needs ~430 TFLOP/s, far above the CUDA-core fp32 rate,
+// so the contraction runs as a UMMA with the keys as the A operand:
+//     D[128 keys x N heads] (fp32, TMEM) = K_tile[128 x 128] . Q^T[128 x N]
+// Each row of D is one key's per-head dot products, so the epilogue thread that owns TMEM
+// lane i reduces sum_h w_h ReLU(D[i, h]) alone, with no cross-thread reduction.
+//
+// CTA = 6 warps, persistent, one per SM, warp-specialised:
+//   warp 0  TMA producer: key tiles (128 keys x 128 dims, two 128-byte-swizzled halves)
+//           into a ring of kStages buffers; the row's queries (N x 128) into one of two buffers
+//   warp 1  MMA issuer (one thread) and TMEM owner: 8 UMMAs (K = 16 each) per tile into one
+//           of kAccBufs TMEM accumulators; tcgen05.commit frees the smem stage and publishes
+//           the accumulator
+//   warps 2-5  epilogue: tcgen05.ld of the 64-column accumulator (thread = key), weighted
+//           ReLU sum in fp32, coalesced store of the score.
+// Work: the (row, key tile) pairs, cut into one contiguous range per CTA. Tiles past the
+// row's visible count are skipped by all three roles alike.
+#include "common.cuh"
+#include "internal.h"
+
+#include <cudaTypedefs.h>
+
+namespace dsv4 {
+namespace {
+
+constexpr int kTileKeys = 128;              // UMMA M
+constexpr int kDim = 128;                   // key width = UMMA K total
+constexpr int kMaxHeads = 64;               // UMMA N upper bound
+constexpr int kStages = 5;
+constexpr int kAccBufs = 4;
+constexpr int kAccCols = 64;                // TMEM columns per accumulator
+constexpr uint32_t kTmemCols = kAccBufs * kAccCols;   // 256 (power of two)
+constexpr uint32_t kKeyTileBytes = kTileKeys * kDim * 2;   // 32 KiB
+constexpr uint32_t kKeyHalfBytes = kKeyTileBytes / 2;      // 128 keys x 64 dims
+constexpr uint32_t kQBufBytes = kMaxHeads * kDim * 2;      // 16 KiB
+constexpr int kThreads = 192;
+constexpr size_t kSmemBytes = 1024 + kStages * kKeyTileBytes + 2 * kQBufBytes;
+
+struct ScoreParams {
+    const float* w;          // [rows, heads]
+    const int32_t* n_comp;   // [batch]
+    const int64_t* q_pos;    // [rows] or null
+    float* scores;           // [rows, max_comp]
+    uint32_t* eword;
+    int rows, n_q, heads, n_pad, max_comp, ratio, tiles_per_row;
+};
+
+struct WorkRange { long long begin, end; };
+
+__device__ __forceinline__ WorkRange cta_range(long long total) {
+    const long long g = gridDim.x, c = blockIdx.x;
+    return {total * c / g, total * (c + 1) / g};
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+index_score_kernel(const __grid_constant__ CUtensorMap kmap,
+                   const __grid_constant__ CUtensorMap qmap, ScoreParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint64_t full_bar[kStages], empty_bar[kStages];
+    __shared__ uint64_t tfull_bar[kAccBufs], tempty_bar[kAccBufs];
+    __shared__ uint64_t qfull_bar[2], qempty_bar[2], done_bar;
+    __shared__ uint32_t tmem_slot;
+    __shared__ volatile int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // 1024-byte aligned operand buffers (the 128-byte swizzle repeats every 1024 bytes)
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* base = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    uint8_t* key_buf = base;
+    uint8_t* q_buf = base + kStages * kKeyTileBytes;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) { mbar_init(&full_bar[i], 1); mbar_init(&empty_bar[i], 1); }
+        for (int i = 0; i < kAccBufs; ++i) { mbar_init(&tfull_bar[i], 1); mbar_init(&tempty_bar[i], 128); }
+        for (int i = 0; i < 2; ++i) { mbar_init(&qfull_bar[i], 1); mbar_init(&qempty_bar[i], 1); }
+        mbar_init(&done_bar, 1);
+        abort_flag = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&qmap);
+    }
+    // query rows past `heads` stay zero for the whole kernel (TMA writes only `heads` rows)
+    for (uint32_t i = threadIdx.x; i < 2 * kQBufBytes / 16; i += kThreads)
+        reinterpret_cast<uint4*>(q_buf)[i] = make_uint4(0, 0, 0, 0);
+    if (warp == 1) tmem_alloc(&tmem_slot, kTmemCols);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = tmem_slot;
+
+    const long long total = static_cast<long long>(p.rows) * p.tiles_per_row;
+    const WorkRange wr = cta_range(total);
+    const uint32_t idesc = idesc_bf16_f32(kTileKeys, p.n_pad);
+    const uint32_t q_half = static_cast<uint32_t>(p.n_pad) * 128u;   // bytes of one 64-dim half
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0, qcount = 0, cur_row = -1, nv = 0;
+            long long issued = 0;
+            uint32_t phase = 0;
+            for (long long t = wr.begin; t < wr.end; ++t) {
+                const int row = static_cast<int>(t / p.tiles_per_row);
+                const int tile = static_cast<int>(t % p.tiles_per_row);
+                if (row != cur_row)
+                    nv = row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, row, nullptr);
+                if (tile * kTileKeys >= nv) continue;
+                if (row != cur_row) {
+                    const int qs = qcount & 1;
+                    if (!mbar_wait(&qempty_bar[qs], ((qcount >> 1) & 1) ^ 1, &abort_flag)) goto fail0;
+                    mbar_arrive_expect_tx(&qfull_bar[qs], static_cast<uint32_t>(p.heads) * kDim * 2);
+                    uint8_t* qd = q_buf + qs * kQBufBytes;
+                    tma_load_2d(qd, &qmap, &qfull_bar[qs], 0, row * p.heads);
+                    tma_load_2d(qd + q_half, &qmap, &qfull_bar[qs], 64, row * p.heads);
+                    cur_row = row;
+                    ++qcount;
+                }
+                if (!mbar_wait(&empty_bar[stage], phase ^ 1, &abort_flag)) goto fail0;
+                mbar_arrive_expect_tx(&full_bar[stage], kKeyTileBytes);
+                {
+                    uint8_t* kd = key_buf + stage * kKeyTileBytes;
+                    const int b = row / p.n_q;
+                    tma_load_3d(kd, &kmap, &full_bar[stage], 0, tile * kTileKeys, b);
+                    tma_load_3d(kd + kKeyHalfBytes, &kmap, &full_bar[stage], 64, tile * kTileKeys, b);
+                    ++issued;
+                }
+                if (++stage == kStages) { stage = 0; phase ^= 1; }
+            }
+            goto done0;
+        fail0:
+            flag_error(p.eword, DSV4_EWORD_TIMEOUT);
+            abort_flag = 1;
+            // let the copies this thread started land before the CTA can exit (bounded)
+            for (long long i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
+                mbar_wait(&full_bar[i % kStages], static_cast<uint32_t>((i / kStages) & 1), nullptr, 100000000ull);
+            if (qcount > 0)
+                mbar_wait(&qfull_bar[(qcount - 1) & 1], static_cast<uint32_t>(((qcount - 1) >> 1) & 1), nullptr, 100000000ull);
+        done0:;
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int stage = 0, acc = 0, qcount = 0, qs = 0, cur_row = -1, nv = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            for (long long t = wr.begin; t < wr.end; ++t) {
+                const int row = static_cast<int>(t / p.tiles_per_row);
+                const int tile = static_cast<int>(t % p.tiles_per_row);
+                int row_nv = nv;
+                if (row != cur_row)
+                    row_nv = row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, row, nullptr);
+                if (tile * kTileKeys >= row_nv) continue;
+                if (row != cur_row) {
+                    if (cur_row >= 0) umma_commit(&qempty_bar[qs]);   // old queries free once done
+                    qs = qcount & 1;
+                    if (!mbar_wait(&qfull_bar[qs], (qcount >> 1) & 1, &abort_flag)) goto fail1;
+                    cur_row = row;
+                    nv = row_nv;
+                    ++qcount;
+                }
+                if (!mbar_wait(&full_bar[stage], phase, &abort_flag)) goto fail1;
+                if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1, &abort_flag)) goto fail1;
+                tc_fence_after();
+                {
+                    const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kAccCols);
+                    const uint32_t a0 = smem_u32(key_buf + stage * kKeyTileBytes);
+                    const uint32_t b0 = smem_u32(q_buf + qs * kQBufBytes);
+#pragma unroll
+                    for (int k = 0; k < kDim / 16; ++k) {
+                        const uint64_t ad = sdesc_kmajor_sw128(a0 + (k >> 2) * kKeyHalfBytes + (k & 3) * 32);
+                        const uint64_t bd = sdesc_kmajor_sw128(b0 + (k >> 2) * q_half + (k & 3) * 32);
+                        umma_bf16(d, ad, bd, idesc, k > 0 ? 1u : 0u);
+                    }
+                }
+                umma_commit(&empty_bar[stage]);
+                umma_commit(&tfull_bar[acc]);
+                if (++stage == kStages) { stage = 0; phase ^= 1; }
+                if (++acc == kAccBufs) { acc = 0; acc_phase ^= 1; }
+            }
+            goto done1;
+        fail1:
+            flag_error(p.eword, DSV4_EWORD_TIMEOUT);
+            abort_flag = 1;
+        done1:
+            // every MMA issued by this thread has completed before TMEM is released
+            umma_commit(&done_bar);
+            if (!mbar_wait(&done_bar, 0, nullptr)) flag_error(p.eword, DSV4_EWORD_TIMEOUT);
+        }
+        __syncwarp();
+    } else {
+        // epilogue: warps 2..5 -> TMEM lane quarter (warp % 4)
+        const int quarter = warp & 3;
+        const int lrow = quarter * 32 + lane;
+        const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+        int acc = 0, cur_row = -1, nv = 0;
+        uint32_t acc_phase = 0;
+        float wv[kMaxHeads];
+        for (long long t = wr.begin; t < wr.end; ++t) {
+            const int row = static_cast<int>(t / p.tiles_per_row);
+            const int tile = static_cast<int>(t % p.tiles_per_row);
+            if (row != cur_row) {
+                nv = row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, row, nullptr);
+                cur_row = row;
+#pragma unroll
+                for (int h = 0; h < kMaxHeads; ++h)
+                    wv[h] = h < p.heads ? __ldg(&p.w[static_cast<size_t>(row) * p.heads + h]) : 0.f;
+            }
+            if (tile * kTileKeys >= nv) continue;
+            if (!mbar_wait(&tfull_bar[acc], acc_phase, &abort_flag)) {
+                flag_error(p.eword, DSV4_EWORD_TIMEOUT);
+                abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            uint32_t r[64];
+            DSV4_TMEM_LD_32x32b_X64(tmem_base + lane_addr + static_cast<uint32_t>(acc * kAccCols), r);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(&tempty_bar[acc]);
+            float s = 0.f;
+#pragma unroll
+            for (int h = 0; h < kMaxHeads; ++h) s = fmaf(wv[h], fmaxf(__uint_as_float(r[h]), 0.f), s);
+            const int key = tile * kTileKeys + lrow;
+            if (key < nv) p.scores[static_cast<size_t>(row) * p.max_comp + key] = s;
+            if (++acc == kAccBufs) { acc = 0; acc_phase ^= 1; }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+}  // namespace
+
+size_t index_ws_bytes(const dsv4_index_args& a) {
+    const int rows = a.batch * a.n_q;
+    size_t b = 0;
+    if (!a.scores_out) b += align_up(static_cast<size_t>(rows) * a.max_comp * 4, 256);
+    b += topk_ws_bytes(rows, a.max_comp, a.top_k);
+    return b;
+}
+
+namespace {
+int launch_scores(const dsv4_index_args& a, float* scores, uint32_t* eword, cudaStream_t stream) {
+    const int rows = a.batch * a.n_q;
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode) return DSV4_ERR_LAUNCH;
+    CUtensorMap kmap, qmap;
+    {
+        cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(a.max_comp),
+                              static_cast<cuuint64_t>(a.batch)};
+        cuuint64_t strides[2] = {kDim * 2ull, static_cast<cuuint64_t>(a.max_comp) * kDim * 2ull};
+        cuuint32_t box[3] = {64, kTileKeys, 1};
+        cuuint32_t estr[3] = {1, 1, 1};
+        if (encode(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.keys), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return DSV4_ERR_LAUNCH;
+    }
+    {
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(rows) * a.heads};
+        cuuint64_t strides[1] = {kDim * 2ull};
+        cuuint32_t box[2] = {64, static_cast<cuuint32_t>(a.heads)};
+        cuuint32_t estr[2] = {1, 1};
+        if (encode(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.q), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return DSV4_ERR_LAUNCH;
+    }
+    ScoreParams p;
+    p.w = a.w;
+    p.n_comp = a.n_comp;
+    p.q_pos = a.q_pos;
+    p.scores = scores;
+    p.eword = eword;
+    p.rows = rows;
+    p.n_q = a.n_q;
+    p.heads = a.heads;
+    p.n_pad = (a.heads + 15) / 16 * 16;
+    p.max_comp = a.max_comp;
+    p.ratio = a.ratio;
+    p.tiles_per_row = (a.max_comp + kTileKeys - 1) / kTileKeys;
+    const long long total = static_cast<long long>(rows) * p.tiles_per_row;
+    if (total > 0) {
+        static bool attr_set = false;
+        if (!attr_set) {
+            cudaFuncSetAttribute(index_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSmemBytes));
+            attr_set = true;
+        }
+        long long grid = sm_count();
+        if (grid > total) grid = total;
+        index_score_kernel<<<static_cast<int>(grid), kThreads, kSmemBytes, stream>>>(kmap, qmap, p);
+        count_launch();
+        if (cudaGetLastError() != cudaSuccess) return DSV4_ERR_LAUNCH;
+    }
+    return DSV4_OK;
+}
+}  // namespace
+
+int launch_index_score(const dsv4_index_args& a, uint32_t* eword, cudaStream_t stream) {
+    if (a.batch * a.n_q == 0) return DSV4_OK;
+    return launch_scores(a, a.scores_out, eword, stream);
+}
+
+int launch_indexer(const dsv4_index_args& a, uint8_t* ws, uint32_t* eword, cudaStream_t stream) {
+    const int rows = a.batch * a.n_q;
+    if (rows == 0) return DSV4_OK;
+    float* scores = a.scores_out;
+    uint8_t* rest = ws;
+    if (!scores) {
+        scores = reinterpret_cast<float*>(ws);
+        rest = ws + align_up(static_cast<size_t>(rows) * a.max_comp * 4, 256);
+    }
+    if (int rc = launch_scores(a, scores, eword, stream)) return rc;
+    TopkRows t;
+    t.scores = scores;
+    t.n_vis = nullptr;
+    t.n_comp = a.n_comp;
+    t.q_pos = a.q_pos;
+    t.n_q = a.n_q;
+    t.ratio = a.ratio;
+    t.idx_out = a.idx_out;
+    t.rows = rows;
+    t.max_comp = a.max_comp;
+    t.top_k = a.top_k;
+    return launch_topk(t, rest, eword, stream);
+}
+
+}  // namespace dsv4

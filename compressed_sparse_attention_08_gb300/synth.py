@@ -24,6 +24,10 @@ Ann. Math. Statist. 1958.
 """
 from __future__ import annotations
 
+import ctypes
+import os
+import subprocess
+
 import numpy as np
 
 _G = np.uint64(0x9E3779B97F4A7C15)
@@ -87,8 +91,39 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
     return (np.ascontiguousarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
-def normal_f32(seed: int, tensor_id: int, shape, mean: float = 0.0, std: float = 1.0) -> np.ndarray:
-    """float32 array of N(mean, std) draws for stream (seed, tensor_id)."""
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_FILL_SRC = os.path.join(_HERE, "synth_fill.c")
+_FILL_LIB = os.path.join(_HERE, "_synth_fill.so")
+_fill = None
+
+
+def _fill_lib():
+    """The multithreaded C fill (same stream, same bits); None if it cannot be built."""
+    global _fill
+    if _fill is None:
+        try:
+            if not os.path.exists(_FILL_LIB) or os.path.getmtime(_FILL_LIB) < os.path.getmtime(_FILL_SRC):
+                tmp = _FILL_LIB + f".tmp{os.getpid()}"
+                subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-fPIC", "-shared",
+                                       "-pthread", _FILL_SRC, "-o", tmp, "-lm"])
+                os.replace(tmp, _FILL_LIB)
+            lib = ctypes.CDLL(_FILL_LIB)
+            for f in (lib.synth_normal_bf16, lib.synth_normal_f32):
+                f.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_double,
+                              ctypes.c_double, ctypes.c_void_p, ctypes.c_int]
+                f.restype = None
+            _fill = lib
+        except (OSError, subprocess.CalledProcessError):
+            _fill = False
+    return _fill or None
+
+
+def _threads():
+    return max(1, min(32, os.cpu_count() or 1))
+
+
+def normal_f32_numpy(seed: int, tensor_id: int, shape, mean: float = 0.0, std: float = 1.0) -> np.ndarray:
+    """float32 array of N(mean, std) draws for stream (seed, tensor_id) (numpy implementation)."""
     n = int(np.prod(shape)) if len(shape) else 1
     key = _stream_key(seed, tensor_id)
     out = np.empty(n, dtype=np.float32)
@@ -98,14 +133,38 @@ def normal_f32(seed: int, tensor_id: int, shape, mean: float = 0.0, std: float =
     return out.reshape(shape)
 
 
-def normal_bf16(seed: int, tensor_id: int, shape, mean: float = 0.0, std: float = 1.0) -> np.ndarray:
-    """bfloat16 bit patterns (uint16 array) of N(mean, std) draws for stream (seed, tensor_id)."""
+def normal_bf16_numpy(seed: int, tensor_id: int, shape, mean: float = 0.0, std: float = 1.0) -> np.ndarray:
+    """bfloat16 bit patterns of N(mean, std) draws for stream (seed, tensor_id) (numpy)."""
     n = int(np.prod(shape)) if len(shape) else 1
     key = _stream_key(seed, tensor_id)
     out = np.empty(n, dtype=np.uint16)
     for s in range(0, n, _CHUNK):
         c = min(_CHUNK, n - s)
         out[s:s + c] = f32_to_bf16_bits((mean + std * _normals_f64(key, s, c)).astype(np.float32))
+    return out.reshape(shape)
+
+
+def normal_f32(seed: int, tensor_id: int, shape, mean: float = 0.0, std: float = 1.0) -> np.ndarray:
+    """float32 array of N(mean, std) draws for stream (seed, tensor_id)."""
+    lib = _fill_lib()
+    if lib is None:
+        return normal_f32_numpy(seed, tensor_id, shape, mean, std)
+    n = int(np.prod(shape)) if len(shape) else 1
+    out = np.empty(n, dtype=np.float32)
+    lib.synth_normal_f32(int(_stream_key(seed, tensor_id)), 0, n, float(mean), float(std),
+                         out.ctypes.data, _threads())
+    return out.reshape(shape)
+
+
+def normal_bf16(seed: int, tensor_id: int, shape, mean: float = 0.0, std: float = 1.0) -> np.ndarray:
+    """bfloat16 bit patterns (uint16 array) of N(mean, std) draws for stream (seed, tensor_id)."""
+    lib = _fill_lib()
+    if lib is None:
+        return normal_bf16_numpy(seed, tensor_id, shape, mean, std)
+    n = int(np.prod(shape)) if len(shape) else 1
+    out = np.empty(n, dtype=np.uint16)
+    lib.synth_normal_bf16(int(_stream_key(seed, tensor_id)), 0, n, float(mean), float(std),
+                          out.ctypes.data, _threads())
     return out.reshape(shape)
 
 

@@ -121,6 +121,12 @@ size_t dsv4_indexer_topk_workspace_size(const dsv4_index_args* args);
 int dsv4_indexer_topk(const dsv4_index_args* args, void* ws, size_t ws_bytes,
                       dsv4_stream_t stream);
 
+/* The scoring half of stage 2 alone: writes I[s, t, j] for the visible j into
+ * args->scores_out (required here) and leaves idx_out untouched. Same sources as above. */
+size_t dsv4_index_score_workspace_size(const dsv4_index_args* args);
+int dsv4_index_score(const dsv4_index_args* args, void* ws, size_t ws_bytes,
+                     dsv4_stream_t stream);
+
 /* ---------------------------------------------------------------------------------------
  * Stage 3 alone. Top-k of caller-given fp32 scores, same rule as above.
  * scores [rows, max_comp]; n_vis [rows] visible counts; idx_out [rows, top_k].

@@ -292,7 +292,7 @@ int oracle_sparse_attn(const uint16_t* q, const float* sink, const uint16_t* com
             int64_t lo = hi - window + 1;
             if (lo < 0) lo = 0;
             int slot = 0;
-            for (int64_t r = lo; r <= hi && r < win_len[b]; ++r, ++slot) {
+            for (int64_t r = lo; r <= hi && r < win_len[b] && slot < window; ++r, ++slot) {
                 const uint16_t* src = win + (static_cast<size_t>(b) * win_rows + r) * D;
                 rows.push_back(src);
                 if (g) std::memcpy(g + static_cast<size_t>(top_k + slot) * D, src, sizeof(uint16_t) * D);

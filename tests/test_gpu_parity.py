@@ -1,0 +1,459 @@
+"""GPU parity: every stage of the CSA step against the fp64 oracle on seeded inputs.
+
+Runs through the C ABI (ctypes binding) on cuda:0. Sizes: the five workloads at full size
+(the oracle checks sampled sequences/queries where a full check would take minutes), plus
+small ragged and degenerate cases.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+from compressed_sparse_attention_08_gb300 import synth
+from compressed_sparse_attention_08_gb300.workloads import WORKLOADS, make_inputs
+from helpers import (assert_bf16_close, check_topk_row, dev, dev_bf16, host_bf16,
+                     topk_valid_for_scores, bf16_to_f64)
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from compressed_sparse_attention_08_gb300 import _build
+    _build.build()
+
+
+def csa():
+    import compressed_sparse_attention_08_gb300 as m
+    return m
+
+
+def ws_tensor(nbytes):
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device="cuda")
+
+
+_INPUTS = {}
+
+
+def inputs(cfg):
+    if cfg not in _INPUTS:
+        _INPUTS[cfg] = make_inputs(WORKLOADS[cfg])
+    return _INPUTS[cfg]
+
+
+def _oracle_keys(x, wl):
+    """Compressed indexer keys for workloads that compress the whole context (oracle)."""
+    bits, _ = oracle.compress(x["C_I"], x["Z_I"], x["bias_I"], x["gamma_I"], x["pos0"], wl.ratio,
+                              wl.rope_dim)
+    return bits
+
+
+def _oracle_kv(x, wl, seqs=None):
+    C, Z, pos0 = x["C"], x["Z"], x["pos0"]
+    if seqs is not None:
+        C, Z, pos0 = C[seqs], Z[seqs], pos0[seqs]
+    return oracle.compress(C, Z, x["bias"], x["gamma"], pos0, wl.ratio, wl.rope_dim)
+
+
+def _gpu_compress(C, Z, bias, gamma, pos0, ratio, out_rows=None, out_row0=None, out=None, rope_dim=64):
+    m = csa()
+    B, T, d = C.shape
+    if out is None:
+        out = torch.zeros(B, out_rows or T // ratio, d, dtype=torch.bfloat16, device="cuda")
+    m.dsv4_compress(dev_bf16(C), dev_bf16(Z), dev(bias), dev(gamma), dev(pos0), out, ratio=ratio,
+                    rope_dim=rope_dim, out_row0=None if out_row0 is None else dev(out_row0))
+    torch.cuda.synchronize()
+    return out
+
+
+# ------------------------------------------------------------------ stage 1: compressor
+@pytest.mark.parametrize("cfg", [0, 1])
+def test_compress_full_context(cfg):
+    wl = WORKLOADS[cfg]
+    x = inputs(cfg)
+    got = host_bf16(_gpu_compress(x["C"], x["Z"], x["bias"], x["gamma"], x["pos0"], wl.ratio))
+    seqs = None if cfg == 0 else [0, 7, 15]
+    _, ref = _oracle_kv(x, wl, seqs)
+    assert_bf16_close(got if seqs is None else got[seqs], ref, f"cfg{cfg} main KV")
+    gk = host_bf16(_gpu_compress(x["C_I"], x["Z_I"], x["bias_I"], x["gamma_I"], x["pos0"], wl.ratio))
+    _, rk = oracle.compress(x["C_I"], x["Z_I"], x["bias_I"], x["gamma_I"], x["pos0"], wl.ratio, wl.rope_dim)
+    assert_bf16_close(gk, rk, f"cfg{cfg} indexer keys")
+
+
+def test_compress_hca_ratio128():
+    wl = WORKLOADS[2]
+    x = inputs(2)
+    got = host_bf16(_gpu_compress(x["C"], x["Z"], x["bias"], x["gamma"], x["pos0"], wl.ratio))
+    seqs = [0, 31, 63]
+    _, ref = _oracle_kv(x, wl, seqs)
+    assert got.shape == (64, 64, 512)
+    assert_bf16_close(got[seqs], ref, "HCA ratio 128")
+
+
+def test_compress_newest_block_into_cache():
+    """1M context: the newest block of each sequence lands in row n_comp - 1 of the cache."""
+    wl = WORKLOADS[3]
+    x = inputs(3)
+    cache = torch.zeros(4, wl.max_comp, 512, dtype=torch.bfloat16, device="cuda")
+    _gpu_compress(x["C"], x["Z"], x["bias"], x["gamma"], x["pos0"], wl.ratio, out=cache,
+                  out_row0=x["append_row"])
+    _, ref = _oracle_kv(x, wl)
+    rows = host_bf16(cache[:, wl.max_comp - 1:wl.max_comp]).reshape(4, 1, 512)
+    assert_bf16_close(rows, ref, "newest block")
+    assert int(torch.count_nonzero(cache[:, :wl.max_comp - 1].view(torch.int16))) == 0
+
+
+def test_compress_prefill_chunk():
+    wl = WORKLOADS[4]
+    x = inputs(4)
+    cache = torch.zeros(1, wl.max_comp, 512, dtype=torch.bfloat16, device="cuda")
+    _gpu_compress(x["C"], x["Z"], x["bias"], x["gamma"], x["pos0"], wl.ratio, out=cache,
+                  out_row0=x["append_row"])
+    _, ref = _oracle_kv(x, wl)
+    got = host_bf16(cache[:, 16384:])
+    assert_bf16_close(got, ref, "prefill chunk entries")
+
+
+# ------------------------------------------------------------------ stage 2: indexer + top-k
+def _run_indexer(q, w, keys, n_comp, top_k, ratio=4, q_pos=None, want_scores=True):
+    m = csa()
+    B, n_q = q.shape[:2]
+    max_comp = keys.shape[1]
+    qd, wd, kd, nd = dev_bf16(q), dev(w), dev_bf16(keys), dev(n_comp)
+    pd = None if q_pos is None else dev(q_pos)
+    idx = torch.empty(B, n_q, top_k, dtype=torch.int32, device="cuda")
+    sc = torch.full((B, n_q, max_comp), float("nan"), dtype=torch.float32, device="cuda") if want_scores else None
+    nbytes = m.dsv4_indexer_topk_workspace_size(qd, wd, kd, nd, idx, ratio=ratio, q_pos=pd, scores_out=sc)
+    ws = ws_tensor(nbytes)
+    m.dsv4_indexer_topk(qd, wd, kd, nd, idx, ws, ratio=ratio, q_pos=pd, scores_out=sc)
+    torch.cuda.synchronize()
+    st, ew = m.dsv4_read_error_word(ws)
+    assert ew == 0, f"device error word {ew:#x}"
+    return idx.cpu().numpy(), (sc.cpu().numpy() if sc is not None else None)
+
+
+def _check_scores(got, ref, n_vis):
+    g = got[:n_vis].astype(np.float64)
+    r = ref[:n_vis]
+    scale = np.mean(np.abs(r)) + 1e-30
+    err = np.abs(g - r)
+    assert np.all(err <= 2e-5 * scale + 2e-5 * np.abs(r)), f"scores: max err {err.max():.3e} (scale {scale:.3e})"
+
+
+@pytest.mark.parametrize("cfg", [0, 1])
+def test_indexer_topk_decode(cfg):
+    wl = WORKLOADS[cfg]
+    x = inputs(cfg)
+    keys = _oracle_keys(x, wl)
+    idx, sc = _run_indexer(x["q_I"], x["w"], keys, x["n_comp"], wl.top_k)
+    ref_s, nv = oracle.index_scores(x["q_I"], x["w"], keys, x["n_comp"], wl.ratio)
+    ref_i = oracle.topk(ref_s, nv, wl.top_k)
+    swaps = 0
+    for b in range(wl.batch):
+        _check_scores(sc[b, 0], ref_s[b, 0], nv[b, 0])
+        swaps += check_topk_row(idx[b, 0], ref_i[b, 0], ref_s[b, 0], nv[b, 0], wl.top_k, f"b{b}")
+        topk_valid_for_scores(idx[b, 0], sc[b, 0], nv[b, 0], wl.top_k, f"b{b}")
+    assert swaps <= wl.batch
+
+
+def test_indexer_topk_1m_context():
+    """262,144 keys per sequence, top-2048: the long-row selection path."""
+    wl = WORKLOADS[3]
+    x = inputs(3)
+    idx, sc = _run_indexer(x["q_I"], x["w"], x["keys"], x["n_comp"], wl.top_k)
+    for b in range(4):
+        topk_valid_for_scores(idx[b, 0], sc[b, 0], wl.n_comp, wl.top_k, f"b{b}")
+    for b in (0, 3):
+        ref_s, nv = oracle.index_scores(x["q_I"][b:b + 1], x["w"][b:b + 1], x["keys"][b:b + 1],
+                                        x["n_comp"][b:b + 1], wl.ratio)
+        ref_i = oracle.topk(ref_s, nv, wl.top_k)
+        _check_scores(sc[b, 0], ref_s[0, 0], nv[0, 0])
+        check_topk_row(idx[b, 0], ref_i[0, 0], ref_s[0, 0], nv[0, 0], wl.top_k, f"b{b}")
+
+
+def test_indexer_topk_prefill_causal():
+    """2048 queries over 16,896 keys with the causal block rule; sampled queries vs oracle."""
+    wl = WORKLOADS[4]
+    x = inputs(4)
+    idx, sc = _run_indexer(x["q_I"], x["w"], x["keys"], x["n_comp"], wl.top_k, q_pos=x["q_pos"])
+    sample = np.array([0, 1, 2, 3, 4, 777, 1024, 2045, 2046, 2047])
+    ref_s, nv = oracle.index_scores(x["q_I"][:, sample], x["w"][:, sample], x["keys"], x["n_comp"],
+                                    wl.ratio, q_pos=x["q_pos"][:, sample])
+    ref_i = oracle.topk(ref_s, nv, wl.top_k)
+    for j, t in enumerate(sample):
+        assert nv[0, j] == 16384 + (t + 1) // 4
+        _check_scores(sc[0, t], ref_s[0, j], nv[0, j])
+        check_topk_row(idx[0, t], ref_i[0, j], ref_s[0, j], nv[0, j], wl.top_k, f"q{t}")
+    for t in range(0, 2048, 97):
+        n = 16384 + (t + 1) // 4
+        topk_valid_for_scores(idx[0, t], sc[0, t], n, wl.top_k, f"q{t}")
+
+
+def test_indexer_small_heads_ragged():
+    """8 heads (N = 16 UMMA with zero-padded queries), ragged n_comp, fewer keys than top_k."""
+    rng = np.random.default_rng(5)
+    B, H, N, k = 4, 8, 700, 96
+    q = synth.f32_to_bf16_bits(rng.standard_normal((B, 1, H, 128)).astype(np.float32))
+    keys = synth.f32_to_bf16_bits(rng.standard_normal((B, N, 128)).astype(np.float32))
+    w = rng.standard_normal((B, 1, H)).astype(np.float32)
+    n_comp = np.array([700, 0, 50, 129], np.int32)
+    idx, sc = _run_indexer(q, w, keys, n_comp, k)
+    ref_s, nv = oracle.index_scores(q, w, keys, n_comp, 4)
+    ref_i = oracle.topk(ref_s, nv, k)
+    for b in range(B):
+        if nv[b, 0]:
+            _check_scores(sc[b, 0], ref_s[b, 0], nv[b, 0])
+        check_topk_row(idx[b, 0], ref_i[b, 0], ref_s[b, 0], nv[b, 0], k, f"b{b}")
+
+
+# ------------------------------------------------------------------ stage 3 alone: exact top-k
+def _run_topk(scores, n_vis, k):
+    m = csa()
+    sd, nd = dev(scores.astype(np.float32)), dev(n_vis.astype(np.int32))
+    idx = torch.empty(scores.shape[0], k, dtype=torch.int32, device="cuda")
+    ws = ws_tensor(m.dsv4_topk_workspace_size(sd, nd, idx))
+    m.dsv4_topk(sd, nd, idx, ws)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy()
+
+
+@pytest.mark.parametrize("max_comp,k", [(3000, 64), (40000, 2048), (262144, 2048)])
+def test_topk_exact_with_planted_ties(max_comp, k):
+    rows = 6
+    s = synth.normal_f32(11, 18, (rows, max_comp), 0.0, 8.0)
+    s[0] = np.round(s[0] * 4) / 4                    # heavy ties everywhere
+    s[1, ::3] = 0.0
+    s[1, 1::3] = -0.0                                 # +0 and -0 must tie
+    s[2] = 1.5                                        # every score equal
+    s[3, : max_comp // 2] = s[3, max_comp // 2:][: max_comp // 2]   # duplicated halves
+    n_vis = np.array([max_comp, max_comp - 1, max_comp, max_comp // 3 + 1, k, 5], np.int32)
+    got = _run_topk(s, n_vis, k)
+    want = oracle.topk(s, n_vis, k)
+    for r in range(rows):
+        assert np.array_equal(got[r], want[r]), f"row {r}: first diff at {np.argmax(got[r] != want[r])}"
+
+
+# ------------------------------------------------------------------ stage 4: gather + attention
+def _run_attn(x, wl, idx, want_gather=True, top_k=None):
+    m = csa()
+    q, sink = dev_bf16(x["q"]), dev(x["sink"])
+    kv = dev_bf16(x["comp_kv_dev"])
+    n_comp, win, win_len = dev(x["n_comp"]), dev_bf16(x["win"]), dev(x["win_len"])
+    B, n_q, H, D = x["q"].shape
+    top_k = top_k or (idx.shape[-1] if idx is not None else kv.shape[1])
+    out = torch.empty(B, n_q, H, D, dtype=torch.bfloat16, device="cuda")
+    gather = torch.full((B, n_q, top_k + wl.window, D), 7.0, dtype=torch.bfloat16, device="cuda") if want_gather else None
+    kw = dict(idx=None if idx is None else dev(idx), top_k=top_k, window=wl.window, ratio=wl.ratio,
+              q_pos=None if x.get("q_pos") is None else dev(x["q_pos"]), gather=gather)
+    ws = ws_tensor(m.dsv4_sparse_attn_workspace_size(q, sink, kv, n_comp, win, win_len, out, **kw))
+    m.dsv4_sparse_attn_decode(q, sink, kv, n_comp, win, win_len, out, ws, **kw)
+    torch.cuda.synchronize()
+    st, ew = m.dsv4_read_error_word(ws)
+    return host_bf16(out), (host_bf16(gather) if gather is not None else None), ew
+
+
+def _attn_case(cfg):
+    wl = WORKLOADS[cfg]
+    x = dict(inputs(cfg))
+    if wl.pregen_cache:
+        x["comp_kv_dev"] = x["comp_kv"]
+    else:
+        x["comp_kv_dev"] = _oracle_kv(x, wl)[0]
+    return wl, x
+
+
+@pytest.mark.parametrize("cfg", [0, 1, 3])
+def test_sparse_attention_decode(cfg):
+    wl, x = _attn_case(cfg)
+    B = wl.batch
+    idx = synth.uniform_index_sets(wl.seed, 17, B, x["n_comp"], wl.top_k).reshape(B, 1, wl.top_k)
+    got, gat, ew = _run_attn(x, wl, idx)
+    assert ew == 0
+    seqs = list(range(B)) if B <= 4 else [0, 5, 15]
+    ref_bits, ref, ref_g = oracle.sparse_attn(x["q"][seqs], x["sink"], x["comp_kv_dev"][seqs],
+                                              x["n_comp"][seqs], idx[seqs], x["win"][seqs],
+                                              x["win_len"][seqs], wl.top_k, wl.window, wl.ratio,
+                                              want_gather=True)
+    assert_bf16_close(got[seqs], ref, f"cfg{cfg} attention")
+    assert np.array_equal(gat[seqs], ref_g), "gather buffer differs"
+
+
+def test_hca_dense_attention():
+    wl, x = _attn_case(2)
+    got, gat, ew = _run_attn(x, wl, None)
+    assert ew == 0
+    seqs = [0, 17, 63]
+    _, ref, ref_g = oracle.sparse_attn(x["q"][seqs], x["sink"], x["comp_kv_dev"][seqs],
+                                       x["n_comp"][seqs], None, x["win"][seqs], x["win_len"][seqs],
+                                       wl.max_comp, wl.window, wl.ratio, want_gather=True)
+    assert_bf16_close(got[seqs], ref, "HCA attention")
+    assert np.array_equal(gat[seqs], ref_g)
+
+
+def test_prefill_attention_sampled_queries():
+    wl, x = _attn_case(4)
+    nvis = np.array([16384 + (t + 1) // 4 for t in range(2048)], np.int32)
+    idx = synth.uniform_index_sets(4, 17, 2048, nvis, wl.top_k).reshape(1, 2048, wl.top_k)
+    got, gat, ew = _run_attn(x, wl, idx, want_gather=False)
+    assert ew == 0
+    sample = np.array([0, 1, 126, 127, 128, 1000, 2047], np.int32)
+    _, ref, _ = oracle.sparse_attn(x["q"][:, sample], x["sink"], x["comp_kv_dev"], x["n_comp"],
+                                   idx[:, sample], x["win"], x["win_len"], wl.top_k, wl.window,
+                                   wl.ratio, q_pos=x["q_pos"][:, sample], q_abs=sample,
+                                   n_q_total=2048)
+    assert_bf16_close(got[:, sample], ref, "prefill attention")
+
+
+def test_attention_edge_cases_and_bad_index():
+    """Ragged n_comp (including 0), short and empty windows, -1 padding, and an index past the
+    visible range (masked, reported as DSV4_EWORD_BAD_INDEX)."""
+    rng = np.random.default_rng(8)
+    B, H, D, N, k, W = 4, 64, 512, 300, 64, 128
+    x = {"q": synth.f32_to_bf16_bits(rng.standard_normal((B, 1, H, D)).astype(np.float32)),
+         "sink": rng.standard_normal(H).astype(np.float32),
+         "comp_kv_dev": synth.f32_to_bf16_bits(rng.standard_normal((B, N, D)).astype(np.float32)),
+         "n_comp": np.array([300, 0, 37, 129], np.int32),
+         "win": synth.f32_to_bf16_bits(rng.standard_normal((B, W, D)).astype(np.float32)),
+         "win_len": np.array([128, 0, 5, 128], np.int32)}
+
+    class WL:
+        window, ratio = W, 4
+
+    idx = synth.uniform_index_sets(3, 17, B, x["n_comp"], k).reshape(B, 1, k)
+    got, gat, ew = _run_attn(x, WL, idx)
+    assert ew == 0
+    _, ref, ref_g = oracle.sparse_attn(x["q"], x["sink"], x["comp_kv_dev"], x["n_comp"], idx,
+                                       x["win"], x["win_len"], k, W, 4, want_gather=True)
+    assert_bf16_close(got, ref, "edge cases")
+    assert np.array_equal(gat, ref_g)
+    bad = idx.copy()
+    bad[2, 0, 3] = 200                      # sequence 2 has only 37 visible entries
+    got2, _, ew2 = _run_attn(x, WL, bad)
+    assert ew2 & csa().DSV4_EWORD_BAD_INDEX
+    masked = bad.copy()
+    masked[2, 0, 3] = -1
+    _, ref2, _ = oracle.sparse_attn(x["q"], x["sink"], x["comp_kv_dev"], x["n_comp"], masked,
+                                    x["win"], x["win_len"], k, W, 4)
+    assert_bf16_close(got2, ref2, "masked bad index")
+
+
+# ------------------------------------------------------------------ the fused decode step
+def _fused_step(x, wl, graph=False):
+    """Compress (whole context) + indexer top-k + gather/attention in one dsv4_csa_decode."""
+    m = csa()
+    from compressed_sparse_attention_08_gb300 import _abi
+    B, T, D = x["C"].shape
+    Di = x["C_I"].shape[2]
+    t = {}
+    t["C"], t["Z"] = dev_bf16(x["C"]), dev_bf16(x["Z"])
+    t["CI"], t["ZI"] = dev_bf16(x["C_I"]), dev_bf16(x["Z_I"])
+    t["bias"], t["gamma"] = dev(x["bias"]), dev(x["gamma"])
+    t["biasI"], t["gammaI"] = dev(x["bias_I"]), dev(x["gamma_I"])
+    t["pos0"] = dev(x["pos0"])
+    t["kv"] = torch.zeros(B, wl.max_comp, D, dtype=torch.bfloat16, device="cuda")
+    t["keys"] = torch.zeros(B, wl.max_comp, Di, dtype=torch.bfloat16, device="cuda")
+    t["q_I"], t["w"] = dev_bf16(x["q_I"]), dev(x["w"])
+    t["n_comp"] = dev(x["n_comp"])
+    t["idx"] = torch.empty(B, 1, wl.top_k, dtype=torch.int32, device="cuda")
+    t["q"], t["sink"] = dev_bf16(x["q"]), dev(x["sink"])
+    t["win"], t["win_len"] = dev_bf16(x["win"]), dev(x["win_len"])
+    t["out"] = torch.empty(B, 1, wl.heads, D, dtype=torch.bfloat16, device="cuda")
+    t["gather"] = torch.empty(B, 1, wl.top_k + wl.window, D, dtype=torch.bfloat16, device="cuda")
+    ck = _abi.compress_args(t["C"], t["Z"], t["bias"], t["gamma"], t["pos0"], t["kv"], ratio=wl.ratio)
+    cq = _abi.compress_args(t["CI"], t["ZI"], t["biasI"], t["gammaI"], t["pos0"], t["keys"], ratio=wl.ratio)
+    ia = _abi.index_args(t["q_I"], t["w"], t["keys"], t["n_comp"], t["idx"], ratio=wl.ratio)
+    aa = _abi.attn_args(t["q"], t["sink"], t["kv"], t["n_comp"], t["win"], t["win_len"], t["out"],
+                        idx=t["idx"], window=wl.window, ratio=wl.ratio, gather=t["gather"])
+    ws = ws_tensor(m.dsv4_csa_decode_workspace_size(attn=aa, index=ia, compress_kv=ck, compress_keys=cq))
+    m.dsv4_csa_decode(ws, attn=aa, index=ia, compress_kv=ck, compress_keys=cq)
+    torch.cuda.synchronize()
+    launches = m.dsv4_last_launch_count()
+    return t, (ck, cq, ia, aa, ws), launches
+
+
+@pytest.mark.parametrize("cfg", [0, 1])
+def test_fused_decode_step(cfg):
+    wl = WORKLOADS[cfg]
+    x = inputs(cfg)
+    t, _, launches = _fused_step(x, wl)
+    assert launches >= 5
+    kv_bits = host_bf16(t["kv"])
+    keys_bits = host_bf16(t["keys"])
+    ref_kv_bits, ref_kv = _oracle_kv(x, wl)
+    ref_keys_bits, ref_keys = oracle.compress(x["C_I"], x["Z_I"], x["bias_I"], x["gamma_I"],
+                                              x["pos0"], wl.ratio, wl.rope_dim)
+    assert_bf16_close(kv_bits, ref_kv, "fused: compressed KV")
+    assert_bf16_close(keys_bits, ref_keys, "fused: indexer keys")
+    ref_s, nv = oracle.index_scores(x["q_I"], x["w"], ref_keys_bits, x["n_comp"], wl.ratio)
+    ref_i = oracle.topk(ref_s, nv, wl.top_k)
+    idx = t["idx"].cpu().numpy()
+    # the GPU scores its own bf16 keys, which may differ from the oracle's by one bf16 step per
+    # element; the resulting score shift is bounded per key by sum_h |w_h| sum_d |q_hd| ulp(k_d)
+    ulp = np.abs(bf16_to_f64(ref_keys_bits)) * 2.0 ** -7 + 1e-38
+    qa = np.abs(bf16_to_f64(x["q_I"]))                      # [B,1,H,Di]
+    wa = np.abs(x["w"].astype(np.float64))                  # [B,1,H]
+    band = np.einsum("bd,bsd->bs", np.einsum("bh,bhd->bd", wa[:, 0], qa[:, 0]), ulp)
+    same = True
+    for b in range(wl.batch):
+        if np.array_equal(idx[b, 0], ref_i[b, 0]):
+            continue
+        same = False
+        s = ref_s[b, 0, : nv[b, 0]]
+        kth = np.sort(s)[::-1][wl.top_k - 1]
+        diff = np.setxor1d(idx[b, 0][idx[b, 0] >= 0], ref_i[b, 0][ref_i[b, 0] >= 0])
+        assert np.all(np.abs(s[diff] - kth) <= 2 * band[b, diff].max() + 1e-5 * abs(kth)), f"b{b}"
+    if same:
+        _, ref_o, ref_g = oracle.sparse_attn(x["q"], x["sink"], ref_kv_bits, x["n_comp"], ref_i,
+                                             x["win"], x["win_len"], wl.top_k, wl.window, wl.ratio,
+                                             want_gather=True)
+        assert_bf16_close(host_bf16(t["out"]), ref_o, "fused: attention output")
+
+
+def test_fused_decode_graph_replay_matches_eager():
+    """The whole step captured in a CUDA graph replays to the eager result, bit for bit,
+    after the inputs are changed in place."""
+    wl = WORKLOADS[0]
+    x = inputs(0)
+    m = csa()
+    t, (ck, cq, ia, aa, ws), _ = _fused_step(x, wl)
+    eager = {k: t[k].clone() for k in ("out", "idx", "gather", "kv", "keys")}
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            m.dsv4_csa_decode(ws, attn=aa, index=ia, compress_kv=ck, compress_keys=cq, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    for k in ("out", "idx", "gather"):
+        t[k].zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    for k, v in eager.items():
+        assert torch.equal(t[k].view(torch.int16) if t[k].dtype == torch.bfloat16 else t[k],
+                           v.view(torch.int16) if v.dtype == torch.bfloat16 else v), k
+    # new query, same graph
+    q2 = synth.normal_bf16(99, 12, x["q"].shape)
+    t["q"].copy_(dev_bf16(q2))
+    g.replay()
+    torch.cuda.synchronize()
+    out_graph = t["out"].clone()
+    m.dsv4_csa_decode(ws, attn=aa, index=ia, compress_kv=ck, compress_keys=cq)
+    torch.cuda.synchronize()
+    assert torch.equal(out_graph.view(torch.int16), t["out"].view(torch.int16))
+
+
+def test_invalid_arguments_rejected_before_launch():
+    m = csa()
+    q = torch.zeros(1, 1, 64, 128, dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros(1, 1, 64, dtype=torch.float32, device="cuda")
+    keys = torch.zeros(1, 100, 128, dtype=torch.bfloat16, device="cuda")
+    n = torch.zeros(1, dtype=torch.int32, device="cuda")
+    idx = torch.empty(1, 1, 200, dtype=torch.int32, device="cuda")   # top_k > max_comp
+    ws = ws_tensor(1 << 20)
+    with pytest.raises(m.Dsv4Error) as e:
+        m.dsv4_indexer_topk(q, w, keys, n, idx, ws, ratio=4)
+    assert e.value.status == m.DSV4_ERR_INVALID_ARG

@@ -1,0 +1,132 @@
+"""CPU-only checks of the C ABI library: it builds for sm_103a, loads without a GPU, exports
+every function that include/dsv4.h declares, rejects bad arguments on the host before any
+CUDA call, and sizes workspaces sensibly. No compute calls are made here."""
+from __future__ import annotations
+
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from compressed_sparse_attention_08_gb300 import _build, _abi
+    _build.build()
+    return _abi.library()
+
+
+def header_functions():
+    with open(os.path.join(ROOT, "include", "dsv4.h")) as fh:
+        text = fh.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsv4_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_function(lib):
+    names = header_functions()
+    assert len(names) >= 13
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/dsv4.h but not exported"
+    from compressed_sparse_attention_08_gb300 import EXPORTED_SYMBOLS
+    assert sorted(EXPORTED_SYMBOLS) == names
+
+
+def test_status_strings_and_sizing(lib):
+    from compressed_sparse_attention_08_gb300 import _abi
+    for s in range(6):
+        assert _abi.dsv4_status_string(s)
+    with open(os.path.join(ROOT, "tests", "golden", "page_sizes.json")) as fh:
+        g = json.load(fh)
+    for case in g["max_comp"]:
+        assert _abi.dsv4_max_comp(case["context"], case["ratio"]) == case["entries"]
+    assert _abi.dsv4_max_comp(10, 4) == 3 and _abi.dsv4_max_comp(8, 0) == -1
+
+
+FAKE = 0x7F0000000000   # aligned fake device addresses: never dereferenced on the host path
+
+
+def _p(i):
+    return ctypes.c_void_p(FAKE + 4096 * i)
+
+
+def _index_args(**over):
+    from compressed_sparse_attention_08_gb300._abi import IndexArgs
+    a = dict(q=_p(1), w=_p(2), keys=_p(3), n_comp=_p(4), q_pos=None, idx_out=_p(5), scores_out=None,
+             batch=4, n_q=1, heads=64, dim=128, max_comp=262144, top_k=2048, ratio=4)
+    a.update(over)
+    return IndexArgs(**a)
+
+
+def _attn_args(**over):
+    from compressed_sparse_attention_08_gb300._abi import AttnArgs
+    a = dict(q=_p(1), sink=_p(2), comp_kv=_p(3), n_comp=_p(4), idx=_p(5), q_pos=None, win=_p(6),
+             win_len=_p(7), gather=None, out=_p(8), batch=4, n_q=1, heads=64, dim=512,
+             max_comp=262144, top_k=2048, window=128, win_rows=128, ratio=4, scale=0.0442)
+    a.update(over)
+    return AttnArgs(**a)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(top_k=300000), dict(top_k=0), dict(dim=64), dict(heads=12), dict(heads=72),
+    dict(q=None), dict(q=ctypes.c_void_p(FAKE + 8)), dict(n_q=0), dict(ratio=0), dict(max_comp=0),
+])
+def test_indexer_rejects_on_host(lib, bad):
+    a = _index_args(**bad)
+    ws_bytes = lib.dsv4_indexer_topk_workspace_size(ctypes.byref(a))
+    rc = lib.dsv4_indexer_topk(ctypes.byref(a), _p(9), ws_bytes, None)
+    assert rc == 1
+
+
+def test_indexer_rejects_small_workspace(lib):
+    a = _index_args()
+    need = lib.dsv4_indexer_topk_workspace_size(ctypes.byref(a))
+    # scores (4 MiB) + top-k survivors (8 MiB) + histograms
+    assert need >= 4 * 262144 * 4 + 4 * 262144 * 8
+    assert lib.dsv4_indexer_topk(ctypes.byref(a), _p(9), need - 1, None) == 1
+
+
+@pytest.mark.parametrize("bad", [
+    dict(dim=100), dict(heads=0), dict(heads=65), dict(idx=None),   # dense needs top_k == max_comp
+    dict(top_k=262145), dict(win_rows=0), dict(scale=float("inf")), dict(out=None),
+    dict(gather=ctypes.c_void_p(FAKE + 4)),
+])
+def test_attention_rejects_on_host(lib, bad):
+    a = _attn_args(**bad)
+    rc = lib.dsv4_sparse_attn_decode(ctypes.byref(a), _p(9), 1 << 40, None)
+    assert rc == 1
+
+
+def test_compress_rejects_on_host(lib):
+    from compressed_sparse_attention_08_gb300._abi import CompressArgs
+    base = dict(C=_p(1), Z=_p(2), bias=_p(3), gamma=_p(4), pos0=_p(5), out=_p(6), out_row0=None,
+                batch=4, tokens=16, dim=512, ratio=4, rope_dim=64, out_rows=4, eps=1e-6,
+                rope_theta=10000.0)
+    for bad in (dict(tokens=15), dict(rope_dim=63), dict(rope_dim=1024), dict(dim=2048),
+                dict(out_rows=3), dict(eps=-1.0), dict(C=None), dict(ratio=0)):
+        a = CompressArgs(**{**base, **bad})
+        assert lib.dsv4_compress(ctypes.byref(a), None) == 1, bad
+
+
+def test_fused_requires_consistent_stages(lib):
+    from compressed_sparse_attention_08_gb300._abi import CsaArgs, IndexArgs, AttnArgs
+    ia = _index_args()
+    aa = _attn_args(idx=ia.idx_out)
+    c = CsaArgs(None, None, ctypes.pointer(ia), ctypes.pointer(aa))
+    need = lib.dsv4_csa_decode_workspace_size(ctypes.byref(c))
+    assert need >= lib.dsv4_indexer_topk_workspace_size(ctypes.byref(ia))
+    aa2 = _attn_args(idx=_p(42))          # attention must read the indexer's output
+    c2 = CsaArgs(None, None, ctypes.pointer(ia), ctypes.pointer(aa2))
+    assert lib.dsv4_csa_decode(ctypes.byref(c2), _p(9), need, None) == 1
+
+
+def test_binding_refuses_without_library(tmp_path, monkeypatch):
+    from compressed_sparse_attention_08_gb300 import _abi
+    monkeypatch.setattr(_abi, "_lib", None)
+    monkeypatch.setattr(_abi, "library_path", lambda: str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        _abi.library()
