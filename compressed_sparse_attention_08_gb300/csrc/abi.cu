@@ -38,7 +38,7 @@ bool compress_ok(const dsv4_compress_args* a) {
         return false;
     if (a->batch < 0 || a->tokens < 0 || a->ratio < 1 || a->dim < 2 || a->dim > 1024) return false;
     if (a->tokens % a->ratio != 0) return false;
-    if (a->rope_dim < 0 || a->rope_dim > a->dim || (a->rope_dim & 1)) return false;
+    if (a->rope_dim < 0 || a->rope_dim > a->dim || a->rope_dim > 128 || (a->rope_dim & 1)) return false;
     if (a->out_rows < 1) return false;
     if (!a->out_row0 && a->out_rows < a->tokens / a->ratio) return false;
     if (!(a->eps >= 0.f) || !std::isfinite(a->eps) || !std::isfinite(a->rope_theta) || a->rope_theta <= 0.0)
@@ -148,7 +148,7 @@ int dsv4_indexer_topk(const dsv4_index_args* a, void* ws, size_t ws_bytes, dsv4_
         return DSV4_ERR_INVALID_ARG;
     if (int rc = device_check()) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), st) != cudaSuccess) return DSV4_ERR_LAUNCH;
+    if (cudaMemsetAsync(ws, 0, kWsHeader + index_zero_bytes(*a), st) != cudaSuccess) return DSV4_ERR_LAUNCH;
     return launch_indexer(*a, body_of(ws), eword_of(ws), st);
 }
 
@@ -190,6 +190,9 @@ int dsv4_topk(const dsv4_topk_args* a, void* ws, size_t ws_bytes, dsv4_stream_t 
     t.rows = a->rows;
     t.max_comp = a->max_comp;
     t.top_k = a->top_k;
+    t.hist_zeroed = false;
+    t.hist_built = false;
+    t.pdl = true;
     return launch_topk(t, body_of(ws), eword_of(ws), st);
 }
 
@@ -241,11 +244,12 @@ int dsv4_csa_decode(const dsv4_csa_args* a, void* ws, size_t ws_bytes, dsv4_stre
         return DSV4_ERR_INVALID_ARG;
     if (int rc = device_check()) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), st) != cudaSuccess) return DSV4_ERR_LAUNCH;
+    const size_t zero = kWsHeader + (a->index ? index_zero_bytes(*a->index) : 0);
+    if (cudaMemsetAsync(ws, 0, zero, st) != cudaSuccess) return DSV4_ERR_LAUNCH;
     int rc = DSV4_OK;
-    if (a->compress_kv && (rc = launch_compress(*a->compress_kv, st))) return rc;
-    if (a->compress_keys && (rc = launch_compress(*a->compress_keys, st))) return rc;
-    if (a->index && (rc = launch_indexer(*a->index, body_of(ws), eword_of(ws), st))) return rc;
+    if ((rc = launch_compress2(a->compress_kv, a->compress_keys, st))) return rc;
+    if (a->index && (rc = launch_indexer(*a->index, body_of(ws), eword_of(ws), st, a->compress_keys)))
+        return rc;
     return launch_attn(*a->attn, body_of(ws), eword_of(ws), st);
 }
 

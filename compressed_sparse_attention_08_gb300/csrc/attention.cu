@@ -135,8 +135,9 @@ attn_kernel(AttnParams p) {
     const int c0 = split * p.chunks_per_split;
     const int c1 = c0 + p.chunks_per_split < p.n_chunks ? c0 + p.chunks_per_split : p.n_chunks;
 
+    pdl_trigger();
     if (tid < HP) { m_run[tid] = -INFINITY; l_run[tid] = 0.f; }
-    // Q (rows >= H are zero)
+    // Q (rows >= H are zero); the queries are inputs, so they load before the wait below
     for (int i = tid; i < HP * CPR; i += kNT) {
         const int h = i / CPR, c = i - h * CPR;
         uint8_t* dst = sQ + swz<ROWB>(h, c);
@@ -183,6 +184,7 @@ attn_kernel(AttnParams p) {
 #pragma unroll
     for (int i = 0; i < C::DW / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
+    pdl_wait();             // the index list (and the workspace) belong to the kernels before
     if (c0 < c1) {
         resolve(c0, 0);
         __syncthreads();
@@ -360,30 +362,47 @@ template <int D, int HP>
 __global__ void __launch_bounds__(128)
 attn_combine_kernel(AttnParams p) {
     __shared__ float wgt[256];
-    __shared__ float den_s;
-    const int row = blockIdx.x, h = blockIdx.y;
+    __shared__ float red[4];
+    __shared__ float bcast[2];
+    const int row = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
     const int ns = p.n_splits;
+    pdl_wait();
     const float* ml = p.part_ml + static_cast<size_t>(row) * ns * HP * 2;
-    if (threadIdx.x == 0) {
-        const float snk = p.sink[h];
-        float M = snk;
-        for (int s = 0; s < ns; ++s) M = fmaxf(M, ml[(s * HP + h) * 2]);
-        float den = expf(snk - M);
-        for (int s = 0; s < ns; ++s) {
-            const float m = ml[(s * HP + h) * 2], l = ml[(s * HP + h) * 2 + 1];
-            const float e = m == -INFINITY ? 0.f : expf(m - M);
-            wgt[s] = e;
-            den += l * e;
-        }
-        den_s = den;
-    }
+    const float snk = p.sink[h];
+    // the splits' maxima and sums, in parallel (ns <= 256: two per thread)
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    if (tid < ns) { m0 = ml[(tid * HP + h) * 2]; l0 = ml[(tid * HP + h) * 2 + 1]; }
+    if (tid + 128 < ns) { m1 = ml[((tid + 128) * HP + h) * 2]; l1 = ml[((tid + 128) * HP + h) * 2 + 1]; }
+    float M = fmaxf(m0, m1);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    if ((tid & 31) == 0) red[tid >> 5] = M;
     __syncthreads();
-    const float inv = 1.0f / den_s;
-    const float* po = p.part_o + static_cast<size_t>(row) * ns * HP * D;
-    for (int d = threadIdx.x; d < D; d += 128) {
-        float acc = 0.f;
-        for (int s = 0; s < ns; ++s) acc = fmaf(po[(static_cast<size_t>(s) * HP + h) * D + d], wgt[s], acc);
-        p.out[(static_cast<size_t>(row) * p.H + h) * D + d] = __float2bfloat16_rn(acc * inv);
+    M = fmaxf(fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3])), snk);
+    const float e0 = m0 == -INFINITY ? 0.f : expf(m0 - M);
+    const float e1 = m1 == -INFINITY ? 0.f : expf(m1 - M);
+    if (tid < ns) wgt[tid] = e0;
+    if (tid + 128 < ns) wgt[tid + 128] = e1;
+    float den = l0 * e0 + l1 * e1;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    __syncthreads();
+    if ((tid & 31) == 0) red[tid >> 5] = den;
+    __syncthreads();
+    if (tid == 0) bcast[0] = 1.0f / (red[0] + red[1] + red[2] + red[3] + expf(snk - M));
+    __syncthreads();
+    const float inv = bcast[0];
+    const float* po = p.part_o + static_cast<size_t>(row) * ns * HP * D + static_cast<size_t>(h) * D;
+    for (int d = tid * 2; d < D; d += 256) {
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll 8
+        for (int s = 0; s < ns; ++s) {
+            const float2 v = *reinterpret_cast<const float2*>(po + static_cast<size_t>(s) * HP * D + d);
+            a0 = fmaf(v.x, wgt[s], a0);
+            a1 = fmaf(v.y, wgt[s], a1);
+        }
+        *reinterpret_cast<uint32_t*>(p.out + (static_cast<size_t>(row) * p.H + h) * D + d) =
+            pack_bf16(a0 * inv, a1 * inv);
     }
 }
 
@@ -443,14 +462,14 @@ int run(const dsv4_attn_args& a, const Plan& pl, uint8_t* ws, uint32_t* eword, c
         attr_set = true;
     }
     dim3 grid(pl.n_splits, p.rows);
-    attn_kernel<D, HP><<<grid, kNT, C::SMEM, st>>>(p);
     count_launch();
-    if (cudaGetLastError() != cudaSuccess) return DSV4_ERR_LAUNCH;
+    if (launch_k(attn_kernel<D, HP>, grid, dim3(kNT), C::SMEM, st, true, p) != cudaSuccess)
+        return DSV4_ERR_LAUNCH;
     if (pl.n_splits > 1) {
         dim3 g2(p.rows, a.heads);
-        attn_combine_kernel<D, HP><<<g2, 128, 0, st>>>(p);
         count_launch();
-        if (cudaGetLastError() != cudaSuccess) return DSV4_ERR_LAUNCH;
+        if (launch_k(attn_combine_kernel<D, HP>, g2, dim3(128), 0, st, true, p) != cudaSuccess)
+            return DSV4_ERR_LAUNCH;
     }
     return DSV4_OK;
 }

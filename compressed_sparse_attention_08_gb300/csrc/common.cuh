@@ -218,3 +218,29 @@ __device__ __forceinline__ int row_visible(const int32_t* n_vis, const int32_t* 
     return static_cast<int>(v);
 }
 }  // namespace dsv4
+
+namespace dsv4 {
+// Programmatic dependent launch. A kernel launched with launch_k(..., pdl = true) may start
+// while the previous kernel on the stream is still running; it must call pdl_wait() before it
+// reads anything that kernel writes and before its own global writes that kernel could see.
+// pdl_trigger() lets the next kernel launch early. Both are no-ops for kernels launched
+// without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t stream, bool pdl, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = pdl ? attr : nullptr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+}  // namespace dsv4

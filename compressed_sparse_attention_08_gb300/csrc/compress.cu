@@ -7,12 +7,21 @@
 // (interleaved-pair RoPE of the last rope_dim channels).
 //
 // Design: the reduce is tiny (ratio x dim values per entry) and latency-bound, so the
-// three steps are fused in one kernel: each thread owns channels c = tid + 128 i, runs the
-// max pass and the exp/sum pass over the block's tokens in fp32 (reads hit L1), the CTA
-// reduces sum(x^2) with warp shuffles, and the rope pairs are rotated from shared memory
-// with angles formed in fp64 (positions reach 2^20, where an fp32 angle would be off by
-// hundredths of a radian). One bf16 rounding at the output, written straight into the
-// caller's cache rows.
+// three steps are fused in one kernel, and one launch serves up to two compressions (the
+// main KV and the indexer keys of a decode step). Each thread owns channels
+// c = tid + 128 i and runs an online softmax (running max, rescaled sums) over the block's
+// tokens in fp32, 8 tokens at a time with all loads of a chunk issued before any is used;
+// the CTA reduces sum(x^2) with warp shuffles, and the rope pairs are rotated from shared
+// memory.
+// RoPE angles: positions reach 2^20, where an fp32 angle pos * f would be off by hundredths
+// of a radian, so the angle is formed in fp64 from a host-computed table of the
+// frequencies f_j = theta^(-2j/rope_dim), reduced to [-pi, pi] with a two-constant
+// Cody-Waite reduction using fused multiply-adds (W. J. Cody and W. Waite, "Software Manual
+// for the Elementary Functions", 1980; the FMA form as in J.-M. Muller, "Elementary
+// Functions", ch. 11), and only then passed to the fp32 sincos. One bf16 rounding at the
+// output, written straight into the caller's cache rows.
+#include <cmath>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -21,23 +30,36 @@ namespace {
 
 constexpr int kThreads = 128;
 constexpr int kMaxChan = 8;          // dim <= 1024
+constexpr int kMaxPairs = 64;        // rope_dim <= 128
+
+struct CompressJob {
+    const __nv_bfloat16* C;
+    const __nv_bfloat16* Z;
+    const float* bias;
+    const float* gamma;
+    const int64_t* pos0;
+    __nv_bfloat16* out;
+    const int32_t* out_row0;
+    int batch, tokens, dim, ratio, rope_dim, out_rows, n_blocks;
+    float eps;
+    double two_pi_hi, two_pi_lo, inv_two_pi;
+    double freq[kMaxPairs];
+};
 
 __global__ void __launch_bounds__(kThreads)
-compress_kernel(const __nv_bfloat16* __restrict__ C, const __nv_bfloat16* __restrict__ Z,
-                const float* __restrict__ bias, const float* __restrict__ gamma,
-                const int64_t* __restrict__ pos0, __nv_bfloat16* __restrict__ out,
-                const int32_t* __restrict__ out_row0, int tokens, int dim, int ratio,
-                int rope_dim, int out_rows, float eps, double theta) {
+compress_kernel(const __grid_constant__ CompressJob j0, const __grid_constant__ CompressJob j1) {
+    pdl_trigger();
+    const CompressJob& j = blockIdx.z == 0 ? j0 : j1;
     const int b = blockIdx.x;          // block (entry) within the sequence
     const int s = blockIdx.y;          // sequence
     const int tid = threadIdx.x;
-    const int n_blocks = tokens / ratio;
-    if (b >= n_blocks) return;
+    if (b >= j.n_blocks || s >= j.batch) return;
+    const int dim = j.dim, ratio = j.ratio;
 
     __shared__ float y[1024];
     __shared__ float warp_sum[kThreads / 32];
 
-    const size_t tok0 = static_cast<size_t>(s) * tokens + static_cast<size_t>(b) * ratio;
+    const size_t tok0 = static_cast<size_t>(s) * j.tokens + static_cast<size_t>(b) * ratio;
     float x[kMaxChan];
     float sq = 0.f;
 #pragma unroll
@@ -45,17 +67,34 @@ compress_kernel(const __nv_bfloat16* __restrict__ C, const __nv_bfloat16* __rest
         const int c = tid + i * kThreads;
         x[i] = 0.f;
         if (c >= dim) continue;
-        float m = -INFINITY;
-        for (int t = 0; t < ratio; ++t) {
-            const float a = __bfloat162float(Z[(tok0 + t) * dim + c]) + bias[static_cast<size_t>(t) * dim + c];
-            m = fmaxf(m, a);
-        }
-        float den = 0.f, num = 0.f;
-        for (int t = 0; t < ratio; ++t) {
-            const float a = __bfloat162float(Z[(tok0 + t) * dim + c]) + bias[static_cast<size_t>(t) * dim + c];
-            const float e = expf(a - m);
-            den += e;
-            num = fmaf(e, __bfloat162float(C[(tok0 + t) * dim + c]), num);   // no bias on C
+        float m = -INFINITY, den = 0.f, num = 0.f;
+        for (int t0 = 0; t0 < ratio; t0 += 8) {
+            float a[8], cv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int t = t0 + u;
+                if (t < ratio) {
+                    a[u] = __bfloat162float(j.Z[(tok0 + t) * dim + c]) + j.bias[static_cast<size_t>(t) * dim + c];
+                    cv[u] = __bfloat162float(j.C[(tok0 + t) * dim + c]);
+                } else {
+                    a[u] = -INFINITY;
+                    cv[u] = 0.f;
+                }
+            }
+            float mc = a[0];
+#pragma unroll
+            for (int u = 1; u < 8; ++u) mc = fmaxf(mc, a[u]);
+            const float mn = fmaxf(m, mc);
+            const float sc = m == -INFINITY ? 0.f : expf(m - mn);
+            den *= sc;
+            num *= sc;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const float e = a[u] == -INFINITY ? 0.f : expf(a[u] - mn);
+                den += e;
+                num = fmaf(e, cv[u], num);   // no bias on C
+            }
+            m = mn;
         }
         x[i] = num / den;
         sq = fmaf(x[i], x[i], sq);
@@ -68,44 +107,79 @@ compress_kernel(const __nv_bfloat16* __restrict__ C, const __nv_bfloat16* __rest
     float tot = 0.f;
 #pragma unroll
     for (int w = 0; w < kThreads / 32; ++w) tot += warp_sum[w];
-    const float inv = 1.0f / sqrtf(tot / static_cast<float>(dim) + eps);
+    const float inv = 1.0f / sqrtf(tot / static_cast<float>(dim) + j.eps);
 #pragma unroll
     for (int i = 0; i < kMaxChan; ++i) {
         const int c = tid + i * kThreads;
-        if (c < dim) y[c] = x[i] * inv * gamma[c];
+        if (c < dim) y[c] = x[i] * inv * j.gamma[c];
     }
     __syncthreads();
-    // RoPE: pair j rotates channels (d0, d0 + 1), d0 = dim - rope_dim + 2j
-    const int64_t pos = pos0[s] + static_cast<int64_t>(b) * ratio;
-    for (int j = tid; j < rope_dim / 2; j += kThreads) {
-        const int d0 = dim - rope_dim + 2 * j;
-        const double ang = static_cast<double>(pos) * pow(theta, -2.0 * j / rope_dim);
-        double sd, cd;
-        sincos(ang, &sd, &cd);
-        const float cs = static_cast<float>(cd), sn = static_cast<float>(sd);
+    // RoPE: pair p rotates channels (d0, d0 + 1), d0 = dim - rope_dim + 2p, by pos * f_p
+    const double pos = static_cast<double>(j.pos0[s] + static_cast<int64_t>(b) * ratio);
+    for (int p = tid; p < j.rope_dim / 2; p += kThreads) {
+        const int d0 = dim - j.rope_dim + 2 * p;
+        const double ang = pos * j.freq[p];
+        const double kq = rint(ang * j.inv_two_pi);
+        double r = fma(-kq, j.two_pi_hi, ang);
+        r = fma(-kq, j.two_pi_lo, r);
+        float sn, cs;
+        sincosf(static_cast<float>(r), &sn, &cs);
         const float e = y[d0], o = y[d0 + 1];
         y[d0] = e * cs - o * sn;
         y[d0 + 1] = e * sn + o * cs;
     }
     __syncthreads();
-    const int row = (out_row0 ? out_row0[s] : 0) + b;
-    if (row < 0 || row >= out_rows) return;   // host checks make this unreachable
-    __nv_bfloat16* dst = out + (static_cast<size_t>(s) * out_rows + row) * dim;
+    const int row = (j.out_row0 ? j.out_row0[s] : 0) + b;
+    if (row < 0 || row >= j.out_rows) return;   // rows outside the destination are not written
+    __nv_bfloat16* dst = j.out + (static_cast<size_t>(s) * j.out_rows + row) * dim;
     for (int c = tid; c < dim; c += kThreads) dst[c] = __float2bfloat16_rn(y[c]);
+}
+
+CompressJob make_job(const dsv4_compress_args& a) {
+    CompressJob j;
+    j.C = static_cast<const __nv_bfloat16*>(a.C);
+    j.Z = static_cast<const __nv_bfloat16*>(a.Z);
+    j.bias = a.bias;
+    j.gamma = a.gamma;
+    j.pos0 = a.pos0;
+    j.out = static_cast<__nv_bfloat16*>(a.out);
+    j.out_row0 = a.out_row0;
+    j.batch = a.batch;
+    j.tokens = a.tokens;
+    j.dim = a.dim;
+    j.ratio = a.ratio;
+    j.rope_dim = a.rope_dim;
+    j.out_rows = a.out_rows;
+    j.n_blocks = a.tokens / a.ratio;
+    j.eps = a.eps;
+    // 2*pi as an unevaluated sum hi + lo of two doubles; lo = 2*pi - hi to double precision
+    // (2*pi = 6.28318530717958647692528676655900576839...).
+    j.two_pi_hi = 6.283185307179586;
+    j.two_pi_lo = 2.4492935982947064e-16;
+    j.inv_two_pi = 1.0 / j.two_pi_hi;
+    for (int p = 0; p < kMaxPairs; ++p)
+        j.freq[p] = p < a.rope_dim / 2 ? std::pow(a.rope_theta, -2.0 * p / a.rope_dim) : 0.0;
+    return j;
 }
 
 }  // namespace
 
-int launch_compress(const dsv4_compress_args& a, cudaStream_t stream) {
-    const int n_blocks = a.tokens / a.ratio;
-    if (a.batch == 0 || n_blocks == 0) return DSV4_OK;
-    dim3 grid(n_blocks, a.batch);
-    compress_kernel<<<grid, kThreads, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(a.C), static_cast<const __nv_bfloat16*>(a.Z), a.bias,
-        a.gamma, a.pos0, static_cast<__nv_bfloat16*>(a.out), a.out_row0, a.tokens, a.dim,
-        a.ratio, a.rope_dim, a.out_rows, a.eps, a.rope_theta);
+int launch_compress2(const dsv4_compress_args* a, const dsv4_compress_args* b, cudaStream_t stream) {
+    if (!a && !b) return DSV4_OK;
+    if (!a) { a = b; b = nullptr; }
+    const CompressJob j0 = make_job(*a);
+    const CompressJob j1 = b ? make_job(*b) : j0;
+    const int nb = j0.n_blocks > j1.n_blocks ? j0.n_blocks : j1.n_blocks;
+    const int bs = j0.batch > j1.batch ? j0.batch : j1.batch;
+    if (nb == 0 || bs == 0) return DSV4_OK;
+    dim3 grid(nb, bs, b ? 2 : 1);
+    compress_kernel<<<grid, kThreads, 0, stream>>>(j0, j1);
     count_launch();
     return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_LAUNCH;
+}
+
+int launch_compress(const dsv4_compress_args& a, cudaStream_t stream) {
+    return launch_compress2(&a, nullptr, stream);
 }
 
 }  // namespace dsv4

@@ -21,7 +21,11 @@
 //           of kAccBufs TMEM accumulators; tcgen05.commit frees the smem stage and publishes
 //           the accumulator
 //   warps 2-5  epilogue: tcgen05.ld of the 64-column accumulator (thread = key), weighted
-//           ReLU sum in fp32, coalesced store of the score.
+//           ReLU sum in fp32, coalesced store of the score; optionally a shared-memory
+//           histogram of the scores' top 12 key bits, flushed per row into the top-k
+//           workspace (so the long-row top-k needs no histogram pass of its own).
+// Launched with programmatic dependent launch: the producer waits for the preceding kernel
+// (the compressor) only before a tile that holds key rows that kernel writes.
 // Work: the (row, key tile) pairs, cut into one contiguous range per CTA. Tiles past the
 // row's visible count are skipped by all three roles alike.
 #include "common.cuh"
@@ -43,6 +47,7 @@ constexpr uint32_t kKeyTileBytes = kTileKeys * kDim * 2;   // 32 KiB
 constexpr uint32_t kKeyHalfBytes = kKeyTileBytes / 2;      // 128 keys x 64 dims
 constexpr uint32_t kQBufBytes = kMaxHeads * kDim * 2;      // 16 KiB
 constexpr int kThreads = 192;
+constexpr int kHistBins = 4096;             // top 12 bits of the order-preserving score key
 constexpr size_t kSmemBytes = 1024 + kStages * kKeyTileBytes + 2 * kQBufBytes;
 
 struct ScoreParams {
@@ -50,6 +55,9 @@ struct ScoreParams {
     const int32_t* n_comp;   // [batch]
     const int64_t* q_pos;    // [rows] or null
     float* scores;           // [rows, max_comp]
+    uint32_t* hist;          // [rows, 4096] top-12-bit key histogram (zeroed), or null
+    const int32_t* fresh_row0;  // [batch] first key row the preceding kernel writes, or null
+    int fresh_rows;          // rows it writes per sequence (0: none)
     uint32_t* eword;
     int rows, n_q, heads, n_pad, max_comp, ratio, tiles_per_row;
 };
@@ -70,8 +78,10 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
     __shared__ uint64_t qfull_bar[2], qempty_bar[2], done_bar;
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
+    __shared__ uint32_t s_hist[kHistBins];          // top-12-bit key histogram of the current row
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_trigger();
     // 1024-byte aligned operand buffers (the 128-byte swizzle repeats every 1024 bytes)
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* base = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -91,6 +101,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
     // query rows past `heads` stay zero for the whole kernel (TMA writes only `heads` rows)
     for (uint32_t i = threadIdx.x; i < 2 * kQBufBytes / 16; i += kThreads)
         reinterpret_cast<uint4*>(q_buf)[i] = make_uint4(0, 0, 0, 0);
+    for (int i = threadIdx.x; i < kHistBins; i += kThreads) s_hist[i] = 0;
     if (warp == 1) tmem_alloc(&tmem_slot, kTmemCols);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     tc_fence_before();
@@ -106,6 +117,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
     if (warp == 0) {
         if (lane == 0) {
             int stage = 0, qcount = 0, cur_row = -1, nv = 0;
+            bool waited = false;
             long long issued = 0;
             uint32_t phase = 0;
             for (long long t = wr.begin; t < wr.end; ++t) {
@@ -124,6 +136,16 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                     cur_row = row;
                     ++qcount;
                 }
+                if (!waited && p.fresh_rows > 0) {
+                    // key rows written by the preceding kernel (the newest block's key): wait
+                    // for it before streaming a tile that overlaps them
+                    const int b_ = row / p.n_q;
+                    const int f0 = p.fresh_row0 ? p.fresh_row0[b_] : 0;
+                    if (tile * kTileKeys < f0 + p.fresh_rows && f0 < (tile + 1) * kTileKeys) {
+                        pdl_wait();
+                        waited = true;
+                    }
+                }
                 if (!mbar_wait(&empty_bar[stage], phase ^ 1, &abort_flag)) goto fail0;
                 mbar_arrive_expect_tx(&full_bar[stage], kKeyTileBytes);
                 {
@@ -135,6 +157,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                 }
                 if (++stage == kStages) { stage = 0; phase ^= 1; }
             }
+            if (!waited) pdl_wait();        // this grid never completes before its predecessor
             goto done0;
         fail0:
             flag_error(p.eword, DSV4_EWORD_TIMEOUT);
@@ -144,6 +167,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                 mbar_wait(&full_bar[i % kStages], static_cast<uint32_t>((i / kStages) & 1), nullptr, 100000000ull);
             if (qcount > 0)
                 mbar_wait(&qfull_bar[(qcount - 1) & 1], static_cast<uint32_t>(((qcount - 1) >> 1) & 1), nullptr, 100000000ull);
+            if (!waited) pdl_wait();
         done0:;
         }
     } else if (warp == 1) {
@@ -198,25 +222,42 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
         // epilogue: warps 2..5 -> TMEM lane quarter (warp % 4)
         const int quarter = warp & 3;
         const int lrow = quarter * 32 + lane;
+        const int etid = threadIdx.x - 64;                 // 0..127 within the epilogue
         const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
         int acc = 0, cur_row = -1, nv = 0;
         uint32_t acc_phase = 0;
+        bool dead = false;        // a wait ran out: keep walking the tiles (same barriers), no work
         float wv[kMaxHeads];
+        // The histogram is private to the CTA and flushed to the row's global histogram when
+        // the row changes. Every epilogue thread passes the same flush barriers, dead or not.
+        auto flush = [&](int r) {
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            for (int i = etid; i < kHistBins; i += 128) {
+                const uint32_t v = s_hist[i];
+                if (v) {
+                    atomicAdd(&p.hist[static_cast<size_t>(r) * kHistBins + i], v);
+                    s_hist[i] = 0;
+                }
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+        };
         for (long long t = wr.begin; t < wr.end; ++t) {
             const int row = static_cast<int>(t / p.tiles_per_row);
             const int tile = static_cast<int>(t % p.tiles_per_row);
             if (row != cur_row) {
+                if (p.hist && cur_row >= 0) flush(cur_row);
                 nv = row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, row, nullptr);
                 cur_row = row;
 #pragma unroll
                 for (int h = 0; h < kMaxHeads; ++h)
                     wv[h] = h < p.heads ? __ldg(&p.w[static_cast<size_t>(row) * p.heads + h]) : 0.f;
             }
-            if (tile * kTileKeys >= nv) continue;
+            if (tile * kTileKeys >= nv || dead) continue;
             if (!mbar_wait(&tfull_bar[acc], acc_phase, &abort_flag)) {
                 flag_error(p.eword, DSV4_EWORD_TIMEOUT);
                 abort_flag = 1;
-                break;
+                dead = true;
+                continue;
             }
             tc_fence_after();
             uint32_t r[64];
@@ -228,9 +269,13 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
 #pragma unroll
             for (int h = 0; h < kMaxHeads; ++h) s = fmaf(wv[h], fmaxf(__uint_as_float(r[h]), 0.f), s);
             const int key = tile * kTileKeys + lrow;
-            if (key < nv) p.scores[static_cast<size_t>(row) * p.max_comp + key] = s;
+            if (key < nv) {
+                p.scores[static_cast<size_t>(row) * p.max_comp + key] = s;
+                if (p.hist) atomicAdd(&s_hist[float_to_key(s) >> 20], 1u);
+            }
             if (++acc == kAccBufs) { acc = 0; acc_phase ^= 1; }
         }
+        if (p.hist && cur_row >= 0) flush(cur_row);
     }
     tc_fence_before();
     __syncthreads();
@@ -256,13 +301,19 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 size_t index_ws_bytes(const dsv4_index_args& a) {
     const int rows = a.batch * a.n_q;
     size_t b = 0;
+    b += align_up(topk_ws_bytes(rows, a.max_comp, a.top_k), 256);
     if (!a.scores_out) b += align_up(static_cast<size_t>(rows) * a.max_comp * 4, 256);
-    b += topk_ws_bytes(rows, a.max_comp, a.top_k);
     return b;
 }
 
+size_t index_zero_bytes(const dsv4_index_args& a) {
+    const int rows = a.batch * a.n_q;
+    return topk_uses_hist(a.max_comp) ? topk_hist_bytes(rows) : 0;
+}
+
 namespace {
-int launch_scores(const dsv4_index_args& a, float* scores, uint32_t* eword, cudaStream_t stream) {
+int launch_scores(const dsv4_index_args& a, float* scores, uint32_t* hist, uint32_t* eword,
+                  cudaStream_t stream, const dsv4_compress_args* fresh) {
     const int rows = a.batch * a.n_q;
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return DSV4_ERR_LAUNCH;
@@ -293,6 +344,9 @@ int launch_scores(const dsv4_index_args& a, float* scores, uint32_t* eword, cuda
     p.n_comp = a.n_comp;
     p.q_pos = a.q_pos;
     p.scores = scores;
+    p.hist = hist;
+    p.fresh_row0 = fresh ? fresh->out_row0 : nullptr;
+    p.fresh_rows = fresh ? fresh->tokens / fresh->ratio : 0;
     p.eword = eword;
     p.rows = rows;
     p.n_q = a.n_q;
@@ -311,9 +365,10 @@ int launch_scores(const dsv4_index_args& a, float* scores, uint32_t* eword, cuda
         }
         long long grid = sm_count();
         if (grid > total) grid = total;
-        index_score_kernel<<<static_cast<int>(grid), kThreads, kSmemBytes, stream>>>(kmap, qmap, p);
         count_launch();
-        if (cudaGetLastError() != cudaSuccess) return DSV4_ERR_LAUNCH;
+        if (launch_k(index_score_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes,
+                     stream, true, kmap, qmap, p) != cudaSuccess)
+            return DSV4_ERR_LAUNCH;
     }
     return DSV4_OK;
 }
@@ -321,19 +376,21 @@ int launch_scores(const dsv4_index_args& a, float* scores, uint32_t* eword, cuda
 
 int launch_index_score(const dsv4_index_args& a, uint32_t* eword, cudaStream_t stream) {
     if (a.batch * a.n_q == 0) return DSV4_OK;
-    return launch_scores(a, a.scores_out, eword, stream);
+    return launch_scores(a, a.scores_out, nullptr, eword, stream, nullptr);
 }
 
-int launch_indexer(const dsv4_index_args& a, uint8_t* ws, uint32_t* eword, cudaStream_t stream) {
+int launch_indexer(const dsv4_index_args& a, uint8_t* ws, uint32_t* eword, cudaStream_t stream,
+                   const dsv4_compress_args* fresh_keys) {
     const int rows = a.batch * a.n_q;
     if (rows == 0) return DSV4_OK;
+    // workspace: [top-k workspace (its histogram first, zeroed by the caller)][scores]
+    uint8_t* topk_ws = ws;
     float* scores = a.scores_out;
-    uint8_t* rest = ws;
-    if (!scores) {
-        scores = reinterpret_cast<float*>(ws);
-        rest = ws + align_up(static_cast<size_t>(rows) * a.max_comp * 4, 256);
-    }
-    if (int rc = launch_scores(a, scores, eword, stream)) return rc;
+    if (!scores)
+        scores = reinterpret_cast<float*>(ws + align_up(topk_ws_bytes(rows, a.max_comp, a.top_k), 256));
+    // the top-k histogram is built by the scoring epilogue (shared-memory counts, flushed per row)
+    uint32_t* hist = topk_uses_hist(a.max_comp) ? topk_hist_buffer(topk_ws) : nullptr;
+    if (int rc = launch_scores(a, scores, hist, eword, stream, fresh_keys)) return rc;
     TopkRows t;
     t.scores = scores;
     t.n_vis = nullptr;
@@ -345,7 +402,10 @@ int launch_indexer(const dsv4_index_args& a, uint8_t* ws, uint32_t* eword, cudaS
     t.rows = rows;
     t.max_comp = a.max_comp;
     t.top_k = a.top_k;
-    return launch_topk(t, rest, eword, stream);
+    t.hist_zeroed = true;
+    t.hist_built = hist != nullptr;
+    t.pdl = true;
+    return launch_topk(t, topk_ws, eword, stream);
 }
 
 }  // namespace dsv4

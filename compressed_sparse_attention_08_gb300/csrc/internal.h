@@ -11,6 +11,8 @@
 namespace dsv4 {
 
 int launch_compress(const dsv4_compress_args& a, cudaStream_t stream);
+// Up to two compressions (e.g. main KV and indexer keys) in one launch; either may be null.
+int launch_compress2(const dsv4_compress_args* a, const dsv4_compress_args* b, cudaStream_t stream);
 
 // Top-k over fp32 score rows. Exactly one of n_vis (an int32 [rows] array) or the indexer
 // geometry (n_comp [batch], q_pos [batch, n_q] or null, ratio) gives each row's visible count.
@@ -22,12 +24,25 @@ struct TopkRows {
     int n_q, ratio;
     int32_t* idx_out;        // [rows, top_k]
     int rows, max_comp, top_k;
+    bool hist_zeroed;        // the long-row histogram and tickets were zeroed by the caller
+    bool hist_built;         // ... and already filled (by the scoring epilogue)
+    bool pdl;                // launch with programmatic dependent launch
 };
 size_t topk_ws_bytes(int rows, int max_comp, int top_k);
 int launch_topk(const TopkRows& t, uint8_t* ws, uint32_t* eword, cudaStream_t stream);
+// Long rows keep a top-12-bit key histogram ([rows, 4096] u32, then [rows] tickets) at the
+// start of the top-k workspace; a producer of scores may fill it (after it was zeroed).
+bool topk_uses_hist(int max_comp);
+uint32_t* topk_hist_buffer(uint8_t* topk_ws);
+size_t topk_hist_bytes(int rows);
 
 size_t index_ws_bytes(const dsv4_index_args& a);
-int launch_indexer(const dsv4_index_args& a, uint8_t* ws, uint32_t* eword, cudaStream_t stream);
+// Bytes at the start of the indexer workspace that must be zero when the call starts (the
+// long-row histogram and tickets); callers clear them together with the error word.
+size_t index_zero_bytes(const dsv4_index_args& a);
+// fresh_keys: the compression that writes key rows just before (its rows are waited for).
+int launch_indexer(const dsv4_index_args& a, uint8_t* ws, uint32_t* eword, cudaStream_t stream,
+                   const dsv4_compress_args* fresh_keys = nullptr);
 // Scores only (a.scores_out required); no top-k.
 int launch_index_score(const dsv4_index_args& a, uint32_t* eword, cudaStream_t stream);
 

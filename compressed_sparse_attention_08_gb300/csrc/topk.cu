@@ -8,15 +8,19 @@
 // masked, no host read of the count).
 //
 // Every score becomes an order-preserving 32-bit key (-0 and +0 share a key). The k-th
-// largest key T is found by radix selection (four 8-bit digits); `need` more copies of T are
-// taken, lowest indices first; one ordered pass (block prefix sums) writes the winners in
-// index order. Two implementations of the same rule:
+// largest key T is found by radix selection (8-bit digits); the first `need_T` keys equal to
+// T, in index order, complete the set. The winners are written in index order without a
+// block-wide scan per element: each warp owns a contiguous run of positions, counts its
+// (key > T) and (key == T) elements with ballots, one scan over the warps gives every warp
+// its starting counts, and element i lands at  #greater-before(i) + min(#ties-before(i),
+// need_T). Two implementations of the same rule:
 //   * rows that fit in shared memory (max_comp <= kSmallCap): one CTA per row, keys in smem.
-//   * long rows (1M context: 262,144 scores): the row is cut into P slices. A histogram
-//     kernel counts the top 12 key bits per row; a filter kernel finds the 12-bit bin that
-//     holds the k-th key and keeps, in index order, every element at or above that bin
-//     (a few thousand of 262,144); the last CTA of the row to finish (atomic ticket, no
-//     spinning) runs the exact selection on that short list.
+//   * long rows (1M context: 262,144 scores): the row is cut into P slices, one CTA each. A
+//     histogram of the top 12 key bits per row (built by the scoring kernel's epilogue when
+//     the scores come from the indexer, else by a histogram kernel) gives the 12-bit bin
+//     that holds the k-th key; every CTA keeps, in index order, the elements of its slice at
+//     or above that bin (a few thousand of 262,144 in all); the last CTA of the row to
+//     finish (atomic ticket, no spinning) selects exactly within that short list.
 #include "common.cuh"
 #include "internal.h"
 
@@ -28,65 +32,67 @@ constexpr int kBins = 4096;          // top-12-bit histogram of the long-row pat
 constexpr int kBinShift = 20;
 constexpr int kFinalCap = 12288;     // (key, index) pairs the finalizer keeps in smem
 constexpr int kMaxSlices = 64;
+constexpr int kNT = 1024;
 
-// Exclusive block prefix sum of 0/1 flags; `total` receives the block total.
-template <int NT>
-__device__ __forceinline__ int block_excl(bool flag, int* wsum, int& total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const unsigned m = __ballot_sync(0xffffffffu, flag);
-    const int pre = __popc(m & ((1u << lane) - 1u));
-    if (lane == 0) wsum[warp] = __popc(m);
-    __syncthreads();
-    if (warp == 0) {
-        int v = lane < NT / 32 ? wsum[lane] : 0;
+// Inclusive scan over the 32 lanes of a warp.
+__device__ __forceinline__ int warp_incl(int v) {
+    const int lane = threadIdx.x & 31;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int t = __shfl_up_sync(0xffffffffu, v, o);
-            if (lane >= o) v += t;
-        }
-        wsum[lane] = v;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
     }
-    __syncthreads();
-    const int base = warp ? wsum[warp - 1] : 0;
-    total = wsum[NT / 32 - 1];
-    __syncthreads();
-    return base + pre;
+    return v;
 }
 
-// Radix selection of the k-th largest key among n (1 <= k <= n). On return T is that key
-// and need_T how many keys equal to T belong to the top k.
+// Shared-memory histogram increment, aggregated over the lanes of a warp that hit the same
+// bin (scores cluster: without this, thousands of lanes serialise on one counter). Every
+// lane of the warp must call it (active or not).
+__device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t bin, bool active) {
+    const unsigned act = __ballot_sync(0xffffffffu, active);
+    if (!active) return;
+    const unsigned peers = __match_any_sync(act, bin);
+    if ((threadIdx.x & 31) == static_cast<unsigned>(__ffs(peers) - 1))
+        atomicAdd(&hist[bin], static_cast<uint32_t>(__popc(peers)));
+}
+
+// Radix selection among the keys whose top `known_bits` bits equal those of `prefix`
+// (all keys when known_bits is 0): finds the k-th largest of them (1 <= k <= their count)
+// with 8-bit digits below the known bits. On return T is that key and need_T how many keys
+// equal to T belong to the top k.
 template <int NT, class KeyAt>
 __device__ void radix_select(int n, int k, KeyAt key_at, uint32_t* hist, int* bc,
-                             uint32_t& T, int& need_T) {
-    uint32_t prefix = 0, mask = 0;
+                             uint32_t& T, int& need_T, uint32_t prefix = 0, int known_bits = 0) {
+    uint32_t mask = known_bits ? ~0u << (32 - known_bits) : 0u;
+    prefix &= mask;
     int need = k;
-    for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int low = 32 - known_bits; low > 0;) {
+        const int width = low >= 8 ? 8 : low;
+        const int shift = low - width;
+        const uint32_t dmask = (1u << width) - 1u;
         for (int i = threadIdx.x; i < 256; i += NT) hist[i] = 0;
         __syncthreads();
-        for (int i = threadIdx.x; i < n; i += NT) {
-            const uint32_t key = key_at(i);
-            if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+        for (int base = 0; base < n; base += NT) {
+            const int i = base + threadIdx.x;
+            const uint32_t key = i < n ? key_at(i) : 0u;
+            const bool match = i < n && (key & mask) == prefix;
+            hist_add(hist, (key >> shift) & dmask, match);
         }
         __syncthreads();
         if (threadIdx.x < 32) {
             const int lane = threadIdx.x;
-            uint32_t c[8], s = 0;
+            int c[8], s = 0;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) { c[i] = hist[255 - (lane * 8 + i)]; s += c[i]; }
-            uint32_t inc = s;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t t = __shfl_up_sync(0xffffffffu, inc, o);
-                if (lane >= o) inc += t;
-            }
-            const uint32_t before = inc - s;
-            if (before < static_cast<uint32_t>(need) && inc >= static_cast<uint32_t>(need)) {
-                uint32_t acc = before;
+            for (int i = 0; i < 8; ++i) { c[i] = static_cast<int>(hist[255 - (lane * 8 + i)]); s += c[i]; }
+            const int inc = warp_incl(s);
+            const int before = inc - s;
+            if (before < need && inc >= need) {
+                int acc = before;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    if (acc + c[i] >= static_cast<uint32_t>(need)) {
+                    if (acc + c[i] >= need) {
                         bc[0] = 255 - (lane * 8 + i);
-                        bc[1] = static_cast<int>(acc);
+                        bc[1] = acc;
                         break;
                     }
                     acc += c[i];
@@ -97,32 +103,52 @@ __device__ void radix_select(int n, int k, KeyAt key_at, uint32_t* hist, int* bc
         const uint32_t d = static_cast<uint32_t>(bc[0]);
         need -= bc[1];
         prefix |= d << shift;
-        mask |= 0xFFu << shift;
+        mask |= dmask << shift;
+        low = shift;
         __syncthreads();
     }
     T = prefix;
     need_T = need;
 }
 
-// Write, in position order, the index of every element with key > T and of the first
-// need_T elements with key == T. Stops once k indices are out.
+// Write the winners (key > T, and the first need_T keys == T) of positions 0..n-1 in
+// position order: element i goes to out[#greater-before(i) + min(#ties-before(i), need_T)].
 template <int NT, class KeyAt, class IdxAt>
-__device__ void ordered_compact(int n, int k, uint32_t T, int need_T, KeyAt key_at,
-                                IdxAt idx_at, int32_t* out, int* wsum) {
-    int ties_before = 0, written = 0;
-    for (int base = 0; base < n && written < k; base += NT) {
-        const int i = base + threadIdx.x;
-        const uint32_t key = i < n ? key_at(i) : 0u;
-        const bool tie = i < n && key == T;
-        const bool gt = i < n && key > T;
-        int tot_t, tot_s;
-        const int tr = block_excl<NT>(tie, wsum, tot_t);
-        const bool sel = gt || (tie && ties_before + tr < need_T);
-        const int pos = block_excl<NT>(sel, wsum, tot_s);
-        if (sel) out[written + pos] = idx_at(i);
-        ties_before += tot_t;
-        written += tot_s;
+__device__ void ordered_select(int n, uint32_t T, int need_T, KeyAt key_at, IdxAt idx_at,
+                               int32_t* out, int* s_gt, int* s_tie) {
+    constexpr int NW = NT / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int per = (n + NW - 1) / NW;
+    const int lo = warp * per < n ? warp * per : n;
+    const int hi = lo + per < n ? lo + per : n;
+    int gt = 0, tie = 0;
+    for (int base = lo; base < hi; base += 32) {
+        const int i = base + lane;
+        const uint32_t key = i < hi ? key_at(i) : 0u;
+        gt += __popc(__ballot_sync(0xffffffffu, i < hi && key > T));
+        tie += __popc(__ballot_sync(0xffffffffu, i < hi && key == T));
     }
+    if (lane == 0) { s_gt[warp] = gt; s_tie[warp] = tie; }
+    __syncthreads();
+    if (warp == 0) {
+        const int g = lane < NW ? s_gt[lane] : 0, t = lane < NW ? s_tie[lane] : 0;
+        const int gi = warp_incl(g), ti = warp_incl(t);
+        if (lane < NW) { s_gt[lane] = gi - g; s_tie[lane] = ti - t; }
+    }
+    __syncthreads();
+    int gb = s_gt[warp], tb = s_tie[warp];
+    const unsigned lt = (1u << lane) - 1u;
+    for (int base = lo; base < hi; base += 32) {
+        const int i = base + lane;
+        const uint32_t key = i < hi ? key_at(i) : 0u;
+        const bool g = i < hi && key > T, t = i < hi && key == T;
+        const unsigned bg = __ballot_sync(0xffffffffu, g), bt = __ballot_sync(0xffffffffu, t);
+        const int g_before = gb + __popc(bg & lt), t_before = tb + __popc(bt & lt);
+        if (g || (t && t_before < need_T)) out[g_before + (t_before < need_T ? t_before : need_T)] = idx_at(i);
+        gb += __popc(bg);
+        tb += __popc(bt);
+    }
+    __syncthreads();
 }
 
 // Rows where every visible entry is selected: 0..n-1 then -1.
@@ -137,8 +163,10 @@ __global__ void __launch_bounds__(NT)
 topk_small_kernel(TopkRows t, uint32_t* eword) {
     extern __shared__ uint32_t skeys[];
     __shared__ uint32_t hist[256];
-    __shared__ int wsum[32];
+    __shared__ int s_a[32], s_b[32];
     __shared__ int bc[2];
+    pdl_trigger();
+    pdl_wait();
     const int row = blockIdx.x;
     const int n = row_visible(t.n_vis, t.n_comp, t.q_pos, t.n_q, t.ratio, t.max_comp, row, eword);
     const int k = n < t.top_k ? n : t.top_k;
@@ -155,19 +183,19 @@ topk_small_kernel(TopkRows t, uint32_t* eword) {
     int need_T;
     auto key_at = [&](int i) { return skeys[i]; };
     radix_select<NT>(n, k, key_at, hist, bc, T, need_T);
-    ordered_compact<NT>(n, k, T, need_T, key_at, [](int i) { return i; }, out, wsum);
+    ordered_select<NT>(n, T, need_T, key_at, [](int i) { return i; }, out, s_a, s_b);
 }
 
 // ------------------------------------------------------------------ long rows
 struct LongWs {
     uint32_t* hist;     // [rows, kBins]
-    int32_t* counts;    // [rows, P]
-    uint32_t* done;     // [rows]
+    uint32_t* done;     // [rows] tickets
+    int32_t* counts;    // [rows, kMaxSlices]
     uint2* pairs;       // [rows, max_comp]: (key, index) survivors, slice p at p * L
 };
 
 __device__ __forceinline__ void slice_range(int n, int L, int p, int& lo, int& hi) {
-    lo = p * L;
+    lo = p * L < n ? p * L : n;
     hi = lo + L < n ? lo + L : n;
 }
 
@@ -175,6 +203,8 @@ template <int NT>
 __global__ void __launch_bounds__(NT)
 topk_hist_kernel(TopkRows t, LongWs w, int L, uint32_t* eword) {
     __shared__ uint32_t h[kBins];
+    pdl_trigger();
+    pdl_wait();
     const int row = blockIdx.x, p = blockIdx.y;
     const int n = row_visible(t.n_vis, t.n_comp, t.q_pos, t.n_q, t.ratio, t.max_comp, row, eword);
     if (n <= t.top_k) return;
@@ -192,82 +222,117 @@ topk_hist_kernel(TopkRows t, LongWs w, int L, uint32_t* eword) {
 }
 
 template <int NT>
-__global__ void __launch_bounds__(NT)
+__global__ void __launch_bounds__(NT, 1)
 topk_filter_kernel(TopkRows t, LongWs w, int L, int P, uint32_t* eword) {
+    constexpr int NW = NT / 32;
     extern __shared__ uint2 spairs[];           // kFinalCap pairs (finalizer only)
-    __shared__ uint32_t hist[kBins];
-    __shared__ int wsum[32];
+    __shared__ uint32_t hist[256];
+    __shared__ int s_a[32], s_b[32];
     __shared__ int bc[2];
     __shared__ int offs[kMaxSlices + 1];
     __shared__ int is_last;
+    pdl_trigger();
+    pdl_wait();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int row = blockIdx.x, p = blockIdx.y;
     const int n = row_visible(t.n_vis, t.n_comp, t.q_pos, t.n_q, t.ratio, t.max_comp, row, eword);
-    const int top_k = t.top_k;
-    int32_t* out = t.idx_out + static_cast<size_t>(row) * top_k;
-    if (n <= top_k) {                            // every visible entry is selected
-        const int per = (top_k + P - 1) / P;
-        write_all(out, n, top_k, p * per + threadIdx.x, (p + 1) * per, NT);
+    const int k = t.top_k;
+    int32_t* out = t.idx_out + static_cast<size_t>(row) * k;
+    if (n <= k) {                                // every visible entry is selected
+        const int per = (k + P - 1) / P;
+        write_all(out, n, k, p * per + threadIdx.x, (p + 1) * per, NT);
         return;
     }
-    const int k = top_k;
-    // 1. the 12-bit bin holding the k-th largest key (same answer in every CTA of the row)
-    const uint32_t* g = w.hist + static_cast<size_t>(row) * kBins;
-    for (int i = threadIdx.x; i < kBins; i += NT) hist[i] = g[i];
-    __syncthreads();
+    // 1. the 12-bit bin tb holding the k-th largest key, and how many keys lie above it
     {
-        constexpr int per = kBins / NT;          // bins per thread, taken from the top down
-        uint32_t c[per], s = 0;
+        constexpr int per = kBins / NT;          // bins per thread, from the top down
+        const uint32_t* g = w.hist + static_cast<size_t>(row) * kBins;
+        int c[per], s = 0;
 #pragma unroll
-        for (int i = 0; i < per; ++i) { c[i] = hist[kBins - 1 - (threadIdx.x * per + i)]; s += c[i]; }
-        // inclusive block scan of s in thread order
-        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-        uint32_t inc = s;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t v = __shfl_up_sync(0xffffffffu, inc, o);
-            if (lane >= o) inc += v;
-        }
-        if (lane == 31) wsum[warp] = static_cast<int>(inc);
+        for (int i = 0; i < per; ++i) { c[i] = static_cast<int>(__ldcg(&g[kBins - 1 - (threadIdx.x * per + i)])); s += c[i]; }
+        int inc = warp_incl(s);
+        if (lane == 31) s_a[warp] = inc;
         __syncthreads();
         if (warp == 0) {
-            int v = lane < NT / 32 ? wsum[lane] : 0;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int u = __shfl_up_sync(0xffffffffu, v, o);
-                if (lane >= o) v += u;
-            }
-            wsum[lane] = v;
+            const int v = lane < NW ? s_a[lane] : 0;
+            const int vi = warp_incl(v);
+            if (lane < NW) s_a[lane] = vi - v;
         }
         __syncthreads();
-        inc += warp ? static_cast<uint32_t>(wsum[warp - 1]) : 0u;
-        const uint32_t before = inc - s;
-        if (before < static_cast<uint32_t>(k) && inc >= static_cast<uint32_t>(k)) {
-            uint32_t acc = before;
+        inc += s_a[warp];
+        const int before = inc - s;
+        if (before < k && inc >= k) {
+            int acc = before;
+#pragma unroll
             for (int i = 0; i < per; ++i) {
-                if (acc + c[i] >= static_cast<uint32_t>(k)) { bc[0] = kBins - 1 - (threadIdx.x * per + i); break; }
+                if (acc + c[i] >= k) {
+                    bc[0] = kBins - 1 - (threadIdx.x * per + i);
+                    bc[1] = acc;                    // keys in bins above tb
+                    break;
+                }
                 acc += c[i];
             }
         }
         __syncthreads();
     }
     const uint32_t tb = static_cast<uint32_t>(bc[0]);
-    __syncthreads();
-    // 2. survivors of this slice (bin >= tb), in index order
+    const int above = bc[1];
+    // 2. survivors of this slice (bin >= tb), in index order, warp-contiguous runs; each
+    //    lane holds up to kRegs keys of its warp's run in registers (one round trip)
     int lo, hi;
     slice_range(n, L, p, lo, hi);
-    const float* s = t.scores + static_cast<size_t>(row) * t.max_comp;
+    const float* sc = t.scores + static_cast<size_t>(row) * t.max_comp;
     uint2* seg = w.pairs + static_cast<size_t>(row) * t.max_comp + static_cast<size_t>(p) * L;
-    int cnt = 0;
-    for (int base = lo; base < hi; base += NT) {
-        const int i = base + threadIdx.x;
-        const uint32_t key = i < hi ? float_to_key(s[i]) : 0u;
-        const bool keep = i < hi && (key >> kBinShift) >= tb;
-        int tot;
-        const int pos = block_excl<NT>(keep, wsum, tot);
-        if (keep) seg[cnt + pos] = make_uint2(key, static_cast<uint32_t>(i));
-        cnt += tot;
+    {
+        constexpr int kRegs = 8;
+        const int len = hi - lo;
+        const int per = (len + NW - 1) / NW;
+        const int wlo = lo + (warp * per < len ? warp * per : len);
+        const int whi = wlo + per < hi ? wlo + per : hi;
+        const unsigned lt = (1u << lane) - 1u;
+        int cnt = 0;
+        for (int b0 = wlo; b0 < whi; b0 += 32 * kRegs) {
+            uint32_t key[kRegs];
+#pragma unroll
+            for (int r = 0; r < kRegs; ++r) {
+                const int i = b0 + r * 32 + lane;
+                key[r] = i < whi ? float_to_key(__ldcg(&sc[i])) : 0u;
+            }
+#pragma unroll
+            for (int r = 0; r < kRegs; ++r) {
+                const int i = b0 + r * 32 + lane;
+                cnt += __popc(__ballot_sync(0xffffffffu, i < whi && (key[r] >> kBinShift) >= tb));
+            }
+        }
+        __syncthreads();                         // s_a is reused
+        if (lane == 0) s_a[warp] = cnt;
+        __syncthreads();
+        if (warp == 0) {
+            const int v = lane < NW ? s_a[lane] : 0;
+            const int vi = warp_incl(v);
+            if (lane < NW) s_a[lane] = vi - v;
+            if (lane == NW - 1) s_b[0] = vi;
+        }
+        __syncthreads();
+        int pos = s_a[warp];
+        for (int b0 = wlo; b0 < whi; b0 += 32 * kRegs) {
+            uint32_t key[kRegs];
+#pragma unroll
+            for (int r = 0; r < kRegs; ++r) {
+                const int i = b0 + r * 32 + lane;
+                key[r] = i < whi ? float_to_key(__ldcg(&sc[i])) : 0u;
+            }
+#pragma unroll
+            for (int r = 0; r < kRegs; ++r) {
+                const int i = b0 + r * 32 + lane;
+                const bool keep = i < whi && (key[r] >> kBinShift) >= tb;
+                const unsigned bk = __ballot_sync(0xffffffffu, keep);
+                if (keep) seg[pos + __popc(bk & lt)] = make_uint2(key[r], static_cast<uint32_t>(i));
+                pos += __popc(bk);
+            }
+        }
+        if (threadIdx.x == 0) w.counts[static_cast<size_t>(row) * kMaxSlices + p] = s_b[0];
     }
-    if (threadIdx.x == 0) w.counts[static_cast<size_t>(row) * P + p] = cnt;
     // 3. the last CTA of the row to get here finishes the row (no waiting on anyone)
     __threadfence();
     __syncthreads();
@@ -278,57 +343,60 @@ topk_filter_kernel(TopkRows t, LongWs w, int L, int P, uint32_t* eword) {
     __syncthreads();
     if (!is_last) return;
     __threadfence();
-    if (threadIdx.x == 0) {
-        int acc = 0;
-        for (int q = 0; q < P; ++q) {
-            offs[q] = acc;
-            acc += __ldcg(&w.counts[static_cast<size_t>(row) * P + q]);
-        }
-        offs[P] = acc;
-        w.done[row] = 0;                         // ready for the next call
+    if (threadIdx.x < 64) {                      // exclusive scan of the P <= 64 slice counts
+        int v = threadIdx.x < P ? __ldcg(&w.counts[static_cast<size_t>(row) * kMaxSlices + threadIdx.x]) : 0;
+        v = warp_incl(v);
+        if (threadIdx.x == 31) s_b[1] = v;
+        offs[threadIdx.x + 1] = v;
+        if (threadIdx.x == 0) offs[0] = 0;
     }
+    __syncthreads();
+    if (threadIdx.x >= 32 && threadIdx.x < 64) offs[threadIdx.x + 1] += s_b[1];
     __syncthreads();
     const int total = offs[P];
     const uint2* rowpairs = w.pairs + static_cast<size_t>(row) * t.max_comp;
-    for (int j = k + threadIdx.x; j < top_k; j += NT) out[j] = -1;
+    auto slice_of = [&](int i) {                 // slice q with offs[q] <= i < offs[q + 1]
+        int a = 0, b = P - 1;
+        while (a < b) {
+            const int mid = (a + b + 1) >> 1;
+            if (offs[mid] <= i) a = mid; else b = mid - 1;
+        }
+        return a;
+    };
     uint32_t T;
     int need_T;
     if (total <= kFinalCap) {
-        for (int q = 0; q < P; ++q) {
-            const int c = offs[q + 1] - offs[q];
-            for (int i = threadIdx.x; i < c; i += NT)
-                spairs[offs[q] + i] = __ldcg(&rowpairs[static_cast<size_t>(q) * L + i]);
+        for (int i = threadIdx.x; i < total; i += NT) {
+            const int q = slice_of(i);
+            spairs[i] = __ldcg(&rowpairs[static_cast<size_t>(q) * L + (i - offs[q])]);
         }
         __syncthreads();
         auto key_at = [&](int i) { return spairs[i].x; };
         auto idx_at = [&](int i) { return static_cast<int32_t>(spairs[i].y); };
-        radix_select<NT>(total, k, key_at, hist, bc, T, need_T);
-        ordered_compact<NT>(total, k, T, need_T, key_at, idx_at, out, wsum);
+        radix_select<NT>(total, k - above, key_at, hist, bc, T, need_T, tb << kBinShift, 32 - kBinShift);
+        ordered_select<NT>(total, T, need_T, key_at, idx_at, out, s_a, s_b);
     } else {
         // degenerate score distributions (huge ties): the same steps on the slices in place
         auto at = [&](int i) {
-            int q = 0;
-            while (q + 1 < P && offs[q + 1] <= i) ++q;
+            const int q = slice_of(i);
             return __ldcg(&rowpairs[static_cast<size_t>(q) * L + (i - offs[q])]);
         };
         auto key_at = [&](int i) { return at(i).x; };
         auto idx_at = [&](int i) { return static_cast<int32_t>(at(i).y); };
-        radix_select<NT>(total, k, key_at, hist, bc, T, need_T);
-        ordered_compact<NT>(total, k, T, need_T, key_at, idx_at, out, wsum);
+        radix_select<NT>(total, k - above, key_at, hist, bc, T, need_T, tb << kBinShift, 32 - kBinShift);
+        ordered_select<NT>(total, T, need_T, key_at, idx_at, out, s_a, s_b);
     }
 }
-
-constexpr int kNT = 512;
 
 struct LongPlan { int P, L; };
 
 LongPlan long_plan(int rows, int max_comp) {
-    int P = (2 * 148 + rows - 1) / (rows > 0 ? rows : 1);
+    const int sms = sm_count() > 0 ? sm_count() : 148;
+    int P = (sms + rows - 1) / (rows > 0 ? rows : 1);
     if (P < 1) P = 1;
     if (P > kMaxSlices) P = kMaxSlices;
     int L = (max_comp + P - 1) / P;
-    L = (L + 255) / 256 * 256;
-    if (L < 1024) L = 1024;
+    L = (L + 1023) / 1024 * 1024;
     P = (max_comp + L - 1) / L;
     if (P < 1) P = 1;
     return {P, L};
@@ -339,14 +407,17 @@ LongPlan long_plan(int rows, int max_comp) {
 size_t topk_ws_bytes(int rows, int max_comp, int top_k) {
     (void)top_k;
     if (max_comp <= kSmallCap) return 0;
-    const LongPlan pl = long_plan(rows, max_comp);
     size_t b = 0;
-    b += align_up(static_cast<size_t>(rows) * kBins * 4, 256);
-    b += align_up(static_cast<size_t>(rows) * pl.P * 4, 256);
-    b += align_up(static_cast<size_t>(rows) * 4, 256);
+    b += static_cast<size_t>(rows) * kBins * 4;           // histograms, then
+    b += align_up(static_cast<size_t>(rows) * 4, 256);    // tickets (one memset clears both)
+    b += align_up(static_cast<size_t>(rows) * kMaxSlices * 4, 256);
     b += align_up(static_cast<size_t>(rows) * max_comp * 8, 256);
     return b;
 }
+
+uint32_t* topk_hist_buffer(uint8_t* ws) { return reinterpret_cast<uint32_t*>(ws); }
+size_t topk_hist_bytes(int rows) { return static_cast<size_t>(rows) * (kBins + 1) * 4; }
+bool topk_uses_hist(int max_comp) { return max_comp > kSmallCap; }
 
 int launch_topk(const TopkRows& t, uint8_t* ws, uint32_t* eword, cudaStream_t stream) {
     if (t.rows == 0) return DSV4_OK;
@@ -358,22 +429,22 @@ int launch_topk(const TopkRows& t, uint8_t* ws, uint32_t* eword, cudaStream_t st
                                  kSmallCap * 4);
             attr_set = true;
         }
-        topk_small_kernel<kNT><<<t.rows, kNT, smem, stream>>>(t, eword);
         count_launch();
-        return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_LAUNCH;
+        return launch_k(topk_small_kernel<kNT>, dim3(t.rows), dim3(kNT), smem, stream, t.pdl, t, eword)
+                   == cudaSuccess ? DSV4_OK : DSV4_ERR_LAUNCH;
     }
     const LongPlan pl = long_plan(t.rows, t.max_comp);
     LongWs w;
     uint8_t* p = ws;
     w.hist = reinterpret_cast<uint32_t*>(p);
-    p += align_up(static_cast<size_t>(t.rows) * kBins * 4, 256);
-    w.counts = reinterpret_cast<int32_t*>(p);
-    p += align_up(static_cast<size_t>(t.rows) * pl.P * 4, 256);
+    p += static_cast<size_t>(t.rows) * kBins * 4;
     w.done = reinterpret_cast<uint32_t*>(p);
     p += align_up(static_cast<size_t>(t.rows) * 4, 256);
+    w.counts = reinterpret_cast<int32_t*>(p);
+    p += align_up(static_cast<size_t>(t.rows) * kMaxSlices * 4, 256);
     w.pairs = reinterpret_cast<uint2*>(p);
-    if (cudaMemsetAsync(w.hist, 0, static_cast<size_t>(t.rows) * kBins * 4, stream) != cudaSuccess ||
-        cudaMemsetAsync(w.done, 0, static_cast<size_t>(t.rows) * 4, stream) != cudaSuccess)
+    if (!t.hist_zeroed &&
+        cudaMemsetAsync(w.hist, 0, topk_hist_bytes(t.rows), stream) != cudaSuccess)
         return DSV4_ERR_LAUNCH;
     static bool attr_set = false;
     if (!attr_set) {
@@ -382,10 +453,14 @@ int launch_topk(const TopkRows& t, uint8_t* ws, uint32_t* eword, cudaStream_t st
         attr_set = true;
     }
     dim3 grid(t.rows, pl.P);
-    topk_hist_kernel<kNT><<<grid, kNT, 0, stream>>>(t, w, pl.L, eword);
-    topk_filter_kernel<kNT><<<grid, kNT, kFinalCap * 8, stream>>>(t, w, pl.L, pl.P, eword);
-    count_launch(2);
-    return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_LAUNCH;
+    if (!t.hist_built) {
+        count_launch();
+        if (launch_k(topk_hist_kernel<kNT>, grid, dim3(kNT), 0, stream, t.pdl, t, w, pl.L, eword) != cudaSuccess)
+            return DSV4_ERR_LAUNCH;
+    }
+    count_launch();
+    return launch_k(topk_filter_kernel<kNT>, grid, dim3(kNT), size_t(kFinalCap * 8), stream, t.pdl, t, w,
+                    pl.L, pl.P, eword) == cudaSuccess ? DSV4_OK : DSV4_ERR_LAUNCH;
 }
 
 }  // namespace dsv4
