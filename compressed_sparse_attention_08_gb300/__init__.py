@@ -11,7 +11,7 @@ from ._abi import (  # noqa: F401
     DSV4_ERR_UNSUPPORTED, DSV4_EWORD_BAD_INDEX, DSV4_EWORD_TIMEOUT, Dsv4Error, library,
     library_path, dsv4_compress, dsv4_indexer_topk, dsv4_indexer_topk_workspace_size,
     dsv4_index_score, dsv4_index_score_workspace_size,
-    dsv4_topk, dsv4_topk_workspace_size, dsv4_sparse_attn_decode,
+    dsv4_topk, dsv4_topk_workspace_size, dsv4_topk_noalloc, dsv4_sparse_attn_decode,
     dsv4_sparse_attn_workspace_size, dsv4_csa_decode, dsv4_csa_decode_workspace_size,
     dsv4_read_error_word, dsv4_status_string, dsv4_last_launch_count, dsv4_max_comp,
     EXPORTED_SYMBOLS,

@@ -24,7 +24,7 @@ DSV4_EWORD_TIMEOUT = 0x2
 EXPORTED_SYMBOLS = (
     "dsv4_compress", "dsv4_indexer_topk_workspace_size", "dsv4_indexer_topk",
     "dsv4_index_score_workspace_size", "dsv4_index_score",
-    "dsv4_topk_workspace_size", "dsv4_topk", "dsv4_sparse_attn_workspace_size",
+    "dsv4_topk_workspace_size", "dsv4_topk", "dsv4_topk_noalloc", "dsv4_sparse_attn_workspace_size",
     "dsv4_sparse_attn_decode", "dsv4_csa_decode_workspace_size", "dsv4_csa_decode",
     "dsv4_status_string", "dsv4_read_error_word", "dsv4_last_launch_count", "dsv4_max_comp",
 )
@@ -96,6 +96,8 @@ def library():
         lib.dsv4_topk_workspace_size.argtypes = [ctypes.POINTER(TopkArgs)]
         lib.dsv4_topk_workspace_size.restype = ctypes.c_size_t
         lib.dsv4_topk.argtypes = [ctypes.POINTER(TopkArgs), P, ctypes.c_size_t, P]
+        lib.dsv4_topk_noalloc.argtypes = [ctypes.POINTER(TopkArgs), P]
+        lib.dsv4_topk_noalloc.restype = I
         lib.dsv4_sparse_attn_workspace_size.argtypes = [ctypes.POINTER(AttnArgs)]
         lib.dsv4_sparse_attn_workspace_size.restype = ctypes.c_size_t
         lib.dsv4_sparse_attn_decode.argtypes = [ctypes.POINTER(AttnArgs), P, ctypes.c_size_t, P]
@@ -242,6 +244,15 @@ def dsv4_topk(scores, n_vis, idx_out, ws, *, stream=None):
     a = topk_args(scores, n_vis, idx_out)
     _check(library().dsv4_topk(ctypes.byref(a), _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
                                _stream(stream)), "dsv4_topk")
+
+
+def dsv4_topk_noalloc(scores, n_vis, idx_out, *, stream=None):
+    """dsv4_topk without a workspace, for callers that cannot allocate device memory: the
+    library's fixed 16 MiB per-GPU scratch array is used instead. Calls must not overlap on
+    the GPU; sizes needing more scratch than the array holds raise Dsv4Error
+    (DSV4_ERR_INVALID_ARG)."""
+    a = topk_args(scores, n_vis, idx_out)
+    _check(library().dsv4_topk_noalloc(ctypes.byref(a), _stream(stream)), "dsv4_topk_noalloc")
 
 
 def dsv4_sparse_attn_workspace_size(q, sink, comp_kv, n_comp, win, win_len, out, **kw):

@@ -142,6 +142,21 @@ typedef struct dsv4_topk_args {
 size_t dsv4_topk_workspace_size(const dsv4_topk_args* args);
 int dsv4_topk(const dsv4_topk_args* args, void* ws, size_t ws_bytes, dsv4_stream_t stream);
 
+/* Stage 3 alone, for callers that cannot allocate device memory (for instance code running
+ * inside an allocator hook, a serving loop that forbids cudaMalloc after start-up, or a
+ * plug-in that receives only its input and output buffers). The pages have no counterpart
+ * for this entry point: it is a convenience of this library. Same arguments, rule and
+ * results as dsv4_topk, but no workspace: the scratch it needs lives in a fixed 16 MiB
+ * device array that the library reserves on each GPU it runs on and keeps until the process
+ * exits. Calls whose scratch need (dsv4_topk_workspace_size(args)) exceeds 16 MiB return
+ * DSV4_ERR_INVALID_ARG before any launch (for 262,144-entry rows: up to 7 rows per call).
+ * The first call on a device looks up the array's device address (make that first call
+ * before any stream capture). Every call shares the one array, so calls that overlap on the
+ * GPU (different streams, or different host threads) race and must not be issued; each call
+ * clears what it needs. Device-side findings (counts out of range) are not reported by this
+ * variant. No memory is allocated or freed. */
+int dsv4_topk_noalloc(const dsv4_topk_args* args, dsv4_stream_t stream);
+
 /* ---------------------------------------------------------------------------------------
  * Stage 4. Gather into the caller's buffer + MQA attention with a per-head sink.
  *
