@@ -4,6 +4,7 @@
 // except dsv4_read_error_word, which exists for tests and diagnostics.
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -74,7 +75,7 @@ bool attn_ok(const dsv4_attn_args* a) {
         return false;
     if (a->batch < 0 || a->n_q < 1) return false;
     if (a->dim != 128 && a->dim != 256 && a->dim != 512) return false;
-    if (a->heads < 1 || a->heads > 64) return false;
+    if (a->heads < 1 || a->heads > 64 || (a->heads > 16 && a->heads % 16 != 0)) return false;
     if (a->max_comp < 1 || a->top_k < 1 || a->window < 0 || a->win_rows < 1 || a->ratio < 1) return false;
     if (a->idx ? a->top_k > a->max_comp : a->top_k != a->max_comp) return false;
     if (!std::isfinite(a->scale)) return false;
@@ -93,6 +94,18 @@ struct LaunchScope {
 }  // namespace
 
 void count_launch(int n) { g_launches += n; }
+
+void prefer_max_shared(const void* kernel) {
+    static std::mutex mu;
+    static const void* seen[256];
+    static int n_seen = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n_seen; ++i)
+        if (seen[i] == kernel) return;
+    cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         cudaSharedmemCarveoutMaxShared);
+    if (n_seen < 256) seen[n_seen++] = kernel;
+}
 
 int sm_count() {
     static int cache[64] = {0};

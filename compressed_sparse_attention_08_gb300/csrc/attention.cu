@@ -9,19 +9,22 @@
 // master..pure-nvfp4", single_shot_inference.py eager_attention (scale = 1/sqrt(hd)).
 //
 // Design (decode: few queries, many rows; prefill: many queries):
-//   * the row list of one query is its top_k compressed slots then its window slots; it is
-//     cut into 64-row chunks and the chunks into `n_splits` contiguous ranges, one CTA per
-//     (range, query) so that a 4-sequence decode still fills the GPU (split-K);
-//   * each CTA stages Q (heads x D, zero-padded to a multiple of 16 heads) once, then
-//     streams chunks through two cp.async buffers: the rows are gathered by index straight
-//     from the cache (16-byte copies), written to the gather buffer from shared memory, and
-//     consumed by bf16 tensor-core MMAs (fp32 accumulate): S = Q K^T, an online softmax in
-//     fp32, O += P V with P rounded to bf16;
+//   * a gather kernel materialises the gather buffer (the caller's, or workspace): one warp
+//     per row, 16-byte vector loads of whole rows with several rows in flight per warp, so
+//     the random 1 KB rows stream at memory speed across every SM;
+//   * the attention kernel then reads that contiguous, L2-resident buffer in 64-row chunks
+//     with TMA tile loads (8 per chunk, one per 64-dim box, 128-byte swizzle) into two
+//     alternating buffers; Q arrives the same way, once per CTA;
+//   * the chunks of one query (compressed slots first, then window slots) are cut into
+//     `n_splits` contiguous ranges and the heads into groups of 16, one CTA per (range,
+//     query, head group): a 4-sequence decode still fills the GPU while each split stays
+//     long enough that its fp32 partial (16 heads x D) is small next to the rows it read;
+//   * bf16 tensor-core MMAs (fp32 accumulate): S = Q K^T, an online softmax in fp32,
+//     O += P V with P rounded to bf16; masked slots (index -1, past the window) are excluded
+//     from the softmax;
 //   * a split writes (m, l, O) partials; the combine kernel merges them per (query, head)
 //     and adds the sink once: o = sum_s O_s e^(m_s-M) / (sum_s l_s e^(m_s-M) + e^(sink-M)),
 //     M = max(sink, m_s). With one split the CTA finishes the output itself.
-// Shared-memory rows use a 16-byte-chunk XOR swizzle (chunk ^ (row & 7)) so the ldmatrix
-// reads are free of bank conflicts.
 #include "common.cuh"
 #include "internal.h"
 
@@ -32,29 +35,20 @@ constexpr int kCH = 64;      // rows per chunk
 constexpr int kNT = 256;     // 8 warps
 
 struct AttnParams {
-    const __nv_bfloat16* q;        // [rows, H, D]
     const float* sink;             // [H]
-    const __nv_bfloat16* comp_kv;  // [B, max_comp, D]
     const int32_t* n_comp;         // [B]
     const int32_t* idx;            // [rows, top_k] or null
     const int64_t* q_pos;          // [rows] or null
-    const __nv_bfloat16* win;      // [B, win_rows, D]
     const int32_t* win_len;        // [B]
-    __nv_bfloat16* gather;         // [rows, slots, D] or null
     __nv_bfloat16* out;            // [rows, H, D]
-    float* part_ml;                // [rows, n_splits, HP, 2]
-    float* part_o;                 // [rows, n_splits, HP, D]
+    float* part_ml;                // [rows, n_splits, hstride, 2]
+    float* part_o;                 // [rows, n_splits, hstride, D]
     uint32_t* eword;
-    int rows, n_q, H, max_comp, top_k, window, win_rows, ratio, slots, n_chunks,
-        chunks_per_split, n_splits;
+    int rows, n_q, H, max_comp, top_k, window, win_rows, ratio, slots, comp_chunks, n_chunks,
+        chunks_per_split, n_splits, oob_row;
+    int n_hg, hstride;             // head groups per query, heads per partial record (n_hg*HP)
     float scale;
 };
-
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_u32(smem)), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t* r) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -75,16 +69,85 @@ __device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-
-// byte offset of 16-byte chunk `c` of row `r` in a swizzled array with ROWB bytes per row
-template <int ROWB>
-__device__ __forceinline__ uint32_t swz(int r, int c) {
-    return static_cast<uint32_t>(r * ROWB + ((c ^ (r & 7)) << 4));
+// Byte offset of 16-byte chunk c16 of row r in a tile stored as 64-element (128-byte) boxes of
+// `rows` rows each, 128-byte swizzle (chunk ^ (row & 7)) within every box.
+__device__ __forceinline__ uint32_t boxoff(int r, int c16, int rows) {
+    return static_cast<uint32_t>((c16 >> 3) * rows * 128 + r * 128 + (((c16 & 7) ^ (r & 7)) << 4));
+}
+// Row-major 64-column bf16 tile (128-byte rows), same swizzle.
+__device__ __forceinline__ uint32_t swz128(int r, int c16) {
+    return static_cast<uint32_t>(r * 128 + ((c16 ^ (r & 7)) << 4));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// ------------------------------------------------------------------ gather
+// Rows of the gather buffer: slot j < top_k holds comp_kv[b, idx[j]] (zeros for -1), slot
+// top_k + i the i-th window row of the query (zeros past the window). One warp per row, each
+// lane moving 16-byte pieces; every warp takes kRowsPerWarp rows with all loads issued before
+// any store, so hundreds of random 1 KB rows are in flight per SM.
+constexpr int kRowsPerWarp = 4;
+
+template <int D>
+__global__ void __launch_bounds__(256)
+gather_kernel(AttnParams p, const __nv_bfloat16* __restrict__ comp_kv,
+              const __nv_bfloat16* __restrict__ win, __nv_bfloat16* __restrict__ gbuf) {
+    constexpr int U = D / 8;                      // 16-byte pieces per row
+    constexpr int PL = (U + 31) / 32;             // pieces per lane
+    pdl_trigger();
+    pdl_wait();                                   // the index list comes from the kernel before
+    const int lane = threadIdx.x & 31;
+    const long long total = static_cast<long long>(p.rows) * p.slots;
+    const long long first = (static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * kRowsPerWarp;
+    uint4 v[kRowsPerWarp][PL];
+    long long dst_row[kRowsPerWarp];
+#pragma unroll
+    for (int k = 0; k < kRowsPerWarp; ++k) {
+        const long long gr = first + k;
+        dst_row[k] = gr < total ? gr : -1;
+        const __nv_bfloat16* src = nullptr;
+        if (gr < total) {
+            const int row = static_cast<int>(gr / p.slots), slot = static_cast<int>(gr - static_cast<long long>(row) * p.slots);
+            const int b = row / p.n_q, t = row - b * p.n_q;
+            if (slot < p.top_k) {
+                const int nv = row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, row, nullptr);
+                int e;
+                if (p.idx) {
+                    e = p.idx[static_cast<size_t>(row) * p.top_k + slot];
+                    if (e >= nv) { if (lane == 0) flag_error(p.eword, DSV4_EWORD_BAD_INDEX); e = -1; }
+                } else {
+                    e = slot < nv ? slot : -1;
+                }
+                if (e >= 0) src = comp_kv + (static_cast<size_t>(b) * p.max_comp + e) * D;
+            } else {
+                int wl = p.win_len[b];
+                wl = wl < 0 ? 0 : (wl > p.win_rows ? p.win_rows : wl);
+                const int w_hi = t + wl - p.n_q;
+                const int w_lo = w_hi - p.window + 1 > 0 ? w_hi - p.window + 1 : 0;
+                const int w_top = w_hi < wl - 1 ? w_hi : wl - 1;
+                const int w_cnt = w_top >= w_lo ? w_top - w_lo + 1 : 0;
+                const int wi = slot - p.top_k;
+                if (wi < w_cnt) src = win + (static_cast<size_t>(b) * p.win_rows + w_lo + wi) * D;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < PL; ++j) {
+            const int u = lane + 32 * j;
+            v[k][j] = (src && u < U) ? __ldcs(reinterpret_cast<const uint4*>(src) + u) : make_uint4(0, 0, 0, 0);
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < kRowsPerWarp; ++k) {
+        if (dst_row[k] < 0) continue;
+#pragma unroll
+        for (int j = 0; j < PL; ++j) {
+            const int u = lane + 32 * j;
+            if (u < U) reinterpret_cast<uint4*>(gbuf + dst_row[k] * D)[u] = v[k][j];
+        }
+    }
 }
 
 template <int D, int HP>
@@ -94,22 +157,27 @@ struct Cfg {
     static constexpr int RW = kCH / NRG;        // chunk rows per warp in S
     static constexpr int NDG = 8 / NHG;         // dim groups of the O tile
     static constexpr int DW = D / NDG;          // dims per warp in O
-    static constexpr int ROWB = D * 2;
-    static constexpr size_t OFF_KV = static_cast<size_t>(HP) * ROWB;
-    static constexpr size_t OFF_P = OFF_KV + 2ull * kCH * ROWB;
+    static constexpr int NBOX = D / 64;
+    static constexpr size_t KVBUF = static_cast<size_t>(kCH) * D * 2;
+    static constexpr size_t OFF_KV = static_cast<size_t>(HP) * D * 2;
+    static constexpr size_t OFF_P = OFF_KV + 2 * KVBUF;
     static constexpr size_t OFF_F = OFF_P + static_cast<size_t>(HP) * 128;
     static constexpr size_t N_F = 2ull * NRG * HP + 3ull * HP;
-    static constexpr size_t OFF_SRC = align_up(OFF_F + N_F * 4, 16);
-    static constexpr size_t SMEM = OFF_SRC + 2ull * kCH * sizeof(void*);
+    static constexpr size_t OFF_I = align_up(OFF_F + N_F * 4, 16);
+    static constexpr size_t OFF_BAR = align_up(OFF_I + 4ull * kCH * 4, 16);
+    static constexpr size_t SMEM = OFF_BAR + 3 * 8 + 1024;   // + alignment slack
     static_assert(RW % 8 == 0 && DW % 16 == 0, "tile split");
 };
 
 template <int D, int HP>
 __global__ void __launch_bounds__(kNT, 1)
-attn_kernel(AttnParams p) {
+attn_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap gmap,
+            AttnParams p) {
     using C = Cfg<D, HP>;
-    constexpr int ROWB = C::ROWB, CPR = D / 8;            // 16-byte chunks per row
-    extern __shared__ __align__(128) uint8_t sm[];
+    constexpr int CPR = D / 8;                             // 16-byte chunks per row
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* sm = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     uint8_t* sQ = sm;
     uint8_t* sKV = sm + C::OFF_KV;
     uint8_t* sP = sm + C::OFF_P;
@@ -118,13 +186,17 @@ attn_kernel(AttnParams p) {
     float* m_run = red_sum + C::NRG * HP;
     float* l_run = m_run + HP;
     float* alpha_s = l_run + HP;
-    const __nv_bfloat16** rowsrc = reinterpret_cast<const __nv_bfloat16**>(sm + C::OFF_SRC);
+    int* okf = reinterpret_cast<int*>(sm + C::OFF_I);        // [2][kCH] row is valid
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);   // q, kv0, kv1
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, tq = lane & 3;
-    const int row = blockIdx.y, split = blockIdx.x;
+    const int row = blockIdx.y, split = blockIdx.x, hgrp = blockIdx.z;
+    const int hbase = hgrp * HP;                           // first head of this CTA
+    const int Hc = p.H - hbase < HP ? p.H - hbase : HP;    // heads handled here
     const int b = row / p.n_q, t = row - b * p.n_q;
-    const int nv = row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, row, p.eword);
+    const int nv = row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, row,
+                               hgrp == 0 && split == 0 ? p.eword : nullptr);
     int wl = p.win_len[b];
     wl = wl < 0 ? 0 : (wl > p.win_rows ? p.win_rows : wl);
     const int w_hi = t + wl - p.n_q;                       // the query's own window row
@@ -137,41 +209,58 @@ attn_kernel(AttnParams p) {
 
     pdl_trigger();
     if (tid < HP) { m_run[tid] = -INFINITY; l_run[tid] = 0.f; }
-    // Q (rows >= H are zero); the queries are inputs, so they load before the wait below
-    for (int i = tid; i < HP * CPR; i += kNT) {
-        const int h = i / CPR, c = i - h * CPR;
-        uint8_t* dst = sQ + swz<ROWB>(h, c);
-        if (h < p.H) cp_async16(dst, p.q + (static_cast<size_t>(row) * p.H + h) * D + c * 8);
-        else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+    // query rows past this CTA's heads stay zero (TMA writes only the first Hc rows of a box)
+    for (int i = tid; i < C::NBOX * (HP - Hc) * 8; i += kNT) {
+        const int box = i / ((HP - Hc) * 8), rem = i - box * (HP - Hc) * 8;
+        const int r = Hc + rem / 8, c = rem & 7;
+        *reinterpret_cast<uint4*>(sQ + box * HP * 128 + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
     }
-    auto resolve = [&](int chunk, int buf) {
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        mbar_init(&bars[2], 1);
+        fence_barrier_init();
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+    if (tid == 0) {                  // the queries are inputs: they load before the wait below
+        tma_prefetch_desc(&gmap);
+        mbar_arrive_expect_tx(&bars[0], static_cast<uint32_t>(Hc) * D * 2);
+        for (int box = 0; box < C::NBOX; ++box)
+            tma_load_2d(sQ + box * HP * 128, &qmap, &bars[0], box * 64, row * p.H + hbase);
+    }
+
+    // rows of chunk c into buffer buf: validity flags, then 64-row tile loads from the gather
+    // buffer (written by the gather kernel, so it is in L2)
+    auto issue = [&](int c, int buf) {
+        const bool comp = c < p.comp_chunks;
+        const int slot0 = comp ? c * kCH : kc + (c - p.comp_chunks) * kCH;
         if (tid < kCH) {
-            const int slot = chunk * kCH + tid;
-            const __nv_bfloat16* src = nullptr;
-            if (slot < kc) {
-                int e;
-                if (p.idx) {
-                    e = p.idx[static_cast<size_t>(row) * p.top_k + slot];
-                    if (e >= nv) { flag_error(p.eword, DSV4_EWORD_BAD_INDEX); e = -1; }
-                } else {
-                    e = slot < nv ? slot : -1;
+            int ok = 0;
+            if (comp) {
+                const int slot = slot0 + tid;
+                if (slot < kc) {
+                    if (p.idx) {
+                        const int e = p.idx[static_cast<size_t>(row) * p.top_k + slot];
+                        ok = e >= 0 && e < nv;
+                    } else {
+                        ok = slot < nv;
+                    }
                 }
-                if (e >= 0) src = p.comp_kv + (static_cast<size_t>(b) * p.max_comp + e) * D;
-            } else if (slot < p.slots) {
-                const int wi = slot - kc;
-                if (wi < w_cnt) src = p.win + (static_cast<size_t>(b) * p.win_rows + w_lo + wi) * D;
+            } else {
+                ok = (c - p.comp_chunks) * kCH + tid < w_cnt ? 1 : 0;
             }
-            rowsrc[buf * kCH + tid] = src;
+            okf[buf * kCH + tid] = ok;
         }
-    };
-    auto load = [&](int buf) {
-        uint8_t* dstb = sKV + static_cast<size_t>(buf) * kCH * ROWB;
-        for (int i = tid; i < kCH * CPR; i += kNT) {
-            const int r = i / CPR, c = i - r * CPR;
-            const __nv_bfloat16* src = rowsrc[buf * kCH + r];
-            uint8_t* dst = dstb + swz<ROWB>(r, c);
-            if (src) cp_async16(dst, src + c * 8);
-            else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+        __syncthreads();
+        if (tid == 0) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            uint64_t* bar = &bars[1 + buf];
+            mbar_arrive_expect_tx(bar, static_cast<uint32_t>(kCH) * D * 2);
+            uint8_t* dst = sKV + buf * C::KVBUF;
+            const int y = row * p.slots + slot0;
+            for (int box = 0; box < C::NBOX; ++box)
+                tma_load_2d(dst + box * kCH * 128, &gmap, bar, box * 64, y);
         }
     };
 
@@ -185,58 +274,45 @@ attn_kernel(AttnParams p) {
     for (int i = 0; i < C::DW / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
     pdl_wait();             // the index list (and the workspace) belong to the kernels before
-    if (c0 < c1) {
-        resolve(c0, 0);
-        __syncthreads();
-        load(0);
-    }
-    cp_async_commit();
+    bool dead = false;      // a bounded wait ran out: keep the barrier sequence, skip the math
+    if (!mbar_wait(&bars[0], 0, nullptr)) { flag_error(p.eword, DSV4_EWORD_TIMEOUT); dead = true; }
+    if (c0 < c1) issue(c0, 0);
+    uint32_t phase[2] = {0u, 0u};
     for (int c = c0; c < c1; ++c) {
         const int buf = (c - c0) & 1;
-        if (c + 1 < c1) {
-            resolve(c + 1, buf ^ 1);
-            __syncthreads();
-            load(buf ^ 1);
+        if (c + 1 < c1) issue(c + 1, buf ^ 1);
+        if (!dead && !mbar_wait(&bars[1 + buf], phase[buf], nullptr)) {
+            flag_error(p.eword, DSV4_EWORD_TIMEOUT);
+            dead = true;
         }
-        cp_async_commit();
-        cp_async_wait1();
-        __syncthreads();
-        const uint8_t* kvb = sKV + static_cast<size_t>(buf) * kCH * ROWB;
-        const __nv_bfloat16* const* src = rowsrc + buf * kCH;
-        // gather buffer: every slot of the chunk, zeros where masked
-        if (p.gather) {
-            for (int i = tid; i < kCH * CPR; i += kNT) {
-                const int r = i / CPR, cc = i - r * CPR;
-                const int slot = c * kCH + r;
-                if (slot >= p.slots) continue;
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (src[r]) v = *reinterpret_cast<const uint4*>(kvb + swz<ROWB>(r, cc));
-                *reinterpret_cast<uint4*>(p.gather + (static_cast<size_t>(row) * p.slots + slot) * D + cc * 8) = v;
-            }
-        }
+        phase[buf] ^= 1u;
+        const uint8_t* kvb = sKV + buf * C::KVBUF;
+        const int* ok = okf + buf * kCH;
         // ---- S = Q K^T for (16 heads) x (RW rows)
         float s[C::RW / 8][4];
 #pragma unroll
         for (int i = 0; i < C::RW / 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
         const uint32_t qa = smem_u32(sQ), kva = smem_u32(kvb);
+        if (!dead) {
 #pragma unroll 4
-        for (int k0 = 0; k0 < D; k0 += 16) {
-            uint32_t a[4];
-            ldsm_x4(qa + swz<ROWB>(hg * 16 + (lane & 15), (k0 >> 3) + (lane >> 4)), a);
-            if constexpr (C::RW >= 16) {
+            for (int k0 = 0; k0 < D; k0 += 16) {
+                uint32_t a[4];
+                ldsm_x4(qa + boxoff(hg * 16 + (lane & 15), (k0 >> 3) + (lane >> 4), HP), a);
+                if constexpr (C::RW >= 16) {
 #pragma unroll
-                for (int n2 = 0; n2 < C::RW / 16; ++n2) {
-                    uint32_t bb[4];
-                    const int rb = C::RW * rg + 16 * n2 + (lane & 7) + ((lane >> 4) << 3);
-                    ldsm_x4(kva + swz<ROWB>(rb, (k0 >> 3) + ((lane >> 3) & 1)), bb);
-                    mma_bf16(s[2 * n2], a, bb[0], bb[1]);
-                    mma_bf16(s[2 * n2 + 1], a, bb[2], bb[3]);
+                    for (int n2 = 0; n2 < C::RW / 16; ++n2) {
+                        uint32_t bb[4];
+                        const int rb = C::RW * rg + 16 * n2 + (lane & 7) + ((lane >> 4) << 3);
+                        ldsm_x4(kva + boxoff(rb, (k0 >> 3) + ((lane >> 3) & 1), kCH), bb);
+                        mma_bf16(s[2 * n2], a, bb[0], bb[1]);
+                        mma_bf16(s[2 * n2 + 1], a, bb[2], bb[3]);
+                    }
+                } else {
+                    uint32_t bb[2];
+                    const int rb = C::RW * rg + (lane & 7);
+                    ldsm_x2(kva + boxoff(rb, (k0 >> 3) + ((lane >> 3) & 1), kCH), bb);
+                    mma_bf16(s[0], a, bb[0], bb[1]);
                 }
-            } else {
-                uint32_t bb[2];
-                const int rb = C::RW * rg + (lane & 7);
-                ldsm_x2(kva + swz<ROWB>(rb, (k0 >> 3) + ((lane >> 3) & 1)), bb);
-                mma_bf16(s[0], a, bb[0], bb[1]);
             }
         }
         // ---- mask, scale, chunk max per head
@@ -244,7 +320,7 @@ attn_kernel(AttnParams p) {
 #pragma unroll
         for (int nt = 0; nt < C::RW / 8; ++nt) {
             const int col = C::RW * rg + 8 * nt + 2 * tq;
-            const bool v0 = src[col] != nullptr, v1 = src[col + 1] != nullptr;
+            const bool v0 = ok[col] && !dead, v1 = ok[col + 1] && !dead;
             s[nt][0] = v0 ? s[nt][0] * p.scale : -INFINITY;
             s[nt][1] = v1 ? s[nt][1] * p.scale : -INFINITY;
             s[nt][2] = v0 ? s[nt][2] * p.scale : -INFINITY;
@@ -275,8 +351,8 @@ attn_kernel(AttnParams p) {
             sum0 += p0 + p1;
             sum1 += p2 + p3;
             const int col = C::RW * rg + 8 * nt + 2 * tq;
-            *reinterpret_cast<uint32_t*>(sP + swz<128>(h0, col >> 3) + (col & 7) * 2) = pack_bf16(p0, p1);
-            *reinterpret_cast<uint32_t*>(sP + swz<128>(h1, col >> 3) + (col & 7) * 2) = pack_bf16(p2, p3);
+            *reinterpret_cast<uint32_t*>(sP + swz128(h0, col >> 3) + (col & 7) * 2) = pack_bf16(p0, p1);
+            *reinterpret_cast<uint32_t*>(sP + swz128(h1, col >> 3) + (col & 7) * 2) = pack_bf16(p2, p3);
         }
         sum0 += __shfl_xor_sync(0xffffffffu, sum0, 1);
         sum0 += __shfl_xor_sync(0xffffffffu, sum0, 2);
@@ -301,37 +377,37 @@ attn_kernel(AttnParams p) {
 #pragma unroll
             for (int i = 0; i < C::DW / 8; ++i) { o[i][0] *= al0; o[i][1] *= al0; o[i][2] *= al1; o[i][3] *= al1; }
             const uint32_t pa = smem_u32(sP);
+            if (!dead) {
 #pragma unroll
-            for (int kk = 0; kk < kCH / 16; ++kk) {
-                uint32_t a[4];
-                ldsm_x4(pa + swz<128>(hg * 16 + (lane & 15), 2 * kk + (lane >> 4)), a);
+                for (int kk = 0; kk < kCH / 16; ++kk) {
+                    uint32_t a[4];
+                    ldsm_x4(pa + swz128(hg * 16 + (lane & 15), 2 * kk + (lane >> 4)), a);
 #pragma unroll
-                for (int n2 = 0; n2 < C::DW / 16; ++n2) {
-                    const int d0 = C::DW * dg + 16 * n2;
-                    uint32_t bb[4];
-                    ldsm_x4_t(kva + swz<ROWB>(16 * kk + (lane & 7) + (((lane >> 3) & 1) << 3), (d0 >> 3) + (lane >> 4)), bb);
-                    mma_bf16(o[2 * n2], a, bb[0], bb[1]);
-                    mma_bf16(o[2 * n2 + 1], a, bb[2], bb[3]);
+                    for (int n2 = 0; n2 < C::DW / 16; ++n2) {
+                        const int d0 = C::DW * dg + 16 * n2;
+                        uint32_t bb[4];
+                        ldsm_x4_t(kva + boxoff(16 * kk + (lane & 7) + (((lane >> 3) & 1) << 3),
+                                               (d0 >> 3) + (lane >> 4), kCH), bb);
+                        mma_bf16(o[2 * n2], a, bb[0], bb[1]);
+                        mma_bf16(o[2 * n2 + 1], a, bb[2], bb[3]);
+                    }
                 }
             }
         }
         __syncthreads();
     }
-    cp_async_wait1();
-    asm volatile("cp.async.wait_all;" ::: "memory");
-    __syncthreads();
     if (p.n_splits == 1) {
         // finish here: sink once, normalise, bf16
         const float* sk = p.sink;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             const int h = half ? h1 : h0;
-            if (h >= p.H) continue;
-            const float m = m_run[h], l = l_run[h], snk = sk[h];
+            if (h >= Hc) continue;
+            const float m = m_run[h], l = l_run[h], snk = sk[hbase + h];
             const float M = fmaxf(m, snk);
             const float em = m == -INFINITY ? 0.f : expf(m - M);
             const float f = em / (l * em + expf(snk - M));
-            __nv_bfloat16* dst = p.out + (static_cast<size_t>(row) * p.H + h) * D;
+            __nv_bfloat16* dst = p.out + (static_cast<size_t>(row) * p.H + hbase + h) * D;
 #pragma unroll
             for (int i = 0; i < C::DW / 8; ++i) {
                 const int d = C::DW * dg + 8 * i + 2 * tq;
@@ -340,7 +416,7 @@ attn_kernel(AttnParams p) {
         }
     } else {
         const size_t part = static_cast<size_t>(row) * p.n_splits + split;
-        float* po = p.part_o + part * HP * D;
+        float* po = p.part_o + (part * p.hstride + hbase) * D;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             const int h = half ? h1 : h0;
@@ -352,8 +428,8 @@ attn_kernel(AttnParams p) {
             }
         }
         if (tid < HP) {
-            p.part_ml[(part * HP + tid) * 2 + 0] = m_run[tid];
-            p.part_ml[(part * HP + tid) * 2 + 1] = l_run[tid];
+            p.part_ml[(part * p.hstride + hbase + tid) * 2 + 0] = m_run[tid];
+            p.part_ml[(part * p.hstride + hbase + tid) * 2 + 1] = l_run[tid];
         }
     }
 }
@@ -367,12 +443,13 @@ attn_combine_kernel(AttnParams p) {
     const int row = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
     const int ns = p.n_splits;
     pdl_wait();
-    const float* ml = p.part_ml + static_cast<size_t>(row) * ns * HP * 2;
+    const int HS = p.hstride;
+    const float* ml = p.part_ml + static_cast<size_t>(row) * ns * HS * 2;
     const float snk = p.sink[h];
     // the splits' maxima and sums, in parallel (ns <= 256: two per thread)
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    if (tid < ns) { m0 = ml[(tid * HP + h) * 2]; l0 = ml[(tid * HP + h) * 2 + 1]; }
-    if (tid + 128 < ns) { m1 = ml[((tid + 128) * HP + h) * 2]; l1 = ml[((tid + 128) * HP + h) * 2 + 1]; }
+    if (tid < ns) { m0 = ml[(tid * HS + h) * 2]; l0 = ml[(tid * HS + h) * 2 + 1]; }
+    if (tid + 128 < ns) { m1 = ml[((tid + 128) * HS + h) * 2]; l1 = ml[((tid + 128) * HS + h) * 2 + 1]; }
     float M = fmaxf(m0, m1);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
@@ -392,12 +469,12 @@ attn_combine_kernel(AttnParams p) {
     if (tid == 0) bcast[0] = 1.0f / (red[0] + red[1] + red[2] + red[3] + expf(snk - M));
     __syncthreads();
     const float inv = bcast[0];
-    const float* po = p.part_o + static_cast<size_t>(row) * ns * HP * D + static_cast<size_t>(h) * D;
+    const float* po = p.part_o + static_cast<size_t>(row) * ns * HS * D + static_cast<size_t>(h) * D;
     for (int d = tid * 2; d < D; d += 256) {
         float a0 = 0.f, a1 = 0.f;
 #pragma unroll 8
         for (int s = 0; s < ns; ++s) {
-            const float2 v = *reinterpret_cast<const float2*>(po + static_cast<size_t>(s) * HP * D + d);
+            const float2 v = *reinterpret_cast<const float2*>(po + static_cast<size_t>(s) * HS * D + d);
             a0 = fmaf(v.x, wgt[s], a0);
             a1 = fmaf(v.y, wgt[s], a1);
         }
@@ -406,16 +483,19 @@ attn_combine_kernel(AttnParams p) {
     }
 }
 
-struct Plan { int slots, n_chunks, chunks_per_split, n_splits, hp; };
+struct Plan { int slots, comp_chunks, n_chunks, chunks_per_split, n_splits, hp, n_hg; };
 
 Plan make_plan(const dsv4_attn_args& a) {
     Plan pl;
     const int rows = a.batch * a.n_q;
     pl.slots = a.top_k + a.window;
-    pl.n_chunks = (pl.slots + kCH - 1) / kCH;
-    pl.hp = a.heads <= 16 ? 16 : (a.heads <= 32 ? 32 : 64);
+    pl.comp_chunks = (a.top_k + kCH - 1) / kCH;
+    pl.n_chunks = pl.comp_chunks + (a.window + kCH - 1) / kCH;
+    pl.hp = 16;                                   // heads per CTA
+    pl.n_hg = (a.heads + pl.hp - 1) / pl.hp;
     const int sms = sm_count() > 0 ? sm_count() : 148;
-    int want = rows > 0 ? (sms + rows - 1) / rows : 1;
+    const int units = rows * pl.n_hg;
+    int want = units > 0 ? (sms + units - 1) / units : 1;
     if (want < 1) want = 1;
     if (want > pl.n_chunks) want = pl.n_chunks;
     if (want > 256) want = 256;
@@ -427,19 +507,27 @@ Plan make_plan(const dsv4_attn_args& a) {
 template <int D, int HP>
 int run(const dsv4_attn_args& a, const Plan& pl, uint8_t* ws, uint32_t* eword, cudaStream_t st) {
     using C = Cfg<D, HP>;
+    const int rows = a.batch * a.n_q;
+    // the gather buffer: the caller's, else a workspace region after the partials
+    const size_t hs = static_cast<size_t>(pl.n_hg) * HP;
+    const size_t ml_b = align_up(static_cast<size_t>(rows) * pl.n_splits * hs * 2 * 4, 256);
+    const size_t po_b = pl.n_splits > 1 ? align_up(static_cast<size_t>(rows) * pl.n_splits * hs * D * 4, 256) : 0;
+    __nv_bfloat16* gbuf = a.gather ? static_cast<__nv_bfloat16*>(a.gather)
+                                   : reinterpret_cast<__nv_bfloat16*>(ws + ml_b + po_b);
+    CUtensorMap qmap, gmap;
+    if (!encode_2d_bf16(&qmap, a.q, D, static_cast<uint64_t>(rows) * a.heads, 64,
+                        a.heads < HP ? a.heads : HP) ||
+        !encode_2d_bf16(&gmap, gbuf, D, static_cast<uint64_t>(rows) * pl.slots, 64, kCH))
+        return DSV4_ERR_LAUNCH;
     AttnParams p;
-    p.q = static_cast<const __nv_bfloat16*>(a.q);
     p.sink = a.sink;
-    p.comp_kv = static_cast<const __nv_bfloat16*>(a.comp_kv);
     p.n_comp = a.n_comp;
     p.idx = a.idx;
     p.q_pos = a.q_pos;
-    p.win = static_cast<const __nv_bfloat16*>(a.win);
     p.win_len = a.win_len;
-    p.gather = static_cast<__nv_bfloat16*>(a.gather);
     p.out = static_cast<__nv_bfloat16*>(a.out);
     p.eword = eword;
-    p.rows = a.batch * a.n_q;
+    p.rows = rows;
     p.n_q = a.n_q;
     p.H = a.heads;
     p.max_comp = a.max_comp;
@@ -448,25 +536,35 @@ int run(const dsv4_attn_args& a, const Plan& pl, uint8_t* ws, uint32_t* eword, c
     p.win_rows = a.win_rows;
     p.ratio = a.ratio;
     p.slots = pl.slots;
+    p.comp_chunks = pl.comp_chunks;
     p.n_chunks = pl.n_chunks;
     p.chunks_per_split = pl.chunks_per_split;
     p.n_splits = pl.n_splits;
+    p.oob_row = a.batch * a.max_comp;          // first row past the cache: reads as zeros
+    p.n_hg = pl.n_hg;
+    p.hstride = pl.n_hg * HP;
     p.scale = a.scale;
-    const size_t ml_bytes = align_up(static_cast<size_t>(p.rows) * pl.n_splits * HP * 2 * 4, 256);
     p.part_ml = reinterpret_cast<float*>(ws);
-    p.part_o = reinterpret_cast<float*>(ws + ml_bytes);
+    p.part_o = reinterpret_cast<float*>(ws + ml_b);
     static bool attr_set = false;
     if (!attr_set) {
         cudaFuncSetAttribute(attn_kernel<D, HP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(C::SMEM));
         attr_set = true;
     }
-    dim3 grid(pl.n_splits, p.rows);
+    const long long grows = static_cast<long long>(rows) * pl.slots;
+    const long long gblocks = (grows + 8 * kRowsPerWarp - 1) / (8 * kRowsPerWarp);
     count_launch();
-    if (launch_k(attn_kernel<D, HP>, grid, dim3(kNT), C::SMEM, st, true, p) != cudaSuccess)
+    if (launch_k(gather_kernel<D>, dim3(static_cast<unsigned>(gblocks)), dim3(256), 0, st, true, p,
+                 static_cast<const __nv_bfloat16*>(a.comp_kv), static_cast<const __nv_bfloat16*>(a.win),
+                 gbuf) != cudaSuccess)
+        return DSV4_ERR_LAUNCH;
+    dim3 grid(pl.n_splits, rows, pl.n_hg);
+    count_launch();
+    if (launch_k(attn_kernel<D, HP>, grid, dim3(kNT), C::SMEM, st, true, qmap, gmap, p) != cudaSuccess)
         return DSV4_ERR_LAUNCH;
     if (pl.n_splits > 1) {
-        dim3 g2(p.rows, a.heads);
+        dim3 g2(rows, a.heads);
         count_launch();
         if (launch_k(attn_combine_kernel<D, HP>, g2, dim3(128), 0, st, true, p) != cudaSuccess)
             return DSV4_ERR_LAUNCH;
@@ -478,30 +576,20 @@ int run(const dsv4_attn_args& a, const Plan& pl, uint8_t* ws, uint32_t* eword, c
 
 size_t attn_ws_bytes(const dsv4_attn_args& a) {
     const Plan pl = make_plan(a);
-    if (pl.n_splits <= 1) return 0;
     const size_t rows = static_cast<size_t>(a.batch) * a.n_q;
-    return align_up(rows * pl.n_splits * pl.hp * 2 * 4, 256) +
-           align_up(rows * pl.n_splits * pl.hp * static_cast<size_t>(a.dim) * 4, 256);
+    const size_t hs = static_cast<size_t>(pl.n_hg) * pl.hp;
+    size_t b = align_up(rows * pl.n_splits * hs * 2 * 4, 256);
+    if (pl.n_splits > 1) b += align_up(rows * pl.n_splits * hs * static_cast<size_t>(a.dim) * 4, 256);
+    if (!a.gather) b += align_up(rows * pl.slots * static_cast<size_t>(a.dim) * 2, 256);
+    return b;
 }
 
 int launch_attn(const dsv4_attn_args& a, uint8_t* ws, uint32_t* eword, cudaStream_t st) {
     if (a.batch * a.n_q == 0) return DSV4_OK;
     const Plan pl = make_plan(a);
-    if (a.dim == 512) {
-        if (pl.hp == 16) return run<512, 16>(a, pl, ws, eword, st);
-        if (pl.hp == 32) return run<512, 32>(a, pl, ws, eword, st);
-        return run<512, 64>(a, pl, ws, eword, st);
-    }
-    if (a.dim == 256) {
-        if (pl.hp == 16) return run<256, 16>(a, pl, ws, eword, st);
-        if (pl.hp == 32) return run<256, 32>(a, pl, ws, eword, st);
-        return run<256, 64>(a, pl, ws, eword, st);
-    }
-    if (a.dim == 128) {
-        if (pl.hp == 16) return run<128, 16>(a, pl, ws, eword, st);
-        if (pl.hp == 32) return run<128, 32>(a, pl, ws, eword, st);
-        return run<128, 64>(a, pl, ws, eword, st);
-    }
+    if (a.dim == 512) return run<512, 16>(a, pl, ws, eword, st);
+    if (a.dim == 256) return run<256, 16>(a, pl, ws, eword, st);
+    if (a.dim == 128) return run<128, 16>(a, pl, ws, eword, st);
     return DSV4_ERR_INVALID_ARG;
 }
 

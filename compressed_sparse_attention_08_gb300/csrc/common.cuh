@@ -228,9 +228,15 @@ namespace dsv4 {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" :::); }
 
+// Every kernel of the library asks for the largest shared-memory carveout. Kernels that
+// overlap under programmatic dependent launch can then share an SM: a small kernel left with
+// a smaller carveout would keep the next big kernel's CTA off its SM until it drained.
+void prefer_max_shared(const void* kernel);
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                      cudaStream_t stream, bool pdl, Args... args) {
+    prefer_max_shared(reinterpret_cast<const void*>(kernel));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;

@@ -46,20 +46,42 @@ struct CompressJob {
     double freq[kMaxPairs];
 };
 
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 1)
 compress_kernel(const __grid_constant__ CompressJob j0, const __grid_constant__ CompressJob j1) {
     pdl_trigger();
-    const CompressJob& j = blockIdx.z == 0 ? j0 : j1;
+    // every field of the selected job once, into registers (a runtime choice between two
+    // parameter structs would otherwise turn each use into a slow generic load)
+    const bool second = blockIdx.z != 0;
+    const __nv_bfloat16* __restrict__ Cp = second ? j1.C : j0.C;
+    const __nv_bfloat16* __restrict__ Zp = second ? j1.Z : j0.Z;
+    const float* __restrict__ biasp = second ? j1.bias : j0.bias;
+    const float* __restrict__ gammap = second ? j1.gamma : j0.gamma;
+    const int64_t* pos0p = second ? j1.pos0 : j0.pos0;
+    __nv_bfloat16* outp = second ? j1.out : j0.out;
+    const int32_t* row0p = second ? j1.out_row0 : j0.out_row0;
+    const int batch = second ? j1.batch : j0.batch;
+    const int tokens = second ? j1.tokens : j0.tokens;
+    const int dim = second ? j1.dim : j0.dim;
+    const int ratio = second ? j1.ratio : j0.ratio;
+    const int rope_dim = second ? j1.rope_dim : j0.rope_dim;
+    const int out_rows = second ? j1.out_rows : j0.out_rows;
+    const int n_blocks = second ? j1.n_blocks : j0.n_blocks;
+    const float eps = second ? j1.eps : j0.eps;
+    const double two_pi_hi = j0.two_pi_hi, two_pi_lo = j0.two_pi_lo, inv_two_pi = j0.inv_two_pi;
     const int b = blockIdx.x;          // block (entry) within the sequence
     const int s = blockIdx.y;          // sequence
     const int tid = threadIdx.x;
-    if (b >= j.n_blocks || s >= j.batch) return;
-    const int dim = j.dim, ratio = j.ratio;
+    if (b >= n_blocks || s >= batch) return;
 
     __shared__ float y[1024];
     __shared__ float warp_sum[kThreads / 32];
+    __shared__ double freq[kMaxPairs];
+    if (tid < kMaxPairs) freq[tid] = second ? j1.freq[tid] : j0.freq[tid];
+    // loads that do not depend on the reduction, issued early
+    const int64_t pos_s = pos0p[s];
+    const int row_base = row0p ? row0p[s] : 0;
 
-    const size_t tok0 = static_cast<size_t>(s) * j.tokens + static_cast<size_t>(b) * ratio;
+    const size_t tok0 = static_cast<size_t>(s) * tokens + static_cast<size_t>(b) * ratio;
     float x[kMaxChan];
     float sq = 0.f;
 #pragma unroll
@@ -74,8 +96,8 @@ compress_kernel(const __grid_constant__ CompressJob j0, const __grid_constant__ 
             for (int u = 0; u < 8; ++u) {
                 const int t = t0 + u;
                 if (t < ratio) {
-                    a[u] = __bfloat162float(j.Z[(tok0 + t) * dim + c]) + j.bias[static_cast<size_t>(t) * dim + c];
-                    cv[u] = __bfloat162float(j.C[(tok0 + t) * dim + c]);
+                    a[u] = __bfloat162float(Zp[(tok0 + t) * dim + c]) + biasp[static_cast<size_t>(t) * dim + c];
+                    cv[u] = __bfloat162float(Cp[(tok0 + t) * dim + c]);
                 } else {
                     a[u] = -INFINITY;
                     cv[u] = 0.f;
@@ -107,21 +129,21 @@ compress_kernel(const __grid_constant__ CompressJob j0, const __grid_constant__ 
     float tot = 0.f;
 #pragma unroll
     for (int w = 0; w < kThreads / 32; ++w) tot += warp_sum[w];
-    const float inv = 1.0f / sqrtf(tot / static_cast<float>(dim) + j.eps);
+    const float inv = 1.0f / sqrtf(tot / static_cast<float>(dim) + eps);
 #pragma unroll
     for (int i = 0; i < kMaxChan; ++i) {
         const int c = tid + i * kThreads;
-        if (c < dim) y[c] = x[i] * inv * j.gamma[c];
+        if (c < dim) y[c] = x[i] * inv * gammap[c];
     }
     __syncthreads();
     // RoPE: pair p rotates channels (d0, d0 + 1), d0 = dim - rope_dim + 2p, by pos * f_p
-    const double pos = static_cast<double>(j.pos0[s] + static_cast<int64_t>(b) * ratio);
-    for (int p = tid; p < j.rope_dim / 2; p += kThreads) {
-        const int d0 = dim - j.rope_dim + 2 * p;
-        const double ang = pos * j.freq[p];
-        const double kq = rint(ang * j.inv_two_pi);
-        double r = fma(-kq, j.two_pi_hi, ang);
-        r = fma(-kq, j.two_pi_lo, r);
+    const double pos = static_cast<double>(pos_s + static_cast<int64_t>(b) * ratio);
+    for (int p = tid; p < rope_dim / 2; p += kThreads) {
+        const int d0 = dim - rope_dim + 2 * p;
+        const double ang = pos * freq[p];
+        const double kq = rint(ang * inv_two_pi);
+        double r = fma(-kq, two_pi_hi, ang);
+        r = fma(-kq, two_pi_lo, r);
         float sn, cs;
         sincosf(static_cast<float>(r), &sn, &cs);
         const float e = y[d0], o = y[d0 + 1];
@@ -129,9 +151,9 @@ compress_kernel(const __grid_constant__ CompressJob j0, const __grid_constant__ 
         y[d0 + 1] = e * sn + o * cs;
     }
     __syncthreads();
-    const int row = (j.out_row0 ? j.out_row0[s] : 0) + b;
-    if (row < 0 || row >= j.out_rows) return;   // rows outside the destination are not written
-    __nv_bfloat16* dst = j.out + (static_cast<size_t>(s) * j.out_rows + row) * dim;
+    const int row = row_base + b;
+    if (row < 0 || row >= out_rows) return;     // rows outside the destination are not written
+    __nv_bfloat16* dst = outp + (static_cast<size_t>(s) * out_rows + row) * dim;
     for (int c = tid; c < dim; c += kThreads) dst[c] = __float2bfloat16_rn(y[c]);
 }
 
@@ -173,9 +195,9 @@ int launch_compress2(const dsv4_compress_args* a, const dsv4_compress_args* b, c
     const int bs = j0.batch > j1.batch ? j0.batch : j1.batch;
     if (nb == 0 || bs == 0) return DSV4_OK;
     dim3 grid(nb, bs, b ? 2 : 1);
-    compress_kernel<<<grid, kThreads, 0, stream>>>(j0, j1);
     count_launch();
-    return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_LAUNCH;
+    return launch_k(compress_kernel, grid, dim3(kThreads), 0, stream, false, j0, j1) == cudaSuccess
+               ? DSV4_OK : DSV4_ERR_LAUNCH;
 }
 
 int launch_compress(const dsv4_compress_args& a, cudaStream_t stream) {

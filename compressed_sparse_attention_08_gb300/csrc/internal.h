@@ -2,6 +2,7 @@
 // host (abi.cu); workspaces are sized by the matching *_ws_bytes function.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
@@ -45,6 +46,11 @@ int launch_indexer(const dsv4_index_args& a, uint8_t* ws, uint32_t* eword, cudaS
                    const dsv4_compress_args* fresh_keys = nullptr);
 // Scores only (a.scores_out required); no top-k.
 int launch_index_score(const dsv4_index_args& a, uint32_t* eword, cudaStream_t stream);
+
+// 2D bf16 tensor map, row-major [rows, inner] (inner contiguous), 128-byte swizzle, boxes of
+// box_inner x box_rows elements; out-of-range boxes read as zeros. Host only, no allocation.
+bool encode_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                    uint32_t box_inner, uint32_t box_rows);
 
 size_t attn_ws_bytes(const dsv4_attn_args& a);
 int launch_attn(const dsv4_attn_args& a, uint8_t* ws, uint32_t* eword, cudaStream_t stream);

@@ -190,6 +190,7 @@ typedef struct dsv4_attn_args {
     void* gather;             /* bf16 [batch, n_q, top_k + window, dim], or NULL            */
     void* out;                /* bf16 [batch, n_q, heads, dim]                              */
     int batch, n_q, heads, dim, max_comp, top_k, window, win_rows, ratio;
+                              /* heads: 1..16, or a multiple of 16 up to 64; dim: 128/256/512 */
     float scale;              /* 1/sqrt(dim) on the pages                                   */
 } dsv4_attn_args;
 
