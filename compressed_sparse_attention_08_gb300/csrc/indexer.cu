@@ -120,6 +120,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
             bool waited = false;
             long long issued = 0;
             uint32_t phase = 0;
+            const uint64_t stream_policy = l2_evict_first_policy();   // keys are read once
             for (long long t = wr.begin; t < wr.end; ++t) {
                 const int row = static_cast<int>(t / p.tiles_per_row);
                 const int tile = static_cast<int>(t % p.tiles_per_row);
@@ -151,8 +152,9 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                 {
                     uint8_t* kd = key_buf + stage * kKeyTileBytes;
                     const int b = row / p.n_q;
-                    tma_load_3d(kd, &kmap, &full_bar[stage], 0, tile * kTileKeys, b);
-                    tma_load_3d(kd + kKeyHalfBytes, &kmap, &full_bar[stage], 64, tile * kTileKeys, b);
+                    tma_load_3d_hint(kd, &kmap, &full_bar[stage], 0, tile * kTileKeys, b, stream_policy);
+                    tma_load_3d_hint(kd + kKeyHalfBytes, &kmap, &full_bar[stage], 64, tile * kTileKeys, b,
+                                     stream_policy);
                     ++issued;
                 }
                 if (++stage == kStages) { stage = 0; phase ^= 1; }

@@ -19,8 +19,10 @@
 //     histogram of the top 12 key bits per row (built by the scoring kernel's epilogue when
 //     the scores come from the indexer, else by a histogram kernel) gives the 12-bit bin
 //     that holds the k-th key; every CTA keeps, in index order, the elements of its slice at
-//     or above that bin (a few thousand of 262,144 in all); the last CTA of the row to
-//     finish (atomic ticket, no spinning) selects exactly within that short list.
+//     or above that bin (a few thousand of 262,144 in all) and counts bits 19..8 of the keys
+//     in that bin into a second histogram; the last CTA of the row to finish (atomic ticket,
+//     no spinning) reads the second histogram, so one 8-bit radix pass over the short list
+//     gives the exact k-th key.
 #include "common.cuh"
 #include "internal.h"
 
@@ -188,7 +190,8 @@ topk_small_kernel(TopkRows t, uint32_t* eword) {
 
 // ------------------------------------------------------------------ long rows
 struct LongWs {
-    uint32_t* hist;     // [rows, kBins]
+    uint32_t* hist;     // [rows, kBins]: top 12 key bits (bits 31..20) of every visible key
+    uint32_t* hist2;    // [rows, kBins]: bits 19..8 of the keys in the threshold bin
     uint32_t* done;     // [rows] tickets
     int32_t* counts;    // [rows, kMaxSlices]
     uint2* pairs;       // [rows, max_comp]: (key, index) survivors, slice p at p * L
@@ -197,6 +200,43 @@ struct LongWs {
 __device__ __forceinline__ void slice_range(int n, int L, int p, int& lo, int& hi) {
     lo = p * L < n ? p * L : n;
     hi = lo + L < n ? lo + L : n;
+}
+
+// The bin of a kBins-bin histogram that holds the k-th largest key (1 <= k <= total count),
+// counting from the top bin down, and how many keys lie in the bins above it: bc[0] = bin,
+// bc[1] = count above. Thread t passes in c[i] the count of bin kBins-1-(t*per+i). Every
+// thread of the CTA calls it.
+template <int NT>
+__device__ __forceinline__ void find_bin(const int (&c)[kBins / NT], int k, int* s_a, int* bc) {
+    constexpr int NW = NT / 32, per = kBins / NT;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int s = 0;
+#pragma unroll
+    for (int i = 0; i < per; ++i) s += c[i];
+    int inc = warp_incl(s);
+    if (lane == 31) s_a[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        const int v = lane < NW ? s_a[lane] : 0;
+        const int vi = warp_incl(v);
+        if (lane < NW) s_a[lane] = vi - v;
+    }
+    __syncthreads();
+    inc += s_a[warp];
+    const int before = inc - s;
+    if (before < k && inc >= k) {
+        int acc = before;
+#pragma unroll
+        for (int i = 0; i < per; ++i) {
+            if (acc + c[i] >= k) {
+                bc[0] = kBins - 1 - (static_cast<int>(threadIdx.x) * per + i);
+                bc[1] = acc;
+                break;
+            }
+            acc += c[i];
+        }
+    }
+    __syncthreads();
 }
 
 template <int NT>
@@ -221,10 +261,17 @@ topk_hist_kernel(TopkRows t, LongWs w, int L, uint32_t* eword) {
         if (h[i]) atomicAdd(&g[i], h[i]);
 }
 
+// Long rows, P CTAs per row. Each CTA: the 12-bit threshold bin tb from the row histogram;
+// the survivors of its slice (key bin >= tb) in index order into its segment of the pair
+// list; bits 19..8 of the keys in bin tb into the row's second histogram. The last CTA of
+// the row (atomic ticket, no spinning) finds the second-level bin from that histogram, so one
+// 8-bit radix pass over the survivors gives the exact k-th key, and writes the k indices.
 template <int NT>
 __global__ void __launch_bounds__(NT, 1)
 topk_filter_kernel(TopkRows t, LongWs w, int L, int P, uint32_t* eword) {
     constexpr int NW = NT / 32;
+    constexpr int kRegs = 8;                     // scores per lane kept in registers
+    constexpr int per_bin = kBins / NT;
     extern __shared__ uint2 spairs[];           // kFinalCap pairs (finalizer only)
     __shared__ uint32_t hist[256];
     __shared__ int s_a[32], s_b[32];
@@ -235,105 +282,93 @@ topk_filter_kernel(TopkRows t, LongWs w, int L, int P, uint32_t* eword) {
     pdl_wait();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int row = blockIdx.x, p = blockIdx.y;
-    const int n = row_visible(t.n_vis, t.n_comp, t.q_pos, t.n_q, t.ratio, t.max_comp, row, eword);
     const int k = t.top_k;
+    // The row histogram, this slice's scores and the visible count do not depend on one
+    // another: issue their loads together. The slice is read over its full extent (inside
+    // the row's max_comp scores); entries at or past the visible count are masked below.
+    const uint32_t* g1 = w.hist + static_cast<size_t>(row) * kBins;
+    int c[per_bin];
+#pragma unroll
+    for (int i = 0; i < per_bin; ++i)
+        c[i] = static_cast<int>(__ldcg(&g1[kBins - 1 - (static_cast<int>(threadIdx.x) * per_bin + i)]));
+    const int slo = p * L;                       // < max_comp: P = ceil(max_comp / L)
+    const int shi = slo + L < t.max_comp ? slo + L : t.max_comp;
+    const int wper = (shi - slo + NW - 1) / NW;  // warp-contiguous runs of the slice
+    const int wlo = slo + (warp * wper < shi - slo ? warp * wper : shi - slo);
+    const int whi = wlo + wper < shi ? wlo + wper : shi;
+    const bool in_regs = wper <= 32 * kRegs;     // the same for every warp of the CTA
+    const float* sc = t.scores + static_cast<size_t>(row) * t.max_comp;
+    float v0[kRegs];
+    if (in_regs) {
+#pragma unroll
+        for (int r = 0; r < kRegs; ++r) {
+            const int i = wlo + r * 32 + lane;
+            v0[r] = i < whi ? __ldcg(&sc[i]) : 0.f;
+        }
+    }
+    const int n = row_visible(t.n_vis, t.n_comp, t.q_pos, t.n_q, t.ratio, t.max_comp, row, eword);
     int32_t* out = t.idx_out + static_cast<size_t>(row) * k;
     if (n <= k) {                                // every visible entry is selected
         const int per = (k + P - 1) / P;
         write_all(out, n, k, p * per + threadIdx.x, (p + 1) * per, NT);
         return;
     }
+    const int hi = whi < n ? whi : n;            // visible end of this warp's run
     // 1. the 12-bit bin tb holding the k-th largest key, and how many keys lie above it
-    {
-        constexpr int per = kBins / NT;          // bins per thread, from the top down
-        const uint32_t* g = w.hist + static_cast<size_t>(row) * kBins;
-        int c[per], s = 0;
-#pragma unroll
-        for (int i = 0; i < per; ++i) { c[i] = static_cast<int>(__ldcg(&g[kBins - 1 - (threadIdx.x * per + i)])); s += c[i]; }
-        int inc = warp_incl(s);
-        if (lane == 31) s_a[warp] = inc;
-        __syncthreads();
-        if (warp == 0) {
-            const int v = lane < NW ? s_a[lane] : 0;
-            const int vi = warp_incl(v);
-            if (lane < NW) s_a[lane] = vi - v;
-        }
-        __syncthreads();
-        inc += s_a[warp];
-        const int before = inc - s;
-        if (before < k && inc >= k) {
-            int acc = before;
-#pragma unroll
-            for (int i = 0; i < per; ++i) {
-                if (acc + c[i] >= k) {
-                    bc[0] = kBins - 1 - (threadIdx.x * per + i);
-                    bc[1] = acc;                    // keys in bins above tb
-                    break;
-                }
-                acc += c[i];
-            }
-        }
-        __syncthreads();
-    }
+    find_bin<NT>(c, k, s_a, bc);
     const uint32_t tb = static_cast<uint32_t>(bc[0]);
     const int above = bc[1];
-    // 2. survivors of this slice (bin >= tb), in index order, warp-contiguous runs; each
-    //    lane holds up to kRegs keys of its warp's run in registers (one round trip)
-    int lo, hi;
-    slice_range(n, L, p, lo, hi);
-    const float* sc = t.scores + static_cast<size_t>(row) * t.max_comp;
-    uint2* seg = w.pairs + static_cast<size_t>(row) * t.max_comp + static_cast<size_t>(p) * L;
-    {
-        constexpr int kRegs = 8;
-        const int len = hi - lo;
-        const int per = (len + NW - 1) / NW;
-        const int wlo = lo + (warp * per < len ? warp * per : len);
-        const int whi = wlo + per < hi ? wlo + per : hi;
-        const unsigned lt = (1u << lane) - 1u;
-        int cnt = 0;
-        for (int b0 = wlo; b0 < whi; b0 += 32 * kRegs) {
-            uint32_t key[kRegs];
+    // 2. count this warp's survivors (bin >= tb); keys in bin tb also go into the second
+    //    histogram
+    uint32_t* g2 = w.hist2 + static_cast<size_t>(row) * kBins;
+    uint2* seg = w.pairs + static_cast<size_t>(row) * t.max_comp + static_cast<size_t>(slo);
+    const unsigned lt = (1u << lane) - 1u;
+    int cnt = 0;
+    for (int b0 = wlo; b0 < whi; b0 += 32 * kRegs) {
+        uint32_t key[kRegs];
 #pragma unroll
-            for (int r = 0; r < kRegs; ++r) {
-                const int i = b0 + r * 32 + lane;
-                key[r] = i < whi ? float_to_key(__ldcg(&sc[i])) : 0u;
-            }
-#pragma unroll
-            for (int r = 0; r < kRegs; ++r) {
-                const int i = b0 + r * 32 + lane;
-                cnt += __popc(__ballot_sync(0xffffffffu, i < whi && (key[r] >> kBinShift) >= tb));
-            }
+        for (int r = 0; r < kRegs; ++r) {
+            const int i = b0 + r * 32 + lane;
+            key[r] = float_to_key(in_regs ? v0[r] : (i < hi ? __ldcg(&sc[i]) : 0.f));
         }
-        __syncthreads();                         // s_a is reused
-        if (lane == 0) s_a[warp] = cnt;
-        __syncthreads();
-        if (warp == 0) {
-            const int v = lane < NW ? s_a[lane] : 0;
-            const int vi = warp_incl(v);
-            if (lane < NW) s_a[lane] = vi - v;
-            if (lane == NW - 1) s_b[0] = vi;
-        }
-        __syncthreads();
-        int pos = s_a[warp];
-        for (int b0 = wlo; b0 < whi; b0 += 32 * kRegs) {
-            uint32_t key[kRegs];
 #pragma unroll
-            for (int r = 0; r < kRegs; ++r) {
-                const int i = b0 + r * 32 + lane;
-                key[r] = i < whi ? float_to_key(__ldcg(&sc[i])) : 0u;
-            }
-#pragma unroll
-            for (int r = 0; r < kRegs; ++r) {
-                const int i = b0 + r * 32 + lane;
-                const bool keep = i < whi && (key[r] >> kBinShift) >= tb;
-                const unsigned bk = __ballot_sync(0xffffffffu, keep);
-                if (keep) seg[pos + __popc(bk & lt)] = make_uint2(key[r], static_cast<uint32_t>(i));
-                pos += __popc(bk);
-            }
+        for (int r = 0; r < kRegs; ++r) {
+            const int i = b0 + r * 32 + lane;
+            const bool vis = i < hi;
+            const uint32_t bin = key[r] >> kBinShift;
+            cnt += __popc(__ballot_sync(0xffffffffu, vis && bin >= tb));
+            if (vis && bin == tb) atomicAdd(&g2[(key[r] >> 8) & (kBins - 1)], 1u);
         }
-        if (threadIdx.x == 0) w.counts[static_cast<size_t>(row) * kMaxSlices + p] = s_b[0];
     }
-    // 3. the last CTA of the row to get here finishes the row (no waiting on anyone)
+    if (lane == 0) s_a[warp] = cnt;              // find_bin is done with s_a
+    __syncthreads();
+    if (warp == 0) {
+        const int v = lane < NW ? s_a[lane] : 0;
+        const int vi = warp_incl(v);
+        if (lane < NW) s_a[lane] = vi - v;
+        if (lane == NW - 1) s_b[0] = vi;
+    }
+    __syncthreads();
+    // 3. write them, in index order, at the warp's offset in the slice's segment
+    int pos = s_a[warp];
+    for (int b0 = wlo; b0 < whi; b0 += 32 * kRegs) {
+        uint32_t key[kRegs];
+#pragma unroll
+        for (int r = 0; r < kRegs; ++r) {
+            const int i = b0 + r * 32 + lane;
+            key[r] = float_to_key(in_regs ? v0[r] : (i < hi ? __ldcg(&sc[i]) : 0.f));
+        }
+#pragma unroll
+        for (int r = 0; r < kRegs; ++r) {
+            const int i = b0 + r * 32 + lane;
+            const bool keep = i < hi && (key[r] >> kBinShift) >= tb;
+            const unsigned bk = __ballot_sync(0xffffffffu, keep);
+            if (keep) seg[pos + __popc(bk & lt)] = make_uint2(key[r], static_cast<uint32_t>(i));
+            pos += __popc(bk);
+        }
+    }
+    if (threadIdx.x == 0) w.counts[static_cast<size_t>(row) * kMaxSlices + p] = s_b[0];
+    // 4. the last CTA of the row to get here finishes the row (no waiting on anyone)
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -343,16 +378,26 @@ topk_filter_kernel(TopkRows t, LongWs w, int L, int P, uint32_t* eword) {
     __syncthreads();
     if (!is_last) return;
     __threadfence();
+    // slice counts and the second histogram, loaded together
+    int cv = 0;
+    if (threadIdx.x < 64 && static_cast<int>(threadIdx.x) < P)
+        cv = __ldcg(&w.counts[static_cast<size_t>(row) * kMaxSlices + threadIdx.x]);
+    int c2[per_bin];
+#pragma unroll
+    for (int i = 0; i < per_bin; ++i)
+        c2[i] = static_cast<int>(__ldcg(&g2[kBins - 1 - (static_cast<int>(threadIdx.x) * per_bin + i)]));
     if (threadIdx.x < 64) {                      // exclusive scan of the P <= 64 slice counts
-        int v = threadIdx.x < P ? __ldcg(&w.counts[static_cast<size_t>(row) * kMaxSlices + threadIdx.x]) : 0;
-        v = warp_incl(v);
+        const int v = warp_incl(cv);
         if (threadIdx.x == 31) s_b[1] = v;
         offs[threadIdx.x + 1] = v;
         if (threadIdx.x == 0) offs[0] = 0;
     }
     __syncthreads();
     if (threadIdx.x >= 32 && threadIdx.x < 64) offs[threadIdx.x + 1] += s_b[1];
-    __syncthreads();
+    // the 12-bit sub-bin (bits 19..8) of bin tb holding the k-th key (its syncs publish offs)
+    find_bin<NT>(c2, k - above, s_a, bc);
+    const uint32_t prefix = (tb << kBinShift) | (static_cast<uint32_t>(bc[0]) << 8);
+    const int need = k - above - bc[1];
     const int total = offs[P];
     const uint2* rowpairs = w.pairs + static_cast<size_t>(row) * t.max_comp;
     auto slice_of = [&](int i) {                 // slice q with offs[q] <= i < offs[q + 1]
@@ -366,14 +411,25 @@ topk_filter_kernel(TopkRows t, LongWs w, int L, int P, uint32_t* eword) {
     uint32_t T;
     int need_T;
     if (total <= kFinalCap) {
-        for (int i = threadIdx.x; i < total; i += NT) {
-            const int q = slice_of(i);
-            spairs[i] = __ldcg(&rowpairs[static_cast<size_t>(q) * L + (i - offs[q])]);
+        constexpr int kB = 4;                    // loads in flight per thread
+        for (int i0 = threadIdx.x; i0 < total; i0 += NT * kB) {
+            uint2 v[kB];
+#pragma unroll
+            for (int j = 0; j < kB; ++j) {
+                const int i = i0 + j * NT;
+                if (i < total) {
+                    const int q = slice_of(i);
+                    v[j] = __ldcg(&rowpairs[static_cast<size_t>(q) * L + (i - offs[q])]);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kB; ++j)
+                if (i0 + j * NT < total) spairs[i0 + j * NT] = v[j];
         }
         __syncthreads();
         auto key_at = [&](int i) { return spairs[i].x; };
         auto idx_at = [&](int i) { return static_cast<int32_t>(spairs[i].y); };
-        radix_select<NT>(total, k - above, key_at, hist, bc, T, need_T, tb << kBinShift, 32 - kBinShift);
+        radix_select<NT>(total, need, key_at, hist, bc, T, need_T, prefix, 32 - 8);
         ordered_select<NT>(total, T, need_T, key_at, idx_at, out, s_a, s_b);
     } else {
         // degenerate score distributions (huge ties): the same steps on the slices in place
@@ -383,7 +439,7 @@ topk_filter_kernel(TopkRows t, LongWs w, int L, int P, uint32_t* eword) {
         };
         auto key_at = [&](int i) { return at(i).x; };
         auto idx_at = [&](int i) { return static_cast<int32_t>(at(i).y); };
-        radix_select<NT>(total, k - above, key_at, hist, bc, T, need_T, tb << kBinShift, 32 - kBinShift);
+        radix_select<NT>(total, need, key_at, hist, bc, T, need_T, prefix, 32 - 8);
         ordered_select<NT>(total, T, need_T, key_at, idx_at, out, s_a, s_b);
     }
 }
@@ -408,15 +464,15 @@ size_t topk_ws_bytes(int rows, int max_comp, int top_k) {
     (void)top_k;
     if (max_comp <= kSmallCap) return 0;
     size_t b = 0;
-    b += static_cast<size_t>(rows) * kBins * 4;           // histograms, then
-    b += align_up(static_cast<size_t>(rows) * 4, 256);    // tickets (one memset clears both)
+    b += static_cast<size_t>(rows) * kBins * 4 * 2;       // both histograms, then
+    b += align_up(static_cast<size_t>(rows) * 4, 256);    // tickets (one memset clears all three)
     b += align_up(static_cast<size_t>(rows) * kMaxSlices * 4, 256);
     b += align_up(static_cast<size_t>(rows) * max_comp * 8, 256);
     return b;
 }
 
 uint32_t* topk_hist_buffer(uint8_t* ws) { return reinterpret_cast<uint32_t*>(ws); }
-size_t topk_hist_bytes(int rows) { return static_cast<size_t>(rows) * (kBins + 1) * 4; }
+size_t topk_hist_bytes(int rows) { return static_cast<size_t>(rows) * (2 * kBins + 1) * 4; }
 bool topk_uses_hist(int max_comp) { return max_comp > kSmallCap; }
 
 int launch_topk(const TopkRows& t, uint8_t* ws, uint32_t* eword, cudaStream_t stream) {
@@ -437,6 +493,8 @@ int launch_topk(const TopkRows& t, uint8_t* ws, uint32_t* eword, cudaStream_t st
     LongWs w;
     uint8_t* p = ws;
     w.hist = reinterpret_cast<uint32_t*>(p);
+    p += static_cast<size_t>(t.rows) * kBins * 4;
+    w.hist2 = reinterpret_cast<uint32_t*>(p);
     p += static_cast<size_t>(t.rows) * kBins * 4;
     w.done = reinterpret_cast<uint32_t*>(p);
     p += align_up(static_cast<size_t>(t.rows) * 4, 256);
