@@ -483,6 +483,345 @@ attn_combine_kernel(AttnParams p) {
     }
 }
 
+// ------------------------------------------------------------------ decode: fused gather + tcgen05
+// One CTA per (128-slot chunk, query row, group of NH heads):
+//   * the chunk's rows are copied straight from the compressed cache (or the window) into a
+//     shared tile laid out as D/64 boxes of [128 rows][128 B] with the 128-byte swizzle, by
+//     16-byte cp.async pieces (8 warps x 16 rows; invalid slots are zero-filled). The head
+//     group 0 CTA then TMA-stores the tile into the caller's gather buffer;
+//   * S^T = KV Q^T on the tensor cores: M = 128 slots, N = NH heads, K = D, fp32 in TMEM;
+//   * the 128 x NH scores go through shared memory once, so each thread owns one head and
+//     16 slots: per-head max and sum over the chunk, P = e^(s - m) rounded to bf16 into a
+//     K-major operand tile [NH heads][128 slots];
+//   * O^T = V^T P^T: M = 128 dims per tile (D/128 tiles), N = NH, K = 128 slots. V^T is the
+//     same shared tile read as an MN-major operand (64 dims per 128-byte row, slot rows);
+//   * the chunk's (m, l, O) go to the partials; the combine kernel merges the chunks of a
+//     query and adds the sink once.
+constexpr int kFC = 128;          // slots per chunk (the MMA's M)
+constexpr int kFT = 256;          // 8 warps
+
+template <int D, int NH>
+struct FCfg {
+    static constexpr int NBOX = D / 64;
+    static constexpr int MT = D / 128;                               // M tiles of O^T
+    static constexpr int U = D / 8;                                  // 16-byte pieces per row
+    static constexpr size_t BOX = static_cast<size_t>(kFC) * 128;    // one 64-dim box of the tile
+    static constexpr size_t OFF_Q = BOX * NBOX;
+    static constexpr size_t OFF_P = OFF_Q + static_cast<size_t>(NBOX) * NH * 128;
+    static constexpr size_t OFF_S = OFF_P + 2ull * NH * 128;
+    static constexpr size_t OFF_R = OFF_S + static_cast<size_t>(kFC) * (NH + 1) * 4;
+    static constexpr size_t OFF_OK = OFF_R + 2ull * 8 * NH * 4;
+    static constexpr size_t OFF_BAR = align_up(OFF_OK + kFC * 4, 16);
+    static constexpr size_t SMEM = OFF_BAR + 3 * 8 + 1024;           // + alignment slack
+    static constexpr uint32_t NEED = static_cast<uint32_t>(NH + MT * NH);
+    static constexpr uint32_t TCOLS = NEED <= 32 ? 32 : NEED <= 64 ? 64 : NEED <= 128 ? 128 : NEED <= 256 ? 256 : 512;
+    static_assert(D % 128 == 0 && (NH == 16 || NH == 32), "decode tile shape");
+};
+
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[N]) {
+    if constexpr (N == 8) DSV4_TMEM_LD_32x32b_X8(taddr, r);
+    else if constexpr (N == 16) DSV4_TMEM_LD_32x32b_X16(taddr, r);
+    else DSV4_TMEM_LD_32x32b_X32(taddr, r);
+}
+
+template <int D, int NH>
+__global__ void __launch_bounds__(kFT, 1)
+attn_decode_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap gmap,
+                   AttnParams p, const __nv_bfloat16* __restrict__ comp_kv,
+                   const __nv_bfloat16* __restrict__ win, int write_gather) {
+    using C = FCfg<D, NH>;
+    constexpr int HC = NH / 2;                                       // TMEM columns per warp
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint32_t tmem_slot;
+    __shared__ volatile int abort_flag;
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* sm = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    uint8_t* sKV = sm;
+    uint8_t* sQ = sm + C::OFF_Q;
+    uint8_t* sP = sm + C::OFF_P;
+    float* sS = reinterpret_cast<float*>(sm + C::OFF_S);
+    float* red_m = reinterpret_cast<float*>(sm + C::OFF_R);
+    float* red_l = red_m + 8 * NH;
+    int* okf = reinterpret_cast<int*>(sm + C::OFF_OK);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);   // q loaded, S done, O done
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int chunk = blockIdx.x, row = blockIdx.y, hgrp = blockIdx.z;
+    const int hbase = hgrp * NH;
+    const int Hc = p.H - hbase < NH ? p.H - hbase : NH;
+    const int b = row / p.n_q, t = row - b * p.n_q;
+    pdl_trigger();
+    const int nv = row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, row,
+                               hgrp == 0 && chunk == 0 ? p.eword : nullptr);
+    int wl = p.win_len[b];
+    wl = wl < 0 ? 0 : (wl > p.win_rows ? p.win_rows : wl);
+    const int w_hi = t + wl - p.n_q;                                 // the query's own window row
+    const int w_lo = w_hi - p.window + 1 > 0 ? w_hi - p.window + 1 : 0;
+    const int w_top = w_hi < wl - 1 ? w_hi : wl - 1;
+    const int w_cnt = w_top >= w_lo ? w_top - w_lo + 1 : 0;
+
+    // query rows past this CTA's heads stay zero (TMA writes only the first Hc rows of a box)
+    for (int i = tid; i < C::NBOX * (NH - Hc) * 8; i += kFT) {
+        const int box = i / ((NH - Hc) * 8), rem = i - box * (NH - Hc) * 8;
+        *reinterpret_cast<uint4*>(sQ + box * NH * 128 + (Hc + rem / 8) * 128 + (rem & 7) * 16) =
+            make_uint4(0, 0, 0, 0);
+    }
+    if (tid == 0) {
+        for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0) tmem_alloc(&tmem_slot, C::TCOLS);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    if (tid == 0) {                  // the queries are inputs: they load before the wait below
+        tma_prefetch_desc(&gmap);
+        mbar_arrive_expect_tx(&bars[0], static_cast<uint32_t>(Hc) * D * 2);
+        for (int box = 0; box < C::NBOX; ++box)
+            tma_load_2d(sQ + box * NH * 128, &qmap, &bars[0], box * 64, row * p.H + hbase);
+    }
+
+    pdl_wait();                      // the index list comes from the kernel before
+    // ---- gather: warp w copies slots [16w, 16w + 16) of the chunk; lanes 0..15 resolve them
+    {
+        const int r0 = warp * 16;
+        unsigned long long src = 0;                                  // 0: zero row
+        if (lane < 16) {
+            const int slot = chunk * kFC + r0 + lane;
+            if (slot < p.top_k) {
+                int e;
+                if (p.idx) {
+                    e = p.idx[static_cast<size_t>(row) * p.top_k + slot];
+                    if (e >= nv) { flag_error(p.eword, DSV4_EWORD_BAD_INDEX); e = -1; }
+                } else {
+                    e = slot < nv ? slot : -1;
+                }
+                if (e >= 0)
+                    src = reinterpret_cast<unsigned long long>(comp_kv + (static_cast<size_t>(b) * p.max_comp + e) * D);
+            } else if (slot < p.slots) {
+                const int wi = slot - p.top_k;
+                if (wi < w_cnt)
+                    src = reinterpret_cast<unsigned long long>(win + (static_cast<size_t>(b) * p.win_rows + w_lo + wi) * D);
+            }
+            okf[r0 + lane] = src != 0;
+        }
+        for (int i = lane; i < 16 * C::U; i += 32) {
+            const int r = i / C::U, c = i - r * C::U;
+            const unsigned long long a = __shfl_sync(0xffffffffu, src, r);
+            const int rr = r0 + r;
+            uint8_t* dst = sKV + (c >> 3) * C::BOX + rr * 128 + (((c & 7) ^ (rr & 7)) << 4);
+            if (a) cp_async16(dst, reinterpret_cast<const uint8_t*>(a) + c * 16);
+            else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+        }
+    }
+    cp_async_wait_all();
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+    if (tid == 0) {
+        if (write_gather && hgrp == 0) {                             // the gather buffer's rows
+            for (int box = 0; box < C::NBOX; ++box)
+                tma_store_3d(&gmap, sKV + box * C::BOX, box * 64, chunk * kFC, row);
+            bulk_commit();
+        }
+        // ---- S^T = KV Q^T
+        if (mbar_wait(&bars[0], 0, nullptr)) {
+            tc_fence_after();
+            const uint32_t idesc = idesc_bf16_f32(kFC, NH);
+            const uint32_t a0 = smem_u32(sKV), b0 = smem_u32(sQ);
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k)
+                umma_bf16(tmem, sdesc_kmajor_sw128(a0 + (k >> 2) * C::BOX + (k & 3) * 32),
+                          sdesc_kmajor_sw128(b0 + (k >> 2) * NH * 128 + (k & 3) * 32), idesc, k > 0 ? 1u : 0u);
+            umma_commit(&bars[1]);
+        } else {
+            flag_error(p.eword, DSV4_EWORD_TIMEOUT);
+            abort_flag = 1;
+        }
+    }
+    bool dead = !mbar_wait(&bars[1], 0, &abort_flag);
+    tc_fence_after();
+    // ---- scores -> shared (scaled, masked): warps w and w + 4 read TMEM lane quarter w & 3,
+    //      half of the head columns each
+    {
+        const int q = warp & 3, half = warp >> 2;
+        const int key = q * 32 + lane;
+        uint32_t r[HC];
+        tmem_ld_cols<HC>(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(half * HC), r);
+        tmem_wait_ld();
+        const bool ok = okf[key] != 0 && !dead;
+#pragma unroll
+        for (int c = 0; c < HC; ++c)
+            sS[key * (NH + 1) + half * HC + c] = ok ? __uint_as_float(r[c]) * p.scale : -INFINITY;
+    }
+    __syncthreads();
+    // ---- per head (lane) over slots [16 warp, 16 warp + 16): max, P = e^(s - m), sums
+    float sv[16];
+    float mx = -INFINITY;
+    if (lane < NH) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            sv[i] = sS[(16 * warp + i) * (NH + 1) + lane];
+            mx = fmaxf(mx, sv[i]);
+        }
+        red_m[warp * NH + lane] = mx;
+    }
+    __syncthreads();
+    float m = -INFINITY;
+    if (lane < NH) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) m = fmaxf(m, red_m[j * NH + lane]);
+        float l = 0.f;
+        uint32_t pk[8];
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+            const float p0 = sv[i] == -INFINITY ? 0.f : expf(sv[i] - m);
+            const float p1 = sv[i + 1] == -INFINITY ? 0.f : expf(sv[i + 1] - m);
+            l += p0 + p1;
+            pk[i / 2] = pack_bf16(p0, p1);
+        }
+        red_l[warp * NH + lane] = l;
+        // P[head][slot]: K-major, two 64-slot boxes of [NH rows][128 B], 128-byte swizzle
+        uint8_t* prow = sP + (warp >> 2) * (NH * 128) + lane * 128;
+        const int c0 = 2 * (warp & 3);
+        *reinterpret_cast<uint4*>(prow + ((c0 ^ (lane & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        *reinterpret_cast<uint4*>(prow + (((c0 + 1) ^ (lane & 7)) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    tc_fence_before();
+    __syncthreads();
+    // ---- O^T = V^T P^T (V^T: the KV tile read MN-major)
+    if (tid == 0 && !dead) {
+        tc_fence_after();
+        const uint32_t idesc = idesc_bf16_f32(kFC, NH) | (1u << 15);
+        const uint32_t a0 = smem_u32(sKV), b0 = smem_u32(sP);
+#pragma unroll
+        for (int mt = 0; mt < C::MT; ++mt) {
+#pragma unroll
+            for (int kk = 0; kk < kFC / 16; ++kk)
+                umma_bf16(tmem + static_cast<uint32_t>(NH + mt * NH),
+                          sdesc_mnmajor_sw128(a0 + (2 * mt) * C::BOX + kk * 2048, static_cast<uint32_t>(C::BOX), 1024u),
+                          sdesc_kmajor_sw128(b0 + (kk >> 2) * NH * 128 + (kk & 3) * 32), idesc, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&bars[2]);
+    }
+    const size_t part = static_cast<size_t>(row) * p.n_splits + chunk;
+    if (warp == 0 && lane < Hc) {                                    // this chunk's (m, l) per head
+        float l = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) l += red_l[j * NH + lane];
+        p.part_ml[(part * p.hstride + hbase + lane) * 2 + 0] = dead ? -INFINITY : m;
+        p.part_ml[(part * p.hstride + hbase + lane) * 2 + 1] = dead ? 0.f : l;
+    }
+    if (!dead && !mbar_wait(&bars[2], 0, &abort_flag)) {
+        if (tid == 0) flag_error(p.eword, DSV4_EWORD_TIMEOUT);
+        dead = true;
+    }
+    tc_fence_after();
+    // ---- O^T columns -> partials: lane = dim, one column per head
+    {
+        const int q = warp & 3, half = warp >> 2;
+        float* po = p.part_o + (part * p.hstride + hbase) * D;
+        for (int task = half; task < 2 * C::MT; task += 2) {
+            const int mt = task >> 1, ch = task & 1;
+            uint32_t r[HC];
+            tmem_ld_cols<HC>(tmem + (static_cast<uint32_t>(q * 32) << 16) +
+                                 static_cast<uint32_t>(NH + mt * NH + ch * HC), r);
+            tmem_wait_ld();
+            const int dim = mt * 128 + q * 32 + lane;
+#pragma unroll
+            for (int c = 0; c < HC; ++c)
+                if (ch * HC + c < Hc) po[static_cast<size_t>(ch * HC + c) * D + dim] = dead ? 0.f : __uint_as_float(r[c]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, C::TCOLS);
+    if (tid == 0) {
+        if (write_gather && hgrp == 0) bulk_wait_read();             // the tile is read out
+        if (abort_flag) mbar_wait(&bars[0], 0, nullptr, 100000000ull);   // the query copy landed
+    }
+}
+
+struct DecodePlan { bool use; int n_chunks, nh, n_hg; };
+
+DecodePlan decode_plan(const dsv4_attn_args& a) {
+    DecodePlan d{};
+    const int slots = a.top_k + a.window;
+    d.n_chunks = (slots + kFC - 1) / kFC;
+    d.nh = a.heads % 32 == 0 ? 32 : 16;          // every group full, or one group of <= 16
+    d.n_hg = (a.heads + d.nh - 1) / d.nh;
+    d.use = a.n_q == 1 && (a.dim == 128 || a.dim == 256 || a.dim == 512) && d.n_chunks >= 1 &&
+            d.n_chunks <= 256;
+    return d;
+}
+
+template <int D, int NH>
+int run_decode(const dsv4_attn_args& a, const DecodePlan& dp, uint8_t* ws, uint32_t* eword, cudaStream_t st) {
+    using C = FCfg<D, NH>;
+    const int rows = a.batch * a.n_q;
+    const int slots = a.top_k + a.window;
+    const size_t hs = static_cast<size_t>(dp.n_hg) * NH;
+    const size_t ml_b = align_up(static_cast<size_t>(rows) * dp.n_chunks * hs * 2 * 4, 256);
+    CUtensorMap qmap, gmap;
+    if (!encode_2d_bf16(&qmap, a.q, D, static_cast<uint64_t>(rows) * a.heads, 64, a.heads < NH ? a.heads : NH))
+        return DSV4_ERR_LAUNCH;
+    if (a.gather) {
+        if (!encode_3d_bf16(&gmap, a.gather, D, static_cast<uint64_t>(slots), static_cast<uint64_t>(rows), 64, kFC))
+            return DSV4_ERR_LAUNCH;
+    } else {
+        gmap = qmap;                                   // not used
+    }
+    AttnParams p;
+    p.sink = a.sink;
+    p.n_comp = a.n_comp;
+    p.idx = a.idx;
+    p.q_pos = a.q_pos;
+    p.win_len = a.win_len;
+    p.out = static_cast<__nv_bfloat16*>(a.out);
+    p.eword = eword;
+    p.rows = rows;
+    p.n_q = a.n_q;
+    p.H = a.heads;
+    p.max_comp = a.max_comp;
+    p.top_k = a.top_k;
+    p.window = a.window;
+    p.win_rows = a.win_rows;
+    p.ratio = a.ratio;
+    p.slots = slots;
+    p.comp_chunks = 0;
+    p.n_chunks = dp.n_chunks;
+    p.chunks_per_split = 1;
+    p.n_splits = dp.n_chunks;
+    p.oob_row = 0;
+    p.n_hg = dp.n_hg;
+    p.hstride = static_cast<int>(hs);
+    p.scale = a.scale;
+    p.part_ml = reinterpret_cast<float*>(ws);
+    p.part_o = reinterpret_cast<float*>(ws + ml_b);
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaFuncSetAttribute(attn_decode_kernel<D, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(C::SMEM));
+        attr_set = true;
+    }
+    dim3 grid(dp.n_chunks, rows, dp.n_hg);
+    count_launch();
+    if (launch_k(attn_decode_kernel<D, NH>, grid, dim3(kFT), C::SMEM, st, true, qmap, gmap, p,
+                 static_cast<const __nv_bfloat16*>(a.comp_kv), static_cast<const __nv_bfloat16*>(a.win),
+                 a.gather ? 1 : 0) != cudaSuccess)
+        return DSV4_ERR_LAUNCH;
+    dim3 g2(rows, a.heads);
+    count_launch();
+    if (launch_k(attn_combine_kernel<D, 16>, g2, dim3(128), 0, st, true, p) != cudaSuccess)
+        return DSV4_ERR_LAUNCH;
+    return DSV4_OK;
+}
+
 struct Plan { int slots, comp_chunks, n_chunks, chunks_per_split, n_splits, hp, n_hg; };
 
 Plan make_plan(const dsv4_attn_args& a) {
@@ -575,6 +914,13 @@ int run(const dsv4_attn_args& a, const Plan& pl, uint8_t* ws, uint32_t* eword, c
 }  // namespace
 
 size_t attn_ws_bytes(const dsv4_attn_args& a) {
+    const DecodePlan dp = decode_plan(a);
+    if (dp.use) {
+        const size_t rows = static_cast<size_t>(a.batch) * a.n_q;
+        const size_t hs = static_cast<size_t>(dp.n_hg) * dp.nh;
+        return align_up(rows * dp.n_chunks * hs * 2 * 4, 256) +
+               align_up(rows * dp.n_chunks * hs * static_cast<size_t>(a.dim) * 4, 256);
+    }
     const Plan pl = make_plan(a);
     const size_t rows = static_cast<size_t>(a.batch) * a.n_q;
     const size_t hs = static_cast<size_t>(pl.n_hg) * pl.hp;
@@ -586,6 +932,17 @@ size_t attn_ws_bytes(const dsv4_attn_args& a) {
 
 int launch_attn(const dsv4_attn_args& a, uint8_t* ws, uint32_t* eword, cudaStream_t st) {
     if (a.batch * a.n_q == 0) return DSV4_OK;
+    const DecodePlan dp = decode_plan(a);
+    if (dp.use) {
+        if (dp.nh == 16) {
+            if (a.dim == 512) return run_decode<512, 16>(a, dp, ws, eword, st);
+            if (a.dim == 256) return run_decode<256, 16>(a, dp, ws, eword, st);
+            return run_decode<128, 16>(a, dp, ws, eword, st);
+        }
+        if (a.dim == 512) return run_decode<512, 32>(a, dp, ws, eword, st);
+        if (a.dim == 256) return run_decode<256, 32>(a, dp, ws, eword, st);
+        return run_decode<128, 32>(a, dp, ws, eword, st);
+    }
     const Plan pl = make_plan(a);
     if (a.dim == 512) return run<512, 16>(a, pl, ws, eword, st);
     if (a.dim == 256) return run<256, 16>(a, pl, ws, eword, st);

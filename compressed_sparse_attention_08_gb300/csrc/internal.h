@@ -51,6 +51,9 @@ int launch_index_score(const dsv4_index_args& a, uint32_t* eword, cudaStream_t s
 // box_inner x box_rows elements; out-of-range boxes read as zeros. Host only, no allocation.
 bool encode_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
                     uint32_t box_inner, uint32_t box_rows);
+// 3-D bf16 tensor [outer][mid][inner] (dense), box {box_inner, box_mid, 1}, 128-byte swizzle.
+bool encode_3d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t mid, uint64_t outer,
+                    uint32_t box_inner, uint32_t box_mid);
 
 size_t attn_ws_bytes(const dsv4_attn_args& a);
 int launch_attn(const dsv4_attn_args& a, uint8_t* ws, uint32_t* eword, cudaStream_t stream);
