@@ -15,19 +15,25 @@
 // lane i reduces sum_h w_h ReLU(D[i, h]) alone, with no cross-thread reduction.
 //
 // CTA = 6 warps, persistent, one per SM, warp-specialised:
-//   warp 0  TMA producer: key tiles (128 keys x 128 dims, two 128-byte-swizzled halves)
-//           into a ring of kStages buffers; the row's queries (N x 128) into one of two buffers
-//   warp 1  MMA issuer (one thread) and TMEM owner: 8 UMMAs (K = 16 each) per tile into one
-//           of kAccBufs TMEM accumulators; tcgen05.commit frees the smem stage and publishes
-//           the accumulator
-//   warps 2-5  epilogue: tcgen05.ld of the 64-column accumulator (thread = key), weighted
-//           ReLU sum in fp32, coalesced store of the score; optionally a shared-memory
-//           histogram of the scores' top 12 key bits, flushed per row into the top-k
-//           workspace (so the long-row top-k needs no histogram pass of its own).
+//   warp 0  TMA producer: key stages of 256 keys (two 128-key MMA tiles; two 128-byte-
+//           swizzled boxes of 64 dims x 256 rows) into a ring of kStages 64 KB buffers; the
+//           row's queries (N x 128) into the query buffer
+//   warp 1  MMA issuer (one thread) and TMEM owner: per tile 8 UMMAs (K = 16 each) into one
+//           of kAccBufs TMEM accumulators; tcgen05.commit publishes the accumulator, and frees
+//           the stage once both of its tiles are done
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator (thread = key), weighted ReLU sum in
+//           fp32, coalesced store of the score; optionally a shared-memory histogram of the
+//           scores' top 12 key bits, flushed per row into the top-k workspace (so the
+//           long-row top-k needs no histogram pass of its own).
+// Why 64 KB stages: a stage stays busy from its copy until the MMA that reads it completes,
+// and that hand-off adds a few hundred ns per stage; with 32 KB stages the cost took about a
+// sixth of the bandwidth, with 64 KB stages it is hidden. Shared memory then holds one query
+// buffer, which is all a CTA needs when it scores a single row (decode).
 // Launched with programmatic dependent launch: the producer waits for the preceding kernel
-// (the compressor) only before a tile that holds key rows that kernel writes.
-// Work: the (row, key tile) pairs, cut into one contiguous range per CTA. Tiles past the
-// row's visible count are skipped by all three roles alike.
+// (the compressor) only before a stage that holds key rows that kernel writes.
+// Work: with no more rows than CTAs, every row has its own block of CTAs taking the row's
+// stages in turn; otherwise each CTA takes a contiguous range of (row, stage) pairs. Tiles
+// past the row's visible count are skipped by all three roles alike.
 #include "common.cuh"
 #include "internal.h"
 
@@ -37,18 +43,20 @@ namespace dsv4 {
 namespace {
 
 constexpr int kTileKeys = 128;              // UMMA M
+constexpr int kSub = 2;                     // MMA tiles per stage
+constexpr int kStageKeys = kSub * kTileKeys;
 constexpr int kDim = 128;                   // key width = UMMA K total
 constexpr int kMaxHeads = 64;               // UMMA N upper bound
-constexpr int kStages = 5;
+constexpr int kStages = 3;
 constexpr int kAccBufs = 4;
 constexpr int kAccCols = 64;                // TMEM columns per accumulator
 constexpr uint32_t kTmemCols = kAccBufs * kAccCols;   // 256 (power of two)
-constexpr uint32_t kKeyTileBytes = kTileKeys * kDim * 2;   // 32 KiB
-constexpr uint32_t kKeyHalfBytes = kKeyTileBytes / 2;      // 128 keys x 64 dims
+constexpr uint32_t kStageBytes = kStageKeys * kDim * 2;    // 64 KiB
+constexpr uint32_t kStageHalfBytes = kStageBytes / 2;      // 256 keys x 64 dims
 constexpr uint32_t kQBufBytes = kMaxHeads * kDim * 2;      // 16 KiB
 constexpr int kThreads = 192;
 constexpr int kHistBins = 4096;             // top 12 bits of the order-preserving score key
-constexpr size_t kSmemBytes = 1024 + kStages * kKeyTileBytes + 2 * kQBufBytes;
+constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + kQBufBytes;
 
 struct ScoreParams {
     const float* w;          // [rows, heads]
@@ -59,14 +67,25 @@ struct ScoreParams {
     const int32_t* fresh_row0;  // [batch] first key row the preceding kernel writes, or null
     int fresh_rows;          // rows it writes per sequence (0: none)
     uint32_t* eword;
-    int rows, n_q, heads, n_pad, max_comp, ratio, tiles_per_row;
+    int rows, n_q, heads, n_pad, max_comp, ratio, stages_per_row;
 };
 
-struct WorkRange { long long begin, end; };
+// The stages one CTA scores, as positions f = row * stages_per_row + stage: f = begin,
+// begin + step, ... < end. With no more rows than CTAs, every row gets its own block of CTAs
+// and they take the row's stages in turn (CTA i of n: stages i, i + n, ...), so a CTA keeps
+// one query for the whole kernel and a row's last stage (the one the compressor may have just
+// written) comes last. With more rows than CTAs (prefill), each CTA takes a contiguous range.
+struct Walk { long long begin, end, step; };
 
-__device__ __forceinline__ WorkRange cta_range(long long total) {
+__device__ __forceinline__ Walk cta_walk(int rows, int per_row) {
     const long long g = gridDim.x, c = blockIdx.x;
-    return {total * c / g, total * (c + 1) / g};
+    const long long total = static_cast<long long>(rows) * per_row;
+    if (rows > g) return {total * c / g, total * (c + 1) / g, 1};
+    long long r = c * rows / g;
+    while (r + 1 < rows && g * (r + 1) / rows <= c) ++r;
+    while (r > 0 && g * r / rows > c) --r;
+    const long long cb = g * r / rows, ce = g * (r + 1) / rows;
+    return {r * per_row + (c - cb), (r + 1) * per_row, ce - cb};
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -75,10 +94,12 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t full_bar[kStages], empty_bar[kStages];
     __shared__ uint64_t tfull_bar[kAccBufs], tempty_bar[kAccBufs];
-    __shared__ uint64_t qfull_bar[2], qempty_bar[2], done_bar;
+    __shared__ uint64_t qfull_bar, qempty_bar, done_bar;
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
-    __shared__ uint32_t s_hist[kHistBins];          // top-12-bit key histogram of the current row
+    // top-12-bit key histogram of the current row, two 16-bit counts per word (8 KB: a
+    // compressor CTA still fits beside this CTA on its SM)
+    __shared__ uint32_t s_hist[kHistBins / 2];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_trigger();
@@ -86,12 +107,13 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* base = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     uint8_t* key_buf = base;
-    uint8_t* q_buf = base + kStages * kKeyTileBytes;
+    uint8_t* q_buf = base + kStages * kStageBytes;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) { mbar_init(&full_bar[i], 1); mbar_init(&empty_bar[i], 1); }
         for (int i = 0; i < kAccBufs; ++i) { mbar_init(&tfull_bar[i], 1); mbar_init(&tempty_bar[i], 128); }
-        for (int i = 0; i < 2; ++i) { mbar_init(&qfull_bar[i], 1); mbar_init(&qempty_bar[i], 1); }
+        mbar_init(&qfull_bar, 1);
+        mbar_init(&qempty_bar, 1);
         mbar_init(&done_bar, 1);
         abort_flag = 0;
         fence_barrier_init();
@@ -99,9 +121,9 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
         tma_prefetch_desc(&qmap);
     }
     // query rows past `heads` stay zero for the whole kernel (TMA writes only `heads` rows)
-    for (uint32_t i = threadIdx.x; i < 2 * kQBufBytes / 16; i += kThreads)
+    for (uint32_t i = threadIdx.x; i < kQBufBytes / 16; i += kThreads)
         reinterpret_cast<uint4*>(q_buf)[i] = make_uint4(0, 0, 0, 0);
-    for (int i = threadIdx.x; i < kHistBins; i += kThreads) s_hist[i] = 0;
+    for (int i = threadIdx.x; i < kHistBins / 2; i += kThreads) s_hist[i] = 0;
     if (warp == 1) tmem_alloc(&tmem_slot, kTmemCols);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     tc_fence_before();
@@ -109,8 +131,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
     tc_fence_after();
     const uint32_t tmem_base = tmem_slot;
 
-    const long long total = static_cast<long long>(p.rows) * p.tiles_per_row;
-    const WorkRange wr = cta_range(total);
+    const Walk wk = cta_walk(p.rows, p.stages_per_row);
     const uint32_t idesc = idesc_bf16_f32(kTileKeys, p.n_pad);
     const uint32_t q_half = static_cast<uint32_t>(p.n_pad) * 128u;   // bytes of one 64-dim half
 
@@ -121,39 +142,38 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
             long long issued = 0;
             uint32_t phase = 0;
             const uint64_t stream_policy = l2_evict_first_policy();   // keys are read once
-            for (long long t = wr.begin; t < wr.end; ++t) {
-                const int row = static_cast<int>(t / p.tiles_per_row);
-                const int tile = static_cast<int>(t % p.tiles_per_row);
+            for (long long f = wk.begin; f < wk.end; f += wk.step) {
+                const int row = static_cast<int>(f / p.stages_per_row);
+                const int st = static_cast<int>(f % p.stages_per_row);
                 if (row != cur_row)
                     nv = row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, row, nullptr);
-                if (tile * kTileKeys >= nv) continue;
+                if (st * kStageKeys >= nv) continue;
                 if (row != cur_row) {
-                    const int qs = qcount & 1;
-                    if (!mbar_wait(&qempty_bar[qs], ((qcount >> 1) & 1) ^ 1, &abort_flag)) goto fail0;
-                    mbar_arrive_expect_tx(&qfull_bar[qs], static_cast<uint32_t>(p.heads) * kDim * 2);
-                    uint8_t* qd = q_buf + qs * kQBufBytes;
-                    tma_load_2d(qd, &qmap, &qfull_bar[qs], 0, row * p.heads);
-                    tma_load_2d(qd + q_half, &qmap, &qfull_bar[qs], 64, row * p.heads);
+                    // one query buffer: the previous row's MMAs release it first
+                    if (!mbar_wait(&qempty_bar, (qcount & 1) ^ 1, &abort_flag)) goto fail0;
+                    mbar_arrive_expect_tx(&qfull_bar, static_cast<uint32_t>(p.heads) * kDim * 2);
+                    tma_load_2d(q_buf, &qmap, &qfull_bar, 0, row * p.heads);
+                    tma_load_2d(q_buf + q_half, &qmap, &qfull_bar, 64, row * p.heads);
                     cur_row = row;
                     ++qcount;
                 }
                 if (!waited && p.fresh_rows > 0) {
                     // key rows written by the preceding kernel (the newest block's key): wait
-                    // for it before streaming a tile that overlaps them
+                    // for it before streaming a stage that overlaps them
                     const int b_ = row / p.n_q;
                     const int f0 = p.fresh_row0 ? p.fresh_row0[b_] : 0;
-                    if (tile * kTileKeys < f0 + p.fresh_rows && f0 < (tile + 1) * kTileKeys) {
+                    if (st * kStageKeys < f0 + p.fresh_rows && f0 < (st + 1) * kStageKeys) {
                         pdl_wait();
                         waited = true;
                     }
                 }
                 if (!mbar_wait(&empty_bar[stage], phase ^ 1, &abort_flag)) goto fail0;
-                mbar_arrive_expect_tx(&full_bar[stage], kKeyTileBytes);
+                mbar_arrive_expect_tx(&full_bar[stage], kStageBytes);
                 {
-                    uint8_t* kd = key_buf + stage * kKeyTileBytes;
+                    uint8_t* kd = key_buf + stage * kStageBytes;
                     const int b = row / p.n_q;
-                    tma_load_3d_hint(kd, &kmap, &full_bar[stage], 0, tile * kTileKeys, b, stream_policy);
-                    tma_load_3d_hint(kd + kKeyHalfBytes, &kmap, &full_bar[stage], 64, tile * kTileKeys, b,
+                    tma_load_3d_hint(kd, &kmap, &full_bar[stage], 0, st * kStageKeys, b, stream_policy);
+                    tma_load_3d_hint(kd + kStageHalfBytes, &kmap, &full_bar[stage], 64, st * kStageKeys, b,
                                      stream_policy);
                     ++issued;
                 }
@@ -168,47 +188,50 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
             for (long long i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
                 mbar_wait(&full_bar[i % kStages], static_cast<uint32_t>((i / kStages) & 1), nullptr, 100000000ull);
             if (qcount > 0)
-                mbar_wait(&qfull_bar[(qcount - 1) & 1], static_cast<uint32_t>(((qcount - 1) >> 1) & 1), nullptr, 100000000ull);
+                mbar_wait(&qfull_bar, static_cast<uint32_t>((qcount - 1) & 1), nullptr, 100000000ull);
             if (!waited) pdl_wait();
         done0:;
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            int stage = 0, acc = 0, qcount = 0, qs = 0, cur_row = -1, nv = 0;
+            int stage = 0, acc = 0, qcount = 0, cur_row = -1, nv = 0;
             uint32_t phase = 0, acc_phase = 0;
-            for (long long t = wr.begin; t < wr.end; ++t) {
-                const int row = static_cast<int>(t / p.tiles_per_row);
-                const int tile = static_cast<int>(t % p.tiles_per_row);
+            for (long long f = wk.begin; f < wk.end; f += wk.step) {
+                const int row = static_cast<int>(f / p.stages_per_row);
+                const int st = static_cast<int>(f % p.stages_per_row);
                 int row_nv = nv;
                 if (row != cur_row)
                     row_nv = row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, row, nullptr);
-                if (tile * kTileKeys >= row_nv) continue;
+                if (st * kStageKeys >= row_nv) continue;
                 if (row != cur_row) {
-                    if (cur_row >= 0) umma_commit(&qempty_bar[qs]);   // old queries free once done
-                    qs = qcount & 1;
-                    if (!mbar_wait(&qfull_bar[qs], (qcount >> 1) & 1, &abort_flag)) goto fail1;
+                    if (cur_row >= 0) umma_commit(&qempty_bar);   // old queries free once done
+                    if (!mbar_wait(&qfull_bar, qcount & 1, &abort_flag)) goto fail1;
                     cur_row = row;
                     nv = row_nv;
                     ++qcount;
                 }
                 if (!mbar_wait(&full_bar[stage], phase, &abort_flag)) goto fail1;
-                if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1, &abort_flag)) goto fail1;
-                tc_fence_after();
                 {
-                    const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kAccCols);
-                    const uint32_t a0 = smem_u32(key_buf + stage * kKeyTileBytes);
-                    const uint32_t b0 = smem_u32(q_buf + qs * kQBufBytes);
+                    const uint32_t a_stage = smem_u32(key_buf + stage * kStageBytes);
+                    const uint32_t b0 = smem_u32(q_buf);
+                    for (int j = 0; j < kSub; ++j) {
+                        if ((st * kSub + j) * kTileKeys >= nv) break;   // tile past the visible keys
+                        if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1, &abort_flag)) goto fail1;
+                        tc_fence_after();
+                        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kAccCols);
+                        const uint32_t a0 = a_stage + static_cast<uint32_t>(j * kTileKeys * 128);
 #pragma unroll
-                    for (int k = 0; k < kDim / 16; ++k) {
-                        const uint64_t ad = sdesc_kmajor_sw128(a0 + (k >> 2) * kKeyHalfBytes + (k & 3) * 32);
-                        const uint64_t bd = sdesc_kmajor_sw128(b0 + (k >> 2) * q_half + (k & 3) * 32);
-                        umma_bf16(d, ad, bd, idesc, k > 0 ? 1u : 0u);
+                        for (int k = 0; k < kDim / 16; ++k) {
+                            const uint64_t ad = sdesc_kmajor_sw128(a0 + (k >> 2) * kStageHalfBytes + (k & 3) * 32);
+                            const uint64_t bd = sdesc_kmajor_sw128(b0 + (k >> 2) * q_half + (k & 3) * 32);
+                            umma_bf16(d, ad, bd, idesc, k > 0 ? 1u : 0u);
+                        }
+                        umma_commit(&tfull_bar[acc]);
+                        if (++acc == kAccBufs) { acc = 0; acc_phase ^= 1; }
                     }
                 }
                 umma_commit(&empty_bar[stage]);
-                umma_commit(&tfull_bar[acc]);
                 if (++stage == kStages) { stage = 0; phase ^= 1; }
-                if (++acc == kAccBufs) { acc = 0; acc_phase ^= 1; }
             }
             goto done1;
         fail1:
@@ -231,51 +254,83 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
         bool dead = false;        // a wait ran out: keep walking the tiles (same barriers), no work
         float wv[kMaxHeads];
         // The histogram is private to the CTA and flushed to the row's global histogram when
-        // the row changes. Every epilogue thread passes the same flush barriers, dead or not.
+        // the row changes, and before a 16-bit count could overflow (every 255 stages of 256
+        // keys). Every epilogue thread passes the same flush barriers, dead or not.
+        int since_flush = 0;
         auto flush = [&](int r) {
             asm volatile("bar.sync 1, 128;" ::: "memory");
-            for (int i = etid; i < kHistBins; i += 128) {
+            uint32_t* g = p.hist + static_cast<size_t>(r) * kHistBins;
+            for (int i = etid; i < kHistBins / 2; i += 128) {
                 const uint32_t v = s_hist[i];
                 if (v) {
-                    atomicAdd(&p.hist[static_cast<size_t>(r) * kHistBins + i], v);
+                    if (v & 0xFFFFu) atomicAdd(&g[2 * i], v & 0xFFFFu);
+                    if (v >> 16) atomicAdd(&g[2 * i + 1], v >> 16);
                     s_hist[i] = 0;
                 }
             }
             asm volatile("bar.sync 1, 128;" ::: "memory");
+            since_flush = 0;
         };
-        for (long long t = wr.begin; t < wr.end; ++t) {
-            const int row = static_cast<int>(t / p.tiles_per_row);
-            const int tile = static_cast<int>(t % p.tiles_per_row);
-            if (row != cur_row) {
+        for (long long f = wk.begin; f < wk.end; f += wk.step) {
+            const int row = static_cast<int>(f / p.stages_per_row);
+            const int st = static_cast<int>(f % p.stages_per_row);
+            if (row != cur_row || since_flush == 255) {
                 if (p.hist && cur_row >= 0) flush(cur_row);
+            }
+            ++since_flush;
+            if (row != cur_row) {
                 nv = row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, row, nullptr);
                 cur_row = row;
 #pragma unroll
                 for (int h = 0; h < kMaxHeads; ++h)
                     wv[h] = h < p.heads ? __ldg(&p.w[static_cast<size_t>(row) * p.heads + h]) : 0.f;
             }
-            if (tile * kTileKeys >= nv || dead) continue;
-            if (!mbar_wait(&tfull_bar[acc], acc_phase, &abort_flag)) {
-                flag_error(p.eword, DSV4_EWORD_TIMEOUT);
-                abort_flag = 1;
-                dead = true;
-                continue;
-            }
-            tc_fence_after();
-            uint32_t r[64];
-            DSV4_TMEM_LD_32x32b_X64(tmem_base + lane_addr + static_cast<uint32_t>(acc * kAccCols), r);
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(&tempty_bar[acc]);
-            float s = 0.f;
+            for (int j = 0; j < kSub; ++j) {
+                const int tile = st * kSub + j;
+                if (tile * kTileKeys >= nv || dead) break;
+                if (!mbar_wait(&tfull_bar[acc], acc_phase, &abort_flag)) {
+                    flag_error(p.eword, DSV4_EWORD_TIMEOUT);
+                    abort_flag = 1;
+                    dead = true;
+                    break;
+                }
+                tc_fence_after();
+                // exactly the n_pad columns the MMA wrote (columns past them hold stale values)
+                uint32_t r[64];
+                const uint32_t ta = tmem_base + lane_addr + static_cast<uint32_t>(acc * kAccCols);
+                if (p.n_pad == 64) {
+                    DSV4_TMEM_LD_32x32b_X64(ta, r);
+                } else if (p.n_pad == 32) {
+                    DSV4_TMEM_LD_32x32b_X32(ta, r);
 #pragma unroll
-            for (int h = 0; h < kMaxHeads; ++h) s = fmaf(wv[h], fmaxf(__uint_as_float(r[h]), 0.f), s);
-            const int key = tile * kTileKeys + lrow;
-            if (key < nv) {
-                p.scores[static_cast<size_t>(row) * p.max_comp + key] = s;
-                if (p.hist) atomicAdd(&s_hist[float_to_key(s) >> 20], 1u);
+                    for (int h = 32; h < 64; ++h) r[h] = 0u;
+                } else if (p.n_pad == 48) {
+                    DSV4_TMEM_LD_32x32b_X32(ta, r);
+                    uint32_t* r2 = r + 32;
+                    DSV4_TMEM_LD_32x32b_X16(ta + 32u, r2);
+#pragma unroll
+                    for (int h = 48; h < 64; ++h) r[h] = 0u;
+                } else {
+                    DSV4_TMEM_LD_32x32b_X16(ta, r);
+#pragma unroll
+                    for (int h = 16; h < 64; ++h) r[h] = 0u;
+                }
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(&tempty_bar[acc]);
+                float s = 0.f;
+#pragma unroll
+                for (int h = 0; h < kMaxHeads; ++h) s = fmaf(wv[h], fmaxf(__uint_as_float(r[h]), 0.f), s);
+                const int key = tile * kTileKeys + lrow;
+                if (key < nv) {
+                    p.scores[static_cast<size_t>(row) * p.max_comp + key] = s;
+                    if (p.hist) {
+                        const uint32_t bin = float_to_key(s) >> 20;
+                        atomicAdd(&s_hist[bin >> 1], (bin & 1u) ? 0x10000u : 1u);
+                    }
+                }
+                if (++acc == kAccBufs) { acc = 0; acc_phase ^= 1; }
             }
-            if (++acc == kAccBufs) { acc = 0; acc_phase ^= 1; }
         }
         if (p.hist && cur_row >= 0) flush(cur_row);
     }
@@ -351,7 +406,7 @@ int launch_scores(const dsv4_index_args& a, float* scores, uint32_t* hist, uint3
         cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(a.max_comp),
                               static_cast<cuuint64_t>(a.batch)};
         cuuint64_t strides[2] = {kDim * 2ull, static_cast<cuuint64_t>(a.max_comp) * kDim * 2ull};
-        cuuint32_t box[3] = {64, kTileKeys, 1};
+        cuuint32_t box[3] = {64, kStageKeys, 1};
         cuuint32_t estr[3] = {1, 1, 1};
         if (encode(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.keys), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -383,8 +438,8 @@ int launch_scores(const dsv4_index_args& a, float* scores, uint32_t* hist, uint3
     p.n_pad = (a.heads + 15) / 16 * 16;
     p.max_comp = a.max_comp;
     p.ratio = a.ratio;
-    p.tiles_per_row = (a.max_comp + kTileKeys - 1) / kTileKeys;
-    const long long total = static_cast<long long>(rows) * p.tiles_per_row;
+    p.stages_per_row = (a.max_comp + kStageKeys - 1) / kStageKeys;
+    const long long total = static_cast<long long>(rows) * p.stages_per_row;
     if (total > 0) {
         static bool attr_set = false;
         if (!attr_set) {

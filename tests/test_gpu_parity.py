@@ -210,6 +210,22 @@ def test_indexer_small_heads_ragged():
         check_topk_row(idx[b, 0], ref_i[b, 0], ref_s[b, 0], nv[b, 0], k, f"b{b}")
 
 
+def test_indexer_cache_shorter_than_one_tile():
+    """A 100-row key cache: every key tile reaches past the cache's end."""
+    rng = np.random.default_rng(6)
+    B, H, N, k = 2, 16, 100, 32
+    q = synth.f32_to_bf16_bits(rng.standard_normal((B, 1, H, 128)).astype(np.float32))
+    keys = synth.f32_to_bf16_bits(rng.standard_normal((B, N, 128)).astype(np.float32))
+    w = rng.standard_normal((B, 1, H)).astype(np.float32)
+    n_comp = np.array([100, 37], np.int32)
+    idx, sc = _run_indexer(q, w, keys, n_comp, k)
+    ref_s, nv = oracle.index_scores(q, w, keys, n_comp, 4)
+    ref_i = oracle.topk(ref_s, nv, k)
+    for b in range(B):
+        _check_scores(sc[b, 0], ref_s[b, 0], nv[b, 0])
+        check_topk_row(idx[b, 0], ref_i[b, 0], ref_s[b, 0], nv[b, 0], k, f"b{b}")
+
+
 # ------------------------------------------------------------------ stage 3 alone: exact top-k
 def _run_topk(scores, n_vis, k):
     m = csa()
