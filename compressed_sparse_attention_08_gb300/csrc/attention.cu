@@ -437,16 +437,36 @@ attn_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CU
 template <int D, int HP>
 __global__ void __launch_bounds__(128)
 attn_combine_kernel(AttnParams p) {
+    constexpr int PER = D / 128;                 // dims per thread
+    constexpr int kRegSplits = 24;               // splits whose partial O is loaded up front
     __shared__ float wgt[256];
     __shared__ float red[4];
-    __shared__ float bcast[2];
+    __shared__ float bcast[1];
     const int row = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
     const int ns = p.n_splits;
     pdl_wait();
     const int HS = p.hstride;
     const float* ml = p.part_ml + static_cast<size_t>(row) * ns * HS * 2;
+    const float* po = p.part_o + static_cast<size_t>(row) * ns * HS * D + static_cast<size_t>(h) * D + tid * PER;
+    // every load at once: this thread's dims of the first kRegSplits splits, and the splits'
+    // maxima and sums (ns <= 256: two per thread)
+    float ov[kRegSplits][PER];
+#pragma unroll
+    for (int s = 0; s < kRegSplits; ++s) {
+        if (s < ns) {
+            const float* src = po + static_cast<size_t>(s) * HS * D;
+            if constexpr (PER == 4) {
+                const float4 v = *reinterpret_cast<const float4*>(src);
+                ov[s][0] = v.x; ov[s][1] = v.y; ov[s][2] = v.z; ov[s][3] = v.w;
+            } else if constexpr (PER == 2) {
+                const float2 v = *reinterpret_cast<const float2*>(src);
+                ov[s][0] = v.x; ov[s][1] = v.y;
+            } else {
+                ov[s][0] = *src;
+            }
+        }
+    }
     const float snk = p.sink[h];
-    // the splits' maxima and sums, in parallel (ns <= 256: two per thread)
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     if (tid < ns) { m0 = ml[(tid * HS + h) * 2]; l0 = ml[(tid * HS + h) * 2 + 1]; }
     if (tid + 128 < ns) { m1 = ml[((tid + 128) * HS + h) * 2]; l1 = ml[((tid + 128) * HS + h) * 2 + 1]; }
@@ -469,17 +489,28 @@ attn_combine_kernel(AttnParams p) {
     if (tid == 0) bcast[0] = 1.0f / (red[0] + red[1] + red[2] + red[3] + expf(snk - M));
     __syncthreads();
     const float inv = bcast[0];
-    const float* po = p.part_o + static_cast<size_t>(row) * ns * HS * D + static_cast<size_t>(h) * D;
-    for (int d = tid * 2; d < D; d += 256) {
-        float a0 = 0.f, a1 = 0.f;
-#pragma unroll 8
-        for (int s = 0; s < ns; ++s) {
-            const float2 v = *reinterpret_cast<const float2*>(po + static_cast<size_t>(s) * HS * D + d);
-            a0 = fmaf(v.x, wgt[s], a0);
-            a1 = fmaf(v.y, wgt[s], a1);
+    float acc[PER];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) acc[j] = 0.f;
+#pragma unroll
+    for (int s = 0; s < kRegSplits; ++s)
+        if (s < ns) {
+#pragma unroll
+            for (int j = 0; j < PER; ++j) acc[j] = fmaf(ov[s][j], wgt[s], acc[j]);
         }
-        *reinterpret_cast<uint32_t*>(p.out + (static_cast<size_t>(row) * p.H + h) * D + d) =
-            pack_bf16(a0 * inv, a1 * inv);
+    for (int s = kRegSplits; s < ns; ++s) {
+        const float* src = po + static_cast<size_t>(s) * HS * D;
+#pragma unroll
+        for (int j = 0; j < PER; ++j) acc[j] = fmaf(src[j], wgt[s], acc[j]);
+    }
+    __nv_bfloat16* dst = p.out + (static_cast<size_t>(row) * p.H + h) * D + tid * PER;
+#pragma unroll
+    for (int j = 0; j < PER; j += 2) {
+        if constexpr (PER == 1) {
+            *dst = __float2bfloat16_rn(acc[0] * inv);
+        } else {
+            *reinterpret_cast<uint32_t*>(dst + j) = pack_bf16(acc[j] * inv, acc[j + 1] * inv);
+        }
     }
 }
 

@@ -204,8 +204,8 @@ __device__ __forceinline__ void slice_range(int n, int L, int p, int& lo, int& h
 
 // The bin of a kBins-bin histogram that holds the k-th largest key (1 <= k <= total count),
 // counting from the top bin down, and how many keys lie in the bins above it: bc[0] = bin,
-// bc[1] = count above. Thread t passes in c[i] the count of bin kBins-1-(t*per+i). Every
-// thread of the CTA calls it.
+// bc[1] = count above, bc[2] = the bin's own count. Thread t passes in c[i] the count of bin
+// kBins-1-(t*per+i). Every thread of the CTA calls it.
 template <int NT>
 __device__ __forceinline__ void find_bin(const int (&c)[kBins / NT], int k, int* s_a, int* bc) {
     constexpr int NW = NT / 32, per = kBins / NT;
@@ -231,6 +231,7 @@ __device__ __forceinline__ void find_bin(const int (&c)[kBins / NT], int k, int*
             if (acc + c[i] >= k) {
                 bc[0] = kBins - 1 - (static_cast<int>(threadIdx.x) * per + i);
                 bc[1] = acc;
+                bc[2] = c[i];
                 break;
             }
             acc += c[i];
@@ -275,7 +276,7 @@ topk_filter_kernel(TopkRows t, LongWs w, int L, int P, uint32_t* eword) {
     extern __shared__ uint2 spairs[];           // kFinalCap pairs (finalizer only)
     __shared__ uint32_t hist[256];
     __shared__ int s_a[32], s_b[32];
-    __shared__ int bc[2];
+    __shared__ int bc[3];
     __shared__ int offs[kMaxSlices + 1];
     __shared__ int is_last;
     pdl_trigger();
@@ -378,16 +379,41 @@ topk_filter_kernel(TopkRows t, LongWs w, int L, int P, uint32_t* eword) {
     __syncthreads();
     if (!is_last) return;
     __threadfence();
-    // slice counts and the second histogram, loaded together
-    int cv = 0;
-    if (threadIdx.x < 64 && static_cast<int>(threadIdx.x) < P)
-        cv = __ldcg(&w.counts[static_cast<size_t>(row) * kMaxSlices + threadIdx.x]);
+    // slice counts, the second histogram and the first kPairRegs * 32 survivors of the
+    // slices this warp copies (slices warp and warp + 32; loaded before their counts are
+    // known, from inside each slice's segment), all at once
+    constexpr int kPairRegs = 4;
+    const uint2* rowpairs = w.pairs + static_cast<size_t>(row) * t.max_comp;
+    const int32_t* rowcounts = w.counts + static_cast<size_t>(row) * kMaxSlices;
+    int cnt_w[2] = {0, 0};
+    uint2 pr[2][kPairRegs];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int q = warp + 32 * h;
+        if (q < P) {
+            if (lane == 0) cnt_w[h] = __ldcg(&rowcounts[q]);
+#pragma unroll
+            for (int j = 0; j < kPairRegs; ++j) {
+                const int i = lane + 32 * j;
+                const bool in_row = i < L && static_cast<long long>(q) * L + i < t.max_comp;
+                pr[h][j] = in_row ? __ldcg(&rowpairs[static_cast<size_t>(q) * L + i]) : make_uint2(0u, 0u);
+            }
+        }
+    }
     int c2[per_bin];
 #pragma unroll
     for (int i = 0; i < per_bin; ++i)
         c2[i] = static_cast<int>(__ldcg(&g2[kBins - 1 - (static_cast<int>(threadIdx.x) * per_bin + i)]));
-    if (threadIdx.x < 64) {                      // exclusive scan of the P <= 64 slice counts
-        const int v = warp_incl(cv);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) cnt_w[h] = __shfl_sync(0xffffffffu, cnt_w[h], 0);
+    if (lane == 0) {
+        if (warp < P) offs[warp + 1] = cnt_w[0];
+        if (warp + 32 < P) offs[warp + 33] = cnt_w[1];
+    }
+    __syncthreads();
+    if (warp < 2) {                              // inclusive scan of the P <= 64 slice counts
+        int v = static_cast<int>(threadIdx.x) < P ? offs[threadIdx.x + 1] : 0;
+        v = warp_incl(v);
         if (threadIdx.x == 31) s_b[1] = v;
         offs[threadIdx.x + 1] = v;
         if (threadIdx.x == 0) offs[0] = 0;
@@ -398,8 +424,8 @@ topk_filter_kernel(TopkRows t, LongWs w, int L, int P, uint32_t* eword) {
     find_bin<NT>(c2, k - above, s_a, bc);
     const uint32_t prefix = (tb << kBinShift) | (static_cast<uint32_t>(bc[0]) << 8);
     const int need = k - above - bc[1];
+    const bool whole_sub_bin = need == bc[2] && prefix != 0u;   // every key of the sub-bin is in
     const int total = offs[P];
-    const uint2* rowpairs = w.pairs + static_cast<size_t>(row) * t.max_comp;
     auto slice_of = [&](int i) {                 // slice q with offs[q] <= i < offs[q + 1]
         int a = 0, b = P - 1;
         while (a < b) {
@@ -411,25 +437,31 @@ topk_filter_kernel(TopkRows t, LongWs w, int L, int P, uint32_t* eword) {
     uint32_t T;
     int need_T;
     if (total <= kFinalCap) {
-        constexpr int kB = 4;                    // loads in flight per thread
-        for (int i0 = threadIdx.x; i0 < total; i0 += NT * kB) {
-            uint2 v[kB];
+        // each warp places its slices' survivors at the slices' offsets
 #pragma unroll
-            for (int j = 0; j < kB; ++j) {
-                const int i = i0 + j * NT;
-                if (i < total) {
-                    const int q = slice_of(i);
-                    v[j] = __ldcg(&rowpairs[static_cast<size_t>(q) * L + (i - offs[q])]);
+        for (int h = 0; h < 2; ++h) {
+            const int q = warp + 32 * h;
+            if (q < P) {
+                const int base = offs[q], cnt = cnt_w[h];
+#pragma unroll
+                for (int j = 0; j < kPairRegs; ++j) {
+                    const int i = lane + 32 * j;
+                    if (i < cnt) spairs[base + i] = pr[h][j];
                 }
+                for (int i = kPairRegs * 32 + lane; i < cnt; i += 32)
+                    spairs[base + i] = __ldcg(&rowpairs[static_cast<size_t>(q) * L + i]);
             }
-#pragma unroll
-            for (int j = 0; j < kB; ++j)
-                if (i0 + j * NT < total) spairs[i0 + j * NT] = v[j];
         }
         __syncthreads();
         auto key_at = [&](int i) { return spairs[i].x; };
         auto idx_at = [&](int i) { return static_cast<int32_t>(spairs[i].y); };
-        radix_select<NT>(total, need, key_at, hist, bc, T, need_T, prefix, 32 - 8);
+        if (whole_sub_bin) {
+            // the k keys are exactly those at or above the sub-bin: no selection inside it
+            T = prefix - 1u;
+            need_T = 0;
+        } else {
+            radix_select<NT>(total, need, key_at, hist, bc, T, need_T, prefix, 32 - 8);
+        }
         ordered_select<NT>(total, T, need_T, key_at, idx_at, out, s_a, s_b);
     } else {
         // degenerate score distributions (huge ties): the same steps on the slices in place
@@ -439,7 +471,12 @@ topk_filter_kernel(TopkRows t, LongWs w, int L, int P, uint32_t* eword) {
         };
         auto key_at = [&](int i) { return at(i).x; };
         auto idx_at = [&](int i) { return static_cast<int32_t>(at(i).y); };
-        radix_select<NT>(total, need, key_at, hist, bc, T, need_T, prefix, 32 - 8);
+        if (whole_sub_bin) {
+            T = prefix - 1u;
+            need_T = 0;
+        } else {
+            radix_select<NT>(total, need, key_at, hist, bc, T, need_T, prefix, 32 - 8);
+        }
         ordered_select<NT>(total, T, need_T, key_at, idx_at, out, s_a, s_b);
     }
 }
