@@ -257,10 +257,11 @@ int dsv4_csa_decode(const dsv4_csa_args* a, void* ws, size_t ws_bytes, dsv4_stre
         return DSV4_ERR_INVALID_ARG;
     if (int rc = device_check()) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // the header and the top-k histograms are cleared by the compression launch (the kernels
+    // after it read them only once it has completed), saving a memset in the step
     const size_t zero = kWsHeader + (a->index ? index_zero_bytes(*a->index) : 0);
-    if (cudaMemsetAsync(ws, 0, zero, st) != cudaSuccess) return DSV4_ERR_LAUNCH;
     int rc = DSV4_OK;
-    if ((rc = launch_compress2(a->compress_kv, a->compress_keys, st))) return rc;
+    if ((rc = launch_compress2(a->compress_kv, a->compress_keys, st, ws, zero))) return rc;
     if (a->index && (rc = launch_indexer(*a->index, body_of(ws), eword_of(ws), st, a->compress_keys)))
         return rc;
     return launch_attn(*a->attn, body_of(ws), eword_of(ws), st);

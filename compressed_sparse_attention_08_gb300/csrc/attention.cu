@@ -195,8 +195,7 @@ attn_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CU
     const int hbase = hgrp * HP;                           // first head of this CTA
     const int Hc = p.H - hbase < HP ? p.H - hbase : HP;    // heads handled here
     const int b = row / p.n_q, t = row - b * p.n_q;
-    const int nv = row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, row,
-                               hgrp == 0 && split == 0 ? p.eword : nullptr);
+    const int nv = row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, row, nullptr);
     int wl = p.win_len[b];
     wl = wl < 0 ? 0 : (wl > p.win_rows ? p.win_rows : wl);
     const int w_hi = t + wl - p.n_q;                       // the query's own window row
@@ -274,6 +273,8 @@ attn_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CU
     for (int i = 0; i < C::DW / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
     pdl_wait();             // the index list (and the workspace) belong to the kernels before
+    if (hgrp == 0 && split == 0 && tid == 0)                         // report a bad count once
+        row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, row, p.eword);
     bool dead = false;      // a bounded wait ran out: keep the barrier sequence, skip the math
     if (!mbar_wait(&bars[0], 0, nullptr)) { flag_error(p.eword, DSV4_EWORD_TIMEOUT); dead = true; }
     if (c0 < c1) issue(c0, 0);
@@ -583,8 +584,7 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
     const int Hc = p.H - hbase < NH ? p.H - hbase : NH;
     const int b = row / p.n_q, t = row - b * p.n_q;
     pdl_trigger();
-    const int nv = row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, row,
-                               hgrp == 0 && chunk == 0 ? p.eword : nullptr);
+    const int nv = row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, row, nullptr);
     int wl = p.win_len[b];
     wl = wl < 0 ? 0 : (wl > p.win_rows ? p.win_rows : wl);
     const int w_hi = t + wl - p.n_q;                                 // the query's own window row
@@ -617,6 +617,8 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
     }
 
     pdl_wait();                      // the index list comes from the kernel before
+    if (hgrp == 0 && chunk == 0 && tid == 0)                         // report a bad count once
+        row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, row, p.eword);
     // ---- gather: warp w copies slots [16w, 16w + 16) of the chunk; lanes 0..15 resolve them
     {
         const int r0 = warp * 16;

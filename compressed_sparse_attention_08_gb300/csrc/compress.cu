@@ -46,9 +46,18 @@ struct CompressJob {
     double freq[kMaxPairs];
 };
 
+// zero_p/zero_n16: a workspace region (16-byte words) this launch clears for the kernels after
+// it (the fused decode step), so the step needs no separate memset; they read it only after
+// waiting for this grid.
 __global__ void __launch_bounds__(kThreads, 1)
-compress_kernel(const __grid_constant__ CompressJob j0, const __grid_constant__ CompressJob j1) {
+compress_kernel(const __grid_constant__ CompressJob j0, const __grid_constant__ CompressJob j1,
+                uint4* zero_p, unsigned zero_n16) {
     pdl_trigger();
+    {
+        const unsigned nthr = gridDim.x * gridDim.y * gridDim.z * kThreads;
+        const unsigned gt = ((blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x) * kThreads + threadIdx.x;
+        for (unsigned i = gt; i < zero_n16; i += nthr) zero_p[i] = make_uint4(0, 0, 0, 0);
+    }
     // every field of the selected job once, into registers (a runtime choice between two
     // parameter structs would otherwise turn each use into a slow generic load)
     const bool second = blockIdx.z != 0;
@@ -186,22 +195,29 @@ CompressJob make_job(const dsv4_compress_args& a) {
 
 }  // namespace
 
-int launch_compress2(const dsv4_compress_args* a, const dsv4_compress_args* b, cudaStream_t stream) {
-    if (!a && !b) return DSV4_OK;
+int launch_compress2(const dsv4_compress_args* a, const dsv4_compress_args* b, cudaStream_t stream,
+                     void* zero, size_t zero_bytes) {
+    const unsigned n16 = static_cast<unsigned>((zero_bytes + 15) / 16);
+    auto memset_only = [&]() {
+        return n16 == 0 || cudaMemsetAsync(zero, 0, size_t(n16) * 16, stream) == cudaSuccess ? DSV4_OK
+                                                                                            : DSV4_ERR_LAUNCH;
+    };
+    if (!a && !b) return memset_only();
     if (!a) { a = b; b = nullptr; }
     const CompressJob j0 = make_job(*a);
     const CompressJob j1 = b ? make_job(*b) : j0;
     const int nb = j0.n_blocks > j1.n_blocks ? j0.n_blocks : j1.n_blocks;
     const int bs = j0.batch > j1.batch ? j0.batch : j1.batch;
-    if (nb == 0 || bs == 0) return DSV4_OK;
+    if (nb == 0 || bs == 0) return memset_only();
     dim3 grid(nb, bs, b ? 2 : 1);
     count_launch();
-    return launch_k(compress_kernel, grid, dim3(kThreads), 0, stream, false, j0, j1) == cudaSuccess
+    return launch_k(compress_kernel, grid, dim3(kThreads), 0, stream, false, j0, j1,
+                    static_cast<uint4*>(zero), n16) == cudaSuccess
                ? DSV4_OK : DSV4_ERR_LAUNCH;
 }
 
 int launch_compress(const dsv4_compress_args& a, cudaStream_t stream) {
-    return launch_compress2(&a, nullptr, stream);
+    return launch_compress2(&a, nullptr, stream, nullptr, 0);
 }
 
 }  // namespace dsv4

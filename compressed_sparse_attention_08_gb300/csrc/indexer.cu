@@ -258,6 +258,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
         // keys). Every epilogue thread passes the same flush barriers, dead or not.
         int since_flush = 0;
         auto flush = [&](int r) {
+            pdl_wait();      // the histogram may have been cleared by the preceding kernel
             asm volatile("bar.sync 1, 128;" ::: "memory");
             uint32_t* g = p.hist + static_cast<size_t>(r) * kHistBins;
             for (int i = etid; i < kHistBins / 2; i += 128) {

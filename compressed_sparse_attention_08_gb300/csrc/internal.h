@@ -13,7 +13,11 @@ namespace dsv4 {
 
 int launch_compress(const dsv4_compress_args& a, cudaStream_t stream);
 // Up to two compressions (e.g. main KV and indexer keys) in one launch; either may be null.
-int launch_compress2(const dsv4_compress_args* a, const dsv4_compress_args* b, cudaStream_t stream);
+// Both compressions in one launch; the launch also clears `zero_bytes` bytes at `zero` (a
+// 16-byte aligned workspace region, rounded up to 16 bytes) for the kernels after it, or a
+// memset does when there is nothing to compress.
+int launch_compress2(const dsv4_compress_args* a, const dsv4_compress_args* b, cudaStream_t stream,
+                     void* zero, size_t zero_bytes);
 
 // Top-k over fp32 score rows. Exactly one of n_vis (an int32 [rows] array) or the indexer
 // geometry (n_comp [batch], q_pos [batch, n_q] or null, ratio) gives each row's visible count.
