@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="time only the chunked-prefill indexer scoring (tensor-core bound)")
     return ap.parse_args()
 
 
@@ -91,6 +93,59 @@ def measured_peaks():
             d = json.load(fh)
         return float(d["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def measured_bf16_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            return float(json.load(fh)["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
+def prefill_scoring(m, steps):
+    """The chunked-prefill indexer scoring alone: 2048 new query tokens x 64 heads x 128 dims
+    against the 16,896 compressed keys with the causal block mask. A dense contraction, so
+    it is reported in TFLOP/s against the measured bf16 tensor peak; flops count only the
+    visible (query, key) pairs, 64 heads x 128 dims x 2 each."""
+    import numpy as np
+    import torch
+    from compressed_sparse_attention_08_gb300.workloads import WORKLOADS, make_inputs
+    wl = WORKLOADS[4]
+    x = make_inputs(wl)
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a, np.uint16).view(np.int16)).cuda().view(torch.bfloat16)
+
+    q, keys = bf(x["q_I"]), bf(x["keys"])
+    w = torch.from_numpy(np.ascontiguousarray(x["w"])).cuda()
+    n_comp = torch.from_numpy(x["n_comp"]).cuda()
+    q_pos = torch.from_numpy(x["q_pos"]).cuda()
+    scores = torch.empty(1, wl.new_tokens, wl.max_comp, dtype=torch.float32, device="cuda")
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def run():
+        m.dsv4_index_score(q, w, keys, n_comp, scores, ws, ratio=wl.ratio, q_pos=q_pos, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            run()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(max(1, min(steps, 50)))]
+        for a, b in evs:
+            a.record(stream)
+            run()
+            b.record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    vis = np.minimum(x["n_comp"][0], (x["q_pos"][0] + 1) // wl.ratio)
+    flops = float(vis.sum()) * wl.idx_heads * wl.idx_dim * 2
+    peak, kind = measured_bf16_peak()
+    achieved = flops / (ms * 1e-3) / 1e12
+    return {"workload": wl.name, "bound": "tensor", "kernel": "index_score_kernel",
+            "flops_per_launch": flops, "ms_per_launch": ms, "achieved": achieved, "peak": peak,
+            "peak_kind": kind, "unit": "TFLOP/s", "frac": achieved / peak}
 
 
 def profile_traffic():
@@ -396,6 +451,8 @@ def run_ours(args):
         "gpu_launches": launches * args.steps, "launches_per_step": launches,
         "clocks": clk,
     }
+    if world == 1:
+        line["prefill_scoring"] = prefill_scoring(m, args.steps)
     if world == 1 and not args.no_cpu_baseline:
         x0 = make_inputs(wl, batch=1)
         line["cpu_baseline"] = cpu_baseline(wl, x0)
@@ -406,6 +463,14 @@ def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.prefill_only:
+        import torch
+        if not torch.cuda.is_available():
+            raise SystemExit("bench.py needs a CUDA device")
+        import __graft_entry__
+        __graft_entry__.build()
+        import compressed_sparse_attention_08_gb300 as m
+        print(json.dumps({"prefill_scoring": prefill_scoring(m, args.steps)}), flush=True)
     else:
         run_ours(args)
 
