@@ -56,6 +56,7 @@ def _bind(lib):
     I = ctypes.c_int
     D = ctypes.c_double
     lib.oracle_compress.argtypes = [P, P, P, P, P, I, I, I, I, I, D, D, P, P]
+    lib.oracle_compress_overlap.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, D, D, P, P]
     lib.oracle_index_scores.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P, P]
     lib.oracle_topk.argtypes = [P, P, I, I, I, P]
     lib.oracle_topk_f32.argtypes = [P, P, I, I, I, P]
@@ -67,7 +68,7 @@ def _bind(lib):
     lib.oracle_visible_entries.restype = ctypes.c_int64
     lib.oracle_double_to_bf16.argtypes = [D]
     lib.oracle_double_to_bf16.restype = ctypes.c_uint16
-    for f in (lib.oracle_compress, lib.oracle_index_scores, lib.oracle_topk,
+    for f in (lib.oracle_compress, lib.oracle_compress_overlap, lib.oracle_index_scores, lib.oracle_topk,
               lib.oracle_topk_f32, lib.oracle_sparse_attn):
         f.restype = ctypes.c_int
     return lib
@@ -94,6 +95,28 @@ def compress(C, Z, bias, gamma, pos0, ratio, rope_dim=64, theta=10000.0, eps=1e-
                              rope_dim, float(theta), float(eps), _p(out), _p(out64))
     if rc != 0:
         raise ValueError(f"oracle_compress: bad arguments (rc={rc})")
+    return out, out64
+
+
+def compress_overlap(C, Z, bias, gamma, pos0, ratio, prev_C=None, prev_Z=None, rope_dim=64,
+                     theta=10000.0, eps=1e-6):
+    """Overlapped two-stream (CSA) compressor + RMSNorm + RoPE.  C, Z: uint16 [B, T, 2d]
+    (stream a = channels [0, d), stream b = [d, 2d)); bias fp32 [ratio, 2d]; gamma fp32 [d];
+    pos0 int64 [B]; prev_C, prev_Z uint16 [B, ratio, 2d] or None (the block before C's first
+    block).  Returns (bf16 bits [B, T/ratio, d], float64 same)."""
+    lib = _load()
+    C = _c(C, np.uint16); Z = _c(Z, np.uint16)
+    prev_C = _c(prev_C, np.uint16); prev_Z = _c(prev_Z, np.uint16)
+    bias = _c(bias, np.float32); gamma = _c(gamma, np.float32); pos0 = _c(pos0, np.int64)
+    B, T, w = C.shape
+    d = w // 2
+    out = np.zeros((B, T // ratio, d), np.uint16)
+    out64 = np.zeros((B, T // ratio, d), np.float64)
+    rc = lib.oracle_compress_overlap(_p(C), _p(Z), _p(prev_C), _p(prev_Z), _p(bias), _p(gamma),
+                                     _p(pos0), B, T, d, ratio, rope_dim, float(theta), float(eps),
+                                     _p(out), _p(out64))
+    if rc != 0:
+        raise ValueError(f"oracle_compress_overlap: bad arguments (rc={rc})")
     return out, out64
 
 

@@ -65,6 +65,32 @@ int64_t visible_entries(int64_t n_comp, int64_t p, int ratio) {
 
 extern "C" {
 
+// RMSNorm over the d channels of one entry, then RoPE on its last rope_dim channels at
+// position `pos`, then one RNE rounding to bf16 (shared by both compressor forms).
+static void finish_entry(double* x, int d, int rope_dim, double theta, double eps,
+                         const float* gamma, double pos, uint16_t* out_row, double* out_f64_row) {
+    // RMSNorm over all d channels
+    double ms = 0.0;
+    for (int c = 0; c < d; ++c) ms += x[c] * x[c];
+    ms /= d;
+    double inv = 1.0 / std::sqrt(ms + eps);
+    for (int c = 0; c < d; ++c) x[c] = x[c] * inv * static_cast<double>(gamma[c]);
+    // RoPE on the last rope_dim dims, pair j = (d0, d0+1), d0 = d - rope_dim + 2j
+    for (int j = 0; j < rope_dim / 2; ++j) {
+        const int d0 = d - rope_dim + 2 * j;
+        const double freq = std::pow(theta, -2.0 * j / rope_dim);
+        const double ang = pos * freq;
+        const double cs = std::cos(ang), sn = std::sin(ang);
+        const double e = x[d0], o = x[d0 + 1];
+        x[d0] = e * cs - o * sn;
+        x[d0 + 1] = e * sn + o * cs;
+    }
+    for (int c = 0; c < d; ++c) {
+        out_row[c] = double_to_bf16(x[c]);
+        if (out_f64_row) out_f64_row[c] = x[c];
+    }
+}
+
 // ---------------------------------------------------------------------------
 // a1/a2. Block compressor + RMSNorm + partial RoPE.
 //
@@ -110,28 +136,77 @@ int oracle_compress(const uint16_t* C, const uint16_t* Z, const float* bias,
                 }
                 x[c] = num / den;
             }
-            // RMSNorm over all d channels
-            double ms = 0.0;
-            for (int c = 0; c < d; ++c) ms += x[c] * x[c];
-            ms /= d;
-            double inv = 1.0 / std::sqrt(ms + eps);
-            for (int c = 0; c < d; ++c) x[c] = x[c] * inv * static_cast<double>(gamma[c]);
-            // RoPE on the last rope_dim dims, pair j = (d0, d0+1), d0 = d - rope_dim + 2j
             const double pos = static_cast<double>(pos0[s] + static_cast<int64_t>(b) * ratio);
-            for (int j = 0; j < rope_dim / 2; ++j) {
-                const int d0 = d - rope_dim + 2 * j;
-                const double freq = std::pow(theta, -2.0 * j / rope_dim);
-                const double ang = pos * freq;
-                const double cs = std::cos(ang), sn = std::sin(ang);
-                const double e = x[d0], o = x[d0 + 1];
-                x[d0] = e * cs - o * sn;
-                x[d0 + 1] = e * sn + o * cs;
-            }
+            const size_t row = static_cast<size_t>(s) * nb + b;
+            finish_entry(x.data(), d, rope_dim, theta, eps, gamma, pos, out + row * d,
+                         out_f64 ? out_f64 + row * d : nullptr);
+        }
+    }
+    return 0;
+}
+
+// ---------------------------------------------------------------------------
+// a1 (CSA form). Overlapped two-stream block compressor.
+//
+// [A] compressor_reduce.cu, "CSA compressor reduce kernel": the projections carry 2d channels,
+// stream a (channels [0, d)) and stream b (channels [d, 2d)); entry i pools the ratio tokens
+// of block i - 1 from stream a together with the ratio tokens of block i from stream b (entry
+// 0, which has no block before it, pools only its own block from stream b), with one softmax
+// over all pooled logits per channel and the weighted sum of the matching C values. The
+// positional bias has 2d columns: token t of either part takes bias row t of its stream's
+// half, on the logits only ([B] commit "Fix two correctness bugs", item 1). RMSNorm and RoPE
+// follow as for the plain compressor, at the position of entry i's own first token.
+//
+// C, Z [B, T, 2d] bf16; bias [ratio, 2d] fp32; prev_C, prev_Z [B, ratio, 2d] or null: the
+// block just before the first block of C (its stream a feeds entry 0); null means entry 0 is
+// the sequence's first block. out [B, T/ratio, d].
+int oracle_compress_overlap(const uint16_t* C, const uint16_t* Z, const uint16_t* prev_C,
+                            const uint16_t* prev_Z, const float* bias, const float* gamma,
+                            const int64_t* pos0, int B, int T, int d, int ratio, int rope_dim,
+                            double theta, double eps, uint16_t* out, double* out_f64) {
+    if (B < 0 || T < 0 || d <= 0 || ratio <= 0 || T % ratio != 0) return -1;
+    if (rope_dim < 0 || rope_dim > d || rope_dim % 2 != 0) return -1;
+    if ((prev_C == nullptr) != (prev_Z == nullptr)) return -1;
+    const int nb = T / ratio, w = 2 * d;
+    std::vector<double> x(d), lg(2 * static_cast<size_t>(ratio)), val(2 * static_cast<size_t>(ratio));
+    for (int s = 0; s < B; ++s) {
+        for (int i = 0; i < nb; ++i) {
             for (int c = 0; c < d; ++c) {
-                size_t at = (static_cast<size_t>(s) * nb + b) * d + c;
-                out[at] = double_to_bf16(x[c]);
-                if (out_f64) out_f64[at] = x[c];
+                int n = 0;
+                // stream a: the previous block's tokens
+                if (i > 0 || prev_C) {
+                    for (int t = 0; t < ratio; ++t) {
+                        const size_t at = i > 0
+                            ? (static_cast<size_t>(s) * T + static_cast<size_t>(i - 1) * ratio + t) * w + c
+                            : (static_cast<size_t>(s) * ratio + t) * w + c;
+                        const uint16_t zb = i > 0 ? Z[at] : prev_Z[at];
+                        const uint16_t cb = i > 0 ? C[at] : prev_C[at];
+                        lg[n] = bf16_to_double(zb) + static_cast<double>(bias[static_cast<size_t>(t) * w + c]);
+                        val[n] = bf16_to_double(cb);
+                        ++n;
+                    }
+                }
+                // stream b: this block's tokens
+                for (int t = 0; t < ratio; ++t) {
+                    const size_t at = (static_cast<size_t>(s) * T + static_cast<size_t>(i) * ratio + t) * w + d + c;
+                    lg[n] = bf16_to_double(Z[at]) + static_cast<double>(bias[static_cast<size_t>(t) * w + d + c]);
+                    val[n] = bf16_to_double(C[at]);
+                    ++n;
+                }
+                double mx = -std::numeric_limits<double>::infinity();
+                for (int u = 0; u < n; ++u) mx = std::max(mx, lg[u]);
+                double num = 0.0, den = 0.0;
+                for (int u = 0; u < n; ++u) {
+                    const double e = std::exp(lg[u] - mx);
+                    den += e;
+                    num += e * val[u];
+                }
+                x[c] = num / den;
             }
+            const double pos = static_cast<double>(pos0[s]) + static_cast<double>(i) * ratio;
+            const size_t row = static_cast<size_t>(s) * nb + i;
+            finish_entry(x.data(), d, rope_dim, theta, eps, gamma, pos, out + row * d,
+                         out_f64 ? out_f64 + row * d : nullptr);
         }
     }
     return 0;

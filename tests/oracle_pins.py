@@ -496,4 +496,105 @@ def pin_page_sizes():
             assert oracle.max_comp(ctx, r) == next(n for n in range(ctx + 1) if n * r >= ctx)
 
 
+# ------------------------------------------------------------------ a1, CSA form: overlapped
+# [A] compressor_reduce.cu "CSA compressor reduce kernel": entry i pools block i-1 from stream a
+# (channels [0, d)) and block i from stream b (channels [d, 2d)); entry 0 has only stream b.
+def _overlap(C, Z, bias, prev_C=None, prev_Z=None, pos0=None, ratio=4, rope_dim=0, gamma=None):
+    B, T, w = C.shape
+    d = w // 2
+    gamma = np.ones(d, np.float32) if gamma is None else gamma
+    pos0 = np.zeros(B, np.int64) if pos0 is None else pos0
+    return oracle.compress_overlap(C, Z, bias, gamma, pos0, ratio, prev_C, prev_Z, rope_dim)
+
+
+def _unit_rms(v, eps=1e-6):
+    v = np.asarray(v, np.float64)
+    return v / np.sqrt(np.mean(v * v, axis=-1, keepdims=True) + eps)
+
+
+def pin_overlap_first_entry_is_plain_stream_b():
+    """With no block before it, entry 0 of the two-stream form is the plain compressor applied
+    to stream b alone (C, Z and bias columns [d, 2d)), RMSNorm and RoPE included."""
+    rng = _rng(41)
+    B, r, d = 2, 4, 64
+    C = _bf(rng.standard_normal((B, 3 * r, 2 * d)))
+    Z = _bf(rng.standard_normal((B, 3 * r, 2 * d)))
+    bias = _f(_bf(rng.standard_normal((r, 2 * d)) * 0.5)).astype(np.float32)
+    gamma = _f(_bf(1 + 0.1 * rng.standard_normal(d))).astype(np.float32)
+    pos0 = np.array([0, 640], np.int64)
+    _, got = _overlap(C, Z, bias, pos0=pos0, rope_dim=16, gamma=gamma)
+    _, want = oracle.compress(C[:, :r, d:], Z[:, :r, d:], bias[:, d:], gamma, pos0, r, 16)
+    _close(got[:, 0], want[:, 0], rtol=1e-14, atol=1e-14, msg="entry 0 vs plain on stream b")
+
+
+def pin_overlap_equal_logits_pool_both_blocks():
+    """Equal logits (Z = 0, bias = 0): entry i >= 1 is the mean of block i-1's stream-a values
+    and block i's stream-b values (2 x ratio tokens), then unit RMS."""
+    rng = _rng(42)
+    B, r, d, nb = 2, 4, 32, 5
+    C = _bf(rng.integers(-64, 65, size=(B, nb * r, 2 * d)).astype(np.float32))
+    Z = np.zeros_like(C)
+    bias = np.zeros((r, 2 * d), np.float32)
+    _, got = _overlap(C, Z, bias)
+    c = _f(C)
+    for i in range(1, nb):
+        pooled = np.concatenate([c[:, (i - 1) * r:i * r, :d], c[:, i * r:(i + 1) * r, d:]], axis=1)
+        _close(got[:, i], _unit_rms(pooled.mean(axis=1)), rtol=1e-12, atol=1e-12, msg=f"entry {i}")
+
+
+def pin_overlap_bias_not_on_C():
+    """C = 0 => every entry is 0, for any logits and any bias in either stream ([B] commit
+    "Fix two correctness bugs", item 1)."""
+    rng = _rng(43)
+    B, r, d = 2, 4, 32
+    C = np.zeros((B, 4 * r, 2 * d), np.uint16)
+    Z = _bf(rng.standard_normal((B, 4 * r, 2 * d)))
+    bias = _f(_bf(rng.standard_normal((r, 2 * d)))).astype(np.float32)
+    prev = _bf(rng.standard_normal((B, r, 2 * d)))
+    _, got = _overlap(C, Z, bias, prev_C=np.zeros_like(prev), prev_Z=prev, rope_dim=8)
+    assert np.all(got == 0.0), "bias leaked into the content"
+
+
+def pin_overlap_streams_come_from_the_right_blocks():
+    """A dominant bias on row t0 of one stream's half selects that single token: stream a
+    yields C[block i-1, token t0, channels < d], stream b yields C[block i, token t0,
+    channels >= d]; for entry 0 with a previous block, stream a reads that block."""
+    rng = _rng(44)
+    B, r, d, nb = 2, 4, 32, 3
+    C = _bf(rng.standard_normal((B, nb * r, 2 * d)))
+    Z = _bf(0.1 * rng.standard_normal((B, nb * r, 2 * d)))
+    prev_C = _bf(rng.standard_normal((B, r, 2 * d)))
+    prev_Z = _bf(0.1 * rng.standard_normal((B, r, 2 * d)))
+    c, pc = _f(C), _f(prev_C)
+    for t0 in (0, 3):
+        bias = np.zeros((r, 2 * d), np.float32)
+        bias[t0, :d] = 80.0                                       # stream a, row t0
+        _, got = _overlap(C, Z, bias, prev_C=prev_C, prev_Z=prev_Z)
+        _close(got[:, 0], _unit_rms(pc[:, t0, :d]), rtol=1e-9, atol=1e-9, msg=f"a, entry 0, t0={t0}")
+        for i in range(1, nb):
+            _close(got[:, i], _unit_rms(c[:, (i - 1) * r + t0, :d]), rtol=1e-9, atol=1e-9,
+                   msg=f"a, entry {i}, t0={t0}")
+        bias = np.zeros((r, 2 * d), np.float32)
+        bias[t0, d:] = 80.0                                       # stream b, row t0
+        _, got = _overlap(C, Z, bias, prev_C=prev_C, prev_Z=prev_Z)
+        for i in range(nb):
+            _close(got[:, i], _unit_rms(c[:, i * r + t0, d:]), rtol=1e-9, atol=1e-9,
+                   msg=f"b, entry {i}, t0={t0}")
+
+
+def pin_overlap_previous_block_pointer_matches_longer_buffer():
+    """Passing block 0 as the previous block and the rest as the buffer gives the entries of
+    the longer buffer from entry 1 on, positions shifted by one block (RoPE included)."""
+    rng = _rng(45)
+    B, r, d, nb = 2, 4, 64, 4
+    C = _bf(rng.standard_normal((B, nb * r, 2 * d)))
+    Z = _bf(rng.standard_normal((B, nb * r, 2 * d)))
+    bias = _f(_bf(0.5 * rng.standard_normal((r, 2 * d)))).astype(np.float32)
+    pos0 = np.array([0, 4096], np.int64)
+    _, full = _overlap(C, Z, bias, pos0=pos0, rope_dim=64)
+    _, tail = _overlap(C[:, r:], Z[:, r:], bias, prev_C=C[:, :r], prev_Z=Z[:, :r], pos0=pos0 + r,
+                       rope_dim=64)
+    _close(tail, full[:, 1:], rtol=1e-14, atol=1e-14, msg="previous-block pointer")
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

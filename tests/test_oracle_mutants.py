@@ -37,6 +37,16 @@ MUTANTS = [
      "const int64_t hi = qa + win_len[b] - n_q_total - 1;", 1),
     ("bf16_truncates", "double r = std::nearbyint(scaled);", "double r = std::trunc(scaled);", 1),
     ("max_comp_floor", "return (max_context + ratio - 1) / ratio;", "return max_context / ratio;", 1),
+    ("overlap_a_from_own_block", "static_cast<size_t>(i - 1) * ratio + t) * w + c",
+     "static_cast<size_t>(i) * ratio + t) * w + c", 1),
+    ("overlap_bias_halves_swapped", "bias[static_cast<size_t>(t) * w + c]",
+     "bias[static_cast<size_t>(t) * w + d + c]", 1),
+    ("overlap_bias_on_C", "val[n] = bf16_to_double(cb);",
+     "val[n] = bf16_to_double(cb) + static_cast<double>(bias[static_cast<size_t>(t) * w + c]);", 1),
+    ("overlap_ignores_previous_block", "if (i > 0 || prev_C) {", "if (i > 0) {", 1),
+    ("overlap_position_unscaled", "static_cast<double>(i) * ratio", "static_cast<double>(i)", 1),
+    ("overlap_b_reads_stream_a", "static_cast<size_t>(i) * ratio + t) * w + d + c;",
+     "static_cast<size_t>(i) * ratio + t) * w + c;", 1),
 ]
 
 RUNNER = r"""
