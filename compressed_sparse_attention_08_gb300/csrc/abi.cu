@@ -44,6 +44,9 @@ bool compress_ok(const dsv4_compress_args* a) {
     if (!a->out_row0 && a->out_rows < a->tokens / a->ratio) return false;
     if (!(a->eps >= 0.f) || !std::isfinite(a->eps) || !std::isfinite(a->rope_theta) || a->rope_theta <= 0.0)
         return false;
+    if (a->overlap != 0 && a->overlap != 1) return false;
+    if ((a->prev_C == nullptr) != (a->prev_Z == nullptr)) return false;
+    if (a->prev_C && (!a->overlap || !dev_ptr_ok(a->prev_C) || !dev_ptr_ok(a->prev_Z))) return false;
     return true;
 }
 

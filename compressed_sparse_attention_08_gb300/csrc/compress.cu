@@ -6,6 +6,12 @@
 // item 1 (the positional bias enters the logits Z + B only), and PERFORMANCE_AUDIT.md "P5"
 // (interleaved-pair RoPE of the last rope_dim channels).
 //
+// Two-stream (CSA) form, "nvfp4-megamoe-kernel: compare v0.1-e2e-working...v-c1-c2-c3-20260602",
+// compressor_reduce.cu "CSA compressor reduce kernel": the projections carry 2*dim channels,
+// entry i pools block i-1 from stream a (channels [0, dim)) and block i from stream b
+// (channels [dim, 2 dim)) under one softmax per channel; the bias has 2*dim columns, on the
+// logits only. Entry 0 reads its stream-a block from the previous-block buffer, if given.
+//
 // Design: the reduce is tiny (ratio x dim values per entry) and latency-bound, so the
 // three steps are fused in one kernel, and one launch serves up to two compressions (the
 // main KV and the indexer keys of a decode step). Each thread owns channels
@@ -35,6 +41,9 @@ constexpr int kMaxPairs = 64;        // rope_dim <= 128
 struct CompressJob {
     const __nv_bfloat16* C;
     const __nv_bfloat16* Z;
+    const __nv_bfloat16* prev_C;     // two-stream form: the block before C's first block, or null
+    const __nv_bfloat16* prev_Z;
+    int overlap;                     // 0: plain blocks; 1: two-stream (CSA) form, 2*dim channels
     const float* bias;
     const float* gamma;
     const int64_t* pos0;
@@ -63,6 +72,9 @@ compress_kernel(const __grid_constant__ CompressJob j0, const __grid_constant__ 
     const bool second = blockIdx.z != 0;
     const __nv_bfloat16* __restrict__ Cp = second ? j1.C : j0.C;
     const __nv_bfloat16* __restrict__ Zp = second ? j1.Z : j0.Z;
+    const __nv_bfloat16* __restrict__ prevCp = second ? j1.prev_C : j0.prev_C;
+    const __nv_bfloat16* __restrict__ prevZp = second ? j1.prev_Z : j0.prev_Z;
+    const int overlap = second ? j1.overlap : j0.overlap;
     const float* __restrict__ biasp = second ? j1.bias : j0.bias;
     const float* __restrict__ gammap = second ? j1.gamma : j0.gamma;
     const int64_t* pos0p = second ? j1.pos0 : j0.pos0;
@@ -91,6 +103,25 @@ compress_kernel(const __grid_constant__ CompressJob j0, const __grid_constant__ 
     const int row_base = row0p ? row0p[s] : 0;
 
     const size_t tok0 = static_cast<size_t>(s) * tokens + static_cast<size_t>(b) * ratio;
+    // channels per token row: dim, or 2*dim in the two-stream form (stream a | stream b)
+    const size_t w = overlap ? 2 * static_cast<size_t>(dim) : static_cast<size_t>(dim);
+    // stream a of this entry: the previous block's tokens (in C, or the previous-block buffer
+    // for entry 0), or none for the sequence's first block
+    const __nv_bfloat16* aC = nullptr;
+    const __nv_bfloat16* aZ = nullptr;
+    if (overlap) {
+        if (b > 0) {
+            aC = Cp + (tok0 - ratio) * w;
+            aZ = Zp + (tok0 - ratio) * w;
+        } else if (prevCp) {
+            aC = prevCp + static_cast<size_t>(s) * ratio * w;
+            aZ = prevZp + static_cast<size_t>(s) * ratio * w;
+        }
+    }
+    // this entry's own tokens: all channels (plain) or stream b (channels dim..2*dim-1)
+    const size_t own_off = overlap ? static_cast<size_t>(dim) : 0;
+    const __nv_bfloat16* oC = Cp + tok0 * w + own_off;
+    const __nv_bfloat16* oZ = Zp + tok0 * w + own_off;
     float x[kMaxChan];
     float sq = 0.f;
 #pragma unroll
@@ -99,34 +130,39 @@ compress_kernel(const __grid_constant__ CompressJob j0, const __grid_constant__ 
         x[i] = 0.f;
         if (c >= dim) continue;
         float m = -INFINITY, den = 0.f, num = 0.f;
-        for (int t0 = 0; t0 < ratio; t0 += 8) {
-            float a[8], cv[8];
+        // online softmax over one segment of `ratio` tokens (row stride w), 8 tokens at a time
+        auto segment = [&](const __nv_bfloat16* Cs, const __nv_bfloat16* Zs, const float* bs) {
+            for (int t0 = 0; t0 < ratio; t0 += 8) {
+                float a[8], cv[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int t = t0 + u;
-                if (t < ratio) {
-                    a[u] = __bfloat162float(Zp[(tok0 + t) * dim + c]) + biasp[static_cast<size_t>(t) * dim + c];
-                    cv[u] = __bfloat162float(Cp[(tok0 + t) * dim + c]);
-                } else {
-                    a[u] = -INFINITY;
-                    cv[u] = 0.f;
+                for (int u = 0; u < 8; ++u) {
+                    const int t = t0 + u;
+                    if (t < ratio) {
+                        a[u] = __bfloat162float(Zs[static_cast<size_t>(t) * w + c]) + bs[static_cast<size_t>(t) * w + c];
+                        cv[u] = __bfloat162float(Cs[static_cast<size_t>(t) * w + c]);
+                    } else {
+                        a[u] = -INFINITY;
+                        cv[u] = 0.f;
+                    }
                 }
-            }
-            float mc = a[0];
+                float mc = a[0];
 #pragma unroll
-            for (int u = 1; u < 8; ++u) mc = fmaxf(mc, a[u]);
-            const float mn = fmaxf(m, mc);
-            const float sc = m == -INFINITY ? 0.f : expf(m - mn);
-            den *= sc;
-            num *= sc;
+                for (int u = 1; u < 8; ++u) mc = fmaxf(mc, a[u]);
+                const float mn = fmaxf(m, mc);
+                const float sc = m == -INFINITY ? 0.f : expf(m - mn);
+                den *= sc;
+                num *= sc;
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const float e = a[u] == -INFINITY ? 0.f : expf(a[u] - mn);
-                den += e;
-                num = fmaf(e, cv[u], num);   // no bias on C
+                for (int u = 0; u < 8; ++u) {
+                    const float e = a[u] == -INFINITY ? 0.f : expf(a[u] - mn);
+                    den += e;
+                    num = fmaf(e, cv[u], num);   // no bias on C
+                }
+                m = mn;
             }
-            m = mn;
-        }
+        };
+        if (aC) segment(aC, aZ, biasp);                 // stream a: bias columns [0, dim)
+        segment(oC, oZ, biasp + own_off);               // own block: bias columns [dim, 2 dim) in the two-stream form
         x[i] = num / den;
         sq = fmaf(x[i], x[i], sq);
     }
@@ -170,6 +206,9 @@ CompressJob make_job(const dsv4_compress_args& a) {
     CompressJob j;
     j.C = static_cast<const __nv_bfloat16*>(a.C);
     j.Z = static_cast<const __nv_bfloat16*>(a.Z);
+    j.prev_C = static_cast<const __nv_bfloat16*>(a.prev_C);
+    j.prev_Z = static_cast<const __nv_bfloat16*>(a.prev_Z);
+    j.overlap = a.overlap;
     j.bias = a.bias;
     j.gamma = a.gamma;
     j.pos0 = a.pos0;

@@ -87,6 +87,18 @@ typedef struct dsv4_compress_args {
     int out_rows;             /* rows per sequence in `out` (>= out_row0 + tokens/ratio)  */
     float eps;                /* 1e-6 on the pages                                        */
     double rope_theta;        /* 10000 on the pages                                       */
+    /* Two-stream (CSA) form ([A] compressor_reduce.cu "CSA compressor reduce kernel", with
+     * the bias fix above): overlap = 1 makes C and Z [batch, tokens, 2*dim] (channels
+     * [0, dim) stream a, [dim, 2*dim) stream b) and bias [ratio, 2*dim]; entry b pools
+     * block b-1 from stream a and block b from stream b under one softmax per channel
+     * (2*ratio logits), the bias row t of each stream's half on the logits only. Entry 0
+     * takes its stream-a block from prev_C / prev_Z ([batch, ratio, 2*dim]) when they are
+     * given (both or neither), else pools its own block alone (the sequence's first block).
+     * RMSNorm, RoPE (at the position of the entry's own first token) and the output are as
+     * in the plain form. overlap = 0: the plain form; prev_C / prev_Z must be NULL. */
+    int overlap;
+    const void* prev_C;
+    const void* prev_Z;
 } dsv4_compress_args;
 
 int dsv4_compress(const dsv4_compress_args* args, dsv4_stream_t stream);

@@ -118,6 +118,70 @@ def test_compress_prefill_chunk():
     assert_bf16_close(got, ref, "prefill chunk entries")
 
 
+# ------------------------------------------------------------------ stage 1, two-stream (CSA) form
+def _overlap_inputs(seed, B, T, d, ratio, prev=False):
+    C = synth.normal_bf16(seed, 101, (B, T, 2 * d))
+    Z = synth.normal_bf16(seed, 102, (B, T, 2 * d))
+    bias = synth.bf16_bits_to_f32(synth.normal_bf16(seed, 103, (ratio, 2 * d), 0.0, 0.5))
+    gamma = synth.bf16_bits_to_f32(synth.normal_bf16(seed, 104, (d,), 1.0, 0.1))
+    pC = synth.normal_bf16(seed, 105, (B, ratio, 2 * d)) if prev else None
+    pZ = synth.normal_bf16(seed, 106, (B, ratio, 2 * d)) if prev else None
+    return C, Z, bias, gamma, pC, pZ
+
+
+def _gpu_compress_overlap(C, Z, bias, gamma, pos0, ratio, prev_C=None, prev_Z=None, out=None,
+                          out_row0=None, rope_dim=64):
+    m = csa()
+    B, T, w = C.shape
+    if out is None:
+        out = torch.zeros(B, T // ratio, w // 2, dtype=torch.bfloat16, device="cuda")
+    m.dsv4_compress(dev_bf16(C), dev_bf16(Z), dev(bias), dev(gamma), dev(pos0), out, ratio=ratio,
+                    rope_dim=rope_dim, out_row0=None if out_row0 is None else dev(out_row0),
+                    overlap=True, prev_C=None if prev_C is None else dev_bf16(prev_C),
+                    prev_Z=None if prev_Z is None else dev_bf16(prev_Z))
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("d", [512, 128])
+def test_compress_overlap_full_context(d):
+    """8192 tokens -> 2048 entries per sequence, the sequence's first block without stream a."""
+    B, T, r = 2, 8192, 4
+    C, Z, bias, gamma, _, _ = _overlap_inputs(1, B, T, d, r)
+    pos0 = np.zeros(B, np.int64)
+    got = host_bf16(_gpu_compress_overlap(C, Z, bias, gamma, pos0, r))
+    _, ref = oracle.compress_overlap(C, Z, bias, gamma, pos0, r)
+    assert_bf16_close(got, ref, f"two-stream compressor d={d}")
+
+
+def test_compress_overlap_newest_block_with_previous_block():
+    """Decode: the newest block (stream b) plus the block before it (stream a, from the
+    previous-block buffer) into row n_comp - 1 of a cache."""
+    B, r, d, n_rows = 4, 4, 512, 1000
+    C, Z, bias, gamma, pC, pZ = _overlap_inputs(3, B, r, d, r, prev=True)
+    pos0 = np.array([3996, 396, 1200, 8], np.int64)
+    row0 = (pos0 // r).astype(np.int32)
+    cache = torch.zeros(B, n_rows, d, dtype=torch.bfloat16, device="cuda")
+    _gpu_compress_overlap(C, Z, bias, gamma, pos0, r, pC, pZ, out=cache, out_row0=row0)
+    _, ref = oracle.compress_overlap(C, Z, bias, gamma, pos0, r, pC, pZ)
+    got = host_bf16(cache)
+    for b in range(B):
+        assert_bf16_close(got[b, row0[b]:row0[b] + 1], ref[b], f"seq {b}")
+        others = np.delete(got[b], row0[b], axis=0)
+        assert not np.any(others), f"seq {b}: rows other than the newest were written"
+
+
+def test_compress_overlap_long_blocks():
+    """ratio 16 and 40 (not multiples of the 8-token load chunk), previous block given."""
+    for r in (16, 40):
+        B, T, d = 2, 4 * r, 256
+        C, Z, bias, gamma, pC, pZ = _overlap_inputs(4 + r, B, T, d, r, prev=True)
+        pos0 = np.array([r * 9, r * 100], np.int64)
+        got = host_bf16(_gpu_compress_overlap(C, Z, bias, gamma, pos0, r, pC, pZ))
+        _, ref = oracle.compress_overlap(C, Z, bias, gamma, pos0, r, pC, pZ)
+        assert_bf16_close(got, ref, f"ratio {r}")
+
+
 # ------------------------------------------------------------------ stage 2: indexer + top-k
 def _run_indexer(q, w, keys, n_comp, top_k, ratio=4, q_pos=None, want_scores=True):
     m = csa()

@@ -107,7 +107,9 @@ def test_compress_rejects_on_host(lib):
                 batch=4, tokens=16, dim=512, ratio=4, rope_dim=64, out_rows=4, eps=1e-6,
                 rope_theta=10000.0)
     for bad in (dict(tokens=15), dict(rope_dim=63), dict(rope_dim=1024), dict(dim=2048),
-                dict(out_rows=3), dict(eps=-1.0), dict(C=None), dict(ratio=0)):
+                dict(out_rows=3), dict(eps=-1.0), dict(C=None), dict(ratio=0), dict(overlap=2),
+                dict(overlap=1, prev_C=_p(7)), dict(overlap=0, prev_C=_p(7), prev_Z=_p(8)),
+                dict(overlap=1, prev_C=_p(7), prev_Z=ctypes.c_void_p(FAKE + 4096 * 9 + 8))):
         a = CompressArgs(**{**base, **bad})
         assert lib.dsv4_compress(ctypes.byref(a), None) == 1, bad
 
