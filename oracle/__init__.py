@@ -62,6 +62,8 @@ def _bind(lib):
     lib.oracle_topk_f32.argtypes = [P, P, I, I, I, P]
     lib.oracle_sparse_attn.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I,
                                        I, D, P, P, P]
+    lib.oracle_inverse_rope.argtypes = [P, P, I, I, I, I, D, P, P]
+    lib.oracle_inverse_rope.restype = ctypes.c_int
     lib.oracle_max_comp.argtypes = [ctypes.c_int64, I]
     lib.oracle_max_comp.restype = ctypes.c_int64
     lib.oracle_visible_entries.argtypes = [ctypes.c_int64, ctypes.c_int64, I]
@@ -185,6 +187,24 @@ def sparse_attn(q, sink, comp_kv, n_comp, idx, win, win_len, top_k, window=128, 
     if rc != 0:
         raise ValueError(f"oracle_sparse_attn: bad arguments (rc={rc})")
     return out, out64, gather
+
+
+def inverse_rope(x, pos, rope_dim=64, theta=10000.0):
+    """Inverse RoPE of attention outputs.  x float64 [rows, heads, D] (any leading shape that
+    flattens to rows x heads); pos int64 [rows].  Returns (bf16 bits, float64) of x's shape."""
+    lib = _load()
+    x = np.asarray(x, np.float64)
+    shape = x.shape
+    D, H = shape[-1], shape[-2]
+    rows = int(np.prod(shape[:-2])) if len(shape) > 2 else 1
+    xf = np.ascontiguousarray(x.reshape(rows, H, D))
+    pos = _c(np.asarray(pos).reshape(rows), np.int64)
+    out = np.zeros((rows, H, D), np.uint16)
+    out64 = np.zeros((rows, H, D), np.float64)
+    rc = lib.oracle_inverse_rope(_p(xf), _p(pos), rows, H, D, rope_dim, float(theta), _p(out), _p(out64))
+    if rc != 0:
+        raise ValueError(f"oracle_inverse_rope: bad arguments (rc={rc})")
+    return out.reshape(shape), out64.reshape(shape)
 
 
 def max_comp(max_context, ratio):

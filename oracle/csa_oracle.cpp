@@ -421,4 +421,40 @@ int64_t oracle_visible_entries(int64_t n_comp, int64_t p, int ratio) {
 // bf16 rounding, exported so tests can pin it against exhaustive float checks.
 uint16_t oracle_double_to_bf16(double x) { return double_to_bf16(x); }
 
+// ---------------------------------------------------------------------------
+// Inverse RoPE on the attention output.
+//
+// [B] single_shot_inference.py eager_attention: after FMHA, "Inverse RoPE" is applied to the
+// attention output at the query positions, on the last rope_dim dims of every head. The
+// rotation is the inverse of the one the compressor applies ([A] PERFORMANCE_AUDIT.md "P5"
+// shows it: e' = e c + o s, o' = -e s + o c, pairs (even, odd), angle pos * theta^(-2j/rope_dim)).
+//
+// x [rows, heads, D] double (rows = query rows, e.g. B * n_q); pos [rows] int64.
+// out [rows, heads, D] bf16 bits (one RNE rounding); out_f64 may be null.
+int oracle_inverse_rope(const double* x, const int64_t* pos, int rows, int heads, int D,
+                        int rope_dim, double theta, uint16_t* out, double* out_f64) {
+    if (rows < 0 || heads <= 0 || D <= 0 || rope_dim < 0 || rope_dim > D || rope_dim % 2 != 0) return -1;
+    std::vector<double> v(D);
+    for (int r = 0; r < rows; ++r) {
+        for (int h = 0; h < heads; ++h) {
+            const size_t base = (static_cast<size_t>(r) * heads + h) * D;
+            for (int i = 0; i < D; ++i) v[i] = x[base + i];
+            for (int j = 0; j < rope_dim / 2; ++j) {
+                const int e0 = D - rope_dim + 2 * j;
+                const double freq = std::pow(theta, -(2.0 * j) / rope_dim);
+                const double ang = static_cast<double>(pos[r]) * freq;
+                const double cs = std::cos(ang), sn = std::sin(ang);
+                const double ev = v[e0], ov = v[e0 + 1];
+                v[e0] = ev * cs + ov * sn;
+                v[e0 + 1] = -ev * sn + ov * cs;
+            }
+            for (int i = 0; i < D; ++i) {
+                out[base + i] = double_to_bf16(v[i]);
+                if (out_f64) out_f64[base + i] = v[i];
+            }
+        }
+    }
+    return 0;
+}
+
 }  // extern "C"

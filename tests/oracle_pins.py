@@ -597,4 +597,41 @@ def pin_overlap_previous_block_pointer_matches_longer_buffer():
     _close(tail, full[:, 1:], rtol=1e-14, atol=1e-14, msg="previous-block pointer")
 
 
+# ------------------------------------------------------------------ inverse RoPE on the output
+def pin_inverse_rope_closed_form():
+    """Unit pairs rotate backwards: (1, 0) -> (cos a, -sin a) and (0, 1) -> (sin a, cos a) with
+    a = pos * theta^(-2j/rope_dim); position 0 and channels before the rope part are untouched."""
+    D, rd, H = 96, 64, 2
+    pos = np.array([0, 1, 777, 1048576], np.int64)
+    for e_first in (True, False):
+        x = np.zeros((len(pos), H, D))
+        for j in range(rd // 2):
+            x[:, :, D - rd + 2 * j + (0 if e_first else 1)] = 1.0
+        x[:, :, : D - rd] = 0.25
+        _, got = oracle.inverse_rope(x, pos, rd)
+        for r, p in enumerate(pos):
+            a = p * 10000.0 ** (-2.0 * np.arange(rd // 2) / rd)
+            want_e, want_o = (np.cos(a), -np.sin(a)) if e_first else (np.sin(a), np.cos(a))
+            # angles reach 1e6 rad: one ulp of the angle is ~1e-10 there
+            _close(got[r, :, D - rd::2], np.broadcast_to(want_e, (H, rd // 2)), 1e-9, 1e-9, "even")
+            _close(got[r, :, D - rd + 1::2], np.broadcast_to(want_o, (H, rd // 2)), 1e-9, 1e-9, "odd")
+            assert np.all(got[r, :, : D - rd] == 0.25)
+
+
+def pin_inverse_rope_undoes_the_compressor_rotation():
+    """The inverse rotation at the entry's position recovers the compressor's output before
+    RoPE (the forward rotation is pinned above)."""
+    rng = _rng(51)
+    B, r, d = 2, 4, 128
+    C = _bf(rng.standard_normal((B, 3 * r, d)))
+    Z = _bf(rng.standard_normal((B, 3 * r, d)))
+    bias = _f(_bf(0.5 * rng.standard_normal((r, d)))).astype(np.float32)
+    pos0 = np.array([12, 90000], np.int64)
+    _, rot = _compress(C, Z, bias, pos0=pos0, rope_dim=64)
+    _, plain = _compress(C, Z, bias, pos0=pos0, rope_dim=0)
+    pos = pos0[:, None] + r * np.arange(3)[None, :]
+    _, back = oracle.inverse_rope(rot.reshape(B * 3, 1, d), pos.reshape(-1), 64)
+    _close(back.reshape(B, 3, d), plain, 1e-11, 1e-11, "inverse after forward")
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

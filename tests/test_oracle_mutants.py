@@ -37,6 +37,10 @@ MUTANTS = [
      "const int64_t hi = qa + win_len[b] - n_q_total - 1;", 1),
     ("bf16_truncates", "double r = std::nearbyint(scaled);", "double r = std::trunc(scaled);", 1),
     ("max_comp_floor", "return (max_context + ratio - 1) / ratio;", "return max_context / ratio;", 1),
+    ("inverse_rope_forward_direction", "v[e0] = ev * cs + ov * sn;", "v[e0] = ev * cs - ov * sn;", 1),
+    ("inverse_rope_odd_sign", "v[e0 + 1] = -ev * sn + ov * cs;", "v[e0 + 1] = ev * sn + ov * cs;", 1),
+    ("inverse_rope_frequency", "std::pow(theta, -(2.0 * j) / rope_dim)", "std::pow(theta, -(1.0 * j) / rope_dim)", 1),
+    ("inverse_rope_first_dims", "const int e0 = D - rope_dim + 2 * j;", "const int e0 = 2 * j;", 1),
     ("overlap_a_from_own_block", "static_cast<size_t>(i - 1) * ratio + t) * w + c",
      "static_cast<size_t>(i) * ratio + t) * w + c", 1),
     ("overlap_bias_halves_swapped", "bias[static_cast<size_t>(t) * w + c]",
