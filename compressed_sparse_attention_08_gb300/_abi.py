@@ -55,7 +55,8 @@ class AttnArgs(ctypes.Structure):
     _fields_ = [("q", P), ("sink", P), ("comp_kv", P), ("n_comp", P), ("idx", P), ("q_pos", P),
                 ("win", P), ("win_len", P), ("gather", P), ("out", P), ("batch", I), ("n_q", I),
                 ("heads", I), ("dim", I), ("max_comp", I), ("top_k", I), ("window", I),
-                ("win_rows", I), ("ratio", I), ("scale", ctypes.c_float)]
+                ("win_rows", I), ("ratio", I), ("scale", ctypes.c_float), ("out_rope_pos", P),
+                ("out_rope_dim", I), ("out_rope_theta", ctypes.c_double)]
 
 
 class CsaArgs(ctypes.Structure):
@@ -184,7 +185,10 @@ def topk_args(scores, n_vis, idx_out):
 
 
 def attn_args(q, sink, comp_kv, n_comp, win, win_len, out, *, idx=None, top_k=None, window=128,
-              ratio=4, q_pos=None, gather=None, scale=None):
+              ratio=4, q_pos=None, gather=None, scale=None, out_rope_pos=None, out_rope_dim=64,
+              out_rope_theta=10000.0):
+    """out_rope_pos (int64 [B, n_q]): rotate the output's last out_rope_dim channels back at
+    these positions (inverse RoPE)."""
     bf16, f32, i32, i64 = _dt()
     B, n_q, H, D = q.shape
     max_comp = comp_kv.shape[1]
@@ -197,7 +201,8 @@ def attn_args(q, sink, comp_kv, n_comp, win, win_len, out, *, idx=None, top_k=No
                     _ptr(q_pos, i64, "q_pos", True), _ptr(win, bf16, "win"),
                     _ptr(win_len, i32, "win_len"), _ptr(gather, bf16, "gather", True),
                     _ptr(out, bf16, "out"), B, n_q, H, D, max_comp, top_k, window, win.shape[1],
-                    ratio, scale)
+                    ratio, scale, _ptr(out_rope_pos, i64, "out_rope_pos", True),
+                    out_rope_dim if out_rope_pos is not None else 0, out_rope_theta)
 
 
 # ------------------------------------------------------------------ entry points

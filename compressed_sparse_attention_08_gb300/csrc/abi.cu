@@ -83,6 +83,12 @@ bool attn_ok(const dsv4_attn_args* a) {
     if (a->idx ? a->top_k > a->max_comp : a->top_k != a->max_comp) return false;
     if (!std::isfinite(a->scale)) return false;
     if (static_cast<long long>(a->batch) * a->n_q > 65535ll) return false;   // grid.y
+    if (a->out_rope_pos) {
+        if (!opt_ptr_ok(a->out_rope_pos) || a->out_rope_dim < 2 || (a->out_rope_dim & 1) ||
+            a->out_rope_dim > a->dim || a->out_rope_dim > 128)
+            return false;
+        if (!std::isfinite(a->out_rope_theta) || a->out_rope_theta <= 0.0) return false;
+    }
     return true;
 }
 

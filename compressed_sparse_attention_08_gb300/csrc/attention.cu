@@ -25,6 +25,8 @@
 //   * a split writes (m, l, O) partials; the combine kernel merges them per (query, head)
 //     and adds the sink once: o = sum_s O_s e^(m_s-M) / (sum_s l_s e^(m_s-M) + e^(sink-M)),
 //     M = max(sink, m_s). With one split the CTA finishes the output itself.
+#include <cmath>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -48,7 +50,31 @@ struct AttnParams {
         chunks_per_split, n_splits, oob_row;
     int n_hg, hstride;             // head groups per query, heads per partial record (n_hg*HP)
     float scale;
+    const int64_t* orp;            // [rows] positions of the output's inverse RoPE, or null
+    int or_pairs;                  // rotated pairs: the last 2 * or_pairs channels
+    double or_log2_theta;          // log2(theta): pair j turns at theta^(-2j / rope_dim)
 };
+
+// Inverse RoPE of one output pair (channels c, c + 1, c even) of query row `row`: rotated back
+// by pos * f_j when the pair lies in the last 2 * or_pairs channels of a D-channel head.
+__device__ __forceinline__ void inverse_rope_pair(const AttnParams& p, int row, int c, int D,
+                                                  float& e, float& o) {
+    const int j = (c - (D - 2 * p.or_pairs)) >> 1;
+    if (!p.orp || j < 0) return;
+    const double freq = exp2(-(static_cast<double>(j) / p.or_pairs) * p.or_log2_theta);
+    float sn, cs;
+    sincosf(reduced_angle(static_cast<double>(p.orp[row]) * freq), &sn, &cs);
+    const float e0 = e, o0 = o;
+    e = e0 * cs + o0 * sn;
+    o = -e0 * sn + o0 * cs;
+}
+
+// Fills the inverse-RoPE fields of the kernel parameters from the call's arguments.
+void set_output_rope(AttnParams& p, const dsv4_attn_args& a) {
+    p.orp = a.out_rope_pos;
+    p.or_pairs = a.out_rope_pos ? a.out_rope_dim / 2 : 0;
+    p.or_log2_theta = a.out_rope_pos ? std::log2(a.out_rope_theta) : 0.0;
+}
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t* r) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -174,7 +200,6 @@ __global__ void __launch_bounds__(kNT, 1)
 attn_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap gmap,
             AttnParams p) {
     using C = Cfg<D, HP>;
-    constexpr int CPR = D / 8;                             // 16-byte chunks per row
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* sm = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -412,7 +437,9 @@ attn_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CU
 #pragma unroll
             for (int i = 0; i < C::DW / 8; ++i) {
                 const int d = C::DW * dg + 8 * i + 2 * tq;
-                *reinterpret_cast<uint32_t*>(dst + d) = pack_bf16(o[i][2 * half] * f, o[i][2 * half + 1] * f);
+                float e0 = o[i][2 * half] * f, o0 = o[i][2 * half + 1] * f;
+                inverse_rope_pair(p, row, d, D, e0, o0);
+                *reinterpret_cast<uint32_t*>(dst + d) = pack_bf16(e0, o0);
             }
         }
     } else {
@@ -506,11 +533,21 @@ attn_combine_kernel(AttnParams p) {
     }
     __nv_bfloat16* dst = p.out + (static_cast<size_t>(row) * p.H + h) * D + tid * PER;
 #pragma unroll
-    for (int j = 0; j < PER; j += 2) {
-        if constexpr (PER == 1) {
-            *dst = __float2bfloat16_rn(acc[0] * inv);
-        } else {
-            *reinterpret_cast<uint32_t*>(dst + j) = pack_bf16(acc[j] * inv, acc[j + 1] * inv);
+    for (int j = 0; j < PER; ++j) acc[j] *= inv;
+    if constexpr (PER == 1) {
+        // one channel per thread: the pair partner is the neighbouring lane
+        const float partner = __shfl_xor_sync(0xffffffffu, acc[0], 1);
+        if (p.orp) {
+            float e = (tid & 1) ? partner : acc[0], o = (tid & 1) ? acc[0] : partner;
+            inverse_rope_pair(p, row, tid & ~1, D, e, o);
+            acc[0] = (tid & 1) ? o : e;
+        }
+        *dst = __float2bfloat16_rn(acc[0]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < PER; j += 2) {
+            inverse_rope_pair(p, row, tid * PER + j, D, acc[j], acc[j + 1]);
+            *reinterpret_cast<uint32_t*>(dst + j) = pack_bf16(acc[j], acc[j + 1]);
         }
     }
 }
@@ -834,6 +871,7 @@ int run_decode(const dsv4_attn_args& a, const DecodePlan& dp, uint8_t* ws, uint3
     p.n_hg = dp.n_hg;
     p.hstride = static_cast<int>(hs);
     p.scale = a.scale;
+    set_output_rope(p, a);
     p.part_ml = reinterpret_cast<float*>(ws);
     p.part_o = reinterpret_cast<float*>(ws + ml_b);
     static bool attr_set = false;
@@ -916,6 +954,7 @@ int run(const dsv4_attn_args& a, const Plan& pl, uint8_t* ws, uint32_t* eword, c
     p.n_hg = pl.n_hg;
     p.hstride = pl.n_hg * HP;
     p.scale = a.scale;
+    set_output_rope(p, a);
     p.part_ml = reinterpret_cast<float*>(ws);
     p.part_o = reinterpret_cast<float*>(ws + ml_b);
     static bool attr_set = false;

@@ -214,6 +214,18 @@ __device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t
     return d;
 }
 
+// RoPE angle pos * f, formed in fp64 and reduced to [-pi, pi] with a two-constant Cody-Waite
+// reduction using fused multiply-adds (W. J. Cody and W. Waite, "Software Manual for the
+// Elementary Functions", 1980); 2*pi = hi + lo to double precision. The reduced angle is
+// small enough for the fp32 sincos.
+__device__ __forceinline__ float reduced_angle(double ang) {
+    constexpr double kTwoPiHi = 6.283185307179586, kTwoPiLo = 2.4492935982947064e-16;
+    const double k = rint(ang * (1.0 / kTwoPiHi));
+    double r = fma(-k, kTwoPiHi, ang);
+    r = fma(-k, kTwoPiLo, r);
+    return static_cast<float>(r);
+}
+
 // Instruction descriptor for kind::f16 with bf16 A/B, fp32 D, both operands K-major.
 // Bits: [4,6) D format (1 = f32), [7,10) A format (1 = bf16), [10,13) B format (1 = bf16),
 // [15] A major (0 = K), [16] B major (0 = K), [17,23) N >> 3, [24,29) M >> 4.

@@ -204,6 +204,14 @@ typedef struct dsv4_attn_args {
     int batch, n_q, heads, dim, max_comp, top_k, window, win_rows, ratio;
                               /* heads: 1..16, or a multiple of 16 up to 64; dim: 128/256/512 */
     float scale;              /* 1/sqrt(dim) on the pages                                   */
+    /* Optional inverse RoPE of the output ([B] single_shot_inference.py eager_attention: the
+     * FMHA output is rotated back at the query positions): when out_rope_pos (int64
+     * [batch, n_q]) is given, the last out_rope_dim channels of every head's output are
+     * rotated in pairs (2j, 2j+1) by -pos * out_rope_theta^(-2j/out_rope_dim) before the bf16
+     * rounding. NULL: the output is not rotated. */
+    const int64_t* out_rope_pos;
+    int out_rope_dim;         /* even, 2..min(dim, 128) when out_rope_pos is given          */
+    double out_rope_theta;    /* 10000 on the pages                                         */
 } dsv4_attn_args;
 
 size_t dsv4_sparse_attn_workspace_size(const dsv4_attn_args* args);

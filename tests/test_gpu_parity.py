@@ -318,7 +318,7 @@ def test_topk_exact_with_planted_ties(max_comp, k):
 
 
 # ------------------------------------------------------------------ stage 4: gather + attention
-def _run_attn(x, wl, idx, want_gather=True, top_k=None):
+def _run_attn(x, wl, idx, want_gather=True, top_k=None, out_rope_pos=None):
     m = csa()
     q, sink = dev_bf16(x["q"]), dev(x["sink"])
     kv = dev_bf16(x["comp_kv_dev"])
@@ -329,6 +329,8 @@ def _run_attn(x, wl, idx, want_gather=True, top_k=None):
     gather = torch.full((B, n_q, top_k + wl.window, D), 7.0, dtype=torch.bfloat16, device="cuda") if want_gather else None
     kw = dict(idx=None if idx is None else dev(idx), top_k=top_k, window=wl.window, ratio=wl.ratio,
               q_pos=None if x.get("q_pos") is None else dev(x["q_pos"]), gather=gather)
+    if out_rope_pos is not None:
+        kw["out_rope_pos"] = dev(np.ascontiguousarray(out_rope_pos, np.int64))
     ws = ws_tensor(m.dsv4_sparse_attn_workspace_size(q, sink, kv, n_comp, win, win_len, out, **kw))
     m.dsv4_sparse_attn_decode(q, sink, kv, n_comp, win, win_len, out, ws, **kw)
     torch.cuda.synchronize()
@@ -386,6 +388,40 @@ def test_prefill_attention_sampled_queries():
                                    wl.ratio, q_pos=x["q_pos"][:, sample], q_abs=sample,
                                    n_q_total=2048)
     assert_bf16_close(got[:, sample], ref, "prefill attention")
+
+
+@pytest.mark.parametrize("cfg", [0, 1])
+def test_attention_output_inverse_rope(cfg):
+    """The output rotated back at the query positions (64 rope dims): decode with D = 128
+    (pairs split across neighbouring threads) and D = 512; positions up to 2^20."""
+    wl, x = _attn_case(cfg)
+    B = wl.batch
+    idx = synth.uniform_index_sets(wl.seed, 17, B, x["n_comp"], wl.top_k).reshape(B, 1, wl.top_k)
+    pos = (np.array([1048575, 8192, 123457, 3, 0, 65536, 777, 4095, 1, 2, 9, 99, 999, 9999, 99999, 524288],
+                    np.int64)[:B]).reshape(B, 1)
+    got, _, ew = _run_attn(x, wl, idx, want_gather=False, out_rope_pos=pos)
+    assert ew == 0
+    seqs = list(range(B)) if B <= 4 else [0, 5, 15]
+    _, ref, _ = oracle.sparse_attn(x["q"][seqs], x["sink"], x["comp_kv_dev"][seqs], x["n_comp"][seqs],
+                                   idx[seqs], x["win"][seqs], x["win_len"][seqs], wl.top_k, wl.window,
+                                   wl.ratio)
+    _, ref_rot = oracle.inverse_rope(ref, pos[seqs].reshape(-1), 64)
+    assert_bf16_close(got[seqs], ref_rot, f"cfg{cfg} attention + inverse RoPE")
+
+
+def test_prefill_attention_inverse_rope_sampled_queries():
+    wl, x = _attn_case(4)
+    nvis = np.array([16384 + (t + 1) // 4 for t in range(2048)], np.int32)
+    idx = synth.uniform_index_sets(4, 17, 2048, nvis, wl.top_k).reshape(1, 2048, wl.top_k)
+    got, _, ew = _run_attn(x, wl, idx, want_gather=False, out_rope_pos=x["q_pos"])
+    assert ew == 0
+    sample = np.array([0, 127, 1000, 2047], np.int32)
+    _, ref, _ = oracle.sparse_attn(x["q"][:, sample], x["sink"], x["comp_kv_dev"], x["n_comp"],
+                                   idx[:, sample], x["win"], x["win_len"], wl.top_k, wl.window,
+                                   wl.ratio, q_pos=x["q_pos"][:, sample], q_abs=sample,
+                                   n_q_total=2048)
+    _, ref_rot = oracle.inverse_rope(ref, x["q_pos"][0, sample], 64)
+    assert_bf16_close(got[:, sample], ref_rot, "prefill attention + inverse RoPE")
 
 
 def test_attention_edge_cases_and_bad_index():

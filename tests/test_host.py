@@ -94,6 +94,9 @@ def test_indexer_rejects_small_workspace(lib):
     dict(dim=100), dict(heads=0), dict(heads=65), dict(idx=None),   # dense needs top_k == max_comp
     dict(top_k=262145), dict(win_rows=0), dict(scale=float("inf")), dict(out=None),
     dict(gather=ctypes.c_void_p(FAKE + 4)),
+    dict(out_rope_pos=_p(11), out_rope_dim=0), dict(out_rope_pos=_p(11), out_rope_dim=63),
+    dict(out_rope_pos=_p(11), out_rope_dim=256), dict(out_rope_pos=_p(11), out_rope_dim=64, out_rope_theta=0.0),
+    dict(out_rope_pos=ctypes.c_void_p(FAKE + 4096 * 11 + 4), out_rope_dim=64, out_rope_theta=1e4),
 ])
 def test_attention_rejects_on_host(lib, bad):
     a = _attn_args(**bad)
