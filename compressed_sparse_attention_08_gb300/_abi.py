@@ -22,7 +22,7 @@ DSV4_EWORD_BAD_INDEX = 0x1
 DSV4_EWORD_TIMEOUT = 0x2
 
 EXPORTED_SYMBOLS = (
-    "dsv4_compress", "dsv4_indexer_topk_workspace_size", "dsv4_indexer_topk",
+    "dsv4_compress", "dsv4_compress_step", "dsv4_indexer_topk_workspace_size", "dsv4_indexer_topk",
     "dsv4_index_score_workspace_size", "dsv4_index_score",
     "dsv4_topk_workspace_size", "dsv4_topk", "dsv4_topk_noalloc", "dsv4_sparse_attn_workspace_size",
     "dsv4_sparse_attn_decode", "dsv4_csa_decode_workspace_size", "dsv4_csa_decode",
@@ -38,6 +38,13 @@ class CompressArgs(ctypes.Structure):
                 ("out_row0", P), ("batch", I), ("tokens", I), ("dim", I), ("ratio", I),
                 ("rope_dim", I), ("out_rows", I), ("eps", ctypes.c_float),
                 ("rope_theta", ctypes.c_double), ("overlap", I), ("prev_C", P), ("prev_Z", P)]
+
+
+class StepArgs(ctypes.Structure):
+    _fields_ = [("C", P), ("Z", P), ("bias", P), ("gamma", P), ("pos", P), ("stage", P),
+                ("fill", P), ("n_comp", P), ("out", P), ("batch", I), ("dim", I), ("ratio", I),
+                ("rope_dim", I), ("out_rows", I), ("overlap", I), ("eps", ctypes.c_float),
+                ("rope_theta", ctypes.c_double)]
 
 
 class IndexArgs(ctypes.Structure):
@@ -88,6 +95,7 @@ def library():
                                "`python -m compressed_sparse_attention_08_gb300._build`")
         lib = ctypes.CDLL(path)
         lib.dsv4_compress.argtypes = [ctypes.POINTER(CompressArgs), P]
+        lib.dsv4_compress_step.argtypes = [ctypes.POINTER(StepArgs), P]
         lib.dsv4_indexer_topk_workspace_size.argtypes = [ctypes.POINTER(IndexArgs)]
         lib.dsv4_indexer_topk_workspace_size.restype = ctypes.c_size_t
         lib.dsv4_indexer_topk.argtypes = [ctypes.POINTER(IndexArgs), P, ctypes.c_size_t, P]
@@ -213,6 +221,30 @@ def dsv4_compress(C, Z, bias, gamma, pos0, out, *, ratio, rope_dim=64, eps=1e-6,
                       rope_theta=rope_theta, out_row0=out_row0, overlap=overlap, prev_C=prev_C,
                       prev_Z=prev_Z)
     _check(library().dsv4_compress(ctypes.byref(a), _stream(stream)), "dsv4_compress")
+
+
+def compress_step_state(batch, dim, ratio, *, overlap=False, device="cuda"):
+    """Zeroed state for dsv4_compress_step: (stage, fill, n_comp)."""
+    import torch
+    w = 2 * dim if overlap else dim
+    return (torch.zeros(batch, 2, 2, ratio, w, dtype=torch.bfloat16, device=device),
+            torch.zeros(batch, dtype=torch.int32, device=device),
+            torch.zeros(batch, dtype=torch.int32, device=device))
+
+
+def dsv4_compress_step(C, Z, bias, gamma, pos, stage, fill, n_comp, out, *, ratio, rope_dim=64,
+                       eps=1e-6, rope_theta=10000.0, overlap=False, stream=None):
+    """One decode token per sequence: C, Z [B, w] (w = dim, or 2*dim two-stream); pos int64 [B];
+    state stage / fill / n_comp (see compress_step_state) updated on the device; a completed
+    block goes to out[s, n_comp[s]]."""
+    bf16, f32, i32, i64 = _dt()
+    B, w = C.shape
+    d = out.shape[2]
+    a = StepArgs(_ptr(C, bf16, "C"), _ptr(Z, bf16, "Z"), _ptr(bias, f32, "bias"), _ptr(gamma, f32, "gamma"),
+                 _ptr(pos, i64, "pos"), _ptr(stage, bf16, "stage"), _ptr(fill, i32, "fill"),
+                 _ptr(n_comp, i32, "n_comp"), _ptr(out, bf16, "out"), B, d, ratio, rope_dim,
+                 out.shape[1], 1 if overlap else 0, eps, rope_theta)
+    _check(library().dsv4_compress_step(ctypes.byref(a), _stream(stream)), "dsv4_compress_step")
 
 
 def dsv4_indexer_topk_workspace_size(q, w, keys, n_comp, idx_out, *, ratio, q_pos=None,

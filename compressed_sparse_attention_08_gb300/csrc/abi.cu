@@ -159,6 +159,23 @@ int dsv4_compress(const dsv4_compress_args* a, dsv4_stream_t stream) {
     return launch_compress(*a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int dsv4_compress_step(const dsv4_compress_step_args* a, dsv4_stream_t stream) {
+    LaunchScope scope;
+    if (!a || !dev_ptr_ok(a->C) || !dev_ptr_ok(a->Z) || !dev_ptr_ok(a->bias) || !dev_ptr_ok(a->gamma) ||
+        !dev_ptr_ok(a->pos) || !dev_ptr_ok(a->stage) || !dev_ptr_ok(a->fill) || !dev_ptr_ok(a->n_comp) ||
+        !dev_ptr_ok(a->out))
+        return DSV4_ERR_INVALID_ARG;
+    if (a->batch < 0 || a->batch > 65535 || a->ratio < 1 || a->dim < 2 || a->dim > 1024 || a->out_rows < 1)
+        return DSV4_ERR_INVALID_ARG;
+    if (a->overlap != 0 && a->overlap != 1) return DSV4_ERR_INVALID_ARG;
+    if (a->rope_dim < 0 || a->rope_dim > a->dim || a->rope_dim > 128 || (a->rope_dim & 1))
+        return DSV4_ERR_INVALID_ARG;
+    if (!(a->eps >= 0.f) || !std::isfinite(a->eps) || !std::isfinite(a->rope_theta) || a->rope_theta <= 0.0)
+        return DSV4_ERR_INVALID_ARG;
+    if (int rc = device_check()) return rc;
+    return launch_compress_step(*a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 size_t dsv4_indexer_topk_workspace_size(const dsv4_index_args* a) {
     if (!a) return 0;
     return kWsHeader + index_ws_bytes(*a);

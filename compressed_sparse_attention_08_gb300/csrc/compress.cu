@@ -51,9 +51,108 @@ struct CompressJob {
     const int32_t* out_row0;
     int batch, tokens, dim, ratio, rope_dim, out_rows, n_blocks;
     float eps;
-    double two_pi_hi, two_pi_lo, inv_two_pi;
     double freq[kMaxPairs];
 };
+
+// One compressed entry: the pooled tokens are `ratio` rows of the own block (channels
+// own_off .. own_off + dim - 1 of rows oC/oZ, bias columns own_off..) and, in the two-stream
+// form, `ratio` rows of the previous block's stream a (channels 0..dim-1 of aC/aZ, bias
+// columns 0..), consecutive tokens `w` elements apart.
+struct EntryIn {
+    const __nv_bfloat16* aC;     // stream a (null: none)
+    const __nv_bfloat16* aZ;
+    const __nv_bfloat16* oC;     // own block, row 0, channel 0 of the row
+    const __nv_bfloat16* oZ;
+    size_t w, own_off;
+    const float* bias;           // [ratio, w]
+    const float* gamma;          // [dim]
+    int dim, ratio, rope_dim;
+    float eps;
+    double pos;                  // RoPE position of the entry
+    __nv_bfloat16* dst;          // the entry's output row, or null (computed, not stored)
+};
+
+// The whole CTA (kThreads) computes one entry: per-channel online softmax of Z + bias over the
+// pooled tokens and the weighted sum of C in fp32, RMSNorm over the dim channels, RoPE of the
+// last rope_dim channels with the angle formed in fp64 and Cody-Waite reduced, one bf16
+// rounding. freq: the rope frequencies in shared memory (already visible to the CTA).
+__device__ void entry_math(const EntryIn& in, const double* freq, float* y, float* warp_sum) {
+    const int tid = threadIdx.x;
+    const int dim = in.dim, ratio = in.ratio;
+    const size_t w = in.w;
+    float x[kMaxChan];
+    float sq = 0.f;
+#pragma unroll
+    for (int i = 0; i < kMaxChan; ++i) {
+        const int c = tid + i * kThreads;
+        x[i] = 0.f;
+        if (c >= dim) continue;
+        float m = -INFINITY, den = 0.f, num = 0.f;
+        // online softmax over one segment of `ratio` tokens, 8 tokens at a time with all loads
+        // of a chunk issued before any is used
+        auto segment = [&](const __nv_bfloat16* Cs, const __nv_bfloat16* Zs, const float* bs) {
+            for (int t0 = 0; t0 < ratio; t0 += 8) {
+                float a[8], cv[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int t = t0 + u;
+                    if (t < ratio) {
+                        a[u] = __bfloat162float(Zs[static_cast<size_t>(t) * w + c]) + bs[static_cast<size_t>(t) * w + c];
+                        cv[u] = __bfloat162float(Cs[static_cast<size_t>(t) * w + c]);
+                    } else {
+                        a[u] = -INFINITY;
+                        cv[u] = 0.f;
+                    }
+                }
+                float mc = a[0];
+#pragma unroll
+                for (int u = 1; u < 8; ++u) mc = fmaxf(mc, a[u]);
+                const float mn = fmaxf(m, mc);
+                const float sc = m == -INFINITY ? 0.f : expf(m - mn);
+                den *= sc;
+                num *= sc;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const float e = a[u] == -INFINITY ? 0.f : expf(a[u] - mn);
+                    den += e;
+                    num = fmaf(e, cv[u], num);   // no bias on C
+                }
+                m = mn;
+            }
+        };
+        if (in.aC) segment(in.aC, in.aZ, in.bias);          // stream a: bias columns [0, dim)
+        segment(in.oC + in.own_off, in.oZ + in.own_off, in.bias + in.own_off);
+        x[i] = num / den;
+        sq = fmaf(x[i], x[i], sq);
+    }
+    // RMSNorm: mean of x^2 over all dim channels
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+    if ((tid & 31) == 0) warp_sum[tid >> 5] = sq;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int k = 0; k < kThreads / 32; ++k) tot += warp_sum[k];
+    const float inv = 1.0f / sqrtf(tot / static_cast<float>(dim) + in.eps);
+#pragma unroll
+    for (int i = 0; i < kMaxChan; ++i) {
+        const int c = tid + i * kThreads;
+        if (c < dim) y[c] = x[i] * inv * in.gamma[c];
+    }
+    __syncthreads();
+    // RoPE: pair p rotates channels (d0, d0 + 1), d0 = dim - rope_dim + 2p, by pos * f_p
+    for (int p = tid; p < in.rope_dim / 2; p += kThreads) {
+        const int d0 = dim - in.rope_dim + 2 * p;
+        float sn, cs;
+        sincosf(reduced_angle(in.pos * freq[p]), &sn, &cs);
+        const float e = y[d0], o = y[d0 + 1];
+        y[d0] = e * cs - o * sn;
+        y[d0 + 1] = e * sn + o * cs;
+    }
+    __syncthreads();
+    if (in.dst)
+        for (int c = tid; c < dim; c += kThreads) in.dst[c] = __float2bfloat16_rn(y[c]);
+}
 
 // zero_p/zero_n16: a workspace region (16-byte words) this launch clears for the kernels after
 // it (the fused decode step), so the step needs no separate memset; they read it only after
@@ -88,7 +187,6 @@ compress_kernel(const __grid_constant__ CompressJob j0, const __grid_constant__ 
     const int out_rows = second ? j1.out_rows : j0.out_rows;
     const int n_blocks = second ? j1.n_blocks : j0.n_blocks;
     const float eps = second ? j1.eps : j0.eps;
-    const double two_pi_hi = j0.two_pi_hi, two_pi_lo = j0.two_pi_lo, inv_two_pi = j0.inv_two_pi;
     const int b = blockIdx.x;          // block (entry) within the sequence
     const int s = blockIdx.y;          // sequence
     const int tid = threadIdx.x;
@@ -118,88 +216,24 @@ compress_kernel(const __grid_constant__ CompressJob j0, const __grid_constant__ 
             aZ = prevZp + static_cast<size_t>(s) * ratio * w;
         }
     }
-    // this entry's own tokens: all channels (plain) or stream b (channels dim..2*dim-1)
-    const size_t own_off = overlap ? static_cast<size_t>(dim) : 0;
-    const __nv_bfloat16* oC = Cp + tok0 * w + own_off;
-    const __nv_bfloat16* oZ = Zp + tok0 * w + own_off;
-    float x[kMaxChan];
-    float sq = 0.f;
-#pragma unroll
-    for (int i = 0; i < kMaxChan; ++i) {
-        const int c = tid + i * kThreads;
-        x[i] = 0.f;
-        if (c >= dim) continue;
-        float m = -INFINITY, den = 0.f, num = 0.f;
-        // online softmax over one segment of `ratio` tokens (row stride w), 8 tokens at a time
-        auto segment = [&](const __nv_bfloat16* Cs, const __nv_bfloat16* Zs, const float* bs) {
-            for (int t0 = 0; t0 < ratio; t0 += 8) {
-                float a[8], cv[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int t = t0 + u;
-                    if (t < ratio) {
-                        a[u] = __bfloat162float(Zs[static_cast<size_t>(t) * w + c]) + bs[static_cast<size_t>(t) * w + c];
-                        cv[u] = __bfloat162float(Cs[static_cast<size_t>(t) * w + c]);
-                    } else {
-                        a[u] = -INFINITY;
-                        cv[u] = 0.f;
-                    }
-                }
-                float mc = a[0];
-#pragma unroll
-                for (int u = 1; u < 8; ++u) mc = fmaxf(mc, a[u]);
-                const float mn = fmaxf(m, mc);
-                const float sc = m == -INFINITY ? 0.f : expf(m - mn);
-                den *= sc;
-                num *= sc;
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const float e = a[u] == -INFINITY ? 0.f : expf(a[u] - mn);
-                    den += e;
-                    num = fmaf(e, cv[u], num);   // no bias on C
-                }
-                m = mn;
-            }
-        };
-        if (aC) segment(aC, aZ, biasp);                 // stream a: bias columns [0, dim)
-        segment(oC, oZ, biasp + own_off);               // own block: bias columns [dim, 2 dim) in the two-stream form
-        x[i] = num / den;
-        sq = fmaf(x[i], x[i], sq);
-    }
-    // RMSNorm: mean of x^2 over all dim channels
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-    if ((tid & 31) == 0) warp_sum[tid >> 5] = sq;
-    __syncthreads();
-    float tot = 0.f;
-#pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) tot += warp_sum[w];
-    const float inv = 1.0f / sqrtf(tot / static_cast<float>(dim) + eps);
-#pragma unroll
-    for (int i = 0; i < kMaxChan; ++i) {
-        const int c = tid + i * kThreads;
-        if (c < dim) y[c] = x[i] * inv * gammap[c];
-    }
-    __syncthreads();
-    // RoPE: pair p rotates channels (d0, d0 + 1), d0 = dim - rope_dim + 2p, by pos * f_p
-    const double pos = static_cast<double>(pos_s + static_cast<int64_t>(b) * ratio);
-    for (int p = tid; p < rope_dim / 2; p += kThreads) {
-        const int d0 = dim - rope_dim + 2 * p;
-        const double ang = pos * freq[p];
-        const double kq = rint(ang * inv_two_pi);
-        double r = fma(-kq, two_pi_hi, ang);
-        r = fma(-kq, two_pi_lo, r);
-        float sn, cs;
-        sincosf(static_cast<float>(r), &sn, &cs);
-        const float e = y[d0], o = y[d0 + 1];
-        y[d0] = e * cs - o * sn;
-        y[d0 + 1] = e * sn + o * cs;
-    }
-    __syncthreads();
     const int row = row_base + b;
-    if (row < 0 || row >= out_rows) return;     // rows outside the destination are not written
-    __nv_bfloat16* dst = outp + (static_cast<size_t>(s) * out_rows + row) * dim;
-    for (int c = tid; c < dim; c += kThreads) dst[c] = __float2bfloat16_rn(y[c]);
+    EntryIn in;
+    in.aC = aC;
+    in.aZ = aZ;
+    in.oC = Cp + tok0 * w;
+    in.oZ = Zp + tok0 * w;
+    in.w = w;
+    in.own_off = overlap ? static_cast<size_t>(dim) : 0;
+    in.bias = biasp;
+    in.gamma = gammap;
+    in.dim = dim;
+    in.ratio = ratio;
+    in.rope_dim = rope_dim;
+    in.eps = eps;
+    in.pos = static_cast<double>(pos_s + static_cast<int64_t>(b) * ratio);
+    // rows outside the destination are not written
+    in.dst = row >= 0 && row < out_rows ? outp + (static_cast<size_t>(s) * out_rows + row) * dim : nullptr;
+    entry_math(in, freq, y, warp_sum);
 }
 
 CompressJob make_job(const dsv4_compress_args& a) {
@@ -222,14 +256,82 @@ CompressJob make_job(const dsv4_compress_args& a) {
     j.out_rows = a.out_rows;
     j.n_blocks = a.tokens / a.ratio;
     j.eps = a.eps;
-    // 2*pi as an unevaluated sum hi + lo of two doubles; lo = 2*pi - hi to double precision
-    // (2*pi = 6.28318530717958647692528676655900576839...).
-    j.two_pi_hi = 6.283185307179586;
-    j.two_pi_lo = 2.4492935982947064e-16;
-    j.inv_two_pi = 1.0 / j.two_pi_hi;
     for (int p = 0; p < kMaxPairs; ++p)
         j.freq[p] = p < a.rope_dim / 2 ? std::pow(a.rope_theta, -2.0 * p / a.rope_dim) : 0.0;
     return j;
+}
+
+// ------------------------------------------------------------------ decode-time step
+// One token per sequence per call. The token is staged; when it completes a block, the block
+// is compressed into cache row n_comp and n_comp is bumped, all on the device, so every decode
+// step runs the same launch (one captured graph serves them all).
+// State per sequence s (caller-owned, zero at the start of a sequence): stage
+// [2 blocks (0: in progress, 1: the previous block)][2 (C, Z)][ratio][w] bf16, fill[s] tokens of
+// the block in progress, n_comp[s] entries written.
+struct StepJob {
+    const __nv_bfloat16* C;      // [batch, w] this step's token
+    const __nv_bfloat16* Z;
+    const float* bias;           // [ratio, w]
+    const float* gamma;          // [dim]
+    const int64_t* pos;          // [batch] the token's position
+    __nv_bfloat16* stage;        // [batch, 2, 2, ratio, w]
+    int32_t* fill;               // [batch]
+    int32_t* n_comp;             // [batch]
+    __nv_bfloat16* out;          // [batch, out_rows, dim]
+    int batch, dim, ratio, rope_dim, out_rows, overlap;
+    float eps;
+    double log2_theta;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+compress_step_kernel(const __grid_constant__ StepJob j) {
+    __shared__ float y[1024];
+    __shared__ float warp_sum[kThreads / 32];
+    __shared__ double freq[kMaxPairs];
+    const int s = blockIdx.x, tid = threadIdx.x;
+    if (s >= j.batch) return;
+    const size_t w = j.overlap ? 2 * static_cast<size_t>(j.dim) : static_cast<size_t>(j.dim);
+    const size_t blk = 2 * static_cast<size_t>(j.ratio) * w;          // one staged block (C and Z)
+    __nv_bfloat16* cur = j.stage + static_cast<size_t>(s) * 2 * blk;  // C rows, then Z rows
+    __nv_bfloat16* prev = cur + blk;
+    int f = j.fill[s];
+    if (f < 0 || f >= j.ratio) f = 0;              // not a valid state: restart the block
+    for (size_t c = tid; c < w; c += kThreads) {
+        cur[static_cast<size_t>(f) * w + c] = j.C[static_cast<size_t>(s) * w + c];
+        cur[(static_cast<size_t>(j.ratio) + f) * w + c] = j.Z[static_cast<size_t>(s) * w + c];
+    }
+    __syncthreads();                               // the staged token is visible to the CTA
+    if (f + 1 < j.ratio) {
+        if (tid == 0) j.fill[s] = f + 1;
+        return;
+    }
+    const int nc = j.n_comp[s];
+    if (tid < kMaxPairs)
+        freq[tid] = tid < j.rope_dim / 2 ? exp2(-(2.0 * tid / j.rope_dim) * j.log2_theta) : 0.0;
+    __syncthreads();
+    EntryIn in;
+    in.aC = j.overlap && nc > 0 ? prev : nullptr;  // the sequence's first entry has no stream a
+    in.aZ = prev + static_cast<size_t>(j.ratio) * w;
+    in.oC = cur;
+    in.oZ = cur + static_cast<size_t>(j.ratio) * w;
+    in.w = w;
+    in.own_off = j.overlap ? static_cast<size_t>(j.dim) : 0;
+    in.bias = j.bias;
+    in.gamma = j.gamma;
+    in.dim = j.dim;
+    in.ratio = j.ratio;
+    in.rope_dim = j.rope_dim;
+    in.eps = j.eps;
+    in.pos = static_cast<double>(j.pos[s] - (j.ratio - 1));   // the block's first token
+    // a full cache keeps its rows: the entry is computed but not stored, n_comp stays
+    in.dst = nc >= 0 && nc < j.out_rows ? j.out + (static_cast<size_t>(s) * j.out_rows + nc) * j.dim : nullptr;
+    entry_math(in, freq, y, warp_sum);
+    if (j.overlap)                                 // this block is stream a of the next entry
+        for (size_t c = tid; c < blk; c += kThreads) prev[c] = cur[c];
+    if (tid == 0) {
+        j.fill[s] = 0;
+        if (in.dst) j.n_comp[s] = nc + 1;
+    }
 }
 
 }  // namespace
@@ -257,6 +359,31 @@ int launch_compress2(const dsv4_compress_args* a, const dsv4_compress_args* b, c
 
 int launch_compress(const dsv4_compress_args& a, cudaStream_t stream) {
     return launch_compress2(&a, nullptr, stream, nullptr, 0);
+}
+
+int launch_compress_step(const dsv4_compress_step_args& a, cudaStream_t stream) {
+    if (a.batch == 0) return DSV4_OK;
+    StepJob j;
+    j.C = static_cast<const __nv_bfloat16*>(a.C);
+    j.Z = static_cast<const __nv_bfloat16*>(a.Z);
+    j.bias = a.bias;
+    j.gamma = a.gamma;
+    j.pos = a.pos;
+    j.stage = static_cast<__nv_bfloat16*>(a.stage);
+    j.fill = a.fill;
+    j.n_comp = a.n_comp;
+    j.out = static_cast<__nv_bfloat16*>(a.out);
+    j.batch = a.batch;
+    j.dim = a.dim;
+    j.ratio = a.ratio;
+    j.rope_dim = a.rope_dim;
+    j.out_rows = a.out_rows;
+    j.overlap = a.overlap;
+    j.eps = a.eps;
+    j.log2_theta = std::log2(a.rope_theta);
+    count_launch();
+    return launch_k(compress_step_kernel, dim3(a.batch), dim3(kThreads), 0, stream, false, j) == cudaSuccess
+               ? DSV4_OK : DSV4_ERR_LAUNCH;
 }
 
 }  // namespace dsv4

@@ -103,6 +103,36 @@ typedef struct dsv4_compress_args {
 
 int dsv4_compress(const dsv4_compress_args* args, dsv4_stream_t stream);
 
+/* Stage 1 at decode time, one token per call: the compressor's state lives on the device, so
+ * every decode step issues the same call (one captured CUDA graph serves them all) and no host
+ * code has to know when a block completes ([C] GETTING+CUDAGRAPH_READY.md "SECTION C": the
+ * compressor's host-side decisions are what keeps the step out of a graph; [A] commit "C1"
+ * fixes the cache rows).
+ *
+ * Per sequence s the call stages this token's C and Z; when the staged block holds `ratio`
+ * tokens it is compressed exactly as dsv4_compress would compress it (plain or two-stream form,
+ * RMSNorm, RoPE at the block's first token, pos[s] - ratio + 1) into out[s, n_comp[s]], then
+ * n_comp[s] is incremented and fill[s] reset. In the two-stream form the completed block is
+ * kept as stream a of the next entry; the sequence's first entry (n_comp[s] == 0 when it
+ * completes) has stream b only. When n_comp[s] == out_rows the entry is not stored and n_comp
+ * stays. State (caller-owned, device): stage, fill and n_comp, all zero at the start of a
+ * sequence (or fill zero and n_comp the cache rows already written, at a block boundary). */
+typedef struct dsv4_compress_step_args {
+    const void* C;            /* bf16 [batch, w]  this step's token, w = dim (plain) or 2*dim   */
+    const void* Z;            /* bf16 [batch, w]                                                */
+    const float* bias;        /* fp32 [ratio, w]                                                */
+    const float* gamma;       /* fp32 [dim]                                                     */
+    const int64_t* pos;       /* int64 [batch] position of this token                           */
+    void* stage;              /* bf16 [batch, 2, 2, ratio, w] state                              */
+    int32_t* fill;            /* int32 [batch] state: tokens of the block in progress           */
+    int32_t* n_comp;          /* int32 [batch] state: entries written to `out`                  */
+    void* out;                /* bf16 [batch, out_rows, dim] the compressed cache               */
+    int batch, dim, ratio, rope_dim, out_rows, overlap;
+    float eps;
+    double rope_theta;
+} dsv4_compress_step_args;
+int dsv4_compress_step(const dsv4_compress_step_args* args, dsv4_stream_t stream);
+
 /* ---------------------------------------------------------------------------------------
  * Stage 2. Lightning-indexer score + per-token top-k.
  *

@@ -182,6 +182,74 @@ def test_compress_overlap_long_blocks():
         assert_bf16_close(got, ref, f"ratio {r}")
 
 
+# ------------------------------------------------------------------ stage 1 at decode time: one token per call
+@pytest.mark.parametrize("overlap", [False, True])
+def test_compress_step_matches_block_compressor(overlap):
+    """Token by token through the device-side step (state on the device, one launch per token)
+    for 3 sequences over 30 tokens with ratio 4: the cache rows and counts equal the oracle's
+    compression of the whole token history."""
+    m = csa()
+    B, d, r, T = 3, 512, 4, 30
+    w = 2 * d if overlap else d
+    C = synth.normal_bf16(7, 111, (B, T, w))
+    Z = synth.normal_bf16(7, 112, (B, T, w))
+    bias = synth.bf16_bits_to_f32(synth.normal_bf16(7, 113, (r, w), 0.0, 0.5))
+    gamma = synth.bf16_bits_to_f32(synth.normal_bf16(7, 114, (d,), 1.0, 0.1))
+    pos0 = np.array([0, 4096, 1048000], np.int64)                 # block-aligned starts
+    stage, fill, n_comp = m.compress_step_state(B, d, r, overlap=overlap)
+    cache = torch.zeros(B, 16, d, dtype=torch.bfloat16, device="cuda")
+    Cd, Zd, bd, gd = dev_bf16(C), dev_bf16(Z), dev(bias), dev(gamma)
+    for t in range(T):
+        pos = dev(pos0 + t)
+        m.dsv4_compress_step(Cd[:, t].contiguous(), Zd[:, t].contiguous(), bd, gd, pos, stage, fill,
+                             n_comp, cache, ratio=r, overlap=overlap)
+    torch.cuda.synchronize()
+    nb = T // r
+    assert n_comp.cpu().tolist() == [nb] * B and fill.cpu().tolist() == [T % r] * B
+    Tb = nb * r
+    if overlap:
+        _, ref = oracle.compress_overlap(C[:, :Tb], Z[:, :Tb], bias, gamma, pos0, r)
+    else:
+        _, ref = oracle.compress(C[:, :Tb], Z[:, :Tb], bias, gamma, pos0, r, 64)
+    got = host_bf16(cache)
+    assert_bf16_close(got[:, :nb], ref, "step compressor")
+    assert not np.any(got[:, nb:]), "rows past n_comp were written"
+
+
+def test_compress_step_graph_replay_and_full_cache():
+    """One captured graph replayed for every token (inputs copied into fixed buffers); a cache
+    that is full keeps its rows and its count."""
+    m = csa()
+    B, d, r, T, rows = 2, 128, 4, 24, 5
+    C = synth.normal_bf16(8, 121, (B, T, d))
+    Z = synth.normal_bf16(8, 122, (B, T, d))
+    bias = synth.bf16_bits_to_f32(synth.normal_bf16(8, 123, (r, d), 0.0, 0.5))
+    gamma = synth.bf16_bits_to_f32(synth.normal_bf16(8, 124, (d,), 1.0, 0.1))
+    pos0 = np.array([8, 800], np.int64)
+    stage, fill, n_comp = m.compress_step_state(B, d, r)
+    cache = torch.zeros(B, rows, d, dtype=torch.bfloat16, device="cuda")
+    Cd, Zd = dev_bf16(C), dev_bf16(Z)
+    tok_c = torch.empty(B, d, dtype=torch.bfloat16, device="cuda")
+    tok_z = torch.empty_like(tok_c)
+    pos = torch.empty(B, dtype=torch.int64, device="cuda")
+    posd = dev(pos0)
+    bd, gd = dev(bias), dev(gamma)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            m.dsv4_compress_step(tok_c, tok_z, bd, gd, pos, stage, fill, n_comp, cache, ratio=r, stream=s)
+        for t in range(T):
+            tok_c.copy_(Cd[:, t])
+            tok_z.copy_(Zd[:, t])
+            pos.copy_(posd + t)
+            g.replay()
+    torch.cuda.synchronize()
+    assert n_comp.cpu().tolist() == [rows] * B                   # 6 blocks completed, 5 rows kept
+    _, ref = oracle.compress(C[:, :rows * r], Z[:, :rows * r], bias, gamma, pos0, r, 64)
+    assert_bf16_close(host_bf16(cache), ref, "graph-replayed step compressor")
+
+
 # ------------------------------------------------------------------ stage 2: indexer + top-k
 def _run_indexer(q, w, keys, n_comp, top_k, ratio=4, q_pos=None, want_scores=True):
     m = csa()

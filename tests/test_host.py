@@ -117,6 +117,18 @@ def test_compress_rejects_on_host(lib):
         assert lib.dsv4_compress(ctypes.byref(a), None) == 1, bad
 
 
+def test_compress_step_rejects_on_host(lib):
+    from compressed_sparse_attention_08_gb300._abi import StepArgs
+    base = dict(C=_p(1), Z=_p(2), bias=_p(3), gamma=_p(4), pos=_p(5), stage=_p(6), fill=_p(7),
+                n_comp=_p(8), out=_p(9), batch=4, dim=512, ratio=4, rope_dim=64, out_rows=10,
+                overlap=0, eps=1e-6, rope_theta=10000.0)
+    for bad in (dict(stage=None), dict(fill=None), dict(n_comp=None), dict(ratio=0),
+                dict(dim=2048), dict(rope_dim=65), dict(out_rows=0), dict(overlap=3),
+                dict(rope_theta=-1.0), dict(pos=ctypes.c_void_p(FAKE + 4))):
+        a = StepArgs(**{**base, **bad})
+        assert lib.dsv4_compress_step(ctypes.byref(a), None) == 1, bad
+
+
 def test_fused_requires_consistent_stages(lib):
     from compressed_sparse_attention_08_gb300._abi import CsaArgs, IndexArgs, AttnArgs
     ia = _index_args()
