@@ -62,6 +62,14 @@ def _bind(lib):
     lib.oracle_topk_f32.argtypes = [P, P, I, I, I, P]
     lib.oracle_sparse_attn.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I,
                                        I, D, P, P, P]
+    lib.oracle_quantize_rows_e4m3.argtypes = [P, I, I, P, P]
+    lib.oracle_quantize_rows_e4m3.restype = ctypes.c_int
+    lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_to_double.restype = D
+    lib.oracle_e4m3_from_double.argtypes = [D]
+    lib.oracle_e4m3_from_double.restype = ctypes.c_uint8
+    lib.oracle_index_scores_fp8.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, P, P]
+    lib.oracle_index_scores_fp8.restype = ctypes.c_int
     lib.oracle_inverse_rope.argtypes = [P, P, I, I, I, I, D, P, P]
     lib.oracle_inverse_rope.restype = ctypes.c_int
     lib.oracle_max_comp.argtypes = [ctypes.c_int64, I]
@@ -187,6 +195,51 @@ def sparse_attn(q, sink, comp_kv, n_comp, idx, win, win_len, top_k, window=128, 
     if rc != 0:
         raise ValueError(f"oracle_sparse_attn: bad arguments (rc={rc})")
     return out, out64, gather
+
+
+def e4m3_encode(x):
+    """FP8 E4M3 codes (round to nearest even, saturating) of float64 values, elementwise."""
+    lib = _load()
+    x = np.asarray(x, np.float64)
+    return np.array([lib.oracle_e4m3_from_double(float(v)) for v in x.ravel()], np.uint8).reshape(x.shape)
+
+
+def e4m3_decode(c):
+    lib = _load()
+    c = np.asarray(c, np.uint8)
+    return np.array([lib.oracle_e4m3_to_double(int(v)) for v in c.ravel()], np.float64).reshape(c.shape)
+
+
+def quantize_rows_e4m3(x):
+    """Per-row FP8 E4M3 quantization of fp32 rows x [..., dim]: (codes uint8, scale fp32 [...])."""
+    lib = _load()
+    x = np.ascontiguousarray(x, np.float32)
+    shape = x.shape
+    rows = int(np.prod(shape[:-1]))
+    q = np.zeros(shape, np.uint8)
+    sc = np.zeros(shape[:-1], np.float32)
+    rc = lib.oracle_quantize_rows_e4m3(_p(x), rows, shape[-1], _p(q), _p(sc))
+    if rc != 0:
+        raise ValueError(f"oracle_quantize_rows_e4m3: bad arguments (rc={rc})")
+    return q, sc
+
+
+def index_scores_fp8(q, q_scale, w, keys, k_scale, n_comp, ratio=4, q_pos=None):
+    """Indexer scores of FP8 rows.  q uint8 [B, n_q, H, Di], q_scale fp32 [B, n_q, H], w fp32
+    [B, n_q, H], keys uint8 [B, max_comp, Di], k_scale fp32 [B, max_comp]; as index_scores."""
+    lib = _load()
+    q = _c(q, np.uint8); q_scale = _c(q_scale, np.float32); w = _c(w, np.float32)
+    keys = _c(keys, np.uint8); k_scale = _c(k_scale, np.float32)
+    n_comp = _c(n_comp, np.int32); q_pos = _c(q_pos, np.int64)
+    B, n_q, H, Di = q.shape
+    max_comp = keys.shape[1]
+    scores = np.empty((B, n_q, max_comp), np.float64)
+    n_vis = np.empty((B, n_q), np.int32)
+    rc = lib.oracle_index_scores_fp8(_p(q), _p(q_scale), _p(w), _p(keys), _p(k_scale), _p(n_comp),
+                                     _p(q_pos), B, n_q, H, Di, max_comp, ratio, _p(scores), _p(n_vis))
+    if rc != 0:
+        raise ValueError(f"oracle_index_scores_fp8: bad arguments (rc={rc})")
+    return scores, n_vis
 
 
 def inverse_rope(x, pos, rope_dim=64, theta=10000.0):

@@ -61,6 +61,35 @@ int64_t visible_entries(int64_t n_comp, int64_t p, int ratio) {
     return std::min<int64_t>(n_comp, by_pos);
 }
 
+// FP8 E4M3 (the OCP 8-bit floating point format, "E4M3FN"): 1 sign bit, 4 exponent bits
+// (bias 7), 3 mantissa bits; exponent field 0 holds the subnormals m * 2^-9; the largest
+// finite value is 1.75 * 2^8 = 448 (code 0x7E), code 0x7F is NaN, there is no infinity.
+// Encoding rounds to nearest, ties to even, and saturates to +-448 (finite inputs).
+uint8_t e4m3_from_double(double x) {
+    if (std::isnan(x)) return 0x7F;
+    const uint8_t sign = std::signbit(x) ? 0x80 : 0x00;
+    const double a = std::fabs(x);
+    if (a == 0.0) return sign;
+    int e = std::ilogb(a);                          // a in [2^e, 2^(e+1))
+    if (e < -6) e = -6;                             // below 2^-6: the subnormal spacing 2^-9
+    double q = std::nearbyint(std::ldexp(a, 3 - e)); // a in units of the spacing 2^(e-3)
+    if (q >= 16.0) {                                 // rounded up to the next binade
+        q = 8.0;
+        ++e;
+    }
+    if (e > 8 || (e == 8 && q > 14.0)) return static_cast<uint8_t>(sign | 0x7E);   // saturate
+    if (q < 8.0) return static_cast<uint8_t>(sign | static_cast<uint8_t>(q));       // subnormal
+    return static_cast<uint8_t>(sign | ((e + 7) << 3) | (static_cast<int>(q) - 8));
+}
+
+double e4m3_to_double(uint8_t c) {
+    const double sign = (c & 0x80) ? -1.0 : 1.0;
+    const int ef = (c >> 3) & 0xF, m = c & 7;
+    if (ef == 0xF && m == 7) return std::numeric_limits<double>::quiet_NaN();
+    if (ef == 0) return sign * std::ldexp(static_cast<double>(m), -9);
+    return sign * std::ldexp(1.0 + m / 8.0, ef - 7);
+}
+
 }  // namespace
 
 extern "C" {
@@ -451,6 +480,77 @@ int oracle_inverse_rope(const double* x, const int64_t* pos, int rows, int heads
             for (int i = 0; i < D; ++i) {
                 out[base + i] = double_to_bf16(v[i]);
                 if (out_f64) out_f64[base + i] = v[i];
+            }
+        }
+    }
+    return 0;
+}
+
+// ---------------------------------------------------------------------------
+// FP8 index keys: row quantization and scoring on the quantized rows.
+//
+// [B] single_shot_inference.py (indexer): "Indexer keys are stored as FP8_E4M3 in the KV
+// cache", scored on the FP8 tensor-core path. The pages fix no scale; the reading taken: one
+// fp32 scale per row (a key row, or one head of a query), scale = amax / 448 computed in fp32
+// (1 for an all-zero row), code = E4M3(x / scale) with the division in fp32, so that the codes
+// are a definite function of the fp32 inputs.
+//
+// x [rows, dim] fp32 -> q [rows, dim] E4M3 codes, scale [rows] fp32.
+int oracle_quantize_rows_e4m3(const float* x, int rows, int dim, uint8_t* q, float* scale) {
+    if (rows < 0 || dim <= 0) return -1;
+    for (int r = 0; r < rows; ++r) {
+        const float* xr = x + static_cast<size_t>(r) * dim;
+        float amax = 0.f;
+        for (int i = 0; i < dim; ++i) amax = std::max(amax, std::fabs(xr[i]));
+        const float sc = amax > 0.f ? amax / 448.0f : 1.0f;
+        scale[r] = sc;
+        for (int i = 0; i < dim; ++i) {
+            const float v = xr[i] / sc;                      // fp32 division
+            q[static_cast<size_t>(r) * dim + i] = e4m3_from_double(static_cast<double>(v));
+        }
+    }
+    return 0;
+}
+
+double oracle_e4m3_to_double(uint8_t c) { return e4m3_to_double(c); }
+uint8_t oracle_e4m3_from_double(double x) { return e4m3_from_double(x); }
+
+// The indexer score of the dequantized rows (the a3 definition on q_scale * q and
+// k_scale * k):  I[t, j] = sum_h w[t, h] * ReLU( (q_scale[t,h] q[t,h,:]) . (k_scale[j] k[j,:]) ).
+// q [B, n_q, H, Di] and k [B, max_comp, Di] E4M3 codes; q_scale [B, n_q, H], k_scale
+// [B, max_comp]; the rest as oracle_index_scores.
+int oracle_index_scores_fp8(const uint8_t* q, const float* q_scale, const float* w,
+                            const uint8_t* keys, const float* k_scale, const int32_t* n_comp,
+                            const int64_t* q_pos, int B, int n_q, int H, int Di, int max_comp,
+                            int ratio, double* scores, int32_t* n_vis) {
+    if (B < 0 || n_q < 0 || H <= 0 || Di <= 0 || max_comp < 0 || ratio <= 0) return -1;
+    std::vector<double> qd(static_cast<size_t>(H) * Di), kd(Di);
+    for (int b = 0; b < B; ++b) {
+        if (n_comp[b] < 0 || n_comp[b] > max_comp) return -1;
+        for (int t = 0; t < n_q; ++t) {
+            const size_t row = static_cast<size_t>(b) * n_q + t;
+            const int64_t nv = q_pos ? visible_entries(n_comp[b], q_pos[row], ratio) : n_comp[b];
+            n_vis[row] = static_cast<int32_t>(nv);
+            for (int h = 0; h < H; ++h)
+                for (int i = 0; i < Di; ++i)
+                    qd[static_cast<size_t>(h) * Di + i] =
+                        static_cast<double>(q_scale[row * H + h]) * e4m3_to_double(q[(row * H + h) * Di + i]);
+            for (int j = 0; j < max_comp; ++j) {
+                double& out = scores[row * max_comp + j];
+                if (j >= nv) {
+                    out = -std::numeric_limits<double>::infinity();
+                    continue;
+                }
+                const size_t kr = static_cast<size_t>(b) * max_comp + j;
+                for (int i = 0; i < Di; ++i)
+                    kd[i] = static_cast<double>(k_scale[kr]) * e4m3_to_double(keys[kr * Di + i]);
+                double acc = 0.0;
+                for (int h = 0; h < H; ++h) {
+                    double dot = 0.0;
+                    for (int i = 0; i < Di; ++i) dot += qd[static_cast<size_t>(h) * Di + i] * kd[i];
+                    acc += static_cast<double>(w[row * H + h]) * (dot > 0.0 ? dot : 0.0);   // ReLU
+                }
+                out = acc;
             }
         }
     }

@@ -634,4 +634,102 @@ def pin_inverse_rope_undoes_the_compressor_rotation():
     _close(back.reshape(B, 3, d), plain, 1e-11, 1e-11, "inverse after forward")
 
 
+# ------------------------------------------------------------------ FP8 E4M3 index keys
+def pin_e4m3_codes_from_the_format():
+    """Codes worked out by hand from the E4M3 format (bias 7, 3 mantissa bits, subnormals
+    m * 2^-9, largest finite 448 = 0x7E, round to nearest even, saturating)."""
+    table = [(0.0, 0x00), (-0.0, 0x80), (1.0, 0x38), (1.125, 0x39), (1.0625, 0x38),
+             (1.1875, 0x3A), (-2.0, 0xC0), (240.0, 0x77), (448.0, 0x7E), (464.0, 0x7E),
+             (1e6, 0x7E), (-1e6, 0xFE), (2.0 ** -6, 0x08), (2.0 ** -9, 0x01), (2.0 ** -10, 0x00),
+             (3 * 2.0 ** -10, 0x02), (0.1, 0x1D), (7 * 2.0 ** -9, 0x07), (15 * 2.0 ** -10, 0x08)]
+    got = oracle.e4m3_encode([v for v, _ in table])
+    for (v, want), g in zip(table, got):
+        assert int(g) == want, f"{v}: got {int(g):#04x}, want {want:#04x}"
+    dec = oracle.e4m3_decode(np.array([0x38, 0x7E, 0x01, 0x08, 0xC0, 0x1D], np.uint8))
+    _close(dec, [1.0, 448.0, 2.0 ** -9, 2.0 ** -6, -2.0, 0.1015625], 0, 0, "decode")
+
+
+def pin_e4m3_round_trip_and_order():
+    """Every finite code decodes and re-encodes to itself; encoding is monotonic; the relative
+    error of a normal value is at most 2^-4."""
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
+    vals = oracle.e4m3_decode(codes)
+    assert np.array_equal(oracle.e4m3_encode(vals), codes)
+    rng = _rng(61)
+    x = np.sort(rng.uniform(-500, 500, 4000))
+    dq = oracle.e4m3_decode(oracle.e4m3_encode(x))
+    assert np.all(np.diff(dq) >= 0), "not monotonic"
+    normal = (np.abs(x) >= 2.0 ** -6) & (np.abs(x) <= 448)
+    assert np.all(np.abs(dq[normal] - x[normal]) <= 2.0 ** -4 * np.abs(x[normal]))
+
+
+def pin_quantize_rows_scale():
+    """Each row's largest magnitude maps to +-448 (code 0x7E / 0xFE); an all-zero row has scale
+    1 and zero codes."""
+    rng = _rng(62)
+    x = rng.standard_normal((5, 128)).astype(np.float32)
+    x[3] = 0.0
+    q, sc = oracle.quantize_rows_e4m3(x)
+    for r in (0, 1, 2, 4):
+        i = int(np.argmax(np.abs(x[r])))
+        assert q[r, i] == (0x7E if x[r, i] > 0 else 0xFE)
+        assert sc[r] == np.float32(np.float32(np.abs(x[r, i])) / np.float32(448.0))
+    assert sc[3] == 1.0 and not np.any(q[3])
+
+
+def pin_fp8_scores_equal_plain_scores_on_exact_rows():
+    """Rows whose values are E4M3 values with largest magnitude 448 quantize exactly (scale 1),
+    so the FP8 scores equal the plain scores of the same values."""
+    rng = _rng(63)
+    B, H, Di, N = 2, 8, 128, 40
+    codes = rng.integers(0, 0x7E, size=(B, 1, H, Di)).astype(np.uint8) | (rng.integers(0, 2, size=(B, 1, H, Di)) << 7).astype(np.uint8)
+    kcodes = rng.integers(0, 0x7E, size=(B, N, Di)).astype(np.uint8) | (rng.integers(0, 2, size=(B, N, Di)) << 7).astype(np.uint8)
+    codes[..., 0] = 0x7E
+    kcodes[..., 0] = 0x7E
+    qv = oracle.e4m3_decode(codes).astype(np.float32)
+    kv = oracle.e4m3_decode(kcodes).astype(np.float32)
+    q8, qs = oracle.quantize_rows_e4m3(qv)
+    k8, ks = oracle.quantize_rows_e4m3(kv)
+    assert np.array_equal(q8, codes) and np.array_equal(k8, kcodes) and np.all(qs == 1) and np.all(ks == 1)
+    w = rng.standard_normal((B, 1, H)).astype(np.float32)
+    n_comp = np.array([N, 17], np.int32)
+    got, nv8 = oracle.index_scores_fp8(q8, qs, w, k8, ks, n_comp)
+    # the plain scorer takes bf16 inputs: scale both sides by 1/64 so every E4M3 value is bf16-exact
+    want, nv = oracle.index_scores(_bf(qv / 64), w, _bf(kv / 64), n_comp)
+    assert np.array_equal(nv8, nv)
+    _close(got[np.isfinite(got)], 4096.0 * want[np.isfinite(want)], 1e-12, 1e-12, "fp8 vs plain")
+
+
+def pin_fp8_scores_scale_with_the_rows():
+    """Scaling a key row by 4 or a query head by 8 (powers of two: exact in fp32) leaves the
+    codes unchanged and multiplies the scale; the key's scores then grow 4 times, and head h's
+    share of every score 8 times (ReLU is positively homogeneous)."""
+    rng = _rng(64)
+    B, H, Di, N = 1, 4, 128, 30
+    qv = rng.standard_normal((B, 1, H, Di)).astype(np.float32)
+    kv = rng.standard_normal((B, N, Di)).astype(np.float32)
+    w = np.abs(rng.standard_normal((B, 1, H))).astype(np.float32)
+    n_comp = np.array([N], np.int32)
+    q8, qs = oracle.quantize_rows_e4m3(qv)
+    k8, ks = oracle.quantize_rows_e4m3(kv)
+    base, _ = oracle.index_scores_fp8(q8, qs, w, k8, ks, n_comp)
+    kv2 = kv.copy()
+    kv2[0, 5] *= 4
+    k82, ks2 = oracle.quantize_rows_e4m3(kv2)
+    assert np.array_equal(k82, k8) and ks2[0, 5] == 4 * ks[0, 5]
+    got, _ = oracle.index_scores_fp8(q8, qs, w, k82, ks2, n_comp)
+    _close(got[0, 0, 5], 4 * base[0, 0, 5], 1e-12, 1e-12, "key scale")
+    _close(np.delete(got[0, 0], 5), np.delete(base[0, 0], 5), 0, 0, "other keys")
+    # head 2 alone, then head 2 scaled by 8
+    w1 = np.zeros_like(w)
+    w1[..., 2] = 1.0
+    one, _ = oracle.index_scores_fp8(q8, qs, w1, k8, ks, n_comp)
+    qv2 = qv.copy()
+    qv2[0, 0, 2] *= 8
+    q82, qs2 = oracle.quantize_rows_e4m3(qv2)
+    assert np.array_equal(q82, q8) and qs2[0, 0, 2] == 8 * qs[0, 0, 2]
+    got2, _ = oracle.index_scores_fp8(q82, qs2, w, k8, ks, n_comp)
+    _close(got2, base + 7.0 * float(w[0, 0, 2]) * one, 1e-11, 1e-11, "query scale")
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

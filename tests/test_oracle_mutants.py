@@ -37,6 +37,18 @@ MUTANTS = [
      "const int64_t hi = qa + win_len[b] - n_q_total - 1;", 1),
     ("bf16_truncates", "double r = std::nearbyint(scaled);", "double r = std::trunc(scaled);", 1),
     ("max_comp_floor", "return (max_context + ratio - 1) / ratio;", "return max_context / ratio;", 1),
+    ("e4m3_round_half_up", "double q = std::nearbyint(std::ldexp(a, 3 - e));",
+     "double q = std::floor(std::ldexp(a, 3 - e) + 0.5);", 1),
+    ("e4m3_bias_6", "((e + 7) << 3)", "((e + 6) << 3)", 1),
+    ("e4m3_no_saturation", "if (e > 8 || (e == 8 && q > 14.0))", "if (e > 8)", 1),
+    ("e4m3_subnormal_spacing", "if (e < -6) e = -6;", "if (e < -7) e = -7;", 1),
+    ("quant_scale_max_code", "amax / 448.0f", "amax / 240.0f", 1),
+    ("fp8_score_key_scale_dropped", "static_cast<double>(k_scale[kr]) * e4m3_to_double(keys[kr * Di + i])",
+     "e4m3_to_double(keys[kr * Di + i])", 1),
+    ("fp8_score_no_relu", "(dot > 0.0 ? dot : 0.0);   // ReLU", "dot;   // ReLU", 1),
+    ("fp8_score_query_scale_dropped",
+     "static_cast<double>(q_scale[row * H + h]) * e4m3_to_double(q[(row * H + h) * Di + i]);",
+     "e4m3_to_double(q[(row * H + h) * Di + i]);", 1),
     ("inverse_rope_forward_direction", "v[e0] = ev * cs + ov * sn;", "v[e0] = ev * cs - ov * sn;", 1),
     ("inverse_rope_odd_sign", "v[e0 + 1] = -ev * sn + ov * cs;", "v[e0 + 1] = ev * sn + ov * cs;", 1),
     ("inverse_rope_frequency", "std::pow(theta, -(2.0 * j) / rope_dim)", "std::pow(theta, -(1.0 * j) / rope_dim)", 1),
