@@ -9,7 +9,8 @@ from __future__ import annotations
 from ._abi import (  # noqa: F401
     DSV4_OK, DSV4_ERR_INVALID_ARG, DSV4_ERR_LAUNCH, DSV4_ERR_BAD_INDEX, DSV4_ERR_TIMEOUT,
     DSV4_ERR_UNSUPPORTED, DSV4_EWORD_BAD_INDEX, DSV4_EWORD_TIMEOUT, Dsv4Error, library,
-    library_path, dsv4_compress, dsv4_compress_step, compress_step_state, dsv4_indexer_topk,
+    library_path, dsv4_compress, dsv4_compress_step, compress_step_state, dsv4_quantize_rows_fp8,
+    dsv4_indexer_topk,
     dsv4_indexer_topk_workspace_size,
     dsv4_index_score, dsv4_index_score_workspace_size,
     dsv4_topk, dsv4_topk_workspace_size, dsv4_topk_noalloc, dsv4_sparse_attn_decode,

@@ -22,7 +22,8 @@ DSV4_EWORD_BAD_INDEX = 0x1
 DSV4_EWORD_TIMEOUT = 0x2
 
 EXPORTED_SYMBOLS = (
-    "dsv4_compress", "dsv4_compress_step", "dsv4_indexer_topk_workspace_size", "dsv4_indexer_topk",
+    "dsv4_compress", "dsv4_compress_step", "dsv4_quantize_rows_fp8", "dsv4_indexer_topk_workspace_size",
+    "dsv4_indexer_topk",
     "dsv4_index_score_workspace_size", "dsv4_index_score",
     "dsv4_topk_workspace_size", "dsv4_topk", "dsv4_topk_noalloc", "dsv4_sparse_attn_workspace_size",
     "dsv4_sparse_attn_decode", "dsv4_csa_decode_workspace_size", "dsv4_csa_decode",
@@ -50,7 +51,8 @@ class StepArgs(ctypes.Structure):
 class IndexArgs(ctypes.Structure):
     _fields_ = [("q", P), ("w", P), ("keys", P), ("n_comp", P), ("q_pos", P), ("idx_out", P),
                 ("scores_out", P), ("batch", I), ("n_q", I), ("heads", I), ("dim", I),
-                ("max_comp", I), ("top_k", I), ("ratio", I)]
+                ("max_comp", I), ("top_k", I), ("ratio", I), ("key_fp8", I), ("q_scale", P),
+                ("key_scale", P)]
 
 
 class TopkArgs(ctypes.Structure):
@@ -96,6 +98,7 @@ def library():
         lib = ctypes.CDLL(path)
         lib.dsv4_compress.argtypes = [ctypes.POINTER(CompressArgs), P]
         lib.dsv4_compress_step.argtypes = [ctypes.POINTER(StepArgs), P]
+        lib.dsv4_quantize_rows_fp8.argtypes = [P, I, I, P, P, P]
         lib.dsv4_indexer_topk_workspace_size.argtypes = [ctypes.POINTER(IndexArgs)]
         lib.dsv4_indexer_topk_workspace_size.restype = ctypes.c_size_t
         lib.dsv4_indexer_topk.argtypes = [ctypes.POINTER(IndexArgs), P, ctypes.c_size_t, P]
@@ -176,13 +179,20 @@ def compress_args(C, Z, bias, gamma, pos0, out, *, ratio, rope_dim=64, eps=1e-6,
                         _ptr(prev_C, bf16, "prev_C", True), _ptr(prev_Z, bf16, "prev_Z", True))
 
 
-def index_args(q, w, keys, n_comp, idx_out, *, ratio, q_pos=None, scores_out=None):
+def index_args(q, w, keys, n_comp, idx_out, *, ratio, q_pos=None, scores_out=None, q_scale=None,
+               key_scale=None):
+    """q_scale / key_scale given: q and keys are FP8 E4M3 codes (uint8), as
+    dsv4_quantize_rows_fp8 writes them."""
     bf16, f32, i32, i64 = _dt()
+    import torch
+    fp8 = q_scale is not None
+    kt = torch.uint8 if fp8 else bf16
     B, n_q, H, Di = q.shape
-    return IndexArgs(_ptr(q, bf16, "q"), _ptr(w, f32, "w"), _ptr(keys, bf16, "keys"),
+    return IndexArgs(_ptr(q, kt, "q"), _ptr(w, f32, "w"), _ptr(keys, kt, "keys"),
                      _ptr(n_comp, i32, "n_comp"), _ptr(q_pos, i64, "q_pos", True),
                      _ptr(idx_out, i32, "idx_out"), _ptr(scores_out, f32, "scores_out", True),
-                     B, n_q, H, Di, keys.shape[1], idx_out.shape[-1], ratio)
+                     B, n_q, H, Di, keys.shape[1], idx_out.shape[-1], ratio, 1 if fp8 else 0,
+                     _ptr(q_scale, f32, "q_scale", True), _ptr(key_scale, f32, "key_scale", True))
 
 
 def topk_args(scores, n_vis, idx_out):
@@ -223,6 +233,17 @@ def dsv4_compress(C, Z, bias, gamma, pos0, out, *, ratio, rope_dim=64, eps=1e-6,
     _check(library().dsv4_compress(ctypes.byref(a), _stream(stream)), "dsv4_compress")
 
 
+def dsv4_quantize_rows_fp8(x, q, scale, *, stream=None):
+    """FP8 E4M3 rows: x bf16 [..., dim] -> q uint8 [..., dim], scale fp32 [...]."""
+    import torch
+    bf16, f32, i32, i64 = _dt()
+    dim = x.shape[-1]
+    rows = x.numel() // dim
+    _check(library().dsv4_quantize_rows_fp8(_ptr(x, bf16, "x"), rows, dim, _ptr(q, torch.uint8, "q"),
+                                            _ptr(scale, f32, "scale"), _stream(stream)),
+           "dsv4_quantize_rows_fp8")
+
+
 def compress_step_state(batch, dim, ratio, *, overlap=False, device="cuda"):
     """Zeroed state for dsv4_compress_step: (stage, fill, n_comp)."""
     import torch
@@ -248,31 +269,38 @@ def dsv4_compress_step(C, Z, bias, gamma, pos, stage, fill, n_comp, out, *, rati
 
 
 def dsv4_indexer_topk_workspace_size(q, w, keys, n_comp, idx_out, *, ratio, q_pos=None,
-                                     scores_out=None):
-    a = index_args(q, w, keys, n_comp, idx_out, ratio=ratio, q_pos=q_pos, scores_out=scores_out)
+                                     scores_out=None, q_scale=None, key_scale=None):
+    a = index_args(q, w, keys, n_comp, idx_out, ratio=ratio, q_pos=q_pos, scores_out=scores_out,
+                   q_scale=q_scale, key_scale=key_scale)
     return int(library().dsv4_indexer_topk_workspace_size(ctypes.byref(a)))
 
 
 def dsv4_indexer_topk(q, w, keys, n_comp, idx_out, ws, *, ratio, q_pos=None, scores_out=None,
-                      stream=None):
-    a = index_args(q, w, keys, n_comp, idx_out, ratio=ratio, q_pos=q_pos, scores_out=scores_out)
+                      q_scale=None, key_scale=None, stream=None):
+    """q_scale / key_scale given: FP8 E4M3 queries and keys (see index_args)."""
+    a = index_args(q, w, keys, n_comp, idx_out, ratio=ratio, q_pos=q_pos, scores_out=scores_out,
+                   q_scale=q_scale, key_scale=key_scale)
     _check(library().dsv4_indexer_topk(ctypes.byref(a), _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
                                        _stream(stream)), "dsv4_indexer_topk")
 
 
-def dsv4_index_score_workspace_size(q, w, keys, n_comp, scores_out, *, ratio, q_pos=None):
+def dsv4_index_score_workspace_size(q, w, keys, n_comp, scores_out, *, ratio, q_pos=None,
+                                    q_scale=None, key_scale=None):
     import torch
     idx = torch.empty(1, dtype=torch.int32, device=q.device)
-    a = index_args(q, w, keys, n_comp, idx, ratio=ratio, q_pos=q_pos, scores_out=scores_out)
+    a = index_args(q, w, keys, n_comp, idx, ratio=ratio, q_pos=q_pos, scores_out=scores_out,
+                   q_scale=q_scale, key_scale=key_scale)
     a.top_k = 1
     return int(library().dsv4_index_score_workspace_size(ctypes.byref(a)))
 
 
-def dsv4_index_score(q, w, keys, n_comp, scores_out, ws, *, ratio, q_pos=None, stream=None):
+def dsv4_index_score(q, w, keys, n_comp, scores_out, ws, *, ratio, q_pos=None, q_scale=None,
+                     key_scale=None, stream=None):
     """Scores only (no top-k): scores_out [B, n_q, max_comp] fp32 gets the visible scores."""
     import torch
     idx = torch.empty(1, dtype=torch.int32, device=q.device)
-    a = index_args(q, w, keys, n_comp, idx, ratio=ratio, q_pos=q_pos, scores_out=scores_out)
+    a = index_args(q, w, keys, n_comp, idx, ratio=ratio, q_pos=q_pos, scores_out=scores_out,
+                   q_scale=q_scale, key_scale=key_scale)
     a.top_k = 1
     _check(library().dsv4_index_score(ctypes.byref(a), _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
                                       _stream(stream)), "dsv4_index_score")

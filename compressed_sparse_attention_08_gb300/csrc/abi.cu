@@ -60,6 +60,10 @@ bool index_ok(const dsv4_index_args* a) {
     if (a->max_comp < 1 || a->top_k < 1 || a->top_k > a->max_comp || a->ratio < 1) return false;
     if (static_cast<long long>(a->batch) * a->n_q > (1ll << 30)) return false;
     if (static_cast<long long>(a->batch) * a->n_q * a->heads > (1ll << 31) - 1) return false;
+    if (a->key_fp8 != 0 && a->key_fp8 != 1) return false;
+    if (a->key_fp8 ? (!dev_ptr_ok(a->q_scale) || !dev_ptr_ok(a->key_scale))
+                   : (a->q_scale != nullptr || a->key_scale != nullptr))
+        return false;
     return true;
 }
 
@@ -157,6 +161,15 @@ int dsv4_compress(const dsv4_compress_args* a, dsv4_stream_t stream) {
     if (!compress_ok(a)) return DSV4_ERR_INVALID_ARG;
     if (int rc = device_check()) return rc;
     return launch_compress(*a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dsv4_quantize_rows_fp8(const void* x, int rows, int dim, void* q, float* scale, dsv4_stream_t stream) {
+    LaunchScope scope;
+    if (!dev_ptr_ok(x) || !dev_ptr_ok(q) || !dev_ptr_ok(scale) || rows < 0 || dim < 32 || dim > 1024 ||
+        (dim & (dim - 1)) != 0)
+        return DSV4_ERR_INVALID_ARG;
+    if (int rc = device_check()) return rc;
+    return launch_quantize_rows_fp8(x, rows, dim, q, scale, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int dsv4_compress_step(const dsv4_compress_step_args* a, dsv4_stream_t stream) {

@@ -43,17 +43,27 @@ namespace dsv4 {
 namespace {
 
 constexpr int kTileKeys = 128;              // UMMA M
-constexpr int kSub = 2;                     // MMA tiles per stage
-constexpr int kStageKeys = kSub * kTileKeys;
 constexpr int kDim = 128;                   // key width = UMMA K total
 constexpr int kMaxHeads = 64;               // UMMA N upper bound
 constexpr int kStages = 3;
 constexpr int kAccBufs = 4;
 constexpr int kAccCols = 64;                // TMEM columns per accumulator
 constexpr uint32_t kTmemCols = kAccBufs * kAccCols;   // 256 (power of two)
-constexpr uint32_t kStageBytes = kStageKeys * kDim * 2;    // 64 KiB
-constexpr uint32_t kStageHalfBytes = kStageBytes / 2;      // 256 keys x 64 dims
-constexpr uint32_t kQBufBytes = kMaxHeads * kDim * 2;      // 16 KiB
+constexpr uint32_t kStageBytes = 64 * 1024;                // two 32 KiB TMA boxes
+constexpr uint32_t kBoxBytes = kStageBytes / 2;
+constexpr uint32_t kQBufBytes = kMaxHeads * kDim * 2;      // 16 KiB (bf16 queries)
+
+// Key format: bf16 (two bytes per element, a 256-byte key split into two 64-dim boxes) or FP8
+// E4M3 (one byte, a key is one 128-byte row, the two boxes hold consecutive keys). A stage is
+// 64 KiB either way: 256 or 512 keys, 2 or 4 MMA tiles; one MMA step consumes 32 bytes of K.
+template <bool FP8>
+struct KeyFmt {
+    static constexpr int kElem = FP8 ? 1 : 2;
+    static constexpr int kStageKeys = static_cast<int>(kStageBytes) / (kDim * kElem);
+    static constexpr int kSub = kStageKeys / kTileKeys;
+    static constexpr int kKSteps = kDim * kElem / 32;
+    static constexpr int kBoxInner = 128 / kElem;          // elements per 128-byte box row
+};
 constexpr int kThreads = 192;
 constexpr int kHistBins = 4096;             // top 12 bits of the order-preserving score key
 constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + kQBufBytes;
@@ -67,6 +77,8 @@ struct ScoreParams {
     const int32_t* fresh_row0;  // [batch] first key row the preceding kernel writes, or null
     int fresh_rows;          // rows it writes per sequence (0: none)
     uint32_t* eword;
+    const float* q_scale;    // FP8 keys: [rows, heads] query scales, else null
+    const float* key_scale;  // FP8 keys: [batch, max_comp] key scales, else null
     int rows, n_q, heads, n_pad, max_comp, ratio, stages_per_row;
 };
 
@@ -88,6 +100,7 @@ __device__ __forceinline__ Walk cta_walk(int rows, int per_row) {
     return {r * per_row + (c - cb), (r + 1) * per_row, ce - cb};
 }
 
+template <bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
 index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap qmap, ScoreParams p) {
@@ -101,6 +114,8 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
     // compressor CTA still fits beside this CTA on its SM)
     __shared__ uint32_t s_hist[kHistBins / 2];
 
+    using F = KeyFmt<FP8>;
+    constexpr int kStageKeys = F::kStageKeys, kSub = F::kSub;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_trigger();
     // 1024-byte aligned operand buffers (the 128-byte swizzle repeats every 1024 bytes)
@@ -132,8 +147,8 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
     const uint32_t tmem_base = tmem_slot;
 
     const Walk wk = cta_walk(p.rows, p.stages_per_row);
-    const uint32_t idesc = idesc_bf16_f32(kTileKeys, p.n_pad);
-    const uint32_t q_half = static_cast<uint32_t>(p.n_pad) * 128u;   // bytes of one 64-dim half
+    const uint32_t idesc = FP8 ? idesc_e4m3_f32(kTileKeys, p.n_pad) : idesc_bf16_f32(kTileKeys, p.n_pad);
+    const uint32_t q_half = static_cast<uint32_t>(p.n_pad) * 128u;   // bf16: bytes of one 64-dim half
 
     if (warp == 0) {
         if (lane == 0) {
@@ -151,9 +166,9 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                 if (row != cur_row) {
                     // one query buffer: the previous row's MMAs release it first
                     if (!mbar_wait(&qempty_bar, (qcount & 1) ^ 1, &abort_flag)) goto fail0;
-                    mbar_arrive_expect_tx(&qfull_bar, static_cast<uint32_t>(p.heads) * kDim * 2);
+                    mbar_arrive_expect_tx(&qfull_bar, static_cast<uint32_t>(p.heads) * kDim * F::kElem);
                     tma_load_2d(q_buf, &qmap, &qfull_bar, 0, row * p.heads);
-                    tma_load_2d(q_buf + q_half, &qmap, &qfull_bar, 64, row * p.heads);
+                    if (!FP8) tma_load_2d(q_buf + q_half, &qmap, &qfull_bar, 64, row * p.heads);
                     cur_row = row;
                     ++qcount;
                 }
@@ -172,9 +187,10 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                 {
                     uint8_t* kd = key_buf + stage * kStageBytes;
                     const int b = row / p.n_q;
+                    // bf16: the two 64-dim halves of 256 keys; FP8: two runs of 256 whole keys
                     tma_load_3d_hint(kd, &kmap, &full_bar[stage], 0, st * kStageKeys, b, stream_policy);
-                    tma_load_3d_hint(kd + kStageHalfBytes, &kmap, &full_bar[stage], 64, st * kStageKeys, b,
-                                     stream_policy);
+                    tma_load_3d_hint(kd + kBoxBytes, &kmap, &full_bar[stage], FP8 ? 0 : 64,
+                                     st * kStageKeys + (FP8 ? 256 : 0), b, stream_policy);
                     ++issued;
                 }
                 if (++stage == kStages) { stage = 0; phase ^= 1; }
@@ -221,10 +237,14 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                         const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kAccCols);
                         const uint32_t a0 = a_stage + static_cast<uint32_t>(j * kTileKeys * 128);
 #pragma unroll
-                        for (int k = 0; k < kDim / 16; ++k) {
-                            const uint64_t ad = sdesc_kmajor_sw128(a0 + (k >> 2) * kStageHalfBytes + (k & 3) * 32);
-                            const uint64_t bd = sdesc_kmajor_sw128(b0 + (k >> 2) * q_half + (k & 3) * 32);
-                            umma_bf16(d, ad, bd, idesc, k > 0 ? 1u : 0u);
+                        for (int k = 0; k < F::kKSteps; ++k) {
+                            // 32 bytes of K per step; a bf16 key continues in the second box
+                            const uint32_t ka = FP8 ? k * 32u : (k >> 2) * kBoxBytes + (k & 3) * 32u;
+                            const uint32_t kb = FP8 ? k * 32u : (k >> 2) * q_half + (k & 3) * 32u;
+                            const uint64_t ad = sdesc_kmajor_sw128(a0 + ka);
+                            const uint64_t bd = sdesc_kmajor_sw128(b0 + kb);
+                            if constexpr (FP8) umma_f8(d, ad, bd, idesc, k > 0 ? 1u : 0u);
+                            else umma_bf16(d, ad, bd, idesc, k > 0 ? 1u : 0u);
                         }
                         umma_commit(&tfull_bar[acc]);
                         if (++acc == kAccBufs) { acc = 0; acc_phase ^= 1; }
@@ -283,8 +303,12 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                 nv = row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, row, nullptr);
                 cur_row = row;
 #pragma unroll
-                for (int h = 0; h < kMaxHeads; ++h)
-                    wv[h] = h < p.heads ? __ldg(&p.w[static_cast<size_t>(row) * p.heads + h]) : 0.f;
+                for (int h = 0; h < kMaxHeads; ++h) {
+                    float wh = h < p.heads ? __ldg(&p.w[static_cast<size_t>(row) * p.heads + h]) : 0.f;
+                    // FP8: the head's query scale folds into its weight (ReLU commutes with it)
+                    if (FP8 && h < p.heads) wh *= __ldg(&p.q_scale[static_cast<size_t>(row) * p.heads + h]);
+                    wv[h] = wh;
+                }
             }
             for (int j = 0; j < kSub; ++j) {
                 const int tile = st * kSub + j;
@@ -324,6 +348,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                 for (int h = 0; h < kMaxHeads; ++h) s = fmaf(wv[h], fmaxf(__uint_as_float(r[h]), 0.f), s);
                 const int key = tile * kTileKeys + lrow;
                 if (key < nv) {
+                    if (FP8) s *= __ldg(&p.key_scale[static_cast<size_t>(row / p.n_q) * p.max_comp + key]);
                     p.scores[static_cast<size_t>(row) * p.max_comp + key] = s;
                     if (p.hist) {
                         const uint32_t bin = float_to_key(s) >> 20;
@@ -397,30 +422,33 @@ size_t index_zero_bytes(const dsv4_index_args& a) {
 }
 
 namespace {
-int launch_scores(const dsv4_index_args& a, float* scores, uint32_t* hist, uint32_t* eword,
-                  cudaStream_t stream, const dsv4_compress_args* fresh) {
+template <bool FP8>
+int launch_scores_fmt(const dsv4_index_args& a, float* scores, uint32_t* hist, uint32_t* eword,
+                      cudaStream_t stream, const dsv4_compress_args* fresh) {
+    using F = KeyFmt<FP8>;
     const int rows = a.batch * a.n_q;
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return DSV4_ERR_LAUNCH;
+    const CUtensorMapDataType dt = FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUtensorMap kmap, qmap;
     {
         cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(a.max_comp),
                               static_cast<cuuint64_t>(a.batch)};
-        cuuint64_t strides[2] = {kDim * 2ull, static_cast<cuuint64_t>(a.max_comp) * kDim * 2ull};
-        cuuint32_t box[3] = {64, kStageKeys, 1};
+        cuuint64_t strides[2] = {kDim * 1ull * F::kElem, static_cast<cuuint64_t>(a.max_comp) * kDim * F::kElem};
+        cuuint32_t box[3] = {static_cast<cuuint32_t>(F::kBoxInner), 256, 1};
         cuuint32_t estr[3] = {1, 1, 1};
-        if (encode(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.keys), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+        if (encode(&kmap, dt, 3, const_cast<void*>(a.keys), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return DSV4_ERR_LAUNCH;
     }
     {
         cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(rows) * a.heads};
-        cuuint64_t strides[1] = {kDim * 2ull};
-        cuuint32_t box[2] = {64, static_cast<cuuint32_t>(a.heads)};
+        cuuint64_t strides[1] = {kDim * 1ull * F::kElem};
+        cuuint32_t box[2] = {static_cast<cuuint32_t>(F::kBoxInner), static_cast<cuuint32_t>(a.heads)};
         cuuint32_t estr[2] = {1, 1};
-        if (encode(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.q), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+        if (encode(&qmap, dt, 2, const_cast<void*>(a.q), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return DSV4_ERR_LAUNCH;
     }
@@ -433,29 +461,37 @@ int launch_scores(const dsv4_index_args& a, float* scores, uint32_t* hist, uint3
     p.fresh_row0 = fresh ? fresh->out_row0 : nullptr;
     p.fresh_rows = fresh ? fresh->tokens / fresh->ratio : 0;
     p.eword = eword;
+    p.q_scale = FP8 ? a.q_scale : nullptr;
+    p.key_scale = FP8 ? a.key_scale : nullptr;
     p.rows = rows;
     p.n_q = a.n_q;
     p.heads = a.heads;
     p.n_pad = (a.heads + 15) / 16 * 16;
     p.max_comp = a.max_comp;
     p.ratio = a.ratio;
-    p.stages_per_row = (a.max_comp + kStageKeys - 1) / kStageKeys;
+    p.stages_per_row = (a.max_comp + F::kStageKeys - 1) / F::kStageKeys;
     const long long total = static_cast<long long>(rows) * p.stages_per_row;
     if (total > 0) {
         static bool attr_set = false;
         if (!attr_set) {
-            cudaFuncSetAttribute(index_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            cudaFuncSetAttribute(index_score_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kSmemBytes));
             attr_set = true;
         }
         long long grid = sm_count();
         if (grid > total) grid = total;
         count_launch();
-        if (launch_k(index_score_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes,
+        if (launch_k(index_score_kernel<FP8>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes,
                      stream, true, kmap, qmap, p) != cudaSuccess)
             return DSV4_ERR_LAUNCH;
     }
     return DSV4_OK;
+}
+
+int launch_scores(const dsv4_index_args& a, float* scores, uint32_t* hist, uint32_t* eword,
+                  cudaStream_t stream, const dsv4_compress_args* fresh) {
+    return a.key_fp8 ? launch_scores_fmt<true>(a, scores, hist, eword, stream, fresh)
+                     : launch_scores_fmt<false>(a, scores, hist, eword, stream, fresh);
 }
 }  // namespace
 

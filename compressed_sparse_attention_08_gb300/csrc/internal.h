@@ -13,6 +13,8 @@ namespace dsv4 {
 
 int launch_compress(const dsv4_compress_args& a, cudaStream_t stream);
 int launch_compress_step(const dsv4_compress_step_args& a, cudaStream_t stream);
+// FP8 E4M3 rows: one warp per row, scale = amax / 448 (fp32), codes of x / scale.
+int launch_quantize_rows_fp8(const void* x, int rows, int dim, void* q, float* scale, cudaStream_t stream);
 // Up to two compressions (e.g. main KV and indexer keys) in one launch; either may be null.
 // Both compressions in one launch; the launch also clears `zero_bytes` bytes at `zero` (a
 // 16-byte aligned workspace region, rounded up to 16 bytes) for the kernels after it, or a

@@ -157,6 +157,15 @@ typedef struct dsv4_index_args {
     int32_t* idx_out;         /* int32 [batch, n_q, top_k]                                 */
     float* scores_out;        /* fp32 [batch, n_q, max_comp] copy of the scores, or NULL    */
     int batch, n_q, heads, dim, max_comp, top_k, ratio;
+    /* FP8 index keys ([B] single_shot_inference.py: "Indexer keys are stored as FP8_E4M3 in
+     * the KV cache", scored on the FP8 tensor-core path). key_fp8 = 1: q and keys hold FP8
+     * E4M3 codes ([batch, n_q, heads, dim] and [batch, max_comp, dim] bytes) with one fp32
+     * scale per query head (q_scale [batch, n_q, heads]) and per key (key_scale
+     * [batch, max_comp]), as dsv4_quantize_rows_fp8 writes them; the score is the bf16 form's
+     * definition on the dequantized rows, scale * code. key_fp8 = 0: bf16 rows, scales NULL. */
+    int key_fp8;
+    const float* q_scale;
+    const float* key_scale;
 } dsv4_index_args;
 
 size_t dsv4_indexer_topk_workspace_size(const dsv4_index_args* args);
@@ -264,6 +273,13 @@ typedef struct dsv4_csa_args {
 size_t dsv4_csa_decode_workspace_size(const dsv4_csa_args* args);
 int dsv4_csa_decode(const dsv4_csa_args* args, void* ws, size_t ws_bytes,
                     dsv4_stream_t stream);
+
+/* FP8 E4M3 quantization of bf16 rows (queries or keys for the FP8 indexer): per row
+ * scale = amax / 448 in fp32 (1 for an all-zero row), code = E4M3(x / scale), the division in
+ * fp32, round to nearest even, saturating. x bf16 [rows, dim] -> q [rows, dim] bytes,
+ * scale fp32 [rows]. dim: 32, 64, 128, 256, 512 or 1024. */
+int dsv4_quantize_rows_fp8(const void* x, int rows, int dim, void* q, float* scale,
+                           dsv4_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
  * Utilities.

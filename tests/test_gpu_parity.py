@@ -358,6 +358,87 @@ def test_indexer_cache_shorter_than_one_tile():
         check_topk_row(idx[b, 0], ref_i[b, 0], ref_s[b, 0], nv[b, 0], k, f"b{b}")
 
 
+# ------------------------------------------------------------------ FP8 index keys
+def test_quantize_rows_fp8_matches_oracle():
+    """The GPU quantizer's codes and scales equal the oracle's bit for bit (rows of 32..1024)."""
+    m = csa()
+    rng = np.random.default_rng(21)
+    for rows, dim in ((1000, 128), (64, 512), (3, 32), (5, 1024)):
+        x = synth.f32_to_bf16_bits((rng.standard_normal((rows, dim)) * rng.uniform(0.01, 100, (rows, 1))).astype(np.float32))
+        x[0] = 0                                     # an all-zero row: scale 1
+        xd = dev_bf16(x)
+        q = torch.empty(rows, dim, dtype=torch.uint8, device="cuda")
+        sc = torch.empty(rows, dtype=torch.float32, device="cuda")
+        m.dsv4_quantize_rows_fp8(xd, q, sc)
+        torch.cuda.synchronize()
+        want_q, want_s = oracle.quantize_rows_e4m3(synth.bf16_bits_to_f32(x))
+        assert np.array_equal(q.cpu().numpy(), want_q), f"codes differ ({rows}x{dim})"
+        assert np.array_equal(sc.cpu().numpy(), want_s), f"scales differ ({rows}x{dim})"
+
+
+def _fp8_rows(x_bits):
+    """Oracle quantization of bf16 rows (the inputs of the FP8 scorer come from the oracle)."""
+    return oracle.quantize_rows_e4m3(synth.bf16_bits_to_f32(x_bits))
+
+
+def _run_indexer_fp8(q8, qs, w, k8, ks, n_comp, top_k, ratio=4):
+    m = csa()
+    B, n_q = q8.shape[:2]
+    max_comp = k8.shape[1]
+    qd, kd = dev(q8), dev(k8)
+    qsd, ksd, wd, nd = dev(qs), dev(ks), dev(w), dev(n_comp)
+    idx = torch.empty(B, n_q, top_k, dtype=torch.int32, device="cuda")
+    sc = torch.full((B, n_q, max_comp), float("nan"), dtype=torch.float32, device="cuda")
+    kw = dict(ratio=ratio, scores_out=sc, q_scale=qsd, key_scale=ksd)
+    ws = ws_tensor(m.dsv4_indexer_topk_workspace_size(qd, wd, kd, nd, idx, **kw))
+    m.dsv4_indexer_topk(qd, wd, kd, nd, idx, ws, **kw)
+    torch.cuda.synchronize()
+    st, ew = m.dsv4_read_error_word(ws)
+    assert ew == 0, f"device error word {ew:#x}"
+    return idx.cpu().numpy(), sc.cpu().numpy()
+
+
+@pytest.mark.parametrize("cfg", [1, 3])
+def test_indexer_fp8_keys(cfg):
+    """FP8 E4M3 queries and keys (oracle-quantized): scores against the oracle's FP8 scores,
+    top-k exact up to near ties; at 1M context the selection is also checked against its own
+    scores on every sequence."""
+    wl = WORKLOADS[cfg]
+    x = inputs(cfg)
+    keys = _oracle_keys(x, wl) if cfg == 1 else x["keys"]
+    q8, qs = _fp8_rows(x["q_I"])
+    k8, ks = _fp8_rows(keys)
+    idx, sc = _run_indexer_fp8(q8, qs, x["w"], k8, ks, x["n_comp"], wl.top_k)
+    seqs = [0, 9, 15] if cfg == 1 else [0, 3]
+    for b in seqs:
+        ref_s, nv = oracle.index_scores_fp8(q8[b:b + 1], qs[b:b + 1], x["w"][b:b + 1], k8[b:b + 1],
+                                            ks[b:b + 1], x["n_comp"][b:b + 1], wl.ratio)
+        ref_i = oracle.topk(ref_s, nv, wl.top_k)
+        _check_scores(sc[b, 0], ref_s[0, 0], nv[0, 0])
+        check_topk_row(idx[b, 0], ref_i[0, 0], ref_s[0, 0], nv[0, 0], wl.top_k, f"b{b}")
+    for b in range(wl.batch):
+        topk_valid_for_scores(idx[b, 0], sc[b, 0], x["n_comp"][b], wl.top_k, f"b{b}")
+
+
+def test_indexer_fp8_ragged_and_short():
+    """FP8 keys: 8 heads, ragged n_comp (0 included), a cache that ends inside a 512-key stage."""
+    rng = np.random.default_rng(22)
+    B, H, N, k = 4, 8, 700, 96
+    q = synth.f32_to_bf16_bits(rng.standard_normal((B, 1, H, 128)).astype(np.float32))
+    keys = synth.f32_to_bf16_bits(rng.standard_normal((B, N, 128)).astype(np.float32))
+    w = rng.standard_normal((B, 1, H)).astype(np.float32)
+    n_comp = np.array([700, 0, 50, 513], np.int32)
+    q8, qs = _fp8_rows(q)
+    k8, ks = _fp8_rows(keys)
+    idx, sc = _run_indexer_fp8(q8, qs, w, k8, ks, n_comp, k)
+    ref_s, nv = oracle.index_scores_fp8(q8, qs, w, k8, ks, n_comp, 4)
+    ref_i = oracle.topk(ref_s, nv, k)
+    for b in range(B):
+        if nv[b, 0]:
+            _check_scores(sc[b, 0], ref_s[b, 0], nv[b, 0])
+        check_topk_row(idx[b, 0], ref_i[b, 0], ref_s[b, 0], nv[b, 0], k, f"b{b}")
+
+
 # ------------------------------------------------------------------ stage 3 alone: exact top-k
 def _run_topk(scores, n_vis, k):
     m = csa()
