@@ -148,6 +148,82 @@ def prefill_scoring(m, steps):
             "peak_kind": kind, "unit": "TFLOP/s", "frac": achieved / peak}
 
 
+def fp8_keys_step(m, _abi, t, wl, steps, stream, peak):
+    """The same decode step with the index-key cache in FP8 E4M3 (codes + one fp32 scale per
+    key): the compressor writes the newest key in FP8, the scorer reads 128 + 4 bytes per key
+    instead of 256. The query quantization runs inside the step. Reported beside the bf16
+    headline, not as it."""
+    import torch
+    B = wl.batch
+    keys8 = torch.empty(B, wl.max_comp, wl.idx_dim, dtype=torch.uint8, device="cuda")
+    kscale = torch.empty(B, wl.max_comp, dtype=torch.float32, device="cuda")
+    q8 = torch.empty(t["q_I"].shape, dtype=torch.uint8, device="cuda")
+    qscale = torch.empty(t["q_I"].shape[:-1], dtype=torch.float32, device="cuda")
+    with torch.cuda.stream(stream):
+        m.dsv4_quantize_rows_fp8(t["keys"], keys8, kscale, stream=stream)
+    stream.synchronize()
+    cq = _abi.compress_args(t["C_I"], t["Z_I"], t["bias_I"], t["gamma_I"], t["pos0"], keys8,
+                            ratio=wl.ratio, out_row0=t["append_row"], out_scale=kscale)
+    ck = _abi.compress_args(t["C"], t["Z"], t["bias"], t["gamma"], t["pos0"], t["kv"], ratio=wl.ratio,
+                            out_row0=t["append_row"])
+    ia = _abi.index_args(q8, t["w"], keys8, t["n_comp"], t["idx"], ratio=wl.ratio, q_scale=qscale,
+                         key_scale=kscale)
+    aa = _abi.attn_args(t["q"], t["sink"], t["kv"], t["n_comp"], t["win"], t["win_len"], t["out"],
+                        idx=t["idx"], window=wl.window, ratio=wl.ratio, gather=t["gather"])
+    nbytes = m.dsv4_csa_decode_workspace_size(attn=aa, index=ia, compress_kv=ck, compress_keys=cq)
+    ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device="cuda")
+
+    def step(s):
+        m.dsv4_quantize_rows_fp8(t["q_I"], q8, qscale, stream=s)
+        launches = m.dsv4_last_launch_count()
+        m.dsv4_csa_decode(ws, attn=aa, index=ia, compress_kv=ck, compress_keys=cq, stream=s)
+        return launches + m.dsv4_last_launch_count()
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            launches = step(stream)
+    stream.synchronize()
+    st, ew = m.dsv4_read_error_word(ws, stream)
+    if ew:
+        raise SystemExit(f"device error word {ew:#x} in the FP8-key step")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            step(stream)
+    stream.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(10):
+            graph.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    # the scorer alone on the FP8 cache
+    score_ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    kw = dict(ratio=wl.ratio, stream=stream, q_scale=qscale, key_scale=kscale)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            m.dsv4_index_score(q8, t["w"], keys8, t["n_comp"], t["scores"], score_ws, **kw)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for a, b in evs:
+            a.record(stream)
+            m.dsv4_index_score(q8, t["w"], keys8, t["n_comp"], t["scores"], score_ws, **kw)
+            b.record(stream)
+    torch.cuda.synchronize()
+    score_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    sb = B * wl.n_comp * (wl.idx_dim + 4 + 4) + B * wl.idx_heads * (wl.idx_dim + 4 + 4)
+    gbs = sb / (score_ms * 1e-3) / 1e9
+    return {"value": B / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
+            "launches_per_step": launches, "dtype": "fp8 e4m3 index keys, bf16 KV",
+            "scorer": {"kernel": "index_score_kernel<FP8>", "bytes_per_launch": sb,
+                       "ms_per_launch": score_ms, "achieved": gbs, "peak": peak, "unit": "GB/s",
+                       "frac": gbs / peak}}
+
+
 def profile_traffic():
     """dram bytes per scoring launch from the committed ncu summary, if the kernel source
     still matches the hash recorded there; else None."""
@@ -453,6 +529,7 @@ def run_ours(args):
     }
     if world == 1:
         line["prefill_scoring"] = prefill_scoring(m, args.steps)
+        line["fp8_keys"] = fp8_keys_step(m, _abi, t, wl, args.steps, stream, peak)
     if world == 1 and not args.no_cpu_baseline:
         x0 = make_inputs(wl, batch=1)
         line["cpu_baseline"] = cpu_baseline(wl, x0)

@@ -38,7 +38,8 @@ class CompressArgs(ctypes.Structure):
     _fields_ = [("C", P), ("Z", P), ("bias", P), ("gamma", P), ("pos0", P), ("out", P),
                 ("out_row0", P), ("batch", I), ("tokens", I), ("dim", I), ("ratio", I),
                 ("rope_dim", I), ("out_rows", I), ("eps", ctypes.c_float),
-                ("rope_theta", ctypes.c_double), ("overlap", I), ("prev_C", P), ("prev_Z", P)]
+                ("rope_theta", ctypes.c_double), ("overlap", I), ("prev_C", P), ("prev_Z", P),
+                ("out_fp8", I), ("out_scale", P)]
 
 
 class StepArgs(ctypes.Structure):
@@ -166,17 +167,23 @@ def _dt():
 
 # ------------------------------------------------------------------ argument builders
 def compress_args(C, Z, bias, gamma, pos0, out, *, ratio, rope_dim=64, eps=1e-6,
-                  rope_theta=10000.0, out_row0=None, overlap=False, prev_C=None, prev_Z=None):
+                  rope_theta=10000.0, out_row0=None, overlap=False, prev_C=None, prev_Z=None,
+                  out_scale=None):
     """overlap=True: the two-stream (CSA) form, C and Z [B, T, 2*dim], bias [ratio, 2*dim],
-    optional prev_C / prev_Z [B, ratio, 2*dim] (the block before C's first block)."""
+    optional prev_C / prev_Z [B, ratio, 2*dim] (the block before C's first block).
+    out_scale given: FP8 entries, out uint8 [B, rows, dim] and out_scale fp32 [B, rows]."""
+    import torch
     bf16, f32, i32, i64 = _dt()
     B, T, w = C.shape
     d = w // 2 if overlap else w
+    fp8 = out_scale is not None
     return CompressArgs(_ptr(C, bf16, "C"), _ptr(Z, bf16, "Z"), _ptr(bias, f32, "bias"),
-                        _ptr(gamma, f32, "gamma"), _ptr(pos0, i64, "pos0"), _ptr(out, bf16, "out"),
+                        _ptr(gamma, f32, "gamma"), _ptr(pos0, i64, "pos0"),
+                        _ptr(out, torch.uint8 if fp8 else bf16, "out"),
                         _ptr(out_row0, i32, "out_row0", True), B, T, d, ratio, rope_dim,
                         out.shape[1], eps, rope_theta, 1 if overlap else 0,
-                        _ptr(prev_C, bf16, "prev_C", True), _ptr(prev_Z, bf16, "prev_Z", True))
+                        _ptr(prev_C, bf16, "prev_C", True), _ptr(prev_Z, bf16, "prev_Z", True),
+                        1 if fp8 else 0, _ptr(out_scale, f32, "out_scale", True))
 
 
 def index_args(q, w, keys, n_comp, idx_out, *, ratio, q_pos=None, scores_out=None, q_scale=None,
@@ -226,10 +233,10 @@ def attn_args(q, sink, comp_kv, n_comp, win, win_len, out, *, idx=None, top_k=No
 # ------------------------------------------------------------------ entry points
 def dsv4_compress(C, Z, bias, gamma, pos0, out, *, ratio, rope_dim=64, eps=1e-6,
                   rope_theta=10000.0, out_row0=None, overlap=False, prev_C=None, prev_Z=None,
-                  stream=None):
+                  out_scale=None, stream=None):
     a = compress_args(C, Z, bias, gamma, pos0, out, ratio=ratio, rope_dim=rope_dim, eps=eps,
                       rope_theta=rope_theta, out_row0=out_row0, overlap=overlap, prev_C=prev_C,
-                      prev_Z=prev_Z)
+                      prev_Z=prev_Z, out_scale=out_scale)
     _check(library().dsv4_compress(ctypes.byref(a), _stream(stream)), "dsv4_compress")
 
 

@@ -47,6 +47,8 @@ bool compress_ok(const dsv4_compress_args* a) {
     if (a->overlap != 0 && a->overlap != 1) return false;
     if ((a->prev_C == nullptr) != (a->prev_Z == nullptr)) return false;
     if (a->prev_C && (!a->overlap || !dev_ptr_ok(a->prev_C) || !dev_ptr_ok(a->prev_Z))) return false;
+    if (a->out_fp8 != 0 && a->out_fp8 != 1) return false;
+    if (a->out_fp8 ? !dev_ptr_ok(a->out_scale) : a->out_scale != nullptr) return false;
     return true;
 }
 
@@ -273,6 +275,10 @@ static bool csa_ok(const dsv4_csa_args* a) {
         if (!index_ok(&x)) return false;
         if (y.idx != x.idx_out || y.top_k != x.top_k || y.batch != x.batch || y.n_q != x.n_q ||
             y.max_comp != x.max_comp || y.n_comp != x.n_comp || y.ratio != x.ratio || y.q_pos != x.q_pos)
+            return false;
+        // a key cache written in this step is read in the format it was written in
+        const dsv4_compress_args* k = a->compress_keys;
+        if (k && k->out == x.keys && (k->out_fp8 != x.key_fp8 || (k->out_fp8 && k->out_scale != x.key_scale)))
             return false;
     } else if (a->attn->idx) {
         return false;

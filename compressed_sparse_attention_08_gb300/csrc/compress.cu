@@ -28,6 +28,8 @@
 // output, written straight into the caller's cache rows.
 #include <cmath>
 
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -44,6 +46,8 @@ struct CompressJob {
     const __nv_bfloat16* prev_C;     // two-stream form: the block before C's first block, or null
     const __nv_bfloat16* prev_Z;
     int overlap;                     // 0: plain blocks; 1: two-stream (CSA) form, 2*dim channels
+    float* out_scale;                // FP8 output: [batch, out_rows] entry scales, out holds E4M3
+    int out_fp8;
     const float* bias;
     const float* gamma;
     const int64_t* pos0;
@@ -70,6 +74,8 @@ struct EntryIn {
     float eps;
     double pos;                  // RoPE position of the entry
     __nv_bfloat16* dst;          // the entry's output row, or null (computed, not stored)
+    uint8_t* dst8;               // FP8 output: the entry's E4M3 row (dst is then null), or null
+    float* dst_scale;            // FP8 output: the entry's scale
 };
 
 // The whole CTA (kThreads) computes one entry: per-channel online softmax of Z + bias over the
@@ -152,6 +158,22 @@ __device__ void entry_math(const EntryIn& in, const double* freq, float* y, floa
     __syncthreads();
     if (in.dst)
         for (int c = tid; c < dim; c += kThreads) in.dst[c] = __float2bfloat16_rn(y[c]);
+    if (in.dst8) {
+        // FP8 E4M3 entry: scale = amax / 448 over the entry (fp32), code = E4M3(y / scale)
+        float amax = 0.f;
+        for (int c = tid; c < dim; c += kThreads) amax = fmaxf(amax, fabsf(y[c]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        if ((tid & 31) == 0) warp_sum[tid >> 5] = amax;
+        __syncthreads();
+        float m = 0.f;
+#pragma unroll
+        for (int k = 0; k < kThreads / 32; ++k) m = fmaxf(m, warp_sum[k]);
+        const float sc = m > 0.f ? m / 448.0f : 1.0f;
+        if (tid == 0) *in.dst_scale = sc;
+        for (int c = tid; c < dim; c += kThreads)
+            in.dst8[c] = static_cast<uint8_t>(__nv_cvt_float_to_fp8(y[c] / sc, __NV_SATFINITE, __NV_E4M3));
+    }
 }
 
 // zero_p/zero_n16: a workspace region (16-byte words) this launch clears for the kernels after
@@ -174,6 +196,8 @@ compress_kernel(const __grid_constant__ CompressJob j0, const __grid_constant__ 
     const __nv_bfloat16* __restrict__ prevCp = second ? j1.prev_C : j0.prev_C;
     const __nv_bfloat16* __restrict__ prevZp = second ? j1.prev_Z : j0.prev_Z;
     const int overlap = second ? j1.overlap : j0.overlap;
+    const int out_fp8 = second ? j1.out_fp8 : j0.out_fp8;
+    float* out_scalep = second ? j1.out_scale : j0.out_scale;
     const float* __restrict__ biasp = second ? j1.bias : j0.bias;
     const float* __restrict__ gammap = second ? j1.gamma : j0.gamma;
     const int64_t* pos0p = second ? j1.pos0 : j0.pos0;
@@ -232,7 +256,11 @@ compress_kernel(const __grid_constant__ CompressJob j0, const __grid_constant__ 
     in.eps = eps;
     in.pos = static_cast<double>(pos_s + static_cast<int64_t>(b) * ratio);
     // rows outside the destination are not written
-    in.dst = row >= 0 && row < out_rows ? outp + (static_cast<size_t>(s) * out_rows + row) * dim : nullptr;
+    const bool in_range = row >= 0 && row < out_rows;
+    const size_t orow = static_cast<size_t>(s) * out_rows + row;
+    in.dst = in_range && !out_fp8 ? outp + orow * dim : nullptr;
+    in.dst8 = in_range && out_fp8 ? reinterpret_cast<uint8_t*>(outp) + orow * dim : nullptr;
+    in.dst_scale = in_range && out_fp8 ? out_scalep + orow : nullptr;
     entry_math(in, freq, y, warp_sum);
 }
 
@@ -243,6 +271,8 @@ CompressJob make_job(const dsv4_compress_args& a) {
     j.prev_C = static_cast<const __nv_bfloat16*>(a.prev_C);
     j.prev_Z = static_cast<const __nv_bfloat16*>(a.prev_Z);
     j.overlap = a.overlap;
+    j.out_fp8 = a.out_fp8;
+    j.out_scale = a.out_scale;
     j.bias = a.bias;
     j.gamma = a.gamma;
     j.pos0 = a.pos0;
@@ -325,6 +355,8 @@ compress_step_kernel(const __grid_constant__ StepJob j) {
     in.pos = static_cast<double>(j.pos[s] - (j.ratio - 1));   // the block's first token
     // a full cache keeps its rows: the entry is computed but not stored, n_comp stays
     in.dst = nc >= 0 && nc < j.out_rows ? j.out + (static_cast<size_t>(s) * j.out_rows + nc) * j.dim : nullptr;
+    in.dst8 = nullptr;
+    in.dst_scale = nullptr;
     entry_math(in, freq, y, warp_sum);
     if (j.overlap)                                 // this block is stream a of the next entry
         for (size_t c = tid; c < blk; c += kThreads) prev[c] = cur[c];

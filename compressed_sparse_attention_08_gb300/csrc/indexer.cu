@@ -14,7 +14,7 @@
 // Each row of D is one key's per-head dot products, so the epilogue thread that owns TMEM
 // lane i reduces sum_h w_h ReLU(D[i, h]) alone, with no cross-thread reduction.
 //
-// CTA = 6 warps, persistent, one per SM, warp-specialised:
+// CTA = 6 warps (bf16 keys) or 10 (FP8 keys), persistent, one per SM, warp-specialised:
 //   warp 0  TMA producer: key stages of 256 keys (two 128-key MMA tiles; two 128-byte-
 //           swizzled boxes of 64 dims x 256 rows) into a ring of kStages 64 KB buffers; the
 //           row's queries (N x 128) into the query buffer
@@ -24,7 +24,9 @@
 //   warps 2-5  epilogue: tcgen05.ld of the accumulator (thread = key), weighted ReLU sum in
 //           fp32, coalesced store of the score; optionally a shared-memory histogram of the
 //           scores' top 12 key bits, flushed per row into the top-k workspace (so the
-//           long-row top-k needs no histogram pass of its own).
+//           long-row top-k needs no histogram pass of its own). FP8 keys: warps 2-9, two
+//           groups of four taking alternate accumulators; a 64 KB stage holds 512 keys, and
+//           one group alone could not drain four tiles in the time the stage takes to arrive.
 // Why 64 KB stages: a stage stays busy from its copy until the MMA that reads it completes,
 // and that hand-off adds a few hundred ns per stage; with 32 KB stages the cost took about a
 // sixth of the bandwidth, with 64 KB stages it is hidden. Shared memory then holds one query
@@ -46,9 +48,7 @@ constexpr int kTileKeys = 128;              // UMMA M
 constexpr int kDim = 128;                   // key width = UMMA K total
 constexpr int kMaxHeads = 64;               // UMMA N upper bound
 constexpr int kStages = 3;
-constexpr int kAccBufs = 4;
 constexpr int kAccCols = 64;                // TMEM columns per accumulator
-constexpr uint32_t kTmemCols = kAccBufs * kAccCols;   // 256 (power of two)
 constexpr uint32_t kStageBytes = 64 * 1024;                // two 32 KiB TMA boxes
 constexpr uint32_t kBoxBytes = kStageBytes / 2;
 constexpr uint32_t kQBufBytes = kMaxHeads * kDim * 2;      // 16 KiB (bf16 queries)
@@ -63,8 +63,13 @@ struct KeyFmt {
     static constexpr int kSub = kStageKeys / kTileKeys;
     static constexpr int kKSteps = kDim * kElem / 32;
     static constexpr int kBoxInner = 128 / kElem;          // elements per 128-byte box row
+    static constexpr int kEpiGroups = FP8 ? 2 : 1;         // epilogue groups of 4 warps
+    // TMEM accumulators: two stages' worth of tiles, so the MMAs of a stage wait only for the
+    // epilogue of the stage two back (256 or 512 columns: a power of two)
+    static constexpr int kAccBufs = 2 * kSub;
+    static constexpr uint32_t kTmemCols = kAccBufs * kAccCols;
+    static constexpr int kThreads = 64 + 128 * kEpiGroups;
 };
-constexpr int kThreads = 192;
 constexpr int kHistBins = 4096;             // top 12 bits of the order-preserving score key
 constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + kQBufBytes;
 
@@ -79,7 +84,7 @@ struct ScoreParams {
     uint32_t* eword;
     const float* q_scale;    // FP8 keys: [rows, heads] query scales, else null
     const float* key_scale;  // FP8 keys: [batch, max_comp] key scales, else null
-    int rows, n_q, heads, n_pad, max_comp, ratio, stages_per_row;
+    int rows, n_q, heads, max_comp, ratio, stages_per_row;
 };
 
 // The stages one CTA scores, as positions f = row * stages_per_row + stage: f = begin,
@@ -100,13 +105,14 @@ __device__ __forceinline__ Walk cta_walk(int rows, int per_row) {
     return {r * per_row + (c - cb), (r + 1) * per_row, ce - cb};
 }
 
-template <bool FP8>
-__global__ void __launch_bounds__(kThreads, 1)
+// NP: the heads padded to a multiple of 16 (the UMMA N and the TMEM columns the epilogue reads)
+template <bool FP8, int NP>
+__global__ void __launch_bounds__(KeyFmt<FP8>::kThreads, 1)
 index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap qmap, ScoreParams p) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t full_bar[kStages], empty_bar[kStages];
-    __shared__ uint64_t tfull_bar[kAccBufs], tempty_bar[kAccBufs];
+    __shared__ uint64_t tfull_bar[KeyFmt<FP8>::kAccBufs], tempty_bar[KeyFmt<FP8>::kAccBufs];
     __shared__ uint64_t qfull_bar, qempty_bar, done_bar;
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
@@ -116,6 +122,9 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
 
     using F = KeyFmt<FP8>;
     constexpr int kStageKeys = F::kStageKeys, kSub = F::kSub;
+    constexpr int kThreads = F::kThreads, kEpiGroups = F::kEpiGroups, kAccBufs = F::kAccBufs;
+    constexpr uint32_t kTmemCols = F::kTmemCols;
+    __shared__ __align__(16) float s_wv[kEpiGroups][FP8 ? kMaxHeads : 4];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_trigger();
     // 1024-byte aligned operand buffers (the 128-byte swizzle repeats every 1024 bytes)
@@ -147,8 +156,8 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
     const uint32_t tmem_base = tmem_slot;
 
     const Walk wk = cta_walk(p.rows, p.stages_per_row);
-    const uint32_t idesc = FP8 ? idesc_e4m3_f32(kTileKeys, p.n_pad) : idesc_bf16_f32(kTileKeys, p.n_pad);
-    const uint32_t q_half = static_cast<uint32_t>(p.n_pad) * 128u;   // bf16: bytes of one 64-dim half
+    const uint32_t idesc = FP8 ? idesc_e4m3_f32(kTileKeys, NP) : idesc_bf16_f32(kTileKeys, NP);
+    const uint32_t q_half = static_cast<uint32_t>(NP) * 128u;   // bf16: bytes of one 64-dim half
 
     if (warp == 0) {
         if (lane == 0) {
@@ -264,24 +273,35 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
         }
         __syncwarp();
     } else {
-        // epilogue: warps 2..5 -> TMEM lane quarter (warp % 4)
+        // epilogue: kEpiGroups groups of 4 warps; warp -> TMEM lane quarter (warp % 4); group g
+        // takes the accumulators acc with acc % kEpiGroups == g, so with two groups two tiles
+        // drain at once (FP8: four tiles per stage, twice the keys per byte of bf16)
         const int quarter = warp & 3;
+        const int group = (warp - 2) >> 2;
         const int lrow = quarter * 32 + lane;
-        const int etid = threadIdx.x - 64;                 // 0..127 within the epilogue
+        const int etid = threadIdx.x - 64;                 // 0 .. 128 * kEpiGroups - 1
+        const int gtid = etid & 127;                       // within the group
         const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
         int acc = 0, cur_row = -1, nv = 0;
         uint32_t acc_phase = 0;
         bool dead = false;        // a wait ran out: keep walking the tiles (same barriers), no work
-        float wv[kMaxHeads];
+        // head weights of the current row: registers (bf16) or the group's shared copy (FP8,
+        // broadcast reads; it keeps the thread at a register count that lets a compressor CTA
+        // share the SM)
+        float wv[FP8 ? 1 : NP];
         // The histogram is private to the CTA and flushed to the row's global histogram when
-        // the row changes, and before a 16-bit count could overflow (every 255 stages of 256
-        // keys). Every epilogue thread passes the same flush barriers, dead or not.
+        // the row changes, and before a 16-bit count could overflow (every 255 stages). Every
+        // epilogue thread passes the same flush barriers, dead or not.
         int since_flush = 0;
+        auto group_sync = [](int g) {                      // constant barrier ids 2 and 3
+            if (g == 0) named_bar_sync(2, 128);
+            else named_bar_sync(3, 128);
+        };
         auto flush = [&](int r) {
             pdl_wait();      // the histogram may have been cleared by the preceding kernel
-            asm volatile("bar.sync 1, 128;" ::: "memory");
+            named_bar_sync(1, 128 * kEpiGroups);
             uint32_t* g = p.hist + static_cast<size_t>(r) * kHistBins;
-            for (int i = etid; i < kHistBins / 2; i += 128) {
+            for (int i = etid; i < kHistBins / 2; i += 128 * kEpiGroups) {
                 const uint32_t v = s_hist[i];
                 if (v) {
                     if (v & 0xFFFFu) atomicAdd(&g[2 * i], v & 0xFFFFu);
@@ -289,12 +309,36 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                     s_hist[i] = 0;
                 }
             }
-            asm volatile("bar.sync 1, 128;" ::: "memory");
+            named_bar_sync(1, 128 * kEpiGroups);
             since_flush = 0;
         };
+        // FP8: the key scales of the next stage are loaded one walk item ahead (a DRAM read per
+        // tile would otherwise stall the epilogue once per 128 keys). Every key scale is final
+        // once the preceding kernel (which may write the newest key) has completed.
+        float ks_cur[kSub], ks_next[kSub];
+        auto load_ks = [&](long long g) {
+            if (g >= wk.end) return;
+            const int r_ = static_cast<int>(g / p.stages_per_row);
+            const int s_ = static_cast<int>(g % p.stages_per_row);
+            const float* kb = p.key_scale + static_cast<size_t>(r_ / p.n_q) * p.max_comp;
+#pragma unroll
+            for (int j = 0; j < kSub; ++j) {
+                const int key = (s_ * kSub + j) * kTileKeys + lrow;
+                ks_next[j] = key < p.max_comp ? __ldcg(kb + key) : 0.f;
+            }
+        };
+        if constexpr (FP8) {
+            pdl_wait();
+            load_ks(wk.begin);
+        }
         for (long long f = wk.begin; f < wk.end; f += wk.step) {
             const int row = static_cast<int>(f / p.stages_per_row);
             const int st = static_cast<int>(f % p.stages_per_row);
+            if constexpr (FP8) {
+#pragma unroll
+                for (int j = 0; j < kSub; ++j) ks_cur[j] = ks_next[j];
+                load_ks(f + wk.step);
+            }
             if (row != cur_row || since_flush == 255) {
                 if (p.hist && cur_row >= 0) flush(cur_row);
             }
@@ -302,60 +346,84 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
             if (row != cur_row) {
                 nv = row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, row, nullptr);
                 cur_row = row;
+                if constexpr (FP8) {
+                    // the query scale folds into the head's weight (ReLU commutes with it)
+                    group_sync(group);                          // the group is done with the old row
+                    if (gtid < kMaxHeads) {
+                        const size_t o = static_cast<size_t>(row) * p.heads + gtid;
+                        s_wv[group][gtid] = gtid < p.heads ? __ldg(&p.w[o]) * __ldg(&p.q_scale[o]) : 0.f;
+                    }
+                    group_sync(group);
+                } else {
 #pragma unroll
-                for (int h = 0; h < kMaxHeads; ++h) {
-                    float wh = h < p.heads ? __ldg(&p.w[static_cast<size_t>(row) * p.heads + h]) : 0.f;
-                    // FP8: the head's query scale folds into its weight (ReLU commutes with it)
-                    if (FP8 && h < p.heads) wh *= __ldg(&p.q_scale[static_cast<size_t>(row) * p.heads + h]);
-                    wv[h] = wh;
+                    for (int h = 0; h < NP; ++h)
+                        wv[h] = h < p.heads ? __ldg(&p.w[static_cast<size_t>(row) * p.heads + h]) : 0.f;
                 }
             }
             for (int j = 0; j < kSub; ++j) {
                 const int tile = st * kSub + j;
                 if (tile * kTileKeys >= nv || dead) break;
-                if (!mbar_wait(&tfull_bar[acc], acc_phase, &abort_flag)) {
+                const int my_acc = acc;
+                const uint32_t my_phase = acc_phase;
+                if (++acc == kAccBufs) { acc = 0; acc_phase ^= 1; }
+                if (kEpiGroups > 1 && (my_acc % kEpiGroups) != group) continue;
+                if (!mbar_wait(&tfull_bar[my_acc], my_phase, &abort_flag)) {
                     flag_error(p.eword, DSV4_EWORD_TIMEOUT);
                     abort_flag = 1;
                     dead = true;
                     break;
                 }
                 tc_fence_after();
-                // exactly the n_pad columns the MMA wrote (columns past them hold stale values)
-                uint32_t r[64];
-                const uint32_t ta = tmem_base + lane_addr + static_cast<uint32_t>(acc * kAccCols);
-                if (p.n_pad == 64) {
+                // exactly the NP columns the MMA wrote (columns past them hold stale values)
+                uint32_t r[NP];
+                const uint32_t ta = tmem_base + lane_addr + static_cast<uint32_t>(my_acc * kAccCols);
+                if constexpr (NP == 64) {
                     DSV4_TMEM_LD_32x32b_X64(ta, r);
-                } else if (p.n_pad == 32) {
+                } else if constexpr (NP == 32) {
                     DSV4_TMEM_LD_32x32b_X32(ta, r);
-#pragma unroll
-                    for (int h = 32; h < 64; ++h) r[h] = 0u;
-                } else if (p.n_pad == 48) {
+                } else if constexpr (NP == 48) {
                     DSV4_TMEM_LD_32x32b_X32(ta, r);
                     uint32_t* r2 = r + 32;
                     DSV4_TMEM_LD_32x32b_X16(ta + 32u, r2);
-#pragma unroll
-                    for (int h = 48; h < 64; ++h) r[h] = 0u;
                 } else {
                     DSV4_TMEM_LD_32x32b_X16(ta, r);
-#pragma unroll
-                    for (int h = 16; h < 64; ++h) r[h] = 0u;
                 }
                 tmem_wait_ld();
                 tc_fence_before();
-                mbar_arrive(&tempty_bar[acc]);
+                mbar_arrive(&tempty_bar[my_acc]);
                 float s = 0.f;
+                if constexpr (FP8) {
+                    // four partial sums (heads h mod 4) in two packed pairs: half the FMA
+                    // instructions and a quarter of the dependent-FMA latency per key (the
+                    // epilogue, not HBM, sets the pace of 512-key stages)
+                    const float4* w4 = reinterpret_cast<const float4*>(s_wv[group]);
+                    uint64_t a01 = 0, a23 = 0;
 #pragma unroll
-                for (int h = 0; h < kMaxHeads; ++h) s = fmaf(wv[h], fmaxf(__uint_as_float(r[h]), 0.f), s);
+                    for (int h4 = 0; h4 < NP / 4; ++h4) {
+                        const float4 w = w4[h4];
+                        fma_f32x2(a01, pack_f32x2(fmaxf(__uint_as_float(r[4 * h4 + 0]), 0.f),
+                                                  fmaxf(__uint_as_float(r[4 * h4 + 1]), 0.f)),
+                                  pack_f32x2(w.x, w.y));
+                        fma_f32x2(a23, pack_f32x2(fmaxf(__uint_as_float(r[4 * h4 + 2]), 0.f),
+                                                  fmaxf(__uint_as_float(r[4 * h4 + 3]), 0.f)),
+                                  pack_f32x2(w.z, w.w));
+                    }
+                    float s0, s1, s2, s3;
+                    unpack_f32x2(a01, s0, s1);
+                    unpack_f32x2(a23, s2, s3);
+                    s = ((s0 + s1) + (s2 + s3)) * ks_cur[j];
+                } else {
+#pragma unroll
+                    for (int h = 0; h < NP; ++h) s = fmaf(wv[h], fmaxf(__uint_as_float(r[h]), 0.f), s);
+                }
                 const int key = tile * kTileKeys + lrow;
                 if (key < nv) {
-                    if (FP8) s *= __ldg(&p.key_scale[static_cast<size_t>(row / p.n_q) * p.max_comp + key]);
                     p.scores[static_cast<size_t>(row) * p.max_comp + key] = s;
                     if (p.hist) {
                         const uint32_t bin = float_to_key(s) >> 20;
                         atomicAdd(&s_hist[bin >> 1], (bin & 1u) ? 0x10000u : 1u);
                     }
                 }
-                if (++acc == kAccBufs) { acc = 0; acc_phase ^= 1; }
             }
         }
         if (p.hist && cur_row >= 0) flush(cur_row);
@@ -422,7 +490,7 @@ size_t index_zero_bytes(const dsv4_index_args& a) {
 }
 
 namespace {
-template <bool FP8>
+template <bool FP8, int NP>
 int launch_scores_fmt(const dsv4_index_args& a, float* scores, uint32_t* hist, uint32_t* eword,
                       cudaStream_t stream, const dsv4_compress_args* fresh) {
     using F = KeyFmt<FP8>;
@@ -466,7 +534,6 @@ int launch_scores_fmt(const dsv4_index_args& a, float* scores, uint32_t* hist, u
     p.rows = rows;
     p.n_q = a.n_q;
     p.heads = a.heads;
-    p.n_pad = (a.heads + 15) / 16 * 16;
     p.max_comp = a.max_comp;
     p.ratio = a.ratio;
     p.stages_per_row = (a.max_comp + F::kStageKeys - 1) / F::kStageKeys;
@@ -474,14 +541,14 @@ int launch_scores_fmt(const dsv4_index_args& a, float* scores, uint32_t* hist, u
     if (total > 0) {
         static bool attr_set = false;
         if (!attr_set) {
-            cudaFuncSetAttribute(index_score_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            cudaFuncSetAttribute(index_score_kernel<FP8, NP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kSmemBytes));
             attr_set = true;
         }
         long long grid = sm_count();
         if (grid > total) grid = total;
         count_launch();
-        if (launch_k(index_score_kernel<FP8>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes,
+        if (launch_k(index_score_kernel<FP8, NP>, dim3(static_cast<unsigned>(grid)), dim3(F::kThreads), kSmemBytes,
                      stream, true, kmap, qmap, p) != cudaSuccess)
             return DSV4_ERR_LAUNCH;
     }
@@ -490,8 +557,17 @@ int launch_scores_fmt(const dsv4_index_args& a, float* scores, uint32_t* hist, u
 
 int launch_scores(const dsv4_index_args& a, float* scores, uint32_t* hist, uint32_t* eword,
                   cudaStream_t stream, const dsv4_compress_args* fresh) {
-    return a.key_fp8 ? launch_scores_fmt<true>(a, scores, hist, eword, stream, fresh)
-                     : launch_scores_fmt<false>(a, scores, hist, eword, stream, fresh);
+    const int n_pad = (a.heads + 15) / 16 * 16;
+#define DSV4_SCORES_NP(np)                                                               \
+    if (n_pad == np)                                                                     \
+        return a.key_fp8 ? launch_scores_fmt<true, np>(a, scores, hist, eword, stream, fresh) \
+                         : launch_scores_fmt<false, np>(a, scores, hist, eword, stream, fresh);
+    DSV4_SCORES_NP(16)
+    DSV4_SCORES_NP(32)
+    DSV4_SCORES_NP(48)
+    DSV4_SCORES_NP(64)
+#undef DSV4_SCORES_NP
+    return DSV4_ERR_INVALID_ARG;
 }
 }  // namespace
 

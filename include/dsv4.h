@@ -99,6 +99,12 @@ typedef struct dsv4_compress_args {
     int overlap;
     const void* prev_C;
     const void* prev_Z;
+    /* FP8 key cache (for the FP8 indexer, see dsv4_index_args.key_fp8): out_fp8 = 1 stores each
+     * entry as FP8 E4M3 codes (out: bytes [batch, out_rows, dim]) with its fp32 scale in
+     * out_scale [batch, out_rows], quantized from the entry's fp32 value after RoPE exactly as
+     * dsv4_quantize_rows_fp8 quantizes a row. out_fp8 = 0: bf16 entries, out_scale NULL. */
+    int out_fp8;
+    float* out_scale;
 } dsv4_compress_args;
 
 int dsv4_compress(const dsv4_compress_args* args, dsv4_stream_t stream);

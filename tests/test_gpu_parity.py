@@ -439,6 +439,73 @@ def test_indexer_fp8_ragged_and_short():
         check_topk_row(idx[b, 0], ref_i[b, 0], ref_s[b, 0], nv[b, 0], k, f"b{b}")
 
 
+def _e4m3_ord(codes):
+    """E4M3 codes as signed ordinals (sign-magnitude -> integer line; +0 and -0 both 0)."""
+    c = np.asarray(codes, np.int32)
+    mag = c & 0x7F
+    return np.where(c & 0x80, -mag, mag)
+
+
+def _e4m3_step(codes):
+    """Spacing of the E4M3 grid at each code's magnitude: 2^(max(e, 1) - 10)."""
+    e = (np.asarray(codes, np.int32) & 0x7F) >> 3
+    return np.ldexp(1.0, np.maximum(e, 1) - 10)
+
+
+def _check_fp8_cache(got8, got_s, ref_f64, what):
+    """An FP8 cache written from entries computed in fp32 against the oracle's fp64 entries
+    quantized the same way: scales within 1e-5 relative, codes within one E4M3 step, and
+    almost all codes equal (a code can move only where fp32 and fp64 round across a grid
+    midpoint). Returns the keys whose row differs from the oracle's."""
+    d = ref_f64.shape[-1]
+    want8, want_s = oracle.quantize_rows_e4m3(ref_f64.astype(np.float32).reshape(-1, d))
+    want8 = want8.reshape(got8.shape)
+    want_s = want_s.reshape(got_s.shape)
+    rel = np.abs(got_s.astype(np.float64) - want_s) / want_s
+    assert np.all(rel <= 1e-5), f"{what}: scale rel err {rel.max():.2e}"
+    dist = np.abs(_e4m3_ord(got8) - _e4m3_ord(want8))
+    assert dist.max() <= 1, f"{what}: a code moved {dist.max()} steps"
+    frac = np.count_nonzero(dist) / dist.size
+    assert frac <= 1e-3, f"{what}: {frac:.2e} of the codes differ"
+    return want8, want_s, np.any(dist, axis=-1)
+
+
+def _gpu_compress_fp8(C, Z, bias, gamma, pos0, ratio, overlap=False, prev_C=None, prev_Z=None):
+    m = csa()
+    B, T, w = C.shape
+    d = w // 2 if overlap else w
+    out = torch.zeros(B, T // ratio, d, dtype=torch.uint8, device="cuda")
+    sc = torch.full((B, T // ratio), float("nan"), dtype=torch.float32, device="cuda")
+    m.dsv4_compress(dev_bf16(C), dev_bf16(Z), dev(bias), dev(gamma), dev(pos0), out, ratio=ratio,
+                    overlap=overlap, out_scale=sc,
+                    prev_C=None if prev_C is None else dev_bf16(prev_C),
+                    prev_Z=None if prev_Z is None else dev_bf16(prev_Z))
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), sc.cpu().numpy()
+
+
+@pytest.mark.parametrize("cfg", [0, 1])
+def test_compress_fp8_key_cache(cfg):
+    """The compressor writing the indexer's key cache in FP8 (codes + per-entry scale) against
+    the oracle's entries quantized by the oracle."""
+    wl = WORKLOADS[cfg]
+    x = inputs(cfg)
+    got8, got_s = _gpu_compress_fp8(x["C_I"], x["Z_I"], x["bias_I"], x["gamma_I"], x["pos0"], wl.ratio)
+    _, ref = oracle.compress(x["C_I"], x["Z_I"], x["bias_I"], x["gamma_I"], x["pos0"], wl.ratio,
+                             wl.rope_dim)
+    _check_fp8_cache(got8, got_s, ref, f"fp8 keys cfg{cfg}")
+
+
+def test_compress_overlap_fp8_key_cache():
+    """Two-stream compressor, 128-dim keys, previous block given, FP8 output."""
+    B, r, d = 3, 4, 128
+    C, Z, bias, gamma, pC, pZ = _overlap_inputs(31, B, 64 * r, d, r, prev=True)
+    pos0 = np.array([4 * r, 1000 * r, 0], np.int64)
+    got8, got_s = _gpu_compress_fp8(C, Z, bias, gamma, pos0, r, overlap=True, prev_C=pC, prev_Z=pZ)
+    _, ref = oracle.compress_overlap(C, Z, bias, gamma, pos0, r, pC, pZ)
+    _check_fp8_cache(got8, got_s, ref, "fp8 two-stream keys")
+
+
 # ------------------------------------------------------------------ stage 3 alone: exact top-k
 def _run_topk(scores, n_vis, k):
     m = csa()
@@ -607,20 +674,30 @@ def test_attention_edge_cases_and_bad_index():
 
 
 # ------------------------------------------------------------------ the fused decode step
-def _fused_step(x, wl, graph=False):
-    """Compress (whole context) + indexer top-k + gather/attention in one dsv4_csa_decode."""
+def _fused_step(x, wl, graph=False, fp8=False):
+    """Compress (whole context) + indexer top-k + gather/attention in one dsv4_csa_decode.
+    fp8: the key cache is written and scored in FP8 E4M3 (queries quantized by the oracle),
+    and the step also returns its scores."""
     m = csa()
     from compressed_sparse_attention_08_gb300 import _abi
     B, T, D = x["C"].shape
     Di = x["C_I"].shape[2]
     t = {}
+    fkw, ikw = {}, {}
+    if fp8:
+        q8, qs = _fp8_rows(x["q_I"])
+        t["q8"], t["qs"] = dev(q8), dev(qs)
+        t["key_scale"] = torch.full((B, wl.max_comp), float("nan"), dtype=torch.float32, device="cuda")
+        t["scores"] = torch.full((B, 1, wl.max_comp), float("nan"), dtype=torch.float32, device="cuda")
+        fkw = dict(out_scale=t["key_scale"])
+        ikw = dict(q_scale=t["qs"], key_scale=t["key_scale"], scores_out=t["scores"])
     t["C"], t["Z"] = dev_bf16(x["C"]), dev_bf16(x["Z"])
     t["CI"], t["ZI"] = dev_bf16(x["C_I"]), dev_bf16(x["Z_I"])
     t["bias"], t["gamma"] = dev(x["bias"]), dev(x["gamma"])
     t["biasI"], t["gammaI"] = dev(x["bias_I"]), dev(x["gamma_I"])
     t["pos0"] = dev(x["pos0"])
     t["kv"] = torch.zeros(B, wl.max_comp, D, dtype=torch.bfloat16, device="cuda")
-    t["keys"] = torch.zeros(B, wl.max_comp, Di, dtype=torch.bfloat16, device="cuda")
+    t["keys"] = torch.zeros(B, wl.max_comp, Di, dtype=torch.uint8 if fp8 else torch.bfloat16, device="cuda")
     t["q_I"], t["w"] = dev_bf16(x["q_I"]), dev(x["w"])
     t["n_comp"] = dev(x["n_comp"])
     t["idx"] = torch.empty(B, 1, wl.top_k, dtype=torch.int32, device="cuda")
@@ -629,8 +706,10 @@ def _fused_step(x, wl, graph=False):
     t["out"] = torch.empty(B, 1, wl.heads, D, dtype=torch.bfloat16, device="cuda")
     t["gather"] = torch.empty(B, 1, wl.top_k + wl.window, D, dtype=torch.bfloat16, device="cuda")
     ck = _abi.compress_args(t["C"], t["Z"], t["bias"], t["gamma"], t["pos0"], t["kv"], ratio=wl.ratio)
-    cq = _abi.compress_args(t["CI"], t["ZI"], t["biasI"], t["gammaI"], t["pos0"], t["keys"], ratio=wl.ratio)
-    ia = _abi.index_args(t["q_I"], t["w"], t["keys"], t["n_comp"], t["idx"], ratio=wl.ratio)
+    cq = _abi.compress_args(t["CI"], t["ZI"], t["biasI"], t["gammaI"], t["pos0"], t["keys"], ratio=wl.ratio,
+                            **fkw)
+    ia = _abi.index_args(t["q8"] if fp8 else t["q_I"], t["w"], t["keys"], t["n_comp"], t["idx"],
+                         ratio=wl.ratio, **ikw)
     aa = _abi.attn_args(t["q"], t["sink"], t["kv"], t["n_comp"], t["win"], t["win_len"], t["out"],
                         idx=t["idx"], window=wl.window, ratio=wl.ratio, gather=t["gather"])
     ws = ws_tensor(m.dsv4_csa_decode_workspace_size(attn=aa, index=ia, compress_kv=ck, compress_keys=cq))
@@ -676,6 +755,58 @@ def test_fused_decode_step(cfg):
                                              x["win"], x["win_len"], wl.top_k, wl.window, wl.ratio,
                                              want_gather=True)
         assert_bf16_close(host_bf16(t["out"]), ref_o, "fused: attention output")
+
+
+@pytest.mark.parametrize("cfg", [0, 1])
+def test_fused_decode_step_fp8_keys(cfg):
+    """The fused step with the index-key cache in FP8: the compressor writes codes + scales, the
+    scorer reads them. Cache against the oracle's quantized entries; scores against the
+    oracle's FP8 scores (exactly where the cache row equals the oracle's, else within the
+    shift one E4M3 step per element can cause); the selection is the exact top-k of the
+    step's own scores and equals the oracle's up to near ties and moved keys; attention
+    output against the oracle on the step's selection."""
+    wl = WORKLOADS[cfg]
+    x = inputs(cfg)
+    t, (ck, cq, ia, aa, ws), _ = _fused_step(x, wl, fp8=True)
+    st, ew = csa().dsv4_read_error_word(ws)
+    assert ew == 0, f"device error word {ew:#x}"
+    ref_kv_bits, ref_kv = _oracle_kv(x, wl)
+    assert_bf16_close(host_bf16(t["kv"]), ref_kv, "fused fp8: compressed KV")
+    _, ref_keys = oracle.compress(x["C_I"], x["Z_I"], x["bias_I"], x["gamma_I"], x["pos0"], wl.ratio,
+                                  wl.rope_dim)
+    nc = ref_keys.shape[1]
+    got8 = t["keys"].cpu().numpy()
+    got_s = t["key_scale"].cpu().numpy()
+    k8, ks, moved = _check_fp8_cache(got8[:, :nc], got_s[:, :nc], ref_keys, "fused fp8: key cache")
+    q8, qs = _fp8_rows(x["q_I"])
+    ref_s, nv = oracle.index_scores_fp8(q8, qs, x["w"], k8, ks, x["n_comp"], wl.ratio)
+    ref_i = oracle.topk(ref_s, nv, wl.top_k)
+    # bound on the score shift of a key whose codes moved by one step: every element moving
+    coef = np.einsum("bh,bhd->bd", np.abs(x["w"][:, 0].astype(np.float64) * qs[:, 0]),
+                     np.abs(oracle.e4m3_decode(q8[:, 0])))
+    band = np.einsum("bd,bsd->bs", coef, _e4m3_step(k8)) * ks
+    sc = t["scores"].cpu().numpy()
+    idx = t["idx"].cpu().numpy()
+    same = []
+    for b in range(wl.batch):
+        n = nv[b, 0]
+        g, r = sc[b, 0, :n].astype(np.float64), ref_s[b, 0, :n]
+        tol = 2e-5 * (np.mean(np.abs(r)) + 1e-30) + 2e-5 * np.abs(r)
+        tol = np.where(moved[b, :n], tol + band[b, :n], tol)
+        assert np.all(np.abs(g - r) <= tol), f"b{b}: scores"
+        topk_valid_for_scores(idx[b, 0], sc[b, 0], n, wl.top_k, f"b{b}")
+        if np.array_equal(idx[b, 0], ref_i[b, 0]):
+            same.append(b)
+            continue
+        kth = np.sort(r)[::-1][min(wl.top_k, n) - 1]
+        diff = np.setxor1d(idx[b, 0][idx[b, 0] >= 0], ref_i[b, 0][ref_i[b, 0] >= 0])
+        slack = 1e-5 * abs(kth) + np.where(moved[b, diff], band[b, diff], 0.0) + band[b, moved[b, :n]].max(initial=0.0)
+        assert np.all(np.abs(r[diff] - kth) <= slack), f"b{b}: selection"
+    # attention output on the sequences whose selection equals the oracle's
+    assert same, "no sequence selected exactly the oracle's keys"
+    _, ref_o, _ = oracle.sparse_attn(x["q"], x["sink"], ref_kv_bits, x["n_comp"], ref_i, x["win"],
+                                     x["win_len"], wl.top_k, wl.window, wl.ratio, want_gather=True)
+    assert_bf16_close(host_bf16(t["out"])[same], ref_o[same], "fused fp8: attention output")
 
 
 def test_fused_decode_graph_replay_matches_eager():

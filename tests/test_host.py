@@ -112,7 +112,9 @@ def test_compress_rejects_on_host(lib):
     for bad in (dict(tokens=15), dict(rope_dim=63), dict(rope_dim=1024), dict(dim=2048),
                 dict(out_rows=3), dict(eps=-1.0), dict(C=None), dict(ratio=0), dict(overlap=2),
                 dict(overlap=1, prev_C=_p(7)), dict(overlap=0, prev_C=_p(7), prev_Z=_p(8)),
-                dict(overlap=1, prev_C=_p(7), prev_Z=ctypes.c_void_p(FAKE + 4096 * 9 + 8))):
+                dict(overlap=1, prev_C=_p(7), prev_Z=ctypes.c_void_p(FAKE + 4096 * 9 + 8)),
+                dict(out_fp8=2, out_scale=_p(7)), dict(out_fp8=1), dict(out_scale=_p(7)),
+                dict(out_fp8=1, out_scale=ctypes.c_void_p(FAKE + 4096 * 7 + 4))):
         a = CompressArgs(**{**base, **bad})
         assert lib.dsv4_compress(ctypes.byref(a), None) == 1, bad
 
@@ -139,6 +141,21 @@ def test_fused_requires_consistent_stages(lib):
     aa2 = _attn_args(idx=_p(42))          # attention must read the indexer's output
     c2 = CsaArgs(None, None, ctypes.pointer(ia), ctypes.pointer(aa2))
     assert lib.dsv4_csa_decode(ctypes.byref(c2), _p(9), need, None) == 1
+
+
+def test_fused_key_cache_format_must_match(lib):
+    """A key cache written in the step is scored in the format it was written in."""
+    from compressed_sparse_attention_08_gb300._abi import CsaArgs, CompressArgs
+    ia = _index_args(key_fp8=1, q_scale=_p(20), key_scale=_p(21))
+    aa = _attn_args(idx=ia.idx_out)
+    base = dict(C=_p(1), Z=_p(2), bias=_p(3), gamma=_p(4), pos0=_p(5), out=ia.keys, out_row0=None,
+                batch=4, tokens=16, dim=128, ratio=4, rope_dim=64, out_rows=262144, eps=1e-6,
+                rope_theta=10000.0)
+    for bad in (dict(), dict(out_fp8=1, out_scale=_p(22))):   # bf16 entries; another scale array
+        cq = CompressArgs(**{**base, **bad})
+        c = CsaArgs(None, ctypes.pointer(cq), ctypes.pointer(ia), ctypes.pointer(aa))
+        need = lib.dsv4_csa_decode_workspace_size(ctypes.byref(c))
+        assert lib.dsv4_csa_decode(ctypes.byref(c), _p(9), need, None) == 1, bad
 
 
 def test_binding_refuses_without_library(tmp_path, monkeypatch):
