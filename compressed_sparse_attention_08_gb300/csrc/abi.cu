@@ -217,7 +217,8 @@ int dsv4_index_score(const dsv4_index_args* a, void* ws, size_t ws_bytes, dsv4_s
         return DSV4_ERR_INVALID_ARG;
     if (int rc = device_check()) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), st) != cudaSuccess) return DSV4_ERR_LAUNCH;
+    // the header holds the error word and the scorer's stage-claim counters
+    if (cudaMemsetAsync(ws, 0, kWsHeader, st) != cudaSuccess) return DSV4_ERR_LAUNCH;
     return launch_index_score(*a, eword_of(ws), st);
 }
 

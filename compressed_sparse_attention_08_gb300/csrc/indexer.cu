@@ -34,8 +34,13 @@
 // Launched with programmatic dependent launch: the producer waits for the preceding kernel
 // (the compressor) only before a stage that holds key rows that kernel writes.
 // Work: with no more rows than CTAs, every row has its own block of CTAs taking the row's
-// stages in turn; otherwise each CTA takes a contiguous range of (row, stage) pairs. Tiles
-// past the row's visible count are skipped by all three roles alike.
+// stages in turn; with at most 48 rows (decode) only the first nine tenths of each row
+// are shared out that way and the rest is claimed one stage at a time from a counter in
+// the workspace header, because the SMs do not stream equally fast (a static share left the
+// slowest CTA about 3 us behind the median at 1M keys per row). Otherwise each CTA takes a
+// contiguous range of (row, stage) pairs. The producer hands every stage's (row, stage) to
+// the MMA warp and the epilogue through a small ring of ids in shared memory, an id of -1
+// ending the stream; tiles past the row's visible count are skipped.
 #include "common.cuh"
 #include "internal.h"
 
@@ -71,6 +76,10 @@ struct KeyFmt {
     static constexpr int kThreads = 64 + 128 * kEpiGroups;
 };
 constexpr int kHistBins = 4096;             // top 12 bits of the order-preserving score key
+constexpr int kIdRing = 8;                  // stage ids in flight from the producer
+// stage-claim counters: words [kClaimWord, kClaimWord + rows) of the zeroed workspace header
+constexpr int kClaimWord = 16;
+constexpr int kMaxClaimRows = 48;
 constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + kQBufBytes;
 
 struct ScoreParams {
@@ -84,6 +93,7 @@ struct ScoreParams {
     uint32_t* eword;
     const float* q_scale;    // FP8 keys: [rows, heads] query scales, else null
     const float* key_scale;  // FP8 keys: [batch, max_comp] key scales, else null
+    uint32_t* claim;         // [rows] zeroed stage-claim counters, or null (static shares only)
     int rows, n_q, heads, max_comp, ratio, stages_per_row;
 };
 
@@ -113,7 +123,9 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t full_bar[kStages], empty_bar[kStages];
     __shared__ uint64_t tfull_bar[KeyFmt<FP8>::kAccBufs], tempty_bar[KeyFmt<FP8>::kAccBufs];
-    __shared__ uint64_t qfull_bar, qempty_bar, done_bar;
+    __shared__ uint64_t qfull_bar, qempty_bar, done_bar, epi_bar;
+    __shared__ uint64_t idfull_bar[kIdRing], idempty_bar[kIdRing];
+    __shared__ int2 s_id[kIdRing];                  // (row, stage) of each stage handed over
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
     // top-12-bit key histogram of the current row, two 16-bit counts per word (8 KB: a
@@ -124,7 +136,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
     constexpr int kStageKeys = F::kStageKeys, kSub = F::kSub;
     constexpr int kThreads = F::kThreads, kEpiGroups = F::kEpiGroups, kAccBufs = F::kAccBufs;
     constexpr uint32_t kTmemCols = F::kTmemCols;
-    __shared__ __align__(16) float s_wv[kEpiGroups][FP8 ? kMaxHeads : 4];
+    constexpr int kFlushStages = 65535 / kStageKeys;   // a 16-bit bin count cannot overflow
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_trigger();
     // 1024-byte aligned operand buffers (the 128-byte swizzle repeats every 1024 bytes)
@@ -139,6 +151,8 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
         mbar_init(&qfull_bar, 1);
         mbar_init(&qempty_bar, 1);
         mbar_init(&done_bar, 1);
+        mbar_init(&epi_bar, 128 * kEpiGroups);
+        for (int i = 0; i < kIdRing; ++i) { mbar_init(&idfull_bar[i], 1); mbar_init(&idempty_bar[i], 4 * kEpiGroups); }
         abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&kmap);
@@ -156,24 +170,71 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
     const uint32_t tmem_base = tmem_slot;
 
     const Walk wk = cta_walk(p.rows, p.stages_per_row);
+    const int spr = p.stages_per_row;
     const uint32_t idesc = FP8 ? idesc_e4m3_f32(kTileKeys, NP) : idesc_bf16_f32(kTileKeys, NP);
     const uint32_t q_half = static_cast<uint32_t>(NP) * 128u;   // bf16: bytes of one 64-dim half
 
     if (warp == 0) {
         if (lane == 0) {
-            int stage = 0, qcount = 0, cur_row = -1, nv = 0;
-            bool waited = false;
-            long long issued = 0;
+            // Stage order: the CTA's share of the walk; for a row with its own block of CTAs
+            // and a claim counter, only the first nine tenths of the row are shared out in
+            // advance and the rest is claimed one stage at a time, so that CTAs on SMs that
+            // stream faster take more and the row's CTAs finish together.
+            const bool dyn = p.claim != nullptr && wk.step > 1;
+            const int row0 = static_cast<int>(wk.begin / spr);
+            const int cutoff = dyn ? static_cast<int>((static_cast<long long>(spr) * 9 / 10) / wk.step * wk.step) : spr;
+            int stage = 0, qcount = 0, cur_row = -1, vis_row = -1, nv = 0, ahead = -1;
+            bool waited = false, claiming = false;
+            long long issued = 0, seq = 0, f = wk.begin;
             uint32_t phase = 0;
             const uint64_t stream_policy = l2_evict_first_policy();   // keys are read once
-            for (long long f = wk.begin; f < wk.end; f += wk.step) {
-                const int row = static_cast<int>(f / p.stages_per_row);
-                const int st = static_cast<int>(f % p.stages_per_row);
-                if (row != cur_row)
+            auto claim = [&]() {
+                // the counters are cleared by the work before this grid
+                if (!waited) { pdl_wait(); waited = true; }
+                ahead = static_cast<int>(atomicAdd(&p.claim[row0], 1u));
+            };
+            for (;;) {
+                int row, st;
+                if (!claiming) {
+                    if (f >= wk.end || static_cast<int>(f % spr) >= cutoff) {
+                        if (!dyn) break;
+                        claiming = true;
+                        continue;
+                    }
+                    row = static_cast<int>(f / spr);
+                    st = static_cast<int>(f % spr);
+                    f += wk.step;
+                    // before the last stage of the share: the first claim's round trip hides
+                    // behind it
+                    if (dyn && ahead < 0 && (f >= wk.end || static_cast<int>(f % spr) >= cutoff)) claim();
+                } else {
+                    if (ahead < 0) claim();
+                    row = row0;
+                    st = cutoff + ahead;
+                    if (row != vis_row) {
+                        nv = row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, row, nullptr);
+                        vis_row = row;
+                    }
+                    if (st >= spr || st * kStageKeys >= nv) break;     // the row is all taken
+                    claim();                                            // the next one, early
+                }
+                if (row != vis_row) {
                     nv = row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, row, nullptr);
+                    vis_row = row;
+                }
                 if (st * kStageKeys >= nv) continue;
+                {
+                    // hand the stage to the MMA warp and the epilogue
+                    const int slot = static_cast<int>(seq % kIdRing);
+                    if (!mbar_wait(&idempty_bar[slot], static_cast<uint32_t>(((seq / kIdRing) & 1) ^ 1), &abort_flag))
+                        goto fail0;
+                    s_id[slot] = make_int2(row, st);
+                    mbar_arrive(&idfull_bar[slot]);
+                    ++seq;
+                }
                 if (row != cur_row) {
-                    // one query buffer: the previous row's MMAs release it first
+                    // one query buffer: the MMA warp learns of the new row from the stage id
+                    // just handed over and releases the old queries once their MMAs are done
                     if (!mbar_wait(&qempty_bar, (qcount & 1) ^ 1, &abort_flag)) goto fail0;
                     mbar_arrive_expect_tx(&qfull_bar, static_cast<uint32_t>(p.heads) * kDim * F::kElem);
                     tma_load_2d(q_buf, &qmap, &qfull_bar, 0, row * p.heads);
@@ -204,6 +265,14 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                 }
                 if (++stage == kStages) { stage = 0; phase ^= 1; }
             }
+            {
+                // end of the stream
+                const int slot = static_cast<int>(seq % kIdRing);
+                if (!mbar_wait(&idempty_bar[slot], static_cast<uint32_t>(((seq / kIdRing) & 1) ^ 1), &abort_flag))
+                    goto fail0;
+                s_id[slot] = make_int2(-1, -1);
+                mbar_arrive(&idfull_bar[slot]);
+            }
             if (!waited) pdl_wait();        // this grid never completes before its predecessor
             goto done0;
         fail0:
@@ -221,18 +290,17 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
         if (lane == 0) {
             int stage = 0, acc = 0, qcount = 0, cur_row = -1, nv = 0;
             uint32_t phase = 0, acc_phase = 0;
-            for (long long f = wk.begin; f < wk.end; f += wk.step) {
-                const int row = static_cast<int>(f / p.stages_per_row);
-                const int st = static_cast<int>(f % p.stages_per_row);
-                int row_nv = nv;
-                if (row != cur_row)
-                    row_nv = row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, row, nullptr);
-                if (st * kStageKeys >= row_nv) continue;
+            for (long long seq = 0;; ++seq) {
+                const int slot = static_cast<int>(seq % kIdRing);
+                if (!mbar_wait(&idfull_bar[slot], static_cast<uint32_t>((seq / kIdRing) & 1), &abort_flag)) goto fail1;
+                const int2 id = s_id[slot];
+                if (id.x < 0) break;
+                const int row = id.x, st = id.y;
                 if (row != cur_row) {
                     if (cur_row >= 0) umma_commit(&qempty_bar);   // old queries free once done
                     if (!mbar_wait(&qfull_bar, qcount & 1, &abort_flag)) goto fail1;
                     cur_row = row;
-                    nv = row_nv;
+                    nv = row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, row, nullptr);
                     ++qcount;
                 }
                 if (!mbar_wait(&full_bar[stage], phase, &abort_flag)) goto fail1;
@@ -280,97 +348,100 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
         const int group = (warp - 2) >> 2;
         const int lrow = quarter * 32 + lane;
         const int etid = threadIdx.x - 64;                 // 0 .. 128 * kEpiGroups - 1
-        const int gtid = etid & 127;                       // within the group
         const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
         int acc = 0, cur_row = -1, nv = 0;
-        uint32_t acc_phase = 0;
-        bool dead = false;        // a wait ran out: keep walking the tiles (same barriers), no work
-        // head weights of the current row: registers (bf16) or the group's shared copy (FP8,
-        // broadcast reads; it keeps the thread at a register count that lets a compressor CTA
-        // share the SM)
-        float wv[FP8 ? 1 : NP];
-        // The histogram is private to the CTA and flushed to the row's global histogram when
-        // the row changes, and before a 16-bit count could overflow (every 255 stages). Every
-        // epilogue thread passes the same flush barriers, dead or not.
-        int since_flush = 0;
-        auto group_sync = [](int g) {                      // constant barrier ids 2 and 3
-            if (g == 0) named_bar_sync(2, 128);
-            else named_bar_sync(3, 128);
+        uint32_t acc_phase = 0, fl_parity = 0;
+        bool ok = true;
+        float wv[NP];             // the row's head weights (FP8: times the head's query scale)
+        // Every wait of the epilogue is an mbarrier wait, bounded in time and ended early once
+        // any role has given up, so a failure anywhere cannot leave a thread waiting.
+        auto epi_sync = [&]() -> bool {
+            mbar_arrive(&epi_bar);
+            const bool r = mbar_wait(&epi_bar, fl_parity, &abort_flag);
+            fl_parity ^= 1;
+            return r;
         };
+        // The histogram is private to the CTA and flushed to the row's global histogram when
+        // the row changes, and before a 16-bit count could overflow (every kFlushStages stages).
+        int since_flush = 0;
         auto flush = [&](int r) {
             pdl_wait();      // the histogram may have been cleared by the preceding kernel
-            named_bar_sync(1, 128 * kEpiGroups);
-            uint32_t* g = p.hist + static_cast<size_t>(r) * kHistBins;
-            for (int i = etid; i < kHistBins / 2; i += 128 * kEpiGroups) {
-                const uint32_t v = s_hist[i];
-                if (v) {
-                    if (v & 0xFFFFu) atomicAdd(&g[2 * i], v & 0xFFFFu);
-                    if (v >> 16) atomicAdd(&g[2 * i + 1], v >> 16);
-                    s_hist[i] = 0;
+            if (epi_sync()) {
+                uint32_t* g = p.hist + static_cast<size_t>(r) * kHistBins;
+                for (int i = etid; i < kHistBins / 2; i += 128 * kEpiGroups) {
+                    const uint32_t v = s_hist[i];
+                    if (v) {
+                        if (v & 0xFFFFu) atomicAdd(&g[2 * i], v & 0xFFFFu);
+                        if (v >> 16) atomicAdd(&g[2 * i + 1], v >> 16);
+                        s_hist[i] = 0;
+                    }
                 }
+                epi_sync();
             }
-            named_bar_sync(1, 128 * kEpiGroups);
             since_flush = 0;
         };
-        // FP8: the key scales of the next stage are loaded one walk item ahead (a DRAM read per
-        // tile would otherwise stall the epilogue once per 128 keys). Every key scale is final
-        // once the preceding kernel (which may write the newest key) has completed.
+        // the next stage's id, read one stage ahead; each warp releases the slot once read
+        auto read_id = [&](long long sq, int2& id) -> bool {
+            const int slot = static_cast<int>(sq % kIdRing);
+            if (!mbar_wait(&idfull_bar[slot], static_cast<uint32_t>((sq / kIdRing) & 1), &abort_flag)) return false;
+            const volatile int* v = reinterpret_cast<const volatile int*>(&s_id[slot]);
+            id = make_int2(v[0], v[1]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&idempty_bar[slot]);
+            return true;
+        };
+        // FP8: the key scales of a stage load while the stage before it is scored (a DRAM read
+        // per tile would otherwise stall the epilogue once per 128 keys). Every key scale is
+        // final once the preceding kernel (which may write the newest key) has completed.
         float ks_cur[kSub], ks_next[kSub];
-        auto load_ks = [&](long long g) {
-            if (g >= wk.end) return;
-            const int r_ = static_cast<int>(g / p.stages_per_row);
-            const int s_ = static_cast<int>(g % p.stages_per_row);
-            const float* kb = p.key_scale + static_cast<size_t>(r_ / p.n_q) * p.max_comp;
+        auto load_ks = [&](int2 id) {
+            const float* kb = p.key_scale + static_cast<size_t>(id.x / p.n_q) * p.max_comp;
 #pragma unroll
             for (int j = 0; j < kSub; ++j) {
-                const int key = (s_ * kSub + j) * kTileKeys + lrow;
+                const int key = (id.y * kSub + j) * kTileKeys + lrow;
                 ks_next[j] = key < p.max_comp ? __ldcg(kb + key) : 0.f;
             }
         };
+        int2 id_cur = make_int2(-1, -1), id_next;
+        ok = read_id(0, id_cur);
         if constexpr (FP8) {
             pdl_wait();
-            load_ks(wk.begin);
+            if (ok && id_cur.x >= 0) load_ks(id_cur);
         }
-        for (long long f = wk.begin; f < wk.end; f += wk.step) {
-            const int row = static_cast<int>(f / p.stages_per_row);
-            const int st = static_cast<int>(f % p.stages_per_row);
+        for (long long sq = 1; ok && id_cur.x >= 0; ++sq) {
+            id_next = make_int2(-1, -1);
+            if (!read_id(sq, id_next)) ok = false;
             if constexpr (FP8) {
 #pragma unroll
                 for (int j = 0; j < kSub; ++j) ks_cur[j] = ks_next[j];
-                load_ks(f + wk.step);
+                if (ok && id_next.x >= 0) load_ks(id_next);
             }
-            if (row != cur_row || since_flush == 255) {
+            const int row = id_cur.x, st = id_cur.y;
+            if (row != cur_row || since_flush == kFlushStages) {
                 if (p.hist && cur_row >= 0) flush(cur_row);
             }
             ++since_flush;
             if (row != cur_row) {
                 nv = row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, row, nullptr);
                 cur_row = row;
-                if constexpr (FP8) {
-                    // the query scale folds into the head's weight (ReLU commutes with it)
-                    group_sync(group);                          // the group is done with the old row
-                    if (gtid < kMaxHeads) {
-                        const size_t o = static_cast<size_t>(row) * p.heads + gtid;
-                        s_wv[group][gtid] = gtid < p.heads ? __ldg(&p.w[o]) * __ldg(&p.q_scale[o]) : 0.f;
-                    }
-                    group_sync(group);
-                } else {
 #pragma unroll
-                    for (int h = 0; h < NP; ++h)
-                        wv[h] = h < p.heads ? __ldg(&p.w[static_cast<size_t>(row) * p.heads + h]) : 0.f;
+                for (int h = 0; h < NP; ++h) {
+                    const size_t o = static_cast<size_t>(row) * p.heads + h;
+                    float wh = h < p.heads ? __ldg(&p.w[o]) : 0.f;
+                    // FP8: the query scale folds into the head's weight (ReLU commutes with it)
+                    if (FP8 && h < p.heads) wh *= __ldg(&p.q_scale[o]);
+                    wv[h] = wh;
                 }
             }
-            for (int j = 0; j < kSub; ++j) {
+            for (int j = 0; j < kSub && ok; ++j) {
                 const int tile = st * kSub + j;
-                if (tile * kTileKeys >= nv || dead) break;
+                if (tile * kTileKeys >= nv) break;
                 const int my_acc = acc;
                 const uint32_t my_phase = acc_phase;
                 if (++acc == kAccBufs) { acc = 0; acc_phase ^= 1; }
                 if (kEpiGroups > 1 && (my_acc % kEpiGroups) != group) continue;
                 if (!mbar_wait(&tfull_bar[my_acc], my_phase, &abort_flag)) {
-                    flag_error(p.eword, DSV4_EWORD_TIMEOUT);
-                    abort_flag = 1;
-                    dead = true;
+                    ok = false;
                     break;
                 }
                 tc_fence_after();
@@ -396,17 +467,15 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                     // four partial sums (heads h mod 4) in two packed pairs: half the FMA
                     // instructions and a quarter of the dependent-FMA latency per key (the
                     // epilogue, not HBM, sets the pace of 512-key stages)
-                    const float4* w4 = reinterpret_cast<const float4*>(s_wv[group]);
                     uint64_t a01 = 0, a23 = 0;
 #pragma unroll
                     for (int h4 = 0; h4 < NP / 4; ++h4) {
-                        const float4 w = w4[h4];
                         fma_f32x2(a01, pack_f32x2(fmaxf(__uint_as_float(r[4 * h4 + 0]), 0.f),
                                                   fmaxf(__uint_as_float(r[4 * h4 + 1]), 0.f)),
-                                  pack_f32x2(w.x, w.y));
+                                  pack_f32x2(wv[4 * h4 + 0], wv[4 * h4 + 1]));
                         fma_f32x2(a23, pack_f32x2(fmaxf(__uint_as_float(r[4 * h4 + 2]), 0.f),
                                                   fmaxf(__uint_as_float(r[4 * h4 + 3]), 0.f)),
-                                  pack_f32x2(w.z, w.w));
+                                  pack_f32x2(wv[4 * h4 + 2], wv[4 * h4 + 3]));
                     }
                     float s0, s1, s2, s3;
                     unpack_f32x2(a01, s0, s1);
@@ -425,6 +494,11 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                     }
                 }
             }
+            id_cur = id_next;
+        }
+        if (!ok) {
+            flag_error(p.eword, DSV4_EWORD_TIMEOUT);
+            abort_flag = 1;
         }
         if (p.hist && cur_row >= 0) flush(cur_row);
     }
@@ -531,6 +605,7 @@ int launch_scores_fmt(const dsv4_index_args& a, float* scores, uint32_t* hist, u
     p.eword = eword;
     p.q_scale = FP8 ? a.q_scale : nullptr;
     p.key_scale = FP8 ? a.key_scale : nullptr;
+    p.claim = eword && rows <= kMaxClaimRows ? eword + kClaimWord : nullptr;
     p.rows = rows;
     p.n_q = a.n_q;
     p.heads = a.heads;

@@ -506,6 +506,32 @@ def test_compress_overlap_fp8_key_cache():
     _check_fp8_cache(got8, got_s, ref, "fp8 two-stream keys")
 
 
+def test_indexer_fp8_one_bin_long_rows():
+    """FP8 keys, 153 rows (more rows than SMs: each CTA scores a contiguous run of stages of
+    one row, up to 257 stages of 512 keys) with every score equal: every key of a row lands in
+    one histogram bin, more than a 16-bit count holds between flushes unless the scorer
+    flushes often enough. The selection must be the first top_k keys (ties: lower index)."""
+    m = csa()
+    B, H, N, k = 153, 8, 131072, 64
+    one = 0x38                                          # E4M3 code of 1.0
+    q8 = torch.full((B, 1, H, 128), one, dtype=torch.uint8, device="cuda")
+    qs = torch.ones(B, 1, H, dtype=torch.float32, device="cuda")
+    k8 = torch.full((B, N, 128), one, dtype=torch.uint8, device="cuda")
+    ks = torch.ones(B, N, dtype=torch.float32, device="cuda")
+    w = torch.full((B, 1, H), 1.0 / H, dtype=torch.float32, device="cuda")
+    n_comp = torch.full((B,), N, dtype=torch.int32, device="cuda")
+    idx = torch.empty(B, 1, k, dtype=torch.int32, device="cuda")
+    kw = dict(ratio=4, q_scale=qs, key_scale=ks)
+    ws = ws_tensor(m.dsv4_indexer_topk_workspace_size(q8, w, k8, n_comp, idx, **kw))
+    m.dsv4_indexer_topk(q8, w, k8, n_comp, idx, ws, **kw)
+    torch.cuda.synchronize()
+    st, ew = m.dsv4_read_error_word(ws)
+    assert ew == 0, f"device error word {ew:#x}"
+    want = np.broadcast_to(np.arange(k, dtype=np.int32), (B, k))
+    assert np.array_equal(idx[:, 0].cpu().numpy(), want)
+    del k8
+
+
 # ------------------------------------------------------------------ stage 3 alone: exact top-k
 def _run_topk(scores, n_vis, k):
     m = csa()
