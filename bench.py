@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefill-only", action="store_true",
                     help="time only the chunked-prefill indexer scoring (tensor-core bound)")
+    ap.add_argument("--fp8-only", action="store_true",
+                    help="time only the decode step with the FP8 index-key cache")
     return ap.parse_args()
 
 
@@ -221,13 +223,14 @@ def fp8_keys_step(m, _abi, t, wl, steps, stream, peak):
             "launches_per_step": launches, "dtype": "fp8 e4m3 index keys, bf16 KV",
             "scorer": {"kernel": "index_score_kernel<FP8>", "bytes_per_launch": sb,
                        "ms_per_launch": score_ms, "achieved": gbs, "peak": peak, "unit": "GB/s",
-                       "frac": gbs / peak}}
+                       "frac": gbs / peak,
+                       "traffic": profile_traffic("index_score_kernel_fp8_csa_decode_ctx1048576_b4.md")}}
 
 
-def profile_traffic():
+def profile_traffic(name="index_score_kernel_csa_decode_ctx1048576_b4.md"):
     """dram bytes per scoring launch from the committed ncu summary, if the kernel source
     still matches the hash recorded there; else None."""
-    path = os.path.join(ROOT, "profiles", "index_score_kernel_csa_decode_ctx1048576_b4.md")
+    path = os.path.join(ROOT, "profiles", name)
     src = os.path.join(ROOT, "compressed_sparse_attention_08_gb300", "csrc", "indexer.cu")
     if not os.path.exists(path):
         return None
@@ -406,6 +409,10 @@ def run_ours(args):
     nbytes = m.dsv4_csa_decode_workspace_size(attn=aa, index=ia, compress_kv=ck, compress_keys=cq)
     ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device="cuda")
     stream = torch.cuda.Stream()
+    if args.fp8_only:
+        peak, _ = measured_peaks()
+        print(json.dumps({"fp8_keys": fp8_keys_step(m, _abi, t, wl, args.steps, stream, peak)}), flush=True)
+        return
 
     def step(s=None):
         m.dsv4_csa_decode(ws, attn=aa, index=ia, compress_kv=ck, compress_keys=cq, stream=s)
