@@ -15,14 +15,14 @@
 // its starting counts, and element i lands at  #greater-before(i) + min(#ties-before(i),
 // need_T). Two implementations of the same rule:
 //   * rows that fit in shared memory (max_comp <= kSmallCap): one CTA per row, keys in smem.
-//   * long rows (1M context: 262,144 scores): the row is cut into P slices, one CTA each. A
-//     histogram of the top 12 key bits per row (built by the scoring kernel's epilogue when
-//     the scores come from the indexer, else by a histogram kernel) gives the 12-bit bin
-//     that holds the k-th key; every CTA keeps, in index order, the elements of its slice at
-//     or above that bin (a few thousand of 262,144 in all) and counts bits 19..8 of the keys
-//     in that bin into a second histogram; the last CTA of the row to finish (atomic ticket,
-//     no spinning) reads the second histogram, so one 8-bit radix pass over the short list
-//     gives the exact k-th key.
+//   * long rows (1M context: 262,144 scores): one thread-block cluster of 16 CTAs per row,
+//     one slice each. A histogram of the top 12 key bits per row (built by the scoring
+//     kernel's epilogue when the scores come from the indexer, else by a histogram kernel)
+//     gives the 12-bit bin that holds the k-th key; every CTA keeps, in index order, the
+//     elements of its slice at or above that bin (a few thousand of 262,144 in all) and
+//     counts bits 19..8 of the keys in that bin; counts, that second histogram and the kept
+//     elements meet in the shared memory of the cluster's first CTA, so one 8-bit radix pass
+//     over the short list gives the exact k-th key.
 #include "common.cuh"
 #include "internal.h"
 
@@ -35,6 +35,7 @@ constexpr int kBinShift = 20;
 constexpr int kFinalCap = 12288;     // (key, index) pairs the finalizer keeps in smem
 constexpr int kMaxSlices = 64;
 constexpr int kNT = 1024;
+constexpr int kCl = 16;              // CTAs per row in the long-row cluster kernel (non-portable size)
 
 // Inclusive scan over the 32 lanes of a warp.
 __device__ __forceinline__ int warp_incl(int v) {
@@ -191,10 +192,7 @@ topk_small_kernel(TopkRows t, uint32_t* eword) {
 // ------------------------------------------------------------------ long rows
 struct LongWs {
     uint32_t* hist;     // [rows, kBins]: top 12 key bits (bits 31..20) of every visible key
-    uint32_t* hist2;    // [rows, kBins]: bits 19..8 of the keys in the threshold bin
-    uint32_t* done;     // [rows] tickets
-    int32_t* counts;    // [rows, kMaxSlices]
-    uint2* pairs;       // [rows, max_comp]: (key, index) survivors, slice p at p * L
+    uint2* pairs;       // [rows, max_comp]: (key, index) survivors when they outnumber kFinalCap
 };
 
 __device__ __forceinline__ void slice_range(int n, int L, int p, int& lo, int& hi) {
@@ -262,28 +260,41 @@ topk_hist_kernel(TopkRows t, LongWs w, int L, uint32_t* eword) {
         if (h[i]) atomicAdd(&g[i], h[i]);
 }
 
-// Long rows, P CTAs per row. Each CTA: the 12-bit threshold bin tb from the row histogram;
-// the survivors of its slice (key bin >= tb) in index order into its segment of the pair
-// list; bits 19..8 of the keys in bin tb into the row's second histogram. The last CTA of
-// the row (atomic ticket, no spinning) finds the second-level bin from that histogram, so one
-// 8-bit radix pass over the survivors gives the exact k-th key, and writes the k indices.
-template <int NT>
+// Long rows, one cluster of CL CTAs per row; CTA r takes slice r of the row. Every CTA: the
+// 12-bit threshold bin tb from the row histogram; its survivors (key bin >= tb), counted;
+// bits 19..8 of its keys in bin tb into a shared histogram. Through distributed shared
+// memory each CTA then adds that histogram into CTA 0's and posts its count there; after a
+// cluster barrier every CTA knows every count, and writes its survivors, in index order,
+// straight into CTA 0's shared list at its offset (into the global list when the survivors
+// outnumber the shared list). After a last cluster barrier CTA 0 finds the second-level bin,
+// so one 8-bit radix pass (none when the whole sub-bin is selected) gives the exact k-th key,
+// and writes the k indices. No global atomics, tickets or round trips through L2 between
+// the phases.
+template <int NT, int CL>
 __global__ void __launch_bounds__(NT, 1)
-topk_filter_kernel(TopkRows t, LongWs w, int L, int P, uint32_t* eword) {
+topk_cluster_kernel(TopkRows t, LongWs w, int L, uint32_t* eword) {
     constexpr int NW = NT / 32;
-    constexpr int kRegs = 8;                     // scores per lane kept in registers
+    constexpr int kRegs = 16;                    // scores per lane kept in registers
     constexpr int per_bin = kBins / NT;
-    extern __shared__ uint2 spairs[];           // kFinalCap pairs (finalizer only)
+    extern __shared__ uint2 spairs[];           // CTA 0: the survivors (kFinalCap pairs)
+    __shared__ uint32_t h2loc[kBins];           // this CTA's bits 19..8 of bin tb
+    __shared__ uint32_t h2sum[kBins];           // CTA 0: the row's
     __shared__ uint32_t hist[256];
-    __shared__ int s_a[32], s_b[32];
+    __shared__ int s_a[32], s_b[32], s_w[32];
     __shared__ int bc[3];
-    __shared__ int offs[kMaxSlices + 1];
-    __shared__ int is_last;
+    __shared__ int cl_count[CL];                // CTA 0: survivors per CTA
+    __shared__ int offs[CL + 1];
     pdl_trigger();
-    pdl_wait();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int row = blockIdx.x, p = blockIdx.y;
+    const uint32_t rank = cluster_rank();
+    const int row = blockIdx.y;
     const int k = t.top_k;
+    // the sums CTA 0 collects start at zero before any CTA adds into them
+    for (int i = threadIdx.x; i < kBins; i += NT) { h2loc[i] = 0; h2sum[i] = 0; }
+    if (threadIdx.x < CL) cl_count[threadIdx.x] = 0;
+    __syncthreads();
+    cluster_arrive();
+    pdl_wait();
     // The row histogram, this slice's scores and the visible count do not depend on one
     // another: issue their loads together. The slice is read over its full extent (inside
     // the row's max_comp scores); entries at or past the visible count are masked below.
@@ -292,26 +303,30 @@ topk_filter_kernel(TopkRows t, LongWs w, int L, int P, uint32_t* eword) {
 #pragma unroll
     for (int i = 0; i < per_bin; ++i)
         c[i] = static_cast<int>(__ldcg(&g1[kBins - 1 - (static_cast<int>(threadIdx.x) * per_bin + i)]));
-    const int slo = p * L;                       // < max_comp: P = ceil(max_comp / L)
+    const int slo = static_cast<int>(rank) * L < t.max_comp ? static_cast<int>(rank) * L : t.max_comp;
     const int shi = slo + L < t.max_comp ? slo + L : t.max_comp;
     const int wper = (shi - slo + NW - 1) / NW;  // warp-contiguous runs of the slice
     const int wlo = slo + (warp * wper < shi - slo ? warp * wper : shi - slo);
     const int whi = wlo + wper < shi ? wlo + wper : shi;
     const bool in_regs = wper <= 32 * kRegs;     // the same for every warp of the CTA
     const float* sc = t.scores + static_cast<size_t>(row) * t.max_comp;
+    // loaded once, up front, and kept (a volatile load: the compiler may not re-issue it in
+    // the two passes below)
     float v0[kRegs];
     if (in_regs) {
 #pragma unroll
         for (int r = 0; r < kRegs; ++r) {
             const int i = wlo + r * 32 + lane;
-            v0[r] = i < whi ? __ldcg(&sc[i]) : 0.f;
+            v0[r] = 0.f;
+            if (i < whi) asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v0[r]) : "l"(sc + i));
         }
     }
     const int n = row_visible(t.n_vis, t.n_comp, t.q_pos, t.n_q, t.ratio, t.max_comp, row, eword);
     int32_t* out = t.idx_out + static_cast<size_t>(row) * k;
     if (n <= k) {                                // every visible entry is selected
-        const int per = (k + P - 1) / P;
-        write_all(out, n, k, p * per + threadIdx.x, (p + 1) * per, NT);
+        const int per = (k + CL - 1) / CL;
+        write_all(out, n, k, static_cast<int>(rank) * per + threadIdx.x, (static_cast<int>(rank) + 1) * per, NT);
+        cluster_wait();
         return;
     }
     const int hi = whi < n ? whi : n;            // visible end of this warp's run
@@ -321,140 +336,89 @@ topk_filter_kernel(TopkRows t, LongWs w, int L, int P, uint32_t* eword) {
     const int above = bc[1];
     // 2. count this warp's survivors (bin >= tb); keys in bin tb also go into the second
     //    histogram
-    uint32_t* g2 = w.hist2 + static_cast<size_t>(row) * kBins;
-    uint2* seg = w.pairs + static_cast<size_t>(row) * t.max_comp + static_cast<size_t>(slo);
-    const unsigned lt = (1u << lane) - 1u;
     int cnt = 0;
     for (int b0 = wlo; b0 < whi; b0 += 32 * kRegs) {
-        uint32_t key[kRegs];
-#pragma unroll
-        for (int r = 0; r < kRegs; ++r) {
-            const int i = b0 + r * 32 + lane;
-            key[r] = float_to_key(in_regs ? v0[r] : (i < hi ? __ldcg(&sc[i]) : 0.f));
-        }
 #pragma unroll
         for (int r = 0; r < kRegs; ++r) {
             const int i = b0 + r * 32 + lane;
             const bool vis = i < hi;
-            const uint32_t bin = key[r] >> kBinShift;
-            cnt += __popc(__ballot_sync(0xffffffffu, vis && bin >= tb));
-            if (vis && bin == tb) atomicAdd(&g2[(key[r] >> 8) & (kBins - 1)], 1u);
+            const uint32_t key = float_to_key(in_regs ? v0[r] : (vis ? __ldcg(&sc[i]) : 0.f));
+            const uint32_t bin = key >> kBinShift;
+            const unsigned bs = __ballot_sync(0xffffffffu, vis && bin >= tb);
+            if (bs == 0u) continue;                 // most groups of 32 keep nothing
+            cnt += __popc(bs);
+            // few keys fall in bin tb, spread over 4096 sub-bins: plain atomics
+            if (vis && bin == tb) atomicAdd(&h2loc[(key >> 8) & (kBins - 1)], 1u);
         }
     }
-    if (lane == 0) s_a[warp] = cnt;              // find_bin is done with s_a
+    if (lane == 0) s_w[warp] = cnt;
     __syncthreads();
     if (warp == 0) {
-        const int v = lane < NW ? s_a[lane] : 0;
+        const int v = lane < NW ? s_w[lane] : 0;
         const int vi = warp_incl(v);
-        if (lane < NW) s_a[lane] = vi - v;
-        if (lane == NW - 1) s_b[0] = vi;
+        if (lane < NW) s_w[lane] = vi - v;       // the warp's offset within the CTA
+        if (lane == NW - 1) s_b[0] = vi;         // the CTA's count
     }
+    // 3. post the count and the second histogram to CTA 0 (its sums are zeroed: wait for that)
+    cluster_wait();
     __syncthreads();
-    // 3. write them, in index order, at the warp's offset in the slice's segment
-    int pos = s_a[warp];
-    for (int b0 = wlo; b0 < whi; b0 += 32 * kRegs) {
-        uint32_t key[kRegs];
-#pragma unroll
-        for (int r = 0; r < kRegs; ++r) {
-            const int i = b0 + r * 32 + lane;
-            key[r] = float_to_key(in_regs ? v0[r] : (i < hi ? __ldcg(&sc[i]) : 0.f));
-        }
-#pragma unroll
-        for (int r = 0; r < kRegs; ++r) {
-            const int i = b0 + r * 32 + lane;
-            const bool keep = i < hi && (key[r] >> kBinShift) >= tb;
-            const unsigned bk = __ballot_sync(0xffffffffu, keep);
-            if (keep) seg[pos + __popc(bk & lt)] = make_uint2(key[r], static_cast<uint32_t>(i));
-            pos += __popc(bk);
+    if (threadIdx.x == 0) st_cluster_u32(cluster_map(&cl_count[rank], 0), static_cast<uint32_t>(s_b[0]));
+    {
+        const uint32_t h2r = cluster_map(h2sum, 0);
+        for (int i = threadIdx.x; i < kBins; i += NT) {
+            const uint32_t v = h2loc[i];
+            if (v) red_cluster_add(h2r + 4u * static_cast<uint32_t>(i), v);
         }
     }
-    if (threadIdx.x == 0) w.counts[static_cast<size_t>(row) * kMaxSlices + p] = s_b[0];
-    // 4. the last CTA of the row to get here finishes the row (no waiting on anyone)
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const unsigned ticket = atomicAdd(&w.done[row], 1u);
-        is_last = ticket == static_cast<unsigned>(P - 1);
+    cluster_arrive();
+    cluster_wait();
+    // 4. every CTA's offset in the row's list; the survivors go there in index order
+    if (warp == 0) {
+        const int v = lane < CL ? static_cast<int>(ld_cluster_u32(cluster_map(&cl_count[lane], 0))) : 0;
+        const int vi = warp_incl(v);
+        if (lane < CL) offs[lane + 1] = vi;
+        if (lane == 0) offs[0] = 0;
     }
     __syncthreads();
-    if (!is_last) return;
-    __threadfence();
-    // slice counts, the second histogram and the first kPairRegs * 32 survivors of the
-    // slices this warp copies (slices warp and warp + 32; loaded before their counts are
-    // known, from inside each slice's segment), all at once
-    constexpr int kPairRegs = 4;
-    const uint2* rowpairs = w.pairs + static_cast<size_t>(row) * t.max_comp;
-    const int32_t* rowcounts = w.counts + static_cast<size_t>(row) * kMaxSlices;
-    int cnt_w[2] = {0, 0};
-    uint2 pr[2][kPairRegs];
+    const int total = offs[CL];
+    const bool in_smem = total <= kFinalCap;
+    {
+        int pos = offs[rank] + s_w[warp];
+        const unsigned lt = (1u << lane) - 1u;
+        const uint32_t sp0 = cluster_map(spairs, 0);
+        uint2* gp = w.pairs + static_cast<size_t>(row) * t.max_comp;
+        for (int b0 = wlo; b0 < whi; b0 += 32 * kRegs) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int q = warp + 32 * h;
-        if (q < P) {
-            if (lane == 0) cnt_w[h] = __ldcg(&rowcounts[q]);
-#pragma unroll
-            for (int j = 0; j < kPairRegs; ++j) {
-                const int i = lane + 32 * j;
-                const bool in_row = i < L && static_cast<long long>(q) * L + i < t.max_comp;
-                pr[h][j] = in_row ? __ldcg(&rowpairs[static_cast<size_t>(q) * L + i]) : make_uint2(0u, 0u);
+            for (int r = 0; r < kRegs; ++r) {
+                const int i = b0 + r * 32 + lane;
+                const uint32_t key = float_to_key(in_regs ? v0[r] : (i < hi ? __ldcg(&sc[i]) : 0.f));
+                const bool keep = i < hi && (key >> kBinShift) >= tb;
+                const unsigned bk = __ballot_sync(0xffffffffu, keep);
+                if (bk == 0u) continue;
+                if (keep) {
+                    const int at = pos + __popc(bk & lt);
+                    if (in_smem) st_cluster_v2(sp0 + 8u * static_cast<uint32_t>(at), key, static_cast<uint32_t>(i));
+                    else gp[at] = make_uint2(key, static_cast<uint32_t>(i));
+                }
+                pos += __popc(bk);
             }
         }
     }
+    cluster_arrive();
+    cluster_wait();
+    if (rank != 0) return;
+    // 5. CTA 0: the 12-bit sub-bin (bits 19..8) of bin tb holding the k-th key
     int c2[per_bin];
 #pragma unroll
     for (int i = 0; i < per_bin; ++i)
-        c2[i] = static_cast<int>(__ldcg(&g2[kBins - 1 - (static_cast<int>(threadIdx.x) * per_bin + i)]));
-#pragma unroll
-    for (int h = 0; h < 2; ++h) cnt_w[h] = __shfl_sync(0xffffffffu, cnt_w[h], 0);
-    if (lane == 0) {
-        if (warp < P) offs[warp + 1] = cnt_w[0];
-        if (warp + 32 < P) offs[warp + 33] = cnt_w[1];
-    }
-    __syncthreads();
-    if (warp < 2) {                              // inclusive scan of the P <= 64 slice counts
-        int v = static_cast<int>(threadIdx.x) < P ? offs[threadIdx.x + 1] : 0;
-        v = warp_incl(v);
-        if (threadIdx.x == 31) s_b[1] = v;
-        offs[threadIdx.x + 1] = v;
-        if (threadIdx.x == 0) offs[0] = 0;
-    }
-    __syncthreads();
-    if (threadIdx.x >= 32 && threadIdx.x < 64) offs[threadIdx.x + 1] += s_b[1];
-    // the 12-bit sub-bin (bits 19..8) of bin tb holding the k-th key (its syncs publish offs)
+        c2[i] = static_cast<int>(h2sum[kBins - 1 - (static_cast<int>(threadIdx.x) * per_bin + i)]);
     find_bin<NT>(c2, k - above, s_a, bc);
     const uint32_t prefix = (tb << kBinShift) | (static_cast<uint32_t>(bc[0]) << 8);
     const int need = k - above - bc[1];
     const bool whole_sub_bin = need == bc[2] && prefix != 0u;   // every key of the sub-bin is in
-    const int total = offs[P];
-    auto slice_of = [&](int i) {                 // slice q with offs[q] <= i < offs[q + 1]
-        int a = 0, b = P - 1;
-        while (a < b) {
-            const int mid = (a + b + 1) >> 1;
-            if (offs[mid] <= i) a = mid; else b = mid - 1;
-        }
-        return a;
-    };
     uint32_t T;
     int need_T;
-    if (total <= kFinalCap) {
-        // each warp places its slices' survivors at the slices' offsets
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int q = warp + 32 * h;
-            if (q < P) {
-                const int base = offs[q], cnt = cnt_w[h];
-#pragma unroll
-                for (int j = 0; j < kPairRegs; ++j) {
-                    const int i = lane + 32 * j;
-                    if (i < cnt) spairs[base + i] = pr[h][j];
-                }
-                for (int i = kPairRegs * 32 + lane; i < cnt; i += 32)
-                    spairs[base + i] = __ldcg(&rowpairs[static_cast<size_t>(q) * L + i]);
-            }
-        }
-        __syncthreads();
-        auto key_at = [&](int i) { return spairs[i].x; };
-        auto idx_at = [&](int i) { return static_cast<int32_t>(spairs[i].y); };
+    auto finish = [&](auto key_at, auto idx_at) {
         if (whole_sub_bin) {
             // the k keys are exactly those at or above the sub-bin: no selection inside it
             T = prefix - 1u;
@@ -463,21 +427,13 @@ topk_filter_kernel(TopkRows t, LongWs w, int L, int P, uint32_t* eword) {
             radix_select<NT>(total, need, key_at, hist, bc, T, need_T, prefix, 32 - 8);
         }
         ordered_select<NT>(total, T, need_T, key_at, idx_at, out, s_a, s_b);
+    };
+    if (in_smem) {
+        finish([&](int i) { return spairs[i].x; }, [&](int i) { return static_cast<int32_t>(spairs[i].y); });
     } else {
-        // degenerate score distributions (huge ties): the same steps on the slices in place
-        auto at = [&](int i) {
-            const int q = slice_of(i);
-            return __ldcg(&rowpairs[static_cast<size_t>(q) * L + (i - offs[q])]);
-        };
-        auto key_at = [&](int i) { return at(i).x; };
-        auto idx_at = [&](int i) { return static_cast<int32_t>(at(i).y); };
-        if (whole_sub_bin) {
-            T = prefix - 1u;
-            need_T = 0;
-        } else {
-            radix_select<NT>(total, need, key_at, hist, bc, T, need_T, prefix, 32 - 8);
-        }
-        ordered_select<NT>(total, T, need_T, key_at, idx_at, out, s_a, s_b);
+        // degenerate score distributions (huge ties): the list in global memory
+        const uint2* gp = w.pairs + static_cast<size_t>(row) * t.max_comp;
+        finish([&](int i) { return __ldcg(&gp[i]).x; }, [&](int i) { return static_cast<int32_t>(__ldcg(&gp[i]).y); });
     }
 }
 
@@ -501,15 +457,13 @@ size_t topk_ws_bytes(int rows, int max_comp, int top_k) {
     (void)top_k;
     if (max_comp <= kSmallCap) return 0;
     size_t b = 0;
-    b += static_cast<size_t>(rows) * kBins * 4 * 2;       // both histograms, then
-    b += align_up(static_cast<size_t>(rows) * 4, 256);    // tickets (one memset clears all three)
-    b += align_up(static_cast<size_t>(rows) * kMaxSlices * 4, 256);
+    b += align_up(static_cast<size_t>(rows) * kBins * 4, 256);   // the row histograms
     b += align_up(static_cast<size_t>(rows) * max_comp * 8, 256);
     return b;
 }
 
 uint32_t* topk_hist_buffer(uint8_t* ws) { return reinterpret_cast<uint32_t*>(ws); }
-size_t topk_hist_bytes(int rows) { return static_cast<size_t>(rows) * (2 * kBins + 1) * 4; }
+size_t topk_hist_bytes(int rows) { return static_cast<size_t>(rows) * kBins * 4; }
 bool topk_uses_hist(int max_comp) { return max_comp > kSmallCap; }
 
 int launch_topk(const TopkRows& t, uint8_t* ws, uint32_t* eword, cudaStream_t stream) {
@@ -530,32 +484,30 @@ int launch_topk(const TopkRows& t, uint8_t* ws, uint32_t* eword, cudaStream_t st
     LongWs w;
     uint8_t* p = ws;
     w.hist = reinterpret_cast<uint32_t*>(p);
-    p += static_cast<size_t>(t.rows) * kBins * 4;
-    w.hist2 = reinterpret_cast<uint32_t*>(p);
-    p += static_cast<size_t>(t.rows) * kBins * 4;
-    w.done = reinterpret_cast<uint32_t*>(p);
-    p += align_up(static_cast<size_t>(t.rows) * 4, 256);
-    w.counts = reinterpret_cast<int32_t*>(p);
-    p += align_up(static_cast<size_t>(t.rows) * kMaxSlices * 4, 256);
+    p += align_up(static_cast<size_t>(t.rows) * kBins * 4, 256);
     w.pairs = reinterpret_cast<uint2*>(p);
     if (!t.hist_zeroed &&
         cudaMemsetAsync(w.hist, 0, topk_hist_bytes(t.rows), stream) != cudaSuccess)
         return DSV4_ERR_LAUNCH;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaFuncSetAttribute(topk_filter_kernel<kNT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(topk_cluster_kernel<kNT, kCl>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kFinalCap * 8);
+        if (kCl > 8) cudaFuncSetAttribute(topk_cluster_kernel<kNT, kCl>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         attr_set = true;
     }
-    dim3 grid(t.rows, pl.P);
     if (!t.hist_built) {
         count_launch();
-        if (launch_k(topk_hist_kernel<kNT>, grid, dim3(kNT), 0, stream, t.pdl, t, w, pl.L, eword) != cudaSuccess)
+        if (launch_k(topk_hist_kernel<kNT>, dim3(t.rows, pl.P), dim3(kNT), 0, stream, t.pdl, t, w, pl.L, eword)
+            != cudaSuccess)
             return DSV4_ERR_LAUNCH;
     }
+    // slices of the cluster kernel: CTA r of a row's cluster takes [r * Lc, (r + 1) * Lc)
+    const int Lc = (t.max_comp + kCl - 1) / kCl;
     count_launch();
-    return launch_k(topk_filter_kernel<kNT>, grid, dim3(kNT), size_t(kFinalCap * 8), stream, t.pdl, t, w,
-                    pl.L, pl.P, eword) == cudaSuccess ? DSV4_OK : DSV4_ERR_LAUNCH;
+    return launch_cluster_k(topk_cluster_kernel<kNT, kCl>, dim3(kCl, t.rows), dim3(kNT), size_t(kFinalCap * 8),
+                            stream, t.pdl, static_cast<unsigned>(kCl), t, w, Lc, eword) == cudaSuccess
+               ? DSV4_OK : DSV4_ERR_LAUNCH;
 }
 
 }  // namespace dsv4
