@@ -32,21 +32,21 @@ struct TopkRows {
     int n_q, ratio;
     int32_t* idx_out;        // [rows, top_k]
     int rows, max_comp, top_k;
-    bool hist_zeroed;        // the long-row histogram and tickets were zeroed by the caller
+    bool hist_zeroed;        // the long-row histogram was zeroed by the caller
     bool hist_built;         // ... and already filled (by the scoring epilogue)
     bool pdl;                // launch with programmatic dependent launch
 };
 size_t topk_ws_bytes(int rows, int max_comp, int top_k);
 int launch_topk(const TopkRows& t, uint8_t* ws, uint32_t* eword, cudaStream_t stream);
-// Long rows keep a top-12-bit key histogram ([rows, 4096] u32, then [rows] tickets) at the
-// start of the top-k workspace; a producer of scores may fill it (after it was zeroed).
+// Long rows keep a top-12-bit key histogram ([rows, 4096] u32) at the start of the top-k
+// workspace; a producer of scores may fill it (after it was zeroed).
 bool topk_uses_hist(int max_comp);
 uint32_t* topk_hist_buffer(uint8_t* topk_ws);
 size_t topk_hist_bytes(int rows);
 
 size_t index_ws_bytes(const dsv4_index_args& a);
 // Bytes at the start of the indexer workspace that must be zero when the call starts (the
-// long-row histogram and tickets); callers clear them together with the error word.
+// long-row histograms); callers clear them together with the error word.
 size_t index_zero_bytes(const dsv4_index_args& a);
 // fresh_keys: the compression that writes key rows just before (its rows are waited for).
 int launch_indexer(const dsv4_index_args& a, uint8_t* ws, uint32_t* eword, cudaStream_t stream,

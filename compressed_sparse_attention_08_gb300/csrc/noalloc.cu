@@ -4,7 +4,7 @@
 // code running inside an allocator callback or an allocator-free serving loop, a host
 // runtime that forbids cudaMalloc after start-up, or a plug-in handed only its input and
 // output buffers. dsv4_topk_noalloc serves them: its scratch space (error word, per-row
-// histograms, tickets and survivor lists of the long-row path) is one file-scope device
+// histograms and survivor lists of the long-row path) is one file-scope device
 // array, reserved when the library's kernels are loaded on a GPU and held there until the
 // process exits. It runs exactly the same kernels as dsv4_topk.
 #include "common.cuh"
@@ -55,7 +55,7 @@ extern "C" int dsv4_topk_noalloc(const dsv4_topk_args* a, dsv4_stream_t stream) 
     if (!scratch) return DSV4_ERR_LAUNCH;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     // the array keeps the previous call's contents: clear the error word (the long-row
-    // histogram and tickets are cleared by the launcher below)
+    // histograms are cleared by the launcher below)
     if (cudaMemsetAsync(scratch, 0, kWsHeader, st) != cudaSuccess) return DSV4_ERR_LAUNCH;
     TopkRows t;
     t.scores = a->scores;
