@@ -48,6 +48,8 @@ def parse():
                     help="time only the chunked-prefill indexer scoring (tensor-core bound)")
     ap.add_argument("--fp8-only", action="store_true",
                     help="time only the decode step with the FP8 index-key cache")
+    ap.add_argument("--decode-workload", type=int, choices=[1, 2], default=None,
+                    help="time only the decode step of workload 1 (8K context, batch 16) or 2 (HCA)")
     return ap.parse_args()
 
 
@@ -225,6 +227,127 @@ def fp8_keys_step(m, _abi, t, wl, steps, stream, peak):
                        "ms_per_launch": score_ms, "achieved": gbs, "peak": peak, "unit": "GB/s",
                        "frac": gbs / peak,
                        "traffic": profile_traffic("index_score_kernel_fp8_csa_decode_ctx1048576_b4.md")}}
+
+
+def decode_step_at(m, _abi, cfg, steps, peak):
+    """The fused decode step of another decode workload (the 8K-context batch-16 CSA layer,
+    the 8K-context batch-64 HCA layer), timed like the headline: the caches are filled once
+    by compressing the whole context, then each step compresses the newest block into the
+    last cache row and runs the rest of the step; one CUDA graph per step. Algorithmic
+    bytes per step as for the headline (keys scanned + gathered rows + outputs)."""
+    import numpy as np
+    import torch
+    from compressed_sparse_attention_08_gb300.workloads import WORKLOADS, make_inputs
+    wl = WORKLOADS[cfg]
+    x = make_inputs(wl)
+    B, D, Di, r, T = wl.batch, wl.head_dim, wl.idx_dim, wl.ratio, wl.context
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a, np.uint16).view(np.int16)).cuda().view(torch.bfloat16)
+
+    def dv(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+    t = {k: bf(x[k]) for k in ("C", "Z", "q", "win")}
+    t.update({k: dv(x[k]) for k in ("bias", "gamma", "pos0", "n_comp", "sink", "win_len")})
+    t["kv"] = torch.zeros(B, wl.max_comp, D, dtype=torch.bfloat16, device="cuda")
+    m.dsv4_compress(t["C"], t["Z"], t["bias"], t["gamma"], t["pos0"], t["kv"], ratio=r)
+    t["pos_n"] = torch.full((B,), T - r, dtype=torch.int64, device="cuda")
+    t["row_n"] = torch.full((B,), wl.n_comp - 1, dtype=torch.int32, device="cuda")
+    t["Cn"], t["Zn"] = t["C"][:, T - r:].contiguous(), t["Z"][:, T - r:].contiguous()
+    ck = _abi.compress_args(t["Cn"], t["Zn"], t["bias"], t["gamma"], t["pos_n"], t["kv"], ratio=r,
+                            out_row0=t["row_n"])
+    cq = ia = None
+    k = wl.max_comp if wl.dense else wl.top_k
+    t["out"] = torch.empty(B, 1, wl.heads, D, dtype=torch.bfloat16, device="cuda")
+    t["gather"] = torch.empty(B, 1, k + wl.window, D, dtype=torch.bfloat16, device="cuda")
+    if not wl.dense:
+        t.update({kk: bf(x[kk]) for kk in ("C_I", "Z_I", "q_I")})
+        t.update({kk: dv(x[kk]) for kk in ("bias_I", "gamma_I", "w")})
+        t["keys"] = torch.zeros(B, wl.max_comp, Di, dtype=torch.bfloat16, device="cuda")
+        m.dsv4_compress(t["C_I"], t["Z_I"], t["bias_I"], t["gamma_I"], t["pos0"], t["keys"], ratio=r)
+        t["CIn"], t["ZIn"] = t["C_I"][:, T - r:].contiguous(), t["Z_I"][:, T - r:].contiguous()
+        cq = _abi.compress_args(t["CIn"], t["ZIn"], t["bias_I"], t["gamma_I"], t["pos_n"], t["keys"], ratio=r,
+                                out_row0=t["row_n"])
+        t["idx"] = torch.empty(B, 1, k, dtype=torch.int32, device="cuda")
+        ia = _abi.index_args(t["q_I"], t["w"], t["keys"], t["n_comp"], t["idx"], ratio=r)
+    aa = _abi.attn_args(t["q"], t["sink"], t["kv"], t["n_comp"], t["win"], t["win_len"], t["out"],
+                        idx=t.get("idx"), top_k=k, window=wl.window, ratio=r, gather=t["gather"])
+    ws = torch.empty(max(m.dsv4_csa_decode_workspace_size(attn=aa, index=ia, compress_kv=ck, compress_keys=cq),
+                         256), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def step(s):
+        m.dsv4_csa_decode(ws, attn=aa, index=ia, compress_kv=ck, compress_keys=cq, stream=s)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step(stream)
+    stream.synchronize()
+    launches = m.dsv4_last_launch_count()
+    st, ew = m.dsv4_read_error_word(ws, stream)
+    if ew:
+        raise SystemExit(f"device error word {ew:#x} in the {wl.name} step")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            step(stream)
+    stream.synchronize()
+    # the workload fits in L2: every timed replay starts from a flushed L2 (a 256 MiB write
+    # between replays, outside the timed events)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    with torch.cuda.stream(stream):
+        for _ in range(5):
+            graph.replay()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for a, b in evs:
+            flush.zero_()
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    keys = 0 if wl.dense else B * wl.n_comp * Di * 2
+    nbytes = keys + B * (k + wl.window) * D * 2 + B * wl.heads * D * 2
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": wl.name, "value": B / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
+            "launches_per_step": launches, "bytes_per_step": nbytes, "achieved": gbs, "peak": peak,
+            "unit_bw": "GB/s", "frac": gbs / peak, "l2": "flushed before every timed replay"}
+
+
+def compressor_time(m, t, wl, steps, stream):
+    """The compressor alone at the headline workload: the newest block of the KV cache and of
+    the key cache, one dsv4_compress call each (in the fused step they share one launch),
+    captured in a CUDA graph so the host does not pace it. A latency-bound reduction:
+    microseconds per pair of calls."""
+    import torch
+
+    def run():
+        m.dsv4_compress(t["C"], t["Z"], t["bias"], t["gamma"], t["pos0"], t["kv"], ratio=wl.ratio,
+                        out_row0=t["append_row"], stream=stream)
+        m.dsv4_compress(t["C_I"], t["Z_I"], t["bias_I"], t["gamma_I"], t["pos0"], t["keys"], ratio=wl.ratio,
+                        out_row0=t["append_row"], stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            run()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            run()
+    stream.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(5):
+            g.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps * 1000.0
 
 
 def device_arena(specs):
@@ -571,6 +694,8 @@ def run_ours(args):
     if world == 1:
         line["prefill_scoring"] = prefill_scoring(m, args.steps)
         line["fp8_keys"] = fp8_keys_step(m, _abi, t, wl, args.steps, stream, peak)
+        line["compressor_us"] = compressor_time(m, t, wl, args.steps, stream)
+        line["other_decode_workloads"] = [decode_step_at(m, _abi, c, args.steps, peak) for c in (1, 2)]
     if world == 1 and not args.no_cpu_baseline:
         x0 = make_inputs(wl, batch=1)
         line["cpu_baseline"] = cpu_baseline(wl, x0)
@@ -581,6 +706,16 @@ def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.decode_workload is not None:
+        import torch
+        if not torch.cuda.is_available():
+            raise SystemExit("bench.py needs a CUDA device")
+        import __graft_entry__
+        __graft_entry__.build()
+        import compressed_sparse_attention_08_gb300 as m
+        from compressed_sparse_attention_08_gb300 import _abi
+        peak, _ = measured_peaks()
+        print(json.dumps(decode_step_at(m, _abi, args.decode_workload, args.steps, peak)), flush=True)
     elif args.prefill_only:
         import torch
         if not torch.cuda.is_available():

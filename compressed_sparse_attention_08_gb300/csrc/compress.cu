@@ -36,8 +36,11 @@
 namespace dsv4 {
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kMaxChan = 8;          // dim <= 1024
+// 256 threads at no more than 128 registers each (launch bounds of two CTAs per SM): a
+// compressor CTA fits beside a scoring CTA, which the fused step starts while it runs
+constexpr int kThreads = 256;
+constexpr int kMaxChan = 4;          // channels per thread: dim <= 1024
+constexpr int kChunk = 4;            // tokens per load round (every channel's loads in flight together)
 constexpr int kMaxPairs = 64;        // rope_dim <= 128
 
 struct CompressJob {
@@ -86,49 +89,70 @@ __device__ void entry_math(const EntryIn& in, const double* freq, float* y, floa
     const int tid = threadIdx.x;
     const int dim = in.dim, ratio = in.ratio;
     const size_t w = in.w;
+    // per channel (c = tid + i * kThreads): online softmax of Z + bias over the pooled tokens
+    // and the weighted sum of C, kChunk tokens at a time; each round issues the loads of all
+    // of the thread's channels before any is used (the rounds are dependent memory trips)
+    float m[kMaxChan], den[kMaxChan], num[kMaxChan];
+#pragma unroll
+    for (int i = 0; i < kMaxChan; ++i) { m[i] = -INFINITY; den[i] = 0.f; num[i] = 0.f; }
+    auto segment = [&](const __nv_bfloat16* Cs, const __nv_bfloat16* Zs, const float* bs) {
+        for (int t0 = 0; t0 < ratio; t0 += kChunk) {
+            // every load of the round (the thread's channels x kChunk tokens) is issued before
+            // the first use: a use right behind its load would stall the in-order issue of the
+            // loads after it
+            __nv_bfloat16 zr[kMaxChan][kChunk], cr[kMaxChan][kChunk];
+            float br[kMaxChan][kChunk];
+#pragma unroll
+            for (int i = 0; i < kMaxChan; ++i) {
+                const int c = tid + i * kThreads;
+                if (c < dim) {
+#pragma unroll
+                    for (int u = 0; u < kChunk; ++u) {
+                        const size_t o = static_cast<size_t>(min(t0 + u, ratio - 1)) * w + c;
+                        zr[i][u] = Zs[o];
+                        br[i][u] = bs[o];
+                        cr[i][u] = Cs[o];
+                    }
+                }
+            }
+            float a[kMaxChan][kChunk], cv[kMaxChan][kChunk];
+#pragma unroll
+            for (int i = 0; i < kMaxChan; ++i) {
+                const bool cok = tid + i * kThreads < dim;
+#pragma unroll
+                for (int u = 0; u < kChunk; ++u) {
+                    const bool ok = cok && t0 + u < ratio;
+                    a[i][u] = ok ? __bfloat162float(zr[i][u]) + br[i][u] : -INFINITY;
+                    cv[i][u] = ok ? __bfloat162float(cr[i][u]) : 0.f;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kMaxChan; ++i) {
+                float mc = a[i][0];
+#pragma unroll
+                for (int u = 1; u < kChunk; ++u) mc = fmaxf(mc, a[i][u]);
+                const float mn = fmaxf(m[i], mc);
+                const float sc = m[i] == -INFINITY ? 0.f : expf(m[i] - mn);
+                den[i] *= sc;
+                num[i] *= sc;
+#pragma unroll
+                for (int u = 0; u < kChunk; ++u) {
+                    const float e = a[i][u] == -INFINITY ? 0.f : expf(a[i][u] - mn);
+                    den[i] += e;
+                    num[i] = fmaf(e, cv[i][u], num[i]);   // no bias on C
+                }
+                m[i] = mn;
+            }
+        }
+    };
+    if (in.aC) segment(in.aC, in.aZ, in.bias);          // stream a: bias columns [0, dim)
+    segment(in.oC + in.own_off, in.oZ + in.own_off, in.bias + in.own_off);
     float x[kMaxChan];
     float sq = 0.f;
 #pragma unroll
     for (int i = 0; i < kMaxChan; ++i) {
         const int c = tid + i * kThreads;
-        x[i] = 0.f;
-        if (c >= dim) continue;
-        float m = -INFINITY, den = 0.f, num = 0.f;
-        // online softmax over one segment of `ratio` tokens, 8 tokens at a time with all loads
-        // of a chunk issued before any is used
-        auto segment = [&](const __nv_bfloat16* Cs, const __nv_bfloat16* Zs, const float* bs) {
-            for (int t0 = 0; t0 < ratio; t0 += 8) {
-                float a[8], cv[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int t = t0 + u;
-                    if (t < ratio) {
-                        a[u] = __bfloat162float(Zs[static_cast<size_t>(t) * w + c]) + bs[static_cast<size_t>(t) * w + c];
-                        cv[u] = __bfloat162float(Cs[static_cast<size_t>(t) * w + c]);
-                    } else {
-                        a[u] = -INFINITY;
-                        cv[u] = 0.f;
-                    }
-                }
-                float mc = a[0];
-#pragma unroll
-                for (int u = 1; u < 8; ++u) mc = fmaxf(mc, a[u]);
-                const float mn = fmaxf(m, mc);
-                const float sc = m == -INFINITY ? 0.f : expf(m - mn);
-                den *= sc;
-                num *= sc;
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const float e = a[u] == -INFINITY ? 0.f : expf(a[u] - mn);
-                    den += e;
-                    num = fmaf(e, cv[u], num);   // no bias on C
-                }
-                m = mn;
-            }
-        };
-        if (in.aC) segment(in.aC, in.aZ, in.bias);          // stream a: bias columns [0, dim)
-        segment(in.oC + in.own_off, in.oZ + in.own_off, in.bias + in.own_off);
-        x[i] = num / den;
+        x[i] = c < dim ? num[i] / den[i] : 0.f;
         sq = fmaf(x[i], x[i], sq);
     }
     // RMSNorm: mean of x^2 over all dim channels
@@ -179,7 +203,7 @@ __device__ void entry_math(const EntryIn& in, const double* freq, float* y, floa
 // zero_p/zero_n16: a workspace region (16-byte words) this launch clears for the kernels after
 // it (the fused decode step), so the step needs no separate memset; they read it only after
 // waiting for this grid.
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 compress_kernel(const __grid_constant__ CompressJob j0, const __grid_constant__ CompressJob j1,
                 uint4* zero_p, unsigned zero_n16) {
     pdl_trigger();
@@ -313,7 +337,7 @@ struct StepJob {
     double log2_theta;
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 compress_step_kernel(const __grid_constant__ StepJob j) {
     __shared__ float y[1024];
     __shared__ float warp_sum[kThreads / 32];
