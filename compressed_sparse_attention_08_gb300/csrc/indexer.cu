@@ -68,12 +68,10 @@ struct KeyFmt {
     static constexpr int kSub = kStageKeys / kTileKeys;
     static constexpr int kKSteps = kDim * kElem / 32;
     static constexpr int kBoxInner = 128 / kElem;          // elements per 128-byte box row
-    static constexpr int kEpiGroups = FP8 ? 2 : 1;         // epilogue groups of 4 warps
     // TMEM accumulators: two stages' worth of tiles, so the MMAs of a stage wait only for the
     // epilogue of the stage two back (256 or 512 columns: a power of two)
     static constexpr int kAccBufs = 2 * kSub;
     static constexpr uint32_t kTmemCols = kAccBufs * kAccCols;
-    static constexpr int kThreads = 64 + 128 * kEpiGroups;
 };
 constexpr int kHistBins = 4096;             // top 12 bits of the order-preserving score key
 constexpr int kIdRing = 8;                  // stage ids in flight from the producer
@@ -94,6 +92,7 @@ struct ScoreParams {
     const float* q_scale;    // FP8 keys: [rows, heads] query scales, else null
     const float* key_scale;  // FP8 keys: [batch, max_comp] key scales, else null
     uint32_t* claim;         // [rows] zeroed stage-claim counters, or null (static shares only)
+    int reuse_keys;          // many rows share the keys (prefill): keep them in L2, stream the scores
     int rows, n_q, heads, max_comp, ratio, stages_per_row;
 };
 
@@ -116,8 +115,9 @@ __device__ __forceinline__ Walk cta_walk(int rows, int per_row) {
 }
 
 // NP: the heads padded to a multiple of 16 (the UMMA N and the TMEM columns the epilogue reads)
-template <bool FP8, int NP>
-__global__ void __launch_bounds__(KeyFmt<FP8>::kThreads, 1)
+// EG: epilogue groups of four warps (threads 64 + 128 EG)
+template <bool FP8, int NP, int EG>
+__global__ void __launch_bounds__(64 + 128 * EG, 1)
 index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap qmap, ScoreParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -134,7 +134,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
 
     using F = KeyFmt<FP8>;
     constexpr int kStageKeys = F::kStageKeys, kSub = F::kSub;
-    constexpr int kThreads = F::kThreads, kEpiGroups = F::kEpiGroups, kAccBufs = F::kAccBufs;
+    constexpr int kEpiGroups = EG, kThreads = 64 + 128 * EG, kAccBufs = F::kAccBufs;
     constexpr uint32_t kTmemCols = F::kTmemCols;
     constexpr int kFlushStages = 65535 / kStageKeys;   // a 16-bit bin count cannot overflow
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -187,7 +187,9 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
             bool waited = false, claiming = false;
             long long issued = 0, seq = 0, f = wk.begin;
             uint32_t phase = 0;
-            const uint64_t stream_policy = l2_evict_first_policy();   // keys are read once
+            // decode: every key is read once (evict first); prefill: every query row re-reads
+            // the same keys (evict last), while its scores stream past them
+            const uint64_t stream_policy = p.reuse_keys ? l2_evict_last_policy() : l2_evict_first_policy();
             auto claim = [&]() {
                 // the counters are cleared by the work before this grid
                 if (!waited) { pdl_wait(); waited = true; }
@@ -465,8 +467,8 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                 float s = 0.f;
                 if constexpr (FP8) {
                     // four partial sums (heads h mod 4) in two packed pairs: half the FMA
-                    // instructions and a quarter of the dependent-FMA latency per key (the
-                    // epilogue, not HBM, sets the pace of 512-key stages)
+                    // instructions and a quarter of the dependent-FMA latency per key (here the
+                    // epilogue, not HBM, sets the pace)
                     uint64_t a01 = 0, a23 = 0;
 #pragma unroll
                     for (int h4 = 0; h4 < NP / 4; ++h4) {
@@ -487,7 +489,9 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                 }
                 const int key = tile * kTileKeys + lrow;
                 if (key < nv) {
-                    p.scores[static_cast<size_t>(row) * p.max_comp + key] = s;
+                    float* dst = p.scores + static_cast<size_t>(row) * p.max_comp + key;
+                    if (p.reuse_keys) __stcs(dst, s);
+                    else *dst = s;
                     if (p.hist) {
                         const uint32_t bin = float_to_key(s) >> 20;
                         atomicAdd(&s_hist[bin >> 1], (bin & 1u) ? 0x10000u : 1u);
@@ -564,7 +568,7 @@ size_t index_zero_bytes(const dsv4_index_args& a) {
 }
 
 namespace {
-template <bool FP8, int NP>
+template <bool FP8, int NP, int EG>
 int launch_scores_fmt(const dsv4_index_args& a, float* scores, uint32_t* hist, uint32_t* eword,
                       cudaStream_t stream, const dsv4_compress_args* fresh) {
     using F = KeyFmt<FP8>;
@@ -606,6 +610,7 @@ int launch_scores_fmt(const dsv4_index_args& a, float* scores, uint32_t* hist, u
     p.q_scale = FP8 ? a.q_scale : nullptr;
     p.key_scale = FP8 ? a.key_scale : nullptr;
     p.claim = eword && rows <= kMaxClaimRows ? eword + kClaimWord : nullptr;
+    p.reuse_keys = rows > sm_count() ? 1 : 0;
     p.rows = rows;
     p.n_q = a.n_q;
     p.heads = a.heads;
@@ -616,14 +621,14 @@ int launch_scores_fmt(const dsv4_index_args& a, float* scores, uint32_t* hist, u
     if (total > 0) {
         static bool attr_set = false;
         if (!attr_set) {
-            cudaFuncSetAttribute(index_score_kernel<FP8, NP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            cudaFuncSetAttribute(index_score_kernel<FP8, NP, EG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kSmemBytes));
             attr_set = true;
         }
         long long grid = sm_count();
         if (grid > total) grid = total;
         count_launch();
-        if (launch_k(index_score_kernel<FP8, NP>, dim3(static_cast<unsigned>(grid)), dim3(F::kThreads), kSmemBytes,
+        if (launch_k(index_score_kernel<FP8, NP, EG>, dim3(static_cast<unsigned>(grid)), dim3(64 + 128 * EG), kSmemBytes,
                      stream, true, kmap, qmap, p) != cudaSuccess)
             return DSV4_ERR_LAUNCH;
     }
@@ -633,10 +638,13 @@ int launch_scores_fmt(const dsv4_index_args& a, float* scores, uint32_t* hist, u
 int launch_scores(const dsv4_index_args& a, float* scores, uint32_t* hist, uint32_t* eword,
                   cudaStream_t stream, const dsv4_compress_args* fresh) {
     const int n_pad = (a.heads + 15) / 16 * 16;
+    // Two epilogue groups where the epilogue, not HBM, sets the pace: FP8 keys (512 keys per
+    // stage). One group for bf16 keys, whose registers then leave room for a compressor CTA
+    // beside the scoring CTA (a second group did not speed up the many-row prefill either).
 #define DSV4_SCORES_NP(np)                                                               \
     if (n_pad == np)                                                                     \
-        return a.key_fp8 ? launch_scores_fmt<true, np>(a, scores, hist, eword, stream, fresh) \
-                         : launch_scores_fmt<false, np>(a, scores, hist, eword, stream, fresh);
+        return a.key_fp8 ? launch_scores_fmt<true, np, 2>(a, scores, hist, eword, stream, fresh) \
+                         : launch_scores_fmt<false, np, 1>(a, scores, hist, eword, stream, fresh);
     DSV4_SCORES_NP(16)
     DSV4_SCORES_NP(32)
     DSV4_SCORES_NP(48)
