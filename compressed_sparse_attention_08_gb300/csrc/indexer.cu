@@ -94,6 +94,8 @@ struct ScoreParams {
     uint32_t* claim;         // [rows] zeroed stage-claim counters, or null (static shares only)
     int reuse_keys;          // many rows share the keys (prefill): keep them in L2, stream the scores
     int rows, n_q, heads, max_comp, ratio, stages_per_row;
+    // the walk's units: QB consecutive query rows of one sequence (QB = 1: a unit is a row)
+    int units, gpb;          // units in all, units per sequence (ceil(n_q / QB))
 };
 
 // The stages one CTA scores, as positions f = row * stages_per_row + stage: f = begin,
@@ -114,9 +116,11 @@ __device__ __forceinline__ Walk cta_walk(int rows, int per_row) {
     return {r * per_row + (c - cb), (r + 1) * per_row, ce - cb};
 }
 
-// NP: the heads padded to a multiple of 16 (the UMMA N and the TMEM columns the epilogue reads)
+// NP: the heads padded to a multiple of 16 (the TMEM columns of one query's heads)
 // EG: epilogue groups of four warps (threads 64 + 128 EG)
-template <bool FP8, int NP, int EG>
+// QB: query rows scored per MMA (UMMA N = QB * NP): with QB = 2 (many rows of bf16 keys,
+//     prefill) each key stage serves two queries, half the key traffic per score
+template <bool FP8, int NP, int EG, int QB>
 __global__ void __launch_bounds__(64 + 128 * EG, 1)
 index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap qmap, ScoreParams p) {
@@ -130,12 +134,15 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
     __shared__ volatile int abort_flag;
     // top-12-bit key histogram of the current row, two 16-bit counts per word (8 KB: a
     // compressor CTA still fits beside this CTA on its SM)
-    __shared__ uint32_t s_hist[kHistBins / 2];
+    // (none with QB = 2: those launches build no histogram, and the query pairs need the room)
+    __shared__ uint32_t s_hist[QB == 1 ? kHistBins / 2 : 1];
 
     using F = KeyFmt<FP8>;
     constexpr int kStageKeys = F::kStageKeys, kSub = F::kSub;
     constexpr int kEpiGroups = EG, kThreads = 64 + 128 * EG, kAccBufs = F::kAccBufs;
-    constexpr uint32_t kTmemCols = F::kTmemCols;
+    constexpr int kAccColsQ = kAccCols * QB;                 // TMEM columns per accumulator
+    constexpr uint32_t kTmemCols = static_cast<uint32_t>(kAccBufs * kAccColsQ);   // 256 or 512
+    static_assert(!(FP8 && QB > 1) && kTmemCols <= 512, "scorer shape");
     constexpr int kFlushStages = 65535 / kStageKeys;   // a 16-bit bin count cannot overflow
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_trigger();
@@ -159,9 +166,9 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
         tma_prefetch_desc(&qmap);
     }
     // query rows past `heads` stay zero for the whole kernel (TMA writes only `heads` rows)
-    for (uint32_t i = threadIdx.x; i < kQBufBytes / 16; i += kThreads)
+    for (uint32_t i = threadIdx.x; i < kQBufBytes * QB / 16; i += kThreads)
         reinterpret_cast<uint4*>(q_buf)[i] = make_uint4(0, 0, 0, 0);
-    for (int i = threadIdx.x; i < kHistBins / 2; i += kThreads) s_hist[i] = 0;
+    for (int i = threadIdx.x; i < (QB == 1 ? kHistBins / 2 : 1); i += kThreads) s_hist[i] = 0;
     if (warp == 1) tmem_alloc(&tmem_slot, kTmemCols);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     tc_fence_before();
@@ -169,10 +176,18 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
     tc_fence_after();
     const uint32_t tmem_base = tmem_slot;
 
-    const Walk wk = cta_walk(p.rows, p.stages_per_row);
+    const Walk wk = cta_walk(p.units, p.stages_per_row);
     const int spr = p.stages_per_row;
-    const uint32_t idesc = FP8 ? idesc_e4m3_f32(kTileKeys, NP) : idesc_bf16_f32(kTileKeys, NP);
-    const uint32_t q_half = static_cast<uint32_t>(NP) * 128u;   // bf16: bytes of one 64-dim half
+    const uint32_t idesc = FP8 ? idesc_e4m3_f32(kTileKeys, NP * QB) : idesc_bf16_f32(kTileKeys, NP * QB);
+    const uint32_t q_half = static_cast<uint32_t>(NP * QB) * 128u;   // bf16: bytes of one 64-dim half
+    // unit u: sequence u / gpb, query rows b * n_q + t0 + q for q < QB with t0 + q < n_q
+    auto unit_row = [&](int u, int q) { return (u / p.gpb) * p.n_q + (u % p.gpb) * QB + q; };
+    auto unit_nq = [&](int u) { const int t0 = (u % p.gpb) * QB; return min(QB, p.n_q - t0); };
+    // a unit sees the keys of its last query (visibility grows with the position)
+    auto unit_visible = [&](int u) {
+        return row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp,
+                           unit_row(u, unit_nq(u) - 1), nullptr);
+    };
 
     if (warp == 0) {
         if (lane == 0) {
@@ -214,14 +229,14 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                     row = row0;
                     st = cutoff + ahead;
                     if (row != vis_row) {
-                        nv = row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, row, nullptr);
+                        nv = unit_visible(row);
                         vis_row = row;
                     }
                     if (st >= spr || st * kStageKeys >= nv) break;     // the row is all taken
                     claim();                                            // the next one, early
                 }
                 if (row != vis_row) {
-                    nv = row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, row, nullptr);
+                    nv = unit_visible(row);
                     vis_row = row;
                 }
                 if (st * kStageKeys >= nv) continue;
@@ -238,16 +253,21 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                     // one query buffer: the MMA warp learns of the new row from the stage id
                     // just handed over and releases the old queries once their MMAs are done
                     if (!mbar_wait(&qempty_bar, (qcount & 1) ^ 1, &abort_flag)) goto fail0;
-                    mbar_arrive_expect_tx(&qfull_bar, static_cast<uint32_t>(p.heads) * kDim * F::kElem);
-                    tma_load_2d(q_buf, &qmap, &qfull_bar, 0, row * p.heads);
-                    if (!FP8) tma_load_2d(q_buf + q_half, &qmap, &qfull_bar, 64, row * p.heads);
+                    const int nqu = unit_nq(row);
+                    mbar_arrive_expect_tx(&qfull_bar, static_cast<uint32_t>(nqu * p.heads) * kDim * F::kElem);
+                    for (int q = 0; q < nqu; ++q) {
+                        // query q's heads at rows [q * NP, q * NP + heads) of the B operand
+                        const int qr = unit_row(row, q) * p.heads;
+                        tma_load_2d(q_buf + q * NP * 128, &qmap, &qfull_bar, 0, qr);
+                        if (!FP8) tma_load_2d(q_buf + q_half + q * NP * 128, &qmap, &qfull_bar, 64, qr);
+                    }
                     cur_row = row;
                     ++qcount;
                 }
                 if (!waited && p.fresh_rows > 0) {
                     // key rows written by the preceding kernel (the newest block's key): wait
                     // for it before streaming a stage that overlaps them
-                    const int b_ = row / p.n_q;
+                    const int b_ = row / p.gpb;
                     const int f0 = p.fresh_row0 ? p.fresh_row0[b_] : 0;
                     if (st * kStageKeys < f0 + p.fresh_rows && f0 < (st + 1) * kStageKeys) {
                         pdl_wait();
@@ -258,7 +278,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                 mbar_arrive_expect_tx(&full_bar[stage], kStageBytes);
                 {
                     uint8_t* kd = key_buf + stage * kStageBytes;
-                    const int b = row / p.n_q;
+                    const int b = row / p.gpb;
                     // bf16: the two 64-dim halves of 256 keys; FP8: two runs of 256 whole keys
                     tma_load_3d_hint(kd, &kmap, &full_bar[stage], 0, st * kStageKeys, b, stream_policy);
                     tma_load_3d_hint(kd + kBoxBytes, &kmap, &full_bar[stage], FP8 ? 0 : 64,
@@ -302,7 +322,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                     if (cur_row >= 0) umma_commit(&qempty_bar);   // old queries free once done
                     if (!mbar_wait(&qfull_bar, qcount & 1, &abort_flag)) goto fail1;
                     cur_row = row;
-                    nv = row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, row, nullptr);
+                    nv = unit_visible(row);
                     ++qcount;
                 }
                 if (!mbar_wait(&full_bar[stage], phase, &abort_flag)) goto fail1;
@@ -313,7 +333,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                         if ((st * kSub + j) * kTileKeys >= nv) break;   // tile past the visible keys
                         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1, &abort_flag)) goto fail1;
                         tc_fence_after();
-                        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kAccCols);
+                        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kAccColsQ);
                         const uint32_t a0 = a_stage + static_cast<uint32_t>(j * kTileKeys * 128);
 #pragma unroll
                         for (int k = 0; k < F::kKSteps; ++k) {
@@ -354,7 +374,9 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
         int acc = 0, cur_row = -1, nv = 0;
         uint32_t acc_phase = 0, fl_parity = 0;
         bool ok = true;
-        float wv[NP];             // the row's head weights (FP8: times the head's query scale)
+        float wv[QB][NP];         // the unit's head weights (FP8: times the head's query scale)
+        int nvq[QB];              // keys visible to each query of the unit
+        int nqu = 1;              // queries in the unit
         // Every wait of the epilogue is an mbarrier wait, bounded in time and ended early once
         // any role has given up, so a failure anywhere cannot leave a thread waiting.
         auto epi_sync = [&]() -> bool {
@@ -370,7 +392,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
             pdl_wait();      // the histogram may have been cleared by the preceding kernel
             if (epi_sync()) {
                 uint32_t* g = p.hist + static_cast<size_t>(r) * kHistBins;
-                for (int i = etid; i < kHistBins / 2; i += 128 * kEpiGroups) {
+                for (int i = etid; i < (QB == 1 ? kHistBins / 2 : 0); i += 128 * kEpiGroups) {
                     const uint32_t v = s_hist[i];
                     if (v) {
                         if (v & 0xFFFFu) atomicAdd(&g[2 * i], v & 0xFFFFu);
@@ -397,7 +419,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
         // final once the preceding kernel (which may write the newest key) has completed.
         float ks_cur[kSub], ks_next[kSub];
         auto load_ks = [&](int2 id) {
-            const float* kb = p.key_scale + static_cast<size_t>(id.x / p.n_q) * p.max_comp;
+            const float* kb = p.key_scale + static_cast<size_t>(id.x / p.gpb) * p.max_comp;
 #pragma unroll
             for (int j = 0; j < kSub; ++j) {
                 const int key = (id.y * kSub + j) * kTileKeys + lrow;
@@ -424,15 +446,21 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
             }
             ++since_flush;
             if (row != cur_row) {
-                nv = row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, row, nullptr);
+                nv = unit_visible(row);
                 cur_row = row;
+                nqu = unit_nq(row);
 #pragma unroll
-                for (int h = 0; h < NP; ++h) {
-                    const size_t o = static_cast<size_t>(row) * p.heads + h;
-                    float wh = h < p.heads ? __ldg(&p.w[o]) : 0.f;
-                    // FP8: the query scale folds into the head's weight (ReLU commutes with it)
-                    if (FP8 && h < p.heads) wh *= __ldg(&p.q_scale[o]);
-                    wv[h] = wh;
+                for (int q = 0; q < QB; ++q) {
+                    const int qrow = unit_row(row, q < nqu ? q : 0);
+                    nvq[q] = QB == 1 ? nv : row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, qrow, nullptr);
+#pragma unroll
+                    for (int h = 0; h < NP; ++h) {
+                        const size_t o = static_cast<size_t>(qrow) * p.heads + h;
+                        float wh = h < p.heads ? __ldg(&p.w[o]) : 0.f;
+                        // FP8: the query scale folds into the head's weight (ReLU commutes with it)
+                        if (FP8 && h < p.heads) wh *= __ldg(&p.q_scale[o]);
+                        wv[q][h] = wh;
+                    }
                 }
             }
             for (int j = 0; j < kSub && ok; ++j) {
@@ -447,54 +475,60 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                     break;
                 }
                 tc_fence_after();
-                // exactly the NP columns the MMA wrote (columns past them hold stale values)
-                uint32_t r[NP];
-                const uint32_t ta = tmem_base + lane_addr + static_cast<uint32_t>(my_acc * kAccCols);
-                if constexpr (NP == 64) {
-                    DSV4_TMEM_LD_32x32b_X64(ta, r);
-                } else if constexpr (NP == 32) {
-                    DSV4_TMEM_LD_32x32b_X32(ta, r);
-                } else if constexpr (NP == 48) {
-                    DSV4_TMEM_LD_32x32b_X32(ta, r);
-                    uint32_t* r2 = r + 32;
-                    DSV4_TMEM_LD_32x32b_X16(ta + 32u, r2);
-                } else {
-                    DSV4_TMEM_LD_32x32b_X16(ta, r);
-                }
-                tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive(&tempty_bar[my_acc]);
-                float s = 0.f;
-                if constexpr (FP8) {
-                    // four partial sums (heads h mod 4) in two packed pairs: half the FMA
-                    // instructions and a quarter of the dependent-FMA latency per key (here the
-                    // epilogue, not HBM, sets the pace)
-                    uint64_t a01 = 0, a23 = 0;
-#pragma unroll
-                    for (int h4 = 0; h4 < NP / 4; ++h4) {
-                        fma_f32x2(a01, pack_f32x2(fmaxf(__uint_as_float(r[4 * h4 + 0]), 0.f),
-                                                  fmaxf(__uint_as_float(r[4 * h4 + 1]), 0.f)),
-                                  pack_f32x2(wv[4 * h4 + 0], wv[4 * h4 + 1]));
-                        fma_f32x2(a23, pack_f32x2(fmaxf(__uint_as_float(r[4 * h4 + 2]), 0.f),
-                                                  fmaxf(__uint_as_float(r[4 * h4 + 3]), 0.f)),
-                                  pack_f32x2(wv[4 * h4 + 2], wv[4 * h4 + 3]));
-                    }
-                    float s0, s1, s2, s3;
-                    unpack_f32x2(a01, s0, s1);
-                    unpack_f32x2(a23, s2, s3);
-                    s = ((s0 + s1) + (s2 + s3)) * ks_cur[j];
-                } else {
-#pragma unroll
-                    for (int h = 0; h < NP; ++h) s = fmaf(wv[h], fmaxf(__uint_as_float(r[h]), 0.f), s);
-                }
                 const int key = tile * kTileKeys + lrow;
-                if (key < nv) {
-                    float* dst = p.scores + static_cast<size_t>(row) * p.max_comp + key;
-                    if (p.reuse_keys) __stcs(dst, s);
-                    else *dst = s;
-                    if (p.hist) {
-                        const uint32_t bin = float_to_key(s) >> 20;
-                        atomicAdd(&s_hist[bin >> 1], (bin & 1u) ? 0x10000u : 1u);
+                for (int q = 0; q < QB; ++q) {
+                    if (q >= nqu) break;
+                    // exactly the NP columns of query q the MMA wrote (columns past them hold
+                    // stale values)
+                    uint32_t r[NP];
+                    const uint32_t ta = tmem_base + lane_addr + static_cast<uint32_t>(my_acc * kAccColsQ + q * NP);
+                    if constexpr (NP == 64) {
+                        DSV4_TMEM_LD_32x32b_X64(ta, r);
+                    } else if constexpr (NP == 32) {
+                        DSV4_TMEM_LD_32x32b_X32(ta, r);
+                    } else if constexpr (NP == 48) {
+                        DSV4_TMEM_LD_32x32b_X32(ta, r);
+                        uint32_t* r2 = r + 32;
+                        DSV4_TMEM_LD_32x32b_X16(ta + 32u, r2);
+                    } else {
+                        DSV4_TMEM_LD_32x32b_X16(ta, r);
+                    }
+                    tmem_wait_ld();
+                    if (q == nqu - 1) {                      // the accumulator is read out
+                        tc_fence_before();
+                        mbar_arrive(&tempty_bar[my_acc]);
+                    }
+                    float s = 0.f;
+                    if constexpr (FP8) {
+                        // four partial sums (heads h mod 4) in two packed pairs: half the FMA
+                        // instructions and a quarter of the dependent-FMA latency per key (here
+                        // the epilogue, not HBM, sets the pace)
+                        uint64_t a01 = 0, a23 = 0;
+#pragma unroll
+                        for (int h4 = 0; h4 < NP / 4; ++h4) {
+                            fma_f32x2(a01, pack_f32x2(fmaxf(__uint_as_float(r[4 * h4 + 0]), 0.f),
+                                                      fmaxf(__uint_as_float(r[4 * h4 + 1]), 0.f)),
+                                      pack_f32x2(wv[q][4 * h4 + 0], wv[q][4 * h4 + 1]));
+                            fma_f32x2(a23, pack_f32x2(fmaxf(__uint_as_float(r[4 * h4 + 2]), 0.f),
+                                                      fmaxf(__uint_as_float(r[4 * h4 + 3]), 0.f)),
+                                      pack_f32x2(wv[q][4 * h4 + 2], wv[q][4 * h4 + 3]));
+                        }
+                        float s0, s1, s2, s3;
+                        unpack_f32x2(a01, s0, s1);
+                        unpack_f32x2(a23, s2, s3);
+                        s = ((s0 + s1) + (s2 + s3)) * ks_cur[j];
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < NP; ++h) s = fmaf(wv[q][h], fmaxf(__uint_as_float(r[h]), 0.f), s);
+                    }
+                    if (key < nvq[q]) {
+                        float* dst = p.scores + static_cast<size_t>(unit_row(row, q)) * p.max_comp + key;
+                        if (p.reuse_keys) __stcs(dst, s);
+                        else *dst = s;
+                        if (QB == 1 && p.hist) {
+                            const uint32_t bin = float_to_key(s) >> 20;
+                            atomicAdd(&s_hist[bin >> 1], (bin & 1u) ? 0x10000u : 1u);
+                        }
                     }
                 }
             }
@@ -568,7 +602,7 @@ size_t index_zero_bytes(const dsv4_index_args& a) {
 }
 
 namespace {
-template <bool FP8, int NP, int EG>
+template <bool FP8, int NP, int EG, int QB>
 int launch_scores_fmt(const dsv4_index_args& a, float* scores, uint32_t* hist, uint32_t* eword,
                       cudaStream_t stream, const dsv4_compress_args* fresh) {
     using F = KeyFmt<FP8>;
@@ -617,18 +651,21 @@ int launch_scores_fmt(const dsv4_index_args& a, float* scores, uint32_t* hist, u
     p.max_comp = a.max_comp;
     p.ratio = a.ratio;
     p.stages_per_row = (a.max_comp + F::kStageKeys - 1) / F::kStageKeys;
-    const long long total = static_cast<long long>(rows) * p.stages_per_row;
+    p.gpb = (a.n_q + QB - 1) / QB;
+    p.units = a.batch * p.gpb;
+    const long long total = static_cast<long long>(p.units) * p.stages_per_row;
     if (total > 0) {
         static bool attr_set = false;
         if (!attr_set) {
-            cudaFuncSetAttribute(index_score_kernel<FP8, NP, EG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kSmemBytes));
+            cudaFuncSetAttribute(index_score_kernel<FP8, NP, EG, QB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSmemBytes + (QB - 1) * kQBufBytes));
             attr_set = true;
         }
         long long grid = sm_count();
         if (grid > total) grid = total;
         count_launch();
-        if (launch_k(index_score_kernel<FP8, NP, EG>, dim3(static_cast<unsigned>(grid)), dim3(64 + 128 * EG), kSmemBytes,
+        if (launch_k(index_score_kernel<FP8, NP, EG, QB>, dim3(static_cast<unsigned>(grid)), dim3(64 + 128 * EG),
+                     kSmemBytes + (QB - 1) * kQBufBytes,
                      stream, true, kmap, qmap, p) != cudaSuccess)
             return DSV4_ERR_LAUNCH;
     }
@@ -641,10 +678,14 @@ int launch_scores(const dsv4_index_args& a, float* scores, uint32_t* hist, uint3
     // Two epilogue groups where the epilogue, not HBM, sets the pace: FP8 keys (512 keys per
     // stage). One group for bf16 keys, whose registers then leave room for a compressor CTA
     // beside the scoring CTA (a second group did not speed up the many-row prefill either).
+    // Two queries per MMA with many rows of bf16 keys and no histogram to build (prefill):
+    // the key stages, not the epilogue, set its pace.
+    const bool pairs = static_cast<long long>(a.batch) * a.n_q > sm_count() && a.n_q >= 2 && !hist;
 #define DSV4_SCORES_NP(np)                                                               \
     if (n_pad == np)                                                                     \
-        return a.key_fp8 ? launch_scores_fmt<true, np, 2>(a, scores, hist, eword, stream, fresh) \
-                         : launch_scores_fmt<false, np, 1>(a, scores, hist, eword, stream, fresh);
+        return a.key_fp8 ? launch_scores_fmt<true, np, 2, 1>(a, scores, hist, eword, stream, fresh) \
+               : pairs   ? launch_scores_fmt<false, np, 1, 2>(a, scores, hist, eword, stream, fresh) \
+                         : launch_scores_fmt<false, np, 1, 1>(a, scores, hist, eword, stream, fresh);
     DSV4_SCORES_NP(16)
     DSV4_SCORES_NP(32)
     DSV4_SCORES_NP(48)
