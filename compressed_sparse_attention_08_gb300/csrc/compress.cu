@@ -40,7 +40,9 @@ namespace {
 // compressor CTA fits beside a scoring CTA, which the fused step starts while it runs
 constexpr int kThreads = 256;
 constexpr int kMaxChan = 4;          // channels per thread: dim <= 1024
-constexpr int kChunk = 4;            // tokens per load round (every channel's loads in flight together)
+// tokens per load round (every channel's loads in flight together): 4 for short blocks under
+// the register bound above, 8 for long blocks (ratio >= 16, where nothing runs beside)
+constexpr int kChunkShort = 4, kChunkLong = 8, kLongRatio = 16;
 constexpr int kMaxPairs = 64;        // rope_dim <= 128
 
 struct CompressJob {
@@ -85,6 +87,7 @@ struct EntryIn {
 // pooled tokens and the weighted sum of C in fp32, RMSNorm over the dim channels, RoPE of the
 // last rope_dim channels with the angle formed in fp64 and Cody-Waite reduced, one bf16
 // rounding. freq: the rope frequencies in shared memory (already visible to the CTA).
+template <int kChunk>
 __device__ void entry_math(const EntryIn& in, const double* freq, float* y, float* warp_sum) {
     const int tid = threadIdx.x;
     const int dim = in.dim, ratio = in.ratio;
@@ -203,7 +206,8 @@ __device__ void entry_math(const EntryIn& in, const double* freq, float* y, floa
 // zero_p/zero_n16: a workspace region (16-byte words) this launch clears for the kernels after
 // it (the fused decode step), so the step needs no separate memset; they read it only after
 // waiting for this grid.
-__global__ void __launch_bounds__(kThreads, 2)
+template <int kChunk, int kMinBlocks>
+__global__ void __launch_bounds__(kThreads, kMinBlocks)
 compress_kernel(const __grid_constant__ CompressJob j0, const __grid_constant__ CompressJob j1,
                 uint4* zero_p, unsigned zero_n16) {
     pdl_trigger();
@@ -285,7 +289,7 @@ compress_kernel(const __grid_constant__ CompressJob j0, const __grid_constant__ 
     in.dst = in_range && !out_fp8 ? outp + orow * dim : nullptr;
     in.dst8 = in_range && out_fp8 ? reinterpret_cast<uint8_t*>(outp) + orow * dim : nullptr;
     in.dst_scale = in_range && out_fp8 ? out_scalep + orow : nullptr;
-    entry_math(in, freq, y, warp_sum);
+    entry_math<kChunk>(in, freq, y, warp_sum);
 }
 
 CompressJob make_job(const dsv4_compress_args& a) {
@@ -381,7 +385,7 @@ compress_step_kernel(const __grid_constant__ StepJob j) {
     in.dst = nc >= 0 && nc < j.out_rows ? j.out + (static_cast<size_t>(s) * j.out_rows + nc) * j.dim : nullptr;
     in.dst8 = nullptr;
     in.dst_scale = nullptr;
-    entry_math(in, freq, y, warp_sum);
+    entry_math<kChunkShort>(in, freq, y, warp_sum);
     if (j.overlap)                                 // this block is stream a of the next entry
         for (size_t c = tid; c < blk; c += kThreads) prev[c] = cur[c];
     if (tid == 0) {
@@ -408,7 +412,12 @@ int launch_compress2(const dsv4_compress_args* a, const dsv4_compress_args* b, c
     if (nb == 0 || bs == 0) return memset_only();
     dim3 grid(nb, bs, b ? 2 : 1);
     count_launch();
-    return launch_k(compress_kernel, grid, dim3(kThreads), 0, stream, false, j0, j1,
+    const int rmax = j0.ratio > j1.ratio ? j0.ratio : j1.ratio;
+    if (rmax >= kLongRatio)
+        return launch_k(compress_kernel<kChunkLong, 1>, grid, dim3(kThreads), 0, stream, false, j0, j1,
+                        static_cast<uint4*>(zero), n16) == cudaSuccess
+                   ? DSV4_OK : DSV4_ERR_LAUNCH;
+    return launch_k(compress_kernel<kChunkShort, 2>, grid, dim3(kThreads), 0, stream, false, j0, j1,
                     static_cast<uint4*>(zero), n16) == cudaSuccess
                ? DSV4_OK : DSV4_ERR_LAUNCH;
 }
