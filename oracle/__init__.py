@@ -64,6 +64,10 @@ def _bind(lib):
                                        I, D, P, P, P]
     lib.oracle_quantize_rows_e4m3.argtypes = [P, I, I, P, P]
     lib.oracle_quantize_rows_e4m3.restype = ctypes.c_int
+    lib.oracle_quantize_kv_mixed.argtypes = [P, I, I, I, P, P, P]
+    lib.oracle_quantize_kv_mixed.restype = ctypes.c_int
+    lib.oracle_dequant_kv_mixed.argtypes = [P, P, P, I, I, I, P]
+    lib.oracle_dequant_kv_mixed.restype = ctypes.c_int
     lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
     lib.oracle_e4m3_to_double.restype = D
     lib.oracle_e4m3_from_double.argtypes = [D]
@@ -208,6 +212,39 @@ def e4m3_decode(c):
     lib = _load()
     c = np.asarray(c, np.uint8)
     return np.array([lib.oracle_e4m3_to_double(int(v)) for v in c.ravel()], np.float64).reshape(c.shape)
+
+
+def quantize_kv_mixed(x, rope_dim=64):
+    """Mixed compressed-KV storage of fp32 rows x [..., dim]: (nope codes uint8 [..., dim -
+    rope_dim], scale fp32 [...], rope bf16 bits uint16 [..., rope_dim])."""
+    lib = _load()
+    x = np.ascontiguousarray(x, np.float32)
+    shape = x.shape
+    rows = int(np.prod(shape[:-1]))
+    dim = shape[-1]
+    nope = np.zeros(shape[:-1] + (dim - rope_dim,), np.uint8)
+    sc = np.zeros(shape[:-1], np.float32)
+    rope = np.zeros(shape[:-1] + (rope_dim,), np.uint16)
+    rc = lib.oracle_quantize_kv_mixed(_p(x), rows, dim, rope_dim, _p(nope), _p(sc), _p(rope))
+    if rc != 0:
+        raise ValueError("oracle_quantize_kv_mixed: bad arguments")
+    return nope, sc, rope
+
+
+def dequant_kv_mixed(nope, scale, rope):
+    """bf16 bits [..., dim] of the rows the attention multiplies (see quantize_kv_mixed)."""
+    lib = _load()
+    nope = np.ascontiguousarray(nope, np.uint8)
+    scale = np.ascontiguousarray(scale, np.float32)
+    rope = np.ascontiguousarray(rope, np.uint16)
+    rope_dim = rope.shape[-1]
+    dim = nope.shape[-1] + rope_dim
+    rows = int(np.prod(nope.shape[:-1]))
+    out = np.zeros(nope.shape[:-1] + (dim,), np.uint16)
+    rc = lib.oracle_dequant_kv_mixed(_p(nope), _p(scale), _p(rope), rows, dim, rope_dim, _p(out))
+    if rc != 0:
+        raise ValueError("oracle_dequant_kv_mixed: bad arguments")
+    return out
 
 
 def quantize_rows_e4m3(x):

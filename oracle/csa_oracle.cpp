@@ -512,6 +512,54 @@ int oracle_quantize_rows_e4m3(const float* x, int rows, int dim, uint8_t* q, flo
     return 0;
 }
 
+// ---------------------------------------------------------------------------
+// Mixed FP8 / bf16 compressed KV cache.
+//
+// [B] single_shot_inference.py eager_attention, "Compressor -> compressed KV (mixed storage:
+// FP8 + BF16 RoPE)": the first dim - rope_dim channels of a compressed entry (the part
+// without RoPE) are kept as FP8 E4M3 with one scale per entry, the last rope_dim channels as
+// bf16, and the attention reads both parts back. The pages fix no scale rule; the readings
+// taken: codes and scale of the part without RoPE as in oracle_quantize_rows_e4m3 (amax of
+// that part only / 448, fp32); the RoPE part is the bf16 RNE of the fp32 entry; a gathered
+// entry is dequantized to bf16 before the attention products, each channel
+// bf16( fp32( e4m3(code) * scale ) ), the RoPE channels as stored.
+//
+// x [rows, dim] fp32 -> nope [rows, dim - rope_dim] codes, scale [rows] fp32,
+// rope [rows, rope_dim] bf16 bits.
+int oracle_quantize_kv_mixed(const float* x, int rows, int dim, int rope_dim, uint8_t* nope,
+                             float* scale, uint16_t* rope) {
+    if (rows < 0 || dim <= 0 || rope_dim < 0 || rope_dim >= dim) return -1;
+    const int nd = dim - rope_dim;
+    for (int r = 0; r < rows; ++r) {
+        const float* xr = x + static_cast<size_t>(r) * dim;
+        float amax = 0.f;
+        for (int i = 0; i < nd; ++i) amax = std::max(amax, std::fabs(xr[i]));
+        const float sc = amax > 0.f ? amax / 448.f : 1.f;   // as oracle_quantize_rows_e4m3
+        scale[r] = sc;
+        for (int i = 0; i < nd; ++i)
+            nope[static_cast<size_t>(r) * nd + i] = e4m3_from_double(static_cast<double>(xr[i] / sc));
+        for (int i = 0; i < rope_dim; ++i)
+            rope[static_cast<size_t>(r) * rope_dim + i] = double_to_bf16(static_cast<double>(xr[nd + i]));
+    }
+    return 0;
+}
+
+// The bf16 rows the attention multiplies: [rows, dim] bf16 bits from the mixed storage.
+int oracle_dequant_kv_mixed(const uint8_t* nope, const float* scale, const uint16_t* rope,
+                            int rows, int dim, int rope_dim, uint16_t* out) {
+    if (rows < 0 || dim <= 0 || rope_dim < 0 || rope_dim >= dim) return -1;
+    const int nd = dim - rope_dim;
+    for (int r = 0; r < rows; ++r) {
+        uint16_t* o = out + static_cast<size_t>(r) * dim;
+        for (int i = 0; i < nd; ++i) {
+            const float v = static_cast<float>(e4m3_to_double(nope[static_cast<size_t>(r) * nd + i])) * scale[r];
+            o[i] = double_to_bf16(static_cast<double>(v));      // fp32 product, then bf16
+        }
+        for (int i = 0; i < rope_dim; ++i) o[nd + i] = rope[static_cast<size_t>(r) * rope_dim + i];
+    }
+    return 0;
+}
+
 double oracle_e4m3_to_double(uint8_t c) { return e4m3_to_double(c); }
 uint8_t oracle_e4m3_from_double(double x) { return e4m3_from_double(x); }
 

@@ -732,4 +732,48 @@ def pin_fp8_scores_scale_with_the_rows():
     _close(got2, base + 7.0 * float(w[0, 0, 2]) * one, 1e-11, 1e-11, "query scale")
 
 
+# ------------------------------------------------------------------ mixed FP8 / bf16 KV cache
+def pin_kv_mixed_exact_rows_round_trip():
+    """An entry whose part without RoPE holds E4M3 values with largest magnitude 448 (scale 1)
+    and whose RoPE part holds bf16 values comes back bit for bit; the RoPE part is not folded
+    into the scale even when it is the larger part."""
+    rng = _rng(71)
+    rows, dim, rd = 6, 512, 64
+    codes = rng.integers(0, 0x7E, size=(rows, dim - rd)).astype(np.uint8) | \
+        (rng.integers(0, 2, size=(rows, dim - rd)) << 7).astype(np.uint8)
+    codes[:, 3] = 0x7E
+    nope_v = oracle.e4m3_decode(codes).astype(np.float32)
+    rope_bits = _bf(rng.standard_normal((rows, rd)) * 1000.0)      # larger than 448
+    x = np.concatenate([nope_v, synth.bf16_bits_to_f32(rope_bits)], axis=1)
+    nope, sc, rope = oracle.quantize_kv_mixed(x, rd)
+    assert np.array_equal(nope, codes) and np.all(sc == 1.0) and np.array_equal(rope, rope_bits)
+    back = oracle.dequant_kv_mixed(nope, sc, rope)
+    assert np.array_equal(synth.bf16_bits_to_f32(back), x), "round trip"
+
+
+def pin_kv_mixed_scale_and_bound():
+    """Scaling the part without RoPE by 2^k scales the entry's scale by 2^k and keeps its codes;
+    the dequantized channels are within half an E4M3 step (plus the bf16 rounding) of the
+    fp32 entry; an entry whose part without RoPE is zero has scale 1 and zero codes."""
+    rng = _rng(72)
+    rows, dim, rd = 5, 512, 64
+    x = (rng.standard_normal((rows, dim)) * rng.uniform(0.01, 50, (rows, 1))).astype(np.float32)
+    x[2, : dim - rd] = 0.0
+    nope, sc, rope = oracle.quantize_kv_mixed(x, rd)
+    assert sc[2] == 1.0 and not np.any(nope[2])
+    x2 = x.copy()
+    x2[:, : dim - rd] *= 8.0
+    nope2, sc2, rope2 = oracle.quantize_kv_mixed(x2, rd)
+    assert np.array_equal(nope2, nope) and np.array_equal(rope2, rope)
+    assert np.array_equal(sc2[[0, 1, 3, 4]], 8.0 * sc[[0, 1, 3, 4]])
+    back = synth.bf16_bits_to_f32(oracle.dequant_kv_mixed(nope, sc, rope)).astype(np.float64)
+    xn = x[:, : dim - rd].astype(np.float64)
+    # E4M3 spacing at |x| / scale: 2^(e - 3) for |x| / scale in [2^e, 2^(e+1)), e >= -6
+    e = np.maximum(np.floor(np.log2(np.maximum(np.abs(xn) / sc[:, None], 2.0 ** -6))), -6)
+    step = np.exp2(e - 3)
+    bound = 0.5 * step * sc[:, None] + 2.0 ** -8 * np.abs(xn) + 1e-30
+    assert np.all(np.abs(back[:, : dim - rd] - xn) <= bound * (1 + 1e-6)), "dequant bound"
+    assert np.array_equal(back[:, dim - rd:], synth.bf16_bits_to_f32(_bf(x[:, dim - rd:])).astype(np.float64))
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -43,12 +43,20 @@ MUTANTS = [
     ("e4m3_no_saturation", "if (e > 8 || (e == 8 && q > 14.0))", "if (e > 8)", 1),
     ("e4m3_subnormal_spacing", "if (e < -6) e = -6;", "if (e < -7) e = -7;", 1),
     ("quant_scale_max_code", "amax / 448.0f", "amax / 240.0f", 1),
+    ("kv_mixed_scale_max_code", "amax / 448.f", "amax / 240.f", 1),
     ("fp8_score_key_scale_dropped", "static_cast<double>(k_scale[kr]) * e4m3_to_double(keys[kr * Di + i])",
      "e4m3_to_double(keys[kr * Di + i])", 1),
     ("fp8_score_no_relu", "(dot > 0.0 ? dot : 0.0);   // ReLU", "dot;   // ReLU", 1),
     ("fp8_score_query_scale_dropped",
      "static_cast<double>(q_scale[row * H + h]) * e4m3_to_double(q[(row * H + h) * Di + i]);",
      "e4m3_to_double(q[(row * H + h) * Di + i]);", 1),
+    ("kv_mixed_amax_includes_rope", "for (int i = 0; i < nd; ++i) amax = std::max(amax, std::fabs(xr[i]));",
+     "for (int i = 0; i < dim; ++i) amax = std::max(amax, std::fabs(xr[i]));", 1),
+    ("kv_mixed_dequant_scale_dropped",
+     "static_cast<float>(e4m3_to_double(nope[static_cast<size_t>(r) * nd + i])) * scale[r];",
+     "static_cast<float>(e4m3_to_double(nope[static_cast<size_t>(r) * nd + i]));", 1),
+    ("kv_mixed_rope_from_first_dims", "double_to_bf16(static_cast<double>(xr[nd + i]))",
+     "double_to_bf16(static_cast<double>(xr[i]))", 1),
     ("inverse_rope_forward_direction", "v[e0] = ev * cs + ov * sn;", "v[e0] = ev * cs - ov * sn;", 1),
     ("inverse_rope_odd_sign", "v[e0 + 1] = -ev * sn + ov * cs;", "v[e0 + 1] = ev * sn + ov * cs;", 1),
     ("inverse_rope_frequency", "std::pow(theta, -(2.0 * j) / rope_dim)", "std::pow(theta, -(1.0 * j) / rope_dim)", 1),
