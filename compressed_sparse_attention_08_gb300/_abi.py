@@ -39,7 +39,7 @@ class CompressArgs(ctypes.Structure):
                 ("out_row0", P), ("batch", I), ("tokens", I), ("dim", I), ("ratio", I),
                 ("rope_dim", I), ("out_rows", I), ("eps", ctypes.c_float),
                 ("rope_theta", ctypes.c_double), ("overlap", I), ("prev_C", P), ("prev_Z", P),
-                ("out_fp8", I), ("out_scale", P)]
+                ("out_fp8", I), ("out_scale", P), ("out_rope", P)]
 
 
 class StepArgs(ctypes.Structure):
@@ -66,7 +66,8 @@ class AttnArgs(ctypes.Structure):
                 ("win", P), ("win_len", P), ("gather", P), ("out", P), ("batch", I), ("n_q", I),
                 ("heads", I), ("dim", I), ("max_comp", I), ("top_k", I), ("window", I),
                 ("win_rows", I), ("ratio", I), ("scale", ctypes.c_float), ("out_rope_pos", P),
-                ("out_rope_dim", I), ("out_rope_theta", ctypes.c_double)]
+                ("out_rope_dim", I), ("out_rope_theta", ctypes.c_double), ("kv_fp8", I),
+                ("kv_nope", P), ("kv_scale", P), ("kv_rope", P), ("kv_rope_dim", I)]
 
 
 class CsaArgs(ctypes.Structure):
@@ -168,22 +169,26 @@ def _dt():
 # ------------------------------------------------------------------ argument builders
 def compress_args(C, Z, bias, gamma, pos0, out, *, ratio, rope_dim=64, eps=1e-6,
                   rope_theta=10000.0, out_row0=None, overlap=False, prev_C=None, prev_Z=None,
-                  out_scale=None):
+                  out_scale=None, out_rope=None):
     """overlap=True: the two-stream (CSA) form, C and Z [B, T, 2*dim], bias [ratio, 2*dim],
     optional prev_C / prev_Z [B, ratio, 2*dim] (the block before C's first block).
-    out_scale given: FP8 entries, out uint8 [B, rows, dim] and out_scale fp32 [B, rows]."""
+    out_scale given: FP8 entries, out uint8 [B, rows, dim] and out_scale fp32 [B, rows].
+    out_scale and out_rope given: the mixed KV storage, out uint8 [B, rows, dim - rope_dim]
+    codes, out_scale fp32 [B, rows], out_rope bf16 [B, rows, rope_dim]."""
     import torch
     bf16, f32, i32, i64 = _dt()
     B, T, w = C.shape
     d = w // 2 if overlap else w
     fp8 = out_scale is not None
+    mode = 2 if (fp8 and out_rope is not None) else (1 if fp8 else 0)
     return CompressArgs(_ptr(C, bf16, "C"), _ptr(Z, bf16, "Z"), _ptr(bias, f32, "bias"),
                         _ptr(gamma, f32, "gamma"), _ptr(pos0, i64, "pos0"),
                         _ptr(out, torch.uint8 if fp8 else bf16, "out"),
                         _ptr(out_row0, i32, "out_row0", True), B, T, d, ratio, rope_dim,
                         out.shape[1], eps, rope_theta, 1 if overlap else 0,
                         _ptr(prev_C, bf16, "prev_C", True), _ptr(prev_Z, bf16, "prev_Z", True),
-                        1 if fp8 else 0, _ptr(out_scale, f32, "out_scale", True))
+                        mode, _ptr(out_scale, f32, "out_scale", True),
+                        _ptr(out_rope, bf16, "out_rope", True))
 
 
 def index_args(q, w, keys, n_comp, idx_out, *, ratio, q_pos=None, scores_out=None, q_scale=None,
@@ -211,32 +216,39 @@ def topk_args(scores, n_vis, idx_out):
 
 def attn_args(q, sink, comp_kv, n_comp, win, win_len, out, *, idx=None, top_k=None, window=128,
               ratio=4, q_pos=None, gather=None, scale=None, out_rope_pos=None, out_rope_dim=64,
-              out_rope_theta=10000.0):
+              out_rope_theta=10000.0, kv_nope=None, kv_scale=None, kv_rope=None):
     """out_rope_pos (int64 [B, n_q]): rotate the output's last out_rope_dim channels back at
-    these positions (inverse RoPE)."""
+    these positions (inverse RoPE). comp_kv None and kv_nope / kv_scale / kv_rope given: the
+    mixed FP8 / bf16 compressed KV (codes uint8 [B, max_comp, D - rd], scales fp32
+    [B, max_comp], RoPE part bf16 [B, max_comp, rd])."""
+    import torch
     bf16, f32, i32, i64 = _dt()
     B, n_q, H, D = q.shape
-    max_comp = comp_kv.shape[1]
+    kv_fp8 = comp_kv is None
+    max_comp = kv_nope.shape[1] if kv_fp8 else comp_kv.shape[1]
     if top_k is None:
         top_k = idx.shape[-1] if idx is not None else max_comp
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    return AttnArgs(_ptr(q, bf16, "q"), _ptr(sink, f32, "sink"), _ptr(comp_kv, bf16, "comp_kv"),
+    return AttnArgs(_ptr(q, bf16, "q"), _ptr(sink, f32, "sink"), _ptr(comp_kv, bf16, "comp_kv", kv_fp8),
                     _ptr(n_comp, i32, "n_comp"), _ptr(idx, i32, "idx", True),
                     _ptr(q_pos, i64, "q_pos", True), _ptr(win, bf16, "win"),
                     _ptr(win_len, i32, "win_len"), _ptr(gather, bf16, "gather", True),
                     _ptr(out, bf16, "out"), B, n_q, H, D, max_comp, top_k, window, win.shape[1],
                     ratio, scale, _ptr(out_rope_pos, i64, "out_rope_pos", True),
-                    out_rope_dim if out_rope_pos is not None else 0, out_rope_theta)
+                    out_rope_dim if out_rope_pos is not None else 0, out_rope_theta,
+                    1 if kv_fp8 else 0, _ptr(kv_nope, torch.uint8, "kv_nope", True),
+                    _ptr(kv_scale, f32, "kv_scale", True), _ptr(kv_rope, bf16, "kv_rope", True),
+                    kv_rope.shape[-1] if kv_fp8 else 0)
 
 
 # ------------------------------------------------------------------ entry points
 def dsv4_compress(C, Z, bias, gamma, pos0, out, *, ratio, rope_dim=64, eps=1e-6,
                   rope_theta=10000.0, out_row0=None, overlap=False, prev_C=None, prev_Z=None,
-                  out_scale=None, stream=None):
+                  out_scale=None, out_rope=None, stream=None):
     a = compress_args(C, Z, bias, gamma, pos0, out, ratio=ratio, rope_dim=rope_dim, eps=eps,
                       rope_theta=rope_theta, out_row0=out_row0, overlap=overlap, prev_C=prev_C,
-                      prev_Z=prev_Z, out_scale=out_scale)
+                      prev_Z=prev_Z, out_scale=out_scale, out_rope=out_rope)
     _check(library().dsv4_compress(ctypes.byref(a), _stream(stream)), "dsv4_compress")
 
 

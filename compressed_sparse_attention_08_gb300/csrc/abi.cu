@@ -47,8 +47,13 @@ bool compress_ok(const dsv4_compress_args* a) {
     if (a->overlap != 0 && a->overlap != 1) return false;
     if ((a->prev_C == nullptr) != (a->prev_Z == nullptr)) return false;
     if (a->prev_C && (!a->overlap || !dev_ptr_ok(a->prev_C) || !dev_ptr_ok(a->prev_Z))) return false;
-    if (a->out_fp8 != 0 && a->out_fp8 != 1) return false;
+    if (a->out_fp8 < 0 || a->out_fp8 > 2) return false;
     if (a->out_fp8 ? !dev_ptr_ok(a->out_scale) : a->out_scale != nullptr) return false;
+    // mixed storage: the RoPE part in out_rope (none when rope_dim is 0)
+    if (a->out_fp8 == 2 ? (a->rope_dim > 0 ? !dev_ptr_ok(a->out_rope) : a->out_rope != nullptr)
+                        : a->out_rope != nullptr)
+        return false;
+    if (a->out_fp8 == 2 && a->rope_dim >= a->dim) return false;
     return true;
 }
 
@@ -78,7 +83,7 @@ bool topk_ok(const dsv4_topk_args* a) {
 
 bool attn_ok(const dsv4_attn_args* a) {
     if (!a) return false;
-    if (!dev_ptr_ok(a->q) || !dev_ptr_ok(a->sink) || !dev_ptr_ok(a->comp_kv) || !dev_ptr_ok(a->n_comp) ||
+    if (!dev_ptr_ok(a->q) || !dev_ptr_ok(a->sink) || !dev_ptr_ok(a->n_comp) ||
         !dev_ptr_ok(a->win) || !dev_ptr_ok(a->win_len) || !dev_ptr_ok(a->out) ||
         !opt_ptr_ok(a->idx) || !opt_ptr_ok(a->q_pos) || !opt_ptr_ok(a->gather))
         return false;
@@ -88,6 +93,18 @@ bool attn_ok(const dsv4_attn_args* a) {
     if (a->max_comp < 1 || a->top_k < 1 || a->window < 0 || a->win_rows < 1 || a->ratio < 1) return false;
     if (a->idx ? a->top_k > a->max_comp : a->top_k != a->max_comp) return false;
     if (!std::isfinite(a->scale)) return false;
+    // the compressed rows: bf16 in comp_kv, or the mixed FP8 / bf16 storage (decode only)
+    if (a->kv_fp8 == 0) {
+        if (!dev_ptr_ok(a->comp_kv) || a->kv_nope || a->kv_scale || a->kv_rope) return false;
+    } else if (a->kv_fp8 == 1) {
+        if (a->comp_kv || !dev_ptr_ok(a->kv_nope) || !dev_ptr_ok(a->kv_scale) || !dev_ptr_ok(a->kv_rope))
+            return false;
+        if (a->n_q != 1 || a->kv_rope_dim < 8 || a->kv_rope_dim % 8 || a->kv_rope_dim > a->dim - 8) return false;
+        // read by the fused decode kernel only: at most 256 chunks of 128 slots
+        if ((static_cast<long long>(a->top_k) + a->window + 127) / 128 > 256) return false;
+    } else {
+        return false;
+    }
     if (static_cast<long long>(a->batch) * a->n_q > 65535ll) return false;   // grid.y
     if (a->out_rope_pos) {
         if (!opt_ptr_ok(a->out_rope_pos) || a->out_rope_dim < 2 || (a->out_rope_dim & 1) ||
@@ -279,10 +296,20 @@ static bool csa_ok(const dsv4_csa_args* a) {
             return false;
         // a key cache written in this step is read in the format it was written in
         const dsv4_compress_args* k = a->compress_keys;
+        // (the KV cache written in this step is checked below)
         if (k && k->out == x.keys && (k->out_fp8 != x.key_fp8 || (k->out_fp8 && k->out_scale != x.key_scale)))
             return false;
     } else if (a->attn->idx) {
         return false;
+    }
+    // a KV cache written in this step is read in the layout it was written in
+    const dsv4_compress_args* kv = a->compress_kv;
+    const dsv4_attn_args& at = *a->attn;
+    if (kv && (kv->out == at.comp_kv || kv->out == at.kv_nope)) {
+        const bool mixed = kv->out_fp8 == 2;
+        if (mixed != (at.kv_fp8 == 1) || kv->out_fp8 == 1) return false;
+        if (mixed && (kv->out_scale != at.kv_scale || kv->out_rope != at.kv_rope || kv->rope_dim != at.kv_rope_dim))
+            return false;
     }
     return true;
 }

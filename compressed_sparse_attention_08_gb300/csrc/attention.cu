@@ -27,6 +27,8 @@
 //     M = max(sink, m_s). With one split the CTA finishes the output itself.
 #include <cmath>
 
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -53,6 +55,11 @@ struct AttnParams {
     const int64_t* orp;            // [rows] positions of the output's inverse RoPE, or null
     int or_pairs;                  // rotated pairs: the last 2 * or_pairs channels
     double or_log2_theta;          // log2(theta): pair j turns at theta^(-2j / rope_dim)
+    // mixed FP8 / bf16 compressed KV (decode kernel only), else null
+    const uint8_t* kv_nope;        // [B, max_comp, nope_dim] E4M3 codes
+    const float* kv_scale;         // [B, max_comp]
+    const __nv_bfloat16* kv_rope;  // [B, max_comp, D - nope_dim]
+    int nope_dim;
 };
 
 // Inverse RoPE of one output pair (channels c, c + 1, c even) of query row `row`: rotated back
@@ -659,7 +666,9 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
     // ---- gather: warp w copies slots [16w, 16w + 16) of the chunk; lanes 0..15 resolve them
     {
         const int r0 = warp * 16;
-        unsigned long long src = 0;                                  // 0: zero row
+        unsigned long long src = 0;                                  // bf16 row; 0: none
+        long long ent = -1;                                          // mixed storage: entry row
+        float escale = 0.f;
         if (lane < 16) {
             const int slot = chunk * kFC + r0 + lane;
             if (slot < p.top_k) {
@@ -670,22 +679,81 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                 } else {
                     e = slot < nv ? slot : -1;
                 }
-                if (e >= 0)
-                    src = reinterpret_cast<unsigned long long>(comp_kv + (static_cast<size_t>(b) * p.max_comp + e) * D);
+                if (e >= 0) {
+                    if (p.kv_nope) {
+                        ent = static_cast<long long>(b) * p.max_comp + e;
+                        escale = __ldg(&p.kv_scale[ent]);
+                    } else {
+                        src = reinterpret_cast<unsigned long long>(comp_kv + (static_cast<size_t>(b) * p.max_comp + e) * D);
+                    }
+                }
             } else if (slot < p.slots) {
                 const int wi = slot - p.top_k;
                 if (wi < w_cnt)
                     src = reinterpret_cast<unsigned long long>(win + (static_cast<size_t>(b) * p.win_rows + w_lo + wi) * D);
             }
-            okf[r0 + lane] = src != 0;
+            okf[r0 + lane] = src != 0 || ent >= 0;
         }
-        for (int i = lane; i < 16 * C::U; i += 32) {
-            const int r = i / C::U, c = i - r * C::U;
-            const unsigned long long a = __shfl_sync(0xffffffffu, src, r);
-            const int rr = r0 + r;
-            uint8_t* dst = sKV + (c >> 3) * C::BOX + rr * 128 + (((c & 7) ^ (rr & 7)) << 4);
-            if (a) cp_async16(dst, reinterpret_cast<const uint8_t*>(a) + c * 16);
-            else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+        if (!p.kv_nope) {
+            for (int i = lane; i < 16 * C::U; i += 32) {
+                const int r = i / C::U, c = i - r * C::U;
+                const unsigned long long a = __shfl_sync(0xffffffffu, src, r);
+                const int rr = r0 + r;
+                uint8_t* dst = sKV + (c >> 3) * C::BOX + rr * 128 + (((c & 7) ^ (rr & 7)) << 4);
+                if (a) cp_async16(dst, reinterpret_cast<const uint8_t*>(a) + c * 16);
+                else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+            }
+        } else {
+            // mixed storage: a 16-byte bf16 piece c of a compressed row is 8 codes (piece c <
+            // ncp) dequantized here, or a piece of its bf16 RoPE part; every load of the warp's
+            // 16 rows is issued (codes into registers) before the first is converted
+            constexpr int kPer = 16 * C::U / 32;                     // pieces per lane
+            const int ncp = p.nope_dim / 8;
+            const int rope_b = (D - p.nope_dim) * 2;                 // bytes of a RoPE part
+            uint2 code[kPer];
+#pragma unroll
+            for (int k = 0; k < kPer; ++k) {
+                const int i = lane + 32 * k;
+                const int r = i / C::U, c = i - r * C::U;
+                const unsigned long long a = __shfl_sync(0xffffffffu, src, r);
+                const long long en = __shfl_sync(0xffffffffu, ent, r);
+                const int rr = r0 + r;
+                uint8_t* dst = sKV + (c >> 3) * C::BOX + rr * 128 + (((c & 7) ^ (rr & 7)) << 4);
+                code[k] = make_uint2(0u, 0u);
+                if (a) {
+                    cp_async16(dst, reinterpret_cast<const uint8_t*>(a) + c * 16);
+                } else if (en >= 0) {
+                    if (c < ncp)
+                        code[k] = __ldg(reinterpret_cast<const uint2*>(p.kv_nope + static_cast<size_t>(en) * p.nope_dim) + c);
+                    else
+                        cp_async16(dst, reinterpret_cast<const uint8_t*>(p.kv_rope) + static_cast<size_t>(en) * rope_b +
+                                            (c - ncp) * 16);
+                } else {
+                    *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kPer; ++k) {
+                const int i = lane + 32 * k;
+                const int r = i / C::U, c = i - r * C::U;
+                const long long en = __shfl_sync(0xffffffffu, ent, r);
+                const float sc = __shfl_sync(0xffffffffu, escale, r);
+                if (en >= 0 && c < ncp) {                            // (a compressed row)
+                    // channel = bf16( fp32(E4M3 code) * scale ): codes in byte order
+                    uint32_t o[4];
+                    const uint32_t w2[2] = {code[k].x, code[k].y};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const __nv_fp8x2_storage_t pr =
+                            static_cast<__nv_fp8x2_storage_t>((w2[h >> 1] >> (16 * (h & 1))) & 0xFFFFu);
+                        const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3)));
+                        o[h] = pack_bf16(f.x * sc, f.y * sc);
+                    }
+                    const int rr = r0 + r;
+                    uint8_t* dst = sKV + (c >> 3) * C::BOX + rr * 128 + (((c & 7) ^ (rr & 7)) << 4);
+                    *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
+                }
+            }
         }
     }
     cp_async_wait_all();
@@ -872,6 +940,10 @@ int run_decode(const dsv4_attn_args& a, const DecodePlan& dp, uint8_t* ws, uint3
     p.hstride = static_cast<int>(hs);
     p.scale = a.scale;
     set_output_rope(p, a);
+    p.kv_nope = a.kv_fp8 ? static_cast<const uint8_t*>(a.kv_nope) : nullptr;
+    p.kv_scale = a.kv_fp8 ? a.kv_scale : nullptr;
+    p.kv_rope = a.kv_fp8 ? static_cast<const __nv_bfloat16*>(a.kv_rope) : nullptr;
+    p.nope_dim = a.kv_fp8 ? D - a.kv_rope_dim : D;
     p.part_ml = reinterpret_cast<float*>(ws);
     p.part_o = reinterpret_cast<float*>(ws + ml_b);
     static bool attr_set = false;

@@ -52,7 +52,8 @@ struct CompressJob {
     const __nv_bfloat16* prev_Z;
     int overlap;                     // 0: plain blocks; 1: two-stream (CSA) form, 2*dim channels
     float* out_scale;                // FP8 output: [batch, out_rows] entry scales, out holds E4M3
-    int out_fp8;
+    int out_fp8;                     // 0 bf16; 1 FP8 entries; 2 mixed (FP8 + bf16 RoPE part)
+    __nv_bfloat16* out_rope;         // mixed: [batch, out_rows, rope_dim]
     const float* bias;
     const float* gamma;
     const int64_t* pos0;
@@ -81,6 +82,9 @@ struct EntryIn {
     __nv_bfloat16* dst;          // the entry's output row, or null (computed, not stored)
     uint8_t* dst8;               // FP8 output: the entry's E4M3 row (dst is then null), or null
     float* dst_scale;            // FP8 output: the entry's scale
+    int q_dim;                   // FP8 output: channels [0, q_dim) quantized (dim, or
+                                 // dim - rope_dim for the mixed KV storage)
+    __nv_bfloat16* dst_rope;     // mixed KV storage: channels [q_dim, dim) as bf16, or null
 };
 
 // The whole CTA (kThreads) computes one entry: per-channel online softmax of Z + bias over the
@@ -186,9 +190,11 @@ __device__ void entry_math(const EntryIn& in, const double* freq, float* y, floa
     if (in.dst)
         for (int c = tid; c < dim; c += kThreads) in.dst[c] = __float2bfloat16_rn(y[c]);
     if (in.dst8) {
-        // FP8 E4M3 entry: scale = amax / 448 over the entry (fp32), code = E4M3(y / scale)
+        // FP8 E4M3 channels [0, q_dim): scale = amax / 448 over them (fp32), code =
+        // E4M3(y / scale); the mixed storage keeps channels [q_dim, dim) (the RoPE part) as bf16
+        const int qd = in.q_dim;
         float amax = 0.f;
-        for (int c = tid; c < dim; c += kThreads) amax = fmaxf(amax, fabsf(y[c]));
+        for (int c = tid; c < qd; c += kThreads) amax = fmaxf(amax, fabsf(y[c]));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         if ((tid & 31) == 0) warp_sum[tid >> 5] = amax;
@@ -198,8 +204,10 @@ __device__ void entry_math(const EntryIn& in, const double* freq, float* y, floa
         for (int k = 0; k < kThreads / 32; ++k) m = fmaxf(m, warp_sum[k]);
         const float sc = m > 0.f ? m / 448.0f : 1.0f;
         if (tid == 0) *in.dst_scale = sc;
-        for (int c = tid; c < dim; c += kThreads)
+        for (int c = tid; c < qd; c += kThreads)
             in.dst8[c] = static_cast<uint8_t>(__nv_cvt_float_to_fp8(y[c] / sc, __NV_SATFINITE, __NV_E4M3));
+        if (in.dst_rope)
+            for (int c = qd + tid; c < dim; c += kThreads) in.dst_rope[c - qd] = __float2bfloat16_rn(y[c]);
     }
 }
 
@@ -226,6 +234,7 @@ compress_kernel(const __grid_constant__ CompressJob j0, const __grid_constant__ 
     const int overlap = second ? j1.overlap : j0.overlap;
     const int out_fp8 = second ? j1.out_fp8 : j0.out_fp8;
     float* out_scalep = second ? j1.out_scale : j0.out_scale;
+    __nv_bfloat16* out_ropep = second ? j1.out_rope : j0.out_rope;
     const float* __restrict__ biasp = second ? j1.bias : j0.bias;
     const float* __restrict__ gammap = second ? j1.gamma : j0.gamma;
     const int64_t* pos0p = second ? j1.pos0 : j0.pos0;
@@ -286,9 +295,13 @@ compress_kernel(const __grid_constant__ CompressJob j0, const __grid_constant__ 
     // rows outside the destination are not written
     const bool in_range = row >= 0 && row < out_rows;
     const size_t orow = static_cast<size_t>(s) * out_rows + row;
+    // mixed storage: codes of the channels without RoPE, rows of dim - rope_dim bytes
+    const int q_dim = out_fp8 == 2 ? dim - (second ? j1.rope_dim : j0.rope_dim) : dim;
     in.dst = in_range && !out_fp8 ? outp + orow * dim : nullptr;
-    in.dst8 = in_range && out_fp8 ? reinterpret_cast<uint8_t*>(outp) + orow * dim : nullptr;
+    in.dst8 = in_range && out_fp8 ? reinterpret_cast<uint8_t*>(outp) + orow * q_dim : nullptr;
     in.dst_scale = in_range && out_fp8 ? out_scalep + orow : nullptr;
+    in.q_dim = q_dim;
+    in.dst_rope = in_range && out_fp8 == 2 ? out_ropep + orow * (dim - q_dim) : nullptr;
     entry_math<kChunk>(in, freq, y, warp_sum);
 }
 
@@ -301,6 +314,7 @@ CompressJob make_job(const dsv4_compress_args& a) {
     j.overlap = a.overlap;
     j.out_fp8 = a.out_fp8;
     j.out_scale = a.out_scale;
+    j.out_rope = static_cast<__nv_bfloat16*>(a.out_rope);
     j.bias = a.bias;
     j.gamma = a.gamma;
     j.pos0 = a.pos0;
@@ -385,6 +399,8 @@ compress_step_kernel(const __grid_constant__ StepJob j) {
     in.dst = nc >= 0 && nc < j.out_rows ? j.out + (static_cast<size_t>(s) * j.out_rows + nc) * j.dim : nullptr;
     in.dst8 = nullptr;
     in.dst_scale = nullptr;
+    in.q_dim = j.dim;
+    in.dst_rope = nullptr;
     entry_math<kChunkShort>(in, freq, y, warp_sum);
     if (j.overlap)                                 // this block is stream a of the next entry
         for (size_t c = tid; c < blk; c += kThreads) prev[c] = cur[c];

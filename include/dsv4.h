@@ -105,6 +105,14 @@ typedef struct dsv4_compress_args {
      * dsv4_quantize_rows_fp8 quantizes a row. out_fp8 = 0: bf16 entries, out_scale NULL. */
     int out_fp8;
     float* out_scale;
+    /* Mixed FP8 / bf16 KV cache ([B] single_shot_inference.py eager_attention, "compressed KV
+     * (mixed storage: FP8 + BF16 RoPE)"): out_fp8 = 2 stores the entry's first
+     * dim - rope_dim channels as FP8 E4M3 codes in out (bytes [batch, out_rows,
+     * dim - rope_dim]) with one fp32 scale per entry in out_scale (amax of those channels /
+     * 448, as dsv4_quantize_rows_fp8), and its last rope_dim channels as bf16 in out_rope
+     * ([batch, out_rows, rope_dim]); dsv4_attn_args.kv_fp8 reads that storage. out_rope is
+     * NULL unless out_fp8 = 2. */
+    void* out_rope;
 } dsv4_compress_args;
 
 int dsv4_compress(const dsv4_compress_args* args, dsv4_stream_t stream);
@@ -257,6 +265,18 @@ typedef struct dsv4_attn_args {
     const int64_t* out_rope_pos;
     int out_rope_dim;         /* even, 2..min(dim, 128) when out_rope_pos is given          */
     double out_rope_theta;    /* 10000 on the pages                                         */
+    /* Mixed FP8 / bf16 compressed KV (dsv4_compress_args.out_fp8 = 2): with kv_fp8 = 1,
+     * comp_kv is NULL and the compressed rows come from kv_nope (E4M3 codes [batch, max_comp,
+     * dim - kv_rope_dim]), kv_scale (fp32 [batch, max_comp]) and kv_rope (bf16 [batch,
+     * max_comp, kv_rope_dim]); each gathered row is dequantized to bf16, channel by channel
+     * bf16(fp32(code) * scale), the RoPE part as stored, and that bf16 row is what the
+     * attention multiplies and what the gather buffer receives. kv_rope_dim: a multiple of 8,
+     * 8..dim-8. Decode only (n_q = 1). kv_fp8 = 0: the three are NULL. */
+    int kv_fp8;
+    const void* kv_nope;
+    const float* kv_scale;
+    const void* kv_rope;
+    int kv_rope_dim;
 } dsv4_attn_args;
 
 size_t dsv4_sparse_attn_workspace_size(const dsv4_attn_args* args);

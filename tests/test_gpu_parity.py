@@ -606,6 +606,90 @@ def test_sparse_attention_decode(cfg):
     assert np.array_equal(gat[seqs], ref_g), "gather buffer differs"
 
 
+def _mixed_kv(comp_bits, rope_dim=64):
+    """The mixed FP8 / bf16 storage of bf16 cache rows (the oracle's quantization), and the
+    bf16 rows the attention then multiplies (the oracle's dequantization)."""
+    nope, sc, rope = oracle.quantize_kv_mixed(synth.bf16_bits_to_f32(comp_bits), rope_dim)
+    return (nope, sc, rope), oracle.dequant_kv_mixed(nope, sc, rope)
+
+
+def _run_attn_mixed(x, wl, idx, mixed, top_k=None):
+    m = csa()
+    nope, sc, rope = mixed
+    q, sink = dev_bf16(x["q"]), dev(x["sink"])
+    n_comp, win, win_len = dev(x["n_comp"]), dev_bf16(x["win"]), dev(x["win_len"])
+    B, n_q, H, D = x["q"].shape
+    top_k = top_k or (idx.shape[-1] if idx is not None else nope.shape[1])
+    out = torch.empty(B, n_q, H, D, dtype=torch.bfloat16, device="cuda")
+    gather = torch.full((B, n_q, top_k + wl.window, D), 7.0, dtype=torch.bfloat16, device="cuda")
+    kw = dict(idx=None if idx is None else dev(idx), top_k=top_k, window=wl.window, ratio=wl.ratio,
+              gather=gather, kv_nope=dev(nope), kv_scale=dev(sc), kv_rope=dev_bf16(rope))
+    ws = ws_tensor(m.dsv4_sparse_attn_workspace_size(q, sink, None, n_comp, win, win_len, out, **kw))
+    m.dsv4_sparse_attn_decode(q, sink, None, n_comp, win, win_len, out, ws, **kw)
+    torch.cuda.synchronize()
+    st, ew = m.dsv4_read_error_word(ws)
+    return host_bf16(out), host_bf16(gather), ew
+
+
+@pytest.mark.parametrize("cfg", [1, 3])
+def test_sparse_attention_decode_mixed_kv(cfg):
+    """Compressed rows in the mixed FP8 / bf16 storage: the gather buffer holds exactly the
+    oracle's dequantized rows (and the window rows), the output matches the oracle's attention
+    over them."""
+    wl, x = _attn_case(cfg)
+    B = wl.batch
+    seqs = [0, 3] if cfg == 3 else [0, 5, 15]
+    comp = x["comp_kv_dev"]
+    if cfg == 3:
+        mixed, deq = _mixed_kv(comp[:, : 40000])              # the first 40,000 rows suffice
+        n_comp = np.minimum(x["n_comp"], 40000).astype(np.int32)
+        x = dict(x, n_comp=n_comp)
+    else:
+        mixed, deq = _mixed_kv(comp)
+    idx = synth.uniform_index_sets(wl.seed, 19, B, x["n_comp"], wl.top_k).reshape(B, 1, wl.top_k)
+    got, gat, ew = _run_attn_mixed(x, wl, idx, mixed)
+    assert ew == 0
+    _, ref, ref_g = oracle.sparse_attn(x["q"][seqs], x["sink"], deq[seqs], x["n_comp"][seqs], idx[seqs],
+                                       x["win"][seqs], x["win_len"][seqs], wl.top_k, wl.window, wl.ratio,
+                                       want_gather=True)
+    assert np.array_equal(gat[seqs], ref_g), "gather buffer differs from the dequantized rows"
+    assert_bf16_close(got[seqs], ref, f"cfg{cfg} attention over mixed KV")
+
+
+def test_hca_dense_attention_mixed_kv():
+    """The dense (HCA) form over the mixed storage, every compressed row and the window."""
+    wl, x = _attn_case(2)
+    mixed, deq = _mixed_kv(x["comp_kv_dev"])
+    got, gat, ew = _run_attn_mixed(x, wl, None, mixed)
+    assert ew == 0
+    seqs = [0, 17, 63]
+    _, ref, ref_g = oracle.sparse_attn(x["q"][seqs], x["sink"], deq[seqs], x["n_comp"][seqs], None,
+                                       x["win"][seqs], x["win_len"][seqs], wl.max_comp, wl.window,
+                                       wl.ratio, want_gather=True)
+    assert np.array_equal(gat[seqs], ref_g)
+    assert_bf16_close(got[seqs], ref, "HCA attention over mixed KV")
+
+
+def test_compress_mixed_kv_cache():
+    """The compressor writing the mixed storage (codes and scale of the 448 channels without
+    RoPE, bf16 RoPE part) against the oracle's entries quantized by the oracle."""
+    wl = WORKLOADS[1]
+    x = inputs(1)
+    m = csa()
+    B, T, D = x["C"].shape
+    rows, rd = T // wl.ratio, wl.rope_dim
+    nope = torch.zeros(B, rows, D - rd, dtype=torch.uint8, device="cuda")
+    sc = torch.full((B, rows), float("nan"), dtype=torch.float32, device="cuda")
+    rope = torch.zeros(B, rows, rd, dtype=torch.bfloat16, device="cuda")
+    m.dsv4_compress(dev_bf16(x["C"]), dev_bf16(x["Z"]), dev(x["bias"]), dev(x["gamma"]), dev(x["pos0"]),
+                    nope, ratio=wl.ratio, rope_dim=rd, out_scale=sc, out_rope=rope)
+    torch.cuda.synchronize()
+    _, ref = oracle.compress(x["C"], x["Z"], x["bias"], x["gamma"], x["pos0"], wl.ratio, rd)
+    got8, got_s = nope.cpu().numpy(), sc.cpu().numpy()
+    _check_fp8_cache(got8, got_s, ref[..., : D - rd], "mixed KV: part without RoPE")
+    assert_bf16_close(host_bf16(rope), ref[..., D - rd:], "mixed KV: RoPE part")
+
+
 def test_hca_dense_attention():
     wl, x = _attn_case(2)
     got, gat, ew = _run_attn(x, wl, None)
@@ -700,7 +784,7 @@ def test_attention_edge_cases_and_bad_index():
 
 
 # ------------------------------------------------------------------ the fused decode step
-def _fused_step(x, wl, graph=False, fp8=False):
+def _fused_step(x, wl, graph=False, fp8=False, mixed=False):
     """Compress (whole context) + indexer top-k + gather/attention in one dsv4_csa_decode.
     fp8: the key cache is written and scored in FP8 E4M3 (queries quantized by the oracle),
     and the step also returns its scores."""
@@ -722,7 +806,14 @@ def _fused_step(x, wl, graph=False, fp8=False):
     t["bias"], t["gamma"] = dev(x["bias"]), dev(x["gamma"])
     t["biasI"], t["gammaI"] = dev(x["bias_I"]), dev(x["gamma_I"])
     t["pos0"] = dev(x["pos0"])
-    t["kv"] = torch.zeros(B, wl.max_comp, D, dtype=torch.bfloat16, device="cuda")
+    rd = wl.rope_dim
+    if mixed:
+        # the KV cache in the mixed FP8 / bf16 storage, written by the step's compressor
+        t["kv"] = torch.zeros(B, wl.max_comp, D - rd, dtype=torch.uint8, device="cuda")
+        t["kv_scale"] = torch.full((B, wl.max_comp), float("nan"), dtype=torch.float32, device="cuda")
+        t["kv_rope"] = torch.zeros(B, wl.max_comp, rd, dtype=torch.bfloat16, device="cuda")
+    else:
+        t["kv"] = torch.zeros(B, wl.max_comp, D, dtype=torch.bfloat16, device="cuda")
     t["keys"] = torch.zeros(B, wl.max_comp, Di, dtype=torch.uint8 if fp8 else torch.bfloat16, device="cuda")
     t["q_I"], t["w"] = dev_bf16(x["q_I"]), dev(x["w"])
     t["n_comp"] = dev(x["n_comp"])
@@ -731,13 +822,15 @@ def _fused_step(x, wl, graph=False, fp8=False):
     t["win"], t["win_len"] = dev_bf16(x["win"]), dev(x["win_len"])
     t["out"] = torch.empty(B, 1, wl.heads, D, dtype=torch.bfloat16, device="cuda")
     t["gather"] = torch.empty(B, 1, wl.top_k + wl.window, D, dtype=torch.bfloat16, device="cuda")
-    ck = _abi.compress_args(t["C"], t["Z"], t["bias"], t["gamma"], t["pos0"], t["kv"], ratio=wl.ratio)
+    mkw = dict(out_scale=t["kv_scale"], out_rope=t["kv_rope"]) if mixed else {}
+    ck = _abi.compress_args(t["C"], t["Z"], t["bias"], t["gamma"], t["pos0"], t["kv"], ratio=wl.ratio, **mkw)
     cq = _abi.compress_args(t["CI"], t["ZI"], t["biasI"], t["gammaI"], t["pos0"], t["keys"], ratio=wl.ratio,
                             **fkw)
     ia = _abi.index_args(t["q8"] if fp8 else t["q_I"], t["w"], t["keys"], t["n_comp"], t["idx"],
                          ratio=wl.ratio, **ikw)
-    aa = _abi.attn_args(t["q"], t["sink"], t["kv"], t["n_comp"], t["win"], t["win_len"], t["out"],
-                        idx=t["idx"], window=wl.window, ratio=wl.ratio, gather=t["gather"])
+    akw = dict(kv_nope=t["kv"], kv_scale=t["kv_scale"], kv_rope=t["kv_rope"]) if mixed else {}
+    aa = _abi.attn_args(t["q"], t["sink"], None if mixed else t["kv"], t["n_comp"], t["win"], t["win_len"],
+                        t["out"], idx=t["idx"], window=wl.window, ratio=wl.ratio, gather=t["gather"], **akw)
     ws = ws_tensor(m.dsv4_csa_decode_workspace_size(attn=aa, index=ia, compress_kv=ck, compress_keys=cq))
     m.dsv4_csa_decode(ws, attn=aa, index=ia, compress_kv=ck, compress_keys=cq)
     torch.cuda.synchronize()
@@ -833,6 +926,37 @@ def test_fused_decode_step_fp8_keys(cfg):
     _, ref_o, _ = oracle.sparse_attn(x["q"], x["sink"], ref_kv_bits, x["n_comp"], ref_i, x["win"],
                                      x["win_len"], wl.top_k, wl.window, wl.ratio, want_gather=True)
     assert_bf16_close(host_bf16(t["out"])[same], ref_o[same], "fused fp8: attention output")
+
+
+@pytest.mark.parametrize("cfg", [0, 1])
+def test_fused_decode_step_mixed_kv(cfg):
+    """The fused step with the KV cache in the mixed FP8 / bf16 storage: the compressor writes
+    it, the attention reads it. Cache against the oracle's quantized entries; where the
+    step's selection equals the oracle's, the output against the oracle's attention over the
+    oracle's dequantized rows."""
+    wl = WORKLOADS[cfg]
+    x = inputs(cfg)
+    t, (ck, cq, ia, aa, ws), _ = _fused_step(x, wl, mixed=True)
+    st, ew = csa().dsv4_read_error_word(ws)
+    assert ew == 0, f"device error word {ew:#x}"
+    D, rd = x["C"].shape[2], wl.rope_dim
+    _, ref_kv = _oracle_kv(x, wl)
+    nc = ref_kv.shape[1]
+    _check_fp8_cache(t["kv"].cpu().numpy()[:, :nc], t["kv_scale"].cpu().numpy()[:, :nc],
+                     ref_kv[..., : D - rd], "fused mixed KV")
+    assert_bf16_close(host_bf16(t["kv_rope"])[:, :nc], ref_kv[..., D - rd:], "fused mixed KV: RoPE part")
+    # the oracle's storage of its own entries (the fp32 value of each, as the compressor's)
+    deq = oracle.dequant_kv_mixed(*oracle.quantize_kv_mixed(ref_kv.astype(np.float32), rd))
+    ref_keys_bits, _ = oracle.compress(x["C_I"], x["Z_I"], x["bias_I"], x["gamma_I"], x["pos0"], wl.ratio,
+                                       wl.rope_dim)
+    ref_s, nv = oracle.index_scores(x["q_I"], x["w"], ref_keys_bits, x["n_comp"], wl.ratio)
+    ref_i = oracle.topk(ref_s, nv, wl.top_k)
+    idx = t["idx"].cpu().numpy()
+    same = [b for b in range(wl.batch) if np.array_equal(idx[b, 0], ref_i[b, 0])]
+    assert same, "no sequence selected exactly the oracle's keys"
+    _, ref_o, _ = oracle.sparse_attn(x["q"], x["sink"], deq, x["n_comp"], ref_i, x["win"], x["win_len"],
+                                     wl.top_k, wl.window, wl.ratio, want_gather=True)
+    assert_bf16_close(host_bf16(t["out"])[same], ref_o[same], "fused mixed KV: attention output")
 
 
 def test_fused_decode_graph_replay_matches_eager():

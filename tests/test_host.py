@@ -97,6 +97,14 @@ def test_indexer_rejects_small_workspace(lib):
     dict(out_rope_pos=_p(11), out_rope_dim=0), dict(out_rope_pos=_p(11), out_rope_dim=63),
     dict(out_rope_pos=_p(11), out_rope_dim=256), dict(out_rope_pos=_p(11), out_rope_dim=64, out_rope_theta=0.0),
     dict(out_rope_pos=ctypes.c_void_p(FAKE + 4096 * 11 + 4), out_rope_dim=64, out_rope_theta=1e4),
+    # mixed FP8 / bf16 KV: comp_kv must be NULL, the three parts given, the RoPE part 8..dim-8
+    dict(kv_fp8=1, kv_nope=_p(12), kv_scale=_p(13), kv_rope=_p(14), kv_rope_dim=64),
+    dict(comp_kv=None, kv_fp8=1, kv_nope=_p(12), kv_scale=_p(13), kv_rope=None, kv_rope_dim=64),
+    dict(comp_kv=None, kv_fp8=1, kv_nope=_p(12), kv_scale=_p(13), kv_rope=_p(14), kv_rope_dim=60),
+    dict(comp_kv=None, kv_fp8=1, kv_nope=_p(12), kv_scale=_p(13), kv_rope=_p(14), kv_rope_dim=512),
+    dict(comp_kv=None, kv_fp8=1, kv_nope=_p(12), kv_scale=_p(13), kv_rope=_p(14), kv_rope_dim=64, n_q=2),
+    dict(comp_kv=None, kv_fp8=2, kv_nope=_p(12), kv_scale=_p(13), kv_rope=_p(14), kv_rope_dim=64),
+    dict(kv_nope=_p(12)),
 ])
 def test_attention_rejects_on_host(lib, bad):
     a = _attn_args(**bad)
@@ -113,8 +121,10 @@ def test_compress_rejects_on_host(lib):
                 dict(out_rows=3), dict(eps=-1.0), dict(C=None), dict(ratio=0), dict(overlap=2),
                 dict(overlap=1, prev_C=_p(7)), dict(overlap=0, prev_C=_p(7), prev_Z=_p(8)),
                 dict(overlap=1, prev_C=_p(7), prev_Z=ctypes.c_void_p(FAKE + 4096 * 9 + 8)),
-                dict(out_fp8=2, out_scale=_p(7)), dict(out_fp8=1), dict(out_scale=_p(7)),
-                dict(out_fp8=1, out_scale=ctypes.c_void_p(FAKE + 4096 * 7 + 4))):
+                dict(out_fp8=3, out_scale=_p(7)), dict(out_fp8=1), dict(out_scale=_p(7)),
+                dict(out_fp8=1, out_scale=ctypes.c_void_p(FAKE + 4096 * 7 + 4)),
+                dict(out_fp8=2, out_scale=_p(7)), dict(out_fp8=1, out_scale=_p(7), out_rope=_p(8)),
+                dict(out_rope=_p(8)), dict(out_fp8=2, out_scale=_p(7), out_rope=_p(8), rope_dim=512)):
         a = CompressArgs(**{**base, **bad})
         assert lib.dsv4_compress(ctypes.byref(a), None) == 1, bad
 
