@@ -152,10 +152,12 @@ def prefill_scoring(m, steps):
             "peak_kind": kind, "unit": "TFLOP/s", "frac": achieved / peak}
 
 
-def fp8_keys_step(m, _abi, t, wl, steps, stream, peak):
+def fp8_keys_step(m, _abi, t, wl, steps, stream, peak, mixed_kv=False):
     """The same decode step with the index-key cache in FP8 E4M3 (codes + one fp32 scale per
     key): the compressor writes the newest key in FP8, the scorer reads 128 + 4 bytes per key
-    instead of 256. The query quantization runs inside the step. Reported beside the bf16
+    instead of 256. The query quantization runs inside the step. mixed_kv: the KV cache too in
+    the pages' mixed storage (E4M3 codes of the 448 channels without RoPE, one fp32 scale,
+    bf16 RoPE part: 580 bytes per gathered row instead of 1024). Reported beside the bf16
     headline, not as it."""
     import torch
     B = wl.batch
@@ -168,12 +170,27 @@ def fp8_keys_step(m, _abi, t, wl, steps, stream, peak):
     stream.synchronize()
     cq = _abi.compress_args(t["C_I"], t["Z_I"], t["bias_I"], t["gamma_I"], t["pos0"], keys8,
                             ratio=wl.ratio, out_row0=t["append_row"], out_scale=kscale)
-    ck = _abi.compress_args(t["C"], t["Z"], t["bias"], t["gamma"], t["pos0"], t["kv"], ratio=wl.ratio,
-                            out_row0=t["append_row"])
+    rd, D = wl.rope_dim, wl.head_dim
+    if mixed_kv:
+        # the cache's rows in the mixed storage (input preparation on the device, untimed)
+        kvf = t["kv"].float()
+        amax = kvf[..., : D - rd].abs().amax(dim=-1)
+        kv_scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax)).contiguous()
+        kv_nope = (kvf[..., : D - rd] / kv_scale[..., None]).to(torch.float8_e4m3fn).view(torch.uint8).contiguous()
+        kv_rope = t["kv"][..., D - rd:].contiguous()
+        del kvf
+        ck = _abi.compress_args(t["C"], t["Z"], t["bias"], t["gamma"], t["pos0"], kv_nope, ratio=wl.ratio,
+                                out_row0=t["append_row"], out_scale=kv_scale, out_rope=kv_rope)
+        aa = _abi.attn_args(t["q"], t["sink"], None, t["n_comp"], t["win"], t["win_len"], t["out"],
+                            idx=t["idx"], window=wl.window, ratio=wl.ratio, gather=t["gather"],
+                            kv_nope=kv_nope, kv_scale=kv_scale, kv_rope=kv_rope)
+    else:
+        ck = _abi.compress_args(t["C"], t["Z"], t["bias"], t["gamma"], t["pos0"], t["kv"], ratio=wl.ratio,
+                                out_row0=t["append_row"])
+        aa = _abi.attn_args(t["q"], t["sink"], t["kv"], t["n_comp"], t["win"], t["win_len"], t["out"],
+                            idx=t["idx"], window=wl.window, ratio=wl.ratio, gather=t["gather"])
     ia = _abi.index_args(q8, t["w"], keys8, t["n_comp"], t["idx"], ratio=wl.ratio, q_scale=qscale,
                          key_scale=kscale)
-    aa = _abi.attn_args(t["q"], t["sink"], t["kv"], t["n_comp"], t["win"], t["win_len"], t["out"],
-                        idx=t["idx"], window=wl.window, ratio=wl.ratio, gather=t["gather"])
     nbytes = m.dsv4_csa_decode_workspace_size(attn=aa, index=ia, compress_kv=ck, compress_keys=cq)
     ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device="cuda")
 
@@ -221,8 +238,14 @@ def fp8_keys_step(m, _abi, t, wl, steps, stream, peak):
     score_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
     sb = B * wl.n_comp * (wl.idx_dim + 4 + 4) + B * wl.idx_heads * (wl.idx_dim + 4 + 4)
     gbs = sb / (score_ms * 1e-3) / 1e9
+    # the step's algorithmic bytes: keys (codes + scale) scanned, gathered rows, outputs
+    row_b = (D - rd) + 4 + rd * 2 if mixed_kv else D * 2
+    step_b = (B * wl.n_comp * (wl.idx_dim + 4) + B * wl.top_k * row_b + B * wl.window * D * 2 +
+              B * wl.heads * D * 2)
     return {"value": B / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
-            "launches_per_step": launches, "dtype": "fp8 e4m3 index keys, bf16 KV",
+            "launches_per_step": launches,
+            "dtype": "fp8 e4m3 index keys, " + ("mixed fp8/bf16 KV" if mixed_kv else "bf16 KV"),
+            "step_bytes": step_b, "step_frac": step_b / (ms * 1e-3) / 1e9 / peak,
             "scorer": {"kernel": "index_score_kernel<FP8>", "bytes_per_launch": sb,
                        "ms_per_launch": score_ms, "achieved": gbs, "peak": peak, "unit": "GB/s",
                        "frac": gbs / peak,
@@ -694,6 +717,7 @@ def run_ours(args):
     if world == 1:
         line["prefill_scoring"] = prefill_scoring(m, args.steps)
         line["fp8_keys"] = fp8_keys_step(m, _abi, t, wl, args.steps, stream, peak)
+        line["fp8_keys_mixed_kv"] = fp8_keys_step(m, _abi, t, wl, args.steps, stream, peak, mixed_kv=True)
         line["compressor_us"] = compressor_time(m, t, wl, args.steps, stream)
         line["other_decode_workloads"] = [decode_step_at(m, _abi, c, args.steps, peak) for c in (1, 2)]
     if world == 1 and not args.no_cpu_baseline:
