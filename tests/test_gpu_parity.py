@@ -959,6 +959,78 @@ def test_fused_decode_step_mixed_kv(cfg):
     assert_bf16_close(host_bf16(t["out"])[same], ref_o[same], "fused mixed KV: attention output")
 
 
+def test_fused_decode_step_1m_context_as_benchmarked():
+    """The fused step exactly as the benchmark runs it (1M-token context, batch 4, the caches
+    pre-filled, the newest block compressed into the last row of both caches in the step,
+    stage claims, one CUDA graph), checked on sequences 0 and 3: the new cache rows against
+    the oracle's compression of the newest block; the selection against the oracle's top-k
+    over the input keys with the oracle's newest key (exact up to near ties and the bf16
+    rounding of that one key); the attention output against the oracle where the selection
+    is the oracle's."""
+    m = csa()
+    from compressed_sparse_attention_08_gb300 import _abi
+    wl = WORKLOADS[3]
+    x = inputs(3)
+    B, D, Di = wl.batch, wl.head_dim, wl.idx_dim
+    t = {k: dev_bf16(x[k]) for k in ("C", "Z", "C_I", "Z_I", "q_I", "q", "win")}
+    t.update({k: dev(x[k]) for k in ("bias", "gamma", "bias_I", "gamma_I", "pos0", "append_row", "w",
+                                     "n_comp", "sink", "win_len")})
+    t["kv"], t["keys"] = dev_bf16(x["comp_kv"]), dev_bf16(x["keys"])
+    t["idx"] = torch.empty(B, 1, wl.top_k, dtype=torch.int32, device="cuda")
+    t["out"] = torch.empty(B, 1, wl.heads, D, dtype=torch.bfloat16, device="cuda")
+    t["gather"] = torch.empty(B, 1, wl.top_k + wl.window, D, dtype=torch.bfloat16, device="cuda")
+    ck = _abi.compress_args(t["C"], t["Z"], t["bias"], t["gamma"], t["pos0"], t["kv"], ratio=wl.ratio,
+                            out_row0=t["append_row"])
+    cq = _abi.compress_args(t["C_I"], t["Z_I"], t["bias_I"], t["gamma_I"], t["pos0"], t["keys"],
+                            ratio=wl.ratio, out_row0=t["append_row"])
+    ia = _abi.index_args(t["q_I"], t["w"], t["keys"], t["n_comp"], t["idx"], ratio=wl.ratio)
+    aa = _abi.attn_args(t["q"], t["sink"], t["kv"], t["n_comp"], t["win"], t["win_len"], t["out"],
+                        idx=t["idx"], window=wl.window, ratio=wl.ratio, gather=t["gather"])
+    ws = ws_tensor(m.dsv4_csa_decode_workspace_size(attn=aa, index=ia, compress_kv=ck, compress_keys=cq))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        m.dsv4_csa_decode(ws, attn=aa, index=ia, compress_kv=ck, compress_keys=cq, stream=s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            m.dsv4_csa_decode(ws, attn=aa, index=ia, compress_kv=ck, compress_keys=cq, stream=s)
+        g.replay()
+    torch.cuda.synchronize()
+    st, ew = m.dsv4_read_error_word(ws)
+    assert ew == 0, f"device error word {ew:#x}"
+    row = int(x["append_row"][0])
+    seqs = [0, 3]
+    new_kv_bits, new_kv = oracle.compress(x["C"][seqs], x["Z"][seqs], x["bias"], x["gamma"], x["pos0"][seqs],
+                                          wl.ratio, wl.rope_dim)
+    new_key_bits, new_key = oracle.compress(x["C_I"][seqs], x["Z_I"][seqs], x["bias_I"], x["gamma_I"],
+                                            x["pos0"][seqs], wl.ratio, wl.rope_dim)
+    kv_rows = t["kv"][seqs, row].cpu().view(torch.int16).numpy().view(np.uint16)
+    key_rows = t["keys"][seqs, row].cpu().view(torch.int16).numpy().view(np.uint16)
+    assert_bf16_close(kv_rows[:, None], new_kv, "newest KV row")
+    assert_bf16_close(key_rows[:, None], new_key, "newest key row")
+    idx = t["idx"].cpu().numpy()
+    out = host_bf16(t["out"])
+    for j, b in enumerate(seqs):
+        keys_b = x["keys"][b:b + 1].copy()
+        keys_b[0, row] = new_key_bits[j, 0]
+        ref_s, nv = oracle.index_scores(x["q_I"][b:b + 1], x["w"][b:b + 1], keys_b, x["n_comp"][b:b + 1], wl.ratio)
+        ref_i = oracle.topk(ref_s, nv, wl.top_k)
+        if not np.array_equal(idx[b, 0], ref_i[0, 0]):
+            # only near ties, or the newest key (its bf16 entry may differ by one rounding step)
+            sc = ref_s[0, 0, : nv[0, 0]]
+            kth = np.sort(sc)[::-1][wl.top_k - 1]
+            diff = np.setxor1d(idx[b, 0], ref_i[0, 0])
+            near = np.abs(sc[diff] - kth) <= 1e-5 * abs(kth)
+            assert np.all(near | (diff == row)), f"b{b}: selection differs beyond near ties"
+            continue
+        kv_b = x["comp_kv"][b:b + 1].copy()
+        kv_b[0, row] = new_kv_bits[j, 0]
+        _, ref_o, _ = oracle.sparse_attn(x["q"][b:b + 1], x["sink"], kv_b, x["n_comp"][b:b + 1], ref_i,
+                                         x["win"][b:b + 1], x["win_len"][b:b + 1], wl.top_k, wl.window,
+                                         wl.ratio, want_gather=True)
+        assert_bf16_close(out[b:b + 1], ref_o, f"b{b}: attention output")
+
+
 def test_fused_decode_graph_replay_matches_eager():
     """The whole step captured in a CUDA graph replays to the eager result, bit for bit,
     after the inputs are changed in place."""
