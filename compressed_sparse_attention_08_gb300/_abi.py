@@ -46,7 +46,7 @@ class StepArgs(ctypes.Structure):
     _fields_ = [("C", P), ("Z", P), ("bias", P), ("gamma", P), ("pos", P), ("stage", P),
                 ("fill", P), ("n_comp", P), ("out", P), ("batch", I), ("dim", I), ("ratio", I),
                 ("rope_dim", I), ("out_rows", I), ("overlap", I), ("eps", ctypes.c_float),
-                ("rope_theta", ctypes.c_double)]
+                ("rope_theta", ctypes.c_double), ("out_fp8", I), ("out_scale", P), ("out_rope", P)]
 
 
 class IndexArgs(ctypes.Structure):
@@ -273,17 +273,23 @@ def compress_step_state(batch, dim, ratio, *, overlap=False, device="cuda"):
 
 
 def dsv4_compress_step(C, Z, bias, gamma, pos, stage, fill, n_comp, out, *, ratio, rope_dim=64,
-                       eps=1e-6, rope_theta=10000.0, overlap=False, stream=None):
+                       eps=1e-6, rope_theta=10000.0, overlap=False, out_scale=None, out_rope=None,
+                       stream=None):
     """One decode token per sequence: C, Z [B, w] (w = dim, or 2*dim two-stream); pos int64 [B];
     state stage / fill / n_comp (see compress_step_state) updated on the device; a completed
-    block goes to out[s, n_comp[s]]."""
+    block goes to out[s, n_comp[s]]. out_scale (and out_rope): the FP8 (mixed) cache formats,
+    as compress_args."""
+    import torch
     bf16, f32, i32, i64 = _dt()
     B, w = C.shape
-    d = out.shape[2]
+    fp8 = out_scale is not None
+    mode = 2 if (fp8 and out_rope is not None) else (1 if fp8 else 0)
+    d = out.shape[2] + (out_rope.shape[2] if mode == 2 else 0)
     a = StepArgs(_ptr(C, bf16, "C"), _ptr(Z, bf16, "Z"), _ptr(bias, f32, "bias"), _ptr(gamma, f32, "gamma"),
                  _ptr(pos, i64, "pos"), _ptr(stage, bf16, "stage"), _ptr(fill, i32, "fill"),
-                 _ptr(n_comp, i32, "n_comp"), _ptr(out, bf16, "out"), B, d, ratio, rope_dim,
-                 out.shape[1], 1 if overlap else 0, eps, rope_theta)
+                 _ptr(n_comp, i32, "n_comp"), _ptr(out, torch.uint8 if fp8 else bf16, "out"), B, d, ratio,
+                 rope_dim, out.shape[1], 1 if overlap else 0, eps, rope_theta, mode,
+                 _ptr(out_scale, f32, "out_scale", True), _ptr(out_rope, bf16, "out_rope", True))
     _check(library().dsv4_compress_step(ctypes.byref(a), _stream(stream)), "dsv4_compress_step")
 
 

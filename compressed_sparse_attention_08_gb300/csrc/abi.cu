@@ -204,6 +204,12 @@ int dsv4_compress_step(const dsv4_compress_step_args* a, dsv4_stream_t stream) {
         return DSV4_ERR_INVALID_ARG;
     if (!(a->eps >= 0.f) || !std::isfinite(a->eps) || !std::isfinite(a->rope_theta) || a->rope_theta <= 0.0)
         return DSV4_ERR_INVALID_ARG;
+    if (a->out_fp8 < 0 || a->out_fp8 > 2) return DSV4_ERR_INVALID_ARG;
+    if (a->out_fp8 ? !dev_ptr_ok(a->out_scale) : a->out_scale != nullptr) return DSV4_ERR_INVALID_ARG;
+    if (a->out_fp8 == 2 ? (a->rope_dim > 0 ? !dev_ptr_ok(a->out_rope) : a->out_rope != nullptr)
+                        : a->out_rope != nullptr)
+        return DSV4_ERR_INVALID_ARG;
+    if (a->out_fp8 == 2 && a->rope_dim >= a->dim) return DSV4_ERR_INVALID_ARG;
     if (int rc = device_check()) return rc;
     return launch_compress_step(*a, reinterpret_cast<cudaStream_t>(stream));
 }

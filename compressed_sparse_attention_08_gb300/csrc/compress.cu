@@ -349,10 +349,13 @@ struct StepJob {
     __nv_bfloat16* stage;        // [batch, 2, 2, ratio, w]
     int32_t* fill;               // [batch]
     int32_t* n_comp;             // [batch]
-    __nv_bfloat16* out;          // [batch, out_rows, dim]
+    __nv_bfloat16* out;          // [batch, out_rows, dim] (or the FP8 / mixed layouts)
     int batch, dim, ratio, rope_dim, out_rows, overlap;
     float eps;
     double log2_theta;
+    int out_fp8;                 // as CompressJob
+    float* out_scale;
+    __nv_bfloat16* out_rope;
 };
 
 __global__ void __launch_bounds__(kThreads, 2)
@@ -396,17 +399,20 @@ compress_step_kernel(const __grid_constant__ StepJob j) {
     in.eps = j.eps;
     in.pos = static_cast<double>(j.pos[s] - (j.ratio - 1));   // the block's first token
     // a full cache keeps its rows: the entry is computed but not stored, n_comp stays
-    in.dst = nc >= 0 && nc < j.out_rows ? j.out + (static_cast<size_t>(s) * j.out_rows + nc) * j.dim : nullptr;
-    in.dst8 = nullptr;
-    in.dst_scale = nullptr;
-    in.q_dim = j.dim;
-    in.dst_rope = nullptr;
+    const bool stored = nc >= 0 && nc < j.out_rows;
+    const size_t orow = static_cast<size_t>(s) * j.out_rows + nc;
+    const int q_dim = j.out_fp8 == 2 ? j.dim - j.rope_dim : j.dim;
+    in.dst = stored && !j.out_fp8 ? j.out + orow * j.dim : nullptr;
+    in.dst8 = stored && j.out_fp8 ? reinterpret_cast<uint8_t*>(j.out) + orow * q_dim : nullptr;
+    in.dst_scale = stored && j.out_fp8 ? j.out_scale + orow : nullptr;
+    in.q_dim = q_dim;
+    in.dst_rope = stored && j.out_fp8 == 2 ? j.out_rope + orow * (j.dim - q_dim) : nullptr;
     entry_math<kChunkShort>(in, freq, y, warp_sum);
     if (j.overlap)                                 // this block is stream a of the next entry
         for (size_t c = tid; c < blk; c += kThreads) prev[c] = cur[c];
     if (tid == 0) {
         j.fill[s] = 0;
-        if (in.dst) j.n_comp[s] = nc + 1;
+        if (stored) j.n_comp[s] = nc + 1;
     }
 }
 
@@ -462,6 +468,9 @@ int launch_compress_step(const dsv4_compress_step_args& a, cudaStream_t stream) 
     j.overlap = a.overlap;
     j.eps = a.eps;
     j.log2_theta = std::log2(a.rope_theta);
+    j.out_fp8 = a.out_fp8;
+    j.out_scale = a.out_scale;
+    j.out_rope = static_cast<__nv_bfloat16*>(a.out_rope);
     count_launch();
     return launch_k(compress_step_kernel, dim3(a.batch), dim3(kThreads), 0, stream, false, j) == cudaSuccess
                ? DSV4_OK : DSV4_ERR_LAUNCH;

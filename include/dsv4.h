@@ -144,6 +144,13 @@ typedef struct dsv4_compress_step_args {
     int batch, dim, ratio, rope_dim, out_rows, overlap;
     float eps;
     double rope_theta;
+    /* Output format, as dsv4_compress_args: out_fp8 = 0 bf16 rows; 1 FP8 E4M3 rows (out:
+     * bytes [batch, out_rows, dim]) with scales in out_scale [batch, out_rows]; 2 the mixed
+     * KV storage (out: codes [batch, out_rows, dim - rope_dim], out_scale, out_rope bf16
+     * [batch, out_rows, rope_dim]). */
+    int out_fp8;
+    float* out_scale;
+    void* out_rope;
 } dsv4_compress_step_args;
 int dsv4_compress_step(const dsv4_compress_step_args* args, dsv4_stream_t stream);
 

@@ -216,6 +216,40 @@ def test_compress_step_matches_block_compressor(overlap):
     assert not np.any(got[:, nb:]), "rows past n_comp were written"
 
 
+@pytest.mark.parametrize("mode", ["fp8", "mixed"])
+def test_compress_step_fp8_outputs(mode):
+    """The device-side decode compressor writing an FP8 key cache (128-wide entries) or the
+    mixed KV storage (512-wide entries), token by token, against the oracle's compression of
+    the whole token history quantized by the oracle."""
+    m = csa()
+    B, r, T = 3, 4, 24
+    d = 128 if mode == "fp8" else 512
+    rd = 64
+    C = synth.normal_bf16(9, 131, (B, T, d))
+    Z = synth.normal_bf16(9, 132, (B, T, d))
+    bias = synth.bf16_bits_to_f32(synth.normal_bf16(9, 133, (r, d), 0.0, 0.5))
+    gamma = synth.bf16_bits_to_f32(synth.normal_bf16(9, 134, (d,), 1.0, 0.1))
+    pos0 = np.array([0, 8192, 1048000], np.int64)
+    stage, fill, n_comp = m.compress_step_state(B, d, r)
+    rows = 8
+    qd = d if mode == "fp8" else d - rd
+    out = torch.zeros(B, rows, qd, dtype=torch.uint8, device="cuda")
+    sc = torch.full((B, rows), float("nan"), dtype=torch.float32, device="cuda")
+    rope = torch.zeros(B, rows, rd, dtype=torch.bfloat16, device="cuda") if mode == "mixed" else None
+    Cd, Zd, bd, gd = dev_bf16(C), dev_bf16(Z), dev(bias), dev(gamma)
+    for t in range(T):
+        m.dsv4_compress_step(Cd[:, t].contiguous(), Zd[:, t].contiguous(), bd, gd, dev(pos0 + t), stage, fill,
+                             n_comp, out, ratio=r, rope_dim=rd, out_scale=sc, out_rope=rope)
+    torch.cuda.synchronize()
+    nb = T // r
+    assert n_comp.cpu().tolist() == [nb] * B
+    _, ref = oracle.compress(C, Z, bias, gamma, pos0, r, rd)
+    _check_fp8_cache(out.cpu().numpy()[:, :nb], sc.cpu().numpy()[:, :nb], ref[..., :qd], f"step {mode}")
+    if mode == "mixed":
+        assert_bf16_close(host_bf16(rope)[:, :nb], ref[..., qd:], "step mixed: RoPE part")
+    assert not np.any(out.cpu().numpy()[:, nb:]), "rows past n_comp were written"
+
+
 def test_compress_step_graph_replay_and_full_cache():
     """One captured graph replayed for every token (inputs copied into fixed buffers); a cache
     that is full keeps its rows and its count."""

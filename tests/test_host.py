@@ -136,7 +136,10 @@ def test_compress_step_rejects_on_host(lib):
                 overlap=0, eps=1e-6, rope_theta=10000.0)
     for bad in (dict(stage=None), dict(fill=None), dict(n_comp=None), dict(ratio=0),
                 dict(dim=2048), dict(rope_dim=65), dict(out_rows=0), dict(overlap=3),
-                dict(rope_theta=-1.0), dict(pos=ctypes.c_void_p(FAKE + 4))):
+                dict(rope_theta=-1.0), dict(pos=ctypes.c_void_p(FAKE + 4)),
+                dict(out_fp8=3, out_scale=_p(10)), dict(out_fp8=1), dict(out_scale=_p(10)),
+                dict(out_fp8=2, out_scale=_p(10)), dict(out_rope=_p(11)),
+                dict(out_fp8=2, out_scale=_p(10), out_rope=_p(11), rope_dim=512)):
         a = StepArgs(**{**base, **bad})
         assert lib.dsv4_compress_step(ctypes.byref(a), None) == 1, bad
 
