@@ -391,6 +391,57 @@ def device_arena(specs):
     return buf, views
 
 
+def prefill_attention(m, steps):
+    """The chunked-prefill attention alone: 2048 queries x 64 heads x 512 dims, each over its
+    1024 selected compressed entries and its own 128-token window (causal), no gather buffer.
+    Reported in TFLOP/s (QK and PV, 4 flops per head, slot and dim) against the measured bf16
+    tensor peak."""
+    import numpy as np
+    import torch
+    from compressed_sparse_attention_08_gb300 import synth
+    from compressed_sparse_attention_08_gb300.workloads import WORKLOADS, make_inputs
+    wl = WORKLOADS[4]
+    x = make_inputs(wl)
+    n_q = wl.new_tokens
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a, np.uint16).view(np.int16)).cuda().view(torch.bfloat16)
+
+    def dv(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+    nvis = np.minimum(x["n_comp"][0], (x["q_pos"][0] + 1) // wl.ratio).astype(np.int32)
+    idx = synth.uniform_index_sets(wl.seed, 17, n_q, nvis, wl.top_k).reshape(1, n_q, wl.top_k)
+    q, sink, kv = bf(x["q"]), dv(x["sink"]), bf(x["comp_kv"])
+    n_comp, win, win_len, q_pos = dv(x["n_comp"]), bf(x["win"]), dv(x["win_len"]), dv(x["q_pos"])
+    idx_d = dv(idx)
+    out = torch.empty(1, n_q, wl.heads, wl.head_dim, dtype=torch.bfloat16, device="cuda")
+    kw = dict(idx=idx_d, top_k=wl.top_k, window=wl.window, ratio=wl.ratio, q_pos=q_pos)
+    ws = torch.empty(max(m.dsv4_sparse_attn_workspace_size(q, sink, kv, n_comp, win, win_len, out, **kw), 256),
+                     dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def run():
+        m.dsv4_sparse_attn_decode(q, sink, kv, n_comp, win, win_len, out, ws, stream=stream, **kw)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            run()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(max(1, min(steps, 20)))]
+        for a, b in evs:
+            a.record(stream)
+            run()
+            b.record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    flops = float(n_q) * wl.heads * (wl.top_k + wl.window) * wl.head_dim * 4
+    peak, kind = measured_bf16_peak()
+    achieved = flops / (ms * 1e-3) / 1e12
+    return {"workload": wl.name, "bound": "tensor", "flops_per_call": flops, "ms_per_call": ms,
+            "achieved": achieved, "peak": peak, "peak_kind": kind, "unit": "TFLOP/s", "frac": achieved / peak}
+
+
 def profile_traffic(name="index_score_kernel_csa_decode_ctx1048576_b4.md"):
     """dram bytes per scoring launch from the committed ncu summary, if the kernel source
     still matches the hash recorded there; else None."""
@@ -716,6 +767,7 @@ def run_ours(args):
     }
     if world == 1:
         line["prefill_scoring"] = prefill_scoring(m, args.steps)
+        line["prefill_attention"] = prefill_attention(m, args.steps)
         line["fp8_keys"] = fp8_keys_step(m, _abi, t, wl, args.steps, stream, peak)
         line["fp8_keys_mixed_kv"] = fp8_keys_step(m, _abi, t, wl, args.steps, stream, peak, mixed_kv=True)
         line["compressor_us"] = compressor_time(m, t, wl, args.steps, stream)
@@ -747,7 +799,8 @@ def main():
         import __graft_entry__
         __graft_entry__.build()
         import compressed_sparse_attention_08_gb300 as m
-        print(json.dumps({"prefill_scoring": prefill_scoring(m, args.steps)}), flush=True)
+        print(json.dumps({"prefill_scoring": prefill_scoring(m, args.steps),
+                          "prefill_attention": prefill_attention(m, args.steps)}), flush=True)
     else:
         run_ours(args)
 

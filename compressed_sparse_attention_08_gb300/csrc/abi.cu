@@ -99,9 +99,7 @@ bool attn_ok(const dsv4_attn_args* a) {
     } else if (a->kv_fp8 == 1) {
         if (a->comp_kv || !dev_ptr_ok(a->kv_nope) || !dev_ptr_ok(a->kv_scale) || !dev_ptr_ok(a->kv_rope))
             return false;
-        if (a->n_q != 1 || a->kv_rope_dim < 8 || a->kv_rope_dim % 8 || a->kv_rope_dim > a->dim - 8) return false;
-        // read by the fused decode kernel only: at most 256 chunks of 128 slots
-        if ((static_cast<long long>(a->top_k) + a->window + 127) / 128 > 256) return false;
+        if (a->kv_rope_dim < 8 || a->kv_rope_dim % 8 || a->kv_rope_dim > a->dim - 8) return false;
     } else {
         return false;
     }

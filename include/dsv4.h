@@ -278,7 +278,7 @@ typedef struct dsv4_attn_args {
      * max_comp, kv_rope_dim]); each gathered row is dequantized to bf16, channel by channel
      * bf16(fp32(code) * scale), the RoPE part as stored, and that bf16 row is what the
      * attention multiplies and what the gather buffer receives. kv_rope_dim: a multiple of 8,
-     * 8..dim-8. Decode only (n_q = 1). kv_fp8 = 0: the three are NULL. */
+     * 8..dim-8. kv_fp8 = 0: the three are NULL. */
     int kv_fp8;
     const void* kv_nope;
     const float* kv_scale;

@@ -736,6 +736,27 @@ def test_hca_dense_attention():
     assert np.array_equal(gat[seqs], ref_g)
 
 
+def test_dense_attention_many_chunks():
+    """The dense form over 39,999 compressed rows and a full window: 314 chunks of 128 slots,
+    more than the combine holds in registers (it loops over the rest)."""
+    from types import SimpleNamespace
+    rng = np.random.default_rng(31)
+    H, D, N = 8, 128, 40000
+    wl = SimpleNamespace(window=128, ratio=4)
+    x = {"q": synth.f32_to_bf16_bits(rng.standard_normal((1, 1, H, D)).astype(np.float32)),
+         "sink": rng.standard_normal(H).astype(np.float32),
+         "comp_kv_dev": synth.f32_to_bf16_bits(rng.standard_normal((1, N, D)).astype(np.float32)),
+         "n_comp": np.array([N - 1], np.int32),
+         "win": synth.f32_to_bf16_bits(rng.standard_normal((1, 128, D)).astype(np.float32)),
+         "win_len": np.array([128], np.int32), "q_pos": None}
+    got, gat, ew = _run_attn(x, wl, None)
+    assert ew == 0
+    _, ref, ref_g = oracle.sparse_attn(x["q"], x["sink"], x["comp_kv_dev"], x["n_comp"], None, x["win"],
+                                       x["win_len"], N, 128, 4, want_gather=True)
+    assert np.array_equal(gat, ref_g)
+    assert_bf16_close(got, ref, "dense attention over 314 chunks")
+
+
 def test_prefill_attention_sampled_queries():
     wl, x = _attn_case(4)
     nvis = np.array([16384 + (t + 1) // 4 for t in range(2048)], np.int32)

@@ -102,7 +102,6 @@ def test_indexer_rejects_small_workspace(lib):
     dict(comp_kv=None, kv_fp8=1, kv_nope=_p(12), kv_scale=_p(13), kv_rope=None, kv_rope_dim=64),
     dict(comp_kv=None, kv_fp8=1, kv_nope=_p(12), kv_scale=_p(13), kv_rope=_p(14), kv_rope_dim=60),
     dict(comp_kv=None, kv_fp8=1, kv_nope=_p(12), kv_scale=_p(13), kv_rope=_p(14), kv_rope_dim=512),
-    dict(comp_kv=None, kv_fp8=1, kv_nope=_p(12), kv_scale=_p(13), kv_rope=_p(14), kv_rope_dim=64, n_q=2),
     dict(comp_kv=None, kv_fp8=2, kv_nope=_p(12), kv_scale=_p(13), kv_rope=_p(14), kv_rope_dim=64),
     dict(kv_nope=_p(12)),
 ])
