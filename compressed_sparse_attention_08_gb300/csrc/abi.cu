@@ -93,7 +93,7 @@ bool attn_ok(const dsv4_attn_args* a) {
     if (a->max_comp < 1 || a->top_k < 1 || a->window < 0 || a->win_rows < 1 || a->ratio < 1) return false;
     if (a->idx ? a->top_k > a->max_comp : a->top_k != a->max_comp) return false;
     if (!std::isfinite(a->scale)) return false;
-    // the compressed rows: bf16 in comp_kv, or the mixed FP8 / bf16 storage (decode only)
+    // the compressed rows: bf16 in comp_kv, or the mixed FP8 / bf16 storage
     if (a->kv_fp8 == 0) {
         if (!dev_ptr_ok(a->comp_kv) || a->kv_nope || a->kv_scale || a->kv_rope) return false;
     } else if (a->kv_fp8 == 1) {

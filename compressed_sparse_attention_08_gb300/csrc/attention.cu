@@ -8,13 +8,15 @@
 // PERFORMANCE_AUDIT.md "P4" (V is the gathered K row itself); "nvfp4-megamoe-kernel: compare
 // master..pure-nvfp4", single_shot_inference.py eager_attention (scale = 1/sqrt(hd)).
 //
-// Design: one tcgen05 kernel for decode and prefill alike. A query row's slots (its
-// top_k selected compressed entries, then its window rows) are cut into 128-slot chunks, the
-// heads into groups of 32 (or 16), one CTA per (chunk, query row, head group); each CTA
-// gathers its chunk straight from the caches into shared memory, scores it against the
-// group's queries on the tensor cores and writes per-chunk (m, l, O) partials; the combine
-// kernel merges the chunks of every (query, head) and adds the sink once:
+// Design: tcgen05 kernels for decode and prefill alike. A query row's slots (its top_k
+// selected compressed entries, then its window rows) are cut into 128-slot chunks, the heads
+// into groups of 32 (or 16). With few query rows (decode) there is one CTA per (chunk, query
+// row, head group); each CTA gathers its chunk straight from the caches into shared memory,
+// scores it against the group's queries on the tensor cores and writes per-chunk (m, l, O)
+// partials; the combine kernel merges the chunks of every (query, head) and adds the sink once:
 //   o = sum_c O_c e^(m_c - M) / (sum_c l_c e^(m_c - M) + e^(sink - M)),  M = max(sink, m_c).
+// With many query rows (prefill) one CTA per (query row, head group) walks the row's chunks
+// with the same steps and a running maximum and sum, and writes the output itself.
 #include <cmath>
 
 #include <cuda_fp8.h>
@@ -217,6 +219,109 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[N]) {
     else DSV4_TMEM_LD_32x32b_X32(taddr, r);
 }
 
+// The gather of one chunk: warp w copies slots [16w, 16w + 16) of chunk `chunk` of query row
+// `row` into the shared tile (cp.async for bf16 rows, zero fill for slots without a row; the
+// mixed storage's codes are dequantized here) and marks in okf[] which slots hold a row. Lanes
+// 0..15 resolve the slots; every lane of the CTA must call it (the shuffles take all lanes).
+// The caller waits for the copies (cp_async_wait_all) and fences them for the tensor cores.
+template <int D, int NH>
+__device__ __forceinline__ void gather_chunk(const AttnParams& p, const __nv_bfloat16* __restrict__ comp_kv,
+                                             const __nv_bfloat16* __restrict__ win, uint8_t* sKV, int* okf,
+                                             int chunk, int row, int b, int nv, int w_lo, int w_cnt,
+                                             int warp, int lane) {
+    using C = FCfg<D, NH>;
+    const int r0 = warp * 16;
+    unsigned long long src = 0;                                  // bf16 row; 0: none
+    long long ent = -1;                                          // mixed storage: entry row
+    float escale = 0.f;
+    if (lane < 16) {
+        const int slot = chunk * kFC + r0 + lane;
+        if (slot < p.top_k) {
+            int e;
+            if (p.idx) {
+                e = p.idx[static_cast<size_t>(row) * p.top_k + slot];
+                if (e >= nv) { flag_error(p.eword, DSV4_EWORD_BAD_INDEX); e = -1; }
+            } else {
+                e = slot < nv ? slot : -1;
+            }
+            if (e >= 0) {
+                if (p.kv_nope) {
+                    ent = static_cast<long long>(b) * p.max_comp + e;
+                    escale = __ldg(&p.kv_scale[ent]);
+                } else {
+                    src = reinterpret_cast<unsigned long long>(comp_kv + (static_cast<size_t>(b) * p.max_comp + e) * D);
+                }
+            }
+        } else if (slot < p.slots) {
+            const int wi = slot - p.top_k;
+            if (wi < w_cnt)
+                src = reinterpret_cast<unsigned long long>(win + (static_cast<size_t>(b) * p.win_rows + w_lo + wi) * D);
+        }
+        okf[r0 + lane] = src != 0 || ent >= 0;
+    }
+    if (!p.kv_nope) {
+        for (int i = lane; i < 16 * C::U; i += 32) {
+            const int r = i / C::U, c = i - r * C::U;
+            const unsigned long long a = __shfl_sync(0xffffffffu, src, r);
+            const int rr = r0 + r;
+            uint8_t* dst = sKV + (c >> 3) * C::BOX + rr * 128 + (((c & 7) ^ (rr & 7)) << 4);
+            if (a) cp_async16(dst, reinterpret_cast<const uint8_t*>(a) + c * 16);
+            else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+        }
+    } else {
+        // mixed storage: a 16-byte bf16 piece c of a compressed row is 8 codes (piece c <
+        // ncp) dequantized here, or a piece of its bf16 RoPE part; every load of the warp's
+        // 16 rows is issued (codes into registers) before the first is converted
+        constexpr int kPer = 16 * C::U / 32;                     // pieces per lane
+        const int ncp = p.nope_dim / 8;
+        const int rope_b = (D - p.nope_dim) * 2;                 // bytes of a RoPE part
+        uint2 code[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int i = lane + 32 * k;
+            const int r = i / C::U, c = i - r * C::U;
+            const unsigned long long a = __shfl_sync(0xffffffffu, src, r);
+            const long long en = __shfl_sync(0xffffffffu, ent, r);
+            const int rr = r0 + r;
+            uint8_t* dst = sKV + (c >> 3) * C::BOX + rr * 128 + (((c & 7) ^ (rr & 7)) << 4);
+            code[k] = make_uint2(0u, 0u);
+            if (a) {
+                cp_async16(dst, reinterpret_cast<const uint8_t*>(a) + c * 16);
+            } else if (en >= 0) {
+                if (c < ncp)
+                    code[k] = __ldg(reinterpret_cast<const uint2*>(p.kv_nope + static_cast<size_t>(en) * p.nope_dim) + c);
+                else
+                    cp_async16(dst, reinterpret_cast<const uint8_t*>(p.kv_rope) + static_cast<size_t>(en) * rope_b +
+                                        (c - ncp) * 16);
+            } else {
+                *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int i = lane + 32 * k;
+            const int r = i / C::U, c = i - r * C::U;
+            const long long en = __shfl_sync(0xffffffffu, ent, r);
+            const float sc = __shfl_sync(0xffffffffu, escale, r);
+            if (en >= 0 && c < ncp) {                            // (a compressed row)
+                // channel = bf16( fp32(E4M3 code) * scale ): codes in byte order
+                uint32_t o[4];
+                const uint32_t w2[2] = {code[k].x, code[k].y};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const __nv_fp8x2_storage_t pr =
+                        static_cast<__nv_fp8x2_storage_t>((w2[h >> 1] >> (16 * (h & 1))) & 0xFFFFu);
+                    const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3)));
+                    o[h] = pack_bf16(f.x * sc, f.y * sc);
+                }
+                const int rr = r0 + r;
+                uint8_t* dst = sKV + (c >> 3) * C::BOX + rr * 128 + (((c & 7) ^ (rr & 7)) << 4);
+                *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        }
+    }
+}
+
 template <int D, int NH>
 __global__ void __launch_bounds__(kFT, 1)
 attn_decode_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap gmap,
@@ -279,99 +384,7 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
     pdl_wait();                      // the index list comes from the kernel before
     if (hgrp == 0 && chunk == 0 && tid == 0)                         // report a bad count once
         row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, row, p.eword);
-    // ---- gather: warp w copies slots [16w, 16w + 16) of the chunk; lanes 0..15 resolve them
-    {
-        const int r0 = warp * 16;
-        unsigned long long src = 0;                                  // bf16 row; 0: none
-        long long ent = -1;                                          // mixed storage: entry row
-        float escale = 0.f;
-        if (lane < 16) {
-            const int slot = chunk * kFC + r0 + lane;
-            if (slot < p.top_k) {
-                int e;
-                if (p.idx) {
-                    e = p.idx[static_cast<size_t>(row) * p.top_k + slot];
-                    if (e >= nv) { flag_error(p.eword, DSV4_EWORD_BAD_INDEX); e = -1; }
-                } else {
-                    e = slot < nv ? slot : -1;
-                }
-                if (e >= 0) {
-                    if (p.kv_nope) {
-                        ent = static_cast<long long>(b) * p.max_comp + e;
-                        escale = __ldg(&p.kv_scale[ent]);
-                    } else {
-                        src = reinterpret_cast<unsigned long long>(comp_kv + (static_cast<size_t>(b) * p.max_comp + e) * D);
-                    }
-                }
-            } else if (slot < p.slots) {
-                const int wi = slot - p.top_k;
-                if (wi < w_cnt)
-                    src = reinterpret_cast<unsigned long long>(win + (static_cast<size_t>(b) * p.win_rows + w_lo + wi) * D);
-            }
-            okf[r0 + lane] = src != 0 || ent >= 0;
-        }
-        if (!p.kv_nope) {
-            for (int i = lane; i < 16 * C::U; i += 32) {
-                const int r = i / C::U, c = i - r * C::U;
-                const unsigned long long a = __shfl_sync(0xffffffffu, src, r);
-                const int rr = r0 + r;
-                uint8_t* dst = sKV + (c >> 3) * C::BOX + rr * 128 + (((c & 7) ^ (rr & 7)) << 4);
-                if (a) cp_async16(dst, reinterpret_cast<const uint8_t*>(a) + c * 16);
-                else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
-            }
-        } else {
-            // mixed storage: a 16-byte bf16 piece c of a compressed row is 8 codes (piece c <
-            // ncp) dequantized here, or a piece of its bf16 RoPE part; every load of the warp's
-            // 16 rows is issued (codes into registers) before the first is converted
-            constexpr int kPer = 16 * C::U / 32;                     // pieces per lane
-            const int ncp = p.nope_dim / 8;
-            const int rope_b = (D - p.nope_dim) * 2;                 // bytes of a RoPE part
-            uint2 code[kPer];
-#pragma unroll
-            for (int k = 0; k < kPer; ++k) {
-                const int i = lane + 32 * k;
-                const int r = i / C::U, c = i - r * C::U;
-                const unsigned long long a = __shfl_sync(0xffffffffu, src, r);
-                const long long en = __shfl_sync(0xffffffffu, ent, r);
-                const int rr = r0 + r;
-                uint8_t* dst = sKV + (c >> 3) * C::BOX + rr * 128 + (((c & 7) ^ (rr & 7)) << 4);
-                code[k] = make_uint2(0u, 0u);
-                if (a) {
-                    cp_async16(dst, reinterpret_cast<const uint8_t*>(a) + c * 16);
-                } else if (en >= 0) {
-                    if (c < ncp)
-                        code[k] = __ldg(reinterpret_cast<const uint2*>(p.kv_nope + static_cast<size_t>(en) * p.nope_dim) + c);
-                    else
-                        cp_async16(dst, reinterpret_cast<const uint8_t*>(p.kv_rope) + static_cast<size_t>(en) * rope_b +
-                                            (c - ncp) * 16);
-                } else {
-                    *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
-                }
-            }
-#pragma unroll
-            for (int k = 0; k < kPer; ++k) {
-                const int i = lane + 32 * k;
-                const int r = i / C::U, c = i - r * C::U;
-                const long long en = __shfl_sync(0xffffffffu, ent, r);
-                const float sc = __shfl_sync(0xffffffffu, escale, r);
-                if (en >= 0 && c < ncp) {                            // (a compressed row)
-                    // channel = bf16( fp32(E4M3 code) * scale ): codes in byte order
-                    uint32_t o[4];
-                    const uint32_t w2[2] = {code[k].x, code[k].y};
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        const __nv_fp8x2_storage_t pr =
-                            static_cast<__nv_fp8x2_storage_t>((w2[h >> 1] >> (16 * (h & 1))) & 0xFFFFu);
-                        const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3)));
-                        o[h] = pack_bf16(f.x * sc, f.y * sc);
-                    }
-                    const int rr = r0 + r;
-                    uint8_t* dst = sKV + (c >> 3) * C::BOX + rr * 128 + (((c & 7) ^ (rr & 7)) << 4);
-                    *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
-                }
-            }
-        }
-    }
+    gather_chunk<D, NH>(p, comp_kv, win, sKV, okf, chunk, row, b, nv, w_lo, w_cnt, warp, lane);
     cp_async_wait_all();
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
@@ -501,7 +514,257 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
     }
 }
 
-struct DecodePlan { int n_chunks, nh, n_hg; };
+// ------------------------------------------------------------------ many query rows: one CTA walks a row
+// When the (query row, head group) pairs alone fill the GPU twice over, splitting rows into
+// chunks only adds partials: one CTA per (query row, head group), the groups of a row side by
+// side, then walks the row's chunks in order with the same gather, S^T and O^T steps, keeps
+// each head's running maximum and sum (online softmax: the running O is scaled by
+// e^(m_old - m_new) before the chunk's O is added), holds the running O^T in registers (each
+// thread its dims for half of the group's heads), and at the end adds the sink once and
+// writes the normalised output. The next chunk's gather starts as soon as the O^T MMA has
+// read the tile, ahead of the O^T read-out.
+template <int D, int NH>
+__global__ void __launch_bounds__(kFT, 1)
+attn_rows_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap gmap,
+                 AttnParams p, const __nv_bfloat16* __restrict__ comp_kv,
+                 const __nv_bfloat16* __restrict__ win, int write_gather) {
+    using C = FCfg<D, NH>;
+    constexpr int HC = NH / 2;                                       // TMEM columns per warp
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint32_t tmem_slot;
+    __shared__ volatile int abort_flag;
+    __shared__ float s_fac[NH];      // per head: e^(m_old - m_new) of a chunk; at the end 1 / den
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* sm = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    uint8_t* sKV = sm;
+    uint8_t* sQ = sm + C::OFF_Q;
+    uint8_t* sP = sm + C::OFF_P;
+    float* sS = reinterpret_cast<float*>(sm + C::OFF_S);
+    float* red_m = reinterpret_cast<float*>(sm + C::OFF_R);
+    float* red_l = red_m + 8 * NH;
+    int* okf = reinterpret_cast<int*>(sm + C::OFF_OK);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);   // q loaded, S done, O done
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int hgrp = static_cast<int>(blockIdx.x % p.n_hg), row = static_cast<int>(blockIdx.x / p.n_hg);
+    const int hbase = hgrp * NH;
+    const int Hc = p.H - hbase < NH ? p.H - hbase : NH;
+    const int b = row / p.n_q, t = row - b * p.n_q;
+    pdl_trigger();
+    const int nv = row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, row, nullptr);
+    int wl = p.win_len[b];
+    wl = wl < 0 ? 0 : (wl > p.win_rows ? p.win_rows : wl);
+    const int w_hi = t + wl - p.n_q;                                 // the query's own window row
+    const int w_lo = w_hi - p.window + 1 > 0 ? w_hi - p.window + 1 : 0;
+    const int w_top = w_hi < wl - 1 ? w_hi : wl - 1;
+    const int w_cnt = w_top >= w_lo ? w_top - w_lo + 1 : 0;
+
+    for (int i = tid; i < C::NBOX * (NH - Hc) * 8; i += kFT) {       // query rows past the heads
+        const int box = i / ((NH - Hc) * 8), rem = i - box * (NH - Hc) * 8;
+        *reinterpret_cast<uint4*>(sQ + box * NH * 128 + (Hc + rem / 8) * 128 + (rem & 7) * 16) =
+            make_uint4(0, 0, 0, 0);
+    }
+    if (tid == 0) {
+        for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0) tmem_alloc(&tmem_slot, C::TCOLS);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    if (tid == 0) {
+        tma_prefetch_desc(&gmap);
+        mbar_arrive_expect_tx(&bars[0], static_cast<uint32_t>(Hc) * D * 2);
+        for (int box = 0; box < C::NBOX; ++box)
+            tma_load_2d(sQ + box * NH * 128, &qmap, &bars[0], box * 64, row * p.H + hbase);
+    }
+
+    pdl_wait();                      // the index lists come from the kernel before
+    if (hgrp == 0 && tid == 0) row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, row, p.eword);
+
+    const int q4 = warp & 3, half = warp >> 2;   // TMEM lane quarter, half of the head columns
+    float acc[C::MT][HC];                         // running O^T: dims mt*128 + 32*q4 + lane
+#pragma unroll
+    for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+        for (int c = 0; c < HC; ++c) acc[mt][c] = 0.f;
+    float m_run = -INFINITY, l_run = 0.f;         // lanes < NH: head `lane` (every warp alike)
+    bool dead = false;
+    gather_chunk<D, NH>(p, comp_kv, win, sKV, okf, 0, row, b, nv, w_lo, w_cnt, warp, lane);
+    for (int chunk = 0; chunk < p.n_chunks; ++chunk) {
+        const uint32_t ph = static_cast<uint32_t>(chunk & 1);
+        cp_async_wait_all();
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            if (write_gather && hgrp == 0) {
+                for (int box = 0; box < C::NBOX; ++box)
+                    tma_store_3d(&gmap, sKV + box * C::BOX, box * 64, chunk * kFC, row);
+                bulk_commit();
+            }
+            if (!dead && chunk == 0 && !mbar_wait(&bars[0], 0, nullptr)) dead = true;
+            if (!dead) {                            // S^T = KV Q^T
+                tc_fence_after();
+                const uint32_t idesc = idesc_bf16_f32(kFC, NH);
+                const uint32_t a0 = smem_u32(sKV), b0 = smem_u32(sQ);
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k)
+                    umma_bf16(tmem, sdesc_kmajor_sw128(a0 + (k >> 2) * C::BOX + (k & 3) * 32),
+                              sdesc_kmajor_sw128(b0 + (k >> 2) * NH * 128 + (k & 3) * 32), idesc, k > 0 ? 1u : 0u);
+                umma_commit(&bars[1]);
+            } else if (!abort_flag) {
+                flag_error(p.eword, DSV4_EWORD_TIMEOUT);
+                abort_flag = 1;
+            }
+        }
+        if (!dead && !mbar_wait(&bars[1], ph, &abort_flag)) {
+            dead = true;
+            if (tid == 0) { flag_error(p.eword, DSV4_EWORD_TIMEOUT); abort_flag = 1; }
+        }
+        tc_fence_after();
+        {                                            // scores -> shared (scaled, masked)
+            const int key = q4 * 32 + lane;
+            uint32_t r[HC];
+            tmem_ld_cols<HC>(tmem + (static_cast<uint32_t>(q4 * 32) << 16) + static_cast<uint32_t>(half * HC), r);
+            tmem_wait_ld();
+            const bool ok = okf[key] != 0 && !dead;
+#pragma unroll
+            for (int c = 0; c < HC; ++c)
+                sS[key * (NH + 1) + half * HC + c] = ok ? __uint_as_float(r[c]) * p.scale : -INFINITY;
+        }
+        __syncthreads();
+        float sv[16];
+        float mx = -INFINITY;
+        if (lane < NH) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                sv[i] = sS[(16 * warp + i) * (NH + 1) + lane];
+                mx = fmaxf(mx, sv[i]);
+            }
+            red_m[warp * NH + lane] = mx;
+        }
+        __syncthreads();
+        float fac = 0.f;
+        if (lane < NH) {
+            float m_new = m_run;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) m_new = fmaxf(m_new, red_m[j * NH + lane]);
+            float l = 0.f;
+            uint32_t pk[8];
+#pragma unroll
+            for (int i = 0; i < 16; i += 2) {
+                const float p0 = sv[i] == -INFINITY ? 0.f : expf(sv[i] - m_new);
+                const float p1 = sv[i + 1] == -INFINITY ? 0.f : expf(sv[i + 1] - m_new);
+                l += p0 + p1;
+                pk[i / 2] = pack_bf16(p0, p1);
+            }
+            red_l[warp * NH + lane] = l;
+            uint8_t* prow = sP + (warp >> 2) * (NH * 128) + lane * 128;
+            const int c0 = 2 * (warp & 3);
+            *reinterpret_cast<uint4*>(prow + ((c0 ^ (lane & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            *reinterpret_cast<uint4*>(prow + (((c0 + 1) ^ (lane & 7)) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            fac = m_run == -INFINITY ? 0.f : expf(m_run - m_new);
+            if (warp == 0) s_fac[lane] = fac;
+            m_run = m_new;
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0 && !dead) {                     // O^T = V^T P^T into fresh accumulators
+            tc_fence_after();
+            const uint32_t idesc = idesc_bf16_f32(kFC, NH) | (1u << 15);
+            const uint32_t a0 = smem_u32(sKV), b0 = smem_u32(sP);
+#pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt) {
+#pragma unroll
+                for (int kk = 0; kk < kFC / 16; ++kk)
+                    umma_bf16(tmem + static_cast<uint32_t>(NH + mt * NH),
+                              sdesc_mnmajor_sw128(a0 + (2 * mt) * C::BOX + kk * 2048, static_cast<uint32_t>(C::BOX), 1024u),
+                              sdesc_kmajor_sw128(b0 + (kk >> 2) * NH * 128 + (kk & 3) * 32), idesc, kk > 0 ? 1u : 0u);
+            }
+            umma_commit(&bars[2]);
+        }
+        if (warp == 0 && lane < NH) {
+            float l = 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) l += red_l[j * NH + lane];
+            l_run = l_run * fac + l;
+        }
+        if (!dead && !mbar_wait(&bars[2], ph, &abort_flag)) {
+            dead = true;
+            if (tid == 0) { flag_error(p.eword, DSV4_EWORD_TIMEOUT); abort_flag = 1; }
+        }
+        tc_fence_after();
+        // the tile is read: the next chunk's rows go in while this chunk's O^T is read out
+        if (chunk + 1 < p.n_chunks) {
+            if (write_gather && hgrp == 0) {
+                if (tid == 0) bulk_wait_read();      // the gather buffer's copy of the tile
+                __syncthreads();
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            gather_chunk<D, NH>(p, comp_kv, win, sKV, okf, chunk + 1, row, b, nv, w_lo, w_cnt, warp, lane);
+        }
+        {
+            uint32_t r[C::MT][HC];
+#pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt)
+                tmem_ld_cols<HC>(tmem + (static_cast<uint32_t>(q4 * 32) << 16) +
+                                     static_cast<uint32_t>(NH + mt * NH + half * HC), r[mt]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < HC; ++c) {
+                const float f = s_fac[half * HC + c];
+#pragma unroll
+                for (int mt = 0; mt < C::MT; ++mt)
+                    acc[mt][c] = fmaf(acc[mt][c], f, dead ? 0.f : __uint_as_float(r[mt][c]));
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0 && lane < NH) {                    // the sink once, and 1 / denominator
+        const float snk = lane < Hc ? p.sink[hbase + lane] : 0.f;
+        const float M = fmaxf(m_run, snk);
+        const float e = m_run == -INFINITY ? 0.f : expf(m_run - M);
+        s_fac[lane] = e / fmaf(l_run, e, expf(snk - M));
+    }
+    __syncthreads();
+    {
+        __nv_bfloat16* po = p.out + (static_cast<size_t>(row) * p.H + hbase) * D;
+#pragma unroll
+        for (int c = 0; c < HC; ++c) {
+            const int h = half * HC + c;
+            const float f = s_fac[h];
+#pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt) {
+                const int dim = mt * 128 + q4 * 32 + lane;
+                float v = dead ? 0.f : acc[mt][c] * f;
+                const float partner = __shfl_xor_sync(0xffffffffu, v, 1);
+                float e = (lane & 1) ? partner : v, o = (lane & 1) ? v : partner;
+                inverse_rope_pair(p, row, dim & ~1, D, e, o);
+                if (!(lane & 1) && h < Hc)
+                    *reinterpret_cast<uint32_t*>(po + static_cast<size_t>(h) * D + dim) = pack_bf16(e, o);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, C::TCOLS);
+    if (tid == 0) {
+        if (write_gather && hgrp == 0) bulk_wait_read();
+        if (abort_flag) mbar_wait(&bars[0], 0, nullptr, 100000000ull);   // the query copy landed
+    }
+}
+
+// (query row, head group) pairs from which one CTA walks each row: two per SM of a 152-SM part
+constexpr long long kRowWalkCtas = 304;
+
+struct DecodePlan { int n_chunks, nh, n_hg; bool walk; };
 
 DecodePlan decode_plan(const dsv4_attn_args& a) {
     DecodePlan d{};
@@ -509,6 +772,7 @@ DecodePlan decode_plan(const dsv4_attn_args& a) {
     d.n_chunks = static_cast<int>((slots + kFC - 1) / kFC);
     d.nh = a.heads % 32 == 0 ? 32 : 16;          // every group full, or one group of <= 16
     d.n_hg = (a.heads + d.nh - 1) / d.nh;
+    d.walk = static_cast<long long>(a.batch) * a.n_q * d.n_hg >= kRowWalkCtas;
     return d;
 }
 
@@ -561,7 +825,17 @@ int run_decode(const dsv4_attn_args& a, const DecodePlan& dp, uint8_t* ws, uint3
     if (!attr_set) {
         cudaFuncSetAttribute(attn_decode_kernel<D, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(C::SMEM));
+        cudaFuncSetAttribute(attn_rows_kernel<D, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(C::SMEM));
         attr_set = true;
+    }
+    if (dp.walk) {                                     // one CTA per (query row, head group)
+        count_launch();
+        return launch_k(attn_rows_kernel<D, NH>, dim3(static_cast<unsigned>(rows) * dp.n_hg), dim3(kFT), C::SMEM,
+                        st, true, qmap, gmap, p, static_cast<const __nv_bfloat16*>(a.comp_kv),
+                        static_cast<const __nv_bfloat16*>(a.win), a.gather ? 1 : 0) == cudaSuccess
+                   ? DSV4_OK
+                   : DSV4_ERR_LAUNCH;
     }
     dim3 grid(dp.n_chunks, rows, dp.n_hg);
     count_launch();
@@ -581,6 +855,7 @@ int run_decode(const dsv4_attn_args& a, const DecodePlan& dp, uint8_t* ws, uint3
 
 size_t attn_ws_bytes(const dsv4_attn_args& a) {
     const DecodePlan dp = decode_plan(a);
+    if (dp.walk) return 0;                             // no partials
     const size_t rows = static_cast<size_t>(a.batch) * a.n_q;
     const size_t hs = static_cast<size_t>(dp.n_hg) * dp.nh;
     return align_up(rows * dp.n_chunks * hs * 2 * 4, 256) +

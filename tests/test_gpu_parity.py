@@ -647,7 +647,7 @@ def _mixed_kv(comp_bits, rope_dim=64):
     return (nope, sc, rope), oracle.dequant_kv_mixed(nope, sc, rope)
 
 
-def _run_attn_mixed(x, wl, idx, mixed, top_k=None):
+def _run_attn_mixed(x, wl, idx, mixed, top_k=None, q_pos=None):
     m = csa()
     nope, sc, rope = mixed
     q, sink = dev_bf16(x["q"]), dev(x["sink"])
@@ -657,7 +657,8 @@ def _run_attn_mixed(x, wl, idx, mixed, top_k=None):
     out = torch.empty(B, n_q, H, D, dtype=torch.bfloat16, device="cuda")
     gather = torch.full((B, n_q, top_k + wl.window, D), 7.0, dtype=torch.bfloat16, device="cuda")
     kw = dict(idx=None if idx is None else dev(idx), top_k=top_k, window=wl.window, ratio=wl.ratio,
-              gather=gather, kv_nope=dev(nope), kv_scale=dev(sc), kv_rope=dev_bf16(rope))
+              gather=gather, kv_nope=dev(nope), kv_scale=dev(sc), kv_rope=dev_bf16(rope),
+              q_pos=None if q_pos is None else dev(q_pos))
     ws = ws_tensor(m.dsv4_sparse_attn_workspace_size(q, sink, None, n_comp, win, win_len, out, **kw))
     m.dsv4_sparse_attn_decode(q, sink, None, n_comp, win, win_len, out, ws, **kw)
     torch.cuda.synchronize()
@@ -836,6 +837,91 @@ def test_attention_edge_cases_and_bad_index():
     _, ref2, _ = oracle.sparse_attn(x["q"], x["sink"], x["comp_kv_dev"], x["n_comp"], masked,
                                     x["win"], x["win_len"], k, W, 4)
     assert_bf16_close(got2, ref2, "masked bad index")
+
+
+def _walk_case(seed=41):
+    """Many query rows per sequence (4 x 40 rows x 2 head groups: one CTA walks each row's
+    chunks): ragged causal visibility (n_comp 300, 0, 37, 129 capped by the query positions),
+    windows of 168, 0, 45 and 100 rows, 64 selected slots and 128 window slots per row."""
+    rng = np.random.default_rng(seed)
+    B, n_q, H, D, N, k, W = 4, 40, 64, 512, 300, 64, 128
+    q_pos = (np.array([1160, 0, 100, 400], np.int64)[:, None] + np.arange(n_q, dtype=np.int64)[None, :])
+    x = {"q": synth.f32_to_bf16_bits(rng.standard_normal((B, n_q, H, D)).astype(np.float32)),
+         "sink": rng.standard_normal(H).astype(np.float32),
+         "comp_kv_dev": synth.f32_to_bf16_bits(rng.standard_normal((B, N, D)).astype(np.float32)),
+         "n_comp": np.array([300, 0, 37, 129], np.int32),
+         "win": synth.f32_to_bf16_bits(rng.standard_normal((B, W + n_q, D)).astype(np.float32)),
+         "win_len": np.array([W + n_q, 0, 45, 100], np.int32),
+         "q_pos": q_pos}
+    nvis = np.minimum(x["n_comp"][:, None], (q_pos + 1) // 4).reshape(-1).astype(np.int32)
+    idx = synth.uniform_index_sets(seed, 17, B * n_q, nvis, k).reshape(B, n_q, k)
+
+    class WL:
+        window, ratio = W, 4
+
+    return WL, x, idx, nvis
+
+
+def test_attention_row_walk_edge_cases():
+    """The row-walking kernel: outputs and the gather buffer of every row against the oracle,
+    then an index past a row's visible range (masked, reported as DSV4_EWORD_BAD_INDEX)."""
+    wl, x, idx, nvis = _walk_case()
+    got, gat, ew = _run_attn(x, wl, idx)
+    assert ew == 0
+    _, ref, ref_g = oracle.sparse_attn(x["q"], x["sink"], x["comp_kv_dev"], x["n_comp"], idx, x["win"],
+                                       x["win_len"], 64, wl.window, 4, q_pos=x["q_pos"], want_gather=True)
+    assert np.array_equal(gat, ref_g), "gather buffer differs"
+    assert_bf16_close(got, ref, "row-walk attention")
+    bad = idx.copy()
+    bad[2, 5, 3] = int(nvis[2 * 40 + 5]) + 2             # past that row's visible entries
+    got2, _, ew2 = _run_attn(x, wl, bad, want_gather=False)
+    assert ew2 & csa().DSV4_EWORD_BAD_INDEX
+    masked = bad.copy()
+    masked[2, 5, 3] = -1
+    _, ref2, _ = oracle.sparse_attn(x["q"], x["sink"], x["comp_kv_dev"], x["n_comp"], masked, x["win"],
+                                    x["win_len"], 64, wl.window, 4, q_pos=x["q_pos"])
+    assert_bf16_close(got2, ref2, "row-walk attention, masked bad index")
+
+
+def test_attention_row_walk_mixed_kv():
+    """The row-walking kernel over the mixed FP8 / bf16 storage: the gather buffer holds the
+    oracle's dequantized rows, the output matches the oracle's attention over them."""
+    wl, x, idx, _ = _walk_case(43)
+    mixed, deq = _mixed_kv(x["comp_kv_dev"])
+    got, gat, ew = _run_attn_mixed(x, wl, idx, mixed, q_pos=x["q_pos"])
+    assert ew == 0
+    _, ref, ref_g = oracle.sparse_attn(x["q"], x["sink"], deq, x["n_comp"], idx, x["win"], x["win_len"],
+                                       64, wl.window, 4, q_pos=x["q_pos"], want_gather=True)
+    assert np.array_equal(gat, ref_g), "gather buffer differs"
+    assert_bf16_close(got, ref, "row-walk attention over mixed KV")
+
+
+def test_attention_row_walk_small_heads_inverse_rope():
+    """The row-walking kernel with D = 128 and 8 heads (one group of 16, half empty), 320 query
+    rows, a ragged last chunk (40 + 128 slots), and the output rotated back (each RoPE pair
+    split across neighbouring lanes)."""
+    rng = np.random.default_rng(45)
+    n_q, H, D, N, k, W = 320, 8, 128, 256, 40, 128
+    q_pos = 704 + np.arange(n_q, dtype=np.int64)[None, :]
+    x = {"q": synth.f32_to_bf16_bits(rng.standard_normal((1, n_q, H, D)).astype(np.float32)),
+         "sink": rng.standard_normal(H).astype(np.float32),
+         "comp_kv_dev": synth.f32_to_bf16_bits(rng.standard_normal((1, N, D)).astype(np.float32)),
+         "n_comp": np.array([256], np.int32),
+         "win": synth.f32_to_bf16_bits(rng.standard_normal((1, W + n_q, D)).astype(np.float32)),
+         "win_len": np.array([W + n_q], np.int32), "q_pos": q_pos}
+    nvis = np.minimum(256, (q_pos[0] + 1) // 4).astype(np.int32)
+    idx = synth.uniform_index_sets(45, 17, n_q, nvis, k).reshape(1, n_q, k)
+
+    class WL:
+        window, ratio = W, 4
+
+    got, gat, ew = _run_attn(x, WL, idx, out_rope_pos=q_pos)
+    assert ew == 0
+    _, ref, ref_g = oracle.sparse_attn(x["q"], x["sink"], x["comp_kv_dev"], x["n_comp"], idx, x["win"],
+                                       x["win_len"], k, W, 4, q_pos=q_pos, want_gather=True)
+    assert np.array_equal(gat, ref_g), "gather buffer differs"
+    _, ref_rot = oracle.inverse_rope(ref.reshape(n_q, H, D), q_pos[0], 64)
+    assert_bf16_close(got.reshape(n_q, H, D), ref_rot, "row-walk attention + inverse RoPE, D = 128")
 
 
 # ------------------------------------------------------------------ the fused decode step
