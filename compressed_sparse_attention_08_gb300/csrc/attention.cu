@@ -219,27 +219,37 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[N]) {
     else DSV4_TMEM_LD_32x32b_X32(taddr, r);
 }
 
-// The gather of one chunk: warp w copies slots [16w, 16w + 16) of chunk `chunk` of query row
-// `row` into the shared tile (cp.async for bf16 rows, zero fill for slots without a row; the
-// mixed storage's codes are dequantized here) and marks in okf[] which slots hold a row. Lanes
-// 0..15 resolve the slots; every lane of the CTA must call it (the shuffles take all lanes).
-// The caller waits for the copies (cp_async_wait_all) and fences them for the tensor cores.
-template <int D, int NH>
-__device__ __forceinline__ void gather_chunk(const AttnParams& p, const __nv_bfloat16* __restrict__ comp_kv,
-                                             const __nv_bfloat16* __restrict__ win, uint8_t* sKV, int* okf,
-                                             int chunk, int row, int b, int nv, int w_lo, int w_cnt,
-                                             int warp, int lane) {
-    using C = FCfg<D, NH>;
+// Where one slot's row comes from (lanes 0..15 of warp w hold slots 16w .. 16w + 15 of a chunk).
+struct SlotSrc {
+    unsigned long long src;        // a bf16 row; 0: none
+    long long ent;                 // mixed storage: the entry's row; -1: none
+    float escale;                  // mixed storage: the entry's scale
+    int ok;                        // the slot holds a row
+};
+
+// The index-list entry of this lane's slot of chunk `chunk` (lanes 0..15; -1 elsewhere), loaded
+// on its own so that the load can be issued well before its use.
+__device__ __forceinline__ int load_slot_index(const AttnParams& p, int chunk, int row, int warp, int lane) {
+    const int slot = chunk * kFC + warp * 16 + lane;
+    return lane < 16 && p.idx && slot < p.top_k ? p.idx[static_cast<size_t>(row) * p.top_k + slot] : -1;
+}
+
+// Resolves the slots of chunk `chunk` of query row `row` from their index-list entries (or the
+// dense count): the visible range (an index past it is reported and masked), the window rows.
+template <int D>
+__device__ __forceinline__ SlotSrc resolve_slots(const AttnParams& p, const __nv_bfloat16* __restrict__ comp_kv,
+                                                 const __nv_bfloat16* __restrict__ win, int e_list, int chunk,
+                                                 int b, int nv, int w_lo, int w_cnt, int warp, int lane) {
     const int r0 = warp * 16;
-    unsigned long long src = 0;                                  // bf16 row; 0: none
-    long long ent = -1;                                          // mixed storage: entry row
+    unsigned long long src = 0;
+    long long ent = -1;
     float escale = 0.f;
     if (lane < 16) {
         const int slot = chunk * kFC + r0 + lane;
         if (slot < p.top_k) {
             int e;
             if (p.idx) {
-                e = p.idx[static_cast<size_t>(row) * p.top_k + slot];
+                e = e_list;
                 if (e >= nv) { flag_error(p.eword, DSV4_EWORD_BAD_INDEX); e = -1; }
             } else {
                 e = slot < nv ? slot : -1;
@@ -257,8 +267,24 @@ __device__ __forceinline__ void gather_chunk(const AttnParams& p, const __nv_bfl
             if (wi < w_cnt)
                 src = reinterpret_cast<unsigned long long>(win + (static_cast<size_t>(b) * p.win_rows + w_lo + wi) * D);
         }
-        okf[r0 + lane] = src != 0 || ent >= 0;
     }
+    return SlotSrc{src, ent, escale, src != 0 || ent >= 0};
+}
+
+// The gather of one chunk: warp w copies its 16 resolved slots into the shared tile (cp.async
+// for bf16 rows, zero fill for slots without a row; the mixed storage's codes are dequantized
+// here) and marks in okf[] which slots hold a row. Every lane of the CTA must call it (the
+// shuffles take all lanes). The caller waits for the copies (cp_async_wait_all) and fences
+// them for the tensor cores.
+template <int D, int NH>
+__device__ __forceinline__ void copy_slots(const AttnParams& p, const SlotSrc& s, uint8_t* sKV, int* okf,
+                                           int warp, int lane) {
+    using C = FCfg<D, NH>;
+    const int r0 = warp * 16;
+    const unsigned long long src = s.src;
+    const long long ent = s.ent;
+    const float escale = s.escale;
+    if (lane < 16) okf[r0 + lane] = s.ok;
     if (!p.kv_nope) {
         for (int i = lane; i < 16 * C::U; i += 32) {
             const int r = i / C::U, c = i - r * C::U;
@@ -320,6 +346,16 @@ __device__ __forceinline__ void gather_chunk(const AttnParams& p, const __nv_bfl
             }
         }
     }
+}
+
+template <int D, int NH>
+__device__ __forceinline__ void gather_chunk(const AttnParams& p, const __nv_bfloat16* __restrict__ comp_kv,
+                                             const __nv_bfloat16* __restrict__ win, uint8_t* sKV, int* okf,
+                                             int chunk, int row, int b, int nv, int w_lo, int w_cnt,
+                                             int warp, int lane) {
+    const int e = load_slot_index(p, chunk, row, warp, lane);
+    copy_slots<D, NH>(p, resolve_slots<D>(p, comp_kv, win, e, chunk, b, nv, w_lo, w_cnt, warp, lane), sKV, okf,
+                      warp, lane);
 }
 
 template <int D, int NH>
@@ -521,8 +557,9 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
 // each head's running maximum and sum (online softmax: the running O is scaled by
 // e^(m_old - m_new) before the chunk's O is added), holds the running O^T in registers (each
 // thread its dims for half of the group's heads), and at the end adds the sink once and
-// writes the normalised output. The next chunk's gather starts as soon as the O^T MMA has
-// read the tile, ahead of the O^T read-out.
+// writes the normalised output (through shared memory, in whole rows). The next chunk's
+// gather starts as soon as the O^T MMA has read the tile (its index entries were loaded a
+// chunk earlier), and a chunk's O^T is read out of TMEM while the next chunk's S^T MMA runs.
 template <int D, int NH>
 __global__ void __launch_bounds__(kFT, 1)
 attn_rows_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap gmap,
@@ -530,6 +567,7 @@ attn_rows_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                  const __nv_bfloat16* __restrict__ win, int write_gather) {
     using C = FCfg<D, NH>;
     constexpr int HC = NH / 2;                                       // TMEM columns per warp
+    static_assert(NH * D * 4 <= C::BOX * C::NBOX, "the fp32 output fits in the tile");
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
@@ -594,12 +632,31 @@ attn_rows_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     float m_run = -INFINITY, l_run = 0.f;         // lanes < NH: head `lane` (every warp alike)
     bool dead = false;
     gather_chunk<D, NH>(p, comp_kv, win, sKV, okf, 0, row, b, nv, w_lo, w_cnt, warp, lane);
+    int next_e = -1;                                 // the next chunk's index entry, loaded a chunk ahead
+    // running O^T = running O^T * e^(m_old - m_new) + the last chunk's O^T (TMEM columns NH..)
+    auto add_chunk_o = [&]() {
+        tc_fence_after();
+        uint32_t r[C::MT][HC];
+#pragma unroll
+        for (int mt = 0; mt < C::MT; ++mt)
+            tmem_ld_cols<HC>(tmem + (static_cast<uint32_t>(q4 * 32) << 16) +
+                                 static_cast<uint32_t>(NH + mt * NH + half * HC), r[mt]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < HC; ++c) {
+            const float f = s_fac[half * HC + c];
+#pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt)
+                acc[mt][c] = fmaf(acc[mt][c], f, dead ? 0.f : __uint_as_float(r[mt][c]));
+        }
+    };
     for (int chunk = 0; chunk < p.n_chunks; ++chunk) {
         const uint32_t ph = static_cast<uint32_t>(chunk & 1);
         cp_async_wait_all();
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tc_fence_before();
         __syncthreads();
+        if (chunk + 1 < p.n_chunks) next_e = load_slot_index(p, chunk + 1, row, warp, lane);
         if (tid == 0) {
             if (write_gather && hgrp == 0) {
                 for (int box = 0; box < C::NBOX; ++box)
@@ -621,6 +678,7 @@ attn_rows_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                 abort_flag = 1;
             }
         }
+        if (chunk > 0) add_chunk_o();                // the previous chunk's O^T, while S^T runs
         if (!dead && !mbar_wait(&bars[1], ph, &abort_flag)) {
             dead = true;
             if (tid == 0) { flag_error(p.eword, DSV4_EWORD_TIMEOUT); abort_flag = 1; }
@@ -699,31 +757,18 @@ attn_rows_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
             if (tid == 0) { flag_error(p.eword, DSV4_EWORD_TIMEOUT); abort_flag = 1; }
         }
         tc_fence_after();
-        // the tile is read: the next chunk's rows go in while this chunk's O^T is read out
+        // the tile is read: the next chunk's rows go in (its S^T then runs beside this O^T's read-out)
         if (chunk + 1 < p.n_chunks) {
             if (write_gather && hgrp == 0) {
                 if (tid == 0) bulk_wait_read();      // the gather buffer's copy of the tile
                 __syncthreads();
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            gather_chunk<D, NH>(p, comp_kv, win, sKV, okf, chunk + 1, row, b, nv, w_lo, w_cnt, warp, lane);
-        }
-        {
-            uint32_t r[C::MT][HC];
-#pragma unroll
-            for (int mt = 0; mt < C::MT; ++mt)
-                tmem_ld_cols<HC>(tmem + (static_cast<uint32_t>(q4 * 32) << 16) +
-                                     static_cast<uint32_t>(NH + mt * NH + half * HC), r[mt]);
-            tmem_wait_ld();
-#pragma unroll
-            for (int c = 0; c < HC; ++c) {
-                const float f = s_fac[half * HC + c];
-#pragma unroll
-                for (int mt = 0; mt < C::MT; ++mt)
-                    acc[mt][c] = fmaf(acc[mt][c], f, dead ? 0.f : __uint_as_float(r[mt][c]));
-            }
+            copy_slots<D, NH>(p, resolve_slots<D>(p, comp_kv, win, next_e, chunk + 1, b, nv, w_lo, w_cnt, warp, lane),
+                              sKV, okf, warp, lane);
         }
     }
+    if (p.n_chunks > 0) add_chunk_o();
     tc_fence_before();
     __syncthreads();
     if (warp == 0 && lane < NH) {                    // the sink once, and 1 / denominator
@@ -732,23 +777,32 @@ attn_rows_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         const float e = m_run == -INFINITY ? 0.f : expf(m_run - M);
         s_fac[lane] = e / fmaf(l_run, e, expf(snk - M));
     }
+    if (tid == 0 && write_gather && hgrp == 0) bulk_wait_read();   // the tile's last copy out
+    __syncthreads();
+    // the normalised output goes through the (free) tile as fp32 [NH heads][D], then out in
+    // 16-byte pieces of whole head rows, each piece's RoPE pairs rotated back in the thread
+    float* sO = reinterpret_cast<float*>(sKV);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+#pragma unroll
+    for (int c = 0; c < HC; ++c) {
+        const int h = half * HC + c;
+        const float f = s_fac[h];
+#pragma unroll
+        for (int mt = 0; mt < C::MT; ++mt)
+            sO[h * D + mt * 128 + q4 * 32 + lane] = dead ? 0.f : acc[mt][c] * f;
+    }
     __syncthreads();
     {
         __nv_bfloat16* po = p.out + (static_cast<size_t>(row) * p.H + hbase) * D;
+        for (int i = tid; i < Hc * (D / 8); i += kFT) {
+            const int h = i / (D / 8), k = i - h * (D / 8);
+            const float4 u0 = *reinterpret_cast<const float4*>(sO + h * D + k * 8);
+            const float4 u1 = *reinterpret_cast<const float4*>(sO + h * D + k * 8 + 4);
+            float v[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
-        for (int c = 0; c < HC; ++c) {
-            const int h = half * HC + c;
-            const float f = s_fac[h];
-#pragma unroll
-            for (int mt = 0; mt < C::MT; ++mt) {
-                const int dim = mt * 128 + q4 * 32 + lane;
-                float v = dead ? 0.f : acc[mt][c] * f;
-                const float partner = __shfl_xor_sync(0xffffffffu, v, 1);
-                float e = (lane & 1) ? partner : v, o = (lane & 1) ? v : partner;
-                inverse_rope_pair(p, row, dim & ~1, D, e, o);
-                if (!(lane & 1) && h < Hc)
-                    *reinterpret_cast<uint32_t*>(po + static_cast<size_t>(h) * D + dim) = pack_bf16(e, o);
-            }
+            for (int j = 0; j < 4; ++j) inverse_rope_pair(p, row, k * 8 + 2 * j, D, v[2 * j], v[2 * j + 1]);
+            *reinterpret_cast<uint4*>(po + static_cast<size_t>(h) * D + k * 8) =
+                make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
         }
     }
     tc_fence_before();
