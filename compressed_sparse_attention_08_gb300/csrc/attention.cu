@@ -169,11 +169,15 @@ attn_combine_kernel(AttnParams p) {
         }
         *dst = __float2bfloat16_rn(acc[0]);
     } else {
+        // the thread's PER channels in one store (a warp writes one contiguous piece)
+        uint32_t pk[PER / 2];
 #pragma unroll
         for (int j = 0; j < PER; j += 2) {
             inverse_rope_pair(p, row, tid * PER + j, D, acc[j], acc[j + 1]);
-            *reinterpret_cast<uint32_t*>(dst + j) = pack_bf16(acc[j], acc[j + 1]);
+            pk[j / 2] = pack_bf16(acc[j], acc[j + 1]);
         }
+        if constexpr (PER == 4) *reinterpret_cast<uint2*>(dst) = make_uint2(pk[0], pk[1]);
+        else *reinterpret_cast<uint32_t*>(dst) = pk[0];
     }
 }
 
