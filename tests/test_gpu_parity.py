@@ -924,6 +924,43 @@ def test_attention_row_walk_small_heads_inverse_rope():
     assert_bf16_close(got.reshape(n_q, H, D), ref_rot, "row-walk attention + inverse RoPE, D = 128")
 
 
+@pytest.mark.parametrize("form", ["split", "walk", "walk_mixed"])
+def test_attention_d256_three_head_groups(form):
+    """D = 256 and 48 heads (three groups of 16), a 64-row window, ragged visibility: decode
+    (one CTA per chunk, partials and combine; 3 query rows) and many query rows (one CTA walks
+    each row; 2 x 60 rows), the latter also over the mixed FP8 / bf16 storage."""
+    rng = np.random.default_rng({"split": 51, "walk": 52, "walk_mixed": 53}[form])
+    H, D, N, k, W = 48, 256, 200, 48, 64
+    B, n_q = (3, 1) if form == "split" else (2, 60)
+    x = {"q": synth.f32_to_bf16_bits(rng.standard_normal((B, n_q, H, D)).astype(np.float32)),
+         "sink": rng.standard_normal(H).astype(np.float32),
+         "comp_kv_dev": synth.f32_to_bf16_bits(rng.standard_normal((B, N, D)).astype(np.float32)),
+         "n_comp": np.array([200, 31, 120][:B], np.int32),
+         "win": synth.f32_to_bf16_bits(rng.standard_normal((B, W + n_q, D)).astype(np.float32)),
+         "win_len": np.array([W + n_q, 20, 50][:B], np.int32)}
+    if n_q > 1:
+        x["q_pos"] = np.array([700, 90], np.int64)[:, None] + np.arange(n_q, dtype=np.int64)[None, :]
+        nvis = np.minimum(x["n_comp"][:, None], (x["q_pos"] + 1) // 4).reshape(-1).astype(np.int32)
+    else:
+        nvis = x["n_comp"]
+    idx = synth.uniform_index_sets(54, 17, B * n_q, nvis, k).reshape(B, n_q, k)
+
+    class WL:
+        window, ratio = W, 4
+
+    kv = x["comp_kv_dev"]
+    if form == "walk_mixed":
+        mixed, kv = _mixed_kv(x["comp_kv_dev"])
+        got, gat, ew = _run_attn_mixed(x, WL, idx, mixed, q_pos=x["q_pos"])
+    else:
+        got, gat, ew = _run_attn(x, WL, idx)
+    assert ew == 0
+    _, ref, ref_g = oracle.sparse_attn(x["q"], x["sink"], kv, x["n_comp"], idx, x["win"], x["win_len"], k, W, 4,
+                                       q_pos=x.get("q_pos"), want_gather=True)
+    assert np.array_equal(gat, ref_g), "gather buffer differs"
+    assert_bf16_close(got, ref, f"D = 256, 48 heads ({form})")
+
+
 # ------------------------------------------------------------------ the fused decode step
 def _fused_step(x, wl, graph=False, fp8=False, mixed=False):
     """Compress (whole context) + indexer top-k + gather/attention in one dsv4_csa_decode.
