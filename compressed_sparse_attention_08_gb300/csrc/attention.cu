@@ -290,13 +290,23 @@ __device__ __forceinline__ void copy_slots(const AttnParams& p, const SlotSrc& s
     const float escale = s.escale;
     if (lane < 16) okf[r0 + lane] = s.ok;
     if (!p.kv_nope) {
-        for (int i = lane; i < 16 * C::U; i += 32) {
-            const int r = i / C::U, c = i - r * C::U;
-            const unsigned long long a = __shfl_sync(0xffffffffu, src, r);
-            const int rr = r0 + r;
-            uint8_t* dst = sKV + (c >> 3) * C::BOX + rr * 128 + (((c & 7) ^ (rr & 7)) << 4);
-            if (a) cp_async16(dst, reinterpret_cast<const uint8_t*>(a) + c * 16);
-            else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+        // one shuffle of a row's source per pass, U / 32 pieces per lane (D = 512: 2), or
+        // 32 / U rows per pass when a row has fewer than 32 pieces
+        constexpr int RPI = C::U >= 32 ? 1 : 32 / C::U;
+        constexpr int PPL = C::U >= 32 ? C::U / 32 : 1;
+        const int sub = C::U >= 32 ? 0 : lane / C::U;
+        const int c0 = C::U >= 32 ? lane : lane - sub * C::U;
+#pragma unroll 4
+        for (int r = 0; r < 16; r += RPI) {
+            const unsigned long long a = __shfl_sync(0xffffffffu, src, r + sub);
+            const int rr = r0 + r + sub;
+#pragma unroll
+            for (int j = 0; j < PPL; ++j) {
+                const int c = c0 + 32 * j;
+                uint8_t* dst = sKV + (c >> 3) * C::BOX + rr * 128 + (((c & 7) ^ (rr & 7)) << 4);
+                if (a) cp_async16(dst, reinterpret_cast<const uint8_t*>(a) + c * 16);
+                else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+            }
         }
     } else {
         // mixed storage: a 16-byte bf16 piece c of a compressed row is 8 codes (piece c <
