@@ -289,13 +289,13 @@ __device__ __forceinline__ void copy_slots(const AttnParams& p, const SlotSrc& s
     const long long ent = s.ent;
     const float escale = s.escale;
     if (lane < 16) okf[r0 + lane] = s.ok;
+    // one shuffle of a row's source per pass, U / 32 pieces per lane (D = 512: 2), or 32 / U
+    // rows per pass when a row has fewer than 32 pieces
+    constexpr int RPI = C::U >= 32 ? 1 : 32 / C::U;
+    constexpr int PPL = C::U >= 32 ? C::U / 32 : 1;
+    const int sub = C::U >= 32 ? 0 : lane / C::U;
+    const int c0 = C::U >= 32 ? lane : lane - sub * C::U;
     if (!p.kv_nope) {
-        // one shuffle of a row's source per pass, U / 32 pieces per lane (D = 512: 2), or
-        // 32 / U rows per pass when a row has fewer than 32 pieces
-        constexpr int RPI = C::U >= 32 ? 1 : 32 / C::U;
-        constexpr int PPL = C::U >= 32 ? C::U / 32 : 1;
-        const int sub = C::U >= 32 ? 0 : lane / C::U;
-        const int c0 = C::U >= 32 ? lane : lane - sub * C::U;
 #pragma unroll 4
         for (int r = 0; r < 16; r += RPI) {
             const unsigned long long a = __shfl_sync(0xffffffffu, src, r + sub);
@@ -312,51 +312,55 @@ __device__ __forceinline__ void copy_slots(const AttnParams& p, const SlotSrc& s
         // mixed storage: a 16-byte bf16 piece c of a compressed row is 8 codes (piece c <
         // ncp) dequantized here, or a piece of its bf16 RoPE part; every load of the warp's
         // 16 rows is issued (codes into registers) before the first is converted
-        constexpr int kPer = 16 * C::U / 32;                     // pieces per lane
+        constexpr int kPer = (16 / RPI) * PPL;                   // pieces per lane
         const int ncp = p.nope_dim / 8;
         const int rope_b = (D - p.nope_dim) * 2;                 // bytes of a RoPE part
         uint2 code[kPer];
 #pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-            const int i = lane + 32 * k;
-            const int r = i / C::U, c = i - r * C::U;
-            const unsigned long long a = __shfl_sync(0xffffffffu, src, r);
-            const long long en = __shfl_sync(0xffffffffu, ent, r);
-            const int rr = r0 + r;
-            uint8_t* dst = sKV + (c >> 3) * C::BOX + rr * 128 + (((c & 7) ^ (rr & 7)) << 4);
-            code[k] = make_uint2(0u, 0u);
-            if (a) {
-                cp_async16(dst, reinterpret_cast<const uint8_t*>(a) + c * 16);
-            } else if (en >= 0) {
-                if (c < ncp)
-                    code[k] = __ldg(reinterpret_cast<const uint2*>(p.kv_nope + static_cast<size_t>(en) * p.nope_dim) + c);
-                else
-                    cp_async16(dst, reinterpret_cast<const uint8_t*>(p.kv_rope) + static_cast<size_t>(en) * rope_b +
-                                        (c - ncp) * 16);
-            } else {
-                *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+        for (int r = 0; r < 16; r += RPI) {
+            const unsigned long long a = __shfl_sync(0xffffffffu, src, r + sub);
+            const long long en = __shfl_sync(0xffffffffu, ent, r + sub);
+            const int rr = r0 + r + sub;
+#pragma unroll
+            for (int j = 0; j < PPL; ++j) {
+                const int k = (r / RPI) * PPL + j, c = c0 + 32 * j;
+                uint8_t* dst = sKV + (c >> 3) * C::BOX + rr * 128 + (((c & 7) ^ (rr & 7)) << 4);
+                code[k] = make_uint2(0u, 0u);
+                if (a) {
+                    cp_async16(dst, reinterpret_cast<const uint8_t*>(a) + c * 16);
+                } else if (en >= 0) {
+                    if (c < ncp)
+                        code[k] = __ldg(reinterpret_cast<const uint2*>(p.kv_nope + static_cast<size_t>(en) * p.nope_dim) + c);
+                    else
+                        cp_async16(dst, reinterpret_cast<const uint8_t*>(p.kv_rope) + static_cast<size_t>(en) * rope_b +
+                                            (c - ncp) * 16);
+                } else {
+                    *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+                }
             }
         }
 #pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-            const int i = lane + 32 * k;
-            const int r = i / C::U, c = i - r * C::U;
-            const long long en = __shfl_sync(0xffffffffu, ent, r);
-            const float sc = __shfl_sync(0xffffffffu, escale, r);
-            if (en >= 0 && c < ncp) {                            // (a compressed row)
-                // channel = bf16( fp32(E4M3 code) * scale ): codes in byte order
-                uint32_t o[4];
-                const uint32_t w2[2] = {code[k].x, code[k].y};
+        for (int r = 0; r < 16; r += RPI) {
+            const long long en = __shfl_sync(0xffffffffu, ent, r + sub);
+            const float sc = __shfl_sync(0xffffffffu, escale, r + sub);
+            const int rr = r0 + r + sub;
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const __nv_fp8x2_storage_t pr =
-                        static_cast<__nv_fp8x2_storage_t>((w2[h >> 1] >> (16 * (h & 1))) & 0xFFFFu);
-                    const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3)));
-                    o[h] = pack_bf16(f.x * sc, f.y * sc);
+            for (int j = 0; j < PPL; ++j) {
+                const int k = (r / RPI) * PPL + j, c = c0 + 32 * j;
+                if (en >= 0 && c < ncp) {                        // (a compressed row)
+                    // channel = bf16( fp32(E4M3 code) * scale ): codes in byte order
+                    uint32_t o[4];
+                    const uint32_t w2[2] = {code[k].x, code[k].y};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const __nv_fp8x2_storage_t pr =
+                            static_cast<__nv_fp8x2_storage_t>((w2[h >> 1] >> (16 * (h & 1))) & 0xFFFFu);
+                        const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3)));
+                        o[h] = pack_bf16(f.x * sc, f.y * sc);
+                    }
+                    uint8_t* dst = sKV + (c >> 3) * C::BOX + rr * 128 + (((c & 7) ^ (rr & 7)) << 4);
+                    *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
                 }
-                const int rr = r0 + r;
-                uint8_t* dst = sKV + (c >> 3) * C::BOX + rr * 128 + (((c & 7) ^ (rr & 7)) << 4);
-                *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
             }
         }
     }
