@@ -90,6 +90,36 @@ def test_indexer_rejects_small_workspace(lib):
     assert lib.dsv4_indexer_topk(ctypes.byref(a), _p(9), need - 1, None) == 1
 
 
+def _align256(n):
+    return (n + 255) // 256 * 256
+
+
+def _split_ws(rows, chunks, heads, dim):
+    """The split form's partials: (m, l) and the fp32 O per (row, chunk, head)."""
+    hs = (heads + 31) // 32 * 32 if heads % 32 == 0 else (heads + 15) // 16 * 16
+    return _align256(rows * chunks * hs * 2 * 4) + _align256(rows * chunks * hs * dim * 4)
+
+
+def test_attention_workspace_split_and_walk(lib):
+    """Decode (few query rows) splits each row into 128-slot chunks and needs partials; from
+    304 (query row, head group) pairs on, one CTA walks each row and needs the header only."""
+    header = lib.dsv4_sparse_attn_workspace_size(ctypes.byref(_attn_args(batch=1, n_q=2048, top_k=1024,
+                                                                         max_comp=16896, q_pos=_p(10))))
+    assert header == 256
+    # the bench decode: 4 rows x 17 chunks x 64 heads x 512 dims
+    need = lib.dsv4_sparse_attn_workspace_size(ctypes.byref(_attn_args()))
+    assert need == header + _split_ws(4, 17, 64, 512)
+    # the threshold: 64 heads = 2 groups of 32, 16 heads = 1 group
+    for heads, rows_split in ((64, 151), (16, 303)):
+        a = _attn_args(batch=1, n_q=rows_split, heads=heads, q_pos=_p(10))
+        assert lib.dsv4_sparse_attn_workspace_size(ctypes.byref(a)) == header + _split_ws(rows_split, 17, heads, 512)
+        a = _attn_args(batch=1, n_q=rows_split + 1, heads=heads, q_pos=_p(10))
+        assert lib.dsv4_sparse_attn_workspace_size(ctypes.byref(a)) == header
+    # 48 heads: three groups of 16
+    a = _attn_args(batch=3, n_q=1, heads=48, dim=256, top_k=48, window=64, max_comp=200)
+    assert lib.dsv4_sparse_attn_workspace_size(ctypes.byref(a)) == header + _split_ws(3, 1, 48, 256)
+
+
 @pytest.mark.parametrize("bad", [
     dict(dim=100), dict(heads=0), dict(heads=65), dict(idx=None),   # dense needs top_k == max_comp
     dict(top_k=262145), dict(win_rows=0), dict(scale=float("inf")), dict(out=None),
