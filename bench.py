@@ -547,6 +547,14 @@ def _cpu_model():
     return "unknown"
 
 
+# ----------------------------------------------------------------------------- shared config
+def workload_config(wl):
+    """The workload as both arms report it (same keys, same values)."""
+    return {"workload": wl.name, "batch_per_gpu": wl.batch, "context": wl.context,
+            "n_comp": wl.n_comp, "top_k": wl.top_k, "window": wl.window,
+            "idx_heads": wl.idx_heads, "heads": wl.heads, "head_dim": wl.head_dim}
+
+
 # ----------------------------------------------------------------------------- reference arm
 def run_reference(args):
     ws, rank, _ = dist_env()
@@ -566,10 +574,10 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1000.0 * total / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name, "batch": 1, "context": wl.context, "top_k": wl.top_k},
+            "config": dict(workload_config(wl), l2="host run: the oracle on one core"),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                             "sample": "one sequence (1 token) of the 1M-context decode step per "
-                                       "timed step, fp64 oracle, single thread"},
+                             "sample": "one sequence (1 token) of the 1M-context batch-4 decode step "
+                                       "per timed step, fp64 oracle, single thread"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -748,11 +756,9 @@ def run_ours(args):
         "metric": METRIC, "value": job_throughput(B, world, ms), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": wl.name, "batch_per_gpu": B, "context": wl.context,
-                   "n_comp": wl.n_comp, "top_k": wl.top_k, "window": wl.window,
-                   "idx_heads": wl.idx_heads, "heads": wl.heads, "head_dim": D,
-                   "l2": "inputs larger than L2: 256 MiB of keys streamed per step, 1 GiB KV cache",
-                   "graph": "one CUDA graph per step, replayed"},
+        "config": dict(workload_config(wl),
+                       l2="inputs larger than L2: 256 MiB of keys streamed per step, 1 GiB KV cache",
+                       graph="one CUDA graph per step, replayed"),
         "roofline": {"bound": "hbm", "kernel": "index_score_kernel", "achieved": score_gbs,
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": score_gbs / peak,
                      "traffic": profile_traffic(), "bytes_per_launch": sb,
