@@ -286,6 +286,12 @@ typedef struct dsv4_attn_args {
     int kv_rope_dim;
 } dsv4_attn_args;
 
+/* Workspace: the 256-byte header (error word) plus, when few query rows are given (fewer than
+ * 304 pairs of query row and head group; groups of 32 heads when heads is a multiple of 32,
+ * else of 16), the split form's per-chunk partials: rows x ceil((top_k + window) / 128) x
+ * (heads rounded up to whole groups) x (dim + 2) x 4 bytes, the (m, l) and O parts each
+ * rounded up to 256. With more rows one CTA walks each row and the header alone suffices.
+ * Returns 0 for a NULL args. */
 size_t dsv4_sparse_attn_workspace_size(const dsv4_attn_args* args);
 int dsv4_sparse_attn_decode(const dsv4_attn_args* args, void* ws, size_t ws_bytes,
                             dsv4_stream_t stream);
