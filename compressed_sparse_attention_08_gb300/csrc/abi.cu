@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <vector>
 
 #include "common.cuh"
 #include "internal.h"
@@ -125,16 +126,24 @@ struct LaunchScope {
 
 void count_launch(int n) { g_launches += n; }
 
-void prefer_max_shared(const void* kernel) {
+void once_per_device(const void* kernel, int kind, const std::function<void()>& set) {
+    struct Key { const void* kernel; int dev, kind; };
     static std::mutex mu;
-    static const void* seen[256];
-    static int n_seen = 0;
+    static std::vector<Key> done;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
     std::lock_guard<std::mutex> lock(mu);
-    for (int i = 0; i < n_seen; ++i)
-        if (seen[i] == kernel) return;
-    cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                         cudaSharedmemCarveoutMaxShared);
-    if (n_seen < 256) seen[n_seen++] = kernel;
+    for (const Key& k : done)
+        if (k.kernel == kernel && k.dev == dev && k.kind == kind) return;
+    set();
+    done.push_back(Key{kernel, dev, kind});
+}
+
+void prefer_max_shared(const void* kernel) {
+    once_per_device(kernel, kAttrCarveout, [kernel] {
+        cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    });
 }
 
 int sm_count() {

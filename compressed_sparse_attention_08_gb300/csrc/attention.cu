@@ -893,14 +893,12 @@ int run_decode(const dsv4_attn_args& a, const DecodePlan& dp, uint8_t* ws, uint3
     p.nope_dim = a.kv_fp8 ? D - a.kv_rope_dim : D;
     p.part_ml = reinterpret_cast<float*>(ws);
     p.part_o = reinterpret_cast<float*>(ws + ml_b);
-    static bool attr_set = false;
-    if (!attr_set) {
+    once_per_device(reinterpret_cast<const void*>(attn_decode_kernel<D, NH>), kAttrLaunch, [] {
         cudaFuncSetAttribute(attn_decode_kernel<D, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(C::SMEM));
         cudaFuncSetAttribute(attn_rows_kernel<D, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(C::SMEM));
-        attr_set = true;
-    }
+    });
     if (dp.walk) {                                     // one CTA per (query row, head group)
         count_launch();
         return launch_k(attn_rows_kernel<D, NH>, dim3(static_cast<unsigned>(rows) * dp.n_hg), dim3(kFT), C::SMEM,

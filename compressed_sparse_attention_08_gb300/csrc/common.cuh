@@ -10,6 +10,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cstdint>
+#include <functional>
 
 #include "dsv4.h"
 
@@ -389,6 +390,12 @@ __device__ __forceinline__ void red_cluster_add(uint32_t addr, uint32_t v) {
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+
+// Runs `set` the first time it is called for (kernel, kind) on the current device: function
+// attributes are per device. One lock covers the check and `set`, so no caller launches the
+// kernel before its attributes are in place.
+void once_per_device(const void* kernel, int kind, const std::function<void()>& set);
+enum { kAttrCarveout = 0, kAttrLaunch = 1 };
 
 // Every kernel of the library asks for the largest shared-memory carveout. Kernels that
 // overlap under programmatic dependent launch can then share an SM: a small kernel left with

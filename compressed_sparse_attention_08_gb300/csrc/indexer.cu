@@ -655,12 +655,10 @@ int launch_scores_fmt(const dsv4_index_args& a, float* scores, uint32_t* hist, u
     p.units = a.batch * p.gpb;
     const long long total = static_cast<long long>(p.units) * p.stages_per_row;
     if (total > 0) {
-        static bool attr_set = false;
-        if (!attr_set) {
+        once_per_device(reinterpret_cast<const void*>(index_score_kernel<FP8, NP, EG, QB>), kAttrLaunch, [] {
             cudaFuncSetAttribute(index_score_kernel<FP8, NP, EG, QB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kSmemBytes + (QB - 1) * kQBufBytes));
-            attr_set = true;
-        }
+        });
         long long grid = sm_count();
         if (grid > total) grid = total;
         count_launch();
