@@ -20,6 +20,9 @@ DSV4_ERR_TIMEOUT = 4
 DSV4_ERR_UNSUPPORTED = 5
 DSV4_EWORD_BAD_INDEX = 0x1
 DSV4_EWORD_TIMEOUT = 0x2
+DSV4_WAIT_FAULT_NONE = 0
+DSV4_WAIT_FAULT_SCORER_STAGE = 1
+DSV4_WAIT_FAULT_ATTN_QUERY = 2
 
 EXPORTED_SYMBOLS = (
     "dsv4_compress", "dsv4_compress_step", "dsv4_quantize_rows_fp8", "dsv4_indexer_topk_workspace_size",
@@ -28,6 +31,7 @@ EXPORTED_SYMBOLS = (
     "dsv4_topk_workspace_size", "dsv4_topk", "dsv4_topk_noalloc", "dsv4_sparse_attn_workspace_size",
     "dsv4_sparse_attn_decode", "dsv4_csa_decode_workspace_size", "dsv4_csa_decode",
     "dsv4_status_string", "dsv4_read_error_word", "dsv4_last_launch_count", "dsv4_max_comp",
+    "dsv4_test_wait_fault",
 )
 
 P = ctypes.c_void_p
@@ -124,6 +128,8 @@ def library():
         lib.dsv4_last_launch_count.restype = I
         lib.dsv4_max_comp.argtypes = [ctypes.c_int64, I]
         lib.dsv4_max_comp.restype = ctypes.c_int64
+        lib.dsv4_test_wait_fault.argtypes = [I, ctypes.c_uint32]
+        lib.dsv4_test_wait_fault.restype = I
         for f in ("dsv4_compress", "dsv4_indexer_topk", "dsv4_index_score", "dsv4_topk", "dsv4_sparse_attn_decode",
                   "dsv4_csa_decode", "dsv4_read_error_word"):
             getattr(lib, f).restype = I
@@ -404,3 +410,10 @@ def dsv4_last_launch_count():
 
 def dsv4_max_comp(max_context, ratio):
     return int(library().dsv4_max_comp(int(max_context), int(ratio)))
+
+
+def dsv4_test_wait_fault(which, wait_limit_us=0):
+    """Test support: from now on every launch of kernel `which` (DSV4_WAIT_FAULT_*) leaves one
+    copy unissued so its bounded wait runs out after wait_limit_us microseconds (0: the
+    default 2 s); DSV4_WAIT_FAULT_NONE restores normal launches."""
+    _check(library().dsv4_test_wait_fault(int(which), int(wait_limit_us)), "dsv4_test_wait_fault")

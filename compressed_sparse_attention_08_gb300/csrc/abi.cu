@@ -2,6 +2,7 @@
 // sizing, dispatch to the kernels on the caller's stream, and small utilities.
 // No entry point allocates, frees, synchronises or reads device memory on the host,
 // except dsv4_read_error_word, which exists for tests and diagnostics.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -20,15 +21,17 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool dev_ptr_ok(const void* p) { return p != nullptr && aligned16(p); }
 bool opt_ptr_ok(const void* p) { return p == nullptr || aligned16(p); }
 
+// The library holds sm_103a code only: any other device is refused before a launch.
 int device_check() {
     static int ok_for_device[64] = {0};   // 0 unknown, 1 ok, 2 unsupported
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return DSV4_ERR_UNSUPPORTED;
     if (dev < 64 && ok_for_device[dev] == 1) return DSV4_OK;
-    int major = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
         return DSV4_ERR_UNSUPPORTED;
-    const int res = major == 10 ? DSV4_OK : DSV4_ERR_UNSUPPORTED;
+    const int res = major == 10 && minor == 3 ? DSV4_OK : DSV4_ERR_UNSUPPORTED;
     if (dev < 64) ok_for_device[dev] = res == DSV4_OK ? 1 : 2;
     return res;
 }
@@ -126,7 +129,22 @@ struct LaunchScope {
 
 void count_launch(int n) { g_launches += n; }
 
-void once_per_device(const void* kernel, int kind, const std::function<void()>& set) {
+namespace {
+std::atomic<int> g_wait_fault{DSV4_WAIT_FAULT_NONE};
+std::atomic<unsigned> g_wait_limit_us{0};
+}  // namespace
+
+WaitCtl wait_ctl(int which) {
+    WaitCtl c{0, kDefaultWaitNs};
+    if (which != DSV4_WAIT_FAULT_NONE && g_wait_fault.load() == which) {
+        c.fault = 1;
+        const unsigned us = g_wait_limit_us.load();
+        if (us) c.wait_ns = 1000ull * us;
+    }
+    return c;
+}
+
+cudaError_t once_per_device(const void* kernel, int kind, const std::function<cudaError_t()>& set) {
     struct Key { const void* kernel; int dev, kind; };
     static std::mutex mu;
     static std::vector<Key> done;
@@ -134,15 +152,18 @@ void once_per_device(const void* kernel, int kind, const std::function<void()>& 
     if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
     std::lock_guard<std::mutex> lock(mu);
     for (const Key& k : done)
-        if (k.kernel == kernel && k.dev == dev && k.kind == kind) return;
-    set();
-    done.push_back(Key{kernel, dev, kind});
+        if (k.kernel == kernel && k.dev == dev && k.kind == kind) return cudaSuccess;
+    const cudaError_t e = set();
+    // a failed setting is not recorded: the next call tries again (and fails its launch)
+    if (e == cudaSuccess) done.push_back(Key{kernel, dev, kind});
+    else cudaGetLastError();       // the error is returned here, not left for a later launch
+    return e;
 }
 
-void prefer_max_shared(const void* kernel) {
-    once_per_device(kernel, kAttrCarveout, [kernel] {
-        cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
+cudaError_t prefer_max_shared(const void* kernel) {
+    return once_per_device(kernel, kAttrCarveout, [kernel] {
+        return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                    cudaSharedmemCarveoutMaxShared);
     });
 }
 
@@ -170,12 +191,20 @@ const char* dsv4_status_string(int status) {
         case DSV4_ERR_LAUNCH: return "kernel launch failed";
         case DSV4_ERR_BAD_INDEX: return "an index outside the visible range was masked";
         case DSV4_ERR_TIMEOUT: return "a bounded device wait ran out";
-        case DSV4_ERR_UNSUPPORTED: return "unsupported device (needs sm_100-class / sm_103)";
+        case DSV4_ERR_UNSUPPORTED: return "unsupported device (the library is built for sm_103 only)";
         default: return "unknown status";
     }
 }
 
 int dsv4_last_launch_count(void) { return g_last_launches; }
+
+int dsv4_test_wait_fault(int which, uint32_t wait_limit_us) {
+    if (which < DSV4_WAIT_FAULT_NONE || which > DSV4_WAIT_FAULT_ATTN_QUERY || wait_limit_us > 2000000u)
+        return DSV4_ERR_INVALID_ARG;
+    g_wait_limit_us.store(wait_limit_us);
+    g_wait_fault.store(which);
+    return DSV4_OK;
+}
 
 int64_t dsv4_max_comp(int64_t max_context, int ratio) {
     if (ratio < 1 || max_context < 0) return -1;

@@ -48,6 +48,8 @@ struct AttnParams {
     const float* kv_scale;         // [B, max_comp]
     const __nv_bfloat16* kv_rope;  // [B, max_comp, D - nope_dim]
     int nope_dim;
+    int fault;                     // test control: the split form does not load its query tile
+    unsigned long long wait_ns;    // limit of each bounded wait
 };
 
 // Inverse RoPE of one output pair (channels c, c + 1, c even) of query row `row`: rotated back
@@ -430,9 +432,11 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
     const uint32_t tmem = tmem_slot;
     if (tid == 0) {                  // the queries are inputs: they load before the wait below
         tma_prefetch_desc(&gmap);
-        mbar_arrive_expect_tx(&bars[0], static_cast<uint32_t>(Hc) * D * 2);
-        for (int box = 0; box < C::NBOX; ++box)
-            tma_load_2d(sQ + box * NH * 128, &qmap, &bars[0], box * 64, row * p.H + hbase);
+        if (!p.fault) {              // (test control: the copy is left out, its wait runs out)
+            mbar_arrive_expect_tx(&bars[0], static_cast<uint32_t>(Hc) * D * 2);
+            for (int box = 0; box < C::NBOX; ++box)
+                tma_load_2d(sQ + box * NH * 128, &qmap, &bars[0], box * 64, row * p.H + hbase);
+        }
     }
 
     pdl_wait();                      // the index list comes from the kernel before
@@ -449,7 +453,7 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
             bulk_commit();
         }
         // ---- S^T = KV Q^T
-        if (mbar_wait(&bars[0], 0, nullptr)) {
+        if (mbar_wait(&bars[0], 0, nullptr, p.wait_ns)) {
             tc_fence_after();
             const uint32_t idesc = idesc_bf16_f32(kFC, NH);
             const uint32_t a0 = smem_u32(sKV), b0 = smem_u32(sQ);
@@ -463,7 +467,7 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
             abort_flag = 1;
         }
     }
-    bool dead = !mbar_wait(&bars[1], 0, &abort_flag);
+    bool dead = !mbar_wait(&bars[1], 0, &abort_flag, p.wait_ns);
     tc_fence_after();
     // ---- scores -> shared (scaled, masked): warps w and w + 4 read TMEM lane quarter w & 3,
     //      half of the head columns each
@@ -537,7 +541,7 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         p.part_ml[(part * p.hstride + hbase + lane) * 2 + 0] = dead ? -INFINITY : m;
         p.part_ml[(part * p.hstride + hbase + lane) * 2 + 1] = dead ? 0.f : l;
     }
-    if (!dead && !mbar_wait(&bars[2], 0, &abort_flag)) {
+    if (!dead && !mbar_wait(&bars[2], 0, &abort_flag, p.wait_ns)) {
         if (tid == 0) flag_error(p.eword, DSV4_EWORD_TIMEOUT);
         dead = true;
     }
@@ -564,7 +568,7 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
     if (warp == 0) tmem_dealloc(tmem, C::TCOLS);
     if (tid == 0) {
         if (write_gather && hgrp == 0) bulk_wait_read();             // the tile is read out
-        if (abort_flag) mbar_wait(&bars[0], 0, nullptr, 100000000ull);   // the query copy landed
+        if (abort_flag && !p.fault) mbar_wait(&bars[0], 0, nullptr, 100000000ull);   // the query copy landed
     }
 }
 
@@ -681,7 +685,7 @@ attn_rows_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                     tma_store_3d(&gmap, sKV + box * C::BOX, box * 64, chunk * kFC, row);
                 bulk_commit();
             }
-            if (!dead && chunk == 0 && !mbar_wait(&bars[0], 0, nullptr)) dead = true;
+            if (!dead && chunk == 0 && !mbar_wait(&bars[0], 0, nullptr, p.wait_ns)) dead = true;
             if (!dead) {                            // S^T = KV Q^T
                 tc_fence_after();
                 const uint32_t idesc = idesc_bf16_f32(kFC, NH);
@@ -697,7 +701,7 @@ attn_rows_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
             }
         }
         if (chunk > 0) add_chunk_o();                // the previous chunk's O^T, while S^T runs
-        if (!dead && !mbar_wait(&bars[1], ph, &abort_flag)) {
+        if (!dead && !mbar_wait(&bars[1], ph, &abort_flag, p.wait_ns)) {
             dead = true;
             if (tid == 0) { flag_error(p.eword, DSV4_EWORD_TIMEOUT); abort_flag = 1; }
         }
@@ -770,7 +774,7 @@ attn_rows_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
             for (int j = 0; j < 8; ++j) l += red_l[j * NH + lane];
             l_run = l_run * fac + l;
         }
-        if (!dead && !mbar_wait(&bars[2], ph, &abort_flag)) {
+        if (!dead && !mbar_wait(&bars[2], ph, &abort_flag, p.wait_ns)) {
             dead = true;
             if (tid == 0) { flag_error(p.eword, DSV4_EWORD_TIMEOUT); abort_flag = 1; }
         }
@@ -833,7 +837,11 @@ attn_rows_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     }
 }
 
-// (query row, head group) pairs from which one CTA walks each row: two per SM of a 152-SM part
+// (query row, head group) pairs from which one CTA walks each row. A fixed crossover measured
+// on a 152-SM GB300 (the walking form took over once it had about two CTAs per SM), not a
+// value derived from the device's SM count: it also fixes the workspace rule stated in the
+// header (partials below it, none at or above it), which must not change from one device to
+// another.
 constexpr long long kRowWalkCtas = 304;
 
 struct DecodePlan { int n_chunks, nh, n_hg; bool walk; };
@@ -893,12 +901,18 @@ int run_decode(const dsv4_attn_args& a, const DecodePlan& dp, uint8_t* ws, uint3
     p.nope_dim = a.kv_fp8 ? D - a.kv_rope_dim : D;
     p.part_ml = reinterpret_cast<float*>(ws);
     p.part_o = reinterpret_cast<float*>(ws + ml_b);
-    once_per_device(reinterpret_cast<const void*>(attn_decode_kernel<D, NH>), kAttrLaunch, [] {
-        cudaFuncSetAttribute(attn_decode_kernel<D, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(C::SMEM));
-        cudaFuncSetAttribute(attn_rows_kernel<D, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(C::SMEM));
-    });
+    const WaitCtl wc = wait_ctl(DSV4_WAIT_FAULT_ATTN_QUERY);
+    p.fault = dp.walk ? 0 : wc.fault;              // the control applies to the split form only
+    p.wait_ns = wc.wait_ns;
+    if (once_per_device(reinterpret_cast<const void*>(attn_decode_kernel<D, NH>), kAttrLaunch, [] {
+            const cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<D, NH>,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       static_cast<int>(C::SMEM));
+            if (e != cudaSuccess) return e;
+            return cudaFuncSetAttribute(attn_rows_kernel<D, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(C::SMEM));
+        }) != cudaSuccess)
+        return DSV4_ERR_LAUNCH;
     if (dp.walk) {                                     // one CTA per (query row, head group)
         count_launch();
         return launch_k(attn_rows_kernel<D, NH>, dim3(static_cast<unsigned>(rows) * dp.n_hg), dim3(kFT), C::SMEM,

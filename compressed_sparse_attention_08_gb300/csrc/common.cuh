@@ -75,12 +75,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// The time limit of a bounded wait unless a test shortens it (dsv4_test_wait_fault).
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
+
 // Wait for the phase with the given parity to complete, for at most `limit_ns`.
 // Returns false on time-out (the caller records the error and winds down). A non-null
 // `abort` flag set by another role of the CTA also ends the wait (returns false).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           const volatile int* abort,
-                                          uint64_t limit_ns = 2000000000ull) {
+                                          uint64_t limit_ns = kDefaultWaitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
@@ -393,19 +396,20 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
 
 // Runs `set` the first time it is called for (kernel, kind) on the current device: function
 // attributes are per device. One lock covers the check and `set`, so no caller launches the
-// kernel before its attributes are in place.
-void once_per_device(const void* kernel, int kind, const std::function<void()>& set);
+// kernel before its attributes are in place. Only a successful `set` is recorded; its error is
+// returned (and a later call runs `set` again).
+cudaError_t once_per_device(const void* kernel, int kind, const std::function<cudaError_t()>& set);
 enum { kAttrCarveout = 0, kAttrLaunch = 1 };
 
 // Every kernel of the library asks for the largest shared-memory carveout. Kernels that
 // overlap under programmatic dependent launch can then share an SM: a small kernel left with
 // a smaller carveout would keep the next big kernel's CTA off its SM until it drained.
-void prefer_max_shared(const void* kernel);
+cudaError_t prefer_max_shared(const void* kernel);
 
 template <typename... KArgs, typename... Args>
 cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                      cudaStream_t stream, bool pdl, Args... args) {
-    prefer_max_shared(reinterpret_cast<const void*>(kernel));
+    if (cudaError_t e = prefer_max_shared(reinterpret_cast<const void*>(kernel))) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
@@ -423,7 +427,7 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
 template <class... KArgs, class... Args>
 cudaError_t launch_cluster_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                              cudaStream_t stream, bool pdl, unsigned cluster_x, Args... args) {
-    prefer_max_shared(reinterpret_cast<const void*>(kernel));
+    if (cudaError_t e = prefer_max_shared(reinterpret_cast<const void*>(kernel))) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;

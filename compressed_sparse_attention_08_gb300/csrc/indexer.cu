@@ -96,6 +96,8 @@ struct ScoreParams {
     int rows, n_q, heads, max_comp, ratio, stages_per_row;
     // the walk's units: QB consecutive query rows of one sequence (QB = 1: a unit is a row)
     int units, gpb;          // units in all, units per sequence (ceil(n_q / QB))
+    int fault;               // test control: the first key stage of each CTA is not loaded
+    unsigned long long wait_ns;   // limit of each bounded wait
 };
 
 // The stages one CTA scores, as positions f = row * stages_per_row + stage: f = begin,
@@ -243,7 +245,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                 {
                     // hand the stage to the MMA warp and the epilogue
                     const int slot = static_cast<int>(seq % kIdRing);
-                    if (!mbar_wait(&idempty_bar[slot], static_cast<uint32_t>(((seq / kIdRing) & 1) ^ 1), &abort_flag))
+                    if (!mbar_wait(&idempty_bar[slot], static_cast<uint32_t>(((seq / kIdRing) & 1) ^ 1), &abort_flag, p.wait_ns))
                         goto fail0;
                     s_id[slot] = make_int2(row, st);
                     mbar_arrive(&idfull_bar[slot]);
@@ -252,7 +254,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                 if (row != cur_row) {
                     // one query buffer: the MMA warp learns of the new row from the stage id
                     // just handed over and releases the old queries once their MMAs are done
-                    if (!mbar_wait(&qempty_bar, (qcount & 1) ^ 1, &abort_flag)) goto fail0;
+                    if (!mbar_wait(&qempty_bar, (qcount & 1) ^ 1, &abort_flag, p.wait_ns)) goto fail0;
                     const int nqu = unit_nq(row);
                     mbar_arrive_expect_tx(&qfull_bar, static_cast<uint32_t>(nqu * p.heads) * kDim * F::kElem);
                     for (int q = 0; q < nqu; ++q) {
@@ -274,7 +276,15 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                         waited = true;
                     }
                 }
-                if (!mbar_wait(&empty_bar[stage], phase ^ 1, &abort_flag)) goto fail0;
+                if (p.fault && issued == 0) {
+                    // test control: this stage's copy is never issued, so the MMA warp's wait for
+                    // it runs out; wait (bounded) until that warp has given up, then wind down
+                    const uint64_t t0 = global_timer_ns();
+                    while (!abort_flag && global_timer_ns() - t0 < 4 * p.wait_ns) {
+                    }
+                    goto fail0;
+                }
+                if (!mbar_wait(&empty_bar[stage], phase ^ 1, &abort_flag, p.wait_ns)) goto fail0;
                 mbar_arrive_expect_tx(&full_bar[stage], kStageBytes);
                 {
                     uint8_t* kd = key_buf + stage * kStageBytes;
@@ -290,7 +300,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
             {
                 // end of the stream
                 const int slot = static_cast<int>(seq % kIdRing);
-                if (!mbar_wait(&idempty_bar[slot], static_cast<uint32_t>(((seq / kIdRing) & 1) ^ 1), &abort_flag))
+                if (!mbar_wait(&idempty_bar[slot], static_cast<uint32_t>(((seq / kIdRing) & 1) ^ 1), &abort_flag, p.wait_ns))
                     goto fail0;
                 s_id[slot] = make_int2(-1, -1);
                 mbar_arrive(&idfull_bar[slot]);
@@ -314,24 +324,24 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
             uint32_t phase = 0, acc_phase = 0;
             for (long long seq = 0;; ++seq) {
                 const int slot = static_cast<int>(seq % kIdRing);
-                if (!mbar_wait(&idfull_bar[slot], static_cast<uint32_t>((seq / kIdRing) & 1), &abort_flag)) goto fail1;
+                if (!mbar_wait(&idfull_bar[slot], static_cast<uint32_t>((seq / kIdRing) & 1), &abort_flag, p.wait_ns)) goto fail1;
                 const int2 id = s_id[slot];
                 if (id.x < 0) break;
                 const int row = id.x, st = id.y;
                 if (row != cur_row) {
                     if (cur_row >= 0) umma_commit(&qempty_bar);   // old queries free once done
-                    if (!mbar_wait(&qfull_bar, qcount & 1, &abort_flag)) goto fail1;
+                    if (!mbar_wait(&qfull_bar, qcount & 1, &abort_flag, p.wait_ns)) goto fail1;
                     cur_row = row;
                     nv = unit_visible(row);
                     ++qcount;
                 }
-                if (!mbar_wait(&full_bar[stage], phase, &abort_flag)) goto fail1;
+                if (!mbar_wait(&full_bar[stage], phase, &abort_flag, p.wait_ns)) goto fail1;
                 {
                     const uint32_t a_stage = smem_u32(key_buf + stage * kStageBytes);
                     const uint32_t b0 = smem_u32(q_buf);
                     for (int j = 0; j < kSub; ++j) {
                         if ((st * kSub + j) * kTileKeys >= nv) break;   // tile past the visible keys
-                        if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1, &abort_flag)) goto fail1;
+                        if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1, &abort_flag, p.wait_ns)) goto fail1;
                         tc_fence_after();
                         const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kAccColsQ);
                         const uint32_t a0 = a_stage + static_cast<uint32_t>(j * kTileKeys * 128);
@@ -381,7 +391,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
         // any role has given up, so a failure anywhere cannot leave a thread waiting.
         auto epi_sync = [&]() -> bool {
             mbar_arrive(&epi_bar);
-            const bool r = mbar_wait(&epi_bar, fl_parity, &abort_flag);
+            const bool r = mbar_wait(&epi_bar, fl_parity, &abort_flag, p.wait_ns);
             fl_parity ^= 1;
             return r;
         };
@@ -407,7 +417,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
         // the next stage's id, read one stage ahead; each warp releases the slot once read
         auto read_id = [&](long long sq, int2& id) -> bool {
             const int slot = static_cast<int>(sq % kIdRing);
-            if (!mbar_wait(&idfull_bar[slot], static_cast<uint32_t>((sq / kIdRing) & 1), &abort_flag)) return false;
+            if (!mbar_wait(&idfull_bar[slot], static_cast<uint32_t>((sq / kIdRing) & 1), &abort_flag, p.wait_ns)) return false;
             const volatile int* v = reinterpret_cast<const volatile int*>(&s_id[slot]);
             id = make_int2(v[0], v[1]);
             __syncwarp();
@@ -470,7 +480,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                 const uint32_t my_phase = acc_phase;
                 if (++acc == kAccBufs) { acc = 0; acc_phase ^= 1; }
                 if (kEpiGroups > 1 && (my_acc % kEpiGroups) != group) continue;
-                if (!mbar_wait(&tfull_bar[my_acc], my_phase, &abort_flag)) {
+                if (!mbar_wait(&tfull_bar[my_acc], my_phase, &abort_flag, p.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -653,12 +663,17 @@ int launch_scores_fmt(const dsv4_index_args& a, float* scores, uint32_t* hist, u
     p.stages_per_row = (a.max_comp + F::kStageKeys - 1) / F::kStageKeys;
     p.gpb = (a.n_q + QB - 1) / QB;
     p.units = a.batch * p.gpb;
+    const WaitCtl wc = wait_ctl(DSV4_WAIT_FAULT_SCORER_STAGE);
+    p.fault = wc.fault;
+    p.wait_ns = wc.wait_ns;
     const long long total = static_cast<long long>(p.units) * p.stages_per_row;
     if (total > 0) {
-        once_per_device(reinterpret_cast<const void*>(index_score_kernel<FP8, NP, EG, QB>), kAttrLaunch, [] {
-            cudaFuncSetAttribute(index_score_kernel<FP8, NP, EG, QB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kSmemBytes + (QB - 1) * kQBufBytes));
-        });
+        if (once_per_device(reinterpret_cast<const void*>(index_score_kernel<FP8, NP, EG, QB>), kAttrLaunch, [] {
+                return cudaFuncSetAttribute(index_score_kernel<FP8, NP, EG, QB>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            static_cast<int>(kSmemBytes + (QB - 1) * kQBufBytes));
+            }) != cudaSuccess)
+            return DSV4_ERR_LAUNCH;
         long long grid = sm_count();
         if (grid > total) grid = total;
         count_launch();

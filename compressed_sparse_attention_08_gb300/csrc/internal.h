@@ -11,6 +11,15 @@
 
 namespace dsv4 {
 
+// Test control of the bounded waits (dsv4_test_wait_fault): for kernel `which`
+// (DSV4_WAIT_FAULT_*), whether its launches leave one copy unissued, and the limit in ns of
+// its bounded waits (the default unless that kernel is the one named).
+struct WaitCtl {
+    int fault;
+    unsigned long long wait_ns;
+};
+WaitCtl wait_ctl(int which);
+
 int launch_compress(const dsv4_compress_args& a, cudaStream_t stream);
 int launch_compress_step(const dsv4_compress_step_args& a, cudaStream_t stream);
 // FP8 E4M3 rows: one warp per row, scale = amax / 448 (fp32), codes of x / scale.

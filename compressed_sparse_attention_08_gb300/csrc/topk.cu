@@ -470,10 +470,11 @@ int launch_topk(const TopkRows& t, uint8_t* ws, uint32_t* eword, cudaStream_t st
     if (t.rows == 0) return DSV4_OK;
     if (t.max_comp <= kSmallCap) {
         const size_t smem = static_cast<size_t>(t.max_comp > 0 ? t.max_comp : 1) * 4;
-        once_per_device(reinterpret_cast<const void*>(topk_small_kernel<kNT>), kAttrLaunch, [] {
-            cudaFuncSetAttribute(topk_small_kernel<kNT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmallCap * 4);
-        });
+        if (once_per_device(reinterpret_cast<const void*>(topk_small_kernel<kNT>), kAttrLaunch, [] {
+                return cudaFuncSetAttribute(topk_small_kernel<kNT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            kSmallCap * 4);
+            }) != cudaSuccess)
+            return DSV4_ERR_LAUNCH;
         count_launch();
         return launch_k(topk_small_kernel<kNT>, dim3(t.rows), dim3(kNT), smem, stream, t.pdl, t, eword)
                    == cudaSuccess ? DSV4_OK : DSV4_ERR_LAUNCH;
@@ -487,11 +488,14 @@ int launch_topk(const TopkRows& t, uint8_t* ws, uint32_t* eword, cudaStream_t st
     if (!t.hist_zeroed &&
         cudaMemsetAsync(w.hist, 0, topk_hist_bytes(t.rows), stream) != cudaSuccess)
         return DSV4_ERR_LAUNCH;
-    once_per_device(reinterpret_cast<const void*>(topk_cluster_kernel<kNT, kCl>), kAttrLaunch, [] {
-        cudaFuncSetAttribute(topk_cluster_kernel<kNT, kCl>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kFinalCap * 8);
-        if (kCl > 8) cudaFuncSetAttribute(topk_cluster_kernel<kNT, kCl>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    });
+    if (once_per_device(reinterpret_cast<const void*>(topk_cluster_kernel<kNT, kCl>), kAttrLaunch, [] {
+            const cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel<kNT, kCl>,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kFinalCap * 8);
+            if (e != cudaSuccess || kCl <= 8) return e;
+            return cudaFuncSetAttribute(topk_cluster_kernel<kNT, kCl>,
+                                        cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        }) != cudaSuccess)
+        return DSV4_ERR_LAUNCH;
     if (!t.hist_built) {
         count_launch();
         if (launch_k(topk_hist_kernel<kNT>, dim3(t.rows, pl.P), dim3(kNT), 0, stream, t.pdl, t, w, pl.L, eword)

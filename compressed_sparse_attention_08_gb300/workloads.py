@@ -153,6 +153,30 @@ def make_inputs(wl: Workload, batch: int | None = None) -> dict:
     return x
 
 
+# Seeds of the extra per-step input sets of step_inputs: wl.seed + VARIANT_SEED_STRIDE * j.
+VARIANT_SEED_STRIDE = 1000
+
+
+def step_inputs(wl: Workload, variant: int) -> dict:
+    """The inputs that change from one decode step to the next (indexer queries ``q_I``, head
+    weights ``w``, attention queries ``q`` and the newest block's ``C, Z, C_I, Z_I``), full
+    batch, for a decode workload (one query per sequence) with pre-generated caches. Variant 0
+    is exactly make_inputs' draw; variant j > 0 draws the same shapes and distributions from
+    seed wl.seed + VARIANT_SEED_STRIDE * j. Replaying a step over several variants makes
+    consecutive steps select different cache rows, as successive decode tokens do."""
+    assert wl.pregen_cache and wl.new_tokens == 1 and not wl.dense
+    seed = wl.seed + VARIANT_SEED_STRIDE * variant
+    B, D, Di, r = wl.batch, wl.head_dim, wl.idx_dim, wl.ratio
+
+    def bf(name, shape):
+        return synth.normal_bf16(seed, TID[name], (B,) + shape)
+
+    x = {"C": bf("C", (r, D)), "Z": bf("Z", (r, D)), "C_I": bf("C_I", (r, Di)), "Z_I": bf("Z_I", (r, Di)),
+         "q_I": bf("q_I", (1, wl.idx_heads, Di)), "q": bf("q", (1, wl.heads, D))}
+    x["w"] = synth.normal_f32(seed, TID["w"], (B, 1, wl.idx_heads), 0.0, 1.0 / np.sqrt(wl.idx_heads))
+    return x
+
+
 def _bf16_prefix(wl, name, full, B, per_seq_shape, mean, std):
     """First B sequences of a [full, ...] draw, without drawing the rest."""
     n_per = int(np.prod(per_seq_shape))

@@ -50,7 +50,7 @@ enum {
     DSV4_ERR_LAUNCH = 2,      /* a kernel launch failed */
     DSV4_ERR_BAD_INDEX = 3,   /* device: an index outside [0, visible) was masked */
     DSV4_ERR_TIMEOUT = 4,     /* device: a bounded wait ran out; the kernel returned early */
-    DSV4_ERR_UNSUPPORTED = 5  /* the device is not sm_103 / sm_100 class */
+    DSV4_ERR_UNSUPPORTED = 5  /* the device is not sm_103 (the only code the library holds) */
 };
 
 /* Device error word bits (dsv4_read_error_word). */
@@ -219,11 +219,13 @@ int dsv4_topk(const dsv4_topk_args* args, void* ws, size_t ws_bytes, dsv4_stream
  * plug-in that receives only its input and output buffers). The pages have no counterpart
  * for this entry point: it is a convenience of this library. Same arguments, rule and
  * results as dsv4_topk, but no workspace: the scratch it needs lives in a fixed 16 MiB
- * device array that the library reserves on each GPU it runs on and keeps until the process
- * exits. Calls whose scratch need (dsv4_topk_workspace_size(args)) exceeds 16 MiB return
+ * device array that the library holds on each GPU it runs on until the process exits.
+ * Calls whose scratch need (dsv4_topk_workspace_size(args)) exceeds 16 MiB return
  * DSV4_ERR_INVALID_ARG before any launch (for 262,144-entry rows: up to 7 rows per call).
- * The first call on a device looks up the array's device address (make that first call
- * before any stream capture). Every call shares the one array, so calls that overlap on the
+ * The first call on a device looks up the array's device address; with lazy module loading
+ * that lookup is also when the driver reserves the 16 MiB on that device, so a failure to
+ * reserve it comes back from that first call as DSV4_ERR_LAUNCH. Make the first call on
+ * each device at start-up, before any stream capture. Every call shares the one array, so calls that overlap on the
  * GPU (different streams, or different host threads) race and must not be issued; each call
  * clears what it needs. Device-side findings (counts out of range) are not reported by this
  * variant. No memory is allocated or freed. */
@@ -319,6 +321,35 @@ int dsv4_csa_decode(const dsv4_csa_args* args, void* ws, size_t ws_bytes,
  * scale fp32 [rows]. dim: 32, 64, 128, 256, 512 or 1024. */
 int dsv4_quantize_rows_fp8(const void* x, int rows, int dim, void* q, float* scale,
                            dsv4_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Test support: running the bounded-wait path on purpose. Not for a serving path.
+ *
+ * Every wait of a kernel on an asynchronous copy, or on another role of its CTA, is bounded
+ * in time: when the limit runs out the kernel records DSV4_EWORD_TIMEOUT in the error word,
+ * lets its own copies in flight land, frees its tensor memory and returns (the call reports
+ * DSV4_ERR_TIMEOUT through dsv4_read_error_word). dsv4_test_wait_fault makes that happen
+ * without any fault: from this call until the next, every launch of the named kernel leaves
+ * one of its copies unissued, so the wait for that copy runs out, and every bounded wait of
+ * that kernel gives up after wait_limit_us microseconds (1 .. 2,000,000; 0 keeps the default
+ * of 2 s). DSV4_WAIT_FAULT_NONE restores normal launches. The setting is process-wide and is
+ * read when a kernel is launched (a graph captured meanwhile keeps it). Returns
+ * DSV4_ERR_INVALID_ARG for an unknown kernel or a limit out of range.
+ *   DSV4_WAIT_FAULT_SCORER_STAGE: the indexer's scoring kernel (dsv4_index_score,
+ *     dsv4_indexer_topk, dsv4_csa_decode) issues no copy for the first key stage of each
+ *     CTA; the tensor-core warp's wait for that stage runs out.
+ *   DSV4_WAIT_FAULT_ATTN_QUERY: the split-form attention kernel (decode: fewer query rows,
+ *     see dsv4_sparse_attn_workspace_size) issues no copy of its query tile; the wait before
+ *     its first tensor-core product runs out.
+ * [A] fmha_multitile_capi.cu (errors of the device path returned through C-ABI status codes,
+ * never by trapping the process).
+ */
+enum {
+    DSV4_WAIT_FAULT_NONE = 0,
+    DSV4_WAIT_FAULT_SCORER_STAGE = 1,
+    DSV4_WAIT_FAULT_ATTN_QUERY = 2
+};
+int dsv4_test_wait_fault(int which, uint32_t wait_limit_us);
 
 /* ---------------------------------------------------------------------------------------
  * Utilities.

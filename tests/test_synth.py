@@ -42,3 +42,16 @@ def test_uniform_index_sets():
     assert list(idx[1]) == sorted(idx[1][:3].tolist()) + [-1, -1]
     assert list(idx[2]) == [-1] * 5
     assert len(set(idx[0].tolist())) == 5 and idx[0].max() < 10
+
+
+def test_step_input_variants():
+    """The benchmark's rotating per-step inputs: variant 0 is the workload's own draw, other
+    variants are different draws of the same shapes."""
+    from compressed_sparse_attention_08_gb300.workloads import WORKLOADS, make_inputs, step_inputs
+    wl = WORKLOADS[3]
+    x = make_inputs(wl, batch=1)          # the first sequence of the full draw
+    v0, v1 = step_inputs(wl, 0), step_inputs(wl, 1)
+    for k, a in v0.items():
+        assert np.array_equal(a[:1], x[k]), k
+        assert v1[k].shape == a.shape and v1[k].dtype == a.dtype
+        assert not np.array_equal(v1[k], a), k

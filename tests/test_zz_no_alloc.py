@@ -3,13 +3,15 @@
 Such callers (allocator hooks, serving loops that forbid cudaMalloc after start-up, plug-ins
 handed only their buffers) get their scratch from a fixed per-GPU array inside the library.
 This file runs last so that a failure here cannot hide the other tests of a run that stops
-at the first failure. It compares the variant with dsv4_topk, which uses a caller
+at the first failure. It compares the variant with the oracle's top-k (the definition: ties
+to the lower index, ascending order, -1 padding) and with dsv4_topk, which uses a caller
 workspace: the indices must be identical (integer output, bit-exact), on two calls in a
 row with different scores, since the shared array keeps the previous call's contents.
 """
 import numpy as np
 import pytest
 
+import oracle
 from compressed_sparse_attention_08_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -44,6 +46,8 @@ def test_noalloc_topk_matches_workspace_variant_twice():
         got = torch.full((rows, k), 7, dtype=torch.int32, device="cuda")
         m.dsv4_topk_noalloc(s, nv, got)
         torch.cuda.synchronize()
+        ref = oracle.topk(s_np, n_np, k)
+        assert np.array_equal(got.cpu().numpy(), ref), f"call {call}: indices differ from the oracle's top-k"
         assert torch.equal(got, want), f"call {call}: indices differ from dsv4_topk"
 
 
