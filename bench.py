@@ -50,6 +50,9 @@ def parse():
                     help="time only the decode step with the FP8 index-key cache")
     ap.add_argument("--decode-workload", type=int, choices=[1, 2], default=None,
                     help="time only the decode step of workload 1 (8K context, batch 16) or 2 (HCA)")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="time only the headline step (no end-to-end, scorer, prefill, FP8 or other "
+                         "workloads): a short run for profilers")
     return ap.parse_args()
 
 
@@ -731,6 +734,15 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
+    if args.headline_only:
+        clk = clocks.stop()
+        if rank == 0:
+            kb, gb, ob = step_bytes(wl)
+            peak, _ = measured_peaks()
+            print(json.dumps({"metric": METRIC, "value": job_throughput(B, world, ms), "unit": "tokens/s",
+                              "ms_per_step": ms, "launches_per_step": launches, "config": workload_config(wl),
+                              "step_frac": (kb + gb + ob) / (ms * 1e-3) / 1e9 / peak, "clocks": clk}), flush=True)
+        return
 
     # ---- dominant kernel alone: the scoring launch, events on its stream
     score_ws = torch.empty(256, dtype=torch.uint8, device="cuda")

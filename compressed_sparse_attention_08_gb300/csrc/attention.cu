@@ -844,7 +844,9 @@ attn_rows_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
 // another.
 constexpr long long kRowWalkCtas = 304;
 
-struct DecodePlan { int n_chunks, nh, n_hg; bool walk; };
+// walk: one CTA walks each (query row, head group); sized_walk: the workspace is sized for that
+// (no partials), which depends on the arguments alone (the 304-pair rule in the header).
+struct DecodePlan { int n_chunks, nh, n_hg; bool walk, sized_walk; };
 
 DecodePlan decode_plan(const dsv4_attn_args& a) {
     DecodePlan d{};
@@ -852,7 +854,17 @@ DecodePlan decode_plan(const dsv4_attn_args& a) {
     d.n_chunks = static_cast<int>((slots + kFC - 1) / kFC);
     d.nh = a.heads % 32 == 0 ? 32 : 16;          // every group full, or one group of <= 16
     d.n_hg = (a.heads + d.nh - 1) / d.nh;
-    d.walk = static_cast<long long>(a.batch) * a.n_q * d.n_hg >= kRowWalkCtas;
+    const long long pairs = static_cast<long long>(a.batch) * a.n_q * d.n_hg;
+    d.sized_walk = pairs >= kRowWalkCtas;
+    d.walk = d.sized_walk;
+    // Rows of at most two chunks whose split CTAs (one per chunk) need a second wave on the
+    // device while one CTA per pair fits in one: walking takes one wave and no merge kernel
+    // (the dense HCA step: 64 sequences x 2 head groups x 2 chunks, where the split form took
+    // 21 us in two waves plus 15 us of merge kernel on GB300).
+    if (!d.walk && d.n_chunks <= 2) {
+        const int sms = sm_count() > 0 ? sm_count() : 148;
+        if (pairs <= sms && pairs * d.n_chunks > sms) d.walk = true;
+    }
     return d;
 }
 
@@ -939,7 +951,7 @@ int run_decode(const dsv4_attn_args& a, const DecodePlan& dp, uint8_t* ws, uint3
 
 size_t attn_ws_bytes(const dsv4_attn_args& a) {
     const DecodePlan dp = decode_plan(a);
-    if (dp.walk) return 0;                             // no partials
+    if (dp.sized_walk) return 0;                       // no partials
     const size_t rows = static_cast<size_t>(a.batch) * a.n_q;
     const size_t hs = static_cast<size_t>(dp.n_hg) * dp.nh;
     return align_up(rows * dp.n_chunks * hs * 2 * 4, 256) +

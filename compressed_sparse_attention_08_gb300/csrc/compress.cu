@@ -43,6 +43,8 @@ constexpr int kMaxChan = 4;          // channels per thread: dim <= 1024
 // tokens per load round (every channel's loads in flight together): 4 for short blocks under
 // the register bound above, 8 for long blocks (ratio >= 16, where nothing runs beside)
 constexpr int kChunkShort = 4, kChunkLong = 8, kLongRatio = 16;
+// long blocks with 8-channel vector loads: threads and tokens per load round
+constexpr int kWideThreads = 512, kWideRound = 4;
 constexpr int kMaxPairs = 64;        // rope_dim <= 128
 
 struct CompressJob {
@@ -86,6 +88,9 @@ struct EntryIn {
                                  // dim - rope_dim for the mixed KV storage)
     __nv_bfloat16* dst_rope;     // mixed KV storage: channels [q_dim, dim) as bf16, or null
 };
+
+template <int NT>
+__device__ void entry_finish(const EntryIn& in, const double* freq, float* y, float* warp_sum);
 
 // The whole CTA (kThreads) computes one entry: per-channel online softmax of Z + bias over the
 // pooled tokens and the weighted sum of C in fp32, RMSNorm over the dim channels, RoPE of the
@@ -154,14 +159,24 @@ __device__ void entry_math(const EntryIn& in, const double* freq, float* y, floa
     };
     if (in.aC) segment(in.aC, in.aZ, in.bias);          // stream a: bias columns [0, dim)
     segment(in.oC + in.own_off, in.oZ + in.own_off, in.bias + in.own_off);
-    float x[kMaxChan];
-    float sq = 0.f;
 #pragma unroll
     for (int i = 0; i < kMaxChan; ++i) {
         const int c = tid + i * kThreads;
-        x[i] = c < dim ? num[i] / den[i] : 0.f;
-        sq = fmaf(x[i], x[i], sq);
+        if (c < dim) y[c] = num[i] / den[i];
     }
+    __syncthreads();
+    entry_finish<kThreads>(in, freq, y, warp_sum);
+}
+
+// RMSNorm, RoPE and the output of an entry whose pooled channels x_c are in y[0, dim) (written
+// by every thread of the CTA before a barrier). Thread t takes channels t + NT i for the
+// sum of squares, as the pooling did.
+template <int NT>
+__device__ void entry_finish(const EntryIn& in, const double* freq, float* y, float* warp_sum) {
+    const int tid = threadIdx.x;
+    const int dim = in.dim;
+    float sq = 0.f;
+    for (int c = tid; c < dim; c += NT) sq = fmaf(y[c], y[c], sq);
     // RMSNorm: mean of x^2 over all dim channels
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
@@ -169,16 +184,12 @@ __device__ void entry_math(const EntryIn& in, const double* freq, float* y, floa
     __syncthreads();
     float tot = 0.f;
 #pragma unroll
-    for (int k = 0; k < kThreads / 32; ++k) tot += warp_sum[k];
+    for (int k = 0; k < NT / 32; ++k) tot += warp_sum[k];
     const float inv = 1.0f / sqrtf(tot / static_cast<float>(dim) + in.eps);
-#pragma unroll
-    for (int i = 0; i < kMaxChan; ++i) {
-        const int c = tid + i * kThreads;
-        if (c < dim) y[c] = x[i] * inv * in.gamma[c];
-    }
+    for (int c = tid; c < dim; c += NT) y[c] = y[c] * inv * in.gamma[c];
     __syncthreads();
     // RoPE: pair p rotates channels (d0, d0 + 1), d0 = dim - rope_dim + 2p, by pos * f_p
-    for (int p = tid; p < in.rope_dim / 2; p += kThreads) {
+    for (int p = tid; p < in.rope_dim / 2; p += NT) {
         const int d0 = dim - in.rope_dim + 2 * p;
         float sn, cs;
         sincosf(reduced_angle(in.pos * freq[p]), &sn, &cs);
@@ -188,40 +199,121 @@ __device__ void entry_math(const EntryIn& in, const double* freq, float* y, floa
     }
     __syncthreads();
     if (in.dst)
-        for (int c = tid; c < dim; c += kThreads) in.dst[c] = __float2bfloat16_rn(y[c]);
+        for (int c = tid; c < dim; c += NT) in.dst[c] = __float2bfloat16_rn(y[c]);
     if (in.dst8) {
         // FP8 E4M3 channels [0, q_dim): scale = amax / 448 over them (fp32), code =
         // E4M3(y / scale); the mixed storage keeps channels [q_dim, dim) (the RoPE part) as bf16
         const int qd = in.q_dim;
         float amax = 0.f;
-        for (int c = tid; c < qd; c += kThreads) amax = fmaxf(amax, fabsf(y[c]));
+        for (int c = tid; c < qd; c += NT) amax = fmaxf(amax, fabsf(y[c]));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        __syncthreads();                         // every thread has read warp_sum above
         if ((tid & 31) == 0) warp_sum[tid >> 5] = amax;
         __syncthreads();
         float m = 0.f;
 #pragma unroll
-        for (int k = 0; k < kThreads / 32; ++k) m = fmaxf(m, warp_sum[k]);
+        for (int k = 0; k < NT / 32; ++k) m = fmaxf(m, warp_sum[k]);
         const float sc = m > 0.f ? m / 448.0f : 1.0f;
         if (tid == 0) *in.dst_scale = sc;
-        for (int c = tid; c < qd; c += kThreads)
+        for (int c = tid; c < qd; c += NT)
             in.dst8[c] = static_cast<uint8_t>(__nv_cvt_float_to_fp8(y[c] / sc, __NV_SATFINITE, __NV_E4M3));
         if (in.dst_rope)
-            for (int c = qd + tid; c < dim; c += kThreads) in.dst_rope[c - qd] = __float2bfloat16_rn(y[c]);
+            for (int c = qd + tid; c < dim; c += NT) in.dst_rope[c - qd] = __float2bfloat16_rn(y[c]);
     }
+}
+
+// Long blocks (ratio >= kLongRatio, dim a multiple of 8): the pooled tokens are shared out over
+// NT / (dim / 8) token groups, each thread taking 8 channels (16-byte loads of C and Z, two of
+// the bias) of every NT / (dim / 8)-th token, kRound tokens per round with all of a round's
+// loads issued before any use; each group's online-softmax state (max, denominator, weighted
+// sum per channel) then goes through shared memory and the groups are merged per channel into
+// y. Dependent load rounds: ratio / (groups * kRound) instead of ratio / kChunkLong.
+template <int NT, int kRound>
+__device__ void pool_wide(const EntryIn& in, float* y, float* st /* [3][NT * 8] */) {
+    const int tid = threadIdx.x;
+    const int dim = in.dim, ratio = in.ratio;
+    const int cg_n = dim / 8, groups = NT / cg_n;
+    const int cg = tid % cg_n, tg = tid / cg_n;
+    const size_t w = in.w;
+    float m[8], den[8], num[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) { m[j] = -INFINITY; den[j] = 0.f; num[j] = 0.f; }
+    auto segment = [&](const __nv_bfloat16* Cs, const __nv_bfloat16* Zs, const float* bs) {
+        for (int t0 = tg; t0 < ratio; t0 += groups * kRound) {
+            uint4 cr[kRound], zr[kRound];
+            float4 b0[kRound], b1[kRound];
+#pragma unroll
+            for (int u = 0; u < kRound; ++u) {
+                const int t = t0 + u * groups;
+                const size_t o = static_cast<size_t>(t < ratio ? t : tg) * w + cg * 8;
+                cr[u] = __ldg(reinterpret_cast<const uint4*>(Cs + o));
+                zr[u] = __ldg(reinterpret_cast<const uint4*>(Zs + o));
+                b0[u] = __ldg(reinterpret_cast<const float4*>(bs + o));
+                b1[u] = __ldg(reinterpret_cast<const float4*>(bs + o + 4));
+            }
+#pragma unroll
+            for (int u = 0; u < kRound; ++u) {
+                if (t0 + u * groups >= ratio) break;
+                const uint32_t zw[4] = {zr[u].x, zr[u].y, zr[u].z, zr[u].w};
+                const uint32_t cw[4] = {cr[u].x, cr[u].y, cr[u].z, cr[u].w};
+                const float bb[8] = {b0[u].x, b0[u].y, b0[u].z, b0[u].w, b1[u].x, b1[u].y, b1[u].z, b1[u].w};
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float a = ((j & 1) ? bf16_hi(zw[j >> 1]) : bf16_lo(zw[j >> 1])) + bb[j];
+                    const float cv = (j & 1) ? bf16_hi(cw[j >> 1]) : bf16_lo(cw[j >> 1]);
+                    const float mn = fmaxf(m[j], a);
+                    const float sc = m[j] == -INFINITY ? 0.f : expf(m[j] - mn);
+                    const float e = expf(a - mn);
+                    den[j] = fmaf(den[j], sc, e);
+                    num[j] = fmaf(num[j], sc, e * cv);      // no bias on C
+                    m[j] = mn;
+                }
+            }
+        }
+    };
+    if (tg < groups) {
+        if (in.aC) segment(in.aC, in.aZ, in.bias);      // stream a: bias columns [0, dim)
+        segment(in.oC + in.own_off, in.oZ + in.own_off, in.bias + in.own_off);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int c = cg * 8 + j;
+            st[tg * dim + c] = m[j];
+            st[NT * 8 + tg * dim + c] = den[j];
+            st[2 * NT * 8 + tg * dim + c] = num[j];
+        }
+    }
+    __syncthreads();
+    // merge the groups per channel: x_c = sum_g num_g e^(m_g - M) / sum_g den_g e^(m_g - M)
+    for (int c = tid; c < dim; c += NT) {
+        float M = -INFINITY;
+        for (int g = 0; g < groups; ++g) M = fmaxf(M, st[g * dim + c]);
+        float dn = 0.f, nm = 0.f;
+        for (int g = 0; g < groups; ++g) {
+            const float mg = st[g * dim + c];
+            const float e = mg == -INFINITY ? 0.f : expf(mg - M);
+            dn = fmaf(st[NT * 8 + g * dim + c], e, dn);
+            nm = fmaf(st[2 * NT * 8 + g * dim + c], e, nm);
+        }
+        y[c] = nm / dn;
+    }
+    __syncthreads();
 }
 
 // zero_p/zero_n16: a workspace region (16-byte words) this launch clears for the kernels after
 // it (the fused decode step), so the step needs no separate memset; they read it only after
 // waiting for this grid.
-template <int kChunk, int kMinBlocks>
-__global__ void __launch_bounds__(kThreads, kMinBlocks)
+// NT threads; kWide: the long-block pooling of pool_wide (dim a multiple of 8; its group states
+// in dynamic shared memory), else entry_math (NT = kThreads).
+template <int kChunk, int kMinBlocks, int NT, bool kWide>
+__global__ void __launch_bounds__(NT, kMinBlocks)
 compress_kernel(const __grid_constant__ CompressJob j0, const __grid_constant__ CompressJob j1,
                 uint4* zero_p, unsigned zero_n16) {
+    static_assert(kWide || NT == kThreads, "the per-channel pooling runs on kThreads threads");
     pdl_trigger();
     {
-        const unsigned nthr = gridDim.x * gridDim.y * gridDim.z * kThreads;
-        const unsigned gt = ((blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x) * kThreads + threadIdx.x;
+        const unsigned nthr = gridDim.x * gridDim.y * gridDim.z * NT;
+        const unsigned gt = ((blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x) * NT + threadIdx.x;
         for (unsigned i = gt; i < zero_n16; i += nthr) zero_p[i] = make_uint4(0, 0, 0, 0);
     }
     // every field of the selected job once, into registers (a runtime choice between two
@@ -254,7 +346,7 @@ compress_kernel(const __grid_constant__ CompressJob j0, const __grid_constant__ 
     if (b >= n_blocks || s >= batch) return;
 
     __shared__ float y[1024];
-    __shared__ float warp_sum[kThreads / 32];
+    __shared__ float warp_sum[NT / 32];
     __shared__ double freq[kMaxPairs];
     if (tid < kMaxPairs) freq[tid] = second ? j1.freq[tid] : j0.freq[tid];
     // loads that do not depend on the reduction, issued early
@@ -302,7 +394,13 @@ compress_kernel(const __grid_constant__ CompressJob j0, const __grid_constant__ 
     in.dst_scale = in_range && out_fp8 ? out_scalep + orow : nullptr;
     in.q_dim = q_dim;
     in.dst_rope = in_range && out_fp8 == 2 ? out_ropep + orow * (dim - q_dim) : nullptr;
-    entry_math<kChunk>(in, freq, y, warp_sum);
+    if constexpr (kWide) {
+        extern __shared__ float group_state[];  // [3][NT * 8]
+        pool_wide<NT, kWideRound>(in, y, group_state);
+        entry_finish<NT>(in, freq, y, warp_sum);
+    } else {
+        entry_math<kChunk>(in, freq, y, warp_sum);
+    }
 }
 
 CompressJob make_job(const dsv4_compress_args& a) {
@@ -435,11 +533,28 @@ int launch_compress2(const dsv4_compress_args* a, const dsv4_compress_args* b, c
     dim3 grid(nb, bs, b ? 2 : 1);
     count_launch();
     const int rmax = j0.ratio > j1.ratio ? j0.ratio : j1.ratio;
-    if (rmax >= kLongRatio)
-        return launch_k(compress_kernel<kChunkLong, 1>, grid, dim3(kThreads), 0, stream, false, j0, j1,
-                        static_cast<uint4*>(zero), n16) == cudaSuccess
+    if (rmax >= kLongRatio) {
+        // every job's channels in 8-channel groups (and their rows 16-byte aligned): the wide
+        // pooling, its group states (3 x 512 x 8 floats) in dynamic shared memory
+        const bool wide = j0.dim % 8 == 0 && (!b || j1.dim % 8 == 0);
+        if (wide) {
+            constexpr size_t kStateBytes = 3ull * kWideThreads * 8 * sizeof(float);
+            if (once_per_device(reinterpret_cast<const void*>(compress_kernel<kChunkLong, 1, kWideThreads, true>),
+                                kAttrLaunch, [] {
+                                    return cudaFuncSetAttribute(compress_kernel<kChunkLong, 1, kWideThreads, true>,
+                                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                                static_cast<int>(kStateBytes));
+                                }) != cudaSuccess)
+                return DSV4_ERR_LAUNCH;
+            return launch_k(compress_kernel<kChunkLong, 1, kWideThreads, true>, grid, dim3(kWideThreads),
+                            kStateBytes, stream, false, j0, j1, static_cast<uint4*>(zero), n16) == cudaSuccess
+                       ? DSV4_OK : DSV4_ERR_LAUNCH;
+        }
+        return launch_k(compress_kernel<kChunkLong, 1, kThreads, false>, grid, dim3(kThreads), 0, stream, false, j0,
+                        j1, static_cast<uint4*>(zero), n16) == cudaSuccess
                    ? DSV4_OK : DSV4_ERR_LAUNCH;
-    return launch_k(compress_kernel<kChunkShort, 2>, grid, dim3(kThreads), 0, stream, false, j0, j1,
+    }
+    return launch_k(compress_kernel<kChunkShort, 2, kThreads, false>, grid, dim3(kThreads), 0, stream, false, j0, j1,
                     static_cast<uint4*>(zero), n16) == cudaSuccess
                ? DSV4_OK : DSV4_ERR_LAUNCH;
 }
