@@ -252,23 +252,36 @@ __device__ void pool_wide(const EntryIn& in, float* y, float* st /* [3][NT * 8] 
                 b0[u] = __ldg(reinterpret_cast<const float4*>(bs + o));
                 b1[u] = __ldg(reinterpret_cast<const float4*>(bs + o + 4));
             }
+            // the round's logits; one rescale of the running sums per round
+            float a[kRound][8], cv[kRound][8];
 #pragma unroll
             for (int u = 0; u < kRound; ++u) {
-                if (t0 + u * groups >= ratio) break;
+                const bool ok = t0 + u * groups < ratio;
                 const uint32_t zw[4] = {zr[u].x, zr[u].y, zr[u].z, zr[u].w};
                 const uint32_t cw[4] = {cr[u].x, cr[u].y, cr[u].z, cr[u].w};
                 const float bb[8] = {b0[u].x, b0[u].y, b0[u].z, b0[u].w, b1[u].x, b1[u].y, b1[u].z, b1[u].w};
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const float a = ((j & 1) ? bf16_hi(zw[j >> 1]) : bf16_lo(zw[j >> 1])) + bb[j];
-                    const float cv = (j & 1) ? bf16_hi(cw[j >> 1]) : bf16_lo(cw[j >> 1]);
-                    const float mn = fmaxf(m[j], a);
-                    const float sc = m[j] == -INFINITY ? 0.f : expf(m[j] - mn);
-                    const float e = expf(a - mn);
-                    den[j] = fmaf(den[j], sc, e);
-                    num[j] = fmaf(num[j], sc, e * cv);      // no bias on C
-                    m[j] = mn;
+                    a[u][j] = ok ? ((j & 1) ? bf16_hi(zw[j >> 1]) : bf16_lo(zw[j >> 1])) + bb[j] : -INFINITY;
+                    cv[u][j] = ok ? ((j & 1) ? bf16_hi(cw[j >> 1]) : bf16_lo(cw[j >> 1])) : 0.f;
                 }
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                float mc = a[0][j];
+#pragma unroll
+                for (int u = 1; u < kRound; ++u) mc = fmaxf(mc, a[u][j]);
+                const float mn = fmaxf(m[j], mc);
+                const float sc = m[j] == -INFINITY ? 0.f : expf(m[j] - mn);
+                den[j] *= sc;
+                num[j] *= sc;
+#pragma unroll
+                for (int u = 0; u < kRound; ++u) {
+                    const float e = a[u][j] == -INFINITY ? 0.f : expf(a[u][j] - mn);
+                    den[j] += e;
+                    num[j] = fmaf(e, cv[u][j], num[j]);   // no bias on C
+                }
+                m[j] = mn;
             }
         }
     };
