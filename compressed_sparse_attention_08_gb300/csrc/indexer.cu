@@ -142,6 +142,10 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
     using F = KeyFmt<FP8>;
     constexpr int kStageKeys = F::kStageKeys, kSub = F::kSub;
     constexpr int kEpiGroups = EG, kThreads = 64 + 128 * EG, kAccBufs = F::kAccBufs;
+    // one epilogue group per query of the unit (QB queries per MMA): both groups read every
+    // accumulator, group g its query g's columns, so a tile's two queries drain at once
+    constexpr bool kSplitQ = QB > 1 && EG == QB && !FP8;
+    constexpr int kWq = kSplitQ ? 1 : QB;              // queries whose weights a thread holds
     constexpr int kAccColsQ = kAccCols * QB;                 // TMEM columns per accumulator
     constexpr uint32_t kTmemCols = static_cast<uint32_t>(kAccBufs * kAccColsQ);   // 256 or 512
     static_assert(!(FP8 && QB > 1) && kTmemCols <= 512, "scorer shape");
@@ -156,7 +160,10 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) { mbar_init(&full_bar[i], 1); mbar_init(&empty_bar[i], 1); }
-        for (int i = 0; i < kAccBufs; ++i) { mbar_init(&tfull_bar[i], 1); mbar_init(&tempty_bar[i], 128); }
+        for (int i = 0; i < kAccBufs; ++i) {
+            mbar_init(&tfull_bar[i], 1);
+            mbar_init(&tempty_bar[i], kSplitQ ? 128 * kEpiGroups : 128);
+        }
         mbar_init(&qfull_bar, 1);
         mbar_init(&qempty_bar, 1);
         mbar_init(&done_bar, 1);
@@ -384,8 +391,9 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
         int acc = 0, cur_row = -1, nv = 0;
         uint32_t acc_phase = 0, fl_parity = 0;
         bool ok = true;
-        float wv[QB][NP];         // the unit's head weights (FP8: times the head's query scale)
-        int nvq[QB];              // keys visible to each query of the unit
+        float wv[kWq][NP];        // the unit's head weights (FP8: times the head's query scale)
+        int nvq[kWq];             // keys visible to each query of the unit
+        const int q_lo = kSplitQ ? group : 0;      // this thread's queries: q_lo .. q_lo + kWq - 1
         int nqu = 1;              // queries in the unit
         // Every wait of the epilogue is an mbarrier wait, bounded in time and ended early once
         // any role has given up, so a failure anywhere cannot leave a thread waiting.
@@ -460,16 +468,17 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                 cur_row = row;
                 nqu = unit_nq(row);
 #pragma unroll
-                for (int q = 0; q < QB; ++q) {
+                for (int qi = 0; qi < kWq; ++qi) {
+                    const int q = q_lo + qi;
                     const int qrow = unit_row(row, q < nqu ? q : 0);
-                    nvq[q] = QB == 1 ? nv : row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, qrow, nullptr);
+                    nvq[qi] = QB == 1 ? nv : row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, qrow, nullptr);
 #pragma unroll
                     for (int h = 0; h < NP; ++h) {
                         const size_t o = static_cast<size_t>(qrow) * p.heads + h;
                         float wh = h < p.heads ? __ldg(&p.w[o]) : 0.f;
                         // FP8: the query scale folds into the head's weight (ReLU commutes with it)
                         if (FP8 && h < p.heads) wh *= __ldg(&p.q_scale[o]);
-                        wv[q][h] = wh;
+                        wv[qi][h] = wh;
                     }
                 }
             }
@@ -479,15 +488,23 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                 const int my_acc = acc;
                 const uint32_t my_phase = acc_phase;
                 if (++acc == kAccBufs) { acc = 0; acc_phase ^= 1; }
-                if (kEpiGroups > 1 && (my_acc % kEpiGroups) != group) continue;
+                if (!kSplitQ && kEpiGroups > 1 && (my_acc % kEpiGroups) != group) continue;
                 if (!mbar_wait(&tfull_bar[my_acc], my_phase, &abort_flag, p.wait_ns)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const int key = tile * kTileKeys + lrow;
-                for (int q = 0; q < QB; ++q) {
-                    if (q >= nqu) break;
+                for (int qi = 0; qi < kWq; ++qi) {
+                    const int q = q_lo + qi;
+                    if (q >= nqu) {
+                        // (a unit's last query row may be missing: its group still frees the tile)
+                        if (kSplitQ) {
+                            tc_fence_before();
+                            mbar_arrive(&tempty_bar[my_acc]);
+                        }
+                        break;
+                    }
                     // exactly the NP columns of query q the MMA wrote (columns past them hold
                     // stale values)
                     uint32_t r[NP];
@@ -504,7 +521,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                         DSV4_TMEM_LD_32x32b_X16(ta, r);
                     }
                     tmem_wait_ld();
-                    if (q == nqu - 1) {                      // the accumulator is read out
+                    if (kSplitQ || q == nqu - 1) {           // the accumulator is read out
                         tc_fence_before();
                         mbar_arrive(&tempty_bar[my_acc]);
                     }
@@ -518,10 +535,10 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                         for (int h4 = 0; h4 < NP / 4; ++h4) {
                             fma_f32x2(a01, pack_f32x2(fmaxf(__uint_as_float(r[4 * h4 + 0]), 0.f),
                                                       fmaxf(__uint_as_float(r[4 * h4 + 1]), 0.f)),
-                                      pack_f32x2(wv[q][4 * h4 + 0], wv[q][4 * h4 + 1]));
+                                      pack_f32x2(wv[qi][4 * h4 + 0], wv[qi][4 * h4 + 1]));
                             fma_f32x2(a23, pack_f32x2(fmaxf(__uint_as_float(r[4 * h4 + 2]), 0.f),
                                                       fmaxf(__uint_as_float(r[4 * h4 + 3]), 0.f)),
-                                      pack_f32x2(wv[q][4 * h4 + 2], wv[q][4 * h4 + 3]));
+                                      pack_f32x2(wv[qi][4 * h4 + 2], wv[qi][4 * h4 + 3]));
                         }
                         float s0, s1, s2, s3;
                         unpack_f32x2(a01, s0, s1);
@@ -529,9 +546,9 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                         s = ((s0 + s1) + (s2 + s3)) * ks_cur[j];
                     } else {
 #pragma unroll
-                        for (int h = 0; h < NP; ++h) s = fmaf(wv[q][h], fmaxf(__uint_as_float(r[h]), 0.f), s);
+                        for (int h = 0; h < NP; ++h) s = fmaf(wv[qi][h], fmaxf(__uint_as_float(r[h]), 0.f), s);
                     }
-                    if (key < nvq[q]) {
+                    if (key < nvq[qi]) {
                         float* dst = p.scores + static_cast<size_t>(unit_row(row, q)) * p.max_comp + key;
                         if (p.reuse_keys) __stcs(dst, s);
                         else *dst = s;
@@ -690,14 +707,13 @@ int launch_scores(const dsv4_index_args& a, float* scores, uint32_t* hist, uint3
     const int n_pad = (a.heads + 15) / 16 * 16;
     // Two epilogue groups where the epilogue, not HBM, sets the pace: FP8 keys (512 keys per
     // stage). One group for bf16 keys, whose registers then leave room for a compressor CTA
-    // beside the scoring CTA (a second group did not speed up the many-row prefill either).
-    // Two queries per MMA with many rows of bf16 keys and no histogram to build (prefill):
-    // the key stages, not the epilogue, set its pace.
+    // beside the scoring CTA. Two queries per MMA with many rows of bf16 keys and no
+    // histogram to build (prefill), each query drained by its own epilogue group.
     const bool pairs = static_cast<long long>(a.batch) * a.n_q > sm_count() && a.n_q >= 2 && !hist;
 #define DSV4_SCORES_NP(np)                                                               \
     if (n_pad == np)                                                                     \
         return a.key_fp8 ? launch_scores_fmt<true, np, 2, 1>(a, scores, hist, eword, stream, fresh) \
-               : pairs   ? launch_scores_fmt<false, np, 1, 2>(a, scores, hist, eword, stream, fresh) \
+               : pairs   ? launch_scores_fmt<false, np, 2, 2>(a, scores, hist, eword, stream, fresh) \
                          : launch_scores_fmt<false, np, 1, 1>(a, scores, hist, eword, stream, fresh);
     DSV4_SCORES_NP(16)
     DSV4_SCORES_NP(32)
