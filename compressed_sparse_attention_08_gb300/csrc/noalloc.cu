@@ -4,7 +4,7 @@
 // code running inside an allocator callback or an allocator-free serving loop, a host
 // runtime that forbids cudaMalloc after start-up, or a plug-in handed only its input and
 // output buffers. dsv4_topk_noalloc serves them: its scratch space (error word, per-row
-// histograms and survivor lists of the long-row path) is one file-scope device array. The
+// histograms of the long-row path) is one file-scope device array. The
 // driver reserves the array on a GPU when this library's device code is loaded there, which
 // with lazy module loading happens at the first call of this entry point on that GPU (the
 // symbol lookup below); it stays reserved until the process exits. Callers should therefore

@@ -16,13 +16,12 @@
 // need_T). Two implementations of the same rule:
 //   * rows that fit in shared memory (max_comp <= kSmallCap): one CTA per row, keys in smem.
 //   * long rows (1M context: 262,144 scores): one thread-block cluster of 16 CTAs per row,
-//     one slice each. A histogram of the top 12 key bits per row (built by the scoring
-//     kernel's epilogue when the scores come from the indexer, else by a histogram kernel)
-//     gives the 12-bit bin that holds the k-th key; every CTA keeps, in index order, the
-//     elements of its slice at or above that bin (a few thousand of 262,144 in all) and
-//     counts bits 19..8 of the keys in that bin; counts, that second histogram and the kept
-//     elements meet in the shared memory of the cluster's first CTA, so one 8-bit radix pass
-//     over the short list gives the exact k-th key.
+//     one slice each, its scores in registers. A histogram of the top 12 key bits per row
+//     (built by the scoring kernel's epilogue when the scores come from the indexer, else by
+//     a histogram kernel) gives the 12-bit bin that holds the k-th key; the counts of bits
+//     19..8 of the keys in that bin, summed over the cluster, give its 24-bit prefix (an 8-bit
+//     pass over the few keys sharing that prefix gives the exact key when some are left out);
+//     every CTA then writes its own winners at the offset the cluster's counts give it.
 #include "common.cuh"
 #include "internal.h"
 
@@ -32,7 +31,6 @@ namespace {
 constexpr int kSmallCap = 32768;     // keys held in shared memory by the one-CTA path
 constexpr int kBins = 4096;          // top-12-bit histogram of the long-row path
 constexpr int kBinShift = 20;
-constexpr int kFinalCap = 12288;     // (key, index) pairs the finalizer keeps in smem
 constexpr int kMaxSlices = 64;
 constexpr int kNT = 1024;
 constexpr int kCl = 16;              // CTAs per row in the long-row cluster kernel (non-portable size)
@@ -192,7 +190,8 @@ topk_small_kernel(TopkRows t, uint32_t* eword) {
 // ------------------------------------------------------------------ long rows
 struct LongWs {
     uint32_t* hist;     // [rows, kBins]: top 12 key bits (bits 31..20) of every visible key
-    uint2* pairs;       // [rows, max_comp]: (key, index) survivors when they outnumber kFinalCap
+    uint32_t* h2;       // [rows, kBins]: bits 19..8 of the keys in the threshold bin
+    uint32_t* h3;       // [rows, 256]: bits 7..0 of the keys sharing the k-th key's prefix
 };
 
 __device__ __forceinline__ void slice_range(int n, int L, int p, int& lo, int& hi) {
@@ -260,40 +259,38 @@ topk_hist_kernel(TopkRows t, LongWs w, int L, uint32_t* eword) {
         if (h[i]) atomicAdd(&g[i], h[i]);
 }
 
-// Long rows, one cluster of CL CTAs per row; CTA r takes slice r of the row. Every CTA: the
-// 12-bit threshold bin tb from the row histogram; its survivors (key bin >= tb), counted;
-// bits 19..8 of its keys in bin tb into a shared histogram. Through distributed shared
-// memory each CTA then adds that histogram into CTA 0's and posts its count there; after a
-// cluster barrier every CTA knows every count, and writes its survivors, in index order,
-// straight into CTA 0's shared list at its offset (into the global list when the survivors
-// outnumber the shared list). After a last cluster barrier CTA 0 finds the second-level bin,
-// so one 8-bit radix pass (none when the whole sub-bin is selected) gives the exact k-th key,
-// and writes the k indices. No global atomics, tickets or round trips through L2 between
-// the phases.
+// Long rows, one cluster of CL CTAs per row; CTA r takes slice r of the row (its scores held
+// in registers). Every CTA: the 12-bit threshold bin tb from the row histogram; bits 19..8 of
+// its keys in bin tb counted in shared memory and added into the row's sub-bin counts in L2
+// (global atomics spread over the L2 slices). After a cluster barrier every CTA reads the
+// summed counts back (one load per thread) and finds the k-th key's 24-bit prefix itself;
+// when some keys with that prefix are left out, a second round over bits 7..0 gives the
+// exact key T. Each CTA then counts its keys above T and its ties at T, the counts go to
+// every CTA through distributed shared memory, and after a last cluster barrier each CTA
+// writes its own winners, in index order, at its offset in the row's index list (ties at T
+// to the lower index: CTA order is index order). No survivor list is gathered and no CTA's
+// shared memory is the target of more than a few dozen remote accesses: remote accesses
+// into one SM are served one at a time, so funnelling the row's data into one CTA costs
+// more than the round trips through L2.
 template <int NT, int CL>
 __global__ void __launch_bounds__(NT, 1)
 topk_cluster_kernel(TopkRows t, LongWs w, int L, uint32_t* eword) {
     constexpr int NW = NT / 32;
     constexpr int kRegs = 16;                    // scores per lane kept in registers
     constexpr int per_bin = kBins / NT;
-    extern __shared__ uint2 spairs[];           // CTA 0: the survivors (kFinalCap pairs)
     __shared__ uint32_t h2loc[kBins];           // this CTA's bits 19..8 of bin tb
-    __shared__ uint32_t h2sum[kBins];           // CTA 0: the row's
-    __shared__ uint32_t hist[256];
-    __shared__ int s_a[32], s_b[32], s_w[32];
+    __shared__ uint32_t h3loc[256];             // its bits 7..0 of the k-th key's prefix (rare)
+    __shared__ int s_a[32], s_gw[32], s_tw[32], s_tot[2];
     __shared__ int bc[3];
-    __shared__ int cl_count[CL];                // CTA 0: survivors per CTA
-    __shared__ int offs[CL + 1];
+    __shared__ uint32_t s_T[2];                 // the exact key and the ties taken (third pass)
+    __shared__ int s_cnt[CL][2];                // every CTA's (keys above T, ties at T)
     pdl_trigger();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t rank = cluster_rank();
     const int row = blockIdx.y;
     const int k = t.top_k;
-    // the sums CTA 0 collects start at zero before any CTA adds into them
-    for (int i = threadIdx.x; i < kBins; i += NT) { h2loc[i] = 0; h2sum[i] = 0; }
-    if (threadIdx.x < CL) cl_count[threadIdx.x] = 0;
-    __syncthreads();
-    cluster_arrive();
+    for (int i = threadIdx.x; i < kBins; i += NT) h2loc[i] = 0;
+    for (int i = threadIdx.x; i < 256; i += NT) h3loc[i] = 0;
     pdl_wait();
     // The row histogram, this slice's scores and the visible count do not depend on one
     // another: issue their loads together. The slice is read over its full extent (inside
@@ -311,7 +308,7 @@ topk_cluster_kernel(TopkRows t, LongWs w, int L, uint32_t* eword) {
     const bool in_regs = wper <= 32 * kRegs;     // the same for every warp of the CTA
     const float* sc = t.scores + static_cast<size_t>(row) * t.max_comp;
     // loaded once, up front, and kept (a volatile load: the compiler may not re-issue it in
-    // the two passes below)
+    // the passes below)
     float v0[kRegs];
     if (in_regs) {
 #pragma unroll
@@ -323,117 +320,158 @@ topk_cluster_kernel(TopkRows t, LongWs w, int L, uint32_t* eword) {
     }
     const int n = row_visible(t.n_vis, t.n_comp, t.q_pos, t.n_q, t.ratio, t.max_comp, row, eword);
     int32_t* out = t.idx_out + static_cast<size_t>(row) * k;
-    if (n <= k) {                                // every visible entry is selected
+    if (n <= k) {                                // every visible entry is selected (every CTA)
         const int per = (k + CL - 1) / CL;
         write_all(out, n, k, static_cast<int>(rank) * per + threadIdx.x, (static_cast<int>(rank) + 1) * per, NT);
-        cluster_wait();
         return;
     }
     const int hi = whi < n ? whi : n;            // visible end of this warp's run
-    // 1. the 12-bit bin tb holding the k-th largest key, and how many keys lie above it
+    // The passes below are bound by instruction issue (16,384 keys per SM), so each key is
+    // formed once and entries past the visible end get key 0. No score has key 0 (it is a NaN
+    // bit pattern; -inf is 0x007fffff), so it lies in no bin from tb on (tb >= 7), shares no
+    // prefix of the k-th key and is never >= T (T > 0): no pass needs an "i < hi" test.
+    uint32_t kr[kRegs];
+#pragma unroll
+    for (int r = 0; r < kRegs; ++r) kr[r] = wlo + r * 32 + lane < hi ? float_to_key(v0[r]) : 0u;
+    // key r of this lane's run (from registers, or read again from L2 for long slices)
+    auto key_of = [&](int b0, int r, int& i) -> uint32_t {
+        i = b0 + r * 32 + lane;
+        return in_regs ? kr[r] : (i < hi ? float_to_key(__ldcg(&sc[i])) : 0u);
+    };
+    // 1. the 12-bit bin tb holding the k-th largest key, and how many keys lie above it (the
+    //    scan's barriers also order the zeroing of h2loc before its use); bits 19..8 of this
+    //    CTA's keys in bin tb into its sub-bin counts, then into the row's in L2
     find_bin<NT>(c, k, s_a, bc);
     const uint32_t tb = static_cast<uint32_t>(bc[0]);
     const int above = bc[1];
-    // 2. count this warp's survivors (bin >= tb); keys in bin tb also go into the second
-    //    histogram
-    int cnt = 0;
     for (int b0 = wlo; b0 < whi; b0 += 32 * kRegs) {
 #pragma unroll
         for (int r = 0; r < kRegs; ++r) {
-            const int i = b0 + r * 32 + lane;
-            const bool vis = i < hi;
-            const uint32_t key = float_to_key(in_regs ? v0[r] : (vis ? __ldcg(&sc[i]) : 0.f));
-            const uint32_t bin = key >> kBinShift;
-            const unsigned bs = __ballot_sync(0xffffffffu, vis && bin >= tb);
-            if (bs == 0u) continue;                 // most groups of 32 keep nothing
-            cnt += __popc(bs);
-            // few keys fall in bin tb, spread over 4096 sub-bins: plain atomics
-            if (vis && bin == tb) atomicAdd(&h2loc[(key >> 8) & (kBins - 1)], 1u);
+            int i;
+            const uint32_t key = key_of(b0, r, i);
+            // few keys fall in bin tb, mostly spread over the 4096 sub-bins (lanes that hit
+            // the same sub-bin, as heavy ties do, add once)
+            hist_add(h2loc, (key >> 8) & (kBins - 1), (key >> kBinShift) == tb);
         }
     }
-    if (lane == 0) s_w[warp] = cnt;
     __syncthreads();
-    if (warp == 0) {
-        const int v = lane < NW ? s_w[lane] : 0;
-        const int vi = warp_incl(v);
-        if (lane < NW) s_w[lane] = vi - v;       // the warp's offset within the CTA
-        if (lane == NW - 1) s_b[0] = vi;         // the CTA's count
+    uint32_t* g2 = w.h2 + static_cast<size_t>(row) * kBins;
+    for (int i = threadIdx.x; i < kBins; i += NT) {
+        const uint32_t v = h2loc[i];
+        if (v) atomicAdd(&g2[i], v);
     }
-    // 3. post the count and the second histogram to CTA 0 (its sums are zeroed: wait for that)
-    cluster_wait();
-    __syncthreads();
-    if (threadIdx.x == 0) st_cluster_u32(cluster_map(&cl_count[rank], 0), static_cast<uint32_t>(s_b[0]));
-    {
-        const uint32_t h2r = cluster_map(h2sum, 0);
-        for (int i = threadIdx.x; i < kBins; i += NT) {
-            const uint32_t v = h2loc[i];
-            if (v) red_cluster_add(h2r + 4u * static_cast<uint32_t>(i), v);
-        }
-    }
-    cluster_arrive();
-    cluster_wait();
-    // 4. every CTA's offset in the row's list; the survivors go there in index order
-    if (warp == 0) {
-        const int v = lane < CL ? static_cast<int>(ld_cluster_u32(cluster_map(&cl_count[lane], 0))) : 0;
-        const int vi = warp_incl(v);
-        if (lane < CL) offs[lane + 1] = vi;
-        if (lane == 0) offs[0] = 0;
-    }
-    __syncthreads();
-    const int total = offs[CL];
-    const bool in_smem = total <= kFinalCap;
-    {
-        int pos = offs[rank] + s_w[warp];
-        const unsigned lt = (1u << lane) - 1u;
-        const uint32_t sp0 = cluster_map(spairs, 0);
-        uint2* gp = w.pairs + static_cast<size_t>(row) * t.max_comp;
-        for (int b0 = wlo; b0 < whi; b0 += 32 * kRegs) {
-#pragma unroll
-            for (int r = 0; r < kRegs; ++r) {
-                const int i = b0 + r * 32 + lane;
-                const uint32_t key = float_to_key(in_regs ? v0[r] : (i < hi ? __ldcg(&sc[i]) : 0.f));
-                const bool keep = i < hi && (key >> kBinShift) >= tb;
-                const unsigned bk = __ballot_sync(0xffffffffu, keep);
-                if (bk == 0u) continue;
-                if (keep) {
-                    const int at = pos + __popc(bk & lt);
-                    if (in_smem) st_cluster_v2(sp0 + 8u * static_cast<uint32_t>(at), key, static_cast<uint32_t>(i));
-                    else gp[at] = make_uint2(key, static_cast<uint32_t>(i));
-                }
-                pos += __popc(bk);
-            }
-        }
-    }
-    cluster_arrive();
-    cluster_wait();
-    if (rank != 0) return;
-    // 5. CTA 0: the 12-bit sub-bin (bits 19..8) of bin tb holding the k-th key
+    cluster_arrive();                            // release: this CTA's counts are in L2
+    cluster_wait();                              // acquire: so are every other CTA's
+    // 2. every CTA: the sub-bin of the k-th key from the row's sums
     int c2[per_bin];
 #pragma unroll
     for (int i = 0; i < per_bin; ++i)
-        c2[i] = static_cast<int>(h2sum[kBins - 1 - (static_cast<int>(threadIdx.x) * per_bin + i)]);
+        c2[i] = static_cast<int>(__ldcg(&g2[kBins - 1 - (static_cast<int>(threadIdx.x) * per_bin + i)]));
     find_bin<NT>(c2, k - above, s_a, bc);
     const uint32_t prefix = (tb << kBinShift) | (static_cast<uint32_t>(bc[0]) << 8);
     const int need = k - above - bc[1];
-    const bool whole_sub_bin = need == bc[2] && prefix != 0u;   // every key of the sub-bin is in
     uint32_t T;
     int need_T;
-    auto finish = [&](auto key_at, auto idx_at) {
-        if (whole_sub_bin) {
-            // the k keys are exactly those at or above the sub-bin: no selection inside it
-            T = prefix - 1u;
-            need_T = 0;
-        } else {
-            radix_select<NT>(total, need, key_at, hist, bc, T, need_T, prefix, 32 - 8);
-        }
-        ordered_select<NT>(total, T, need_T, key_at, idx_at, out, s_a, s_b);
-    };
-    if (in_smem) {
-        finish([&](int i) { return spairs[i].x; }, [&](int i) { return static_cast<int32_t>(spairs[i].y); });
+    if (need == bc[2] && prefix != 0u) {
+        // the whole sub-bin is selected: the k keys are those at or above its lower edge
+        T = prefix - 1u;
+        need_T = 0;
     } else {
-        // degenerate score distributions (huge ties): the list in global memory
-        const uint2* gp = w.pairs + static_cast<size_t>(row) * t.max_comp;
-        finish([&](int i) { return __ldcg(&gp[i]).x; }, [&](int i) { return static_cast<int32_t>(__ldcg(&gp[i]).y); });
+        // 3. (rare) some keys with the k-th key's 24-bit prefix are left out: bits 7..0 of
+        //    those keys over the cluster give the exact key and how many of its ties are taken
+        for (int b0 = wlo; b0 < whi; b0 += 32 * kRegs) {
+#pragma unroll
+            for (int r = 0; r < kRegs; ++r) {
+                int i;
+                const uint32_t key = key_of(b0, r, i);
+                hist_add(h3loc, key & 255u, (key >> 8) == (prefix >> 8));
+            }
+        }
+        __syncthreads();
+        uint32_t* g3 = w.h3 + static_cast<size_t>(row) * 256;
+        for (int i = threadIdx.x; i < 256; i += NT) {
+            const uint32_t v = h3loc[i];
+            if (v) atomicAdd(&g3[i], v);
+        }
+        cluster_arrive();
+        cluster_wait();
+        if (warp == 0) {
+            int cc[8], sum = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                cc[i] = static_cast<int>(__ldcg(&g3[255 - (lane * 8 + i)]));
+                sum += cc[i];
+            }
+            const int inc = warp_incl(sum);
+            const int before = inc - sum;
+            if (before < need && inc >= need) {
+                int acc = before;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (acc + cc[i] >= need) {
+                        s_T[0] = prefix | static_cast<uint32_t>(255 - (lane * 8 + i));
+                        s_T[1] = static_cast<uint32_t>(need - acc);
+                        break;
+                    }
+                    acc += cc[i];
+                }
+            }
+        }
+        __syncthreads();
+        T = s_T[0];
+        need_T = static_cast<int>(s_T[1]);
+    }
+    // 4. this CTA's keys above T and ties at T, per warp and in all; the counts to every CTA
+    //    (every CTA has passed the barrier above, so its shared memory may be written)
+    int gt = 0, tie = 0;                         // this lane's, then the warp's
+    for (int b0 = wlo; b0 < whi; b0 += 32 * kRegs) {
+#pragma unroll
+        for (int r = 0; r < kRegs; ++r) {
+            int i;
+            const uint32_t key = key_of(b0, r, i);
+            gt += key > T;
+            tie += key == T;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        gt += __shfl_xor_sync(0xffffffffu, gt, o);
+        tie += __shfl_xor_sync(0xffffffffu, tie, o);
+    }
+    if (lane == 0) { s_gw[warp] = gt; s_tw[warp] = tie; }
+    __syncthreads();
+    if (warp == 0) {
+        const int g = lane < NW ? s_gw[lane] : 0, tt = lane < NW ? s_tw[lane] : 0;
+        const int gi = warp_incl(g), ti = warp_incl(tt);
+        if (lane < NW) { s_gw[lane] = gi - g; s_tw[lane] = ti - tt; }
+        if (lane == NW - 1) { s_tot[0] = gi; s_tot[1] = ti; }
+    }
+    __syncthreads();
+    if (threadIdx.x < CL) {
+        st_cluster_u32(cluster_map(&s_cnt[rank][0], threadIdx.x), static_cast<uint32_t>(s_tot[0]));
+        st_cluster_u32(cluster_map(&s_cnt[rank][1], threadIdx.x), static_cast<uint32_t>(s_tot[1]));
+    }
+    cluster_arrive();
+    cluster_wait();                              // every CTA's counts are in place
+    // 5. this CTA's winners in index order at its offset: keys above T before it in the row,
+    //    plus the ties at T taken before it
+    int gt_before = 0, tie_before = 0;
+    for (int r2 = 0; r2 < static_cast<int>(rank); ++r2) { gt_before += s_cnt[r2][0]; tie_before += s_cnt[r2][1]; }
+    int gb = gt_before + s_gw[warp], tbf = tie_before + s_tw[warp];
+    const unsigned lt = (1u << lane) - 1u;
+    for (int b0 = wlo; b0 < whi; b0 += 32 * kRegs) {
+#pragma unroll
+        for (int r = 0; r < kRegs; ++r) {
+            int i;
+            const uint32_t key = key_of(b0, r, i);
+            if (__ballot_sync(0xffffffffu, key >= T) == 0u) continue;   // most groups of 32 hold none
+            const bool g = key > T, tq = key == T;
+            const unsigned bg = __ballot_sync(0xffffffffu, g), bt = __ballot_sync(0xffffffffu, tq);
+            const int g_b = gb + __popc(bg & lt), t_b = tbf + __popc(bt & lt);
+            if (g || (tq && t_b < need_T)) out[g_b + (t_b < need_T ? t_b : need_T)] = i;
+            gb += __popc(bg);
+            tbf += __popc(bt);
+        }
     }
 }
 
@@ -456,14 +494,11 @@ LongPlan long_plan(int rows, int max_comp) {
 size_t topk_ws_bytes(int rows, int max_comp, int top_k) {
     (void)top_k;
     if (max_comp <= kSmallCap) return 0;
-    size_t b = 0;
-    b += align_up(static_cast<size_t>(rows) * kBins * 4, 256);   // the row histograms
-    b += align_up(static_cast<size_t>(rows) * max_comp * 8, 256);
-    return b;
+    return align_up(topk_hist_bytes(rows), 256);   // the row histograms, all zeroed per call
 }
 
 uint32_t* topk_hist_buffer(uint8_t* ws) { return reinterpret_cast<uint32_t*>(ws); }
-size_t topk_hist_bytes(int rows) { return static_cast<size_t>(rows) * kBins * 4; }
+size_t topk_hist_bytes(int rows) { return static_cast<size_t>(rows) * (2 * kBins + 256) * 4; }
 bool topk_uses_hist(int max_comp) { return max_comp > kSmallCap; }
 
 int launch_topk(const TopkRows& t, uint8_t* ws, uint32_t* eword, cudaStream_t stream) {
@@ -481,19 +516,16 @@ int launch_topk(const TopkRows& t, uint8_t* ws, uint32_t* eword, cudaStream_t st
     }
     const LongPlan pl = long_plan(t.rows, t.max_comp);
     LongWs w;
-    uint8_t* p = ws;
-    w.hist = reinterpret_cast<uint32_t*>(p);
-    p += align_up(static_cast<size_t>(t.rows) * kBins * 4, 256);
-    w.pairs = reinterpret_cast<uint2*>(p);
+    w.hist = reinterpret_cast<uint32_t*>(ws);
+    w.h2 = w.hist + static_cast<size_t>(t.rows) * kBins;
+    w.h3 = w.h2 + static_cast<size_t>(t.rows) * kBins;
     if (!t.hist_zeroed &&
         cudaMemsetAsync(w.hist, 0, topk_hist_bytes(t.rows), stream) != cudaSuccess)
         return DSV4_ERR_LAUNCH;
     if (once_per_device(reinterpret_cast<const void*>(topk_cluster_kernel<kNT, kCl>), kAttrLaunch, [] {
-            const cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel<kNT, kCl>,
-                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kFinalCap * 8);
-            if (e != cudaSuccess || kCl <= 8) return e;
-            return cudaFuncSetAttribute(topk_cluster_kernel<kNT, kCl>,
-                                        cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            return kCl <= 8 ? cudaSuccess
+                            : cudaFuncSetAttribute(topk_cluster_kernel<kNT, kCl>,
+                                                   cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         }) != cudaSuccess)
         return DSV4_ERR_LAUNCH;
     if (!t.hist_built) {
@@ -505,7 +537,7 @@ int launch_topk(const TopkRows& t, uint8_t* ws, uint32_t* eword, cudaStream_t st
     // slices of the cluster kernel: CTA r of a row's cluster takes [r * Lc, (r + 1) * Lc)
     const int Lc = (t.max_comp + kCl - 1) / kCl;
     count_launch();
-    return launch_cluster_k(topk_cluster_kernel<kNT, kCl>, dim3(kCl, t.rows), dim3(kNT), size_t(kFinalCap * 8),
+    return launch_cluster_k(topk_cluster_kernel<kNT, kCl>, dim3(kCl, t.rows), dim3(kNT), size_t(0),
                             stream, t.pdl, static_cast<unsigned>(kCl), t, w, Lc, eword) == cudaSuccess
                ? DSV4_OK : DSV4_ERR_LAUNCH;
 }

@@ -221,7 +221,8 @@ int dsv4_topk(const dsv4_topk_args* args, void* ws, size_t ws_bytes, dsv4_stream
  * results as dsv4_topk, but no workspace: the scratch it needs lives in a fixed 16 MiB
  * device array that the library holds on each GPU it runs on until the process exits.
  * Calls whose scratch need (dsv4_topk_workspace_size(args)) exceeds 16 MiB return
- * DSV4_ERR_INVALID_ARG before any launch (for 262,144-entry rows: up to 7 rows per call).
+ * DSV4_ERR_INVALID_ARG before any launch (rows of more than 32,768 entries need 33 KiB each:
+ * up to 496 such rows per call).
  * The first call on a device looks up the array's device address; with lazy module loading
  * that lookup is also when the driver reserves the 16 MiB on that device, so a failure to
  * reserve it comes back from that first call as DSV4_ERR_LAUNCH. Make the first call on

@@ -85,8 +85,8 @@ def test_indexer_rejects_on_host(lib, bad):
 def test_indexer_rejects_small_workspace(lib):
     a = _index_args()
     need = lib.dsv4_indexer_topk_workspace_size(ctypes.byref(a))
-    # scores (4 MiB) + top-k survivors (8 MiB) + histograms
-    assert need >= 4 * 262144 * 4 + 4 * 262144 * 8
+    # scores (4 MiB) + the top-k's per-row histograms (4096 + 4096 + 256 bins)
+    assert need >= 4 * 262144 * 4 + 4 * 8448 * 4
     assert lib.dsv4_indexer_topk(ctypes.byref(a), _p(9), need - 1, None) == 1
 
 

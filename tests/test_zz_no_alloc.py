@@ -53,9 +53,11 @@ def test_noalloc_topk_matches_workspace_variant_twice():
 
 def test_noalloc_topk_rejects_sizes_beyond_its_scratch():
     import compressed_sparse_attention_08_gb300 as m
-    s = torch.zeros(8, 262144, dtype=torch.float32, device="cuda")     # needs > 16 MiB
-    nv = torch.full((8,), 262144, dtype=torch.int32, device="cuda")
-    idx = torch.empty(8, 2048, dtype=torch.int32, device="cuda")
+    rows = 600                                    # 600 long rows need 33 KiB each: > 16 MiB
+    s = torch.zeros(rows, 32769, dtype=torch.float32, device="cuda")
+    nv = torch.full((rows,), 32769, dtype=torch.int32, device="cuda")
+    idx = torch.empty(rows, 64, dtype=torch.int32, device="cuda")
+    assert m.dsv4_topk_workspace_size(s, nv, idx) > (16 << 20)
     with pytest.raises(m.Dsv4Error) as e:
         m.dsv4_topk_noalloc(s, nv, idx)
     assert e.value.status == m.DSV4_ERR_INVALID_ARG
