@@ -206,16 +206,22 @@ struct FCfg {
     static constexpr int MT = D / 128;                               // M tiles of O^T
     static constexpr int U = D / 8;                                  // 16-byte pieces per row
     static constexpr size_t BOX = static_cast<size_t>(kFC) * 128;    // one 64-dim box of the tile
+    // 64 heads: the scores go through the query tile, which is dead once S^T is computed (a
+    // separate score buffer would not fit beside the 128 KB KV tile)
+    static constexpr bool kAliasS = NH > 32;
     static constexpr size_t OFF_Q = BOX * NBOX;
     static constexpr size_t OFF_P = OFF_Q + static_cast<size_t>(NBOX) * NH * 128;
-    static constexpr size_t OFF_S = OFF_P + 2ull * NH * 128;
-    static constexpr size_t OFF_R = OFF_S + static_cast<size_t>(kFC) * (NH + 1) * 4;
+    static constexpr size_t OFF_S = kAliasS ? OFF_Q : OFF_P + 2ull * NH * 128;
+    static constexpr size_t OFF_R = kAliasS ? OFF_P + 2ull * NH * 128 : OFF_S + static_cast<size_t>(kFC) * (NH + 1) * 4;
     static constexpr size_t OFF_OK = OFF_R + 2ull * 8 * NH * 4;
     static constexpr size_t OFF_BAR = align_up(OFF_OK + kFC * 4, 16);
     static constexpr size_t SMEM = OFF_BAR + 3 * 8 + 1024;           // + alignment slack
     static constexpr uint32_t NEED = static_cast<uint32_t>(NH + MT * NH);
     static constexpr uint32_t TCOLS = NEED <= 32 ? 32 : NEED <= 64 ? 64 : NEED <= 128 ? 128 : NEED <= 256 ? 256 : 512;
-    static_assert(D % 128 == 0 && (NH == 16 || NH == 32), "decode tile shape");
+    static_assert(D % 128 == 0 && (NH == 16 || NH == 32 || NH == 64), "decode tile shape");
+    static_assert(!kAliasS || static_cast<size_t>(kFC) * (NH + 1) * 4 <= static_cast<size_t>(NBOX) * NH * 128,
+                  "the scores fit in the query tile");
+    static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
 };
 
 template <int N>
@@ -483,37 +489,49 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
             sS[key * (NH + 1) + half * HC + c] = ok ? __uint_as_float(r[c]) * p.scale : -INFINITY;
     }
     __syncthreads();
-    // ---- per head (lane) over slots [16 warp, 16 warp + 16): max, P = e^(s - m), sums
-    float sv[16];
-    float mx = -INFINITY;
-    if (lane < NH) {
+    // ---- per head over slots [16 warp, 16 warp + 16): max, P = e^(s - m), sums. Lane l
+    //      owns heads l, l + 32, ... (HPL of them)
+    constexpr int HPL = NH > 32 ? NH / 32 : 1;
+    float sv[HPL][16];
+    float m[HPL];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            sv[i] = sS[(16 * warp + i) * (NH + 1) + lane];
-            mx = fmaxf(mx, sv[i]);
+    for (int hh = 0; hh < HPL; ++hh) {
+        const int hd = lane + 32 * hh;
+        float mx = -INFINITY;
+        if (hd < NH) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                sv[hh][i] = sS[(16 * warp + i) * (NH + 1) + hd];
+                mx = fmaxf(mx, sv[hh][i]);
+            }
+            red_m[warp * NH + hd] = mx;
         }
-        red_m[warp * NH + lane] = mx;
     }
     __syncthreads();
-    float m = -INFINITY;
-    if (lane < NH) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) m = fmaxf(m, red_m[j * NH + lane]);
-        float l = 0.f;
-        uint32_t pk[8];
+    for (int hh = 0; hh < HPL; ++hh) {
+        const int hd = lane + 32 * hh;
+        m[hh] = -INFINITY;
+        if (hd < NH) {
 #pragma unroll
-        for (int i = 0; i < 16; i += 2) {
-            const float p0 = sv[i] == -INFINITY ? 0.f : expf(sv[i] - m);
-            const float p1 = sv[i + 1] == -INFINITY ? 0.f : expf(sv[i + 1] - m);
-            l += p0 + p1;
-            pk[i / 2] = pack_bf16(p0, p1);
+            for (int j = 0; j < 8; ++j) m[hh] = fmaxf(m[hh], red_m[j * NH + hd]);
+            float l = 0.f;
+            uint32_t pk[8];
+#pragma unroll
+            for (int i = 0; i < 16; i += 2) {
+                const float p0 = sv[hh][i] == -INFINITY ? 0.f : expf(sv[hh][i] - m[hh]);
+                const float p1 = sv[hh][i + 1] == -INFINITY ? 0.f : expf(sv[hh][i + 1] - m[hh]);
+                l += p0 + p1;
+                pk[i / 2] = pack_bf16(p0, p1);
+            }
+            red_l[warp * NH + hd] = l;
+            // P[head][slot]: K-major, two 64-slot boxes of [NH rows][128 B], 128-byte swizzle
+            // (the swizzle row is the head mod 8, the lane's too)
+            uint8_t* prow = sP + (warp >> 2) * (NH * 128) + hd * 128;
+            const int c0 = 2 * (warp & 3);
+            *reinterpret_cast<uint4*>(prow + ((c0 ^ (lane & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            *reinterpret_cast<uint4*>(prow + (((c0 + 1) ^ (lane & 7)) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
         }
-        red_l[warp * NH + lane] = l;
-        // P[head][slot]: K-major, two 64-slot boxes of [NH rows][128 B], 128-byte swizzle
-        uint8_t* prow = sP + (warp >> 2) * (NH * 128) + lane * 128;
-        const int c0 = 2 * (warp & 3);
-        *reinterpret_cast<uint4*>(prow + ((c0 ^ (lane & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        *reinterpret_cast<uint4*>(prow + (((c0 + 1) ^ (lane & 7)) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     tc_fence_before();
@@ -534,12 +552,18 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         umma_commit(&bars[2]);
     }
     const size_t part = static_cast<size_t>(row) * p.n_splits + chunk;
-    if (warp == 0 && lane < Hc) {                                    // this chunk's (m, l) per head
-        float l = 0.f;
+    if (warp == 0) {                                                 // this chunk's (m, l) per head
 #pragma unroll
-        for (int j = 0; j < 8; ++j) l += red_l[j * NH + lane];
-        p.part_ml[(part * p.hstride + hbase + lane) * 2 + 0] = dead ? -INFINITY : m;
-        p.part_ml[(part * p.hstride + hbase + lane) * 2 + 1] = dead ? 0.f : l;
+        for (int hh = 0; hh < HPL; ++hh) {
+            const int hd = lane + 32 * hh;
+            if (hd < Hc) {
+                float l = 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) l += red_l[j * NH + hd];
+                p.part_ml[(part * p.hstride + hbase + hd) * 2 + 0] = dead ? -INFINITY : m[hh];
+                p.part_ml[(part * p.hstride + hbase + hd) * 2 + 1] = dead ? 0.f : l;
+            }
+        }
     }
     if (!dead && !mbar_wait(&bars[2], 0, &abort_flag, p.wait_ns)) {
         if (tid == 0) flag_error(p.eword, DSV4_EWORD_TIMEOUT);
@@ -861,9 +885,20 @@ DecodePlan decode_plan(const dsv4_attn_args& a) {
     // device while one CTA per pair fits in one: walking takes one wave and no merge kernel
     // (the dense HCA step: 64 sequences x 2 head groups x 2 chunks, where the split form took
     // 21 us in two waves plus 15 us of merge kernel on GB300).
+    const int sms = sm_count() > 0 ? sm_count() : 148;
     if (!d.walk && d.n_chunks <= 2) {
-        const int sms = sm_count() > 0 ? sm_count() : 148;
         if (pairs <= sms && pairs * d.n_chunks > sms) d.walk = true;
+    }
+    // Split CTAs of 32 heads that need a second wave while CTAs of 64 heads fit in one (the
+    // 8K-context batch-16 step: 160 CTAs on 152 SMs, where the 8 left over took as long as
+    // the first wave): one CTA per 64 heads. The partials' layout (and the workspace) does
+    // not change: the same heads at the same offsets.
+    if (!d.walk && a.dim == 512 && a.heads % 64 == 0) {
+        const long long ctas = static_cast<long long>(a.batch) * a.n_q * d.n_chunks;
+        if (ctas * (a.heads / 32) > sms && ctas * (a.heads / 64) <= sms) {
+            d.nh = 64;
+            d.n_hg = a.heads / 64;
+        }
     }
     return d;
 }
@@ -920,18 +955,20 @@ int run_decode(const dsv4_attn_args& a, const DecodePlan& dp, uint8_t* ws, uint3
             const cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<D, NH>,
                                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                        static_cast<int>(C::SMEM));
-            if (e != cudaSuccess) return e;
-            return cudaFuncSetAttribute(attn_rows_kernel<D, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(C::SMEM));
+            if (e != cudaSuccess || NH > 32) return e;
+            return cudaFuncSetAttribute(attn_rows_kernel<D, NH <= 32 ? NH : 32>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM));
         }) != cudaSuccess)
         return DSV4_ERR_LAUNCH;
-    if (dp.walk) {                                     // one CTA per (query row, head group)
-        count_launch();
-        return launch_k(attn_rows_kernel<D, NH>, dim3(static_cast<unsigned>(rows) * dp.n_hg), dim3(kFT), C::SMEM,
-                        st, true, qmap, gmap, p, static_cast<const __nv_bfloat16*>(a.comp_kv),
-                        static_cast<const __nv_bfloat16*>(a.win), a.gather ? 1 : 0) == cudaSuccess
-                   ? DSV4_OK
-                   : DSV4_ERR_LAUNCH;
+    if constexpr (NH <= 32) {                          // (64-head CTAs: split form only)
+        if (dp.walk) {                                 // one CTA per (query row, head group)
+            count_launch();
+            return launch_k(attn_rows_kernel<D, NH>, dim3(static_cast<unsigned>(rows) * dp.n_hg), dim3(kFT),
+                            C::SMEM, st, true, qmap, gmap, p, static_cast<const __nv_bfloat16*>(a.comp_kv),
+                            static_cast<const __nv_bfloat16*>(a.win), a.gather ? 1 : 0) == cudaSuccess
+                       ? DSV4_OK
+                       : DSV4_ERR_LAUNCH;
+        }
     }
     dim3 grid(dp.n_chunks, rows, dp.n_hg);
     count_launch();
@@ -961,6 +998,7 @@ size_t attn_ws_bytes(const dsv4_attn_args& a) {
 int launch_attn(const dsv4_attn_args& a, uint8_t* ws, uint32_t* eword, cudaStream_t st) {
     if (a.batch * a.n_q == 0) return DSV4_OK;
     const DecodePlan dp = decode_plan(a);
+    if (dp.nh == 64) return run_decode<512, 64>(a, dp, ws, eword, st);
     if (dp.nh == 16) {
         if (a.dim == 512) return run_decode<512, 16>(a, dp, ws, eword, st);
         if (a.dim == 256) return run_decode<256, 16>(a, dp, ws, eword, st);
