@@ -223,17 +223,20 @@ __device__ void entry_finish(const EntryIn& in, const double* freq, float* y, fl
     }
 }
 
-// Long blocks (ratio >= kLongRatio, dim a multiple of 8): the pooled tokens are shared out over
-// NT / (dim / 8) token groups, each thread taking 8 channels (16-byte loads of C and Z, two of
-// the bias) of every NT / (dim / 8)-th token, kRound tokens per round with all of a round's
-// loads issued before any use; each group's online-softmax state (max, denominator, weighted
-// sum per channel) then goes through shared memory and the groups are merged per channel into
-// y. Dependent load rounds: ratio / (groups * kRound) instead of ratio / kChunkLong.
+// Long blocks (ratio >= kLongRatio, dim a multiple of 8): the pooled tokens of the channels
+// [c_lo, c_lo + cn) are shared out over NT / (cn / 8) token groups, each thread taking 8
+// channels (16-byte loads of C and Z, two of the bias) of every NT / (cn / 8)-th token, kRound
+// tokens per round with all of a round's loads issued before any use; each group's
+// online-softmax state (max, denominator, weighted sum per channel) then goes through shared
+// memory and the groups are merged per channel into y[c_lo, c_lo + cn). Dependent load rounds:
+// ratio / (groups * kRound) instead of ratio / kChunkLong. The channels of a softmax are
+// independent, so an entry's channels may be split over several CTAs (c_lo, cn).
 template <int NT, int kRound>
-__device__ void pool_wide(const EntryIn& in, float* y, float* st /* [3][NT * 8] */) {
+__device__ void pool_wide(const EntryIn& in, float* y, float* st /* [3][NT * 8] */, int c_lo, int cn) {
     const int tid = threadIdx.x;
-    const int dim = in.dim, ratio = in.ratio;
-    const int cg_n = dim / 8, groups = NT / cg_n;
+    const int ratio = in.ratio;
+    const int dim = cn;                          // the channels pooled here
+    const int cg_n = cn / 8, groups = NT / cg_n;
     const int cg = tid % cg_n, tg = tid / cg_n;
     const size_t w = in.w;
     float m[8], den[8], num[8];
@@ -246,7 +249,7 @@ __device__ void pool_wide(const EntryIn& in, float* y, float* st /* [3][NT * 8] 
 #pragma unroll
             for (int u = 0; u < kRound; ++u) {
                 const int t = t0 + u * groups;
-                const size_t o = static_cast<size_t>(t < ratio ? t : tg) * w + cg * 8;
+                const size_t o = static_cast<size_t>(t < ratio ? t : tg) * w + c_lo + cg * 8;
                 cr[u] = __ldg(reinterpret_cast<const uint4*>(Cs + o));
                 zr[u] = __ldg(reinterpret_cast<const uint4*>(Zs + o));
                 b0[u] = __ldg(reinterpret_cast<const float4*>(bs + o));
@@ -308,21 +311,69 @@ __device__ void pool_wide(const EntryIn& in, float* y, float* st /* [3][NT * 8] 
             dn = fmaf(st[NT * 8 + g * dim + c], e, dn);
             nm = fmaf(st[2 * NT * 8 + g * dim + c], e, nm);
         }
-        y[c] = nm / dn;
+        y[c_lo + c] = nm / dn;
     }
     __syncthreads();
+}
+
+// entry_finish for an entry whose channels are split over the S CTAs of a cluster (CTA `part`
+// holds y[c_lo, c_lo + cn)), bf16 output only: the RMSNorm's sum of squares is the one value
+// that needs every channel; each CTA's partial goes into slot `part` of every CTA's s_sq
+// through distributed shared memory, and a cluster barrier makes the S partials visible. The
+// caller has arrived on the cluster barrier once at its start (so that every CTA of the cluster
+// runs before any remote store); this function waits on that phase, then runs one more.
+template <int NT, int S>
+__device__ void entry_finish_split(const EntryIn& in, const double* freq, float* y, float* warp_sum,
+                                   float* s_sq, int c_lo, int cn, uint32_t part) {
+    const int tid = threadIdx.x;
+    const int dim = in.dim;
+    float sq = 0.f;
+    for (int c = c_lo + tid; c < c_lo + cn; c += NT) sq = fmaf(y[c], y[c], sq);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+    if ((tid & 31) == 0) warp_sum[tid >> 5] = sq;
+    __syncthreads();
+    float mine = 0.f;
+#pragma unroll
+    for (int k = 0; k < NT / 32; ++k) mine += warp_sum[k];
+    cluster_wait();                              // every CTA of the cluster has started
+    if (tid < S) st_cluster_u32(cluster_map(&s_sq[part], static_cast<uint32_t>(tid)), __float_as_uint(mine));
+    cluster_arrive();
+    cluster_wait();                              // every CTA's partial is in s_sq
+    float tot = 0.f;
+#pragma unroll
+    for (int r = 0; r < S; ++r) tot += s_sq[r];
+    const float inv = 1.0f / sqrtf(tot / static_cast<float>(dim) + in.eps);
+    for (int c = c_lo + tid; c < c_lo + cn; c += NT) y[c] = y[c] * inv * in.gamma[c];
+    __syncthreads();
+    // RoPE of the pairs whose first channel is here (c_lo is even: a pair is never split)
+    for (int p = tid; p < in.rope_dim / 2; p += NT) {
+        const int d0 = dim - in.rope_dim + 2 * p;
+        if (d0 < c_lo || d0 >= c_lo + cn) continue;
+        float sn, cs;
+        sincosf(reduced_angle(in.pos * freq[p]), &sn, &cs);
+        const float e = y[d0], o = y[d0 + 1];
+        y[d0] = e * cs - o * sn;
+        y[d0 + 1] = e * sn + o * cs;
+    }
+    __syncthreads();
+    if (in.dst)
+        for (int c = c_lo + tid; c < c_lo + cn; c += NT) in.dst[c] = __float2bfloat16_rn(y[c]);
 }
 
 // zero_p/zero_n16: a workspace region (16-byte words) this launch clears for the kernels after
 // it (the fused decode step), so the step needs no separate memset; they read it only after
 // waiting for this grid.
 // NT threads; kWide: the long-block pooling of pool_wide (dim a multiple of 8; its group states
-// in dynamic shared memory), else entry_math (NT = kThreads).
-template <int kChunk, int kMinBlocks, int NT, bool kWide>
+// in dynamic shared memory), else entry_math (NT = kThreads). kSplit > 1 (wide pooling, bf16
+// outputs, dim a multiple of 8 * kSplit): a cluster of kSplit CTAs along x per entry, CTA r
+// taking channels [r dim / kSplit, (r + 1) dim / kSplit) (grid.x = kSplit x blocks).
+template <int kChunk, int kMinBlocks, int NT, bool kWide, int kSplit = 1>
 __global__ void __launch_bounds__(NT, kMinBlocks)
 compress_kernel(const __grid_constant__ CompressJob j0, const __grid_constant__ CompressJob j1,
                 uint4* zero_p, unsigned zero_n16) {
     static_assert(kWide || NT == kThreads, "the per-channel pooling runs on kThreads threads");
+    static_assert(kSplit == 1 || kWide, "only the wide pooling splits an entry's channels");
     pdl_trigger();
     {
         const unsigned nthr = gridDim.x * gridDim.y * gridDim.z * NT;
@@ -353,13 +404,16 @@ compress_kernel(const __grid_constant__ CompressJob j0, const __grid_constant__ 
     const int out_rows = second ? j1.out_rows : j0.out_rows;
     const int n_blocks = second ? j1.n_blocks : j0.n_blocks;
     const float eps = second ? j1.eps : j0.eps;
-    const int b = blockIdx.x;          // block (entry) within the sequence
+    const int b = blockIdx.x / kSplit; // block (entry) within the sequence
+    const uint32_t part = kSplit > 1 ? cluster_rank() : 0u;   // (the CTA's channel share)
     const int s = blockIdx.y;          // sequence
     const int tid = threadIdx.x;
     if (b >= n_blocks || s >= batch) return;
 
     __shared__ float y[1024];
     __shared__ float warp_sum[NT / 32];
+    __shared__ float s_sq[kSplit];           // (split entries) every CTA's sum of squares
+    if constexpr (kSplit > 1) cluster_arrive();   // waited on before the first remote store
     __shared__ double freq[kMaxPairs];
     if (tid < kMaxPairs) freq[tid] = second ? j1.freq[tid] : j0.freq[tid];
     // loads that do not depend on the reduction, issued early
@@ -407,9 +461,14 @@ compress_kernel(const __grid_constant__ CompressJob j0, const __grid_constant__ 
     in.dst_scale = in_range && out_fp8 ? out_scalep + orow : nullptr;
     in.q_dim = q_dim;
     in.dst_rope = in_range && out_fp8 == 2 ? out_ropep + orow * (dim - q_dim) : nullptr;
-    if constexpr (kWide) {
+    if constexpr (kSplit > 1) {
         extern __shared__ float group_state[];  // [3][NT * 8]
-        pool_wide<NT, kWideRound>(in, y, group_state);
+        const int cn = dim / kSplit;
+        pool_wide<NT, kWideRound>(in, y, group_state, static_cast<int>(part) * cn, cn);
+        entry_finish_split<NT, kSplit>(in, freq, y, warp_sum, s_sq, static_cast<int>(part) * cn, cn, part);
+    } else if constexpr (kWide) {
+        extern __shared__ float group_state[];  // [3][NT * 8]
+        pool_wide<NT, kWideRound>(in, y, group_state, 0, dim);
         entry_finish<NT>(in, freq, y, warp_sum);
     } else {
         entry_math<kChunk>(in, freq, y, warp_sum);
@@ -552,6 +611,26 @@ int launch_compress2(const dsv4_compress_args* a, const dsv4_compress_args* b, c
         const bool wide = j0.dim % 8 == 0 && (!b || j1.dim % 8 == 0);
         if (wide) {
             constexpr size_t kStateBytes = 3ull * kWideThreads * 8 * sizeof(float);
+            // Few entries (the decode step's newest block: one per sequence) leave SMs idle
+            // with one CTA per entry: split each entry's channels over a 2-CTA cluster when
+            // the outputs are bf16 and the doubled grid still fits on the device at once.
+            const int sms = sm_count() > 0 ? sm_count() : 148;
+            const bool split = !j0.out_fp8 && (!b || !j1.out_fp8) && j0.dim % 16 == 0 && (!b || j1.dim % 16 == 0) &&
+                               2ll * nb * bs * (b ? 2 : 1) <= sms;
+            if (split) {
+                if (once_per_device(reinterpret_cast<const void*>(compress_kernel<kChunkLong, 1, kWideThreads, true, 2>),
+                                    kAttrLaunch, [] {
+                                        return cudaFuncSetAttribute(compress_kernel<kChunkLong, 1, kWideThreads, true, 2>,
+                                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                                    static_cast<int>(kStateBytes));
+                                    }) != cudaSuccess)
+                    return DSV4_ERR_LAUNCH;
+                const dim3 g2(2u * nb, bs, b ? 2 : 1);
+                return launch_cluster_k(compress_kernel<kChunkLong, 1, kWideThreads, true, 2>, g2, dim3(kWideThreads),
+                                        kStateBytes, stream, false, 2u, j0, j1, static_cast<uint4*>(zero), n16) ==
+                               cudaSuccess
+                           ? DSV4_OK : DSV4_ERR_LAUNCH;
+            }
             if (once_per_device(reinterpret_cast<const void*>(compress_kernel<kChunkLong, 1, kWideThreads, true>),
                                 kAttrLaunch, [] {
                                     return cudaFuncSetAttribute(compress_kernel<kChunkLong, 1, kWideThreads, true>,
