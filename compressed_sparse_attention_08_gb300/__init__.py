@@ -16,6 +16,6 @@ from ._abi import (  # noqa: F401
     dsv4_topk, dsv4_topk_workspace_size, dsv4_topk_noalloc, dsv4_sparse_attn_decode,
     dsv4_sparse_attn_workspace_size, dsv4_csa_decode, dsv4_csa_decode_workspace_size,
     dsv4_read_error_word, dsv4_status_string, dsv4_last_launch_count, dsv4_max_comp,
-    dsv4_test_wait_fault, DSV4_WAIT_FAULT_NONE, DSV4_WAIT_FAULT_SCORER_STAGE,
+    dsv4_test_wait_fault, dsv4_copy_async, DSV4_WAIT_FAULT_NONE, DSV4_WAIT_FAULT_SCORER_STAGE,
     DSV4_WAIT_FAULT_ATTN_QUERY, EXPORTED_SYMBOLS,
 )

@@ -31,7 +31,7 @@ EXPORTED_SYMBOLS = (
     "dsv4_topk_workspace_size", "dsv4_topk", "dsv4_topk_noalloc", "dsv4_sparse_attn_workspace_size",
     "dsv4_sparse_attn_decode", "dsv4_csa_decode_workspace_size", "dsv4_csa_decode",
     "dsv4_status_string", "dsv4_read_error_word", "dsv4_last_launch_count", "dsv4_max_comp",
-    "dsv4_test_wait_fault",
+    "dsv4_test_wait_fault", "dsv4_copy_async",
 )
 
 P = ctypes.c_void_p
@@ -130,6 +130,8 @@ def library():
         lib.dsv4_max_comp.restype = ctypes.c_int64
         lib.dsv4_test_wait_fault.argtypes = [I, ctypes.c_uint32]
         lib.dsv4_test_wait_fault.restype = I
+        lib.dsv4_copy_async.argtypes = [P, P, ctypes.c_size_t, P]
+        lib.dsv4_copy_async.restype = I
         for f in ("dsv4_compress", "dsv4_indexer_topk", "dsv4_index_score", "dsv4_topk", "dsv4_sparse_attn_decode",
                   "dsv4_csa_decode", "dsv4_read_error_word"):
             getattr(lib, f).restype = I
@@ -410,6 +412,24 @@ def dsv4_last_launch_count():
 
 def dsv4_max_comp(max_context, ratio):
     return int(library().dsv4_max_comp(int(max_context), int(ratio)))
+
+
+def dsv4_copy_async(dst, src, stream=None):
+    """Copies tensor src into dst (same byte size, contiguous; each on the GPU or in pinned host
+    memory) with the library's copy kernel, after the kernel before it on the stream."""
+    import torch
+    for t, name in ((dst, "dst"), (src, "src")):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if t.device.type != "cuda" and not t.is_pinned():
+            raise ValueError(f"{name} must be on the GPU or in pinned host memory")
+    nbytes = dst.numel() * dst.element_size()
+    if src.numel() * src.element_size() != nbytes:
+        raise ValueError("dst and src differ in size")
+    _check(library().dsv4_copy_async(ctypes.c_void_p(dst.data_ptr()), ctypes.c_void_p(src.data_ptr()), nbytes,
+                                     _stream(stream)), "dsv4_copy_async")
 
 
 def dsv4_test_wait_fault(which, wait_limit_us=0):

@@ -20,6 +20,15 @@ thread_local int g_last_launches = 0;
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool dev_ptr_ok(const void* p) { return p != nullptr && aligned16(p); }
 bool opt_ptr_ok(const void* p) { return p == nullptr || aligned16(p); }
+// Memory the GPU can address: device, pinned (page-locked) host or managed memory.
+bool gpu_addressable(const void* p) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();                      // (not a sticky error: clear it)
+        return false;
+    }
+    return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeHost || at.type == cudaMemoryTypeManaged;
+}
 
 // The library holds sm_103a code only: any other device is refused before a launch.
 int device_check() {
@@ -183,6 +192,17 @@ int sm_count() {
 using namespace dsv4;
 
 extern "C" {
+
+int dsv4_copy_async(void* dst, const void* src, size_t bytes, dsv4_stream_t stream) {
+    LaunchScope scope;
+    if (bytes == 0) return DSV4_OK;
+    if (!dev_ptr_ok(dst) || !dev_ptr_ok(src) || bytes % 16 != 0) return DSV4_ERR_INVALID_ARG;
+    const uintptr_t d = reinterpret_cast<uintptr_t>(dst), s = reinterpret_cast<uintptr_t>(src);
+    if (d < s + bytes && s < d + bytes) return DSV4_ERR_INVALID_ARG;   // overlapping ranges
+    if (!gpu_addressable(dst) || !gpu_addressable(src)) return DSV4_ERR_INVALID_ARG;
+    if (int rc = device_check()) return rc;
+    return launch_copy(dst, src, bytes, reinterpret_cast<cudaStream_t>(stream));
+}
 
 const char* dsv4_status_string(int status) {
     switch (status) {

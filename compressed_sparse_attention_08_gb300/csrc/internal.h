@@ -21,6 +21,9 @@ struct WaitCtl {
 WaitCtl wait_ctl(int which);
 
 int launch_compress(const dsv4_compress_args& a, cudaStream_t stream);
+// SM copy of bytes (a multiple of 16; 16-byte aligned pointers; device or pinned host memory),
+// launched with programmatic dependent launch after the kernel before it.
+int launch_copy(void* dst, const void* src, size_t bytes, cudaStream_t stream);
 int launch_compress_step(const dsv4_compress_step_args& a, cudaStream_t stream);
 // FP8 E4M3 rows: one warp per row, scale = amax / 448 (fp32), codes of x / scale.
 int launch_quantize_rows_fp8(const void* x, int rows, int dim, void* q, float* scale, cudaStream_t stream);

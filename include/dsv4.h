@@ -359,6 +359,18 @@ const char* dsv4_status_string(int status);
 /* Reads (and clears) the device error word at the start of `ws`. Synchronises the stream:
  * for tests and diagnostics, never on the hot path. */
 int dsv4_read_error_word(void* ws, dsv4_stream_t stream, uint32_t* out);
+/* Copies `bytes` from src to dst on `stream` with one kernel (the SMs move the data), after
+ * the kernel enqueued before it (programmatic dependent launch). Either pointer may be device
+ * memory or pinned host memory (cudaHostAlloc / cudaHostRegister); on a Grace-Blackwell GPU
+ * the SMs reach pinned host memory over the chip-to-chip link, so a decode step's outputs
+ * (a few hundred kilobytes) land in host memory without a copy-engine transfer, which costs
+ * several microseconds more as a node of a captured graph. The pages have no counterpart for
+ * this entry point: it serves the end-to-end step (inputs in, outputs out every step).
+ * Both pointers 16-byte aligned, bytes a multiple of 16, ranges not overlapping, else
+ * DSV4_ERR_INVALID_ARG (as for pageable host memory, which the kernel cannot address);
+ * bytes = 0 does nothing. The caller keeps both buffers alive until the stream passes the
+ * copy. */
+int dsv4_copy_async(void* dst, const void* src, size_t bytes, dsv4_stream_t stream);
 /* Number of kernel launches the last successful call on this host thread enqueued. */
 int dsv4_last_launch_count(void);
 /* Compressed-cache rows for a context: (max_context + ratio - 1) / ratio ([A] commit "C1"). */

@@ -206,3 +206,18 @@ def test_binding_refuses_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(_abi, "library_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         _abi.library()
+
+
+@pytest.mark.parametrize("dst, src, nbytes", [
+    (None, _p(1), 16),                              # null
+    (_p(0), ctypes.c_void_p(FAKE + 4096 + 8), 16),  # unaligned source
+    (_p(0), _p(1), 24),                             # not a multiple of 16
+    (_p(0), ctypes.c_void_p(FAKE + 64), 128),       # overlapping ranges
+])
+def test_copy_rejects_on_host(lib, dst, src, nbytes):
+    """dsv4_copy_async refuses bad arguments before touching the device."""
+    assert lib.dsv4_copy_async(dst, src, nbytes, None) == 1
+
+
+def test_copy_of_nothing_is_a_no_op(lib):
+    assert lib.dsv4_copy_async(_p(0), _p(1), 0, None) == 0
