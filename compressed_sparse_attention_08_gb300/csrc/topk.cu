@@ -158,35 +158,6 @@ __device__ __forceinline__ void write_all(int32_t* out, int n, int top_k, int fr
     for (int j = from; j < to && j < top_k; j += step) out[j] = j < n ? j : -1;
 }
 
-// ------------------------------------------------------------------ one CTA per row
-template <int NT>
-__global__ void __launch_bounds__(NT)
-topk_small_kernel(TopkRows t, uint32_t* eword) {
-    extern __shared__ uint32_t skeys[];
-    __shared__ uint32_t hist[256];
-    __shared__ int s_a[32], s_b[32];
-    __shared__ int bc[2];
-    pdl_trigger();
-    pdl_wait();
-    const int row = blockIdx.x;
-    const int n = row_visible(t.n_vis, t.n_comp, t.q_pos, t.n_q, t.ratio, t.max_comp, row, eword);
-    const int k = n < t.top_k ? n : t.top_k;
-    int32_t* out = t.idx_out + static_cast<size_t>(row) * t.top_k;
-    if (k == n) {
-        write_all(out, n, t.top_k, threadIdx.x, t.top_k, NT);
-        return;
-    }
-    for (int j = k + threadIdx.x; j < t.top_k; j += NT) out[j] = -1;
-    const float* s = t.scores + static_cast<size_t>(row) * t.max_comp;
-    for (int i = threadIdx.x; i < n; i += NT) skeys[i] = float_to_key(s[i]);
-    __syncthreads();
-    uint32_t T;
-    int need_T;
-    auto key_at = [&](int i) { return skeys[i]; };
-    radix_select<NT>(n, k, key_at, hist, bc, T, need_T);
-    ordered_select<NT>(n, T, need_T, key_at, [](int i) { return i; }, out, s_a, s_b);
-}
-
 // ------------------------------------------------------------------ long rows
 struct LongWs {
     uint32_t* hist;     // [rows, kBins]: top 12 key bits (bits 31..20) of every visible key
@@ -235,6 +206,73 @@ __device__ __forceinline__ void find_bin(const int (&c)[kBins / NT], int k, int*
         }
     }
     __syncthreads();
+}
+
+// ------------------------------------------------------------------ one CTA per row
+// Rows up to kSmallCap keys, held in shared memory: a histogram of the top 12 key bits gives
+// the bin of the k-th key, a histogram of bits 19..8 of that bin's keys its 24-bit prefix, and
+// (only when some keys with that prefix are left out) one 8-bit radix pass the exact key.
+template <int NT>
+__global__ void __launch_bounds__(NT)
+topk_small_kernel(TopkRows t, uint32_t* eword) {
+    constexpr int per_bin = kBins / NT;
+    extern __shared__ uint32_t skeys[];
+    __shared__ uint32_t h12[kBins];
+    __shared__ uint32_t hist[256];
+    __shared__ int s_a[32], s_b[32];
+    __shared__ int bc[3];
+    pdl_trigger();
+    for (int i = threadIdx.x; i < kBins; i += NT) h12[i] = 0;
+    pdl_wait();
+    const int row = blockIdx.x;
+    const int n = row_visible(t.n_vis, t.n_comp, t.q_pos, t.n_q, t.ratio, t.max_comp, row, eword);
+    const int k = n < t.top_k ? n : t.top_k;
+    int32_t* out = t.idx_out + static_cast<size_t>(row) * t.top_k;
+    if (k == n) {
+        write_all(out, n, t.top_k, threadIdx.x, t.top_k, NT);
+        return;
+    }
+    for (int j = k + threadIdx.x; j < t.top_k; j += NT) out[j] = -1;
+    const float* s = t.scores + static_cast<size_t>(row) * t.max_comp;
+    for (int i = threadIdx.x; i < n; i += NT) skeys[i] = float_to_key(s[i]);
+    __syncthreads();
+    // 1. the top 12 bits (warp-aggregated: scores share few exponents)
+    for (int base = 0; base < n; base += NT) {
+        const int i = base + threadIdx.x;
+        const uint32_t key = i < n ? skeys[i] : 0u;
+        hist_add(h12, key >> kBinShift, i < n);
+    }
+    __syncthreads();
+    int c[per_bin];
+#pragma unroll
+    for (int i = 0; i < per_bin; ++i) c[i] = static_cast<int>(h12[kBins - 1 - (static_cast<int>(threadIdx.x) * per_bin + i)]);
+    find_bin<NT>(c, k, s_a, bc);                 // (its barriers: every thread has read h12)
+    const uint32_t tb = static_cast<uint32_t>(bc[0]);
+    const int above = bc[1];
+    for (int i = threadIdx.x; i < kBins; i += NT) h12[i] = 0;
+    __syncthreads();
+    // 2. bits 19..8 of the keys in bin tb
+    for (int base = 0; base < n; base += NT) {
+        const int i = base + threadIdx.x;
+        const uint32_t key = i < n ? skeys[i] : 0u;
+        hist_add(h12, (key >> 8) & (kBins - 1), i < n && (key >> kBinShift) == tb);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < per_bin; ++i) c[i] = static_cast<int>(h12[kBins - 1 - (static_cast<int>(threadIdx.x) * per_bin + i)]);
+    find_bin<NT>(c, k - above, s_a, bc);
+    const uint32_t prefix = (tb << kBinShift) | (static_cast<uint32_t>(bc[0]) << 8);
+    const int need = k - above - bc[1];
+    uint32_t T;
+    int need_T;
+    auto key_at = [&](int i) { return skeys[i]; };
+    if (need == bc[2] && prefix != 0u) {
+        T = prefix - 1u;                         // the whole sub-bin is selected
+        need_T = 0;
+    } else {
+        radix_select<NT>(n, need, key_at, hist, bc, T, need_T, prefix, 32 - 8);
+    }
+    ordered_select<NT>(n, T, need_T, key_at, [](int i) { return i; }, out, s_a, s_b);
 }
 
 template <int NT>
