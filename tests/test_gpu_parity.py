@@ -725,6 +725,60 @@ def test_compress_mixed_kv_cache():
     assert_bf16_close(host_bf16(rope), ref[..., D - rd:], "mixed KV: RoPE part")
 
 
+def _plain_inputs(seed, B, T, d, r):
+    C = synth.normal_bf16(seed, 201, (B, T, d))
+    Z = synth.normal_bf16(seed, 202, (B, T, d))
+    bias = synth.bf16_bits_to_f32(synth.normal_bf16(seed, 203, (r, d), 0.0, 0.5))
+    gamma = synth.bf16_bits_to_f32(synth.normal_bf16(seed, 204, (d,), 1.0, 0.1))
+    return C, Z, bias, gamma
+
+
+@pytest.mark.parametrize("mode", ["fp8", "mixed"])
+def test_compress_long_blocks_fp8_outputs(mode):
+    """Ratio 128 with few entries (two per sequence) and FP8 or mixed outputs: the one-CTA wide
+    pooling (few bf16 entries take the 2-CTA channel split instead, which writes bf16 only)."""
+    B, r, d, rd = 8, 128, 512, 64
+    C, Z, bias, gamma = _plain_inputs(41, B, 2 * r, d, r)
+    pos0 = (np.arange(B, dtype=np.int64) * 37 + 3) * r
+    _, ref = oracle.compress(C, Z, bias, gamma, pos0, r, rd)
+    if mode == "fp8":
+        got8, got_s = _gpu_compress_fp8(C, Z, bias, gamma, pos0, r)
+        _check_fp8_cache(got8, got_s, ref, "ratio 128, FP8 output")
+        return
+    m = csa()
+    nope = torch.zeros(B, 2, d - rd, dtype=torch.uint8, device="cuda")
+    sc = torch.full((B, 2), float("nan"), dtype=torch.float32, device="cuda")
+    rope = torch.zeros(B, 2, rd, dtype=torch.bfloat16, device="cuda")
+    m.dsv4_compress(dev_bf16(C), dev_bf16(Z), dev(bias), dev(gamma), dev(pos0), nope, ratio=r, rope_dim=rd,
+                    out_scale=sc, out_rope=rope)
+    torch.cuda.synchronize()
+    _check_fp8_cache(nope.cpu().numpy(), sc.cpu().numpy(), ref[..., : d - rd], "ratio 128, mixed: part without RoPE")
+    assert_bf16_close(host_bf16(rope), ref[..., d - rd:], "ratio 128, mixed: RoPE part")
+
+
+@pytest.mark.parametrize("d, split", [(100, False), (512, True)])
+def test_compress_long_blocks_pooling_forms(d, split):
+    """Ratio 16 in bf16: 100 channels (not a multiple of 8) take the per-channel pooling; 512
+    channels with few entries take the 2-CTA channel split, the newest block written into a
+    cache row at a device offset (the HCA decode step's form)."""
+    B, r = 3, 16
+    T = r if split else 4 * r
+    C, Z, bias, gamma = _plain_inputs(43 + d, B, T, d, r)
+    pos0 = np.array([5 * r, 700 * r, 0], np.int64)
+    _, ref = oracle.compress(C, Z, bias, gamma, pos0, r, 64)
+    if not split:
+        got = host_bf16(_gpu_compress(C, Z, bias, gamma, pos0, r))
+        assert_bf16_close(got, ref, f"ratio {r}, {d} channels")
+        return
+    row0 = np.array([5, 700, 0], np.int32)
+    cache = torch.zeros(B, 1000, d, dtype=torch.bfloat16, device="cuda")
+    _gpu_compress(C, Z, bias, gamma, pos0, r, out=cache, out_row0=row0)
+    got = host_bf16(cache)
+    for b in range(B):
+        assert_bf16_close(got[b, row0[b]:row0[b] + 1], ref[b], f"seq {b}")
+        assert not np.any(np.delete(got[b], row0[b], axis=0)), f"seq {b}: other rows were written"
+
+
 def test_hca_dense_attention():
     wl, x = _attn_case(2)
     got, gat, ew = _run_attn(x, wl, None)
