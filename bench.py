@@ -806,16 +806,27 @@ def run_ours(args):
                 step(stream, 0)
                 m.dsv4_copy_async(host_out, arena_out, stream=stream)
         e2e_graphs.append(g)
+    # as for the device-resident steps: one graph holds one step (copies included) per input set
+    e2e_all = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(e2e_all, stream=stream):
+            for j in range(N_INPUT_SETS):
+                arenas[0].copy_(host_in[j], non_blocking=True)
+                step(stream, 0)
+                m.dsv4_copy_async(host_out, arena_out, stream=stream)
     stream.synchronize()
 
     with torch.cuda.stream(stream):
         for i in range(3):
             e2e_graphs[i % N_INPUT_SETS].replay()
+        e2e_all.replay()
         stream.synchronize()
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         f0.record(stream)
-        for i in range(args.steps):
-            e2e_graphs[i % N_INPUT_SETS].replay()
+        for _ in range(args.steps // N_INPUT_SETS):
+            e2e_all.replay()
+        for i in range(args.steps % N_INPUT_SETS):
+            e2e_graphs[i].replay()
         f1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(f0.elapsed_time(f1) / args.steps, world, "cuda")
