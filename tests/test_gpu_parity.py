@@ -1335,6 +1335,11 @@ def test_fused_decode_step_1m_context_as_benchmarked():
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
         m.dsv4_csa_decode(ws, attn=aa, index=ia, compress_kv=ck, compress_keys=cq, stream=s)
+    s.synchronize()
+    row = int(x["append_row"][0])
+    eager = {k: t[k].clone() for k in ("out", "idx", "gather")}
+    eager["kv"], eager["keys"] = t["kv"][:, row].clone(), t["keys"][:, row].clone()
+    with torch.cuda.stream(s):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=s):
             m.dsv4_csa_decode(ws, attn=aa, index=ia, compress_kv=ck, compress_keys=cq, stream=s)
@@ -1342,7 +1347,12 @@ def test_fused_decode_step_1m_context_as_benchmarked():
     torch.cuda.synchronize()
     st, ew = m.dsv4_read_error_word(ws)
     assert ew == 0, f"device error word {ew:#x}"
-    row = int(x["append_row"][0])
+    # deterministic: the replay (stages claimed by other CTAs, counts summed by atomics in
+    # another order) gives the eager step's bytes
+    for k, v in eager.items():
+        now = t[k][:, row] if k in ("kv", "keys") else t[k]
+        assert torch.equal(now.view(torch.int16) if now.dtype == torch.bfloat16 else now,
+                           v.view(torch.int16) if v.dtype == torch.bfloat16 else v), f"1M step not deterministic: {k}"
     seqs = [0, 3]
     new_kv_bits, new_kv = oracle.compress(x["C"][seqs], x["Z"][seqs], x["bias"], x["gamma"], x["pos0"][seqs],
                                           wl.ratio, wl.rope_dim)
