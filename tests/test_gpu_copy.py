@@ -68,3 +68,33 @@ def test_copy_refuses_pageable_host_memory():
     rc = _abi.library().dsv4_copy_async(ctypes.c_void_p(d.data_ptr()), ctypes.c_void_p(buf.ctypes.data + off), 4096,
                                         None)
     assert rc == m.DSV4_ERR_INVALID_ARG
+
+
+def test_copy_captured_in_a_graph():
+    """The copy captured in a CUDA graph after a kernel (the end-to-end step's form): each
+    replay carries that replay's result to the pinned host buffer."""
+    import compressed_sparse_attention_08_gb300 as m
+    rows, n, k = 4, 2048, 32
+    sc = torch.empty(rows, n, dtype=torch.float32, device="cuda")
+    nv = torch.full((rows,), n, dtype=torch.int32, device="cuda")
+    idx = torch.empty(rows, k, dtype=torch.int32, device="cuda")
+    ws = torch.empty(max(m.dsv4_topk_workspace_size(sc, nv, idx), 256), dtype=torch.uint8, device="cuda")
+    host = torch.zeros(rows, k, dtype=torch.int32).pin_memory()
+    st = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    sc.copy_(torch.randn(rows, n, device="cuda"))
+    with torch.cuda.stream(st):
+        m.dsv4_topk(sc, nv, idx, ws, stream=st)              # (first call outside the capture)
+        st.synchronize()
+        with torch.cuda.graph(g, stream=st):
+            m.dsv4_topk(sc, nv, idx, ws, stream=st)
+            m.dsv4_copy_async(host, idx, stream=st)
+    st.synchronize()
+    for seed in range(3):
+        s_np = np.random.default_rng(100 + seed).standard_normal((rows, n)).astype(np.float32)
+        sc.copy_(torch.from_numpy(s_np).cuda())
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        want = np.sort(np.argsort(-s_np, axis=1, kind="stable")[:, :k], axis=1)
+        assert np.array_equal(host.numpy(), want), f"replay {seed}"
