@@ -33,7 +33,7 @@
 // buffer, which is all a CTA needs when it scores a single row (decode).
 // Launched with programmatic dependent launch: the producer waits for the preceding kernel
 // (the compressor) only before a stage that holds key rows that kernel writes.
-// Work: with no more rows than CTAs, every row has its own block of CTAs taking the row's
+// Work: with no more rows than CTAs, every row has its own set of CTAs (every rows-th one) taking the row's
 // stages in turn; with at most 48 rows (decode) only the first nine tenths of each row
 // are shared out that way and the rest is claimed one stage at a time from a counter in
 // the workspace header, because the SMs do not stream equally fast (a static share left the
@@ -101,8 +101,9 @@ struct ScoreParams {
 };
 
 // The stages one CTA scores, as positions f = row * stages_per_row + stage: f = begin,
-// begin + step, ... < end. With no more rows than CTAs, every row gets its own block of CTAs
-// and they take the row's stages in turn (CTA i of n: stages i, i + n, ...), so a CTA keeps
+// begin + step, ... < end. With no more rows than CTAs, every row gets its own set of CTAs
+// (every rows-th CTA) and they take the row's stages in turn (CTA i of n: stages i, i + n,
+// ...), so a CTA keeps
 // one query for the whole kernel and a row's last stage (the one the compressor may have just
 // written) comes last. With more rows than CTAs (prefill), each CTA takes a contiguous range.
 struct Walk { long long begin, end, step; };
@@ -111,11 +112,10 @@ __device__ __forceinline__ Walk cta_walk(int rows, int per_row) {
     const long long g = gridDim.x, c = blockIdx.x;
     const long long total = static_cast<long long>(rows) * per_row;
     if (rows > g) return {total * c / g, total * (c + 1) / g, 1};
-    long long r = c * rows / g;
-    while (r + 1 < rows && g * (r + 1) / rows <= c) ++r;
-    while (r > 0 && g * r / rows > c) --r;
-    const long long cb = g * r / rows, ce = g * (r + 1) / rows;
-    return {r * per_row + (c - cb), (r + 1) * per_row, ce - cb};
+    // the rows interleaved over the CTAs (CTA c takes row c mod rows): consecutive CTAs land on
+    // neighbouring SMs, and a row given a block of them finished up to ~1.3 us after the others
+    const long long r = c % rows, n_in_row = (g - r + rows - 1) / rows;
+    return {r * per_row + c / rows, (r + 1) * per_row, n_in_row};
 }
 
 // NP: the heads padded to a multiple of 16 (the TMEM columns of one query's heads)
@@ -200,7 +200,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
 
     if (warp == 0) {
         if (lane == 0) {
-            // Stage order: the CTA's share of the walk; for a row with its own block of CTAs
+            // Stage order: the CTA's share of the walk; for a row with its own set of CTAs
             // and a claim counter, only the first nine tenths of the row are shared out in
             // advance and the rest is claimed one stage at a time, so that CTAs on SMs that
             // stream faster take more and the row's CTAs finish together.
