@@ -204,7 +204,10 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
             // and a claim counter, only the first nine tenths of the row are shared out in
             // advance and the rest is claimed one stage at a time, so that CTAs on SMs that
             // stream faster take more and the row's CTAs finish together.
-            const bool dyn = p.claim != nullptr && wk.step > 1;
+            // (claiming pays only when the row has more stages than CTAs; with at most one
+            // stage each, a static share lets every CTA start before the preceding kernel ends,
+            // which the first claim, on counters that kernel clears, would wait for)
+            const bool dyn = p.claim != nullptr && wk.step > 1 && spr > wk.step;
             const int row0 = static_cast<int>(wk.begin / spr);
             const int cutoff = dyn ? static_cast<int>((static_cast<long long>(spr) * 9 / 10) / wk.step * wk.step) : spr;
             int stage = 0, qcount = 0, cur_row = -1, vis_row = -1, nv = 0, ahead = -1;
