@@ -14,19 +14,21 @@
 // Each row of D is one key's per-head dot products, so the epilogue thread that owns TMEM
 // lane i reduces sum_h w_h ReLU(D[i, h]) alone, with no cross-thread reduction.
 //
-// CTA = 6 warps (bf16 keys) or 10 (FP8 keys), persistent, one per SM, warp-specialised:
+// CTA = 6 warps (bf16 keys) or 14 (FP8 keys), persistent, one per SM, warp-specialised:
 //   warp 0  TMA producer: key stages of 256 keys (two 128-key MMA tiles; two 128-byte-
 //           swizzled boxes of 64 dims x 256 rows) into a ring of kStages 64 KB buffers; the
 //           row's queries (N x 128) into the query buffer
 //   warp 1  MMA issuer (one thread) and TMEM owner: per tile 8 UMMAs (K = 16 each) into one
-//           of kAccBufs TMEM accumulators; tcgen05.commit publishes the accumulator, and frees
-//           the stage once both of its tiles are done
+//           of the tile accumulators of a stage slot in TMEM (two slots); one tcgen05.commit
+//           publishes the stage's accumulators, another frees the stage once they are done
 //   warps 2-5  epilogue: tcgen05.ld of the accumulator (thread = key), weighted ReLU sum in
 //           fp32, coalesced store of the score; optionally a shared-memory histogram of the
 //           scores' top 12 key bits, flushed per row into the top-k workspace (so the
-//           long-row top-k needs no histogram pass of its own). FP8 keys: warps 2-9, two
-//           groups of four taking alternate accumulators; a 64 KB stage holds 512 keys, and
-//           one group alone could not drain four tiles in the time the stage takes to arrive.
+//           long-row top-k needs no histogram pass of its own). FP8 keys: warps 2-13, three
+//           groups of four taking the accumulators in turn; a 64 KB stage holds 512 keys, and
+//           one group alone could not drain four tiles in the time the stage takes to arrive
+//           (two groups scored the 1M-key rows in 38.7 us, three in 35.4, four, whose threads
+//           get too few registers, in 37.0).
 // Why 64 KB stages: a stage stays busy from its copy until the MMA that reads it completes,
 // and that hand-off adds a few hundred ns per stage; with 32 KB stages the cost took about a
 // sixth of the bandwidth, with 64 KB stages it is hidden. Shared memory then holds one query
@@ -68,8 +70,8 @@ struct KeyFmt {
     static constexpr int kSub = kStageKeys / kTileKeys;
     static constexpr int kKSteps = kDim * kElem / 32;
     static constexpr int kBoxInner = 128 / kElem;          // elements per 128-byte box row
-    // TMEM accumulators: two stages' worth of tiles, so the MMAs of a stage wait only for the
-    // epilogue of the stage two back (256 or 512 columns: a power of two)
+    // TMEM accumulators: two stage slots of kSub tiles each, so the MMAs of a stage wait only
+    // for the epilogue of the stage two back (256 or 512 columns: a power of two)
     static constexpr int kAccBufs = 2 * kSub;
     static constexpr uint32_t kTmemCols = kAccBufs * kAccCols;
 };
@@ -128,7 +130,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap qmap, ScoreParams p) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t full_bar[kStages], empty_bar[kStages];
-    __shared__ uint64_t tfull_bar[KeyFmt<FP8>::kAccBufs], tempty_bar[KeyFmt<FP8>::kAccBufs];
+    __shared__ uint64_t tfull_bar[2], tempty_bar[2];    // per accumulator slot (one stage)
     __shared__ uint64_t qfull_bar, qempty_bar, done_bar, epi_bar;
     __shared__ uint64_t idfull_bar[kIdRing], idempty_bar[kIdRing];
     __shared__ int2 s_id[kIdRing];                  // (row, stage) of each stage handed over
@@ -160,9 +162,11 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) { mbar_init(&full_bar[i], 1); mbar_init(&empty_bar[i], 1); }
-        for (int i = 0; i < kAccBufs; ++i) {
+        for (int i = 0; i < 2; ++i) {
+            // every tile of the slot is released by the 128 threads of the group that drains it
+            // (with split queries: of every group), whether or not the tile held visible keys
             mbar_init(&tfull_bar[i], 1);
-            mbar_init(&tempty_bar[i], kSplitQ ? 128 * kEpiGroups : 128);
+            mbar_init(&tempty_bar[i], kSub * (kSplitQ ? 128 * kEpiGroups : 128));
         }
         mbar_init(&qfull_bar, 1);
         mbar_init(&qempty_bar, 1);
@@ -247,11 +251,17 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                     if (st >= spr || st * kStageKeys >= nv) break;     // the row is all taken
                     claim();                                            // the next one, early
                 }
-                if (row != vis_row) {
-                    nv = unit_visible(row);
-                    vis_row = row;
+                // The walk's first kStages stages are handed over before the row's visible count
+                // is known: that load took ~1.7 us at kernel start, and the first key copy waited
+                // for it. (A stage past the visible keys costs its copy; the MMA warp and the
+                // epilogue skip its tiles.)
+                if (issued >= kStages) {
+                    if (row != vis_row) {
+                        nv = unit_visible(row);
+                        vis_row = row;
+                    }
+                    if (st * kStageKeys >= nv) continue;
                 }
-                if (st * kStageKeys >= nv) continue;
                 {
                     // hand the stage to the MMA warp and the epilogue
                     const int slot = static_cast<int>(seq % kIdRing);
@@ -330,8 +340,8 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            int stage = 0, acc = 0, qcount = 0, cur_row = -1, nv = 0;
-            uint32_t phase = 0, acc_phase = 0;
+            int stage = 0, qcount = 0, cur_row = -1, nv = 0;
+            uint32_t phase = 0;
             for (long long seq = 0;; ++seq) {
                 const int slot = static_cast<int>(seq % kIdRing);
                 if (!mbar_wait(&idfull_bar[slot], static_cast<uint32_t>((seq / kIdRing) & 1), &abort_flag, p.wait_ns)) goto fail1;
@@ -340,20 +350,25 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                 const int row = id.x, st = id.y;
                 if (row != cur_row) {
                     if (cur_row >= 0) umma_commit(&qempty_bar);   // old queries free once done
+                    nv = unit_visible(row);      // (its load overlaps the wait for the queries)
                     if (!mbar_wait(&qfull_bar, qcount & 1, &abort_flag, p.wait_ns)) goto fail1;
                     cur_row = row;
-                    nv = unit_visible(row);
                     ++qcount;
                 }
                 if (!mbar_wait(&full_bar[stage], phase, &abort_flag, p.wait_ns)) goto fail1;
                 {
+                    // the stage's tiles go to accumulator slot seq & 1 once the epilogue has read
+                    // out what the stage two back left there; one commit publishes them all
+                    // (a wait and a commit per tile kept this thread, not the keys, the bound)
+                    const int as = static_cast<int>(seq & 1);
+                    if (!mbar_wait(&tempty_bar[as], static_cast<uint32_t>(((seq >> 1) & 1) ^ 1), &abort_flag, p.wait_ns))
+                        goto fail1;
+                    tc_fence_after();
                     const uint32_t a_stage = smem_u32(key_buf + stage * kStageBytes);
                     const uint32_t b0 = smem_u32(q_buf);
                     for (int j = 0; j < kSub; ++j) {
                         if ((st * kSub + j) * kTileKeys >= nv) break;   // tile past the visible keys
-                        if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1, &abort_flag, p.wait_ns)) goto fail1;
-                        tc_fence_after();
-                        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kAccColsQ);
+                        const uint32_t d = tmem_base + static_cast<uint32_t>((as * kSub + j) * kAccColsQ);
                         const uint32_t a0 = a_stage + static_cast<uint32_t>(j * kTileKeys * 128);
 #pragma unroll
                         for (int k = 0; k < F::kKSteps; ++k) {
@@ -365,9 +380,8 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                             if constexpr (FP8) umma_f8(d, ad, bd, idesc, k > 0 ? 1u : 0u);
                             else umma_bf16(d, ad, bd, idesc, k > 0 ? 1u : 0u);
                         }
-                        umma_commit(&tfull_bar[acc]);
-                        if (++acc == kAccBufs) { acc = 0; acc_phase ^= 1; }
                     }
+                    umma_commit(&tfull_bar[as]);
                 }
                 umma_commit(&empty_bar[stage]);
                 if (++stage == kStages) { stage = 0; phase ^= 1; }
@@ -384,17 +398,25 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
         __syncwarp();
     } else {
         // epilogue: kEpiGroups groups of 4 warps; warp -> TMEM lane quarter (warp % 4); group g
-        // takes the accumulators acc with acc % kEpiGroups == g, so with two groups two tiles
-        // drain at once (FP8: four tiles per stage, twice the keys per byte of bf16)
+        // drains tile j of the stage with sequence number n when (n * kSub + j) % kEpiGroups == g,
+        // so with several groups as many tiles drain at once (FP8: four tiles per stage, twice
+        // the keys per byte of bf16)
         const int quarter = warp & 3;
         const int group = (warp - 2) >> 2;
         const int lrow = quarter * 32 + lane;
         const int etid = threadIdx.x - 64;                 // 0 .. 128 * kEpiGroups - 1
         const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-        int acc = 0, cur_row = -1, nv = 0;
-        uint32_t acc_phase = 0, fl_parity = 0;
+        int cur_row = -1, nv = 0;
+        uint32_t fl_parity = 0;
         bool ok = true;
-        float wv[kWq][NP];        // the unit's head weights (FP8: times the head's query scale)
+        // The unit's head weights (FP8: times the head's query scale). FP8 keys: three groups
+        // of 448 threads leave a thread ~144 registers, too few for 64 weights beside the 64
+        // accumulator columns it loads, so each warp keeps its copy in the half of the query
+        // buffer that FP8 queries leave free and reads it as broadcast 16-byte loads.
+        constexpr bool kWSmem = FP8;
+        static_assert(!kWSmem || 4 * kEpiGroups * NP * 4 <= static_cast<int>(kQBufBytes) / 2, "weight slots");
+        float wv[kWSmem ? 1 : kWq][kWSmem ? 1 : NP];
+        float* s_wv = reinterpret_cast<float*>(q_buf + kQBufBytes / 2) + (warp - 2) * NP;
         int nvq[kWq];             // keys visible to each query of the unit
         const int q_lo = kSplitQ ? group : 0;      // this thread's queries: q_lo .. q_lo + kWq - 1
         int nqu = 1;              // queries in the unit
@@ -475,28 +497,44 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                     const int q = q_lo + qi;
                     const int qrow = unit_row(row, q < nqu ? q : 0);
                     nvq[qi] = QB == 1 ? nv : row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, qrow, nullptr);
-#pragma unroll
-                    for (int h = 0; h < NP; ++h) {
-                        const size_t o = static_cast<size_t>(qrow) * p.heads + h;
-                        float wh = h < p.heads ? __ldg(&p.w[o]) : 0.f;
+                    if constexpr (kWSmem) {
                         // FP8: the query scale folds into the head's weight (ReLU commutes with it)
-                        if (FP8 && h < p.heads) wh *= __ldg(&p.q_scale[o]);
-                        wv[qi][h] = wh;
+                        __syncwarp();
+                        for (int h = lane; h < NP; h += 32) {
+                            const size_t o = static_cast<size_t>(qrow) * p.heads + h;
+                            s_wv[h] = h < p.heads ? __ldg(&p.w[o]) * __ldg(&p.q_scale[o]) : 0.f;
+                        }
+                        __syncwarp();
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < NP; ++h) {
+                            const size_t o = static_cast<size_t>(qrow) * p.heads + h;
+                            wv[kWSmem ? 0 : qi][kWSmem ? 0 : h] = h < p.heads ? __ldg(&p.w[o]) : 0.f;
+                        }
                     }
                 }
             }
+            // the stage's accumulator slot and the parity of this use of it
+            const long long sn = sq - 1;
+            const int as = static_cast<int>(sn & 1);
+            bool published = false;
             for (int j = 0; j < kSub && ok; ++j) {
                 const int tile = st * kSub + j;
-                if (tile * kTileKeys >= nv) break;
-                const int my_acc = acc;
-                const uint32_t my_phase = acc_phase;
-                if (++acc == kAccBufs) { acc = 0; acc_phase ^= 1; }
-                if (!kSplitQ && kEpiGroups > 1 && (my_acc % kEpiGroups) != group) continue;
-                if (!mbar_wait(&tfull_bar[my_acc], my_phase, &abort_flag, p.wait_ns)) {
-                    ok = false;
-                    break;
+                if (!kSplitQ && kEpiGroups > 1 && static_cast<int>((sn * kSub + j) % kEpiGroups) != group) continue;
+                if (!published) {
+                    // the stage's MMAs are done (and the slot's previous use fully released)
+                    if (!mbar_wait(&tfull_bar[as], static_cast<uint32_t>((sn >> 1) & 1), &abort_flag, p.wait_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    published = true;
                 }
-                tc_fence_after();
+                if (tile * kTileKeys >= nv) {
+                    // no MMA wrote this tile (past the visible keys): the slot counts it anyway
+                    mbar_arrive(&tempty_bar[as]);
+                    continue;
+                }
                 const int key = tile * kTileKeys + lrow;
                 for (int qi = 0; qi < kWq; ++qi) {
                     const int q = q_lo + qi;
@@ -504,14 +542,14 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                         // (a unit's last query row may be missing: its group still frees the tile)
                         if (kSplitQ) {
                             tc_fence_before();
-                            mbar_arrive(&tempty_bar[my_acc]);
+                            mbar_arrive(&tempty_bar[as]);
                         }
                         break;
                     }
                     // exactly the NP columns of query q the MMA wrote (columns past them hold
                     // stale values)
                     uint32_t r[NP];
-                    const uint32_t ta = tmem_base + lane_addr + static_cast<uint32_t>(my_acc * kAccColsQ + q * NP);
+                    const uint32_t ta = tmem_base + lane_addr + static_cast<uint32_t>((as * kSub + j) * kAccColsQ + q * NP);
                     if constexpr (NP == 64) {
                         DSV4_TMEM_LD_32x32b_X64(ta, r);
                     } else if constexpr (NP == 32) {
@@ -526,7 +564,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                     tmem_wait_ld();
                     if (kSplitQ || q == nqu - 1) {           // the accumulator is read out
                         tc_fence_before();
-                        mbar_arrive(&tempty_bar[my_acc]);
+                        mbar_arrive(&tempty_bar[as]);
                     }
                     float s = 0.f;
                     if constexpr (FP8) {
@@ -536,12 +574,13 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                         uint64_t a01 = 0, a23 = 0;
 #pragma unroll
                         for (int h4 = 0; h4 < NP / 4; ++h4) {
+                            const float4 wq = reinterpret_cast<const float4*>(s_wv)[h4];
                             fma_f32x2(a01, pack_f32x2(fmaxf(__uint_as_float(r[4 * h4 + 0]), 0.f),
                                                       fmaxf(__uint_as_float(r[4 * h4 + 1]), 0.f)),
-                                      pack_f32x2(wv[qi][4 * h4 + 0], wv[qi][4 * h4 + 1]));
+                                      pack_f32x2(wq.x, wq.y));
                             fma_f32x2(a23, pack_f32x2(fmaxf(__uint_as_float(r[4 * h4 + 2]), 0.f),
                                                       fmaxf(__uint_as_float(r[4 * h4 + 3]), 0.f)),
-                                      pack_f32x2(wv[qi][4 * h4 + 2], wv[qi][4 * h4 + 3]));
+                                      pack_f32x2(wq.z, wq.w));
                         }
                         float s0, s1, s2, s3;
                         unpack_f32x2(a01, s0, s1);
@@ -549,7 +588,8 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                         s = ((s0 + s1) + (s2 + s3)) * ks_cur[j];
                     } else {
 #pragma unroll
-                        for (int h = 0; h < NP; ++h) s = fmaf(wv[qi][h], fmaxf(__uint_as_float(r[h]), 0.f), s);
+                        for (int h = 0; h < NP; ++h)
+                            s = fmaf(wv[kWSmem ? 0 : qi][kWSmem ? 0 : h], fmaxf(__uint_as_float(r[h]), 0.f), s);
                     }
                     if (key < nvq[qi]) {
                         float* dst = p.scores + static_cast<size_t>(unit_row(row, q)) * p.max_comp + key;
@@ -715,7 +755,7 @@ int launch_scores(const dsv4_index_args& a, float* scores, uint32_t* hist, uint3
     const bool pairs = static_cast<long long>(a.batch) * a.n_q > sm_count() && a.n_q >= 2 && !hist;
 #define DSV4_SCORES_NP(np)                                                               \
     if (n_pad == np)                                                                     \
-        return a.key_fp8 ? launch_scores_fmt<true, np, 2, 1>(a, scores, hist, eword, stream, fresh) \
+        return a.key_fp8 ? launch_scores_fmt<true, np, 3, 1>(a, scores, hist, eword, stream, fresh) \
                : pairs   ? launch_scores_fmt<false, np, 2, 2>(a, scores, hist, eword, stream, fresh) \
                          : launch_scores_fmt<false, np, 1, 1>(a, scores, hist, eword, stream, fresh);
     DSV4_SCORES_NP(16)
