@@ -108,15 +108,20 @@ struct ScoreParams {
 // ...), so a CTA keeps
 // one query for the whole kernel and a row's last stage (the one the compressor may have just
 // written) comes last. With more rows than CTAs (prefill), each CTA takes a contiguous range.
-struct Walk { long long begin, end, step; };
+// Positions are 32-bit (rows x stages stays far below 2^31) and the producer steps through
+// them without dividing: at kernel start its one thread spent ~1.5 us on 64-bit divisions
+// before the first key copy.
+struct Walk { int begin, end, step; };
 
 __device__ __forceinline__ Walk cta_walk(int rows, int per_row) {
-    const long long g = gridDim.x, c = blockIdx.x;
-    const long long total = static_cast<long long>(rows) * per_row;
-    if (rows > g) return {total * c / g, total * (c + 1) / g, 1};
+    const int g = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+    if (rows > g) {
+        const long long total = static_cast<long long>(rows) * per_row;
+        return {static_cast<int>(total * c / g), static_cast<int>(total * (c + 1) / g), 1};
+    }
     // the rows interleaved over the CTAs (CTA c takes row c mod rows): consecutive CTAs land on
     // neighbouring SMs, and a row given a block of them finished up to ~1.3 us after the others
-    const long long r = c % rows, n_in_row = (g - r + rows - 1) / rows;
+    const int r = c % rows, n_in_row = (g - r + rows - 1) / rows;
     return {r * per_row + c / rows, (r + 1) * per_row, n_in_row};
 }
 
@@ -212,11 +217,12 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
             // stage each, a static share lets every CTA start before the preceding kernel ends,
             // which the first claim, on counters that kernel clears, would wait for)
             const bool dyn = p.claim != nullptr && wk.step > 1 && spr > wk.step;
-            const int row0 = static_cast<int>(wk.begin / spr);
-            const int cutoff = dyn ? static_cast<int>((static_cast<long long>(spr) * 9 / 10) / wk.step * wk.step) : spr;
+            const int row0 = wk.begin / spr;
+            const int cutoff = dyn ? (spr * 9 / 10) / wk.step * wk.step : spr;
             int stage = 0, qcount = 0, cur_row = -1, vis_row = -1, nv = 0, ahead = -1;
             bool waited = false, claiming = false;
-            long long issued = 0, seq = 0, f = wk.begin;
+            long long issued = 0, seq = 0;
+            int f = wk.begin, f_row = row0, f_st = wk.begin - row0 * spr;   // position f = (f_row, f_st)
             uint32_t phase = 0;
             // decode: every key is read once (evict first); prefill: every query row re-reads
             // the same keys (evict last), while its scores stream past them
@@ -229,17 +235,18 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
             for (;;) {
                 int row, st;
                 if (!claiming) {
-                    if (f >= wk.end || static_cast<int>(f % spr) >= cutoff) {
+                    if (f >= wk.end || f_st >= cutoff) {
                         if (!dyn) break;
                         claiming = true;
                         continue;
                     }
-                    row = static_cast<int>(f / spr);
-                    st = static_cast<int>(f % spr);
+                    row = f_row;
+                    st = f_st;
                     f += wk.step;
+                    for (f_st += wk.step; f_st >= spr; f_st -= spr) ++f_row;
                     // before the last stage of the share: the first claim's round trip hides
                     // behind it
-                    if (dyn && ahead < 0 && (f >= wk.end || static_cast<int>(f % spr) >= cutoff)) claim();
+                    if (dyn && ahead < 0 && (f >= wk.end || f_st >= cutoff)) claim();
                 } else {
                     if (ahead < 0) claim();
                     row = row0;
@@ -515,12 +522,12 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                 }
             }
             // the stage's accumulator slot and the parity of this use of it
-            const long long sn = sq - 1;
-            const int as = static_cast<int>(sn & 1);
+            const int sn = static_cast<int>(sq - 1);
+            const int as = sn & 1;
             bool published = false;
             for (int j = 0; j < kSub && ok; ++j) {
                 const int tile = st * kSub + j;
-                if (!kSplitQ && kEpiGroups > 1 && static_cast<int>((sn * kSub + j) % kEpiGroups) != group) continue;
+                if (!kSplitQ && kEpiGroups > 1 && (sn * kSub + j) % kEpiGroups != group) continue;
                 if (!published) {
                     // the stage's MMAs are done (and the slot's previous use fully released)
                     if (!mbar_wait(&tfull_bar[as], static_cast<uint32_t>((sn >> 1) & 1), &abort_flag, p.wait_ns)) {
