@@ -861,6 +861,327 @@ attn_rows_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     }
 }
 
+// Walking form with 64 heads per CTA (D = 512). A tcgen05.mma takes about the same time to
+// issue at N = 32 as at N = 64, and a chunk's gather serves every head of the CTA, so one CTA
+// per (query row, 64 heads) does a chunk's work for twice the heads at little more cost than
+// a 32-head CTA. The running O^T of 64 heads (4 tiles x 64 columns) does not fit in the
+// registers, so it stays in TMEM and every chunk's O^T MMA accumulates into it; the online
+// softmax keeps, per head, a reference maximum m that changes only when a chunk's maximum
+// exceeds it by more than kRescaleTau (then the head's columns of O^T and its sum l are
+// scaled by e^(m_old - m_new) through TMEM loads and stores). Every P = e^(s - m) is then at
+// most e^kRescaleTau, and the result is the same softmax: the final O / l does not depend on
+// which reference maximum was used. The 128 x 64 scores are reduced in registers (a butterfly
+// over the warp's 32 slots per head, then the four lane quarters through shared memory)
+// rather than staged in shared memory, which with the 64 KB query tile would not fit.
+constexpr float kRescaleTau = 8.f;
+
+struct Rows64Cfg {
+    static constexpr int D = 512, NH = 64;
+    static constexpr int NBOX = D / 64, MT = D / 128;
+    static constexpr size_t BOX = static_cast<size_t>(kFC) * 128;    // one 64-dim box of the KV tile
+    static constexpr size_t OFF_Q = BOX * NBOX;                      // 128 KB KV tile
+    static constexpr size_t OFF_P = OFF_Q + static_cast<size_t>(NBOX) * NH * 128;   // + 64 KB queries
+    static constexpr size_t OFF_RM = OFF_P + static_cast<size_t>(kFC) * NH * 2;     // + 16 KB P (MN-major)
+    static constexpr size_t OFF_RL = OFF_RM + 4 * NH * 4;           // per lane quarter: chunk maxima
+    static constexpr size_t OFF_M = OFF_RL + 4 * NH * 4;            // per lane quarter: chunk sums
+    static constexpr size_t OFF_L = OFF_M + NH * 4;                 // reference maximum per head
+    static constexpr size_t OFF_F = OFF_L + NH * 4;                 // running sum per head
+    static constexpr size_t OFF_OK = OFF_F + NH * 4;                // this chunk's factor per head
+    static constexpr size_t OFF_BAR = align_up(OFF_OK + kFC * 4, 16);
+    static constexpr size_t SMEM = OFF_BAR + 3 * 8 + 1024;          // + alignment slack
+    static constexpr uint32_t TCOLS = 512;                          // S^T 64 + O^T 4 x 64 columns
+    static_assert(NH * D * 4 <= BOX * NBOX, "the fp32 output fits in the KV tile");
+    static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
+};
+
+// Reduces 32 values per lane over the warp's 32 lanes so that lane l ends with the reduction
+// of element l: at each width w, a lane keeps the half of its elements its bit w selects and
+// receives the other half's partner values from lane ^ w (31 shuffles for 32 elements).
+template <bool kMax>
+__device__ __forceinline__ float warp_transpose_reduce(float (&v)[32], int lane) {
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1) {
+        const bool upper = (lane & w) != 0;
+#pragma unroll
+        for (int i = 0; i < w; ++i) {
+            const float keep = upper ? v[i + w] : v[i];
+            const float send = upper ? v[i] : v[i + w];
+            const float got = __shfl_xor_sync(0xffffffffu, send, w);
+            v[i] = kMax ? fmaxf(keep, got) : keep + got;
+        }
+    }
+    return v[0];
+}
+
+__global__ void __launch_bounds__(kFT, 1)
+attn_rows64_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap gmap,
+                   AttnParams p, const __nv_bfloat16* __restrict__ comp_kv,
+                   const __nv_bfloat16* __restrict__ win, int write_gather) {
+    using C = Rows64Cfg;
+    constexpr int D = C::D, NH = C::NH;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint32_t tmem_slot;
+    __shared__ volatile int abort_flag;
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* sm = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    uint8_t* sKV = sm;
+    uint8_t* sQ = sm + C::OFF_Q;
+    uint8_t* sP = sm + C::OFF_P;
+    float* red_m = reinterpret_cast<float*>(sm + C::OFF_RM);        // [quarter][head]
+    float* red_l = reinterpret_cast<float*>(sm + C::OFF_RL);
+    float* s_m = reinterpret_cast<float*>(sm + C::OFF_M);
+    float* s_l = reinterpret_cast<float*>(sm + C::OFF_L);
+    float* s_f = reinterpret_cast<float*>(sm + C::OFF_F);
+    int* okf = reinterpret_cast<int*>(sm + C::OFF_OK);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);   // q loaded, S done, O done
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int hgrp = static_cast<int>(blockIdx.x % p.n_hg), row = static_cast<int>(blockIdx.x / p.n_hg);
+    const int hbase = hgrp * NH;
+    const int Hc = p.H - hbase < NH ? p.H - hbase : NH;
+    const int b = row / p.n_q, t = row - b * p.n_q;
+    pdl_trigger();
+    const int nv = row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, row, nullptr);
+    int wl = p.win_len[b];
+    wl = wl < 0 ? 0 : (wl > p.win_rows ? p.win_rows : wl);
+    const int w_hi = t + wl - p.n_q;                                 // the query's own window row
+    const int w_lo = w_hi - p.window + 1 > 0 ? w_hi - p.window + 1 : 0;
+    const int w_top = w_hi < wl - 1 ? w_hi : wl - 1;
+    const int w_cnt = w_top >= w_lo ? w_top - w_lo + 1 : 0;
+
+    for (int i = tid; i < C::NBOX * (NH - Hc) * 8; i += kFT) {       // query rows past the heads
+        const int box = i / ((NH - Hc) * 8), rem = i - box * (NH - Hc) * 8;
+        *reinterpret_cast<uint4*>(sQ + box * NH * 128 + (Hc + rem / 8) * 128 + (rem & 7) * 16) =
+            make_uint4(0, 0, 0, 0);
+    }
+    if (tid < NH) {
+        s_m[tid] = -INFINITY;
+        s_l[tid] = 0.f;
+    }
+    if (tid == 0) {
+        for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0) tmem_alloc(&tmem_slot, C::TCOLS);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    if (tid == 0) {
+        tma_prefetch_desc(&gmap);
+        mbar_arrive_expect_tx(&bars[0], static_cast<uint32_t>(Hc) * D * 2);
+        for (int box = 0; box < C::NBOX; ++box)
+            tma_load_2d(sQ + box * NH * 128, &qmap, &bars[0], box * 64, row * p.H + hbase);
+    }
+
+    pdl_wait();                      // the index lists come from the kernel before
+    if (hgrp == 0 && tid == 0) row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, row, p.eword);
+
+    const int q4 = warp & 3, half = warp >> 2;   // TMEM lane quarter (slots / dims), head half
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
+    bool dead = false;
+    gather_chunk<D, NH>(p, comp_kv, win, sKV, okf, 0, row, b, nv, w_lo, w_cnt, warp, lane);
+    int next_e = -1;                                 // the next chunk's index entry, loaded a chunk ahead
+    for (int chunk = 0; chunk < p.n_chunks; ++chunk) {
+        const uint32_t ph = static_cast<uint32_t>(chunk & 1);
+        cp_async_wait_all();
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc_fence_before();
+        __syncthreads();
+        if (chunk + 1 < p.n_chunks) next_e = load_slot_index(p, chunk + 1, row, warp, lane);
+        if (tid == 0) {
+            if (write_gather && hgrp == 0) {
+                for (int box = 0; box < C::NBOX; ++box)
+                    tma_store_3d(&gmap, sKV + box * C::BOX, box * 64, chunk * kFC, row);
+                bulk_commit();
+            }
+            if (!dead && chunk == 0 && !mbar_wait(&bars[0], 0, nullptr, p.wait_ns)) dead = true;
+            if (!dead) {                            // S^T = KV Q^T into columns 0 .. NH - 1
+                tc_fence_after();
+                const uint32_t idesc = idesc_bf16_f32(kFC, NH);
+                const uint32_t a0 = smem_u32(sKV), b0 = smem_u32(sQ);
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k)
+                    umma_bf16(tmem, sdesc_kmajor_sw128(a0 + (k >> 2) * C::BOX + (k & 3) * 32),
+                              sdesc_kmajor_sw128(b0 + (k >> 2) * NH * 128 + (k & 3) * 32), idesc, k > 0 ? 1u : 0u);
+                umma_commit(&bars[1]);
+            } else if (!abort_flag) {
+                flag_error(p.eword, DSV4_EWORD_TIMEOUT);
+                abort_flag = 1;
+            }
+        }
+        if (!dead && !mbar_wait(&bars[1], ph, &abort_flag, p.wait_ns)) {
+            dead = true;
+            if (tid == 0) { flag_error(p.eword, DSV4_EWORD_TIMEOUT); abort_flag = 1; }
+        }
+        tc_fence_after();
+        // ---- the chunk's softmax: thread = slot q4 * 32 + lane, heads 32 * half .. + 31
+        float v[32];
+        {
+            uint32_t r[32];
+            DSV4_TMEM_LD_32x32b_X32(lane_base + static_cast<uint32_t>(32 * half), r);
+            tmem_wait_ld();
+            const bool ok = okf[q4 * 32 + lane] != 0 && !dead;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = ok ? __uint_as_float(r[i]) * p.scale : -INFINITY;
+        }
+        {
+            float sv[32];                            // (the reduction consumes its input)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) sv[i] = v[i];
+            red_m[q4 * NH + 32 * half + lane] = warp_transpose_reduce<true>(sv, lane);
+        }
+        __syncthreads();
+        // each head's chunk maximum against its reference maximum (threads 0 .. NH - 1); a first
+        // finite maximum is always taken (-inf + tau is -inf)
+        bool rescale = false;
+        if (tid < NH) {
+            const float cm = fmaxf(fmaxf(red_m[tid], red_m[NH + tid]), fmaxf(red_m[2 * NH + tid], red_m[3 * NH + tid]));
+            const float mo = s_m[tid];
+            float f = 1.f;
+            if (cm > mo + kRescaleTau) {
+                f = mo == -INFINITY ? 0.f : expf(mo - cm);
+                s_m[tid] = cm;
+                rescale = chunk > 0;
+            }
+            s_f[tid] = f;
+        }
+        const bool any_rescale = __syncthreads_or(rescale) != 0;
+        {
+            // P = e^(s - m) in bf16 as the MN-major B operand of O^T: slot s's 64 heads are one
+            // 128-byte row (128-byte swizzle, 8-row atoms of 1024 B); then each head's sum
+            float mh[32];
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+                const float4 m4 = *reinterpret_cast<const float4*>(s_m + 32 * half + i);
+                mh[i] = m4.x; mh[i + 1] = m4.y; mh[i + 2] = m4.z; mh[i + 3] = m4.w;
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = v[i] == -INFINITY ? 0.f : expf(v[i] - mh[i]);
+            const int s = q4 * 32 + lane;
+            uint8_t* prow = sP + (s >> 3) * 1024 + (s & 7) * 128;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int c = 4 * half + j;          // 16-byte piece: heads 8c .. 8c + 7
+                *reinterpret_cast<uint4*>(prow + ((c ^ (s & 7)) << 4)) =
+                    make_uint4(pack_bf16(v[8 * j], v[8 * j + 1]), pack_bf16(v[8 * j + 2], v[8 * j + 3]),
+                               pack_bf16(v[8 * j + 4], v[8 * j + 5]), pack_bf16(v[8 * j + 6], v[8 * j + 7]));
+            }
+            red_l[q4 * NH + 32 * half + lane] = warp_transpose_reduce<false>(v, lane);
+        }
+        if (any_rescale && !dead) {
+            // the running O^T of the heads whose maximum moved, times e^(m_old - m_new) (the
+            // previous chunk's O^T MMA is complete: its barrier was waited for)
+            float fh[32];
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+                const float4 f4 = *reinterpret_cast<const float4*>(s_f + 32 * half + i);
+                fh[i] = f4.x; fh[i + 1] = f4.y; fh[i + 2] = f4.z; fh[i + 3] = f4.w;
+            }
+#pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt) {
+                uint32_t r[32];
+                const uint32_t ta = lane_base + static_cast<uint32_t>(NH + mt * NH + 32 * half);
+                DSV4_TMEM_LD_32x32b_X32(ta, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * fh[i]);
+                DSV4_TMEM_ST_32x32b_X32(ta, r);
+            }
+            DSV4_TMEM_WAIT_ST();
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc_fence_before();
+        __syncthreads();
+        if (tid < NH)
+            s_l[tid] = fmaf(s_l[tid], s_f[tid],
+                            (red_l[tid] + red_l[NH + tid]) + (red_l[2 * NH + tid] + red_l[3 * NH + tid]));
+        if (tid == 0 && !dead) {                     // O^T += V^T P^T (the first chunk starts it)
+            tc_fence_after();
+            const uint32_t idesc = idesc_bf16_f32(kFC, NH) | (1u << 15) | (1u << 16);
+            const uint32_t a0 = smem_u32(sKV), b0 = smem_u32(sP);
+#pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt) {
+#pragma unroll
+                for (int kk = 0; kk < kFC / 16; ++kk)
+                    umma_bf16(tmem + static_cast<uint32_t>(NH + mt * NH),
+                              sdesc_mnmajor_sw128(a0 + (2 * mt) * C::BOX + kk * 2048, static_cast<uint32_t>(C::BOX), 1024u),
+                              sdesc_mnmajor_sw128(b0 + kk * 2048, 8192u, 1024u), idesc,
+                              (chunk > 0 || kk > 0) ? 1u : 0u);
+            }
+            umma_commit(&bars[2]);
+        }
+        if (!dead && !mbar_wait(&bars[2], ph, &abort_flag, p.wait_ns)) {
+            dead = true;
+            if (tid == 0) { flag_error(p.eword, DSV4_EWORD_TIMEOUT); abort_flag = 1; }
+        }
+        tc_fence_after();
+        // the tile is read: the next chunk's rows go in
+        if (chunk + 1 < p.n_chunks) {
+            if (write_gather && hgrp == 0) {
+                if (tid == 0) bulk_wait_read();      // the gather buffer's copy of the tile
+                __syncthreads();
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            copy_slots<D, NH>(p, resolve_slots<D>(p, comp_kv, win, next_e, chunk + 1, b, nv, w_lo, w_cnt, warp, lane),
+                              sKV, okf, warp, lane);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (tid < NH) {                                  // the sink once, and 1 / denominator
+        const float snk = tid < Hc ? p.sink[hbase + tid] : 0.f;
+        const float mr = s_m[tid];
+        const float M = fmaxf(mr, snk);
+        const float e = mr == -INFINITY ? 0.f : expf(mr - M);
+        s_f[tid] = e / fmaf(s_l[tid], e, expf(snk - M));
+    }
+    if (tid == 0 && write_gather && hgrp == 0) bulk_wait_read();   // the tile's last copy out
+    __syncthreads();
+    tc_fence_after();
+    // the normalised O^T -> fp32 [NH heads][D] in the (free) KV tile, then out in 16-byte
+    // pieces of whole head rows, each piece's RoPE pairs rotated back in the thread
+    float* sO = reinterpret_cast<float*>(sKV);
+    const bool have_o = p.n_chunks > 0 && !dead;
+#pragma unroll
+    for (int mt = 0; mt < C::MT; ++mt) {
+        uint32_t r[32] = {};
+        if (have_o) {
+            DSV4_TMEM_LD_32x32b_X32(lane_base + static_cast<uint32_t>(NH + mt * NH + 32 * half), r);
+            tmem_wait_ld();
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int h = 32 * half + i;
+            sO[h * D + mt * 128 + q4 * 32 + lane] = have_o ? __uint_as_float(r[i]) * s_f[h] : 0.f;
+        }
+    }
+    __syncthreads();
+    {
+        __nv_bfloat16* po = p.out + (static_cast<size_t>(row) * p.H + hbase) * D;
+        for (int i = tid; i < Hc * (D / 8); i += kFT) {
+            const int h = i / (D / 8), k = i - h * (D / 8);
+            const float4 u0 = *reinterpret_cast<const float4*>(sO + h * D + k * 8);
+            const float4 u1 = *reinterpret_cast<const float4*>(sO + h * D + k * 8 + 4);
+            float o[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) inverse_rope_pair(p, row, k * 8 + 2 * j, D, o[2 * j], o[2 * j + 1]);
+            *reinterpret_cast<uint4*>(po + static_cast<size_t>(h) * D + k * 8) =
+                make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]), pack_bf16(o[4], o[5]), pack_bf16(o[6], o[7]));
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, C::TCOLS);
+    if (tid == 0) {
+        if (write_gather && hgrp == 0) bulk_wait_read();
+        if (abort_flag) mbar_wait(&bars[0], 0, nullptr, 100000000ull);   // the query copy landed
+    }
+}
+
 // (query row, head group) pairs from which one CTA walks each row. A fixed crossover measured
 // on a 152-SM GB300 (the walking form took over once it had about two CTAs per SM), not a
 // value derived from the device's SM count: it also fixes the workspace rule stated in the
@@ -888,6 +1209,14 @@ DecodePlan decode_plan(const dsv4_attn_args& a) {
     const int sms = sm_count() > 0 ? sm_count() : 148;
     if (!d.walk && d.n_chunks <= 2) {
         if (pairs <= sms && pairs * d.n_chunks > sms) d.walk = true;
+    }
+    // Walking rows whose 64-head CTAs alone fill the device (the prefill chunk: 2048 rows): one
+    // CTA per 64 heads does a chunk for twice the heads at little more cost (attn_rows64_kernel).
+    // The workspace rule above (32-head pairs) does not change.
+    if (d.walk && a.dim == 512 && a.heads % 64 == 0 &&
+        static_cast<long long>(a.batch) * a.n_q * (a.heads / 64) >= sms) {
+        d.nh = 64;
+        d.n_hg = a.heads / 64;
     }
     // Split CTAs of 32 heads that need a second wave while CTAs of 64 heads fit in one (the
     // 8K-context batch-16 step: 160 CTAs on 152 SMs, where the 8 left over took as long as
@@ -955,12 +1284,26 @@ int run_decode(const dsv4_attn_args& a, const DecodePlan& dp, uint8_t* ws, uint3
             const cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<D, NH>,
                                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                        static_cast<int>(C::SMEM));
-            if (e != cudaSuccess || NH > 32) return e;
+            if (e != cudaSuccess) return e;
+            if constexpr (NH > 32)
+                return cudaFuncSetAttribute(attn_rows64_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            static_cast<int>(Rows64Cfg::SMEM));
             return cudaFuncSetAttribute(attn_rows_kernel<D, NH <= 32 ? NH : 32>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM));
         }) != cudaSuccess)
         return DSV4_ERR_LAUNCH;
-    if constexpr (NH <= 32) {                          // (64-head CTAs: split form only)
+    if constexpr (NH > 32) {
+        if (dp.walk) {                                 // one CTA per (query row, 64 heads)
+            static_assert(D == Rows64Cfg::D && NH == Rows64Cfg::NH, "64-head walk shape");
+            count_launch();
+            return launch_k(attn_rows64_kernel, dim3(static_cast<unsigned>(rows) * dp.n_hg), dim3(kFT),
+                            Rows64Cfg::SMEM, st, true, qmap, gmap, p, static_cast<const __nv_bfloat16*>(a.comp_kv),
+                            static_cast<const __nv_bfloat16*>(a.win), a.gather ? 1 : 0) == cudaSuccess
+                       ? DSV4_OK
+                       : DSV4_ERR_LAUNCH;
+        }
+    }
+    if constexpr (NH <= 32) {
         if (dp.walk) {                                 // one CTA per (query row, head group)
             count_launch();
             return launch_k(attn_rows_kernel<D, NH>, dim3(static_cast<unsigned>(rows) * dp.n_hg), dim3(kFT),

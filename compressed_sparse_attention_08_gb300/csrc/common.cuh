@@ -283,6 +283,20 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
                    "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])             \
                  : "r"(taddr))
 
+// 32 registers per thread -> 32 lanes x 32 consecutive 32-bit TMEM columns (the inverse of
+// the x32 load); tcgen05.wait::st orders the stores before a later tcgen05 operation reads them.
+#define DSV4_TMEM_ST_32x32b_X32(taddr, r)                                                     \
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "                               \
+                 "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"                     \
+                 "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"            \
+                 :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]),          \
+                    "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]),          \
+                    "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),     \
+                    "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]),     \
+                    "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),     \
+                    "r"(r[29]), "r"(r[30]), "r"(r[31]) : "memory")
+#define DSV4_TMEM_WAIT_ST() asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory")
+
 // 32 lanes x 64 consecutive 32-bit TMEM columns -> 64 registers per thread.
 #define DSV4_TMEM_LD_32x32b_X64(taddr, r)                                                     \
     asm volatile(                                                                              \

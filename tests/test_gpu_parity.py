@@ -978,6 +978,42 @@ def test_attention_row_walk_small_heads_inverse_rope():
     assert_bf16_close(got.reshape(n_q, H, D), ref_rot, "row-walk attention + inverse RoPE, D = 128")
 
 
+@pytest.mark.parametrize("late", ["scaled", "aligned"])
+def test_attention_row_walk_64_heads_late_maximum(late):
+    """The 64-head walking kernel (160 rows x 64 heads, 512 dims: one CTA per row), whose
+    running O^T stays in TMEM and whose per-head reference maximum moves only when a chunk's
+    maximum exceeds it by more than 8, with the largest scores in the last of three chunks
+    (the window): "scaled" multiplies the window rows by 3 (scores up to ~6 above the earlier
+    chunks': P up to ~e^6 in bf16, no rescale); "aligned" makes query t's own window row a copy
+    of its query for head t mod 64 (that head's score ~22 against ~3 before: the head's maximum
+    moves and its O^T columns and sum are rescaled, the other heads' stay)."""
+    rng = np.random.default_rng(61 if late == "scaled" else 62)
+    n_q, H, D, N, k, W = 160, 64, 512, 300, 256, 128
+    q_pos = 4000 + np.arange(n_q, dtype=np.int64)[None, :]
+    q = synth.f32_to_bf16_bits(rng.standard_normal((1, n_q, H, D)).astype(np.float32))
+    win = synth.f32_to_bf16_bits(rng.standard_normal((1, W + n_q, D)).astype(np.float32) *
+                                 np.float32(3.0 if late == "scaled" else 1.0))
+    if late == "aligned":
+        for t in range(n_q):
+            win[0, t + W] = q[0, t, t % H]        # query t's newest window row
+    x = {"q": q, "sink": rng.standard_normal(H).astype(np.float32),
+         "comp_kv_dev": synth.f32_to_bf16_bits(rng.standard_normal((1, N, D)).astype(np.float32)),
+         "n_comp": np.array([N], np.int32), "win": win,
+         "win_len": np.array([W + n_q], np.int32), "q_pos": q_pos}
+    nvis = np.full(n_q, N, np.int32)
+    idx = synth.uniform_index_sets(63, 17, n_q, nvis, k).reshape(1, n_q, k)
+
+    class WL:
+        window, ratio = W, 4
+
+    got, gat, ew = _run_attn(x, WL, idx)
+    assert ew == 0
+    _, ref, ref_g = oracle.sparse_attn(x["q"], x["sink"], x["comp_kv_dev"], x["n_comp"], idx, x["win"],
+                                       x["win_len"], k, W, 4, q_pos=q_pos, want_gather=True)
+    assert np.array_equal(gat, ref_g), "gather buffer differs"
+    assert_bf16_close(got, ref, f"64-head row walk, late maximum ({late})")
+
+
 @pytest.mark.parametrize("form", ["split", "walk", "walk_mixed"])
 def test_attention_d256_three_head_groups(form):
     """D = 256 and 48 heads (three groups of 16), a 64-row window, ragged visibility: decode
