@@ -570,9 +570,32 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         dead = true;
     }
     tc_fence_after();
-    // ---- O^T columns -> partials: lane = dim, one column per head
-    {
-        const int q = warp & 3, half = warp >> 2;
+    // ---- O^T columns -> partials: lane = dim, one column per head. 64-head CTAs stage them as
+    //      fp32 [NH heads][D] in the KV tile (free once the O^T MMA and the gather buffer's copy
+    //      have read it) so that they leave in 16-byte pieces of whole head rows: written one
+    //      4-byte column at a time, their 128 KB took ~4.6 us (the 8K-context step: 43.9 -> 42.8
+    //      us); a 32-head CTA's 64 KB gained nothing from it (the 1M-context step: +0.5 us).
+    const int q = warp & 3, half = warp >> 2;
+    if constexpr (NH > 32) {
+        static_assert(NH * D * 4 <= C::BOX * C::NBOX, "the fp32 partial fits in the KV tile");
+        if (tid == 0 && write_gather && hgrp == 0) bulk_wait_read();
+        __syncthreads();
+        float* sO = reinterpret_cast<float*>(sKV);
+        for (int task = half; task < 2 * C::MT; task += 2) {
+            const int mt = task >> 1, ch = task & 1;
+            uint32_t r[HC];
+            tmem_ld_cols<HC>(tmem + (static_cast<uint32_t>(q * 32) << 16) +
+                                 static_cast<uint32_t>(NH + mt * NH + ch * HC), r);
+            tmem_wait_ld();
+            const int dim = mt * 128 + q * 32 + lane;
+#pragma unroll
+            for (int c = 0; c < HC; ++c) sO[(ch * HC + c) * D + dim] = dead ? 0.f : __uint_as_float(r[c]);
+        }
+        __syncthreads();
+        float4* po4 = reinterpret_cast<float4*>(p.part_o + (part * p.hstride + hbase) * D);
+        const float4* s4 = reinterpret_cast<const float4*>(sKV);
+        for (int i = tid; i < Hc * (D / 4); i += kFT) po4[i] = s4[i];
+    } else {
         float* po = p.part_o + (part * p.hstride + hbase) * D;
         for (int task = half; task < 2 * C::MT; task += 2) {
             const int mt = task >> 1, ch = task & 1;
