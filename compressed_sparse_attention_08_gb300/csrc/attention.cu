@@ -125,14 +125,14 @@ attn_combine_kernel(AttnParams p) {
     if ((tid & 31) == 0) red[tid >> 5] = M;
     __syncthreads();
     M = fmaxf(fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3])), snk);
-    const float e0 = m0 == -INFINITY ? 0.f : expf(m0 - M);
-    const float e1 = m1 == -INFINITY ? 0.f : expf(m1 - M);
+    const float e0 = m0 == -INFINITY ? 0.f : exp_e(m0 - M);
+    const float e1 = m1 == -INFINITY ? 0.f : exp_e(m1 - M);
     if (tid < ns) wgt[tid] = e0;
     if (tid + 128 < ns) wgt[tid + 128] = e1;
     float den = l0 * e0 + l1 * e1;
     for (int s = tid + 256; s < ns; s += 128) {
         const float m = ml[(static_cast<size_t>(s) * HS + h) * 2];
-        const float e = m == -INFINITY ? 0.f : expf(m - M);
+        const float e = m == -INFINITY ? 0.f : exp_e(m - M);
         wgt[s] = e;
         den = fmaf(ml[(static_cast<size_t>(s) * HS + h) * 2 + 1], e, den);
     }
@@ -141,7 +141,7 @@ attn_combine_kernel(AttnParams p) {
     __syncthreads();
     if ((tid & 31) == 0) red[tid >> 5] = den;
     __syncthreads();
-    if (tid == 0) bcast[0] = 1.0f / (red[0] + red[1] + red[2] + red[3] + expf(snk - M));
+    if (tid == 0) bcast[0] = 1.0f / (red[0] + red[1] + red[2] + red[3] + exp_e(snk - M));
     __syncthreads();
     const float inv = bcast[0];
     float acc[PER];
@@ -519,8 +519,8 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
             uint32_t pk[8];
 #pragma unroll
             for (int i = 0; i < 16; i += 2) {
-                const float p0 = sv[hh][i] == -INFINITY ? 0.f : expf(sv[hh][i] - m[hh]);
-                const float p1 = sv[hh][i + 1] == -INFINITY ? 0.f : expf(sv[hh][i + 1] - m[hh]);
+                const float p0 = sv[hh][i] == -INFINITY ? 0.f : exp_e(sv[hh][i] - m[hh]);
+                const float p1 = sv[hh][i + 1] == -INFINITY ? 0.f : exp_e(sv[hh][i + 1] - m[hh]);
                 l += p0 + p1;
                 pk[i / 2] = pack_bf16(p0, p1);
             }
@@ -784,8 +784,8 @@ attn_rows_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
             uint32_t pk[8];
 #pragma unroll
             for (int i = 0; i < 16; i += 2) {
-                const float p0 = sv[i] == -INFINITY ? 0.f : expf(sv[i] - m_new);
-                const float p1 = sv[i + 1] == -INFINITY ? 0.f : expf(sv[i + 1] - m_new);
+                const float p0 = sv[i] == -INFINITY ? 0.f : exp_e(sv[i] - m_new);
+                const float p1 = sv[i + 1] == -INFINITY ? 0.f : exp_e(sv[i + 1] - m_new);
                 l += p0 + p1;
                 pk[i / 2] = pack_bf16(p0, p1);
             }
@@ -794,7 +794,7 @@ attn_rows_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
             const int c0 = 2 * (warp & 3);
             *reinterpret_cast<uint4*>(prow + ((c0 ^ (lane & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             *reinterpret_cast<uint4*>(prow + (((c0 + 1) ^ (lane & 7)) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-            fac = m_run == -INFINITY ? 0.f : expf(m_run - m_new);
+            fac = m_run == -INFINITY ? 0.f : exp_e(m_run - m_new);
             if (warp == 0) s_fac[lane] = fac;
             m_run = m_new;
         }
@@ -843,8 +843,8 @@ attn_rows_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     if (warp == 0 && lane < NH) {                    // the sink once, and 1 / denominator
         const float snk = lane < Hc ? p.sink[hbase + lane] : 0.f;
         const float M = fmaxf(m_run, snk);
-        const float e = m_run == -INFINITY ? 0.f : expf(m_run - M);
-        s_fac[lane] = e / fmaf(l_run, e, expf(snk - M));
+        const float e = m_run == -INFINITY ? 0.f : exp_e(m_run - M);
+        s_fac[lane] = e / fmaf(l_run, e, exp_e(snk - M));
     }
     if (tid == 0 && write_gather && hgrp == 0) bulk_wait_read();   // the tile's last copy out
     __syncthreads();

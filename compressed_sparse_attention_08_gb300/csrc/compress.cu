@@ -144,12 +144,12 @@ __device__ void entry_math(const EntryIn& in, const double* freq, float* y, floa
 #pragma unroll
                 for (int u = 1; u < kChunk; ++u) mc = fmaxf(mc, a[i][u]);
                 const float mn = fmaxf(m[i], mc);
-                const float sc = m[i] == -INFINITY ? 0.f : expf(m[i] - mn);
+                const float sc = m[i] == -INFINITY ? 0.f : exp_e(m[i] - mn);
                 den[i] *= sc;
                 num[i] *= sc;
 #pragma unroll
                 for (int u = 0; u < kChunk; ++u) {
-                    const float e = a[i][u] == -INFINITY ? 0.f : expf(a[i][u] - mn);
+                    const float e = a[i][u] == -INFINITY ? 0.f : exp_e(a[i][u] - mn);
                     den[i] += e;
                     num[i] = fmaf(e, cv[i][u], num[i]);   // no bias on C
                 }
@@ -275,12 +275,12 @@ __device__ void pool_wide(const EntryIn& in, float* y, float* st /* [3][NT * 8] 
 #pragma unroll
                 for (int u = 1; u < kRound; ++u) mc = fmaxf(mc, a[u][j]);
                 const float mn = fmaxf(m[j], mc);
-                const float sc = m[j] == -INFINITY ? 0.f : expf(m[j] - mn);
+                const float sc = m[j] == -INFINITY ? 0.f : exp_e(m[j] - mn);
                 den[j] *= sc;
                 num[j] *= sc;
 #pragma unroll
                 for (int u = 0; u < kRound; ++u) {
-                    const float e = a[u][j] == -INFINITY ? 0.f : expf(a[u][j] - mn);
+                    const float e = a[u][j] == -INFINITY ? 0.f : exp_e(a[u][j] - mn);
                     den[j] += e;
                     num[j] = fmaf(e, cv[u][j], num[j]);   // no bias on C
                 }
@@ -307,7 +307,7 @@ __device__ void pool_wide(const EntryIn& in, float* y, float* st /* [3][NT * 8] 
         float dn = 0.f, nm = 0.f;
         for (int g = 0; g < groups; ++g) {
             const float mg = st[g * dim + c];
-            const float e = mg == -INFINITY ? 0.f : expf(mg - M);
+            const float e = mg == -INFINITY ? 0.f : exp_e(mg - M);
             dn = fmaf(st[NT * 8 + g * dim + c], e, dn);
             nm = fmaf(st[2 * NT * 8 + g * dim + c], e, nm);
         }
