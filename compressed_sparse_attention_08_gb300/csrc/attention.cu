@@ -52,18 +52,43 @@ struct AttnParams {
     unsigned long long wait_ns;    // limit of each bounded wait
 };
 
+// (cos, sin) of the inverse RoPE's angle pos * f_j for pair j (< or_pairs) of query row `row`.
+__device__ __forceinline__ float2 inverse_rope_cs(const AttnParams& p, int row, int j) {
+    const double freq = exp2(-(static_cast<double>(j) / p.or_pairs) * p.or_log2_theta);
+    float sn, cs;
+    sincosf(reduced_angle(static_cast<double>(p.orp[row]) * freq), &sn, &cs);
+    return make_float2(cs, sn);
+}
+
 // Inverse RoPE of one output pair (channels c, c + 1, c even) of query row `row`: rotated back
 // by pos * f_j when the pair lies in the last 2 * or_pairs channels of a D-channel head.
 __device__ __forceinline__ void inverse_rope_pair(const AttnParams& p, int row, int c, int D,
                                                   float& e, float& o) {
     const int j = (c - (D - 2 * p.or_pairs)) >> 1;
     if (!p.orp || j < 0) return;
-    const double freq = exp2(-(static_cast<double>(j) / p.or_pairs) * p.or_log2_theta);
-    float sn, cs;
-    sincosf(reduced_angle(static_cast<double>(p.orp[row]) * freq), &sn, &cs);
+    const float2 r = inverse_rope_cs(p, row, j);
     const float e0 = e, o0 = o;
-    e = e0 * cs + o0 * sn;
-    o = -e0 * sn + o0 * cs;
+    e = e0 * r.x + o0 * r.y;
+    o = -e0 * r.y + o0 * r.x;
+}
+
+// The same rotation for the four pairs of an 8-channel piece starting at channel c0, from a
+// table of every rotated pair's (cos, sin) for the CTA's one query row (filled once by
+// inverse_rope_cs): the walking kernels write a row's heads x D outputs and would otherwise
+// form each pair's angle once per head, its fp64 code inlined in the output loop.
+__device__ __forceinline__ void inverse_rope_piece(const AttnParams& p, const float2* tab, int c0, int D,
+                                                   float (&v)[8]) {
+    const int lo = D - 2 * p.or_pairs;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int jj = (c0 + 2 * j - lo) >> 1;
+        if (jj >= 0) {
+            const float2 r = tab[jj];
+            const float e0 = v[2 * j], o0 = v[2 * j + 1];
+            v[2 * j] = e0 * r.x + o0 * r.y;
+            v[2 * j + 1] = -e0 * r.y + o0 * r.x;
+        }
+    }
 }
 
 // Fills the inverse-RoPE fields of the kernel parameters from the call's arguments.
@@ -846,6 +871,12 @@ attn_rows_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         const float e = m_run == -INFINITY ? 0.f : exp_e(m_run - M);
         s_fac[lane] = e / fmaf(l_run, e, exp_e(snk - M));
     }
+    // the inverse RoPE's (cos, sin) per rotated pair of this row, in the (free) score array
+    float2* rtab = reinterpret_cast<float2*>(sS);
+    static_assert(static_cast<size_t>(kFC) * (NH + 1) * 4 >= static_cast<size_t>(D / 2) * sizeof(float2),
+                  "the RoPE table fits");
+    if (p.orp)
+        for (int j = tid; j < p.or_pairs; j += kFT) rtab[j] = inverse_rope_cs(p, row, j);
     if (tid == 0 && write_gather && hgrp == 0) bulk_wait_read();   // the tile's last copy out
     __syncthreads();
     // the normalised output goes through the (free) tile as fp32 [NH heads][D], then out in
@@ -868,8 +899,7 @@ attn_rows_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
             const float4 u0 = *reinterpret_cast<const float4*>(sO + h * D + k * 8);
             const float4 u1 = *reinterpret_cast<const float4*>(sO + h * D + k * 8 + 4);
             float v[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) inverse_rope_pair(p, row, k * 8 + 2 * j, D, v[2 * j], v[2 * j + 1]);
+            if (p.orp) inverse_rope_piece(p, rtab, k * 8, D, v);
             *reinterpret_cast<uint4*>(po + static_cast<size_t>(h) * D + k * 8) =
                 make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
         }
@@ -1165,6 +1195,12 @@ attn_rows64_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         const float e = mr == -INFINITY ? 0.f : exp2f(mr - M);
         s_f[tid] = e / fmaf(s_l[tid], e, exp2f(snk - M));
     }
+    // the inverse RoPE's (cos, sin) per rotated pair of this row, in the (free) reduction
+    // arrays: 2 KB, room for every pair of a 512-channel head
+    float2* rtab = reinterpret_cast<float2*>(red_m);
+    static_assert(C::OFF_M - C::OFF_RM >= static_cast<size_t>(D / 2) * sizeof(float2), "the RoPE table fits");
+    if (p.orp)
+        for (int j = tid; j < p.or_pairs; j += kFT) rtab[j] = inverse_rope_cs(p, row, j);
     if (tid == 0 && write_gather && hgrp == 0) bulk_wait_read();   // the tile's last copy out
     __syncthreads();
     tc_fence_after();
@@ -1197,8 +1233,7 @@ attn_rows64_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
             const float4 u0 = *reinterpret_cast<const float4*>(sO + h * D + k * 8);
             const float4 u1 = *reinterpret_cast<const float4*>(sO + h * D + k * 8 + 4);
             float o[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) inverse_rope_pair(p, row, k * 8 + 2 * j, D, o[2 * j], o[2 * j + 1]);
+            if (p.orp) inverse_rope_piece(p, rtab, k * 8, D, o);
             *reinterpret_cast<uint4*>(po + static_cast<size_t>(h) * D + k * 8) =
                 make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]), pack_bf16(o[4], o[5]), pack_bf16(o[6], o[7]));
         }
