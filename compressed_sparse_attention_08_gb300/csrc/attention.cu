@@ -930,6 +930,7 @@ attn_rows_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
 // rather than staged in shared memory, which with the 64 KB query tile would not fit.
 constexpr float kRescaleTau = 8.f;
 constexpr float kLog2e = 1.4426950408889634f;          // log2(e)
+constexpr float kFastSpan = 64.f;                       // base-2 units: P below 2^64 needs no new reference
 
 struct Rows64Cfg {
     static constexpr int D = 512, NH = 64;
@@ -1038,6 +1039,11 @@ attn_rows64_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
     const int q4 = warp & 3, half = warp >> 2;   // TMEM lane quarter (slots / dims), head half
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
     bool dead = false;
+    // this thread's slot's P summed over the chunks, per head of its half (relative to the
+    // heads' current references; scaled with them), reduced over the slots once at the end
+    float lacc[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) lacc[i] = 0.f;
     gather_chunk<D, NH>(p, comp_kv, win, sKV, okf, 0, row, b, nv, w_lo, w_cnt, warp, lane);
     int next_e = -1;                                 // the next chunk's index entry, loaded a chunk ahead
     for (int chunk = 0; chunk < p.n_chunks; ++chunk) {
@@ -1084,37 +1090,56 @@ attn_rows64_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = ok ? __uint_as_float(r[i]) * sc2 : -INFINITY;
         }
-        {
-            float sv[32];                            // (the reduction consumes its input)
+        // The heads' reference maxima move only when some score of the chunk exceeds its head's
+        // by more than kFastSpan (base-2 units): below that, P = 2^(s' - m') stays far inside
+        // the fp32 and bf16 range and the softmax is the same, so each thread checks its own
+        // scores and one block-wide vote decides (the first chunk, whose references are -inf,
+        // always reduces). Otherwise the chunk's per-head maxima are reduced (a butterfly over
+        // the warp's 32 slots, the lane quarters through shared memory) and a head whose maximum
+        // exceeds its reference by more than kRescaleTau takes it as the new reference.
+        float mh[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) sv[i] = v[i];
-            red_m[q4 * NH + 32 * half + lane] = warp_transpose_reduce<true>(sv, lane);
+        for (int i = 0; i < 32; i += 4) {
+            const float4 m4 = *reinterpret_cast<const float4*>(s_m + 32 * half + i);
+            mh[i] = m4.x; mh[i + 1] = m4.y; mh[i + 2] = m4.z; mh[i + 3] = m4.w;
         }
-        __syncthreads();
-        // each head's chunk maximum against its reference maximum (threads 0 .. NH - 1); a first
-        // finite maximum is always taken (-inf + tau is -inf)
-        bool rescale = false;
-        if (tid < NH) {
-            const float cm = fmaxf(fmaxf(red_m[tid], red_m[NH + tid]), fmaxf(red_m[2 * NH + tid], red_m[3 * NH + tid]));
-            const float mo = s_m[tid];
-            float f = 1.f;
-            if (cm > mo + kRescaleTau * kLog2e) {
-                f = mo == -INFINITY ? 0.f : exp2f(mo - cm);
-                s_m[tid] = cm;
-                rescale = chunk > 0;
+        bool over = false;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) over |= v[i] > mh[i] + kFastSpan;
+        bool any_rescale = false;
+        if (__syncthreads_or(over)) {
+            {
+                float sv[32];                        // (the reduction consumes its input)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) sv[i] = v[i];
+                red_m[q4 * NH + 32 * half + lane] = warp_transpose_reduce<true>(sv, lane);
             }
-            s_f[tid] = f;
-        }
-        const bool any_rescale = __syncthreads_or(rescale) != 0;
-        {
-            // P = e^(s - m) in bf16 as the MN-major B operand of O^T: slot s's 64 heads are one
-            // 128-byte row (128-byte swizzle, 8-row atoms of 1024 B); then each head's sum
-            float mh[32];
+            __syncthreads();
+            // (threads 0 .. NH - 1; a first finite maximum is always taken: -inf + tau is -inf)
+            bool rescale = false;
+            if (tid < NH) {
+                const float cm = fmaxf(fmaxf(red_m[tid], red_m[NH + tid]), fmaxf(red_m[2 * NH + tid], red_m[3 * NH + tid]));
+                const float mo = s_m[tid];
+                float f = 1.f;
+                if (cm > mo + kRescaleTau * kLog2e) {
+                    f = mo == -INFINITY ? 0.f : exp2f(mo - cm);
+                    s_m[tid] = cm;
+                    rescale = chunk > 0;
+                }
+                s_f[tid] = f;
+            }
+            any_rescale = __syncthreads_or(rescale) != 0;
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
                 const float4 m4 = *reinterpret_cast<const float4*>(s_m + 32 * half + i);
                 mh[i] = m4.x; mh[i + 1] = m4.y; mh[i + 2] = m4.z; mh[i + 3] = m4.w;
+                const float4 f4 = *reinterpret_cast<const float4*>(s_f + 32 * half + i);
+                lacc[i] *= f4.x; lacc[i + 1] *= f4.y; lacc[i + 2] *= f4.z; lacc[i + 3] *= f4.w;
             }
+        }
+        {
+            // P = e^(s - m) in bf16 as the MN-major B operand of O^T: slot s's 64 heads are one
+            // 128-byte row (128-byte swizzle, 8-row atoms of 1024 B); then each head's sum
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = v[i] == -INFINITY ? 0.f : exp2f(v[i] - mh[i]);
             const int s = q4 * 32 + lane;
@@ -1126,7 +1151,8 @@ attn_rows64_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                     make_uint4(pack_bf16(v[8 * j], v[8 * j + 1]), pack_bf16(v[8 * j + 2], v[8 * j + 3]),
                                pack_bf16(v[8 * j + 4], v[8 * j + 5]), pack_bf16(v[8 * j + 6], v[8 * j + 7]));
             }
-            red_l[q4 * NH + 32 * half + lane] = warp_transpose_reduce<false>(v, lane);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) lacc[i] += v[i];
         }
         if (any_rescale && !dead) {
             // the running O^T of the heads whose maximum moved, times e^(m_old - m_new) (the
@@ -1152,9 +1178,6 @@ attn_rows64_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tc_fence_before();
         __syncthreads();
-        if (tid < NH)
-            s_l[tid] = fmaf(s_l[tid], s_f[tid],
-                            (red_l[tid] + red_l[NH + tid]) + (red_l[2 * NH + tid] + red_l[3 * NH + tid]));
         if (tid == 0 && !dead) {                     // O^T += V^T P^T (the first chunk starts it)
             tc_fence_after();
             const uint32_t idesc = idesc_bf16_f32(kFC, NH) | (1u << 15) | (1u << 16);
@@ -1186,7 +1209,11 @@ attn_rows64_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                               sKV, okf, warp, lane);
         }
     }
+    // each head's sum over all slots: the butterfly over the warp's 32 slots, then the quarters
+    red_l[q4 * NH + 32 * half + lane] = warp_transpose_reduce<false>(lacc, lane);
     tc_fence_before();
+    __syncthreads();
+    if (tid < NH) s_l[tid] = (red_l[tid] + red_l[NH + tid]) + (red_l[2 * NH + tid] + red_l[3 * NH + tid]);
     __syncthreads();
     if (tid < NH) {                                  // the sink once, and 1 / denominator
         const float snk = (tid < Hc ? p.sink[hbase + tid] : 0.f) * kLog2e;    // (base-2 units)

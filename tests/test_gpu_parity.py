@@ -978,24 +978,29 @@ def test_attention_row_walk_small_heads_inverse_rope():
     assert_bf16_close(got.reshape(n_q, H, D), ref_rot, "row-walk attention + inverse RoPE, D = 128")
 
 
-@pytest.mark.parametrize("late", ["scaled", "aligned"])
+@pytest.mark.parametrize("late", ["scaled", "aligned", "aligned3"])
 def test_attention_row_walk_64_heads_late_maximum(late):
     """The 64-head walking kernel (160 rows x 64 heads, 512 dims: one CTA per row), whose
-    running O^T stays in TMEM and whose per-head reference maximum moves only when a chunk's
-    maximum exceeds it by more than 8, with the largest scores in the last of three chunks
-    (the window): "scaled" multiplies the window rows by 3 (scores up to ~6 above the earlier
-    chunks': P up to ~e^6 in bf16, no rescale); "aligned" makes query t's own window row a copy
-    of its query for head t mod 64 (that head's score ~22 against ~3 before: the head's maximum
-    moves and its O^T columns and sum are rescaled, the other heads' stay)."""
-    rng = np.random.default_rng(61 if late == "scaled" else 62)
+    running O^T stays in TMEM and whose per-head reference maximum moves only when some score
+    of a chunk exceeds its head's by more than 64 in base-2 units (then every head whose chunk
+    maximum exceeds its reference by more than 8 in natural units takes it), with the largest
+    scores in the last of three chunks (the window): "scaled" multiplies the window rows by 3
+    (scores up to ~6 above the earlier chunks': P up to ~e^6 in bf16); "aligned" makes query t's
+    own window row a copy of its query for head t mod 64 (that head's score ~22, ~33 in base-2
+    units, above ~3 before: P up to ~2^33, no new reference); "aligned3" makes it three times
+    the query (~68, ~98 in base-2 units: that head's maximum moves and its O^T columns and sum
+    are rescaled, the other heads' stay)."""
+    rng = np.random.default_rng({"scaled": 61, "aligned": 62, "aligned3": 64}[late])
     n_q, H, D, N, k, W = 160, 64, 512, 300, 256, 128
     q_pos = 4000 + np.arange(n_q, dtype=np.int64)[None, :]
     q = synth.f32_to_bf16_bits(rng.standard_normal((1, n_q, H, D)).astype(np.float32))
     win = synth.f32_to_bf16_bits(rng.standard_normal((1, W + n_q, D)).astype(np.float32) *
                                  np.float32(3.0 if late == "scaled" else 1.0))
-    if late == "aligned":
+    if late != "scaled":
+        qf = (q.astype(np.uint32) << 16).view(np.float32)
+        mult = np.float32(1.0 if late == "aligned" else 3.0)
         for t in range(n_q):
-            win[0, t + W] = q[0, t, t % H]        # query t's newest window row
+            win[0, t + W] = synth.f32_to_bf16_bits(mult * qf[0, t, t % H])   # query t's newest window row
     x = {"q": q, "sink": rng.standard_normal(H).astype(np.float32),
          "comp_kv_dev": synth.f32_to_bf16_bits(rng.standard_normal((1, N, D)).astype(np.float32)),
          "n_comp": np.array([N], np.int32), "win": win,
