@@ -33,6 +33,13 @@
 // and that hand-off adds a few hundred ns per stage; with 32 KB stages the cost took about a
 // sixth of the bandwidth, with 64 KB stages it is hidden. Shared memory then holds one query
 // buffer, which is all a CTA needs when it scores a single row (decode).
+// Many query rows of bf16 keys (prefill, no histogram): each MMA scores a 128-key tile against
+// two or four consecutive query rows of a sequence (UMMA N = 128 or 256), one epilogue group
+// of four warps per query row. The keys then come from L2 (the sequence's whole cache is
+// re-read per query unit), and a tcgen05.mma costs its issuing thread about the same at any
+// N, so four rows per MMA halve both the key reads and the MMA instructions per score; their
+// 256-column accumulators fill TMEM with two slots, and the stage shrinks to one 32 KB tile
+// in a ring of four so that the four 16 KB query buffers fit.
 // Launched with programmatic dependent launch: the producer waits for the preceding kernel
 // (the compressor) only before a stage that holds key rows that kernel writes.
 // Work: with no more rows than CTAs, every row has its own set of CTAs (every rows-th one) taking the row's
@@ -53,34 +60,39 @@ namespace {
 
 constexpr int kTileKeys = 128;              // UMMA M
 constexpr int kDim = 128;                   // key width = UMMA K total
-constexpr int kMaxHeads = 64;               // UMMA N upper bound
-constexpr int kStages = 3;
-constexpr int kAccCols = 64;                // TMEM columns per accumulator
-constexpr uint32_t kStageBytes = 64 * 1024;                // two 32 KiB TMA boxes
-constexpr uint32_t kBoxBytes = kStageBytes / 2;
-constexpr uint32_t kQBufBytes = kMaxHeads * kDim * 2;      // 16 KiB (bf16 queries)
+constexpr int kMaxHeads = 64;               // UMMA N upper bound per query
+constexpr int kAccCols = 64;                // TMEM columns per accumulator and query
+constexpr uint32_t kQBufBytes = kMaxHeads * kDim * 2;      // 16 KiB (bf16 queries) per query
 
-// Key format: bf16 (two bytes per element, a 256-byte key split into two 64-dim boxes) or FP8
-// E4M3 (one byte, a key is one 128-byte row, the two boxes hold consecutive keys). A stage is
-// 64 KiB either way: 256 or 512 keys, 2 or 4 MMA tiles; one MMA step consumes 32 bytes of K.
-template <bool FP8>
+// Key format and stage geometry. bf16 keys: two bytes per element, a 256-byte key split over two
+// 64-dim boxes; FP8 E4M3: one byte, a key is one 128-byte row, the two boxes hold consecutive
+// keys. A stage is two TMA boxes, 64 KiB (256 bf16 or 512 FP8 keys: 2 or 4 MMA tiles) in a
+// ring of three, except with four query rows per MMA (bf16, UMMA N = 256): then a tile's
+// accumulator takes 256 TMEM columns, two stage slots of one tile fill the 512, and a stage is
+// one 128-key tile of 32 KiB in a ring of four. One MMA step consumes 32 bytes of K.
+template <bool FP8, int QB = 1>
 struct KeyFmt {
     static constexpr int kElem = FP8 ? 1 : 2;
+    static constexpr bool kQuad = !FP8 && QB == 4;
+    static constexpr uint32_t kStageBytes = kQuad ? 32u * 1024u : 64u * 1024u;
+    static constexpr int kStages = kQuad ? 4 : 3;
+    static constexpr uint32_t kBoxBytes = kStageBytes / 2;
     static constexpr int kStageKeys = static_cast<int>(kStageBytes) / (kDim * kElem);
+    static constexpr int kBoxRows = FP8 ? kStageKeys / 2 : kStageKeys;   // rows of one TMA box
     static constexpr int kSub = kStageKeys / kTileKeys;
     static constexpr int kKSteps = kDim * kElem / 32;
     static constexpr int kBoxInner = 128 / kElem;          // elements per 128-byte box row
     // TMEM accumulators: two stage slots of kSub tiles each, so the MMAs of a stage wait only
-    // for the epilogue of the stage two back (256 or 512 columns: a power of two)
+    // for the epilogue of the stage two back
     static constexpr int kAccBufs = 2 * kSub;
-    static constexpr uint32_t kTmemCols = kAccBufs * kAccCols;
+    static constexpr size_t kSmem = 1024 + kStages * static_cast<size_t>(kStageBytes) + QB * kQBufBytes;
+    static_assert(kSmem <= 227u * 1024u, "shared memory per CTA");
 };
 constexpr int kHistBins = 4096;             // top 12 bits of the order-preserving score key
 constexpr int kIdRing = 8;                  // stage ids in flight from the producer
 // stage-claim counters: words [kClaimWord, kClaimWord + rows) of the zeroed workspace header
 constexpr int kClaimWord = 16;
 constexpr int kMaxClaimRows = 48;
-constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + kQBufBytes;
 
 struct ScoreParams {
     const float* w;          // [rows, heads]
@@ -127,12 +139,16 @@ __device__ __forceinline__ Walk cta_walk(int rows, int per_row) {
 
 // NP: the heads padded to a multiple of 16 (the TMEM columns of one query's heads)
 // EG: epilogue groups of four warps (threads 64 + 128 EG)
-// QB: query rows scored per MMA (UMMA N = QB * NP): with QB = 2 (many rows of bf16 keys,
-//     prefill) each key stage serves two queries, half the key traffic per score
+// QB: query rows scored per MMA (UMMA N = QB * NP): with QB = 2 or 4 (many rows of bf16 keys,
+//     prefill) each key stage serves two or four queries, a half or a quarter of the key
+//     traffic and of the MMA instructions per score
 template <bool FP8, int NP, int EG, int QB>
 __global__ void __launch_bounds__(64 + 128 * EG, 1)
 index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap qmap, ScoreParams p) {
+    using F = KeyFmt<FP8, QB>;
+    constexpr int kStages = F::kStages;
+    constexpr uint32_t kStageBytes = F::kStageBytes, kBoxBytes = F::kBoxBytes;
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t full_bar[kStages], empty_bar[kStages];
     __shared__ uint64_t tfull_bar[2], tempty_bar[2];    // per accumulator slot (one stage)
@@ -143,10 +159,9 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
     __shared__ volatile int abort_flag;
     // top-12-bit key histogram of the current row, two 16-bit counts per word (8 KB: a
     // compressor CTA still fits beside this CTA on its SM)
-    // (none with QB = 2: those launches build no histogram, and the query pairs need the room)
+    // (none with QB > 1: those launches build no histogram, and the queries need the room)
     __shared__ uint32_t s_hist[QB == 1 ? kHistBins / 2 : 1];
 
-    using F = KeyFmt<FP8>;
     constexpr int kStageKeys = F::kStageKeys, kSub = F::kSub;
     constexpr int kEpiGroups = EG, kThreads = 64 + 128 * EG, kAccBufs = F::kAccBufs;
     // one epilogue group per query of the unit (QB queries per MMA): both groups read every
@@ -316,10 +331,10 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                 {
                     uint8_t* kd = key_buf + stage * kStageBytes;
                     const int b = row / p.gpb;
-                    // bf16: the two 64-dim halves of 256 keys; FP8: two runs of 256 whole keys
+                    // bf16: the two 64-dim halves of the stage's keys; FP8: two runs of 256 whole keys
                     tma_load_3d_hint(kd, &kmap, &full_bar[stage], 0, st * kStageKeys, b, stream_policy);
                     tma_load_3d_hint(kd + kBoxBytes, &kmap, &full_bar[stage], FP8 ? 0 : 64,
-                                     st * kStageKeys + (FP8 ? 256 : 0), b, stream_policy);
+                                     st * kStageKeys + (FP8 ? F::kBoxRows : 0), b, stream_policy);
                     ++issued;
                 }
                 if (++stage == kStages) { stage = 0; phase ^= 1; }
@@ -419,8 +434,13 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
         // The unit's head weights (FP8: times the head's query scale). FP8 keys: three groups
         // of 448 threads leave a thread ~144 registers, too few for 64 weights beside the 64
         // accumulator columns it loads, so each warp keeps its copy in the half of the query
-        // buffer that FP8 queries leave free and reads it as broadcast 16-byte loads.
+        // buffer that FP8 queries leave free and reads it as broadcast 16-byte loads. bf16 keys
+        // keep them in registers: with four queries per MMA the broadcast loads (a wavefront per
+        // 4 bytes) took more of the shared-memory data pipe than the tensor core's operand reads,
+        // so those threads hold their query's 64 weights and read the accumulator 16 columns at
+        // a time instead (112 registers a thread at 576 threads).
         constexpr bool kWSmem = FP8;
+        constexpr bool kChunked = F::kQuad;
         static_assert(!kWSmem || 4 * kEpiGroups * NP * 4 <= static_cast<int>(kQBufBytes) / 2, "weight slots");
         float wv[kWSmem ? 1 : kWq][kWSmem ? 1 : NP];
         float* s_wv = reinterpret_cast<float*>(q_buf + kQBufBytes / 2) + (warp - 2) * NP;
@@ -553,10 +573,40 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                         }
                         break;
                     }
+                    const uint32_t ta0 = tmem_base + lane_addr + static_cast<uint32_t>((as * kSub + j) * kAccColsQ + q * NP);
+                    if constexpr (kChunked) {
+                        // kChunkCols columns per load; four partial sums (heads h mod 4) in two packed pairs
+                        uint64_t a01 = 0, a23 = 0;
+#pragma unroll
+                        for (int c = 0; c < NP; c += 8) {
+                            uint32_t r[8];
+                            DSV4_TMEM_LD_32x32b_X8(ta0 + static_cast<uint32_t>(c), r);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 8; i += 4) {
+                                fma_f32x2(a01, pack_f32x2(fmaxf(__uint_as_float(r[i + 0]), 0.f),
+                                                          fmaxf(__uint_as_float(r[i + 1]), 0.f)),
+                                          pack_f32x2(wv[0][c + i + 0], wv[0][c + i + 1]));
+                                fma_f32x2(a23, pack_f32x2(fmaxf(__uint_as_float(r[i + 2]), 0.f),
+                                                          fmaxf(__uint_as_float(r[i + 3]), 0.f)),
+                                          pack_f32x2(wv[0][c + i + 2], wv[0][c + i + 3]));
+                            }
+                        }
+                        tc_fence_before();
+                        mbar_arrive(&tempty_bar[as]);
+                        float s0, s1, s2, s3;
+                        unpack_f32x2(a01, s0, s1);
+                        unpack_f32x2(a23, s2, s3);
+                        if (key < nvq[qi]) {
+                            float* dst = p.scores + static_cast<size_t>(unit_row(row, q)) * p.max_comp + key;
+                            __stcs(dst, (s0 + s1) + (s2 + s3));
+                        }
+                        continue;
+                    }
                     // exactly the NP columns of query q the MMA wrote (columns past them hold
                     // stale values)
                     uint32_t r[NP];
-                    const uint32_t ta = tmem_base + lane_addr + static_cast<uint32_t>((as * kSub + j) * kAccColsQ + q * NP);
+                    const uint32_t ta = ta0;
                     if constexpr (NP == 64) {
                         DSV4_TMEM_LD_32x32b_X64(ta, r);
                     } else if constexpr (NP == 32) {
@@ -682,7 +732,7 @@ namespace {
 template <bool FP8, int NP, int EG, int QB>
 int launch_scores_fmt(const dsv4_index_args& a, float* scores, uint32_t* hist, uint32_t* eword,
                       cudaStream_t stream, const dsv4_compress_args* fresh) {
-    using F = KeyFmt<FP8>;
+    using F = KeyFmt<FP8, QB>;
     const int rows = a.batch * a.n_q;
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return DSV4_ERR_LAUNCH;
@@ -692,7 +742,7 @@ int launch_scores_fmt(const dsv4_index_args& a, float* scores, uint32_t* hist, u
         cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(a.max_comp),
                               static_cast<cuuint64_t>(a.batch)};
         cuuint64_t strides[2] = {kDim * 1ull * F::kElem, static_cast<cuuint64_t>(a.max_comp) * kDim * F::kElem};
-        cuuint32_t box[3] = {static_cast<cuuint32_t>(F::kBoxInner), 256, 1};
+        cuuint32_t box[3] = {static_cast<cuuint32_t>(F::kBoxInner), static_cast<cuuint32_t>(F::kBoxRows), 1};
         cuuint32_t estr[3] = {1, 1, 1};
         if (encode(&kmap, dt, 3, const_cast<void*>(a.keys), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -738,14 +788,14 @@ int launch_scores_fmt(const dsv4_index_args& a, float* scores, uint32_t* hist, u
         if (once_per_device(reinterpret_cast<const void*>(index_score_kernel<FP8, NP, EG, QB>), kAttrLaunch, [] {
                 return cudaFuncSetAttribute(index_score_kernel<FP8, NP, EG, QB>,
                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            static_cast<int>(kSmemBytes + (QB - 1) * kQBufBytes));
+                                            static_cast<int>(F::kSmem));
             }) != cudaSuccess)
             return DSV4_ERR_LAUNCH;
         long long grid = sm_count();
         if (grid > total) grid = total;
         count_launch();
         if (launch_k(index_score_kernel<FP8, NP, EG, QB>, dim3(static_cast<unsigned>(grid)), dim3(64 + 128 * EG),
-                     kSmemBytes + (QB - 1) * kQBufBytes,
+                     F::kSmem,
                      stream, true, kmap, qmap, p) != cudaSuccess)
             return DSV4_ERR_LAUNCH;
     }
@@ -755,15 +805,19 @@ int launch_scores_fmt(const dsv4_index_args& a, float* scores, uint32_t* hist, u
 int launch_scores(const dsv4_index_args& a, float* scores, uint32_t* hist, uint32_t* eword,
                   cudaStream_t stream, const dsv4_compress_args* fresh) {
     const int n_pad = (a.heads + 15) / 16 * 16;
-    // Two epilogue groups where the epilogue, not HBM, sets the pace: FP8 keys (512 keys per
+    // Three epilogue groups where the epilogue, not HBM, sets the pace: FP8 keys (512 keys per
     // stage). One group for bf16 keys, whose registers then leave room for a compressor CTA
-    // beside the scoring CTA. Two queries per MMA with many rows of bf16 keys and no
-    // histogram to build (prefill), each query drained by its own epilogue group.
-    const bool pairs = static_cast<long long>(a.batch) * a.n_q > sm_count() && a.n_q >= 2 && !hist;
+    // beside the scoring CTA. Four (or, for two or three query rows, two) queries per MMA with
+    // many rows of bf16 keys and no histogram to build (prefill), each query drained by its
+    // own epilogue group: a tcgen05.mma costs its issuing thread about the same at any N, so
+    // the wider MMA halves the instructions per score.
+    const bool multi = static_cast<long long>(a.batch) * a.n_q > sm_count() && a.n_q >= 2 && !hist;
+    const bool quad = multi && a.n_q >= 4;
 #define DSV4_SCORES_NP(np)                                                               \
     if (n_pad == np)                                                                     \
         return a.key_fp8 ? launch_scores_fmt<true, np, 3, 1>(a, scores, hist, eword, stream, fresh) \
-               : pairs   ? launch_scores_fmt<false, np, 2, 2>(a, scores, hist, eword, stream, fresh) \
+               : quad    ? launch_scores_fmt<false, np, 4, 4>(a, scores, hist, eword, stream, fresh) \
+               : multi   ? launch_scores_fmt<false, np, 2, 2>(a, scores, hist, eword, stream, fresh) \
                          : launch_scores_fmt<false, np, 1, 1>(a, scores, hist, eword, stream, fresh);
     DSV4_SCORES_NP(16)
     DSV4_SCORES_NP(32)

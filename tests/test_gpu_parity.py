@@ -392,6 +392,29 @@ def test_indexer_cache_shorter_than_one_tile():
         check_topk_row(idx[b, 0], ref_i[b, 0], ref_s[b, 0], nv[b, 0], k, f"b{b}")
 
 
+@pytest.mark.parametrize("n_q,H", [(2, 64), (3, 40), (4, 64), (5, 64), (7, 40), (12, 16)])
+def test_indexer_several_queries_per_mma(n_q, H):
+    """More query rows than SMs and no histogram: two (n_q 2, 3) or four queries share each
+    key tile's MMA, the last unit of a sequence ragged (n_q 5, 7); causal positions give every
+    query its own visible count, some inside a tile, some past the cache's ragged end."""
+    rng = np.random.default_rng(70 + n_q)
+    B, N, k = 152 // n_q + 1, 700, 64
+    q = synth.f32_to_bf16_bits(rng.standard_normal((B, n_q, H, 128)).astype(np.float32))
+    keys = synth.f32_to_bf16_bits(rng.standard_normal((B, N, 128)).astype(np.float32))
+    w = rng.standard_normal((B, n_q, H)).astype(np.float32)
+    n_comp = rng.integers(0, N + 1, B).astype(np.int32)
+    n_comp[0], n_comp[-1] = N, 0
+    q_pos = rng.integers(0, 4 * N, B).astype(np.int64)[:, None] + np.arange(n_q, dtype=np.int64)[None, :]
+    idx, sc = _run_indexer(q, w, keys, n_comp, k, q_pos=q_pos)
+    ref_s, nv = oracle.index_scores(q, w, keys, n_comp, 4, q_pos=q_pos)
+    ref_i = oracle.topk(ref_s, nv, k)
+    for b in range(B):
+        for t in range(n_q):
+            if nv[b, t]:
+                _check_scores(sc[b, t], ref_s[b, t], nv[b, t])
+            check_topk_row(idx[b, t], ref_i[b, t], ref_s[b, t], nv[b, t], k, f"b{b} q{t}")
+
+
 # ------------------------------------------------------------------ FP8 index keys
 def test_quantize_rows_fp8_matches_oracle():
     """The GPU quantizer's codes and scales equal the oracle's bit for bit (rows of 32..1024)."""
