@@ -445,6 +445,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
         float wv[kWSmem ? 1 : kWq][kWSmem ? 1 : NP];
         float* s_wv = reinterpret_cast<float*>(q_buf + kQBufBytes / 2) + (warp - 2) * NP;
         int nvq[kWq];             // keys visible to each query of the unit
+        float* srow[kWq];         // each query's score row (set once per unit: no division per tile)
         const int q_lo = kSplitQ ? group : 0;      // this thread's queries: q_lo .. q_lo + kWq - 1
         int nqu = 1;              // queries in the unit
         // Every wait of the epilogue is an mbarrier wait, bounded in time and ended early once
@@ -524,6 +525,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                     const int q = q_lo + qi;
                     const int qrow = unit_row(row, q < nqu ? q : 0);
                     nvq[qi] = QB == 1 ? nv : row_visible(nullptr, p.n_comp, p.q_pos, p.n_q, p.ratio, p.max_comp, qrow, nullptr);
+                    srow[qi] = p.scores + static_cast<size_t>(qrow) * p.max_comp;
                     if constexpr (kWSmem) {
                         // FP8: the query scale folds into the head's weight (ReLU commutes with it)
                         __syncwarp();
@@ -598,8 +600,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                         unpack_f32x2(a01, s0, s1);
                         unpack_f32x2(a23, s2, s3);
                         if (key < nvq[qi]) {
-                            float* dst = p.scores + static_cast<size_t>(unit_row(row, q)) * p.max_comp + key;
-                            __stcs(dst, (s0 + s1) + (s2 + s3));
+                            __stcs(srow[qi] + key, (s0 + s1) + (s2 + s3));
                         }
                         continue;
                     }
@@ -649,7 +650,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                             s = fmaf(wv[kWSmem ? 0 : qi][kWSmem ? 0 : h], fmaxf(__uint_as_float(r[h]), 0.f), s);
                     }
                     if (key < nvq[qi]) {
-                        float* dst = p.scores + static_cast<size_t>(unit_row(row, q)) * p.max_comp + key;
+                        float* dst = srow[qi] + key;
                         if (p.reuse_keys) __stcs(dst, s);
                         else *dst = s;
                         if (QB == 1 && p.hist) {
