@@ -234,7 +234,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
             const bool dyn = p.claim != nullptr && wk.step > 1 && spr > wk.step;
             const int row0 = wk.begin / spr;
             const int cutoff = dyn ? (spr * 9 / 10) / wk.step * wk.step : spr;
-            int stage = 0, qcount = 0, cur_row = -1, vis_row = -1, nv = 0, ahead = -1;
+            int stage = 0, qcount = 0, cur_row = -1, cur_b = 0, vis_row = -1, nv = 0, ahead = -1;
             bool waited = false, claiming = false;
             long long issued = 0, seq = 0;
             int f = wk.begin, f_row = row0, f_st = wk.begin - row0 * spr;   // position f = (f_row, f_st)
@@ -306,13 +306,13 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                         if (!FP8) tma_load_2d(q_buf + q_half + q * NP * 128, &qmap, &qfull_bar, 64, qr);
                     }
                     cur_row = row;
+                    cur_b = row / p.gpb;
                     ++qcount;
                 }
                 if (!waited && p.fresh_rows > 0) {
                     // key rows written by the preceding kernel (the newest block's key): wait
                     // for it before streaming a stage that overlaps them
-                    const int b_ = row / p.gpb;
-                    const int f0 = p.fresh_row0 ? p.fresh_row0[b_] : 0;
+                    const int f0 = p.fresh_row0 ? p.fresh_row0[cur_b] : 0;
                     if (st * kStageKeys < f0 + p.fresh_rows && f0 < (st + 1) * kStageKeys) {
                         pdl_wait();
                         waited = true;
@@ -330,11 +330,10 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                 mbar_arrive_expect_tx(&full_bar[stage], kStageBytes);
                 {
                     uint8_t* kd = key_buf + stage * kStageBytes;
-                    const int b = row / p.gpb;
                     // bf16: the two 64-dim halves of the stage's keys; FP8: two runs of 256 whole keys
-                    tma_load_3d_hint(kd, &kmap, &full_bar[stage], 0, st * kStageKeys, b, stream_policy);
+                    tma_load_3d_hint(kd, &kmap, &full_bar[stage], 0, st * kStageKeys, cur_b, stream_policy);
                     tma_load_3d_hint(kd + kBoxBytes, &kmap, &full_bar[stage], FP8 ? 0 : 64,
-                                     st * kStageKeys + (FP8 ? F::kBoxRows : 0), b, stream_policy);
+                                     st * kStageKeys + (FP8 ? F::kBoxRows : 0), cur_b, stream_policy);
                     ++issued;
                 }
                 if (++stage == kStages) { stage = 0; phase ^= 1; }
@@ -489,8 +488,13 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
         // per tile would otherwise stall the epilogue once per 128 keys). Every key scale is
         // final once the preceding kernel (which may write the newest key) has completed.
         float ks_cur[kSub], ks_next[kSub];
+        int ks_row = -1;
+        const float* kb = nullptr;      // the key scales of sequence ks_row / gpb
         auto load_ks = [&](int2 id) {
-            const float* kb = p.key_scale + static_cast<size_t>(id.x / p.gpb) * p.max_comp;
+            if (id.x != ks_row) {
+                ks_row = id.x;
+                kb = p.key_scale + static_cast<size_t>(id.x / p.gpb) * p.max_comp;
+            }
 #pragma unroll
             for (int j = 0; j < kSub; ++j) {
                 const int key = (id.y * kSub + j) * kTileKeys + lrow;
