@@ -392,7 +392,7 @@ def test_indexer_cache_shorter_than_one_tile():
         check_topk_row(idx[b, 0], ref_i[b, 0], ref_s[b, 0], nv[b, 0], k, f"b{b}")
 
 
-@pytest.mark.parametrize("n_q,H", [(2, 64), (3, 40), (4, 64), (5, 64), (7, 40), (12, 16)])
+@pytest.mark.parametrize("n_q,H", [(2, 64), (3, 40), (4, 64), (5, 64), (6, 32), (7, 40), (12, 16)])
 def test_indexer_several_queries_per_mma(n_q, H):
     """More query rows than SMs and no histogram: two (n_q 2, 3) or four queries share each
     key tile's MMA, the last unit of a sequence ragged (n_q 5, 7); causal positions give every
