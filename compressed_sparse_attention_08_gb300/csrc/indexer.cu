@@ -14,7 +14,8 @@
 // Each row of D is one key's per-head dot products, so the epilogue thread that owns TMEM
 // lane i reduces sum_h w_h ReLU(D[i, h]) alone, with no cross-thread reduction.
 //
-// CTA = 6 warps (bf16 keys) or 14 (FP8 keys), persistent, one per SM, warp-specialised:
+// CTA = 6 warps (bf16 keys, one query row per MMA), 10 or 18 (two or four query rows per MMA)
+// or 14 (FP8 keys), persistent, one per SM, warp-specialised:
 //   warp 0  TMA producer: key stages of 256 keys (two 128-key MMA tiles; two 128-byte-
 //           swizzled boxes of 64 dims x 256 rows) into a ring of kStages 64 KB buffers; the
 //           row's queries (N x 128) into the query buffer
@@ -28,7 +29,8 @@
 //           groups of four taking the accumulators in turn; a 64 KB stage holds 512 keys, and
 //           one group alone could not drain four tiles in the time the stage takes to arrive
 //           (two groups scored the 1M-key rows in 38.7 us, three in 35.4, four, whose threads
-//           get too few registers, in 37.0).
+//           get too few registers, in 37.0). Several query rows per MMA: one group of four
+//           warps per query row, every group reading every tile.
 // Why 64 KB stages: a stage stays busy from its copy until the MMA that reads it completes,
 // and that hand-off adds a few hundred ns per stage; with 32 KB stages the cost took about a
 // sixth of the bandwidth, with 64 KB stages it is hidden. Shared memory then holds one query
