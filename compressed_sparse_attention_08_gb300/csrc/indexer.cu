@@ -583,7 +583,7 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
                     }
                     const uint32_t ta0 = tmem_base + lane_addr + static_cast<uint32_t>((as * kSub + j) * kAccColsQ + q * NP);
                     if constexpr (kChunked) {
-                        // kChunkCols columns per load; four partial sums (heads h mod 4) in two packed pairs
+                        // 8 columns per load; four partial sums (heads h mod 4) in two packed pairs
                         uint64_t a01 = 0, a23 = 0;
 #pragma unroll
                         for (int c = 0; c < NP; c += 8) {
