@@ -600,7 +600,8 @@ def _run_topk(scores, n_vis, k):
     return idx.cpu().numpy()
 
 
-@pytest.mark.parametrize("max_comp,k", [(3000, 64), (40000, 2048), (262144, 2048)])
+@pytest.mark.parametrize("max_comp,k", [(33, 8), (700, 96), (2048, 512), (2048, 2047), (3000, 64), (40000, 2048),
+                                         (262144, 2048)])
 def test_topk_exact_with_planted_ties(max_comp, k):
     rows = 6
     s = synth.normal_f32(11, 18, (rows, max_comp), 0.0, 8.0)
