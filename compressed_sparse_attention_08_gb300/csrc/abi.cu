@@ -32,16 +32,17 @@ bool gpu_addressable(const void* p) {
 
 // The library holds sm_103a code only: any other device is refused before a launch.
 int device_check() {
-    static int ok_for_device[64] = {0};   // 0 unknown, 1 ok, 2 unsupported
+    // 0 unknown, 1 ok, 2 unsupported (atomic: first calls may come from several host threads)
+    static std::atomic<int> ok_for_device[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return DSV4_ERR_UNSUPPORTED;
-    if (dev < 64 && ok_for_device[dev] == 1) return DSV4_OK;
+    if (dev < 64 && ok_for_device[dev].load(std::memory_order_relaxed) == 1) return DSV4_OK;
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
         return DSV4_ERR_UNSUPPORTED;
     const int res = major == 10 && minor == 3 ? DSV4_OK : DSV4_ERR_UNSUPPORTED;
-    if (dev < 64) ok_for_device[dev] = res == DSV4_OK ? 1 : 2;
+    if (dev < 64) ok_for_device[dev].store(res == DSV4_OK ? 1 : 2, std::memory_order_relaxed);
     return res;
 }
 
@@ -177,13 +178,16 @@ cudaError_t prefer_max_shared(const void* kernel) {
 }
 
 int sm_count() {
-    static int cache[64] = {0};
+    static std::atomic<int> cache[64] = {};   // (atomic: first calls may come from several threads)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
-    if (dev < 64 && cache[dev]) return cache[dev];
+    if (dev < 64) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c) return c;
+    }
     int n = 0;
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (dev < 64) cache[dev] = n;
+    if (dev < 64) cache[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 
