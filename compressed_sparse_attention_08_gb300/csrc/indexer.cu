@@ -166,8 +166,8 @@ index_score_kernel(const __grid_constant__ CUtensorMap kmap,
 
     constexpr int kStageKeys = F::kStageKeys, kSub = F::kSub;
     constexpr int kEpiGroups = EG, kThreads = 64 + 128 * EG, kAccBufs = F::kAccBufs;
-    // one epilogue group per query of the unit (QB queries per MMA): both groups read every
-    // accumulator, group g its query g's columns, so a tile's two queries drain at once
+    // one epilogue group per query of the unit (QB queries per MMA): every group reads every
+    // accumulator, group g its query g's columns, so a tile's queries drain at once
     constexpr bool kSplitQ = QB > 1 && EG == QB && !FP8;
     constexpr int kWq = kSplitQ ? 1 : QB;              // queries whose weights a thread holds
     constexpr int kAccColsQ = kAccCols * QB;                 // TMEM columns per accumulator
