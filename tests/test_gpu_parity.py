@@ -392,13 +392,15 @@ def test_indexer_cache_shorter_than_one_tile():
         check_topk_row(idx[b, 0], ref_i[b, 0], ref_s[b, 0], nv[b, 0], k, f"b{b}")
 
 
-@pytest.mark.parametrize("n_q,H", [(2, 64), (3, 40), (4, 64), (5, 64), (6, 32), (7, 40), (12, 16)])
-def test_indexer_several_queries_per_mma(n_q, H):
+@pytest.mark.parametrize("n_q,H,N", [(2, 64, 700), (3, 40, 700), (4, 64, 700), (5, 64, 700), (6, 32, 700),
+                                     (7, 40, 700), (12, 16, 700), (5, 64, 100)])
+def test_indexer_several_queries_per_mma(n_q, H, N):
     """More query rows than SMs and no histogram: two (n_q 2, 3) or four queries share each
     key tile's MMA, the last unit of a sequence ragged (n_q 5, 7); causal positions give every
-    query its own visible count, some inside a tile, some past the cache's ragged end."""
-    rng = np.random.default_rng(70 + n_q)
-    B, N, k = 152 // n_q + 1, 700, 64
+    query its own visible count, some inside a tile, some past the cache's ragged end (a cache
+    of 100 rows: the only tile reaches past it)."""
+    rng = np.random.default_rng(70 + n_q + N)
+    B, k = 152 // n_q + 1, 64
     q = synth.f32_to_bf16_bits(rng.standard_normal((B, n_q, H, 128)).astype(np.float32))
     keys = synth.f32_to_bf16_bits(rng.standard_normal((B, N, 128)).astype(np.float32))
     w = rng.standard_normal((B, n_q, H)).astype(np.float32)
