@@ -498,6 +498,40 @@ def test_indexer_fp8_ragged_and_short():
         check_topk_row(idx[b, 0], ref_i[b, 0], ref_s[b, 0], nv[b, 0], k, f"b{b}")
 
 
+def test_indexer_fp8_many_rows_causal():
+    """FP8 keys with more query rows than SMs (4 per sequence, causal positions): the CTAs'
+    contiguous shares of (row, stage) pairs cross row boundaries, so the head weights and the
+    key-scale row change inside a CTA; every row against the oracle's FP8 scores."""
+    rng = np.random.default_rng(23)
+    B, n_q, H, N, k = 40, 4, 64, 700, 64
+    q = synth.f32_to_bf16_bits(rng.standard_normal((B, n_q, H, 128)).astype(np.float32))
+    keys = synth.f32_to_bf16_bits(rng.standard_normal((B, N, 128)).astype(np.float32))
+    w = rng.standard_normal((B, n_q, H)).astype(np.float32)
+    n_comp = rng.integers(0, N + 1, B).astype(np.int32)
+    n_comp[0], n_comp[1] = N, 0
+    q_pos = rng.integers(0, 4 * N, B).astype(np.int64)[:, None] + np.arange(n_q, dtype=np.int64)[None, :]
+    q8, qs = _fp8_rows(q)
+    k8, ks = _fp8_rows(keys)
+    m = csa()
+    qd, kd, qsd, ksd, wd, nd, pd = dev(q8), dev(k8), dev(qs), dev(ks), dev(w), dev(n_comp), dev(q_pos)
+    idx = torch.empty(B, n_q, k, dtype=torch.int32, device="cuda")
+    sc = torch.full((B, n_q, N), float("nan"), dtype=torch.float32, device="cuda")
+    kw = dict(ratio=4, q_pos=pd, scores_out=sc, q_scale=qsd, key_scale=ksd)
+    ws = ws_tensor(m.dsv4_indexer_topk_workspace_size(qd, wd, kd, nd, idx, **kw))
+    m.dsv4_indexer_topk(qd, wd, kd, nd, idx, ws, **kw)
+    torch.cuda.synchronize()
+    st, ew = m.dsv4_read_error_word(ws)
+    assert ew == 0, f"device error word {ew:#x}"
+    got_i, got_s = idx.cpu().numpy(), sc.cpu().numpy()
+    ref_s, nv = oracle.index_scores_fp8(q8, qs, w, k8, ks, n_comp, 4, q_pos=q_pos)
+    ref_i = oracle.topk(ref_s, nv, k)
+    for b in range(B):
+        for t in range(n_q):
+            if nv[b, t]:
+                _check_scores(got_s[b, t], ref_s[b, t], nv[b, t])
+            check_topk_row(got_i[b, t], ref_i[b, t], ref_s[b, t], nv[b, t], k, f"b{b} q{t}")
+
+
 def _e4m3_ord(codes):
     """E4M3 codes as signed ordinals (sign-magnitude -> integer line; +0 and -0 both 0)."""
     c = np.asarray(codes, np.int32)
